@@ -1,0 +1,91 @@
+"""Brute-force numpy statement of LLA decode, for tiny shapes only.
+
+TEST INFRASTRUCTURE ONLY.  Independent of ``lla_oracle.c``: it materialises the
+whole reconstructed K/V stack with matrix products, builds each RoPE rotation
+as an explicit d x d matrix, and takes the softmax directly.  Used to check the
+C oracle on shapes small enough for both to agree to ~1e-12.
+
+Source: "Looped Latent Attention: Cross-Loop KV Compression for Looped
+Transformers" (arXiv 2607.15456v2), §3 Eq. (2)-(3) and "RoPE and
+reconstruction"; attention is the standard scaled dot product the paper leaves
+unchanged.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def rotation_matrix(d: int, pos: float, base: float, style: int = 0) -> np.ndarray:
+    """The d x d rotary matrix R(pos): block rotation of each frequency pair."""
+    R = np.zeros((d, d))
+    for f in range(d // 2):
+        i0, i1 = (f, f + d // 2) if style == 0 else (2 * f, 2 * f + 1)
+        ang = pos * base ** (-2.0 * f / d)
+        c, s = np.cos(ang), np.sin(ang)
+        R[i0, i0], R[i0, i1] = c, -s
+        R[i1, i0], R[i1, i1] = s, c
+    return R
+
+
+def encode(x_stack: np.ndarray, mu: np.ndarray, w_down: np.ndarray) -> np.ndarray:
+    """Eq. (2) for a batch of stacked-loop rows: (x - mu) @ W_down."""
+    return (x_stack - mu) @ w_down
+
+
+def reconstruct(c: np.ndarray, w_up_t: np.ndarray, mu_t: np.ndarray) -> np.ndarray:
+    """Eq. (3): rows c [L][r] -> [L][d] = c @ W_up,t^T + mu_t."""
+    return c @ w_up_t.T + mu_t
+
+
+def decode_per_head(t, q, cache_k, cache_v, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v,
+                    base=10000.0, style=0, pos_offset=0):
+    """Per-head LLA decode at loop t.  Shapes as the C oracle: q [B][H][d],
+    cache_* [B][H][L_max][r], w_up_* [T][H][d][r], mu_* [H][T*d]."""
+    B, H, d = q.shape
+    out = np.zeros((B, H, d))
+    lse = np.zeros((B, H))
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(H):
+            if L == 0:
+                lse[b, h] = -np.inf
+                continue
+            mu_kt = mu_k[h, t * d:(t + 1) * d]
+            mu_vt = mu_v[h, t * d:(t + 1) * d]
+            K = reconstruct(cache_k[b, h, :L], w_up_k[t, h], mu_kt)
+            V = reconstruct(cache_v[b, h, :L], w_up_v[t, h], mu_vt)
+            qr = rotation_matrix(d, q_pos[b] + pos_offset, base, style) @ q[b, h]
+            Kr = np.stack([rotation_matrix(d, j + pos_offset, base, style) @ K[j]
+                           for j in range(L)])
+            s = Kr @ qr / np.sqrt(d)
+            w = np.exp(s - s.max())
+            out[b, h] = (w / w.sum()) @ V
+            lse[b, h] = s.max() + np.log(w.sum())
+    return out, lse
+
+
+def decode_2d(t, q, cache_k, cache_v, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v,
+              base=10000.0, style=0):
+    """LLA-2D decode at loop t: one latent per token shared by all heads.
+    cache_* [B][L_max][r], w_up_* [T][H*d][r], mu_* [T*H*d] (index (t*H+h)*d+e)."""
+    B, H, d = q.shape
+    out = np.zeros((B, H, d))
+    lse = np.zeros((B, H))
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(H):
+            if L == 0:
+                lse[b, h] = -np.inf
+                continue
+            rows = slice(h * d, (h + 1) * d)
+            mu_kt = mu_k[(t * H + h) * d:(t * H + h + 1) * d]
+            mu_vt = mu_v[(t * H + h) * d:(t * H + h + 1) * d]
+            K = reconstruct(cache_k[b, :L], w_up_k[t][rows], mu_kt)
+            V = reconstruct(cache_v[b, :L], w_up_v[t][rows], mu_vt)
+            qr = rotation_matrix(d, q_pos[b], base, style) @ q[b, h]
+            Kr = np.stack([rotation_matrix(d, j, base, style) @ K[j] for j in range(L)])
+            s = Kr @ qr / np.sqrt(d)
+            w = np.exp(s - s.max())
+            out[b, h] = (w / w.sum()) @ V
+            lse[b, h] = s.max() + np.log(w.sum())
+    return out, lse
