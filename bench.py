@@ -1,0 +1,350 @@
+"""Benchmark of the LLA latent-store decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one decode step of one layer of the workload: ``lla_encode`` of each
+sequence's new token (its T-loop K/V stack) followed by ``lla_decode_attn`` for
+loops t = 1..T over all heads and sequences.  The metric is decode-attention
+latent-KV tokens per second per layer-loop: sum_b seq_lens[b] * T / step time.
+
+Rank 0 prints one JSON line.  With N>1 (torchrun, one rank per GPU) every rank
+runs its own sequences (the path shards by sequence with no exchange: weak
+scaling) and the time is the max over ranks.  ``--impl reference`` times the
+oracle (plain fp64 C on the host cores) on a bounded sample of the same
+workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from looped_transformer_cross_gb300 import build as lla_build  # noqa: E402
+from looped_transformer_cross_gb300 import lla  # noqa: E402
+from looped_transformer_cross_gb300.synth import WORKLOADS, make_decode_inputs, widen  # noqa: E402
+
+METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe roofline"
+UNIT = "latent tokens/s per layer-loop"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = max(smax, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- our arm
+
+class DecodeStep:
+    """One layer's state on the device and the per-step call sequence."""
+
+    def __init__(self, w, seed, device):
+        self.w = w
+        self.inp = make_decode_inputs(w, seed, device=device, with_encode=True)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed + 7)
+        # one query per loop (the model's query changes from loop to loop)
+        self.q = (torch.randn((w.T, w.B, w.H, w.d), generator=g, device=device)
+                  .to(self.inp["q"].dtype).contiguous())
+        self.dm = lla.dims(w.T, w.H, w.r_k, w.r_v, rope_base=w.rope_base)
+        c, s = lla.rope_table(self.dm, max(w.L_max, 128))
+        self.cos, self.sin = c.to(device), s.to(device)
+        self.ws = lla.make_workspace(self.dm, w.B, w.L_max, w.B, device=device)
+        self.seq_idx = torch.arange(w.B, dtype=torch.int32, device=device)
+        self.out = torch.empty((w.T, w.B, w.H, w.d), dtype=torch.float32, device=device)
+        self.lse = torch.empty((w.T, w.B, w.H), dtype=torch.float32, device=device)
+        self.tokens = int(self.inp["seq_lens"].sum().item())
+
+    def run(self, ev=None):
+        i, dm = self.inp, self.dm
+        lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, i["q_pos"], i["w_down_k"], i["w_down_v"],
+                   i["mu_k"], i["mu_v"], i["cache_k"], i["cache_v"], self.ws)
+        for t in range(self.w.T):
+            if ev is not None:
+                ev[0][t].record()
+            lla.decode_attn(dm, t, self.q[t], i["cache_k"], i["cache_v"], i["seq_lens"], i["q_pos"],
+                            i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"], self.cos, self.sin,
+                            self.out[t], self.lse[t], self.ws)
+            if ev is not None:
+                ev[1][t].record()
+
+    # launches of this library's kernels per step: encode (bias + GEMM) + T x (decode + combine)
+    def launches(self):
+        return 2 + 2 * self.w.T
+
+
+def barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, dist_on, device):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, dist_on, device):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def e2e_run(step: DecodeStep, steps: int):
+    """Same step through the public API with the per-step inputs coming from pinned
+    host memory and the results read back: new-token stacks, queries, lengths
+    (host->device) and out/lse (device->host)."""
+    i = step.inp
+    host_in = {k: i[k].cpu().pin_memory() for k in ("x_k", "x_v", "seq_lens", "q_pos")}
+    host_q = step.q.cpu().pin_memory()
+    host_out = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    host_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_q.numel() * host_q.element_size()
+    d2h = host_out.numel() * 4 + host_lse.numel() * 4
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for k, v in host_in.items():
+            i[k].copy_(v, non_blocking=True)
+        step.q.copy_(host_q, non_blocking=True)
+        step.run()
+        host_out.copy_(step.out, non_blocking=True)
+        host_lse.copy_(step.lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    dt = time.perf_counter() - t0
+    return dt, h2d, d2h
+
+
+def oracle_sample(w, inp_dev, q_dev, budget_s=12.0):
+    """Time the oracle on the first S sequences (all heads, all loops) of the same
+    inputs; S grows from 1 until the run would take about ``budget_s``."""
+    import oracle
+    odm = oracle.dims(w.T, w.H, w.d, w.r_k, w.r_v, w.variant, w.rope_base)
+    wk, wv = widen(inp_dev["w_up_k"]), widen(inp_dev["w_up_v"])
+    mk, mv = widen(inp_dev["mu_k"]), widen(inp_dev["mu_v"])
+    lens = inp_dev["seq_lens"].cpu().numpy()
+
+    def run(S, loops):
+        ck, cv = widen(inp_dev["cache_k"][:S]), widen(inp_dev["cache_v"][:S])
+        t0 = time.perf_counter()
+        for t in range(loops):
+            oracle.decode(odm, t, widen(q_dev[t][:S]), ck, cv, lens[:S], lens[:S] - 1, wk, wv, mk, mv)
+        return time.perf_counter() - t0
+
+    t1 = run(1, 1)
+    S = int(max(1, min(w.B, budget_s / max(t1 * w.T, 1e-3))))
+    dt = run(S, w.T)
+    tokens = float(lens[:S].sum()) * w.T
+    return {"value": tokens / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "first %d of %d sequences, all %d heads, loops 1..%d (%.0f latent tokens x "
+                      "loops) in %.2f s" % (S, w.B, w.H, w.T, tokens, dt)}
+
+
+def run_ours(args, dist_on, rank, world, device):
+    w = WORKLOADS[args.workload]
+    lla_build.build()
+    lla.lib()
+    step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    st = lla.device_status(step.ws)
+    if st != lla.LLA_OK:
+        raise RuntimeError("device status after warm-up: " + lla.status_string(st))
+
+    T = w.T
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(T)] for _ in range(2)]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(dist_on)
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(args.steps):
+            step.run(ev[k])
+        stop.record()
+        torch.cuda.synchronize()
+        barrier(dist_on)
+    elapsed = start.elapsed_time(stop) / 1e3
+    st = lla.device_status(step.ws)
+    if st != lla.LLA_OK:
+        raise RuntimeError("device status after timing: " + lla.status_string(st))
+    t_max = max_over_ranks(elapsed, dist_on, device)
+    tokens_all = sum_over_ranks(float(step.tokens * T * args.steps), dist_on, device)
+    value = tokens_all / t_max
+
+    # dominant kernel: the decode call (main kernel + its small combine), timed per launch
+    durs = [ev[k][0][t].elapsed_time(ev[k][1][t]) / 1e3 for k in range(args.steps) for t in range(T)]
+    t_call = float(np.mean(durs))
+    lat_bytes = step.tokens * w.H * (w.r_k + w.r_v) * 2
+    hbm, _, src = peaks()
+    achieved = lat_bytes / t_call / 1e9
+
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
+    e2e_dt = max_over_ranks(e2e_dt, dist_on, device)
+    e2e_val = sum_over_ranks(float(step.tokens * T * e2e_steps), dist_on, device) / e2e_dt
+
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
+                   "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi],
+                   "latent_tokens_per_gpu": step.tokens, "parallelism": "dp%d" % world,
+                   "step": "lla_encode of %d new tokens + lla_decode_attn for loops 1..%d" % (w.B, T),
+                   "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
+                       step.inp["cache_k"].numel() * 2 * (1 + w.r_v / w.r_k) / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "lla_decode_attn (decode_bf16_kernel + decode_combine_kernel)",
+                     "algorithmic_bytes_per_launch": lat_bytes, "launch_ms": t_call * 1e3,
+                     "peak_source": src},
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches() * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = oracle_sample(w, step.inp, step.q)
+    return res
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, on a bounded sample of the same
+    workload per step (first sequence, all heads, one loop per step, cycling t)."""
+    import oracle
+    w = WORKLOADS[args.workload]
+    inp = make_decode_inputs(w, 20260000 + 1, device="cuda" if torch.cuda.is_available() else "cpu")
+    odm = oracle.dims(w.T, w.H, w.d, w.r_k, w.r_v, w.variant, w.rope_base)
+    S = 1
+    ck, cv, q = widen(inp["cache_k"][:S]), widen(inp["cache_v"][:S]), widen(inp["q"][:S])
+    wk, wv, mk, mv = (widen(inp[k]) for k in ("w_up_k", "w_up_v", "mu_k", "mu_v"))
+    lens = inp["seq_lens"][:S].cpu().numpy()
+    for i in range(args.warmup):
+        oracle.decode(odm, i % w.T, q, ck, cv, lens, lens - 1, wk, wv, mk, mv)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.decode(odm, i % w.T, q, ck, cv, lens, lens - 1, wk, wv, mk, mv)
+    dt = time.perf_counter() - t0
+    value = float(lens.sum()) * args.steps / dt
+    sample = "sequence 0 of %d (%d tokens), all %d heads, one loop per step" % (w.B, int(lens.sum()), w.H)
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
+                       "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ouro1.4b_rho4_b32_4k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    dist_on = world > 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if dist_on:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    try:
+        res = run_ours(args, dist_on, rank, world, device)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if dist_on:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

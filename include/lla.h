@@ -1,0 +1,168 @@
+/*
+ * lla.h — C ABI of the Looped Latent Attention (LLA) GPU library (liblla.so).
+ *
+ * LLA ("Looped Latent Attention: Cross-Loop KV Compression for Looped
+ * Transformers", arXiv 2607.15456v2) replaces the per-loop K/V cache of a
+ * weight-tied looped decoder (T loops, D layers, H heads of width d) by one K
+ * latent and one V latent per token, layer and head, and rebuilds the loop-t
+ * K/V only when attention reads them (§1, §3; §7 "latent-store path").  This
+ * library is the data-parallel hot path of that latent-store decode:
+ *
+ *   lla_encode       Eq. (2)  c = (x - mu) W_down, written into cache slots
+ *   lla_decode_attn  Eq. (3)  k_t = c_k W_up,k,t^T + mu_k,t (v likewise),
+ *                    RoPE after reconstruction (§3 "RoPE and reconstruction"),
+ *                    softmax(q.k/sqrt(d)) v over each sequence's history,
+ *                    for one layer and one loop, all heads and sequences.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *   the library allocates nothing and keeps no per-call state.  "host"
+ *   pointers are ordinary CPU memory.
+ * - Arrays are dense and row-major, with the shapes given below.  Storage
+ *   types follow lla_dims.dtype: LLA_BF16 stores latents, W, x and q as
+ *   bfloat16 (mu always fp32); LLA_F32 stores everything as fp32.
+ * - Every device pointer must be 16-byte aligned.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream).  Argument errors found on the host return before any launch.
+ *   Values that live on the device (seq_lens, q_pos, seq_idx, pos) are
+ *   checked by the kernels: an out-of-range value is clamped or its token
+ *   skipped, and LLA_ERR_DEVICE_ARG is recorded in the workspace status word
+ *   (read it with lla_device_status).  Every wait inside a kernel is bounded
+ *   (about one second); on expiry the kernel records LLA_ERR_TIMEOUT and
+ *   returns.
+ * - The workspace is caller-allocated device memory of at least
+ *   lla_workspace_size() bytes.  Its first 256 bytes hold the status word and
+ *   must be zero before the first call; the rest is scratch.  Calls that
+ *   share a workspace must be ordered on one stream.
+ * - Constraints: d_head == 128; r_k and r_v multiples of 16 in [16, 256];
+ *   T >= 1; H >= 1.  Other shapes return LLA_ERR_UNSUPPORTED.
+ */
+#ifndef LLA_H
+#define LLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LLA_ABI_VERSION 1
+
+typedef enum {
+    LLA_OK = 0,
+    LLA_ERR_INVALID_ARG = 1,   /* bad host-side argument: nothing launched       */
+    LLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented shape/variant/dtype  */
+    LLA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed              */
+    LLA_ERR_TIMEOUT = 4,       /* a kernel's bounded wait expired (device word)  */
+    LLA_ERR_DEVICE_ARG = 5     /* out-of-range seq_lens/q_pos/seq_idx/pos seen
+                                  by a kernel (device word)                       */
+} lla_status;
+
+typedef enum { LLA_BF16 = 0, LLA_F32 = 1 } lla_dtype;
+
+/* LLA_PER_HEAD: one latent per (token, layer, head) (§3 "Cross-loop codec").
+ * LLA_2D: one latent per (token, layer) shared by all heads, reconstructing
+ * every head (§3 "The LLA-2D variant"). */
+typedef enum { LLA_PER_HEAD = 0, LLA_2D = 1 } lla_variant;
+
+/* RoPE pairing: LLA_ROPE_HALF rotates (i, i + d/2); LLA_ROPE_INTERLEAVED
+ * rotates (2i, 2i+1).  Frequencies theta_f = rope_base^(-2f/d). */
+typedef enum { LLA_ROPE_HALF = 0, LLA_ROPE_INTERLEAVED = 1 } lla_rope_style;
+
+typedef struct {
+    int T;                      /* loops                                   */
+    int H;                      /* heads                                   */
+    int d_head;                 /* head width (must be 128)                */
+    int r_k, r_v;               /* latent ranks                            */
+    lla_variant variant;
+    lla_dtype dtype;
+    float rope_base;            /* e.g. 10000                              */
+    lla_rope_style rope_style;
+} lla_dims;
+
+/* One layer's latent cache (device).  Per-head: k [B][H][L_max][r_k],
+ * v [B][H][L_max][r_v]; element (b,h,j,i) of k at ((b*H+h)*L_max+j)*r_k+i.
+ * LLA-2D: k [B][L_max][r_k], v [B][L_max][r_v]. */
+typedef struct {
+    void* k;
+    void* v;
+    int B;
+    int64_t L_max;
+} lla_cache;
+
+/*
+ * lla_encode — Eq. (2) of §3: for each of N tokens and each head,
+ *     c_k = (x_k - mu_k) W_down,k ,  c_v = (x_v - mu_v) W_down,v
+ * rounded to the cache dtype (round-to-nearest-even) and stored in cache slot
+ * (seq_idx[n], pos[n]).  x is the loop stack of Eq. (1): index t*d+i.
+ *   x_k, x_v        device  [N][H][T*d]      (LLA-2D: [N][T*H*d], index (t*H+h)*d+i)
+ *   seq_idx, pos    device  int32 [N]        slot of token n; entries outside
+ *                                            [0,B) x [0,L_max) are skipped and
+ *                                            flagged LLA_ERR_DEVICE_ARG
+ *   w_down_k/_v     device  [H][T*d][r]      (LLA-2D: [T*H*d][r])
+ *   mu_k, mu_v      device  fp32 [H][T*d]    (LLA-2D: [T*H*d])
+ * Used both for a decode step's new token and for prefill (N = all prompt
+ * tokens of a layer).  Two tokens writing the same slot race.
+ */
+lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, int N,
+                      const int32_t* seq_idx, const int32_t* pos,
+                      const void* w_down_k, const void* w_down_v,
+                      const float* mu_k, const float* mu_v,
+                      lla_cache cache, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * lla_decode_attn — one layer, one loop t (0-based; the paper counts t=1..T),
+ * all heads and all B sequences.  For sequence b with L = seq_lens[b] cached
+ * tokens (positions 0..L-1) and a query at position q_pos[b]:
+ *     k_j = c_k,j W_up,k,t^T + mu_k,t ,  v_j = c_v,j W_up,v,t^T + mu_v,t   (Eq. (3))
+ *     s_j = RoPE(q, q_pos) . RoPE(k_j, j) / sqrt(d)   for j < L
+ *     out = sum_j softmax(s)_j v_j ,  lse = ln sum_j exp(s_j)
+ * mu_t is the t-th d-slice of the codec mean mu of Eq. (2).
+ *   q              device  [B][H][d]               pre-RoPE query
+ *   seq_lens       device  int32 [B]                0 <= L <= L_max (L=0: out=0, lse=-inf)
+ *   q_pos          device  int32 [B]                0 <= q_pos < rope_len
+ *   w_up_k, w_up_v device  [T][H][d][r]             all loops (LLA-2D: [T][H*d][r])
+ *   mu_k, mu_v     device  fp32 [H][T*d]            (LLA-2D: [T*H*d])
+ *   rope_cos/_sin  device  fp32 [rope_len][d/2]     cos/sin(p*theta_f) as made by
+ *                                                   lla_rope_table; rope_len >=
+ *                                                   max(L_max, 128)
+ *   out            device  fp32 [B][H][d]
+ *   lse            device  fp32 [B][H]              natural log
+ * The new token's own K/V are attended only if the caller has encoded them
+ * into slot q_pos (the paper's latent-store decoder reads every cached token
+ * back through its latent); lse lets a caller merge further exact terms.
+ */
+lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
+                           lla_cache cache, const int32_t* seq_lens, const int32_t* q_pos,
+                           const void* w_up_k, const void* w_up_v,
+                           const float* mu_k, const float* mu_v,
+                           const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                           float* out, float* lse,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for calls with at most B sequences of L_max slots and
+ * encode batches of at most max_N tokens, on the current CUDA device.
+ * Returns 0 for invalid dims. */
+size_t lla_workspace_size(const lla_dims* dims, int B, int64_t L_max, int max_N);
+
+/* Host-side RoPE table: cos_out/sin_out (host, fp32 [n_pos][d/2]) get
+ * cos(p*theta_f), sin(p*theta_f) for p < n_pos, computed in fp64 and rounded
+ * once to fp32. */
+lla_status lla_rope_table(const lla_dims* dims, int64_t n_pos, float* cos_out, float* sin_out);
+
+/* Synchronise `stream`, then return the status word the kernels recorded in
+ * `workspace` (LLA_OK if none); clear it when `clear` is non-zero. */
+lla_status lla_device_status(void* workspace, void* stream, int clear);
+
+/* Static description of a status code. */
+const char* lla_status_string(lla_status status);
+
+/* LLA_ABI_VERSION of the loaded library. */
+int lla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLA_H */

@@ -1,0 +1,266 @@
+// lla_api.cu — the C ABI of liblla.so (declared in include/lla.h): host-side
+// argument checks, workspace layout, TMA descriptors and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "lla_kernels.h"
+
+using namespace lla;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D tiled map over a dense row-major tensor [d2][d1][d0] of `esize`-byte elements.
+bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t d0,
+                 uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const int row_bytes = static_cast<int>(b0) * esize;
+  const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct WsLayout {
+  size_t prefix, partials, bias, scores, total;
+};
+
+WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
+  WsLayout w{};
+  size_t off = 256;  // status word
+  w.prefix = off; off += al256(static_cast<size_t>(B + 1) * 4);
+  w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * (d->r_v + 2) * 4);
+  w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
+  w.scores = off;
+  if (d->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * d->H * L_max * 4);
+  w.total = off;
+  return w;
+}
+
+lla_status check_dims(const lla_dims* d) {
+  if (!d) return LLA_ERR_INVALID_ARG;
+  if (d->T < 1 || d->H < 1 || d->d_head < 2 || d->r_k < 1 || d->r_v < 1) return LLA_ERR_INVALID_ARG;
+  if (d->variant != LLA_PER_HEAD && d->variant != LLA_2D) return LLA_ERR_INVALID_ARG;
+  if (d->dtype != LLA_BF16 && d->dtype != LLA_F32) return LLA_ERR_INVALID_ARG;
+  if (d->rope_style != LLA_ROPE_HALF && d->rope_style != LLA_ROPE_INTERLEAVED) return LLA_ERR_INVALID_ARG;
+  if (!(d->rope_base > 0.f) || !std::isfinite(d->rope_base)) return LLA_ERR_INVALID_ARG;
+  if (d->d_head != kHeadDim) return LLA_ERR_UNSUPPORTED;
+  if (d->r_k % 16 || d->r_v % 16 || d->r_k > 256 || d->r_v > 256) return LLA_ERR_UNSUPPORTED;
+  if (d->variant == LLA_2D) return LLA_ERR_UNSUPPORTED;
+  return LLA_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lla_abi_version(void) { return LLA_ABI_VERSION; }
+
+const char* lla_status_string(lla_status s) {
+  switch (s) {
+    case LLA_OK: return "ok";
+    case LLA_ERR_INVALID_ARG: return "invalid argument";
+    case LLA_ERR_UNSUPPORTED: return "unsupported shape, variant or dtype";
+    case LLA_ERR_CUDA: return "CUDA error";
+    case LLA_ERR_TIMEOUT: return "a kernel wait timed out";
+    case LLA_ERR_DEVICE_ARG: return "out-of-range seq_lens/q_pos/seq_idx/pos seen on the device";
+  }
+  return "unknown status";
+}
+
+size_t lla_workspace_size(const lla_dims* dims, int B, int64_t L_max, int max_N) {
+  (void)max_N;
+  if (check_dims(dims) != LLA_OK || B < 0 || L_max < 0) return 0;
+  return ws_layout(dims, B, L_max).total;
+}
+
+lla_status lla_rope_table(const lla_dims* dims, int64_t n_pos, float* cos_out, float* sin_out) {
+  if (!dims || dims->d_head < 2 || dims->d_head % 2 || !(dims->rope_base > 0.f) || n_pos < 0 ||
+      (n_pos > 0 && (!cos_out || !sin_out)))
+    return LLA_ERR_INVALID_ARG;
+  const int half = dims->d_head / 2;
+  for (int f = 0; f < half; ++f) {
+    const double theta = std::pow(static_cast<double>(dims->rope_base), -2.0 * f / dims->d_head);
+    for (int64_t p = 0; p < n_pos; ++p) {
+      const double ang = static_cast<double>(p) * theta;
+      cos_out[p * half + f] = static_cast<float>(std::cos(ang));
+      sin_out[p * half + f] = static_cast<float>(std::sin(ang));
+    }
+  }
+  return LLA_OK;
+}
+
+lla_status lla_device_status(void* workspace, void* stream, int clear) {
+  if (!workspace) return LLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LLA_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LLA_ERR_CUDA;
+  if (clear && v != 0 && cudaMemset(workspace, 0, 4) != cudaSuccess) return LLA_ERR_CUDA;
+  return static_cast<lla_status>(v);
+}
+
+lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_cache cache,
+                           const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
+                           const void* w_up_v, const float* mu_k, const float* mu_v,
+                           const float* rope_cos, const float* rope_sin, int64_t rope_len, float* out,
+                           float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  lla_status st = check_dims(dims);
+  if (st != LLA_OK) return st;
+  if (loop_t < 0 || loop_t >= dims->T || cache.B < 0 || cache.L_max < 1) return LLA_ERR_INVALID_ARG;
+  if (cache.B == 0) return LLA_OK;
+  if (cache.L_max > (int64_t(1) << 30) || static_cast<int64_t>(cache.B) * dims->H > (int64_t(1) << 30))
+    return LLA_ERR_UNSUPPORTED;
+  if (rope_len < cache.L_max || rope_len < kTile) return LLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, cache.k, cache.v, seq_lens, q_pos, w_up_k, w_up_v, mu_k,
+                        mu_v, rope_cos, rope_sin, out, lse, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LLA_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(dims, cache.B, cache.L_max);
+  if (ws_bytes < wl.total) return LLA_ERR_INVALID_ARG;
+
+  const int H = dims->H, d = dims->d_head;
+  const int esize = dims->dtype == LLA_BF16 ? 2 : 4;
+  DecodeArgs a{};
+  a.B = cache.B;
+  a.H = H;
+  a.r_k = dims->r_k;
+  a.r_v = dims->r_v;
+  a.rope_style = dims->rope_style;
+  a.L_max = cache.L_max;
+  a.rope_len = rope_len;
+  a.mu_hstride = static_cast<int64_t>(dims->T) * d;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.q_pos = q_pos;
+  a.cache_k = cache.k;
+  a.cache_v = cache.v;
+  a.w_up_k = static_cast<const uint8_t*>(w_up_k) + static_cast<size_t>(loop_t) * H * d * dims->r_k * esize;
+  a.w_up_v = static_cast<const uint8_t*>(w_up_v) + static_cast<size_t>(loop_t) * H * d * dims->r_v * esize;
+  a.mu_k = mu_k + static_cast<size_t>(loop_t) * d;
+  a.mu_v = mu_v + static_cast<size_t>(loop_t) * d;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  a.out = out;
+  a.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
+  a.partials = reinterpret_cast<float*>(ws + wl.partials);
+  a.scores = reinterpret_cast<float*>(ws + wl.scores);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (dims->dtype == LLA_F32) return launch_decode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+
+  if (!make_decode_plan(dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  if (sms <= 0) return LLA_ERR_CUDA;
+  const int64_t max_tiles = static_cast<int64_t>(cache.B) * H * ((cache.L_max + kTile - 1) / kTile);
+  a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_tiles)));
+  DecodeMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const uint64_t rows = static_cast<uint64_t>(cache.L_max), units = static_cast<uint64_t>(cache.B) * H;
+  for (int c = 0; c < a.plan.kplan.n; ++c) {
+    const int w = a.plan.kplan.width[c];
+    if (!make_map_3d(&maps.k[chunk_map_index(w)], cache.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_k, rows,
+                     units, w, kTile, 1))
+      return LLA_ERR_CUDA;
+  }
+  for (int c = 0; c < a.plan.vplan.n; ++c) {
+    const int w = a.plan.vplan.width[c];
+    if (!make_map_3d(&maps.v[chunk_map_index(w)], cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows,
+                     units, w, kTile, 1))
+      return LLA_ERR_CUDA;
+  }
+  return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, int N, const int32_t* seq_idx,
+                      const int32_t* pos, const void* w_down_k, const void* w_down_v, const float* mu_k,
+                      const float* mu_v, lla_cache cache, void* workspace, size_t ws_bytes, void* stream) {
+  lla_status st = check_dims(dims);
+  if (st != LLA_OK) return st;
+  if (N < 0 || cache.B < 0 || cache.L_max < 1) return LLA_ERR_INVALID_ARG;
+  if (N == 0) return LLA_OK;
+  const void* ptrs[] = {x_k, x_v, seq_idx, pos, w_down_k, w_down_v, mu_k, mu_v, cache.k, cache.v, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LLA_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(dims, cache.B, cache.L_max);
+  if (ws_bytes < wl.total) return LLA_ERR_INVALID_ARG;
+
+  EncodeArgs a{};
+  a.N = N;
+  a.H = dims->H;
+  a.Td = dims->T * dims->d_head;
+  a.r_k = dims->r_k;
+  a.r_v = dims->r_v;
+  a.B = cache.B;
+  a.L_max = cache.L_max;
+  a.x_k = x_k;
+  a.x_v = x_v;
+  a.seq_idx = seq_idx;
+  a.pos = pos;
+  a.w_down_k = w_down_k;
+  a.w_down_v = w_down_v;
+  a.mu_k = mu_k;
+  a.mu_v = mu_v;
+  a.cache_k = cache.k;
+  a.cache_v = cache.v;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.bias = reinterpret_cast<float*>(ws + wl.bias);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dims->dtype == LLA_F32) return launch_encode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+
+  EncodePlan plan;
+  if (!make_encode_plan(dims->r_k, dims->r_v, a.Td, &plan)) return LLA_ERR_UNSUPPORTED;
+  EncodeMaps m;
+  std::memset(&m, 0, sizeof(m));
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map_3d(&m.xk, x_k, BF, 2, a.Td, a.H, N, 64, 1, 128)) return LLA_ERR_CUDA;
+  if (!make_map_3d(&m.xv, x_v, BF, 2, a.Td, a.H, N, 64, 1, 128)) return LLA_ERR_CUDA;
+  for (int c = 0; c < plan.bk.n; ++c) {
+    const int w = plan.bk.width[c];
+    if (!make_map_3d(&m.wk[chunk_map_index(w)], w_down_k, BF, 2, a.r_k, a.Td, a.H, w, 64, 1)) return LLA_ERR_CUDA;
+  }
+  for (int c = 0; c < plan.bv.n; ++c) {
+    const int w = plan.bv.width[c];
+    if (!make_map_3d(&m.wv[chunk_map_index(w)], w_down_v, BF, 2, a.r_v, a.Td, a.H, w, 64, 1)) return LLA_ERR_CUDA;
+  }
+  return launch_encode_bf16(a, plan, m, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+}  // extern "C"

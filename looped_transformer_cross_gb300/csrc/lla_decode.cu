@@ -1,0 +1,818 @@
+// lla_decode.cu — latent-store decode attention of Looped Latent Attention on
+// sm_103a ("Looped Latent Attention: Cross-Loop KV Compression for Looped
+// Transformers", arXiv 2607.15456v2: §3 Eq. (2)-(3), "RoPE and
+// reconstruction", §7 latent-store path, Appendix J "Absorbed attention").
+//
+// Per-head bf16 path, one persistent CTA per SM:
+//   * Work is the flat list of 128-token latent tiles over (sequence, head),
+//     cut into equal contiguous ranges, one per CTA.  A (sequence, head) unit
+//     split between CTAs is merged afterwards from per-CTA records
+//     (m, l, acc_v) by the combine kernel (log-sum-exp merge).
+//   * Warp 0 streams latent tiles with TMA into two shared-memory rings (K and
+//     V), together with the RoPE row of the tile's base position.
+//   * Warp 1 issues tcgen05 MMAs.  Scores: U = C_k Z^T (+ bias) into TMEM, where
+//     Z folds the RoPE-rotated query into W_up,k,t (exact rewrite of
+//     q'.R_j (W c + mu)); Z is split into bf16 hi + lo so the product is
+//     accurate to ~fp32.  Values: D = C_v^T P with the softmax weights P of the
+//     tile as a 16-column operand — the V up-projection is applied once per
+//     (sequence, head) at the end (Appendix J identity).
+//   * Warps 2-5 (one TMEM lane = one token each) turn U into the rotary score
+//     s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f}, keep a per-warp online
+//     softmax, write P, and accumulate D.  cos/sin(j th) come from the angle
+//     sum of the tile base row (in smem) and the lane's own row (registers).
+// Reconstructed keys and values never leave TMEM / registers.
+//
+// fp32 path: plain SIMT kernels (reconstruct k in registers, RoPE from the
+// table, exact softmax), used for the 1e-5 parity mode.
+#include "lla_kernels.h"
+
+#include <cmath>
+
+namespace lla {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
+
+struct alignas(16) DecodeMisc {
+  uint64_t kfull[kMaxStages], kempty[kMaxStages];
+  uint64_t vfull[kMaxStages], vempty[kMaxStages];
+  uint64_t ufull[2], uempty[2], pfull[2], dvfull[2], dvempty[2];
+  uint64_t zfull, mma_done, statsbar[2];
+  uint32_t tmem_base;
+  int abort;
+  int start_b, start_h, start_t, count;
+  int total_seq_tiles;
+  float alpha[4][4];         // [tile & 3][warp] softmax rescale of that tile
+  float stats[2][4][2];      // [unit parity][warp] (m, l)
+  int scan[kDecodeThreads];  // per-thread sequence-chunk tile counts
+};
+static_assert(sizeof(DecodeMisc) <= 2048, "misc region");
+
+struct Walker {
+  int b, h, t, nb, L;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int64_t L_max) {
+  return L < 0 ? 0 : (L > L_max ? static_cast<int>(L_max) : L);
+}
+
+__device__ __forceinline__ void walker_advance(Walker& w, const DecodeArgs& a) {
+  if (++w.t < w.nb) return;
+  w.t = 0;
+  if (++w.h < a.H) return;
+  w.h = 0;
+  while (true) {
+    ++w.b;
+    if (w.b >= a.B) { w.nb = 0; return; }
+    w.L = clamp_len(__ldg(a.seq_lens + w.b), a.L_max);
+    w.nb = (w.L + kTile - 1) / kTile;
+    if (w.nb > 0) return;
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Z (the B operand of the score MMA) for unit (b, h), row e of 128 written by
+// thread e.  With q' = RoPE(q, q_pos) and frequency pair (i0, i1) of f = e mod 64:
+//   rows e < 64 :  Z_e = sc * (q'_i0 W_i0 + q'_i1 W_i1),  bias sc * (q'_i0 mu_i0 + q'_i1 mu_i1)
+//   rows e >= 64:  Z_e = sc * (q'_i1 W_i0 - q'_i0 W_i1),  bias sc * (q'_i1 mu_i0 - q'_i0 mu_i1)
+// so that s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f} with U = c_j Z^T + bias,
+// which equals log2(e) * RoPE(q,q_pos).RoPE(k_j, j) / sqrt(d) for k_j of Eq. (3).
+__device__ void compute_z(const DecodeArgs& a, uint8_t* sm, int b, int h, int e) {
+  const DecodePlan& P = a.plan;
+  int qp = __ldg(a.q_pos + b);
+  if (qp < 0 || qp >= a.rope_len) {
+    record_status(a.status, LLA_ERR_DEVICE_ARG);
+    qp = qp < 0 ? 0 : static_cast<int>(a.rope_len - 1);
+  }
+  const int f = e & 63;
+  const int i0 = a.rope_style == 0 ? f : 2 * f;
+  const int i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
+  const float cq = __ldg(a.rope_cos + static_cast<int64_t>(qp) * 64 + f);
+  const float sq = __ldg(a.rope_sin + static_cast<int64_t>(qp) * 64 + f);
+  const __nv_bfloat16* qv =
+      static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(b) * a.H + h) * kHeadDim;
+  const float x0 = __bfloat162float(qv[i0]), x1 = __bfloat162float(qv[i1]);
+  const float q0 = x0 * cq - x1 * sq;   // q'_i0
+  const float q1 = x0 * sq + x1 * cq;   // q'_i1
+  const float scale = kLog2e * kInvSqrtD;
+  const float ca = (e < 64 ? q0 : q1) * scale;
+  const float cb = (e < 64 ? q1 : -q0) * scale;
+
+  const __nv_bfloat16* W =
+      static_cast<const __nv_bfloat16*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
+  const uint4* w0 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i0) * a.r_k);
+  const uint4* w1 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i1) * a.r_k);
+  for (int c = 0; c < P.kplan.n; ++c) {
+    const int width = P.kplan.width[c], rb = width * 2;
+    for (int g = 0; g < width / 8; ++g) {
+      const int k8 = (P.kplan.start[c] >> 3) + g;
+      float wa[8], wb[8];
+      unpack_bf16x8(__ldg(w0 + k8), wa);
+      unpack_bf16x8(__ldg(w1 + k8), wb);
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float z0 = ca * wa[2 * j] + cb * wb[2 * j];
+        const float z1 = ca * wa[2 * j + 1] + cb * wb[2 * j + 1];
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(z0, z1);
+        const float2 hf = __bfloat1622float2(h2);
+        hi[j] = bf16x2_bits(h2);
+        lo[j] = bf16x2_bits(__floats2bfloat162_rn(z0 - hf.x, z1 - hf.y));
+      }
+      const uint32_t off = P.kplan.off[c] + swizzle_offset(e * rb + g * 16, rb);
+      *reinterpret_cast<uint4*>(sm + P.z_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      if (P.zpasses == 2)
+        *reinterpret_cast<uint4*>(sm + P.z_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+  const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
+  const float zb = ca * __ldg(mu + i0) + cb * __ldg(mu + i1);
+  const __nv_bfloat16 zh = __float2bfloat16_rn(zb);
+  const __nv_bfloat16 zl = __float2bfloat16_rn(zb - __bfloat162float(zh));
+  const uint32_t pair = bf16x2_bits(__halves2bfloat162(zh, zl));
+  *reinterpret_cast<uint4*>(sm + P.aug_b + swizzle_offset(e * 32, 32)) = make_uint4(pair, 0, 0, 0);
+  *reinterpret_cast<uint4*>(sm + P.aug_b + swizzle_offset(e * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
+}
+
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ DecodeMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  // swizzle atoms need 1024-byte alignment in the shared window itself
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const DecodePlan& P = a.plan;
+  const uint32_t sbase = smem_u32(sm);
+  DecodeMisc* misc = reinterpret_cast<DecodeMisc*>(sm + P.misc);
+  volatile int* abort = &misc->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---------------------------------------------------------- work range
+  {
+    const int per_thr = (a.B + kDecodeThreads - 1) / kDecodeThreads;
+    const int b0 = min(a.B, tid * per_thr), b1 = min(a.B, b0 + per_thr);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int L0 = __ldg(a.seq_lens + b);
+      if ((L0 < 0 || L0 > a.L_max) && blockIdx.x == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
+      local += (clamp_len(L0, a.L_max) + kTile - 1) / kTile;
+    }
+    misc->scan[tid] = local;
+    if (tid == 0) misc->abort = 0;
+    __syncthreads();
+    if (warp == 0) {
+      int v[kDecodeThreads / 32];
+      int s = 0;
+#pragma unroll
+      for (int i = 0; i < kDecodeThreads / 32; ++i) { v[i] = misc->scan[lane * (kDecodeThreads / 32) + i]; s += v[i]; }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      int excl = incl - s;
+#pragma unroll
+      for (int i = 0; i < kDecodeThreads / 32; ++i) { misc->scan[lane * (kDecodeThreads / 32) + i] = excl; excl += v[i]; }
+      if (lane == 31) misc->total_seq_tiles = incl;
+    }
+    __syncthreads();
+    const long long total = static_cast<long long>(a.H) * misc->total_seq_tiles;
+    const long long per = max(1LL, (total + a.grid - 1) / a.grid);
+    const long long f0 = static_cast<long long>(blockIdx.x) * per;
+    const long long f1 = min(total, f0 + per);
+    long long P0 = misc->scan[tid];
+    for (int b = b0; b < b1; ++b) {
+      const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
+      if (blockIdx.x == 0) a.prefix[b] = static_cast<int32_t>(P0);
+      if (nb > 0 && f0 < f1 && a.H * P0 <= f0 && f0 < a.H * (P0 + nb)) {
+        const long long rem = f0 - a.H * P0;
+        misc->start_b = b;
+        misc->start_h = static_cast<int>(rem / nb);
+        misc->start_t = static_cast<int>(rem % nb);
+      }
+      P0 += nb;
+    }
+    if (blockIdx.x == 0 && tid == 0) a.prefix[a.B] = misc->total_seq_tiles;
+    if (tid == 0) misc->count = static_cast<int>(f1 > f0 ? f1 - f0 : 0);
+    __syncthreads();
+  }
+  const int count = misc->count;
+  if (count == 0) return;
+
+  Walker start;
+  start.b = misc->start_b;
+  start.h = misc->start_h;
+  start.t = misc->start_t;
+  start.L = clamp_len(__ldg(a.seq_lens + start.b), a.L_max);
+  start.nb = (start.L + kTile - 1) / kTile;
+
+  // ---------------------------------------------------------- set-up
+  auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
+  if (tid == 0) {
+    for (int s = 0; s < P.SK; ++s) { mbar_init(bar(misc->kfull[s]), 1); mbar_init(bar(misc->kempty[s]), 1); }
+    for (int s = 0; s < P.SV; ++s) { mbar_init(bar(misc->vfull[s]), 1); mbar_init(bar(misc->vempty[s]), 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(misc->ufull[i]), 1);
+      mbar_init(bar(misc->uempty[i]), 4);
+      mbar_init(bar(misc->pfull[i]), 4);
+      mbar_init(bar(misc->dvfull[i]), 1);
+      mbar_init(bar(misc->dvempty[i]), 4);
+    }
+    mbar_init(bar(misc->zfull), 128);
+    mbar_init(bar(misc->mma_done), 1);
+    mbar_init(bar(misc->statsbar[0]), 4);
+    mbar_init(bar(misc->statsbar[1]), 4);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < 3; ++i) { prefetch_tmap(&maps.k[i]); prefetch_tmap(&maps.v[i]); }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(&misc->tmem_base), 512);
+  }
+  if (warp >= 2) {
+    const int et = tid - 64;
+    // constant bias operand: columns 0 and 1 of every row are 1 (they meet bias hi / lo)
+    const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
+    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32, 32)) = make_uint4(ones, 0, 0, 0);
+    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
+    // softmax-weight operands start at zero; each warp only ever writes its own row
+    uint4* pz = reinterpret_cast<uint4*>(sm + P.p_buf);
+    for (int i = et; i < 2 * 4096 / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+
+  const uint32_t v_ring = sbase + P.v_ring, k_ring = sbase + P.k_ring;
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      Walker w = start;
+      int issued_k = 0, issued_v = 0;
+      for (int i = 0; i < count; ++i) {
+        const int sk = i % P.SK;
+        if (!mbar_wait(bar(misc->kempty[sk]), ((i / P.SK) & 1) ^ 1, abort, a.status)) break;
+        const uint32_t kb = bar(misc->kfull[sk]);
+        mbar_arrive_expect_tx(kb, P.kplan.bytes);
+        const int z = w.b * a.H + w.h, y = w.t * kTile;
+        for (int c = 0; c < P.kplan.n; ++c)
+          tma_load_3d(k_ring + sk * P.k_stage + P.kplan.off[c], &maps.k[chunk_map_index(P.kplan.width[c])],
+                      kb, P.kplan.start[c], y, z);
+        issued_k = i + 1;
+        const int sv = i % P.SV;
+        if (!mbar_wait(bar(misc->vempty[sv]), ((i / P.SV) & 1) ^ 1, abort, a.status)) break;
+        const uint32_t vb = bar(misc->vfull[sv]);
+        mbar_arrive_expect_tx(vb, P.vplan.bytes + 512);
+        const uint32_t vs = v_ring + sv * P.v_stage;
+        for (int c = 0; c < P.vplan.n; ++c)
+          tma_load_3d(vs + P.vplan.off[c], &maps.v[chunk_map_index(P.vplan.width[c])], vb,
+                      P.vplan.start[c], y, z);
+        bulk_load(vs + P.v_trig, a.rope_cos + static_cast<int64_t>(y) * 64, 256, vb);
+        bulk_load(vs + P.v_trig + 256, a.rope_sin + static_cast<int64_t>(y) * 64, 256, vb);
+        issued_v = i + 1;
+        walker_advance(w, a);
+      }
+      // Let every copy this CTA issued land before the CTA can exit.
+      for (int i = max(0, issued_k - P.SK); i < issued_k; ++i) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar(misc->kfull[i % P.SK]), (i / P.SK) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+      for (int i = max(0, issued_v - P.SV); i < issued_v; ++i) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar(misc->vfull[i % P.SV]), (i / P.SV) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_k = umma_idesc_bf16(128, 128, false, false);
+      const uint32_t idesc_v = umma_idesc_bf16(128, 16, true, false);
+      const uint32_t z_hi = sbase + P.z_hi, z_lo = sbase + P.z_lo;
+      const uint32_t aug_a = sbase + P.aug_a, aug_b = sbase + P.aug_b;
+      const uint32_t p_buf = sbase + P.p_buf;
+      Walker w = start;
+      int zph = 0;
+      bool ok = true;
+      for (int i = 0; i <= count && ok; ++i) {
+        if (i < count) {
+          if (i == 0 || w.t == 0) {
+            if (!(ok = mbar_wait(bar(misc->zfull), zph, abort, a.status))) break;
+            zph ^= 1;
+          }
+          const int sk = i % P.SK, ub = i & 1;
+          if (!(ok = mbar_wait(bar(misc->kfull[sk]), (i / P.SK) & 1, abort, a.status))) break;
+          if (!(ok = mbar_wait(bar(misc->uempty[ub]), ((i >> 1) & 1) ^ 1, abort, a.status))) break;
+          tc_fence_after();
+          const uint32_t d = tmem + ub * 128;
+          const uint32_t ks = k_ring + sk * P.k_stage;
+          uint32_t acc = 0;
+#pragma unroll 1
+          for (int pass = 0; pass < P.zpasses; ++pass) {
+            const uint32_t zb = pass == 0 ? z_hi : z_lo;
+            for (int c = 0; c < P.kplan.n; ++c) {
+              const int rb = P.kplan.width[c] * 2;
+              const uint32_t lay = sw_mode_for_row_bytes(rb);
+              for (int k = 0; k < P.kplan.width[c] / 16; ++k) {
+                const uint64_t ad = umma_desc(ks + P.kplan.off[c] + k * 32, 16, 8 * rb, lay);
+                const uint64_t bd = umma_desc(zb + P.kplan.off[c] + k * 32, 16, 8 * rb, lay);
+                umma_bf16(d, ad, bd, idesc_k, acc);
+                acc = 1;
+              }
+            }
+          }
+          umma_bf16(d, umma_desc(aug_a, 16, 256, kSw32), umma_desc(aug_b, 16, 256, kSw32), idesc_k, 1);
+          umma_commit(bar(misc->kempty[sk]));
+          umma_commit(bar(misc->ufull[ub]));
+          walker_advance(w, a);
+        }
+        if (i > 0) {
+          const int j = i - 1, sv = j % P.SV, jb = j & 1;
+          if (!(ok = mbar_wait(bar(misc->vfull[sv]), (j / P.SV) & 1, abort, a.status))) break;
+          if (!(ok = mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status))) break;
+          if (!(ok = mbar_wait(bar(misc->dvempty[jb]), ((j >> 1) & 1) ^ 1, abort, a.status))) break;
+          tc_fence_after();
+          const uint32_t vs = v_ring + sv * P.v_stage;
+          const uint32_t pb = p_buf + jb * 4096;
+          for (int mb = 0; mb < P.nvb; ++mb) {
+            const int c0 = P.vb_chunk[mb];
+            const int rb = P.vplan.width[c0] * 2;
+            const uint32_t lay = sw_mode_for_row_bytes(rb);
+            const uint32_t lbo = kTile * rb;        // next chunk of the block
+            const uint32_t d = tmem + 256 + (jb * kMaxVBlocks + mb) * 16;
+            for (int k = 0; k < kTile / 16; ++k) {
+              const uint64_t ad = umma_desc(vs + P.vplan.off[c0] + k * 16 * rb, lbo, 8 * rb, lay);
+              const uint64_t bd = umma_desc(pb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024, kSw128);
+              umma_bf16(d, ad, bd, idesc_v, k > 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(bar(misc->vempty[sv]));
+          umma_commit(bar(misc->dvfull[jb]));
+        }
+      }
+      // all issued MMAs complete before TMEM is released
+      umma_commit(bar(misc->mma_done));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else {
+    // ======================================================== epilogue (4 warps)
+    const int et = tid - 64;
+    const int q = warp & 3;             // TMEM lane quadrant of this warp
+    const int row = 32 * q + lane;      // token row within a tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+
+    // cos/sin(row * th_f): the tile-local half of the angle-sum rotation
+    float cl[64], sl[64];
+#pragma unroll
+    for (int f = 0; f < 64; f += 4) {
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.rope_cos + row * 64 + f));
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(a.rope_sin + row * 64 + f));
+      cl[f] = c4.x; cl[f + 1] = c4.y; cl[f + 2] = c4.z; cl[f + 3] = c4.w;
+      sl[f] = s4.x; sl[f + 1] = s4.y; sl[f + 2] = s4.z; sl[f + 3] = s4.w;
+    }
+
+    Walker w = start;
+    int cur_b = -1, cur_h = 0, nfin = 0;
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[kMaxVBlocks][4];
+#pragma unroll
+    for (int mb = 0; mb < kMaxVBlocks; ++mb)
+#pragma unroll
+      for (int n = 0; n < 4; ++n) acc[mb][n] = 0.f;
+    bool ok = true;
+
+    auto consume_d = [&](int j) -> bool {
+      const int jb = j & 1;
+      if (!warp_wait(bar(misc->dvfull[jb]), (j >> 1) & 1, abort, a.status)) return false;
+      if (!warp_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status)) return false;
+      tc_fence_after();
+      float al[4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) al[n] = misc->alpha[j & 3][n];
+#pragma unroll
+      for (int mb = 0; mb < kMaxVBlocks; ++mb) {
+        if (mb < P.nvb) {
+          float dv[4];
+          tmem_ld_x4(tmem + lane_base + 256 + (jb * kMaxVBlocks + mb) * 16, dv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int n = 0; n < 4; ++n) acc[mb][n] = fmaf(acc[mb][n], al[n], dv[n]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(misc->dvempty[jb]));
+      return true;
+    };
+
+    // Merge the four warps' softmax states of the finished unit and write this
+    // CTA's record (m, l, acc_v) for it.  The exchange uses an mbarrier with a
+    // bounded wait, so an aborted warp cannot leave the others stuck.
+    auto finalize = [&]() -> bool {
+      const int par = nfin & 1;
+      const uint32_t ph = (nfin >> 1) & 1;
+      ++nfin;
+      const float lw = warp_sum(l_run);
+      if (lane == 0) {
+        misc->stats[par][q][0] = m_run;
+        misc->stats[par][q][1] = lw;
+        mbar_arrive(bar(misc->statsbar[par]));
+      }
+      if (!warp_wait(bar(misc->statsbar[par]), ph, abort, a.status)) return false;
+      float mm[4], M = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) { mm[n] = misc->stats[par][n][0]; M = fmaxf(M, mm[n]); }
+      float sc[4], Lt = 0.f;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        sc[n] = (mm[n] == -INFINITY) ? 0.f : exp2f(mm[n] - M);
+        Lt += misc->stats[par][n][1] * sc[n];
+      }
+      const long long u = static_cast<long long>(cur_b) * a.H + cur_h;
+      float* rec = a.partials + (u + blockIdx.x) * (a.r_v + 2);
+      if (et == 0) { rec[0] = M; rec[1] = Lt; }
+#pragma unroll
+      for (int mb = 0; mb < kMaxVBlocks; ++mb) {
+        if (mb < P.nvb && row < P.vb_rows[mb]) {
+          float v = 0.f;
+#pragma unroll
+          for (int n = 0; n < 4; ++n) v = fmaf(acc[mb][n], sc[n], v);
+          rec[2 + P.vb_start[mb] + row] = v;
+        }
+      }
+      return true;
+    };
+
+    for (int i = 0; i < count && ok; ++i) {
+      const bool first = (i == 0) || w.t == 0;
+      if (first) {
+        compute_z(a, sm, w.b, w.h, et);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(misc->zfull));
+        if (i > 0) {
+          if (!(ok = consume_d(i - 1))) break;
+          if (!(ok = finalize())) break;
+        }
+        cur_b = w.b; cur_h = w.h;
+        m_run = -INFINITY; l_run = 0.f;
+#pragma unroll
+        for (int mb = 0; mb < kMaxVBlocks; ++mb)
+#pragma unroll
+          for (int n = 0; n < 4; ++n) acc[mb][n] = 0.f;
+      }
+      const int sv = i % P.SV, ub = i & 1;
+      if (!(ok = warp_wait(bar(misc->vfull[sv]), (i / P.SV) & 1, abort, a.status))) break;
+      if (!(ok = warp_wait(bar(misc->ufull[ub]), (i >> 1) & 1, abort, a.status))) break;
+      tc_fence_after();
+
+      // ---- rotary score from U
+      uint8_t* vstage = sm + P.v_ring + sv * P.v_stage;
+      const float4* tcos = reinterpret_cast<const float4*>(vstage + P.v_trig);
+      const float4* tsin = tcos + 16;
+      const uint32_t tU = tmem + lane_base + ub * 128;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float u1[16], u2[16];
+        tmem_ld_x16(tU + 16 * g, u1);
+        tmem_ld_x16(tU + 64 + 16 * g, u2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float4 cb = tcos[4 * g + k4], sb = tsin[4 * g + k4];
+          const float cbv[4] = {cb.x, cb.y, cb.z, cb.w};
+          const float sbv[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int f = 16 * g + 4 * k4 + kk, k = 4 * k4 + kk;
+            const float c = fmaf(cbv[kk], cl[f], -sbv[kk] * sl[f]);   // cos((j0+row) th_f)
+            const float s = fmaf(sbv[kk], cl[f], cbv[kk] * sl[f]);    // sin((j0+row) th_f)
+            s4[kk] = fmaf(c, u1[k], s4[kk]);
+            s4[kk] = fmaf(s, u2[k], s4[kk]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(misc->uempty[ub]));
+
+      // ---- online softmax (log2 domain, reference max per warp)
+      const bool valid = w.t * kTile + row < w.L;
+      const float s = valid ? (s4[0] + s4[1]) + (s4[2] + s4[3]) : -INFINITY;
+      const float m_new = fmaxf(m_run, warp_max(s));
+      float alpha, p;
+      if (m_new == -INFINITY) { alpha = 1.f; p = 0.f; }
+      else { alpha = exp2f(m_run - m_new); p = exp2f(s - m_new); }
+      const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+      l_run = fmaf(l_run, alpha, __bfloat162float(pb));
+      m_run = m_new;
+      {
+        uint8_t* pbuf = sm + P.p_buf + ub * 4096 + (row >> 6) * 2048;
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + swizzle_offset(q * 128 + (row & 63) * 2, 128)) = pb;
+      }
+      if (!valid) {
+        // rows past the sequence end may hold anything: zero them so 0 * x stays 0
+        for (int c = 0; c < P.vplan.n; ++c) {
+          const int rb = P.vplan.width[c] * 2;
+          for (int g = 0; g < rb / 16; ++g)
+            *reinterpret_cast<uint4*>(vstage + P.vplan.off[c] + swizzle_offset(row * rb + g * 16, rb)) =
+                make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (lane == 0) misc->alpha[i & 3][q] = alpha;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(misc->pfull[ub]));
+
+      if (!first) {
+        if (!(ok = consume_d(i - 1))) break;
+      }
+      walker_advance(w, a);
+    }
+    if (ok && consume_d(count - 1)) finalize();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// One block per (sequence, head): merge the per-CTA records of that unit,
+// apply the V up-projection once (Appendix J identity) and normalise.
+__global__ void __launch_bounds__(128)
+decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
+  __shared__ float accs[256];
+  const int u = blockIdx.x, tid = threadIdx.x;
+  const int b = u / a.H, h = u % a.H;
+  const int L = clamp_len(__ldg(a.seq_lens + b), a.L_max);
+  const int nb = (L + kTile - 1) / kTile;
+  float* out = a.out + static_cast<int64_t>(u) * kHeadDim;
+  if (nb == 0) {
+    out[tid] = 0.f;
+    if (tid == 0) a.lse[u] = -INFINITY;
+    return;
+  }
+  const long long total = static_cast<long long>(a.H) * a.prefix[a.B];
+  const long long per = max(1LL, (total + a.grid - 1) / a.grid);
+  const long long F0 = static_cast<long long>(a.H) * a.prefix[b] + static_cast<long long>(h) * nb;
+  const long long F1 = F0 + nb - 1;
+  const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
+  const int rs = a.r_v + 2;
+  const float* rec0 = a.partials + (static_cast<long long>(u) + c0) * rs;
+  float M = -INFINITY;
+  for (int c = 0; c <= c1 - c0; ++c) M = fmaxf(M, rec0[static_cast<long long>(c) * rs]);
+  float Lt = 0.f;
+  for (int c = 0; c <= c1 - c0; ++c) {
+    const float* r = rec0 + static_cast<long long>(c) * rs;
+    Lt += r[1] * exp2f(r[0] - M);
+  }
+  for (int i = tid; i < a.r_v; i += 128) {
+    float v = 0.f;
+    for (int c = 0; c <= c1 - c0; ++c) {
+      const float* r = rec0 + static_cast<long long>(c) * rs;
+      v = fmaf(r[2 + i], exp2f(r[0] - M), v);
+    }
+    accs[i] = v;
+  }
+  __syncthreads();
+  const __nv_bfloat16* Wv = static_cast<const __nv_bfloat16*>(a.w_up_v) +
+                            (static_cast<int64_t>(h) * kHeadDim + tid) * a.r_v;
+  float o = 0.f;
+  for (int i = 0; i < a.r_v; i += 8) {
+    float wv[8];
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(Wv + i)), wv);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o = fmaf(accs[i + k], wv[k], o);
+  }
+  const float mu = __ldg(a.mu_v + static_cast<int64_t>(h) * a.mu_hstride + tid);
+  out[tid] = o / Lt + mu;
+  if (tid == 0) a.lse[u] = (M + log2f(Lt)) * kLn2;
+}
+
+// ------------------------------------------------------------------ fp32 path
+
+// Scores s_j = RoPE(q).RoPE(k_j)/sqrt(d), k_j reconstructed per Eq. (3) in fp32.
+// Block = (unit, 128-token tile); thread = token.
+__global__ void __launch_bounds__(128)
+decode_f32_scores_kernel(const __grid_constant__ DecodeArgs a) {
+  __shared__ float qrot[kHeadDim];
+  __shared__ float ct[kTile][33];       // latent tile chunk [token][32 ranks]
+  __shared__ float wt[kHeadDim][33];    // W_up chunk [dim][32 ranks]
+  const int u = blockIdx.x, tid = threadIdx.x;
+  const int b = u / a.H, h = u % a.H;
+  const int L = clamp_len(__ldg(a.seq_lens + b), a.L_max);
+  const int j0 = blockIdx.y * kTile;
+  if (j0 >= L) return;
+  int qp = __ldg(a.q_pos + b);
+  if (qp < 0 || qp >= a.rope_len) {
+    if (tid == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
+    qp = qp < 0 ? 0 : static_cast<int>(a.rope_len - 1);
+  }
+  const float* qv = static_cast<const float*>(a.q) + static_cast<int64_t>(u) * kHeadDim;
+  if (tid < 64) {
+    const int f = tid;
+    const int i0 = a.rope_style == 0 ? f : 2 * f, i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
+    const float c = a.rope_cos[static_cast<int64_t>(qp) * 64 + f], s = a.rope_sin[static_cast<int64_t>(qp) * 64 + f];
+    qrot[i0] = qv[i0] * c - qv[i1] * s;
+    qrot[i1] = qv[i0] * s + qv[i1] * c;
+  }
+  const float* C = static_cast<const float*>(a.cache_k) + (static_cast<int64_t>(u) * a.L_max + j0) * a.r_k;
+  const float* W = static_cast<const float*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
+  const int rows = min(kTile, static_cast<int>(a.L_max - j0));
+  float kh[kHeadDim];
+#pragma unroll
+  for (int e = 0; e < kHeadDim; ++e) kh[e] = 0.f;
+  for (int k0 = 0; k0 < a.r_k; k0 += 32) {
+    const int kw = min(32, a.r_k - k0);
+    __syncthreads();
+    for (int idx = tid; idx < kTile * 32; idx += 128) {
+      const int r = idx / 32, k = idx % 32;
+      ct[r][k] = (r < rows && k < kw) ? C[static_cast<int64_t>(r) * a.r_k + k0 + k] : 0.f;
+      wt[r][k] = (k < kw) ? W[static_cast<int64_t>(r) * a.r_k + k0 + k] : 0.f;
+    }
+    __syncthreads();
+    for (int k = 0; k < 32; ++k) {
+      const float c = ct[tid][k];
+#pragma unroll
+      for (int e = 0; e < kHeadDim; ++e) kh[e] = fmaf(c, wt[e][k], kh[e]);
+    }
+  }
+  const int j = j0 + tid;
+  if (j < L) {
+    const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
+    float s = 0.f;
+#pragma unroll
+    for (int f = 0; f < 64; ++f) {
+      const int i0 = a.rope_style == 0 ? f : 2 * f, i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
+      const float k0v = kh[i0] + mu[i0], k1v = kh[i1] + mu[i1];
+      const float c = a.rope_cos[static_cast<int64_t>(j) * 64 + f], sn = a.rope_sin[static_cast<int64_t>(j) * 64 + f];
+      s = fmaf(qrot[i0], k0v * c - k1v * sn, s);
+      s = fmaf(qrot[i1], k0v * sn + k1v * c, s);
+    }
+    a.scores[static_cast<int64_t>(u) * a.L_max + j] = s * kInvSqrtD;
+  }
+}
+
+__device__ float block_reduce(float v, float* red, bool is_max) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  v = is_max ? warp_max(v) : warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < nw; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+  return r;
+}
+
+// Softmax over the unit's scores, then out = (sum_j p_j c_v,j) W_up,v,t^T / Z + mu_v,t.
+__global__ void __launch_bounds__(256)
+decode_f32_values_kernel(const __grid_constant__ DecodeArgs a) {
+  __shared__ float red[8];
+  __shared__ float accs[256];
+  const int u = blockIdx.x, tid = threadIdx.x;
+  const int b = u / a.H, h = u % a.H;
+  const int L = clamp_len(__ldg(a.seq_lens + b), a.L_max);
+  float* out = a.out + static_cast<int64_t>(u) * kHeadDim;
+  if (L == 0) {
+    if (tid < kHeadDim) out[tid] = 0.f;
+    if (tid == 0) a.lse[u] = -INFINITY;
+    return;
+  }
+  float* sc = a.scores + static_cast<int64_t>(u) * a.L_max;
+  float m = -INFINITY;
+  for (int j = tid; j < L; j += 256) m = fmaxf(m, sc[j]);
+  m = block_reduce(m, red, true);
+  float z = 0.f;
+  for (int j = tid; j < L; j += 256) {
+    const float p = expf(sc[j] - m);
+    sc[j] = p;
+    z += p;
+  }
+  z = block_reduce(z, red, false);   // also orders the p writes before the reads below
+  const float* Cv = static_cast<const float*>(a.cache_v) + static_cast<int64_t>(u) * a.L_max * a.r_v;
+  if (tid < a.r_v) {
+    float v = 0.f;
+    for (int j = 0; j < L; ++j) v = fmaf(sc[j], Cv[static_cast<int64_t>(j) * a.r_v + tid], v);
+    accs[tid] = v;
+  }
+  __syncthreads();
+  if (tid < kHeadDim) {
+    const float* Wv = static_cast<const float*>(a.w_up_v) + (static_cast<int64_t>(h) * kHeadDim + tid) * a.r_v;
+    float o = 0.f;
+    for (int i = 0; i < a.r_v; ++i) o = fmaf(accs[i], Wv[i], o);
+    out[tid] = o / z + a.mu_v[static_cast<int64_t>(h) * a.mu_hstride + tid];
+  }
+  if (tid == 0) a.lse[u] = m + logf(z);
+}
+
+}  // namespace
+
+bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
+  *p = DecodePlan{};
+  p->kplan = make_chunk_plan(r_k, kTile);
+  p->vplan = make_chunk_plan(r_v, kTile);
+  auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  p->v_trig = al(p->vplan.bytes, 16);
+  p->v_stage = al(p->v_trig + 512, 1024);
+  p->k_stage = al(p->kplan.bytes, 1024);
+  const int zbytes = al(p->kplan.bytes, 1024);
+  // Preference: hi+lo query operand with double-buffered rings, then hi only,
+  // then single-stage rings (large ranks).
+  const int tries[3][3] = {{2, 2, 2}, {1, 2, 2}, {1, 1, 1}};
+  int SK = 0, SV = 0, fixed = 0;
+  for (const auto& t : tries) {
+    p->zpasses = t[0];
+    fixed = p->zpasses * zbytes + 4096 + 4096 + 2 * 4096 + 2048 + 1024;
+    SK = t[1];
+    SV = t[2];
+    if (fixed + SK * p->k_stage + SV * p->v_stage <= kSmemLimit) break;
+    SK = 0;
+  }
+  if (SK == 0) return false;
+  auto fits = [&](int sk, int sv) { return fixed + sk * p->k_stage + sv * p->v_stage <= kSmemLimit; };
+  while (true) {
+    const bool tryk = SK <= SV;
+    if (tryk && SK < kMaxStages && fits(SK + 1, SV)) { ++SK; continue; }
+    if (SV < kMaxStages && fits(SK, SV + 1)) { ++SV; continue; }
+    if (!tryk && SK < kMaxStages && fits(SK + 1, SV)) { ++SK; continue; }
+    break;
+  }
+  p->SK = SK;
+  p->SV = SV;
+  int off = 0;
+  p->v_ring = off; off += SV * p->v_stage;
+  p->k_ring = off; off += SK * p->k_stage;
+  p->z_hi = off; off += zbytes;
+  p->z_lo = off; off += (p->zpasses == 2 ? zbytes : 0);
+  p->aug_a = off; off += 4096;
+  p->aug_b = off; off += 4096;
+  p->p_buf = off; off += 2 * 4096;
+  p->misc = off; off += 2048;
+  p->bytes = off + 1024;
+  // value MMA blocks: up to two 64-wide chunks per block, narrower chunks alone
+  p->nvb = 0;
+  for (int c = 0; c < p->vplan.n;) {
+    if (p->nvb >= kMaxVBlocks) return false;
+    const int w = p->vplan.width[c];
+    const int nch = (w == 64 && c + 1 < p->vplan.n && p->vplan.width[c + 1] == 64) ? 2 : 1;
+    p->vb_chunk[p->nvb] = c;
+    p->vb_rows[p->nvb] = w * nch;
+    p->vb_start[p->nvb] = p->vplan.start[c];
+    ++p->nvb;
+    c += nch;
+  }
+  // a 128-row value MMA of a narrow block reads up to 32 KB past its chunk
+  if (off - (p->v_ring + SV * p->v_stage) < 32768) return false;
+  return true;
+}
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s) {
+  static int configured = 0;
+  if (configured < a.plan.bytes) {
+    cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         a.plan.bytes);
+    if (e != cudaSuccess) return e;
+    configured = a.plan.bytes;
+  }
+  decode_bf16_kernel<<<a.grid, kDecodeThreads, a.plan.bytes, s>>>(a, maps);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_combine_kernel<<<a.B * a.H, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s) {
+  const dim3 g1(a.B * a.H, static_cast<unsigned>((a.L_max + kTile - 1) / kTile));
+  decode_f32_scores_kernel<<<g1, 128, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_f32_values_kernel<<<a.B * a.H, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace lla

@@ -1,0 +1,106 @@
+// lla_kernels.h — parameter blocks and launchers shared by the host API
+// (lla_api.cu) and the kernels (lla_decode.cu, lla_encode.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "lla_sm103.cuh"
+
+namespace lla {
+
+constexpr int kMaxStages = 8;
+constexpr int kMaxVBlocks = 4;
+constexpr int kMaxGrid = 1024;          // upper bound on decode CTAs (workspace sizing)
+constexpr int kDecodeThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
+constexpr int kSmemLimit = 232448;      // dynamic shared memory per block on sm_100/103
+
+// Shared-memory plan of the per-head bf16 decode kernel (byte offsets from a
+// 1024-aligned base).  The V ring comes first so that the M=128 value MMAs of
+// narrow chunks, which read whole 128-row atoms, stay inside the allocation.
+struct DecodePlan {
+  ChunkPlan kplan, vplan;            // latent chunks (128 rows)
+  int SK, SV;                        // ring depths
+  int zpasses;                       // 2: query operand as bf16 hi + lo, 1: hi only
+  int k_stage, v_stage;              // stage strides
+  int v_trig;                        // offset of the RoPE base rows inside a V stage
+  int v_ring, k_ring, z_hi, z_lo, aug_a, aug_b, p_buf, misc;
+  int bytes;                         // total dynamic smem incl. alignment slack
+  int nvb;                           // value MMA blocks (M = 128 rows each)
+  int vb_chunk[kMaxVBlocks], vb_rows[kMaxVBlocks], vb_start[kMaxVBlocks];
+};
+
+struct DecodeArgs {
+  int B, H, r_k, r_v, rope_style, grid;
+  int64_t L_max, rope_len, mu_hstride;
+  const void* q;                     // [B][H][128]
+  const int32_t* seq_lens;           // [B]
+  const int32_t* q_pos;              // [B]
+  const void* cache_k;               // fp32 path only (bf16 path reads via TMA)
+  const void* cache_v;
+  const void* w_up_k;                // loop-t slice [H][128][r_k]
+  const void* w_up_v;                // loop-t slice [H][128][r_v]
+  const float* mu_k;                 // loop-t slice: element (h, e) at mu_k[h*mu_hstride + e]
+  const float* mu_v;
+  const float* rope_cos;             // [rope_len][64]
+  const float* rope_sin;
+  float* out;                        // [B][H][128]
+  float* lse;                        // [B][H]
+  uint32_t* status;                  // workspace status word
+  int32_t* prefix;                   // [B+1] tile prefix over sequences
+  float* partials;                   // [(B*H + grid)][r_v + 2] split records
+  float* scores;                     // fp32 path: [B][H][L_max]
+  DecodePlan plan;
+};
+
+struct DecodeMaps {
+  CUtensorMap k[3];                  // latent K boxes of width 64 / 32 / 16
+  CUtensorMap v[3];
+};
+
+bool make_decode_plan(int r_k, int r_v, DecodePlan* p);
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
+cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
+
+// ----------------------------------------------------------------- encode
+
+struct EncodeArgs {
+  int N, H, Td, r_k, r_v, B;
+  int64_t L_max;
+  const void* x_k;                   // [N][H][Td]
+  const void* x_v;
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  const void* w_down_k;              // [H][Td][r_k]
+  const void* w_down_v;
+  const float* mu_k;                 // [H][Td]
+  const float* mu_v;
+  void* cache_k;
+  void* cache_v;
+  uint32_t* status;
+  float* bias;                       // workspace [2][H][256]: mu W_down per head/axis
+};
+
+struct EncodePlan {
+  ChunkPlan bk, bv;                  // W_down chunks (64 K-rows per stage)
+  int S;                             // ring depth
+  int stage;                         // stage stride
+  int a_off, b_off;                  // inside a stage
+  int ring, misc, bytes;
+  int tmem_cols;
+};
+
+struct EncodeMaps {
+  CUtensorMap xk, xv;                // box (64, 1, 128)
+  CUtensorMap wk[3], wv[3];          // box (w, 64, 1)
+};
+
+bool make_encode_plan(int r_k, int r_v, int Td, EncodePlan* p);
+cudaError_t launch_encode_bf16(const EncodeArgs& a, const EncodePlan& plan, const EncodeMaps& m,
+                               cudaStream_t s);
+cudaError_t launch_encode_f32(const EncodeArgs& a, cudaStream_t s);
+
+}  // namespace lla

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+function include/lla.h declares, and rejects invalid arguments before any launch."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from looped_transformer_cross_gb300 import build, lla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return lla.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(lla_[a-z0-9_]+)\s*\(", txt))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"lla_encode", "lla_decode_attn", "lla_workspace_size", "lla_rope_table",
+            "lla_device_status", "lla_status_string", "lla_abi_version"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.lla_abi_version() == 1
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert lla.status_string(s) and lla.status_string(s) != "unknown status"
+    assert lla.status_string(99) == "unknown status"
+
+
+def test_workspace_size_rules(L):
+    d = lla.dims(4, 16, 96, 160)
+    n = lla.workspace_size(d, 32, 4096)
+    assert n > 256
+    # grows with batch; fp32 mode adds the score buffer
+    assert lla.workspace_size(d, 64, 4096) > n
+    assert lla.workspace_size(lla.dims(4, 16, 96, 160, dtype=lla.LLA_F32), 32, 4096) > n + 32 * 16 * 4096 * 4 - 1
+    bad = lla.dims(4, 16, 96, 160, d_head=64)
+    assert L.lla_workspace_size(ctypes.byref(bad), 1, 16, 0) == 0
+    bad = lla.dims(4, 16, 90, 160)
+    assert L.lla_workspace_size(ctypes.byref(bad), 1, 16, 0) == 0
+
+
+def test_rope_table_is_fp64_rounded_once(L):
+    d = lla.dims(4, 2, 16, 32, rope_base=10000.0)
+    c, s = lla.rope_table(d, 5000)
+    p = np.arange(5000)[:, None].astype(np.float64)
+    theta = 10000.0 ** (-2.0 * np.arange(64) / 128.0)
+    np.testing.assert_array_equal(c.numpy(), np.cos(p * theta).astype(np.float32))
+    np.testing.assert_array_equal(s.numpy(), np.sin(p * theta).astype(np.float32))
+
+
+def _null_call(L, dm, **over):
+    args = dict(loop_t=0, q=None, B=1, L_max=128, rope_len=128, ws_bytes=1 << 20)
+    args.update(over)
+    cache = lla.Cache(None, None, args["B"], args["L_max"])
+    return L.lla_decode_attn(ctypes.byref(dm), args["loop_t"], args["q"], cache, None, None, None,
+                             None, None, None, None, None, args["rope_len"], None, None, None,
+                             args["ws_bytes"], None)
+
+
+def test_decode_rejects_bad_arguments_on_host(L):
+    good = lla.dims(4, 2, 96, 160)
+    assert _null_call(L, lla.dims(4, 2, 96, 160, d_head=64)) == lla.LLA_ERR_UNSUPPORTED
+    assert _null_call(L, lla.dims(4, 2, 100, 160)) == lla.LLA_ERR_UNSUPPORTED
+    assert _null_call(L, lla.dims(4, 2, 96, 272)) == lla.LLA_ERR_UNSUPPORTED
+    assert _null_call(L, lla.dims(0, 2, 96, 160)) == lla.LLA_ERR_INVALID_ARG
+    assert _null_call(L, lla.dims(4, 2, 96, 160, rope_base=-1.0)) == lla.LLA_ERR_INVALID_ARG
+    assert _null_call(L, good, loop_t=4) == lla.LLA_ERR_INVALID_ARG
+    assert _null_call(L, good, loop_t=-1) == lla.LLA_ERR_INVALID_ARG
+    assert _null_call(L, good) == lla.LLA_ERR_INVALID_ARG          # null pointers
+    assert _null_call(L, good, B=0) == lla.LLA_OK                   # nothing to do
+    assert L.lla_decode_attn(None, 0, None, lla.Cache(None, None, 1, 1), None, None, None, None,
+                             None, None, None, None, 1, None, None, None, 0, None) == lla.LLA_ERR_INVALID_ARG
+
+
+def test_encode_rejects_bad_arguments_on_host(L):
+    dm = lla.dims(4, 2, 96, 160)
+    cache = lla.Cache(None, None, 1, 16)
+    assert L.lla_encode(ctypes.byref(dm), None, None, 4, None, None, None, None, None, None, cache,
+                        None, 0, None) == lla.LLA_ERR_INVALID_ARG
+    assert L.lla_encode(ctypes.byref(dm), None, None, 0, None, None, None, None, None, None, cache,
+                        None, 0, None) == lla.LLA_OK
+    assert L.lla_encode(ctypes.byref(dm), None, None, -1, None, None, None, None, None, None, cache,
+                        None, 0, None) == lla.LLA_ERR_INVALID_ARG
+
+
+def test_misaligned_pointer_rejected(L):
+    dm = lla.dims(1, 1, 16, 16)
+    buf = (ctypes.c_char * 4096)()
+    base = ctypes.addressof(buf)
+    p = ctypes.c_void_p(base + (16 - base % 16) % 16 + 4)   # 4 bytes past a 16-byte boundary
+    cache = lla.Cache(p, p, 1, 128)
+    st = L.lla_decode_attn(ctypes.byref(dm), 0, p, cache, p, p, p, p, p, p, p, p, 128, p, p, p, 1 << 30, None)
+    assert st == lla.LLA_ERR_INVALID_ARG
