@@ -55,7 +55,7 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   WsLayout w{};
   size_t off = 256;  // status word
   w.prefix = off; off += al256(static_cast<size_t>(B + 1) * 4);
-  w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * (d->r_v + 2) * 4);
+  w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * 2 * (d->r_v + 2) * 4);
   w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
   w.scores = off;
   if (d->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * d->H * L_max * 4);

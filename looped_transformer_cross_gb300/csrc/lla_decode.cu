@@ -5,21 +5,25 @@
 //
 // Per-head bf16 path, one persistent CTA per SM:
 //   * Work is the flat list of 128-token latent tiles over (sequence, head),
-//     cut into equal contiguous ranges, one per CTA.  A (sequence, head) unit
-//     split between CTAs is merged afterwards from per-CTA records
-//     (m, l, acc_v) by the combine kernel (log-sum-exp merge).
+//     cut into equal contiguous ranges, one per CTA.  Each CTA writes one
+//     record (m, l, acc_v) per (sequence, head) unit it touches and per
+//     epilogue group; the combine kernel merges a unit's records (log-sum-exp
+//     merge) and applies the V up-projection.
 //   * Warp 0 streams latent tiles with TMA into two shared-memory rings (K and
 //     V), together with the RoPE row of the tile's base position.
 //   * Warp 1 issues tcgen05 MMAs.  Scores: U = C_k Z^T (+ bias) into TMEM, where
 //     Z folds the RoPE-rotated query into W_up,k,t (exact rewrite of
 //     q'.R_j (W c + mu)); Z is split into bf16 hi + lo so the product is
 //     accurate to ~fp32.  Values: D = C_v^T P with the softmax weights P of the
-//     tile as a 16-column operand — the V up-projection is applied once per
+//     tile as a 16-column operand -- the V up-projection is applied once per
 //     (sequence, head) at the end (Appendix J identity).
-//   * Warps 2-5 (one TMEM lane = one token each) turn U into the rotary score
-//     s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f}, keep a per-warp online
-//     softmax, write P, and accumulate D.  cos/sin(j th) come from the angle
-//     sum of the tile base row (in smem) and the lane's own row (registers).
+//   * Warps 2-9 form two epilogue groups of four warps (one per TMEM lane
+//     quadrant, one token per lane) that take alternate tiles, so two tiles are
+//     in flight.  Each turns U into the rotary score
+//     s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f}, keeps an online softmax
+//     per warp, writes P and accumulates D.  cos/sin(j th) come from the angle
+//     sum of the tile base row (shared memory) and the lane's own row (kept in
+//     TMEM).
 // Reconstructed keys and values never leave TMEM / registers.
 //
 // fp32 path: plain SIMT kernels (reconstruct k in registers, RoPE from the
@@ -39,17 +43,18 @@ constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
 struct alignas(16) DecodeMisc {
   uint64_t kfull[kMaxStages], kempty[kMaxStages];
   uint64_t vfull[kMaxStages], vempty[kMaxStages];
-  uint64_t ufull[2], uempty[2], pfull[2], dvfull[2], dvempty[2];
-  uint64_t zfull, mma_done, statsbar[2];
+  uint64_t ufull[2], uempty[2], pfull[2], dvfull[2], dvempty[2];  // index = tile & 1 = group
+  uint64_t zfull, zfree, mma_done;
+  uint64_t statsbar[2][2];   // [group][unit parity]
   uint32_t tmem_base;
   int abort;
   int start_b, start_h, start_t, count;
   int total_seq_tiles;
-  float alpha[4][4];         // [tile & 3][warp] softmax rescale of that tile
-  float stats[2][4][2];      // [unit parity][warp] (m, l)
+  float alpha[2][4][4];      // [group][(tile >> 1) & 3][quadrant] softmax rescale
+  float stats[2][2][4][2];   // [group][unit parity][quadrant] (m, l)
   int scan[kDecodeThreads];  // per-thread sequence-chunk tile counts
 };
-static_assert(sizeof(DecodeMisc) <= 2048, "misc region");
+static_assert(sizeof(DecodeMisc) <= 4096, "misc region");
 
 struct Walker {
   int b, h, t, nb, L;
@@ -231,11 +236,12 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       mbar_init(bar(misc->pfull[i]), 4);
       mbar_init(bar(misc->dvfull[i]), 1);
       mbar_init(bar(misc->dvempty[i]), 4);
+      mbar_init(bar(misc->statsbar[i][0]), 4);
+      mbar_init(bar(misc->statsbar[i][1]), 4);
     }
-    mbar_init(bar(misc->zfull), 128);
+    mbar_init(bar(misc->zfull), kTile);
+    mbar_init(bar(misc->zfree), 1);
     mbar_init(bar(misc->mma_done), 1);
-    mbar_init(bar(misc->statsbar[0]), 4);
-    mbar_init(bar(misc->statsbar[1]), 4);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -248,19 +254,40 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
   if (warp >= 2) {
     const int et = tid - 64;
     // constant bias operand: columns 0 and 1 of every row are 1 (they meet bias hi / lo)
-    const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
-    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32, 32)) = make_uint4(ones, 0, 0, 0);
-    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
-    // softmax-weight operands start at zero; each warp only ever writes its own row
+    if (et < kTile) {
+      const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
+      *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32, 32)) = make_uint4(ones, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
+    }
+    // softmax-weight operands start at zero; each quadrant only ever writes its own row
     uint4* pz = reinterpret_cast<uint4*>(sm + P.p_buf);
-    for (int i = et; i < 2 * 4096 / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
+    for (int i = et; i < 2 * 4096 / 16; i += 32 * kEpiWarps) pz[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-
+  if (warp >= 2 && warp < 6) {
+    // cos/sin(row * th_f), f < 64, of this lane's token row -> TMEM columns 384..511
+    // (the tile-local half of the angle-sum rotation, read back with every tile)
+    const int q = warp & 3, row = 32 * q + lane;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kTrigCol;
+    for (int h2 = 0; h2 < 4; ++h2) {
+      const float* src = (h2 < 2 ? a.rope_cos : a.rope_sin) + row * 64 + (h2 & 1) * 32;
+      float v[32];
+#pragma unroll
+      for (int f = 0; f < 32; f += 4) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(src + f));
+        v[f] = x.x; v[f + 1] = x.y; v[f + 2] = x.z; v[f + 3] = x.w;
+      }
+      tmem_st_x32(taddr + 32 * h2, v);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();   // the trig columns are read by both epilogue groups
+  tc_fence_after();
   const uint32_t v_ring = sbase + P.v_ring, k_ring = sbase + P.k_ring;
 
   if (warp == 0) {
@@ -345,6 +372,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           umma_commit(bar(misc->kempty[sk]));
           umma_commit(bar(misc->ufull[ub]));
           walker_advance(w, a);
+          // Z of this unit is free again once its last score MMA has completed
+          if (i + 1 == count || w.t == 0) umma_commit(bar(misc->zfree));
         }
         if (i > 0) {
           const int j = i - 1, sv = j % P.SV, jb = j & 1;
@@ -376,24 +405,21 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
   } else {
-    // ======================================================== epilogue (4 warps)
-    const int et = tid - 64;
+    // ======================================================== epilogue (2 groups x 4 warps)
+    // Group g processes tiles i with (i & 1) == g; warp q of a group owns TMEM
+    // lanes 32q..32q+31 (token rows).  Each group walks every tile of the range so
+    // that it sees every unit boundary: at each boundary it writes its record
+    // (possibly empty) for the finished unit, and the group owning the new unit's
+    // first tile prepares Z.
+    const int g = (warp - 2) >> 2;      // epilogue group
     const int q = warp & 3;             // TMEM lane quadrant of this warp
+    const int gt = (warp - 2) * 32 + lane - 128 * g;   // thread index inside the group
     const int row = 32 * q + lane;      // token row within a tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-
-    // cos/sin(row * th_f): the tile-local half of the angle-sum rotation
-    float cl[64], sl[64];
-#pragma unroll
-    for (int f = 0; f < 64; f += 4) {
-      const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.rope_cos + row * 64 + f));
-      const float4 s4 = __ldg(reinterpret_cast<const float4*>(a.rope_sin + row * 64 + f));
-      cl[f] = c4.x; cl[f + 1] = c4.y; cl[f + 2] = c4.z; cl[f + 3] = c4.w;
-      sl[f] = s4.x; sl[f + 1] = s4.y; sl[f + 2] = s4.z; sl[f + 3] = s4.w;
-    }
+    const uint32_t tT = tmem + lane_base + kTrigCol;
 
     Walker w = start;
-    int cur_b = -1, cur_h = 0, nfin = 0;
+    int cur_b = -1, cur_h = 0, nfin = 0, unit_ord = -1, pending = -1;
     float m_run = -INFINITY, l_run = 0.f;
     float acc[kMaxVBlocks][4];
 #pragma unroll
@@ -403,18 +429,18 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     bool ok = true;
 
     auto consume_d = [&](int j) -> bool {
-      const int jb = j & 1;
-      if (!warp_wait(bar(misc->dvfull[jb]), (j >> 1) & 1, abort, a.status)) return false;
-      if (!warp_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status)) return false;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!warp_wait(bar(misc->dvfull[g]), ph, abort, a.status)) return false;
+      if (!warp_wait(bar(misc->pfull[g]), ph, abort, a.status)) return false;
       tc_fence_after();
       float al[4];
 #pragma unroll
-      for (int n = 0; n < 4; ++n) al[n] = misc->alpha[j & 3][n];
+      for (int n = 0; n < 4; ++n) al[n] = misc->alpha[g][(j >> 1) & 3][n];
 #pragma unroll
       for (int mb = 0; mb < kMaxVBlocks; ++mb) {
         if (mb < P.nvb) {
           float dv[4];
-          tmem_ld_x4(tmem + lane_base + 256 + (jb * kMaxVBlocks + mb) * 16, dv);
+          tmem_ld_x4(tmem + lane_base + 256 + (g * kMaxVBlocks + mb) * 16, dv);
           tmem_wait_ld();
 #pragma unroll
           for (int n = 0; n < 4; ++n) acc[mb][n] = fmaf(acc[mb][n], al[n], dv[n]);
@@ -422,36 +448,40 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(misc->dvempty[jb]));
+      if (lane == 0) mbar_arrive(bar(misc->dvempty[g]));
       return true;
     };
 
-    // Merge the four warps' softmax states of the finished unit and write this
-    // CTA's record (m, l, acc_v) for it.  The exchange uses an mbarrier with a
+    // Merge the group's four warps' softmax states of the finished unit and write
+    // the group's record (m, l, acc_v).  The exchange uses an mbarrier with a
     // bounded wait, so an aborted warp cannot leave the others stuck.
     auto finalize = [&]() -> bool {
+      if (pending >= 0) {
+        if (!consume_d(pending)) return false;
+        pending = -1;
+      }
       const int par = nfin & 1;
       const uint32_t ph = (nfin >> 1) & 1;
       ++nfin;
       const float lw = warp_sum(l_run);
       if (lane == 0) {
-        misc->stats[par][q][0] = m_run;
-        misc->stats[par][q][1] = lw;
-        mbar_arrive(bar(misc->statsbar[par]));
+        misc->stats[g][par][q][0] = m_run;
+        misc->stats[g][par][q][1] = lw;
+        mbar_arrive(bar(misc->statsbar[g][par]));
       }
-      if (!warp_wait(bar(misc->statsbar[par]), ph, abort, a.status)) return false;
+      if (!warp_wait(bar(misc->statsbar[g][par]), ph, abort, a.status)) return false;
       float mm[4], M = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < 4; ++n) { mm[n] = misc->stats[par][n][0]; M = fmaxf(M, mm[n]); }
+      for (int n = 0; n < 4; ++n) { mm[n] = misc->stats[g][par][n][0]; M = fmaxf(M, mm[n]); }
       float sc[4], Lt = 0.f;
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
         sc[n] = (mm[n] == -INFINITY) ? 0.f : exp2f(mm[n] - M);
-        Lt += misc->stats[par][n][1] * sc[n];
+        Lt += misc->stats[g][par][n][1] * sc[n];
       }
       const long long u = static_cast<long long>(cur_b) * a.H + cur_h;
-      float* rec = a.partials + (u + blockIdx.x) * (a.r_v + 2);
-      if (et == 0) { rec[0] = M; rec[1] = Lt; }
+      float* rec = a.partials + ((u + blockIdx.x) * 2 + g) * (a.r_v + 2);
+      if (gt == 0) { rec[0] = M; rec[1] = Lt; }
 #pragma unroll
       for (int mb = 0; mb < kMaxVBlocks; ++mb) {
         if (mb < P.nvb && row < P.vb_rows[mb]) {
@@ -465,14 +495,16 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     };
 
     for (int i = 0; i < count && ok; ++i) {
-      const bool first = (i == 0) || w.t == 0;
-      if (first) {
-        compute_z(a, sm, w.b, w.h, et);
-        fence_proxy_async_smem();
-        mbar_arrive(bar(misc->zfull));
-        if (i > 0) {
-          if (!(ok = consume_d(i - 1))) break;
-          if (!(ok = finalize())) break;
+      if (i == 0 || w.t == 0) {
+        if (i > 0 && !(ok = finalize())) break;
+        ++unit_ord;
+        if ((i & 1) == g) {
+          // the previous unit's score MMAs must be complete before Z is overwritten
+          if (unit_ord > 0 && !(ok = mbar_wait(bar(misc->zfree), (unit_ord - 1) & 1, abort, a.status)))
+            break;
+          compute_z(a, sm, w.b, w.h, gt);
+          fence_proxy_async_smem();
+          mbar_arrive(bar(misc->zfull));
         }
         cur_b = w.b; cur_h = w.h;
         m_run = -INFINITY; l_run = 0.f;
@@ -481,41 +513,51 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
 #pragma unroll
           for (int n = 0; n < 4; ++n) acc[mb][n] = 0.f;
       }
-      const int sv = i % P.SV, ub = i & 1;
+      if ((i & 1) != g) { walker_advance(w, a); continue; }
+
+      const int sv = i % P.SV;
+      const uint32_t ph = (i >> 1) & 1;
       if (!(ok = warp_wait(bar(misc->vfull[sv]), (i / P.SV) & 1, abort, a.status))) break;
-      if (!(ok = warp_wait(bar(misc->ufull[ub]), (i >> 1) & 1, abort, a.status))) break;
+      if (!(ok = warp_wait(bar(misc->ufull[g]), ph, abort, a.status))) break;
       tc_fence_after();
 
-      // ---- rotary score from U
+      // ---- rotary score from U, 16 frequencies at a time
       uint8_t* vstage = sm + P.v_ring + sv * P.v_stage;
       const float4* tcos = reinterpret_cast<const float4*>(vstage + P.v_trig);
       const float4* tsin = tcos + 16;
-      const uint32_t tU = tmem + lane_base + ub * 128;
+      const uint32_t tU = tmem + lane_base + g * 128;
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float u1[16], u2[16];
-        tmem_ld_x16(tU + 16 * g, u1);
-        tmem_ld_x16(tU + 64 + 16 * g, u2);
+      for (int c16 = 0; c16 < 4; ++c16) {
+        float u1[16], u2[16], cl[16], sl[16];
+        tmem_ld_x16(tU + 16 * c16, u1);
+        tmem_ld_x16(tU + 64 + 16 * c16, u2);
+        tmem_ld_x16(tT + 16 * c16, cl);
+        tmem_ld_x16(tT + 64 + 16 * c16, sl);
         tmem_wait_ld();
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 cb = tcos[4 * g + k4], sb = tsin[4 * g + k4];
+          const float4 cb = tcos[4 * c16 + k4], sb = tsin[4 * c16 + k4];
           const float cbv[4] = {cb.x, cb.y, cb.z, cb.w};
           const float sbv[4] = {sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const int f = 16 * g + 4 * k4 + kk, k = 4 * k4 + kk;
+            const int f = 4 * k4 + kk;
             const float c = fmaf(cbv[kk], cl[f], -sbv[kk] * sl[f]);   // cos((j0+row) th_f)
-            const float s = fmaf(sbv[kk], cl[f], cbv[kk] * sl[f]);    // sin((j0+row) th_f)
-            s4[kk] = fmaf(c, u1[k], s4[kk]);
-            s4[kk] = fmaf(s, u2[k], s4[kk]);
+            const float sn = fmaf(sbv[kk], cl[f], cbv[kk] * sl[f]);   // sin((j0+row) th_f)
+            s4[kk] = fmaf(c, u1[f], s4[kk]);
+            s4[kk] = fmaf(sn, u2[f], s4[kk]);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(misc->uempty[ub]));
+      if (lane == 0) mbar_arrive(bar(misc->uempty[g]));
+
+      // The group's previous tile's value block, before P(i) is published: its
+      // pfull/dvfull phases must still be the latest ones of this group's barriers.
+      if (pending >= 0 && !(ok = consume_d(pending))) break;
+      pending = -1;
 
       // ---- online softmax (log2 domain, reference max per warp)
       const bool valid = w.t * kTile + row < w.L;
@@ -528,29 +570,26 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       l_run = fmaf(l_run, alpha, __bfloat162float(pb));
       m_run = m_new;
       {
-        uint8_t* pbuf = sm + P.p_buf + ub * 4096 + (row >> 6) * 2048;
+        uint8_t* pbuf = sm + P.p_buf + g * 4096 + (row >> 6) * 2048;
         *reinterpret_cast<__nv_bfloat16*>(pbuf + swizzle_offset(q * 128 + (row & 63) * 2, 128)) = pb;
       }
       if (!valid) {
         // rows past the sequence end may hold anything: zero them so 0 * x stays 0
         for (int c = 0; c < P.vplan.n; ++c) {
           const int rb = P.vplan.width[c] * 2;
-          for (int g = 0; g < rb / 16; ++g)
-            *reinterpret_cast<uint4*>(vstage + P.vplan.off[c] + swizzle_offset(row * rb + g * 16, rb)) =
+          for (int k = 0; k < rb / 16; ++k)
+            *reinterpret_cast<uint4*>(vstage + P.vplan.off[c] + swizzle_offset(row * rb + k * 16, rb)) =
                 make_uint4(0, 0, 0, 0);
         }
       }
-      if (lane == 0) misc->alpha[i & 3][q] = alpha;
+      if (lane == 0) misc->alpha[g][(i >> 1) & 3][q] = alpha;
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(misc->pfull[ub]));
-
-      if (!first) {
-        if (!(ok = consume_d(i - 1))) break;
-      }
+      if (lane == 0) mbar_arrive(bar(misc->pfull[g]));
+      pending = i;
       walker_advance(w, a);
     }
-    if (ok && consume_d(count - 1)) finalize();
+    if (ok) finalize();
   }
 
   tc_fence_before();
@@ -583,19 +622,22 @@ decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
   const long long F1 = F0 + nb - 1;
   const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
   const int rs = a.r_v + 2;
-  const float* rec0 = a.partials + (static_cast<long long>(u) + c0) * rs;
+  // records of this unit: one per (CTA c in [c0, c1], epilogue group); a group
+  // that saw no token of the unit in that CTA wrote m = -inf, l = 0, acc = 0
+  const float* rec0 = a.partials + (static_cast<long long>(u) + c0) * 2 * rs;
+  const int nrec = 2 * (c1 - c0 + 1);
   float M = -INFINITY;
-  for (int c = 0; c <= c1 - c0; ++c) M = fmaxf(M, rec0[static_cast<long long>(c) * rs]);
+  for (int c = 0; c < nrec; ++c) M = fmaxf(M, rec0[static_cast<long long>(c) * rs]);
   float Lt = 0.f;
-  for (int c = 0; c <= c1 - c0; ++c) {
+  for (int c = 0; c < nrec; ++c) {
     const float* r = rec0 + static_cast<long long>(c) * rs;
-    Lt += r[1] * exp2f(r[0] - M);
+    if (r[0] != -INFINITY) Lt += r[1] * exp2f(r[0] - M);
   }
   for (int i = tid; i < a.r_v; i += 128) {
     float v = 0.f;
-    for (int c = 0; c <= c1 - c0; ++c) {
+    for (int c = 0; c < nrec; ++c) {
       const float* r = rec0 + static_cast<long long>(c) * rs;
-      v = fmaf(r[2 + i], exp2f(r[0] - M), v);
+      if (r[0] != -INFINITY) v = fmaf(r[2 + i], exp2f(r[0] - M), v);
     }
     accs[i] = v;
   }
@@ -747,7 +789,7 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
   int SK = 0, SV = 0, fixed = 0;
   for (const auto& t : tries) {
     p->zpasses = t[0];
-    fixed = p->zpasses * zbytes + 4096 + 4096 + 2 * 4096 + 2048 + 1024;
+    fixed = p->zpasses * zbytes + 4096 + 4096 + 2 * 4096 + 4096 + 1024;
     SK = t[1];
     SV = t[2];
     if (fixed + SK * p->k_stage + SV * p->v_stage <= kSmemLimit) break;
@@ -772,7 +814,7 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
   p->aug_a = off; off += 4096;
   p->aug_b = off; off += 4096;
   p->p_buf = off; off += 2 * 4096;
-  p->misc = off; off += 2048;
+  p->misc = off; off += 4096;
   p->bytes = off + 1024;
   // value MMA blocks: up to two 64-wide chunks per block, narrower chunks alone
   p->nvb = 0;

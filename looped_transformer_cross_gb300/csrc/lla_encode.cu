@@ -43,7 +43,7 @@ __device__ __forceinline__ bool slot_ok(const EncodeArgs& a, int sid, int p) {
   return sid >= 0 && sid < a.B && p >= 0 && p < a.L_max;
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+__global__ void __launch_bounds__(kEncodeThreads, 1)
 encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__ EncodePlan P,
                    const __grid_constant__ EncodeMaps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -229,7 +229,7 @@ cudaError_t launch_encode_bf16(const EncodeArgs& a, const EncodePlan& plan, cons
     configured = plan.bytes;
   }
   const dim3 grid((a.N + 127) / 128, a.H, 2);
-  encode_bf16_kernel<<<grid, kDecodeThreads, plan.bytes, s>>>(a, plan, m);
+  encode_bf16_kernel<<<grid, kEncodeThreads, plan.bytes, s>>>(a, plan, m);
   return cudaGetLastError();
 }
 

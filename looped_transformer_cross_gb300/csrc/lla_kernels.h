@@ -14,7 +14,10 @@ namespace lla {
 constexpr int kMaxStages = 8;
 constexpr int kMaxVBlocks = 4;
 constexpr int kMaxGrid = 1024;          // upper bound on decode CTAs (workspace sizing)
-constexpr int kDecodeThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
+constexpr int kDecodeThreads = 320;     // producer warp, MMA warp, 8 epilogue warps
+constexpr int kEpiWarps = 8;           // decode epilogue warps: two groups of four
+constexpr int kTrigCol = 384;           // TMEM columns 384..511: per-lane cos/sin(row * th_f)
+constexpr int kEncodeThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
 constexpr int kSmemLimit = 232448;      // dynamic shared memory per block on sm_100/103
 
 // Shared-memory plan of the per-head bf16 decode kernel (byte offsets from a
@@ -50,7 +53,7 @@ struct DecodeArgs {
   float* lse;                        // [B][H]
   uint32_t* status;                  // workspace status word
   int32_t* prefix;                   // [B+1] tile prefix over sequences
-  float* partials;                   // [(B*H + grid)][r_v + 2] split records
+  float* partials;                   // [(B*H + grid) * 2][r_v + 2] records per (unit, CTA, group)
   float* scores;                     // fp32 path: [B][H][L_max]
   DecodePlan plan;
 };
