@@ -142,6 +142,37 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
                            float* out, float* lse,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/* Size of the fixed scratch array behind lla_decode_attn_noalloc (8 MiB). */
+#define LLA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * lla_decode_attn_noalloc — lla_decode_attn without a caller workspace, for
+ * callers that cannot allocate device memory (for example a plugin inside a
+ * host framework whose memory pool owns the GPU, or a serving path that must
+ * never call cudaMalloc).  The paper has no counterpart: this is a deployment
+ * convenience.  Arguments and results are those of lla_decode_attn, minus
+ * `workspace` and `ws_bytes`.
+ *   - Scratch lives in a fixed __device__ array of LLA_NOALLOC_SCRATCH_BYTES
+ *     inside this library; every GPU that loads the library keeps it until
+ *     the process exits.  The call allocates nothing.
+ *   - Shapes whose workspace (lla_workspace_size) exceeds that size return
+ *     LLA_ERR_UNSUPPORTED before any launch (e.g. beyond about 5,400 sequence-heads
+ *     at r_v = 160).
+ *   - The first call on each device looks up the array's device address with
+ *     the device current; make that first call before any stream capture.
+ *   - The array is shared by every call and keeps the last call's contents;
+ *     the status word is cleared on `stream` before each launch.  Calls that
+ *     overlap on the GPU race and must be serialised by the caller.  The
+ *     kernels' device status of this variant is not readable through
+ *     lla_device_status (there is no workspace pointer to pass).
+ */
+lla_status lla_decode_attn_noalloc(const lla_dims* dims, int loop_t, const void* q,
+                                   lla_cache cache, const int32_t* seq_lens, const int32_t* q_pos,
+                                   const void* w_up_k, const void* w_up_v,
+                                   const float* mu_k, const float* mu_v,
+                                   const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                                   float* out, float* lse, void* stream);
+
 /* Workspace bytes for calls with at most B sequences of L_max slots and
  * encode batches of at most max_N tokens, on the current CUDA device.
  * Returns 0 for invalid dims. */

@@ -179,3 +179,24 @@ class Decoder:
                     self.w_up_v, self.mu_k, self.mu_v, self.rope_cos, self.rope_sin, out, lse,
                     self.workspace, stream)
         return out, lse
+
+
+def decode_attn_noalloc(dm: Dims, loop_t: int, q, cache_k, cache_v, seq_lens, q_pos, w_up_k,
+                        w_up_v, mu_k, mu_v, rope_cos, rope_sin, out, lse, stream=None):
+    """lla_decode_attn_noalloc: lla_decode_attn with the library's fixed device scratch
+    instead of a caller workspace, for callers that cannot allocate device memory.
+    Calls that overlap on the GPU race on that scratch; make the first call on a
+    device before any stream capture."""
+    f = lib().lla_decode_attn_noalloc
+    if f.restype is not ctypes.c_int:
+        vp = ctypes.c_void_p
+        f.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, vp, Cache, vp, vp, vp, vp, vp, vp, vp, vp,
+                      ctypes.c_int64, vp, vp, vp]
+        f.restype = ctypes.c_int
+    B = int(cache_k.shape[0])
+    L_max = int(cache_k.shape[2] if dm.variant == LLA_PER_HEAD else cache_k.shape[1])
+    cache = Cache(ctypes.c_void_p(cache_k.data_ptr()), ctypes.c_void_p(cache_v.data_ptr()), B, L_max)
+    st = f(ctypes.byref(dm), int(loop_t), _ptr(q), cache, _ptr(seq_lens), _ptr(q_pos), _ptr(w_up_k),
+           _ptr(w_up_v), _ptr(mu_k), _ptr(mu_v), _ptr(rope_cos), _ptr(rope_sin),
+           int(rope_cos.shape[0]), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "lla_decode_attn_noalloc")
