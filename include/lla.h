@@ -156,7 +156,7 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
  *     inside this library; every GPU that loads the library keeps it until
  *     the process exits.  The call allocates nothing.
  *   - Shapes whose workspace (lla_workspace_size) exceeds that size return
- *     LLA_ERR_UNSUPPORTED before any launch (e.g. beyond about 5,400 sequence-heads
+ *     LLA_ERR_UNSUPPORTED before any launch (e.g. beyond about 2,100 sequence-heads
  *     at r_v = 160).
  *   - The first call on each device looks up the array's device address with
  *     the device current; make that first call before any stream capture.

@@ -55,7 +55,7 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   WsLayout w{};
   size_t off = 256;  // status word
   w.prefix = off; off += al256(static_cast<size_t>(B + 1) * 4);
-  w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * 2 * (d->r_v + 2) * 4);
+  w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * kRecordsPerCta * (d->r_v + kRecordHead) * 4);
   w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
   w.scores = off;
   if (d->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * d->H * L_max * 4);
@@ -199,12 +199,9 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
                      units, w, kTile, 1))
       return LLA_ERR_CUDA;
   }
-  for (int c = 0; c < a.plan.vplan.n; ++c) {
-    const int w = a.plan.vplan.width[c];
-    if (!make_map_3d(&maps.v[chunk_map_index(w)], cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows,
-                     units, w, kTile, 1))
-      return LLA_ERR_CUDA;
-  }
+  // V latents: 64-column boxes (the last one zero-filled past r_v), 128B swizzle
+  if (!make_map_3d(&maps.v[0], cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 64, kTile, 1))
+    return LLA_ERR_CUDA;
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 

@@ -3,31 +3,27 @@
 // Transformers", arXiv 2607.15456v2: §3 Eq. (2)-(3), "RoPE and
 // reconstruction", §7 latent-store path, Appendix J "Absorbed attention").
 //
-// Per-head bf16 path, one persistent CTA per SM:
+// Per-head bf16 path, one persistent CTA per SM (6 warps):
 //   * Work is the flat list of 128-token latent tiles over (sequence, head),
-//     cut into equal contiguous ranges, one per CTA.  Each CTA writes one
-//     record (m, l, acc_v) per (sequence, head) unit it touches and per
-//     epilogue group; the combine kernel merges a unit's records (log-sum-exp
-//     merge) and applies the V up-projection.
-//   * Warp 0 streams latent tiles with TMA into two shared-memory rings (K and
-//     V), together with the RoPE row of the tile's base position.
+//     cut into equal contiguous ranges, one per CTA.  For each (sequence, head)
+//     unit it touches a CTA writes one record (m, l, acc_v) per epilogue warp;
+//     the combine kernel merges a unit's records (log-sum-exp merge) and applies
+//     the V up-projection once (Appendix J identity).
+//   * Warp 0 streams latent tiles with TMA into a K ring and a V ring, together
+//     with the RoPE row of the tile's base position.
 //   * Warp 1 issues tcgen05 MMAs.  Scores: U = C_k Z^T (+ bias) into TMEM, where
 //     Z folds the RoPE-rotated query into W_up,k,t (exact rewrite of
-//     q'.R_j (W c + mu)); Z is split into bf16 hi + lo so the product is
-//     accurate to ~fp32.  Values: D = C_v^T P with the softmax weights P of the
-//     tile as a 16-column operand -- the V up-projection is applied once per
-//     (sequence, head) at the end (Appendix J identity).
-//   * Warps 2-9 form two epilogue groups of four warps (one per TMEM lane
-//     quadrant, one token per lane) that take alternate tiles, so two tiles are
-//     in flight.  Each turns U into the rotary score
-//     s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f}, keeps an online softmax
-//     per warp, writes P and accumulates D.  cos/sin(j th) come from the angle
-//     sum of the tile base row (shared memory) and the lane's own row (kept in
-//     TMEM).
+//     q'.R_j (W c + mu)).  Values: D += P C_v, with the tile's softmax weights P
+//     read from TMEM (written over the consumed scores) and the V latent tile as
+//     an MN-major operand, accumulating over the whole unit in TMEM.
+//   * Warps 2-5 (one per TMEM lane quadrant, one token per lane) turn U into the
+//     rotary score s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f}, run an
+//     online softmax per warp (P row 32q of D belongs to warp q) and write P.
+//     cos/sin(j th) come from the angle sum of the tile base row (shared memory)
+//     and the lane's own row (registers).  A warp rescales its accumulator row
+//     only when its running max grows by more than 2^8.
 // Reconstructed keys and values never leave TMEM / registers.
 //
-// fp32 path: plain SIMT kernels (reconstruct k in registers, RoPE from the
-// table, exact softmax), used for the 1e-5 parity mode.
 #include "lla_kernels.h"
 
 #include <cmath>
@@ -39,22 +35,21 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
+constexpr float kRescaleLog2 = 8.f;                 // lazy rescale threshold (log2 units)
+constexpr int kDCol = 256;                          // TMEM columns of the value accumulator
 
 struct alignas(16) DecodeMisc {
   uint64_t kfull[kMaxStages], kempty[kMaxStages];
   uint64_t vfull[kMaxStages], vempty[kMaxStages];
-  uint64_t ufull[2], uempty[2], pfull[2], dvfull[2], dvempty[2];  // index = tile & 1 = group
-  uint64_t zfull, zfree, mma_done;
-  uint64_t statsbar[2][2];   // [group][unit parity]
+  uint64_t ufull[2], pfull[2], vdone[2];   // index = tile & 1
+  uint64_t zfull, dfree, mma_done;
   uint32_t tmem_base;
   int abort;
   int start_b, start_h, start_t, count;
   int total_seq_tiles;
-  float alpha[2][4][4];      // [group][(tile >> 1) & 3][quadrant] softmax rescale
-  float stats[2][2][4][2];   // [group][unit parity][quadrant] (m, l)
   int scan[kDecodeThreads];  // per-thread sequence-chunk tile counts
 };
-static_assert(sizeof(DecodeMisc) <= 4096, "misc region");
+static_assert(sizeof(DecodeMisc) <= 2048, "misc region");
 
 struct Walker {
   int b, h, t, nb, L;
@@ -232,62 +227,34 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     for (int s = 0; s < P.SV; ++s) { mbar_init(bar(misc->vfull[s]), 1); mbar_init(bar(misc->vempty[s]), 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(misc->ufull[i]), 1);
-      mbar_init(bar(misc->uempty[i]), 4);
       mbar_init(bar(misc->pfull[i]), 4);
-      mbar_init(bar(misc->dvfull[i]), 1);
-      mbar_init(bar(misc->dvempty[i]), 4);
-      mbar_init(bar(misc->statsbar[i][0]), 4);
-      mbar_init(bar(misc->statsbar[i][1]), 4);
+      mbar_init(bar(misc->vdone[i]), 1);
     }
     mbar_init(bar(misc->zfull), kTile);
-    mbar_init(bar(misc->zfree), 1);
+    mbar_init(bar(misc->dfree), 4);
     mbar_init(bar(misc->mma_done), 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < 3; ++i) { prefetch_tmap(&maps.k[i]); prefetch_tmap(&maps.v[i]); }
+    for (int i = 0; i < 3; ++i) prefetch_tmap(&maps.k[i]);
+    prefetch_tmap(&maps.v[0]);
   }
   if (warp == 1) {
     __syncwarp();
     tmem_alloc(smem_u32(&misc->tmem_base), 512);
   }
   if (warp >= 2) {
-    const int et = tid - 64;
     // constant bias operand: columns 0 and 1 of every row are 1 (they meet bias hi / lo)
-    if (et < kTile) {
-      const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
-      *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32, 32)) = make_uint4(ones, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
-    }
-    // softmax-weight operands start at zero; each quadrant only ever writes its own row
-    uint4* pz = reinterpret_cast<uint4*>(sm + P.p_buf);
-    for (int i = et; i < 2 * 4096 / 16; i += 32 * kEpiWarps) pz[i] = make_uint4(0, 0, 0, 0);
+    const int et = tid - 64;
+    const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
+    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32, 32)) = make_uint4(ones, 0, 0, 0);
+    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(et * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-  if (warp >= 2 && warp < 6) {
-    // cos/sin(row * th_f), f < 64, of this lane's token row -> TMEM columns 384..511
-    // (the tile-local half of the angle-sum rotation, read back with every tile)
-    const int q = warp & 3, row = 32 * q + lane;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kTrigCol;
-    for (int h2 = 0; h2 < 4; ++h2) {
-      const float* src = (h2 < 2 ? a.rope_cos : a.rope_sin) + row * 64 + (h2 & 1) * 32;
-      float v[32];
-#pragma unroll
-      for (int f = 0; f < 32; f += 4) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(src + f));
-        v[f] = x.x; v[f + 1] = x.y; v[f + 2] = x.z; v[f + 3] = x.w;
-      }
-      tmem_st_x32(taddr + 32 * h2, v);
-    }
-    tmem_wait_st();
-  }
-  tc_fence_before();
-  __syncthreads();   // the trig columns are read by both epilogue groups
-  tc_fence_after();
   const uint32_t v_ring = sbase + P.v_ring, k_ring = sbase + P.k_ring;
 
   if (warp == 0) {
@@ -310,9 +277,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
         const uint32_t vb = bar(misc->vfull[sv]);
         mbar_arrive_expect_tx(vb, P.vplan.bytes + 512);
         const uint32_t vs = v_ring + sv * P.v_stage;
-        for (int c = 0; c < P.vplan.n; ++c)
-          tma_load_3d(vs + P.vplan.off[c], &maps.v[chunk_map_index(P.vplan.width[c])], vb,
-                      P.vplan.start[c], y, z);
+        for (int c = 0; c < P.vplan.n; ++c) tma_load_3d(vs + P.vplan.off[c], &maps.v[0], vb, P.vplan.start[c], y, z);
         bulk_load(vs + P.v_trig, a.rope_cos + static_cast<int64_t>(y) * 64, 256, vb);
         bulk_load(vs + P.v_trig + 256, a.rope_sin + static_cast<int64_t>(y) * 64, 256, vb);
         issued_v = i + 1;
@@ -332,72 +297,75 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     }
   } else if (warp == 1) {
     // ======================================================== MMA issuer
+    // Order per tile: K(i) then V(i-1); at a unit boundary V(i-1) goes first, so
+    // the epilogue can read out the finished unit before it prepares Z for the
+    // next one.  MMAs run in issue order, so K(i) into U[i & 1] never overtakes
+    // V(i-2), which reads P(i-2) from the same columns.
     if (lane == 0) {
       const uint32_t idesc_k = umma_idesc_bf16(128, 128, false, false);
-      const uint32_t idesc_v = umma_idesc_bf16(128, 16, true, false);
-      const uint32_t z_hi = sbase + P.z_hi, z_lo = sbase + P.z_lo;
-      const uint32_t aug_a = sbase + P.aug_a, aug_b = sbase + P.aug_b;
-      const uint32_t p_buf = sbase + P.p_buf;
-      Walker w = start;
-      int zph = 0;
+      const uint32_t idesc_v = umma_idesc_bf16(128, a.r_v, false, true);
+      const uint64_t daa = umma_desc(sbase + P.aug_a, 16, 256, kSw32);
+      const uint64_t dab = umma_desc(sbase + P.aug_b, 16, 256, kSw32);
+      // V tile as the MN-major B operand: 64-column chunks 16 KB apart (LBO), 8
+      // token rows 1 KB apart (SBO); a 16-token K step is +2 KB (+128 in the field)
+      const uint64_t dv0 = umma_desc(v_ring, kTile * 128, 1024, kSw128);
+      const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4, vst = static_cast<uint32_t>(P.v_stage) >> 4;
       bool ok = true;
+      auto issue_v = [&](int j, bool first_of_unit, int unit) -> bool {
+        const int sv = j % P.SV, jb = j & 1;
+        if (!mbar_wait(bar(misc->vfull[sv]), (j / P.SV) & 1, abort, a.status)) return false;
+        if (!mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status)) return false;
+        if (first_of_unit && unit > 0 && !mbar_wait(bar(misc->dfree), (unit - 1) & 1, abort, a.status))
+          return false;
+        tc_fence_after();
+        const uint64_t b0 = dv0 + sv * vst;
+        const uint32_t pa = tmem + jb * 128;
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          umma_bf16_ts(tmem + kDCol, pa + 8 * k, b0 + 128 * k, idesc_v, (first_of_unit && k == 0) ? 0u : 1u);
+        umma_commit(bar(misc->vempty[sv]));
+        umma_commit(bar(misc->vdone[jb]));
+        return true;
+      };
+      Walker w = start;
+      int zph = 0, unit = -1, prev_unit = -1;
+      bool prev_first = false;
       for (int i = 0; i <= count && ok; ++i) {
+        const bool first = i < count && (i == 0 || w.t == 0);
+        if (first) ++unit;
+        if (i > 0 && first && !(ok = issue_v(i - 1, prev_first, prev_unit))) break;
         if (i < count) {
-          if (i == 0 || w.t == 0) {
+          if (first) {
             if (!(ok = mbar_wait(bar(misc->zfull), zph, abort, a.status))) break;
             zph ^= 1;
           }
           const int sk = i % P.SK, ub = i & 1;
           if (!(ok = mbar_wait(bar(misc->kfull[sk]), (i / P.SK) & 1, abort, a.status))) break;
-          if (!(ok = mbar_wait(bar(misc->uempty[ub]), ((i >> 1) & 1) ^ 1, abort, a.status))) break;
           tc_fence_after();
           const uint32_t d = tmem + ub * 128;
-          const uint32_t ks = k_ring + sk * P.k_stage;
+          const uint32_t so = sk * kst;
           uint32_t acc = 0;
-#pragma unroll 1
           for (int pass = 0; pass < P.zpasses; ++pass) {
-            const uint32_t zb = pass == 0 ? z_hi : z_lo;
+            const uint32_t zreg = sbase + (pass == 0 ? P.z_hi : P.z_lo);
             for (int c = 0; c < P.kplan.n; ++c) {
               const int rb = P.kplan.width[c] * 2;
               const uint32_t lay = sw_mode_for_row_bytes(rb);
+              const uint64_t a0 = umma_desc(k_ring + P.kplan.off[c], 16, 8 * rb, lay) + so;
+              const uint64_t b0 = umma_desc(zreg + P.kplan.off[c], 16, 8 * rb, lay);
               for (int k = 0; k < P.kplan.width[c] / 16; ++k) {
-                const uint64_t ad = umma_desc(ks + P.kplan.off[c] + k * 32, 16, 8 * rb, lay);
-                const uint64_t bd = umma_desc(zb + P.kplan.off[c] + k * 32, 16, 8 * rb, lay);
-                umma_bf16(d, ad, bd, idesc_k, acc);
+                umma_bf16(d, a0 + 2 * k, b0 + 2 * k, idesc_k, acc);
                 acc = 1;
               }
             }
           }
-          umma_bf16(d, umma_desc(aug_a, 16, 256, kSw32), umma_desc(aug_b, 16, 256, kSw32), idesc_k, 1);
+          umma_bf16(d, daa, dab, idesc_k, 1);
           umma_commit(bar(misc->kempty[sk]));
           umma_commit(bar(misc->ufull[ub]));
           walker_advance(w, a);
-          // Z of this unit is free again once its last score MMA has completed
-          if (i + 1 == count || w.t == 0) umma_commit(bar(misc->zfree));
         }
-        if (i > 0) {
-          const int j = i - 1, sv = j % P.SV, jb = j & 1;
-          if (!(ok = mbar_wait(bar(misc->vfull[sv]), (j / P.SV) & 1, abort, a.status))) break;
-          if (!(ok = mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status))) break;
-          if (!(ok = mbar_wait(bar(misc->dvempty[jb]), ((j >> 1) & 1) ^ 1, abort, a.status))) break;
-          tc_fence_after();
-          const uint32_t vs = v_ring + sv * P.v_stage;
-          const uint32_t pb = p_buf + jb * 4096;
-          for (int mb = 0; mb < P.nvb; ++mb) {
-            const int c0 = P.vb_chunk[mb];
-            const int rb = P.vplan.width[c0] * 2;
-            const uint32_t lay = sw_mode_for_row_bytes(rb);
-            const uint32_t lbo = kTile * rb;        // next chunk of the block
-            const uint32_t d = tmem + 256 + (jb * kMaxVBlocks + mb) * 16;
-            for (int k = 0; k < kTile / 16; ++k) {
-              const uint64_t ad = umma_desc(vs + P.vplan.off[c0] + k * 16 * rb, lbo, 8 * rb, lay);
-              const uint64_t bd = umma_desc(pb + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024, kSw128);
-              umma_bf16(d, ad, bd, idesc_v, k > 0 ? 1u : 0u);
-            }
-          }
-          umma_commit(bar(misc->vempty[sv]));
-          umma_commit(bar(misc->dvfull[jb]));
-        }
+        if (i > 0 && !first && !(ok = issue_v(i - 1, prev_first, prev_unit))) break;
+        prev_first = first;
+        prev_unit = unit;
       }
       // all issued MMAs complete before TMEM is released
       umma_commit(bar(misc->mma_done));
@@ -405,191 +373,156 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
   } else {
-    // ======================================================== epilogue (2 groups x 4 warps)
-    // Group g processes tiles i with (i & 1) == g; warp q of a group owns TMEM
-    // lanes 32q..32q+31 (token rows).  Each group walks every tile of the range so
-    // that it sees every unit boundary: at each boundary it writes its record
-    // (possibly empty) for the finished unit, and the group owning the new unit's
-    // first tile prepares Z.
-    const int g = (warp - 2) >> 2;      // epilogue group
+    // ======================================================== epilogue (4 warps)
+    const int et = tid - 64;
     const int q = warp & 3;             // TMEM lane quadrant of this warp
-    const int gt = (warp - 2) * 32 + lane - 128 * g;   // thread index inside the group
     const int row = 32 * q + lane;      // token row within a tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t tT = tmem + lane_base + kTrigCol;
+
+    // cos/sin(row * th_f): the tile-local half of the angle-sum rotation
+    float cl[64], sl[64];
+#pragma unroll
+    for (int f = 0; f < 64; f += 4) {
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.rope_cos + row * 64 + f));
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(a.rope_sin + row * 64 + f));
+      cl[f] = c4.x; cl[f + 1] = c4.y; cl[f + 2] = c4.z; cl[f + 3] = c4.w;
+      sl[f] = s4.x; sl[f + 1] = s4.y; sl[f + 2] = s4.z; sl[f + 3] = s4.w;
+    }
 
     Walker w = start;
-    int cur_b = -1, cur_h = 0, nfin = 0, unit_ord = -1, pending = -1;
-    float m_run = -INFINITY, l_run = 0.f;
-    float acc[kMaxVBlocks][4];
-#pragma unroll
-    for (int mb = 0; mb < kMaxVBlocks; ++mb)
-#pragma unroll
-      for (int n = 0; n < 4; ++n) acc[mb][n] = 0.f;
+    int cur_b = -1, cur_h = 0;
+    float m_ref = -INFINITY, l_run = 0.f;
     bool ok = true;
 
-    auto consume_d = [&](int j) -> bool {
-      const uint32_t ph = (j >> 1) & 1;
-      if (!warp_wait(bar(misc->dvfull[g]), ph, abort, a.status)) return false;
-      if (!warp_wait(bar(misc->pfull[g]), ph, abort, a.status)) return false;
+    // Read out this warp's accumulator row of the finished unit (its last value MMA
+    // was tile `last`) and write the warp's record (m, l, acc_v).
+    auto finalize = [&](int last) -> bool {
+      if (!warp_wait(bar(misc->vdone[last & 1]), (last >> 1) & 1, abort, a.status)) return false;
       tc_fence_after();
-      float al[4];
+      const float lw = warp_sum(l_run);
+      const long long u = static_cast<long long>(cur_b) * a.H + cur_h;
+      float* rec = a.partials + ((u + blockIdx.x) * kRecordsPerCta + q) * (a.r_v + kRecordHead);
+      if (lane == 0) { rec[0] = m_ref; rec[1] = lw; }
+      for (int c = 0; c < a.r_v; c += 32) {
+        float v[32];
+        tmem_ld_x32(tmem + lane_base + kDCol + c, v);
+        tmem_wait_ld();
+        if (lane == 0) {
 #pragma unroll
-      for (int n = 0; n < 4; ++n) al[n] = misc->alpha[g][(j >> 1) & 3][n];
-#pragma unroll
-      for (int mb = 0; mb < kMaxVBlocks; ++mb) {
-        if (mb < P.nvb) {
-          float dv[4];
-          tmem_ld_x4(tmem + lane_base + 256 + (g * kMaxVBlocks + mb) * 16, dv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int n = 0; n < 4; ++n) acc[mb][n] = fmaf(acc[mb][n], al[n], dv[n]);
+          for (int k = 0; k < 32; k += 4)
+            if (c + k < a.r_v)
+              *reinterpret_cast<float4*>(rec + kRecordHead + c + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(misc->dvempty[g]));
-      return true;
-    };
-
-    // Merge the group's four warps' softmax states of the finished unit and write
-    // the group's record (m, l, acc_v).  The exchange uses an mbarrier with a
-    // bounded wait, so an aborted warp cannot leave the others stuck.
-    auto finalize = [&]() -> bool {
-      if (pending >= 0) {
-        if (!consume_d(pending)) return false;
-        pending = -1;
-      }
-      const int par = nfin & 1;
-      const uint32_t ph = (nfin >> 1) & 1;
-      ++nfin;
-      const float lw = warp_sum(l_run);
-      if (lane == 0) {
-        misc->stats[g][par][q][0] = m_run;
-        misc->stats[g][par][q][1] = lw;
-        mbar_arrive(bar(misc->statsbar[g][par]));
-      }
-      if (!warp_wait(bar(misc->statsbar[g][par]), ph, abort, a.status)) return false;
-      float mm[4], M = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 4; ++n) { mm[n] = misc->stats[g][par][n][0]; M = fmaxf(M, mm[n]); }
-      float sc[4], Lt = 0.f;
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        sc[n] = (mm[n] == -INFINITY) ? 0.f : exp2f(mm[n] - M);
-        Lt += misc->stats[g][par][n][1] * sc[n];
-      }
-      const long long u = static_cast<long long>(cur_b) * a.H + cur_h;
-      float* rec = a.partials + ((u + blockIdx.x) * 2 + g) * (a.r_v + 2);
-      if (gt == 0) { rec[0] = M; rec[1] = Lt; }
-#pragma unroll
-      for (int mb = 0; mb < kMaxVBlocks; ++mb) {
-        if (mb < P.nvb && row < P.vb_rows[mb]) {
-          float v = 0.f;
-#pragma unroll
-          for (int n = 0; n < 4; ++n) v = fmaf(acc[mb][n], sc[n], v);
-          rec[2 + P.vb_start[mb] + row] = v;
-        }
-      }
+      if (lane == 0) mbar_arrive(bar(misc->dfree));
       return true;
     };
 
     for (int i = 0; i < count && ok; ++i) {
       if (i == 0 || w.t == 0) {
-        if (i > 0 && !(ok = finalize())) break;
-        ++unit_ord;
-        if ((i & 1) == g) {
-          // the previous unit's score MMAs must be complete before Z is overwritten
-          if (unit_ord > 0 && !(ok = mbar_wait(bar(misc->zfree), (unit_ord - 1) & 1, abort, a.status)))
-            break;
-          compute_z(a, sm, w.b, w.h, gt);
-          fence_proxy_async_smem();
-          mbar_arrive(bar(misc->zfull));
-        }
+        if (i > 0 && !(ok = finalize(i - 1))) break;
+        compute_z(a, sm, w.b, w.h, et);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(misc->zfull));
         cur_b = w.b; cur_h = w.h;
-        m_run = -INFINITY; l_run = 0.f;
-#pragma unroll
-        for (int mb = 0; mb < kMaxVBlocks; ++mb)
-#pragma unroll
-          for (int n = 0; n < 4; ++n) acc[mb][n] = 0.f;
+        m_ref = -INFINITY; l_run = 0.f;
       }
-      if ((i & 1) != g) { walker_advance(w, a); continue; }
-
-      const int sv = i % P.SV;
-      const uint32_t ph = (i >> 1) & 1;
+      const int sv = i % P.SV, ub = i & 1;
       if (!(ok = warp_wait(bar(misc->vfull[sv]), (i / P.SV) & 1, abort, a.status))) break;
-      if (!(ok = warp_wait(bar(misc->ufull[g]), ph, abort, a.status))) break;
+      if (!(ok = warp_wait(bar(misc->ufull[ub]), (i >> 1) & 1, abort, a.status))) break;
       tc_fence_after();
 
-      // ---- rotary score from U, 16 frequencies at a time
+      // ---- rotary score from U, 32 frequencies at a time
       uint8_t* vstage = sm + P.v_ring + sv * P.v_stage;
       const float4* tcos = reinterpret_cast<const float4*>(vstage + P.v_trig);
       const float4* tsin = tcos + 16;
-      const uint32_t tU = tmem + lane_base + g * 128;
+      const uint32_t tU = tmem + lane_base + ub * 128;
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16) {
-        float u1[16], u2[16], cl[16], sl[16];
-        tmem_ld_x16(tU + 16 * c16, u1);
-        tmem_ld_x16(tU + 64 + 16 * c16, u2);
-        tmem_ld_x16(tT + 16 * c16, cl);
-        tmem_ld_x16(tT + 64 + 16 * c16, sl);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float u1[32], u2[32];
+        tmem_ld_x32(tU + 32 * h2, u1);
+        tmem_ld_x32(tU + 64 + 32 * h2, u2);
         tmem_wait_ld();
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 cb = tcos[4 * c16 + k4], sb = tsin[4 * c16 + k4];
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 cb = tcos[8 * h2 + k4], sb = tsin[8 * h2 + k4];
           const float cbv[4] = {cb.x, cb.y, cb.z, cb.w};
           const float sbv[4] = {sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const int f = 4 * k4 + kk;
+            const int f = 32 * h2 + 4 * k4 + kk, k = 4 * k4 + kk;
             const float c = fmaf(cbv[kk], cl[f], -sbv[kk] * sl[f]);   // cos((j0+row) th_f)
             const float sn = fmaf(sbv[kk], cl[f], cbv[kk] * sl[f]);   // sin((j0+row) th_f)
-            s4[kk] = fmaf(c, u1[f], s4[kk]);
-            s4[kk] = fmaf(sn, u2[f], s4[kk]);
+            s4[kk] = fmaf(c, u1[k], s4[kk]);
+            s4[kk] = fmaf(sn, u2[k], s4[kk]);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(misc->uempty[g]));
 
-      // The group's previous tile's value block, before P(i) is published: its
-      // pfull/dvfull phases must still be the latest ones of this group's barriers.
-      if (pending >= 0 && !(ok = consume_d(pending))) break;
-      pending = -1;
-
-      // ---- online softmax (log2 domain, reference max per warp)
+      // ---- online softmax (log2 domain, lazy per-warp reference)
       const bool valid = w.t * kTile + row < w.L;
       const float s = valid ? (s4[0] + s4[1]) + (s4[2] + s4[3]) : -INFINITY;
-      const float m_new = fmaxf(m_run, warp_max(s));
-      float alpha, p;
-      if (m_new == -INFINITY) { alpha = 1.f; p = 0.f; }
-      else { alpha = exp2f(m_run - m_new); p = exp2f(s - m_new); }
-      const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-      l_run = fmaf(l_run, alpha, __bfloat162float(pb));
-      m_run = m_new;
-      {
-        uint8_t* pbuf = sm + P.p_buf + g * 4096 + (row >> 6) * 2048;
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + swizzle_offset(q * 128 + (row & 63) * 2, 128)) = pb;
-      }
-      if (!valid) {
-        // rows past the sequence end may hold anything: zero them so 0 * x stays 0
-        for (int c = 0; c < P.vplan.n; ++c) {
-          const int rb = P.vplan.width[c] * 2;
-          for (int k = 0; k < rb / 16; ++k)
-            *reinterpret_cast<uint4*>(vstage + P.vplan.off[c] + swizzle_offset(row * rb + k * 16, rb)) =
-                make_uint4(0, 0, 0, 0);
+      const float m_tile = warp_max(s);
+      if (m_tile > m_ref + kRescaleLog2) {
+        if (m_ref != -INFINITY) {
+          // the accumulator row must be at rest: V(i-1) complete (V(i-2) already is,
+          // as K(i) was issued after it and we hold U(i))
+          if (!(ok = warp_wait(bar(misc->vdone[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort, a.status))) break;
+          tc_fence_after();
+          const float alpha = exp2f(m_ref - m_tile);
+          for (int c = 0; c < a.r_v; c += 32) {
+            float v[32];
+            tmem_ld_x32(tmem + lane_base + kDCol + c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= alpha;
+            tmem_st_x32(tmem + lane_base + kDCol + c, v);
+          }
+          tmem_wait_st();
+          l_run *= alpha;
         }
+        m_ref = m_tile;
       }
-      if (lane == 0) misc->alpha[g][(i >> 1) & 3][q] = alpha;
-      fence_proxy_async_smem();
+      const float p = valid ? exp2f(s - m_ref) : 0.f;
+      const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+      l_run += __bfloat162float(pb);
+
+      // ---- P row 32q of this tile into TMEM (over the consumed scores): lane 0 of
+      // the warp holds p of the warp's 32 tokens packed in columns 16q..16q+15,
+      // every other entry of this warp's lanes is zero
+      {
+        const uint32_t pbits = static_cast<uint32_t>(__bfloat16_as_ushort(pb));
+        const uint32_t pair = pbits | (__shfl_down_sync(0xffffffffu, pbits, 1) << 16);
+        uint32_t mine[16], zero[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t v = __shfl_sync(0xffffffffu, pair, 2 * c);
+          mine[c] = lane == 0 ? v : 0u;
+          zero[c] = 0u;
+        }
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) tmem_st_x16(tU + 16 * blk, blk == q ? mine : zero);
+      }
+      if (__any_sync(0xffffffffu, !valid)) {
+        if (!valid) {
+          // rows past the sequence end may hold anything: zero them so 0 * x stays 0
+          for (int c = 0; c < P.vplan.n; ++c)
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4*>(vstage + P.vplan.off[c] + swizzle_offset(row * 128 + k * 16, 128)) =
+                  make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(misc->pfull[g]));
-      pending = i;
+      if (lane == 0) mbar_arrive(bar(misc->pfull[ub]));
       walker_advance(w, a);
     }
-    if (ok) finalize();
+    if (ok) finalize(count - 1);
   }
 
   tc_fence_before();
@@ -621,11 +554,11 @@ decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
   const long long F0 = static_cast<long long>(a.H) * a.prefix[b] + static_cast<long long>(h) * nb;
   const long long F1 = F0 + nb - 1;
   const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
-  const int rs = a.r_v + 2;
-  // records of this unit: one per (CTA c in [c0, c1], epilogue group); a group
-  // that saw no token of the unit in that CTA wrote m = -inf, l = 0, acc = 0
-  const float* rec0 = a.partials + (static_cast<long long>(u) + c0) * 2 * rs;
-  const int nrec = 2 * (c1 - c0 + 1);
+  const int rs = a.r_v + kRecordHead;
+  // records of this unit: one per (CTA c in [c0, c1], epilogue warp); a warp that
+  // saw no token of the unit in that CTA wrote m = -inf, l = 0, acc = 0
+  const float* rec0 = a.partials + (static_cast<long long>(u) + c0) * kRecordsPerCta * rs;
+  const int nrec = kRecordsPerCta * (c1 - c0 + 1);
   float M = -INFINITY;
   for (int c = 0; c < nrec; ++c) M = fmaxf(M, rec0[static_cast<long long>(c) * rs]);
   float Lt = 0.f;
@@ -637,7 +570,7 @@ decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
     float v = 0.f;
     for (int c = 0; c < nrec; ++c) {
       const float* r = rec0 + static_cast<long long>(c) * rs;
-      if (r[0] != -INFINITY) v = fmaf(r[2 + i], exp2f(r[0] - M), v);
+      if (r[0] != -INFINITY) v = fmaf(r[kRecordHead + i], exp2f(r[0] - M), v);
     }
     accs[i] = v;
   }
@@ -777,19 +710,20 @@ decode_f32_values_kernel(const __grid_constant__ DecodeArgs a) {
 bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
   *p = DecodePlan{};
   p->kplan = make_chunk_plan(r_k, kTile);
-  p->vplan = make_chunk_plan(r_v, kTile);
+  p->vplan = make_chunk_plan_64(r_v, kTile);
   auto al = [](int x, int a) { return (x + a - 1) / a * a; };
   p->v_trig = al(p->vplan.bytes, 16);
   p->v_stage = al(p->v_trig + 512, 1024);
   p->k_stage = al(p->kplan.bytes, 1024);
   const int zbytes = al(p->kplan.bytes, 1024);
-  // Preference: hi+lo query operand with double-buffered rings, then hi only,
-  // then single-stage rings (large ranks).
-  const int tries[3][3] = {{2, 2, 2}, {1, 2, 2}, {1, 1, 1}};
+  // One score pass with the query operand in bf16 (score error ~1e-3 relative);
+  // a second (lo) pass doubles the operand reads of the score MMAs.  Prefer
+  // double-buffered rings; single-stage rings only for the largest ranks.
+  const int tries[2][3] = {{1, 2, 2}, {1, 1, 1}};
   int SK = 0, SV = 0, fixed = 0;
   for (const auto& t : tries) {
     p->zpasses = t[0];
-    fixed = p->zpasses * zbytes + 4096 + 4096 + 2 * 4096 + 4096 + 1024;
+    fixed = p->zpasses * zbytes + 4096 + 4096 + 2048 + 1024;
     SK = t[1];
     SV = t[2];
     if (fixed + SK * p->k_stage + SV * p->v_stage <= kSmemLimit) break;
@@ -797,11 +731,13 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
   }
   if (SK == 0) return false;
   auto fits = [&](int sk, int sv) { return fixed + sk * p->k_stage + sv * p->v_stage <= kSmemLimit; };
+  // The V stage is held longest (until the value MMA, after the softmax), so
+  // deepen the V ring first.
   while (true) {
-    const bool tryk = SK <= SV;
-    if (tryk && SK < kMaxStages && fits(SK + 1, SV)) { ++SK; continue; }
-    if (SV < kMaxStages && fits(SK, SV + 1)) { ++SV; continue; }
-    if (!tryk && SK < kMaxStages && fits(SK + 1, SV)) { ++SK; continue; }
+    const bool tryv = SV <= SK;
+    if (tryv && SV < kMaxStages && fits(SK, SV + 1)) { ++SV; continue; }
+    if (SK < kMaxStages && fits(SK + 1, SV)) { ++SK; continue; }
+    if (!tryv && SV < kMaxStages && fits(SK, SV + 1)) { ++SV; continue; }
     break;
   }
   p->SK = SK;
@@ -813,23 +749,8 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
   p->z_lo = off; off += (p->zpasses == 2 ? zbytes : 0);
   p->aug_a = off; off += 4096;
   p->aug_b = off; off += 4096;
-  p->p_buf = off; off += 2 * 4096;
-  p->misc = off; off += 4096;
+  p->misc = off; off += 2048;
   p->bytes = off + 1024;
-  // value MMA blocks: up to two 64-wide chunks per block, narrower chunks alone
-  p->nvb = 0;
-  for (int c = 0; c < p->vplan.n;) {
-    if (p->nvb >= kMaxVBlocks) return false;
-    const int w = p->vplan.width[c];
-    const int nch = (w == 64 && c + 1 < p->vplan.n && p->vplan.width[c + 1] == 64) ? 2 : 1;
-    p->vb_chunk[p->nvb] = c;
-    p->vb_rows[p->nvb] = w * nch;
-    p->vb_start[p->nvb] = p->vplan.start[c];
-    ++p->nvb;
-    c += nch;
-  }
-  // a 128-row value MMA of a narrow block reads up to 32 KB past its chunk
-  if (off - (p->v_ring + SV * p->v_stage) < 32768) return false;
   return true;
 }
 

@@ -12,27 +12,24 @@
 namespace lla {
 
 constexpr int kMaxStages = 8;
-constexpr int kMaxVBlocks = 4;
 constexpr int kMaxGrid = 1024;          // upper bound on decode CTAs (workspace sizing)
-constexpr int kDecodeThreads = 320;     // producer warp, MMA warp, 8 epilogue warps
-constexpr int kEpiWarps = 8;           // decode epilogue warps: two groups of four
-constexpr int kTrigCol = 384;           // TMEM columns 384..511: per-lane cos/sin(row * th_f)
+constexpr int kDecodeThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
+constexpr int kRecordsPerCta = 4;       // split records per (unit, CTA): one per epilogue warp
+constexpr int kRecordHead = 4;          // record = {m, l, -, -, acc[r_v]}: acc 16-byte aligned
 constexpr int kEncodeThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
 constexpr int kSmemLimit = 232448;      // dynamic shared memory per block on sm_100/103
 
 // Shared-memory plan of the per-head bf16 decode kernel (byte offsets from a
-// 1024-aligned base).  The V ring comes first so that the M=128 value MMAs of
-// narrow chunks, which read whole 128-row atoms, stay inside the allocation.
+// 1024-aligned base).
 struct DecodePlan {
-  ChunkPlan kplan, vplan;            // latent chunks (128 rows)
+  ChunkPlan kplan;                   // K latent chunks (64/32/16 wide, 128 rows)
+  ChunkPlan vplan;                   // V latent chunks, padded to 64 wide
   int SK, SV;                        // ring depths
   int zpasses;                       // 2: query operand as bf16 hi + lo, 1: hi only
   int k_stage, v_stage;              // stage strides
   int v_trig;                        // offset of the RoPE base rows inside a V stage
-  int v_ring, k_ring, z_hi, z_lo, aug_a, aug_b, p_buf, misc;
+  int v_ring, k_ring, z_hi, z_lo, aug_a, aug_b, misc;
   int bytes;                         // total dynamic smem incl. alignment slack
-  int nvb;                           // value MMA blocks (M = 128 rows each)
-  int vb_chunk[kMaxVBlocks], vb_rows[kMaxVBlocks], vb_start[kMaxVBlocks];
 };
 
 struct DecodeArgs {
@@ -53,7 +50,7 @@ struct DecodeArgs {
   float* lse;                        // [B][H]
   uint32_t* status;                  // workspace status word
   int32_t* prefix;                   // [B+1] tile prefix over sequences
-  float* partials;                   // [(B*H + grid) * 2][r_v + 2] records per (unit, CTA, group)
+  float* partials;                   // [(B*H + kMaxGrid) * 4][r_v + 4] records per (unit, CTA, warp)
   float* scores;                     // fp32 path: [B][H][L_max]
   DecodePlan plan;
 };

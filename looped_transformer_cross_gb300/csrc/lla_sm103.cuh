@@ -65,6 +65,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete may be suspended
+// for up to `hint_ns` (resuming as soon as the phase completes), so waiting
+// warps do not take issue slots from the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Bounded: after
 // about one second, or as soon as another role has raised *abort, it records
 // LLA_ERR_TIMEOUT (first expiry only) and returns false.
@@ -73,7 +87,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       record_status(status, LLA_ERR_TIMEOUT);
@@ -83,13 +97,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Warp-collective form: every lane polls, the warp leaves converged and with
-// one decision (a lane that expired at the limit while another saw the phase
-// complete makes the whole warp report failure).
+// Warp-collective form: lane 0 alone polls (polls from every lane would crowd
+// the shared-memory pipe that tcgen05 and TMA traffic also use), then the warp
+// synchronises, which orders lane 0's acquire of the phase before every lane's
+// later reads, and all lanes leave converged with lane 0's decision.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
-  const bool ok = mbar_wait(bar, parity, abort, status);
-  return __all_sync(0xffffffffu, ok);
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // ----------------------------------------------------------------- TMA
@@ -166,13 +183,25 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn_m
          | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Issue one MMA.  No "memory" clobber: the operands are read by the async proxy,
+// ordered by the mbarrier waits before and the tcgen05.commit after (both of
+// which carry one); volatile keeps issue order among the tcgen05 statements.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// Same, with the A operand read from tensor memory (K-major: row m = TMEM lane m,
+// 16 bf16 elements of K packed two per 32-bit column, lower index in the low half).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive on `bar` once all previously issued tcgen05 operations of this thread
@@ -236,6 +265,16 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, float (&v)[32]) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 16 consecutive 32-bit columns of this thread's lane (32x32b shape).
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 
 // Store 32 consecutive columns of this thread's lane (32x32b shape).
@@ -302,6 +341,17 @@ struct ChunkPlan {
   int off[6];       // byte offset of chunk c in a 128-row tile
   int bytes;        // bytes of a 128-row tile (all chunks)
 };
+
+// Rank r padded to 64-element chunks (the tail chunk's missing columns are
+// zero-filled by TMA): uniform 128-byte rows, so one MN-major operand spans them.
+__host__ __device__ inline ChunkPlan make_chunk_plan_64(int r, int rows) {
+  ChunkPlan p{};
+  for (int e = 0; e < r; e += 64) {
+    p.start[p.n] = e; p.width[p.n] = 64; p.off[p.n] = p.n * rows * 128; ++p.n;
+  }
+  p.bytes = p.n * rows * 128;
+  return p;
+}
 
 __host__ __device__ inline ChunkPlan make_chunk_plan(int r, int rows) {
   ChunkPlan p{};
