@@ -48,8 +48,14 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t prefix, partials, bias, scores, total;
+  size_t prefix, partials, bias, scores, zimg, zimg_stride, total;
 };
+
+// Bytes of one unit's query-operand image: Z (128 rows x r_k bf16, K-chunk
+// layout) followed by the 4 KB bias operand, padded to 128 bytes.
+size_t zimg_stride(int r_k) {
+  return (static_cast<size_t>(make_chunk_plan(r_k, kTile).bytes) + 4096 + 127) / 128 * 128;
+}
 
 WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   WsLayout w{};
@@ -59,6 +65,9 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
   w.scores = off;
   if (d->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * d->H * L_max * 4);
+  w.zimg = off;
+  w.zimg_stride = zimg_stride(d->r_k);
+  if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(B) * d->H * w.zimg_stride);
   w.total = off;
   return w;
 }
@@ -181,6 +190,8 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   a.prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
   a.partials = reinterpret_cast<float*>(ws + wl.partials);
   a.scores = reinterpret_cast<float*>(ws + wl.scores);
+  a.zimg = ws + wl.zimg;
+  a.zimg_stride = static_cast<int64_t>(wl.zimg_stride);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (dims->dtype == LLA_F32) return launch_decode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
@@ -199,8 +210,8 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
                      units, w, kTile, 1))
       return LLA_ERR_CUDA;
   }
-  // V latents: 64-column boxes (the last one zero-filled past r_v), 128B swizzle
-  if (!make_map_3d(&maps.v[0], cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 64, kTile, 1))
+  // V latents: 32-column boxes (a tail box zero-filled past r_v), 64B swizzle
+  if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 32, kTile, 1))
     return LLA_ERR_CUDA;
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }

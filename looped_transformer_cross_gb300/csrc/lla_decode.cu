@@ -3,25 +3,28 @@
 // Transformers", arXiv 2607.15456v2: §3 Eq. (2)-(3), "RoPE and
 // reconstruction", §7 latent-store path, Appendix J "Absorbed attention").
 //
-// Per-head bf16 path, one persistent CTA per SM (6 warps):
+// Per-head bf16 path, one persistent CTA per SM (7 warps):
 //   * Work is the flat list of 128-token latent tiles over (sequence, head),
 //     cut into equal contiguous ranges, one per CTA.  For each (sequence, head)
 //     unit it touches a CTA writes one record (m, l, acc_v) per epilogue warp;
 //     the combine kernel merges a unit's records (log-sum-exp merge) and applies
 //     the V up-projection once (Appendix J identity).
-//   * Warp 0 streams latent tiles with TMA into a K ring and a V ring, together
-//     with the RoPE row of the tile's base position.
-//   * Warp 1 issues tcgen05 MMAs.  Scores: U = C_k Z^T (+ bias) into TMEM, where
-//     Z folds the RoPE-rotated query into W_up,k,t (exact rewrite of
-//     q'.R_j (W c + mu)).  Values: D += P C_v, with the tile's softmax weights P
+//   * Warp 0 streams latent tiles with TMA into a K ring and a V ring (V tile i
+//     requested after K tile i+1: it is needed only once tile i's weights exist).
+//   * Warp 1 issues the score MMAs: U = C_k Z^T (+ bias) into TMEM, where Z folds
+//     the RoPE-rotated query into W_up,k,t (exact rewrite of q'.R_j (W c + mu)).
+//     Z of each unit comes ready-made from decode_z_kernel; the producer copies
+//     the next unit's image in while the current one runs (two buffers).
+//   * Warp 6 issues the value MMAs: D += P C_v, with the tile's softmax weights P
 //     read from TMEM (written over the consumed scores) and the V latent tile as
 //     an MN-major operand, accumulating over the whole unit in TMEM.
 //   * Warps 2-5 (one per TMEM lane quadrant, one token per lane) turn U into the
 //     rotary score s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f}, run an
-//     online softmax per warp (P row 32q of D belongs to warp q) and write P.
-//     cos/sin(j th) come from the angle sum of the tile base row (shared memory)
-//     and the lane's own row (registers).  A warp rescales its accumulator row
-//     only when its running max grows by more than 2^8.
+//     online softmax per warp and write P = diag(p): accumulator row j collects
+//     p_j c_v,j over the unit's tiles and the rows are summed when the unit ends.
+//     cos/sin(j th) come from the angle sum of the tile base row (a per-warp
+//     shared-memory copy) and the lane's own row (registers).  A warp rescales its
+//     accumulator row only when its running max grows by more than 2^8.
 // Reconstructed keys and values never leave TMEM / registers.
 //
 #include "lla_kernels.h"
@@ -42,7 +45,8 @@ struct alignas(16) DecodeMisc {
   uint64_t kfull[kMaxStages], kempty[kMaxStages];
   uint64_t vfull[kMaxStages], vempty[kMaxStages];
   uint64_t ufull[2], pfull[2], vdone[2];   // index = tile & 1
-  uint64_t zfull, dfree, mma_done;
+  uint64_t zfull[2], zfree[2];             // index = unit % NZ
+  uint64_t mma_done[2];                    // score / value issuer drained
   uint32_t tmem_base;
   int abort;
   int start_b, start_h, start_t, count;
@@ -86,67 +90,93 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Z (the B operand of the score MMA) for unit (b, h), row e of 128 written by
-// thread e.  With q' = RoPE(q, q_pos) and frequency pair (i0, i1) of f = e mod 64:
-//   rows e < 64 :  Z_e = sc * (q'_i0 W_i0 + q'_i1 W_i1),  bias sc * (q'_i0 mu_i0 + q'_i1 mu_i1)
-//   rows e >= 64:  Z_e = sc * (q'_i1 W_i0 - q'_i0 W_i1),  bias sc * (q'_i1 mu_i0 - q'_i0 mu_i1)
+// Query operand of the score MMA for every (sequence, head) unit, written as the
+// exact shared-memory image the decode kernel copies in with one bulk transfer:
+// Z in the K-chunk layout (swizzled like a latent K tile), then the bias operand
+// (128 rows x 16 bf16, 32B swizzle).  With q' = RoPE(q, q_pos) and the frequency
+// pair (i0, i1) of f < 64:
+//   row f      :  Z_f    = sc * (q'_i0 W_i0 + q'_i1 W_i1),  bias sc * (q'_i0 mu_i0 + q'_i1 mu_i1)
+//   row 64 + f :  Z_64+f = sc * (q'_i1 W_i0 - q'_i0 W_i1),  bias sc * (q'_i1 mu_i0 - q'_i0 mu_i1)
 // so that s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f} with U = c_j Z^T + bias,
-// which equals log2(e) * RoPE(q,q_pos).RoPE(k_j, j) / sqrt(d) for k_j of Eq. (3).
-__device__ void compute_z(const DecodeArgs& a, uint8_t* sm, int b, int h, int e) {
+// which equals log2(e) * RoPE(q,q_pos).RoPE(k_j, j) / sqrt(d) for k_j of Eq. (3)
+// (sc = log2(e) / sqrt(d)).  The bias is split into bf16 hi (column 0) and lo
+// (column 1).  Block = unit, thread f builds rows f and 64 + f.
+__global__ void __launch_bounds__(64) decode_z_kernel(const __grid_constant__ DecodeArgs a) {
+  // the decode kernel may start its set-up now; it waits for this grid before
+  // it reads an image
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const DecodePlan& P = a.plan;
+  const int u = blockIdx.x, f = threadIdx.x;
+  const int b = u / a.H, h = u % a.H;
+  if (clamp_len(__ldg(a.seq_lens + b), a.L_max) == 0) return;
   int qp = __ldg(a.q_pos + b);
   if (qp < 0 || qp >= a.rope_len) {
-    record_status(a.status, LLA_ERR_DEVICE_ARG);
+    if (f == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
     qp = qp < 0 ? 0 : static_cast<int>(a.rope_len - 1);
   }
-  const int f = e & 63;
   const int i0 = a.rope_style == 0 ? f : 2 * f;
   const int i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
-  const float cq = __ldg(a.rope_cos + static_cast<int64_t>(qp) * 64 + f);
-  const float sq = __ldg(a.rope_sin + static_cast<int64_t>(qp) * 64 + f);
   const __nv_bfloat16* qv =
       static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(b) * a.H + h) * kHeadDim;
+  const float cq = __ldg(a.rope_cos + static_cast<int64_t>(qp) * 64 + f);
+  const float sq = __ldg(a.rope_sin + static_cast<int64_t>(qp) * 64 + f);
   const float x0 = __bfloat162float(qv[i0]), x1 = __bfloat162float(qv[i1]);
-  const float q0 = x0 * cq - x1 * sq;   // q'_i0
-  const float q1 = x0 * sq + x1 * cq;   // q'_i1
   const float scale = kLog2e * kInvSqrtD;
-  const float ca = (e < 64 ? q0 : q1) * scale;
-  const float cb = (e < 64 ? q1 : -q0) * scale;
+  const float q0 = (x0 * cq - x1 * sq) * scale;   // sc * q'_i0
+  const float q1 = (x0 * sq + x1 * cq) * scale;   // sc * q'_i1
+  uint8_t* img = a.zimg + static_cast<int64_t>(u) * a.zimg_stride;
+
+  const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
+  const float m0 = __ldg(mu + i0), m1 = __ldg(mu + i1);
+  const float bias[2] = {q0 * m0 + q1 * m1, q1 * m0 - q0 * m1};
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int e = f + 64 * half;
+    const __nv_bfloat16 zh = __float2bfloat16_rn(bias[half]);
+    const __nv_bfloat16 zl = __float2bfloat16_rn(bias[half] - __bfloat162float(zh));
+    const uint32_t pair = bf16x2_bits(__halves2bfloat162(zh, zl));
+    uint8_t* ab = img + P.kplan.bytes;
+    *reinterpret_cast<uint4*>(ab + swizzle_offset(e * 32, 32)) = make_uint4(pair, 0, 0, 0);
+    *reinterpret_cast<uint4*>(ab + swizzle_offset(e * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
+  }
 
   const __nv_bfloat16* W =
       static_cast<const __nv_bfloat16*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
   const uint4* w0 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i0) * a.r_k);
   const uint4* w1 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i1) * a.r_k);
-  for (int c = 0; c < P.kplan.n; ++c) {
-    const int width = P.kplan.width[c], rb = width * 2;
-    for (int g = 0; g < width / 8; ++g) {
-      const int k8 = (P.kplan.start[c] >> 3) + g;
-      float wa[8], wb[8];
-      unpack_bf16x8(__ldg(w0 + k8), wa);
-      unpack_bf16x8(__ldg(w1 + k8), wb);
-      uint32_t hi[4], lo[4];
+  for (int kb = 0; kb < a.r_k; kb += 64) {
+    uint4 ra[8], rb[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float z0 = ca * wa[2 * j] + cb * wb[2 * j];
-        const float z1 = ca * wa[2 * j + 1] + cb * wb[2 * j + 1];
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(z0, z1);
-        const float2 hf = __bfloat1622float2(h2);
-        hi[j] = bf16x2_bits(h2);
-        lo[j] = bf16x2_bits(__floats2bfloat162_rn(z0 - hf.x, z1 - hf.y));
+    for (int g = 0; g < 8; ++g) {
+      const bool in = kb + 8 * g < a.r_k;
+      ra[g] = in ? __ldg(w0 + kb / 8 + g) : make_uint4(0, 0, 0, 0);
+      rb[g] = in ? __ldg(w1 + kb / 8 + g) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int k = kb + 8 * g;
+      if (k >= a.r_k) break;
+      float wa[8], wb[8];
+      unpack_bf16x8(ra[g], wa);
+      unpack_bf16x8(rb[g], wb);
+      uint32_t z0[4], z1[4];   // rows f and 64 + f
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        z0[t] = bf16x2_bits(__floats2bfloat162_rn(q0 * wa[2 * t] + q1 * wb[2 * t],
+                                                  q0 * wa[2 * t + 1] + q1 * wb[2 * t + 1]));
+        z1[t] = bf16x2_bits(__floats2bfloat162_rn(q1 * wa[2 * t] - q0 * wb[2 * t],
+                                                  q1 * wa[2 * t + 1] - q0 * wb[2 * t + 1]));
       }
-      const uint32_t off = P.kplan.off[c] + swizzle_offset(e * rb + g * 16, rb);
-      *reinterpret_cast<uint4*>(sm + P.z_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      if (P.zpasses == 2)
-        *reinterpret_cast<uint4*>(sm + P.z_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      int c = 0;
+      while (c + 1 < P.kplan.n && k >= P.kplan.start[c + 1]) ++c;
+      const int rbytes = P.kplan.width[c] * 2;
+      const int col = (k - P.kplan.start[c]) * 2;
+      uint8_t* zc = img + P.kplan.off[c];
+      *reinterpret_cast<uint4*>(zc + swizzle_offset(f * rbytes + col, rbytes)) = make_uint4(z0[0], z0[1], z0[2], z0[3]);
+      *reinterpret_cast<uint4*>(zc + swizzle_offset((f + 64) * rbytes + col, rbytes)) =
+          make_uint4(z1[0], z1[1], z1[2], z1[3]);
     }
   }
-  const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
-  const float zb = ca * __ldg(mu + i0) + cb * __ldg(mu + i1);
-  const __nv_bfloat16 zh = __float2bfloat16_rn(zb);
-  const __nv_bfloat16 zl = __float2bfloat16_rn(zb - __bfloat162float(zh));
-  const uint32_t pair = bf16x2_bits(__halves2bfloat162(zh, zl));
-  *reinterpret_cast<uint4*>(sm + P.aug_b + swizzle_offset(e * 32, 32)) = make_uint4(pair, 0, 0, 0);
-  *reinterpret_cast<uint4*>(sm + P.aug_b + swizzle_offset(e * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
 }
 
 __global__ void __launch_bounds__(kDecodeThreads, 1)
@@ -229,21 +259,22 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       mbar_init(bar(misc->ufull[i]), 1);
       mbar_init(bar(misc->pfull[i]), 4);
       mbar_init(bar(misc->vdone[i]), 1);
+      mbar_init(bar(misc->zfull[i]), 1);
+      mbar_init(bar(misc->zfree[i]), 1);
     }
-    mbar_init(bar(misc->zfull), kTile);
-    mbar_init(bar(misc->dfree), 4);
-    mbar_init(bar(misc->mma_done), 1);
+    mbar_init(bar(misc->mma_done[0]), 1);
+    mbar_init(bar(misc->mma_done[1]), 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < 3; ++i) prefetch_tmap(&maps.k[i]);
-    prefetch_tmap(&maps.v[0]);
+    prefetch_tmap(&maps.v);
   }
   if (warp == 1) {
     __syncwarp();
     tmem_alloc(smem_u32(&misc->tmem_base), 512);
   }
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
     // constant bias operand: columns 0 and 1 of every row are 1 (they meet bias hi / lo)
     const int et = tid - 64;
     const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
@@ -259,125 +290,155 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
 
   if (warp == 0) {
     // ======================================================== TMA producer
+    // Per unit: its query-operand image (built by decode_z_kernel) into Z buffer
+    // unit % NZ once the score MMAs of the buffer's previous unit are done.  Per
+    // tile: K tile i, then V tile i - vlag (a V stage is held until the tile's
+    // softmax weights exist, so it is filled as late as still hides the load).
     if (lane == 0) {
-      Walker w = start;
-      int issued_k = 0, issued_v = 0;
-      for (int i = 0; i < count; ++i) {
-        const int sk = i % P.SK;
-        if (!mbar_wait(bar(misc->kempty[sk]), ((i / P.SK) & 1) ^ 1, abort, a.status)) break;
-        const uint32_t kb = bar(misc->kfull[sk]);
-        mbar_arrive_expect_tx(kb, P.kplan.bytes);
-        const int z = w.b * a.H + w.h, y = w.t * kTile;
-        for (int c = 0; c < P.kplan.n; ++c)
-          tma_load_3d(k_ring + sk * P.k_stage + P.kplan.off[c], &maps.k[chunk_map_index(P.kplan.width[c])],
-                      kb, P.kplan.start[c], y, z);
-        issued_k = i + 1;
-        const int sv = i % P.SV;
-        if (!mbar_wait(bar(misc->vempty[sv]), ((i / P.SV) & 1) ^ 1, abort, a.status)) break;
-        const uint32_t vb = bar(misc->vfull[sv]);
-        mbar_arrive_expect_tx(vb, P.vplan.bytes + 512);
-        const uint32_t vs = v_ring + sv * P.v_stage;
-        for (int c = 0; c < P.vplan.n; ++c) tma_load_3d(vs + P.vplan.off[c], &maps.v[0], vb, P.vplan.start[c], y, z);
-        bulk_load(vs + P.v_trig, a.rope_cos + static_cast<int64_t>(y) * 64, 256, vb);
-        bulk_load(vs + P.v_trig + 256, a.rope_sin + static_cast<int64_t>(y) * 64, 256, vb);
-        issued_v = i + 1;
-        walker_advance(w, a);
+      Walker wk = start, wv = start;
+      int issued_k = 0, issued_v = 0, issued_z = 0, unit = -1;
+      for (int i = 0; i < count + P.vlag; ++i) {
+        if (i < count) {
+          if (i == 0 || wk.t == 0) {
+            ++unit;
+            const int zb = unit % P.NZ;
+            if (unit >= P.NZ && !mbar_wait(bar(misc->zfree[zb]), ((unit / P.NZ) - 1) & 1, abort, a.status)) break;
+            if (unit == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // images written
+            const uint32_t zf = bar(misc->zfull[zb]);
+            mbar_arrive_expect_tx(zf, P.kplan.bytes + 4096);
+            const uint8_t* img = a.zimg + static_cast<int64_t>(wk.b * a.H + wk.h) * a.zimg_stride;
+            bulk_load(sbase + P.z + zb * P.z_stage, img, P.kplan.bytes, zf);
+            bulk_load(sbase + P.aug_b + zb * 4096, img + P.kplan.bytes, 4096, zf);
+            issued_z = unit + 1;
+          }
+          const int sk = i % P.SK;
+          if (!mbar_wait(bar(misc->kempty[sk]), ((i / P.SK) & 1) ^ 1, abort, a.status)) break;
+          const uint32_t kb = bar(misc->kfull[sk]);
+          mbar_arrive_expect_tx(kb, P.kplan.bytes);
+          const int z = wk.b * a.H + wk.h, y = wk.t * kTile;
+          for (int c = 0; c < P.kplan.n; ++c)
+            tma_load_3d(k_ring + sk * P.k_stage + P.kplan.off[c], &maps.k[chunk_map_index(P.kplan.width[c])],
+                        kb, P.kplan.start[c], y, z);
+          issued_k = i + 1;
+          walker_advance(wk, a);
+        }
+        const int j = i - P.vlag;
+        if (j >= 0) {
+          const int sv = j % P.SV;
+          if (!mbar_wait(bar(misc->vempty[sv]), ((j / P.SV) & 1) ^ 1, abort, a.status)) break;
+          const uint32_t vb = bar(misc->vfull[sv]);
+          mbar_arrive_expect_tx(vb, P.vplan.bytes);
+          const uint32_t vs = v_ring + sv * P.v_stage;
+          const int z = wv.b * a.H + wv.h, y = wv.t * kTile;
+          for (int c = 0; c < P.vplan.n; ++c) tma_load_3d(vs + P.vplan.off[c], &maps.v, vb, P.vplan.start[c], y, z);
+          issued_v = j + 1;
+          walker_advance(wv, a);
+        }
       }
       // Let every copy this CTA issued land before the CTA can exit.
-      for (int i = max(0, issued_k - P.SK); i < issued_k; ++i) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(bar(misc->kfull[i % P.SK]), (i / P.SK) & 1) &&
-               global_timer_ns() - t0 < kWaitLimitNs) {}
-      }
-      for (int i = max(0, issued_v - P.SV); i < issued_v; ++i) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(bar(misc->vfull[i % P.SV]), (i / P.SV) & 1) &&
-               global_timer_ns() - t0 < kWaitLimitNs) {}
-      }
+      auto drain = [&](uint64_t* full, int n, int issued) {
+        for (int i = max(0, issued - n); i < issued; ++i) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(bar(full[i % n]), (i / n) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+        }
+      };
+      drain(misc->kfull, P.SK, issued_k);
+      drain(misc->vfull, P.SV, issued_v);
+      drain(misc->zfull, P.NZ, issued_z);
     }
   } else if (warp == 1) {
-    // ======================================================== MMA issuer
-    // Order per tile: K(i) then V(i-1); at a unit boundary V(i-1) goes first, so
-    // the epilogue can read out the finished unit before it prepares Z for the
-    // next one.  MMAs run in issue order, so K(i) into U[i & 1] never overtakes
-    // V(i-2), which reads P(i-2) from the same columns.
+    // ======================================================== score-MMA issuer
+    // U[i & 1] = C_k(i) Z^T (+ bias).  The columns of U[i & 1] last held P(i-2),
+    // the A operand of value MMA i-2 (issued by warp 6), so K(i) waits for it.
     if (lane == 0) {
       const uint32_t idesc_k = umma_idesc_bf16(128, 128, false, false);
-      const uint32_t idesc_v = umma_idesc_bf16(128, a.r_v, false, true);
       const uint64_t daa = umma_desc(sbase + P.aug_a, 16, 256, kSw32);
-      const uint64_t dab = umma_desc(sbase + P.aug_b, 16, 256, kSw32);
-      // V tile as the MN-major B operand: 64-column chunks 16 KB apart (LBO), 8
-      // token rows 1 KB apart (SBO); a 16-token K step is +2 KB (+128 in the field)
-      const uint64_t dv0 = umma_desc(v_ring, kTile * 128, 1024, kSw128);
-      const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4, vst = static_cast<uint32_t>(P.v_stage) >> 4;
-      bool ok = true;
-      auto issue_v = [&](int j, bool first_of_unit, int unit) -> bool {
+      const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4;
+      Walker w = start;
+      int unit = -1;
+      for (int i = 0; i < count; ++i) {
+        if (i == 0 || w.t == 0) {
+          ++unit;
+          if (!mbar_wait(bar(misc->zfull[unit % P.NZ]), (unit / P.NZ) & 1, abort, a.status)) break;
+        }
+        const int sk = i % P.SK, ub = i & 1, zb = unit % P.NZ;
+        if (!mbar_wait(bar(misc->kfull[sk]), (i / P.SK) & 1, abort, a.status)) break;
+        if (i >= 2 && !mbar_wait(bar(misc->vdone[ub]), ((i - 2) >> 1) & 1, abort, a.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + ub * 128;
+        const uint32_t so = sk * kst;
+        const uint32_t zreg = sbase + P.z + zb * P.z_stage;
+        uint32_t acc = 0;
+        for (int c = 0; c < P.kplan.n; ++c) {
+          const int rb = P.kplan.width[c] * 2;
+          const uint32_t lay = sw_mode_for_row_bytes(rb);
+          const uint64_t a0 = umma_desc(k_ring + P.kplan.off[c], 16, 8 * rb, lay) + so;
+          const uint64_t b0 = umma_desc(zreg + P.kplan.off[c], 16, 8 * rb, lay);
+          for (int k = 0; k < P.kplan.width[c] / 16; ++k) {
+            umma_bf16(d, a0 + 2 * k, b0 + 2 * k, idesc_k, acc);
+            acc = 1;
+          }
+        }
+        umma_bf16(d, daa, umma_desc(sbase + P.aug_b + zb * 4096, 16, 256, kSw32), idesc_k, 1);
+        umma_commit(bar(misc->kempty[sk]));
+        umma_commit(bar(misc->ufull[ub]));
+        if (w.t == w.nb - 1) umma_commit(bar(misc->zfree[zb]));   // unit's Z no longer read
+        walker_advance(w, a);
+      }
+      // this thread's MMAs complete before TMEM is released
+      umma_commit(bar(misc->mma_done[0]));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(bar(misc->mma_done[0]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else if (warp == kWarpVMma) {
+    // ======================================================== value-MMA issuer
+    // D += P(j) C_v(j): P(j) from TMEM (written by the epilogue over U[j & 1]), the
+    // V tile as the MN-major B operand.  The accumulator is never cleared by an
+    // MMA: the epilogue zeroes it when a unit starts.
+    if (lane == 0) {
+      const uint32_t idesc_v = umma_idesc_bf16(128, a.r_v, false, true);
+      // 32-column chunks 8 KB apart (LBO), 8 token rows 512 B apart (SBO); a
+      // 16-token K step is +1 KB (+64 in the address field)
+      const uint64_t dv0 = umma_desc(v_ring, kTile * 64, 512, kSw64);
+      const uint32_t vst = static_cast<uint32_t>(P.v_stage) >> 4;
+      Walker wv = start;
+      for (int j = 0; j < count; ++j) {
         const int sv = j % P.SV, jb = j & 1;
-        if (!mbar_wait(bar(misc->vfull[sv]), (j / P.SV) & 1, abort, a.status)) return false;
-        if (!mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status)) return false;
-        if (first_of_unit && unit > 0 && !mbar_wait(bar(misc->dfree), (unit - 1) & 1, abort, a.status))
-          return false;
+        if (!mbar_wait(bar(misc->vfull[sv]), (j / P.SV) & 1, abort, a.status)) break;
+        if (!mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status)) break;
+        // rows past the sequence end: skip whole 16-token steps, zero the rest of a
+        // partial step (they may hold anything; their weights are 0 and 0 * x stays 0)
+        const int valid = wv.L - wv.t * kTile;
+        const int steps = valid >= kTile ? kTile / 16 : (valid + 15) / 16;
+        if (valid < steps * 16) {
+          uint8_t* vs = sm + P.v_ring + sv * P.v_stage;
+          for (int c = 0; c < P.vplan.n; ++c)
+            for (int r = valid; r < steps * 16; ++r)
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<uint4*>(vs + P.vplan.off[c] + swizzle_offset(r * 64 + g * 16, 64)) =
+                    make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+        }
         tc_fence_after();
         const uint64_t b0 = dv0 + sv * vst;
         const uint32_t pa = tmem + jb * 128;
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          umma_bf16_ts(tmem + kDCol, pa + 8 * k, b0 + 128 * k, idesc_v, (first_of_unit && k == 0) ? 0u : 1u);
+        for (int k = 0; k < steps; ++k) umma_bf16_ts(tmem + kDCol, pa + 8 * k, b0 + 64 * k, idesc_v, 1u);
         umma_commit(bar(misc->vempty[sv]));
         umma_commit(bar(misc->vdone[jb]));
-        return true;
-      };
-      Walker w = start;
-      int zph = 0, unit = -1, prev_unit = -1;
-      bool prev_first = false;
-      for (int i = 0; i <= count && ok; ++i) {
-        const bool first = i < count && (i == 0 || w.t == 0);
-        if (first) ++unit;
-        if (i > 0 && first && !(ok = issue_v(i - 1, prev_first, prev_unit))) break;
-        if (i < count) {
-          if (first) {
-            if (!(ok = mbar_wait(bar(misc->zfull), zph, abort, a.status))) break;
-            zph ^= 1;
-          }
-          const int sk = i % P.SK, ub = i & 1;
-          if (!(ok = mbar_wait(bar(misc->kfull[sk]), (i / P.SK) & 1, abort, a.status))) break;
-          tc_fence_after();
-          const uint32_t d = tmem + ub * 128;
-          const uint32_t so = sk * kst;
-          uint32_t acc = 0;
-          for (int pass = 0; pass < P.zpasses; ++pass) {
-            const uint32_t zreg = sbase + (pass == 0 ? P.z_hi : P.z_lo);
-            for (int c = 0; c < P.kplan.n; ++c) {
-              const int rb = P.kplan.width[c] * 2;
-              const uint32_t lay = sw_mode_for_row_bytes(rb);
-              const uint64_t a0 = umma_desc(k_ring + P.kplan.off[c], 16, 8 * rb, lay) + so;
-              const uint64_t b0 = umma_desc(zreg + P.kplan.off[c], 16, 8 * rb, lay);
-              for (int k = 0; k < P.kplan.width[c] / 16; ++k) {
-                umma_bf16(d, a0 + 2 * k, b0 + 2 * k, idesc_k, acc);
-                acc = 1;
-              }
-            }
-          }
-          umma_bf16(d, daa, dab, idesc_k, 1);
-          umma_commit(bar(misc->kempty[sk]));
-          umma_commit(bar(misc->ufull[ub]));
-          walker_advance(w, a);
-        }
-        if (i > 0 && !first && !(ok = issue_v(i - 1, prev_first, prev_unit))) break;
-        prev_first = first;
-        prev_unit = unit;
+        walker_advance(wv, a);
       }
-      // all issued MMAs complete before TMEM is released
-      umma_commit(bar(misc->mma_done));
+      umma_commit(bar(misc->mma_done[1]));
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      while (!mbar_try_wait(bar(misc->mma_done[1]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
   } else {
-    // ======================================================== epilogue (4 warps)
-    const int et = tid - 64;
+    // ======================================================== epilogue (warps 2-5)
     const int q = warp & 3;             // TMEM lane quadrant of this warp
     const int row = 32 * q + lane;      // token row within a tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // this warp's copy of the tile's RoPE base row: cos[64] then sin[64]
+    float* trig = reinterpret_cast<float*>(sm + P.trig + q * 512);
 
     // cos/sin(row * th_f): the tile-local half of the angle-sum rotation
     float cl[64], sl[64];
@@ -389,54 +450,70 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       sl[f] = s4.x; sl[f + 1] = s4.y; sl[f + 2] = s4.z; sl[f + 3] = s4.w;
     }
 
+    auto zero_acc = [&]() {
+      float zf[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) zf[k] = 0.f;
+      for (int c = 0; c < a.r_v; c += 32) tmem_st_x32(tmem + lane_base + kDCol + c, zf);
+      tmem_wait_st();
+    };
+    auto load_trig = [&](int t, float (&v)[4]) {
+      const int64_t o = static_cast<int64_t>(t) * kTile * 64;
+      v[0] = __ldg(a.rope_cos + o + lane);
+      v[1] = __ldg(a.rope_cos + o + 32 + lane);
+      v[2] = __ldg(a.rope_sin + o + lane);
+      v[3] = __ldg(a.rope_sin + o + 32 + lane);
+    };
+    auto store_trig = [&](const float (&v)[4]) {
+      __syncwarp();
+      trig[lane] = v[0]; trig[32 + lane] = v[1]; trig[64 + lane] = v[2]; trig[96 + lane] = v[3];
+      __syncwarp();
+    };
+
     Walker w = start;
-    int cur_b = -1, cur_h = 0;
+    zero_acc();
+    {
+      float tv[4];
+      load_trig(w.t, tv);
+      store_trig(tv);
+    }
+
+    int cur_b = w.b, cur_h = w.h;
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = true;
 
-    // Read out this warp's accumulator row of the finished unit (its last value MMA
-    // was tile `last`) and write the warp's record (m, l, acc_v).
-    auto finalize = [&](int last) -> bool {
+    // Read out this warp's accumulator rows of a finished unit (its last value MMA
+    // was tile `last`), sum them over the warp's 32 token rows and write the
+    // warp's record (m, l, acc_v).
+    auto finalize = [&](int last, int b, int h, float m, float l) -> bool {
       if (!warp_wait(bar(misc->vdone[last & 1]), (last >> 1) & 1, abort, a.status)) return false;
       tc_fence_after();
-      const float lw = warp_sum(l_run);
-      const long long u = static_cast<long long>(cur_b) * a.H + cur_h;
+      const float lw = warp_sum(l);
+      const long long u = static_cast<long long>(b) * a.H + h;
       float* rec = a.partials + ((u + blockIdx.x) * kRecordsPerCta + q) * (a.r_v + kRecordHead);
-      if (lane == 0) { rec[0] = m_ref; rec[1] = lw; }
+      if (lane == 0) { rec[0] = m; rec[1] = lw; }
       for (int c = 0; c < a.r_v; c += 32) {
         float v[32];
         tmem_ld_x32(tmem + lane_base + kDCol + c, v);
         tmem_wait_ld();
-        if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            if (c + k < a.r_v)
-              *reinterpret_cast<float4*>(rec + kRecordHead + c + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-        }
+        const float col = warp_column_sum32(v);
+        if (c + lane < a.r_v) rec[kRecordHead + c + lane] = col;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(misc->dfree));
       return true;
     };
 
+    Walker wn = w;
+    walker_advance(wn, a);
     for (int i = 0; i < count && ok; ++i) {
-      if (i == 0 || w.t == 0) {
-        if (i > 0 && !(ok = finalize(i - 1))) break;
-        compute_z(a, sm, w.b, w.h, et);
-        fence_proxy_async_smem();
-        mbar_arrive(bar(misc->zfull));
-        cur_b = w.b; cur_h = w.h;
-        m_ref = -INFINITY; l_run = 0.f;
-      }
-      const int sv = i % P.SV, ub = i & 1;
-      if (!(ok = warp_wait(bar(misc->vfull[sv]), (i / P.SV) & 1, abort, a.status))) break;
+      const bool first = i > 0 && w.t == 0;   // a unit starts at tile i (not the CTA's first)
+      float tn[4];
+      if (i + 1 < count) load_trig(wn.t, tn);   // next tile's base row, used after this score
+      const int ub = i & 1;
       if (!(ok = warp_wait(bar(misc->ufull[ub]), (i >> 1) & 1, abort, a.status))) break;
       tc_fence_after();
 
       // ---- rotary score from U, 32 frequencies at a time
-      uint8_t* vstage = sm + P.v_ring + sv * P.v_stage;
-      const float4* tcos = reinterpret_cast<const float4*>(vstage + P.v_trig);
+      const float4* tcos = reinterpret_cast<const float4*>(trig);
       const float4* tsin = tcos + 16;
       const uint32_t tU = tmem + lane_base + ub * 128;
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -461,11 +538,22 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           }
         }
       }
+      if (i + 1 < count) store_trig(tn);
+
+      // ---- a new unit: read out the finished one once its last value MMA is done
+      // (no value MMA of the new unit can start before this warp's P arrives), then
+      // clear the accumulator row for the new unit
+      if (first) {
+        if (!(ok = finalize(i - 1, cur_b, cur_h, m_ref, l_run))) break;
+        zero_acc();
+        cur_b = w.b; cur_h = w.h;
+        m_ref = -INFINITY; l_run = 0.f;
+      }
 
       // ---- online softmax (log2 domain, lazy per-warp reference)
       const bool valid = w.t * kTile + row < w.L;
       const float s = valid ? (s4[0] + s4[1]) + (s4[2] + s4[3]) : -INFINITY;
-      const float m_tile = warp_max(s);
+      const float m_tile = warp_max_redux(s);
       if (m_tile > m_ref + kRescaleLog2) {
         if (m_ref != -INFINITY) {
           // the accumulator row must be at rest: V(i-1) complete (V(i-2) already is,
@@ -490,39 +578,31 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       const __nv_bfloat16 pb = __float2bfloat16_rn(p);
       l_run += __bfloat162float(pb);
 
-      // ---- P row 32q of this tile into TMEM (over the consumed scores): lane 0 of
-      // the warp holds p of the warp's 32 tokens packed in columns 16q..16q+15,
-      // every other entry of this warp's lanes is zero
+      // ---- P = diag(p) over this warp's rows, into TMEM over the consumed scores:
+      // row 32q + lane holds its own weight at token column 32q + lane (bf16 pairs:
+      // column 16q + lane/2, low half for even lanes), every other entry is zero.
+      // The value MMA then adds p_j c_v,j to accumulator row j; rows are summed
+      // once per unit.
       {
-        const uint32_t pbits = static_cast<uint32_t>(__bfloat16_as_ushort(pb));
-        const uint32_t pair = pbits | (__shfl_down_sync(0xffffffffu, pbits, 1) << 16);
+        const uint32_t pbits = static_cast<uint32_t>(__bfloat16_as_ushort(pb)) << ((lane & 1) * 16);
         uint32_t mine[16], zero[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const uint32_t v = __shfl_sync(0xffffffffu, pair, 2 * c);
-          mine[c] = lane == 0 ? v : 0u;
+          mine[c] = c == (lane >> 1) ? pbits : 0u;
           zero[c] = 0u;
         }
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) tmem_st_x16(tU + 16 * blk, blk == q ? mine : zero);
       }
-      if (__any_sync(0xffffffffu, !valid)) {
-        if (!valid) {
-          // rows past the sequence end may hold anything: zero them so 0 * x stays 0
-          for (int c = 0; c < P.vplan.n; ++c)
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4*>(vstage + P.vplan.off[c] + swizzle_offset(row * 128 + k * 16, 128)) =
-                  make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(misc->pfull[ub]));
+
       walker_advance(w, a);
+      walker_advance(wn, a);
     }
-    if (ok) finalize(count - 1);
+    if (ok) finalize(count - 1, cur_b, cur_h, m_ref, l_run);
   }
 
   tc_fence_before();
@@ -710,20 +790,19 @@ decode_f32_values_kernel(const __grid_constant__ DecodeArgs a) {
 bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
   *p = DecodePlan{};
   p->kplan = make_chunk_plan(r_k, kTile);
-  p->vplan = make_chunk_plan_64(r_v, kTile);
+  p->vplan = make_chunk_plan_32(r_v, kTile);
   auto al = [](int x, int a) { return (x + a - 1) / a * a; };
-  p->v_trig = al(p->vplan.bytes, 16);
-  p->v_stage = al(p->v_trig + 512, 1024);
   p->k_stage = al(p->kplan.bytes, 1024);
-  const int zbytes = al(p->kplan.bytes, 1024);
-  // One score pass with the query operand in bf16 (score error ~1e-3 relative);
-  // a second (lo) pass doubles the operand reads of the score MMAs.  Prefer
-  // double-buffered rings; single-stage rings only for the largest ranks.
-  const int tries[2][3] = {{1, 2, 2}, {1, 1, 1}};
+  p->v_stage = al(p->vplan.bytes, 1024);
+  p->z_stage = al(p->kplan.bytes, 1024);
+  p->vlag = 1;
+  // (Z buffers, K stages, V stages) in order of preference: Z built one unit
+  // ahead and double-buffered rings first; single buffers only for the largest ranks.
+  const int tries[5][3] = {{2, 2, 2}, {1, 2, 2}, {1, 1, 2}, {1, 2, 1}, {1, 1, 1}};
   int SK = 0, SV = 0, fixed = 0;
   for (const auto& t : tries) {
-    p->zpasses = t[0];
-    fixed = p->zpasses * zbytes + 4096 + 4096 + 2048 + 1024;
+    p->NZ = t[0];
+    fixed = p->NZ * p->z_stage + 4096 + 8192 + 2048 + 2048 + 1024;
     SK = t[1];
     SV = t[2];
     if (fixed + SK * p->k_stage + SV * p->v_stage <= kSmemLimit) break;
@@ -745,11 +824,11 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
   int off = 0;
   p->v_ring = off; off += SV * p->v_stage;
   p->k_ring = off; off += SK * p->k_stage;
-  p->z_hi = off; off += zbytes;
-  p->z_lo = off; off += (p->zpasses == 2 ? zbytes : 0);
-  p->aug_a = off; off += 4096;
-  p->aug_b = off; off += 4096;
-  p->misc = off; off += 2048;
+  p->z = off;      off += p->NZ * p->z_stage;
+  p->aug_a = off;  off += 4096;
+  p->aug_b = off;  off += 8192;
+  p->trig = off;   off += 2048;
+  p->misc = off;   off += 2048;
   p->bytes = off + 1024;
   return true;
 }
@@ -762,8 +841,22 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cuda
     if (e != cudaSuccess) return e;
     configured = a.plan.bytes;
   }
-  decode_bf16_kernel<<<a.grid, kDecodeThreads, a.plan.bytes, s>>>(a, maps);
+  decode_z_kernel<<<a.B * a.H, 64, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // programmatic dependent launch: the decode grid's set-up overlaps the image
+  // kernel; its producer waits for that grid before the first image copy
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = a.plan.bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a, maps);
   if (e != cudaSuccess) return e;
   decode_combine_kernel<<<a.B * a.H, 128, 0, s>>>(a);
   return cudaGetLastError();

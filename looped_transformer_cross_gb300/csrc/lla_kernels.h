@@ -13,7 +13,8 @@ namespace lla {
 
 constexpr int kMaxStages = 8;
 constexpr int kMaxGrid = 1024;          // upper bound on decode CTAs (workspace sizing)
-constexpr int kDecodeThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
+constexpr int kDecodeThreads = 224;     // producer, score-MMA, 4 epilogue, value-MMA warps
+constexpr int kWarpVMma = 6;            // decode warp issuing the value MMAs
 constexpr int kRecordsPerCta = 4;       // split records per (unit, CTA): one per epilogue warp
 constexpr int kRecordHead = 4;          // record = {m, l, -, -, acc[r_v]}: acc 16-byte aligned
 constexpr int kEncodeThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
@@ -23,12 +24,12 @@ constexpr int kSmemLimit = 232448;      // dynamic shared memory per block on sm
 // 1024-aligned base).
 struct DecodePlan {
   ChunkPlan kplan;                   // K latent chunks (64/32/16 wide, 128 rows)
-  ChunkPlan vplan;                   // V latent chunks, padded to 64 wide
+  ChunkPlan vplan;                   // V latent chunks, 32 wide (64B swizzle)
   int SK, SV;                        // ring depths
-  int zpasses;                       // 2: query operand as bf16 hi + lo, 1: hi only
-  int k_stage, v_stage;              // stage strides
-  int v_trig;                        // offset of the RoPE base rows inside a V stage
-  int v_ring, k_ring, z_hi, z_lo, aug_a, aug_b, misc;
+  int NZ;                            // query-operand (Z) buffers: 2 = built one unit ahead
+  int vlag;                          // V tile i is requested after K tile i + vlag
+  int k_stage, v_stage, z_stage;     // stage strides
+  int v_ring, k_ring, z, aug_a, aug_b, trig, misc;
   int bytes;                         // total dynamic smem incl. alignment slack
 };
 
@@ -52,12 +53,14 @@ struct DecodeArgs {
   int32_t* prefix;                   // [B+1] tile prefix over sequences
   float* partials;                   // [(B*H + kMaxGrid) * 4][r_v + 4] records per (unit, CTA, warp)
   float* scores;                     // fp32 path: [B][H][L_max]
+  uint8_t* zimg;                     // bf16 path: per-unit query-operand images
+  int64_t zimg_stride;               // bytes per unit image (Z chunks, then 4 KB bias operand)
   DecodePlan plan;
 };
 
 struct DecodeMaps {
   CUtensorMap k[3];                  // latent K boxes of width 64 / 32 / 16
-  CUtensorMap v[3];
+  CUtensorMap v;                     // latent V boxes of width 32
 };
 
 bool make_decode_plan(int r_k, int r_v, DecodePlan* p);

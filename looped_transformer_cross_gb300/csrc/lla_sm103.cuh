@@ -322,6 +322,30 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Warp maximum in one instruction (sm_100+); NaN inputs are ignored like fmaxf.
+__device__ __forceinline__ float warp_max_redux(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Column sums of a warp's 32 x 32 block (lane = row, v[] = its 32 columns): after
+// five exchange-and-add rounds lane l holds the sum over all lanes of column l.
+__device__ __forceinline__ float warp_column_sum32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const float send = upper ? v[k] : v[k + w];
+      const float keep = upper ? v[k + w] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -331,25 +355,25 @@ __device__ __forceinline__ float warp_sum(float v) {
 // ----------------------------------------------------------------- latent chunks
 
 // A latent row of rank r (multiple of 16, <= 256) is split into chunks of 64,
-// 32 and 16 elements (largest first).  Each chunk is one TMA box and one
-// shared-memory region whose rows are 128 / 64 / 32 bytes wide, matching the
-// 128B / 64B / 32B swizzle atoms that TMA writes and UMMA reads.
+// 32 and 16 elements (largest first), or into equal chunks of 32.  Each chunk is
+// one TMA box and one shared-memory region whose rows are 128 / 64 / 32 bytes
+// wide, matching the 128B / 64B / 32B swizzle atoms that TMA writes and UMMA reads.
 struct ChunkPlan {
-  int n;            // number of chunks (<= 6)
-  int start[6];     // first element of chunk c
-  int width[6];     // elements in chunk c (64, 32 or 16)
-  int off[6];       // byte offset of chunk c in a 128-row tile
+  int n;            // number of chunks (<= 8)
+  int start[8];     // first element of chunk c
+  int width[8];     // elements in chunk c (64, 32 or 16)
+  int off[8];       // byte offset of chunk c in a 128-row tile
   int bytes;        // bytes of a 128-row tile (all chunks)
 };
 
-// Rank r padded to 64-element chunks (the tail chunk's missing columns are
-// zero-filled by TMA): uniform 128-byte rows, so one MN-major operand spans them.
-__host__ __device__ inline ChunkPlan make_chunk_plan_64(int r, int rows) {
+// Rank r in 32-element chunks (a tail chunk's missing columns are zero-filled by
+// TMA): uniform 64-byte rows, so one MN-major operand with 64B swizzle spans them.
+__host__ __device__ inline ChunkPlan make_chunk_plan_32(int r, int rows) {
   ChunkPlan p{};
-  for (int e = 0; e < r; e += 64) {
-    p.start[p.n] = e; p.width[p.n] = 64; p.off[p.n] = p.n * rows * 128; ++p.n;
+  for (int e = 0; e < r; e += 32) {
+    p.start[p.n] = e; p.width[p.n] = 32; p.off[p.n] = p.n * rows * 64; ++p.n;
   }
-  p.bytes = p.n * rows * 128;
+  p.bytes = p.n * rows * 64;
   return p;
 }
 

@@ -48,9 +48,13 @@ def test_workspace_size_rules(L):
     d = lla.dims(4, 16, 96, 160)
     n = lla.workspace_size(d, 32, 4096)
     assert n > 256
-    # grows with batch; fp32 mode adds the score buffer
+    # grows with batch; bf16 mode holds one query-operand image per (sequence, head)
+    # (128 x r_k bf16 plus the 4 KB bias operand), fp32 mode the score buffer
     assert lla.workspace_size(d, 64, 4096) > n
-    assert lla.workspace_size(lla.dims(4, 16, 96, 160, dtype=lla.LLA_F32), 32, 4096) > n + 32 * 16 * 4096 * 4 - 1
+    assert n >= 32 * 16 * (128 * 96 * 2 + 4096)
+    n32 = lla.workspace_size(lla.dims(4, 16, 96, 160, dtype=lla.LLA_F32), 32, 4096)
+    assert n32 >= 32 * 16 * 4096 * 4
+    assert n32 - 32 * 16 * 4096 * 4 < n - 32 * 16 * (128 * 96 * 2 + 4096) + 256
     bad = lla.dims(4, 16, 96, 160, d_head=64)
     assert L.lla_workspace_size(ctypes.byref(bad), 1, 16, 0) == 0
     bad = lla.dims(4, 16, 90, 160)
