@@ -142,8 +142,8 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
                            float* out, float* lse,
                            void* workspace, size_t ws_bytes, void* stream);
 
-/* Size of the fixed scratch array behind lla_decode_attn_noalloc (8 MiB). */
-#define LLA_NOALLOC_SCRATCH_BYTES (8u << 20)
+/* Size of the fixed scratch array behind lla_decode_attn_noalloc (64 MiB). */
+#define LLA_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /*
  * lla_decode_attn_noalloc — lla_decode_attn without a caller workspace, for
@@ -156,8 +156,8 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
  *     inside this library; every GPU that loads the library keeps it until
  *     the process exits.  The call allocates nothing.
  *   - Shapes whose workspace (lla_workspace_size) exceeds that size return
- *     LLA_ERR_UNSUPPORTED before any launch (e.g. beyond about 2,100 sequence-heads
- *     at r_v = 160).
+ *     LLA_ERR_UNSUPPORTED before any launch (e.g. beyond about 2,000 sequence-heads
+ *     at r_k = 96, r_v = 160).
  *   - The first call on each device looks up the array's device address with
  *     the device current; make that first call before any stream capture.
  *   - The array is shared by every call and keeps the last call's contents;

@@ -48,7 +48,7 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t prefix, partials, bias, scores, zimg, zimg_stride, total;
+  size_t partials, bias, scores, zimg, zimg_stride, total;
 };
 
 // Bytes of one unit's query-operand image: Z (128 rows x r_k bf16, K-chunk
@@ -60,7 +60,6 @@ size_t zimg_stride(int r_k) {
 WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   WsLayout w{};
   size_t off = 256;  // status word
-  w.prefix = off; off += al256(static_cast<size_t>(B + 1) * 4);
   w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * kRecordsPerCta * (d->r_v + kRecordHead) * 4);
   w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
   w.scores = off;
@@ -187,7 +186,6 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   a.lse = lse;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
-  a.prefix = reinterpret_cast<int32_t*>(ws + wl.prefix);
   a.partials = reinterpret_cast<float*>(ws + wl.partials);
   a.scores = reinterpret_cast<float*>(ws + wl.scores);
   a.zimg = ws + wl.zimg;

@@ -77,15 +77,6 @@ __device__ __forceinline__ void walker_advance(Walker& w, const DecodeArgs& a) {
   }
 }
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
@@ -100,82 +91,95 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
 // so that s_j = sum_f cos(j th_f) U_f + sin(j th_f) U_{64+f} with U = c_j Z^T + bias,
 // which equals log2(e) * RoPE(q,q_pos).RoPE(k_j, j) / sqrt(d) for k_j of Eq. (3)
 // (sc = log2(e) / sqrt(d)).  The bias is split into bf16 hi (column 0) and lo
-// (column 1).  Block = unit, thread f builds rows f and 64 + f.
-__global__ void __launch_bounds__(64) decode_z_kernel(const __grid_constant__ DecodeArgs a) {
+// (column 1).  Block = unit: threads 0..63 form sc * q' of each frequency pair and
+// write the bias rows; then items (row pair f, 8-column group g), consecutive in g,
+// so a warp loads contiguous W row segments and writes whole swizzled rows.
+constexpr int kZThreads = 256;
+__global__ void __launch_bounds__(kZThreads) decode_z_kernel(const __grid_constant__ DecodeArgs a) {
   // the decode kernel may start its set-up now; it waits for this grid before
   // it reads an image
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float qs[2][64];   // sc * q'_i0, sc * q'_i1 per frequency
   const DecodePlan& P = a.plan;
-  const int u = blockIdx.x, f = threadIdx.x;
+  const int u = blockIdx.x, tid = threadIdx.x;
   const int b = u / a.H, h = u % a.H;
   if (clamp_len(__ldg(a.seq_lens + b), a.L_max) == 0) return;
-  int qp = __ldg(a.q_pos + b);
-  if (qp < 0 || qp >= a.rope_len) {
-    if (f == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
-    qp = qp < 0 ? 0 : static_cast<int>(a.rope_len - 1);
-  }
-  const int i0 = a.rope_style == 0 ? f : 2 * f;
-  const int i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
-  const __nv_bfloat16* qv =
-      static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(b) * a.H + h) * kHeadDim;
-  const float cq = __ldg(a.rope_cos + static_cast<int64_t>(qp) * 64 + f);
-  const float sq = __ldg(a.rope_sin + static_cast<int64_t>(qp) * 64 + f);
-  const float x0 = __bfloat162float(qv[i0]), x1 = __bfloat162float(qv[i1]);
-  const float scale = kLog2e * kInvSqrtD;
-  const float q0 = (x0 * cq - x1 * sq) * scale;   // sc * q'_i0
-  const float q1 = (x0 * sq + x1 * cq) * scale;   // sc * q'_i1
   uint8_t* img = a.zimg + static_cast<int64_t>(u) * a.zimg_stride;
-
-  const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
-  const float m0 = __ldg(mu + i0), m1 = __ldg(mu + i1);
-  const float bias[2] = {q0 * m0 + q1 * m1, q1 * m0 - q0 * m1};
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int e = f + 64 * half;
-    const __nv_bfloat16 zh = __float2bfloat16_rn(bias[half]);
-    const __nv_bfloat16 zl = __float2bfloat16_rn(bias[half] - __bfloat162float(zh));
-    const uint32_t pair = bf16x2_bits(__halves2bfloat162(zh, zl));
-    uint8_t* ab = img + P.kplan.bytes;
-    *reinterpret_cast<uint4*>(ab + swizzle_offset(e * 32, 32)) = make_uint4(pair, 0, 0, 0);
-    *reinterpret_cast<uint4*>(ab + swizzle_offset(e * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
-  }
-
   const __nv_bfloat16* W =
       static_cast<const __nv_bfloat16*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
-  const uint4* w0 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i0) * a.r_k);
-  const uint4* w1 = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i1) * a.r_k);
-  for (int kb = 0; kb < a.r_k; kb += 64) {
-    uint4 ra[8], rb[8];
+  const int ng = a.r_k / 8;
+  constexpr int kItems = 64 * 32 / kZThreads;   // items per thread at r_k = 256
+  uint4 ra[kItems], rb[kItems];
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const bool in = kb + 8 * g < a.r_k;
-      ra[g] = in ? __ldg(w0 + kb / 8 + g) : make_uint4(0, 0, 0, 0);
-      rb[g] = in ? __ldg(w1 + kb / 8 + g) : make_uint4(0, 0, 0, 0);
+  for (int j = 0; j < kItems; ++j) {   // every load in flight before any use
+    const int it = tid + j * kZThreads;
+    if (it < 64 * ng) {
+      const int f = it / ng, k = 8 * (it - (it / ng) * ng);
+      const int i0 = a.rope_style == 0 ? f : 2 * f;
+      const int i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
+      ra[j] = __ldg(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i0) * a.r_k + k));
+      rb[j] = __ldg(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(i1) * a.r_k + k));
     }
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int k = kb + 8 * g;
-      if (k >= a.r_k) break;
-      float wa[8], wb[8];
-      unpack_bf16x8(ra[g], wa);
-      unpack_bf16x8(rb[g], wb);
-      uint32_t z0[4], z1[4];   // rows f and 64 + f
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        z0[t] = bf16x2_bits(__floats2bfloat162_rn(q0 * wa[2 * t] + q1 * wb[2 * t],
-                                                  q0 * wa[2 * t + 1] + q1 * wb[2 * t + 1]));
-        z1[t] = bf16x2_bits(__floats2bfloat162_rn(q1 * wa[2 * t] - q0 * wb[2 * t],
-                                                  q1 * wa[2 * t + 1] - q0 * wb[2 * t + 1]));
-      }
-      int c = 0;
-      while (c + 1 < P.kplan.n && k >= P.kplan.start[c + 1]) ++c;
-      const int rbytes = P.kplan.width[c] * 2;
-      const int col = (k - P.kplan.start[c]) * 2;
-      uint8_t* zc = img + P.kplan.off[c];
-      *reinterpret_cast<uint4*>(zc + swizzle_offset(f * rbytes + col, rbytes)) = make_uint4(z0[0], z0[1], z0[2], z0[3]);
-      *reinterpret_cast<uint4*>(zc + swizzle_offset((f + 64) * rbytes + col, rbytes)) =
-          make_uint4(z1[0], z1[1], z1[2], z1[3]);
+  }
+  if (tid < 64) {
+    const int f = tid;
+    int qp = __ldg(a.q_pos + b);
+    if (qp < 0 || qp >= a.rope_len) {
+      if (f == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
+      qp = qp < 0 ? 0 : static_cast<int>(a.rope_len - 1);
     }
+    const int i0 = a.rope_style == 0 ? f : 2 * f;
+    const int i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
+    const __nv_bfloat16* qv =
+        static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(b) * a.H + h) * kHeadDim;
+    const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
+    const float cq = __ldg(a.rope_cos + static_cast<int64_t>(qp) * 64 + f);
+    const float sq = __ldg(a.rope_sin + static_cast<int64_t>(qp) * 64 + f);
+    const float x0 = __bfloat162float(qv[i0]), x1 = __bfloat162float(qv[i1]);
+    const float m0 = __ldg(mu + i0), m1 = __ldg(mu + i1);
+    const float scale = kLog2e * kInvSqrtD;
+    const float q0 = (x0 * cq - x1 * sq) * scale;   // sc * q'_i0
+    const float q1 = (x0 * sq + x1 * cq) * scale;   // sc * q'_i1
+    qs[0][f] = q0;
+    qs[1][f] = q1;
+    const float bias[2] = {q0 * m0 + q1 * m1, q1 * m0 - q0 * m1};
+    uint8_t* ab = img + P.kplan.bytes;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int e = f + 64 * half;
+      const __nv_bfloat16 zh = __float2bfloat16_rn(bias[half]);
+      const __nv_bfloat16 zl = __float2bfloat16_rn(bias[half] - __bfloat162float(zh));
+      const uint32_t pair = bf16x2_bits(__halves2bfloat162(zh, zl));
+      *reinterpret_cast<uint4*>(ab + swizzle_offset(e * 32, 32)) = make_uint4(pair, 0, 0, 0);
+      *reinterpret_cast<uint4*>(ab + swizzle_offset(e * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) {
+    const int it = tid + j * kZThreads;
+    if (it >= 64 * ng) break;
+    const int f = it / ng, k = 8 * (it - f * ng);
+    float wa[8], wb[8];
+    unpack_bf16x8(ra[j], wa);
+    unpack_bf16x8(rb[j], wb);
+    const float q0 = qs[0][f], q1 = qs[1][f];
+    uint32_t z0[4], z1[4];   // rows f and 64 + f
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      z0[t] = bf16x2_bits(__floats2bfloat162_rn(q0 * wa[2 * t] + q1 * wb[2 * t],
+                                                q0 * wa[2 * t + 1] + q1 * wb[2 * t + 1]));
+      z1[t] = bf16x2_bits(__floats2bfloat162_rn(q1 * wa[2 * t] - q0 * wb[2 * t],
+                                                q1 * wa[2 * t + 1] - q0 * wb[2 * t + 1]));
+    }
+    int c = 0;
+    while (c + 1 < P.kplan.n && k >= P.kplan.start[c + 1]) ++c;
+    const int rbytes = P.kplan.width[c] * 2;
+    const int col = (k - P.kplan.start[c]) * 2;
+    uint8_t* zc = img + P.kplan.off[c];
+    *reinterpret_cast<uint4*>(zc + swizzle_offset(f * rbytes + col, rbytes)) = make_uint4(z0[0], z0[1], z0[2], z0[3]);
+    *reinterpret_cast<uint4*>(zc + swizzle_offset((f + 64) * rbytes + col, rbytes)) =
+        make_uint4(z1[0], z1[1], z1[2], z1[3]);
   }
 }
 
@@ -227,7 +231,6 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     long long P0 = misc->scan[tid];
     for (int b = b0; b < b1; ++b) {
       const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
-      if (blockIdx.x == 0) a.prefix[b] = static_cast<int32_t>(P0);
       if (nb > 0 && f0 < f1 && a.H * P0 <= f0 && f0 < a.H * (P0 + nb)) {
         const long long rem = f0 - a.H * P0;
         misc->start_b = b;
@@ -236,7 +239,6 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       }
       P0 += nb;
     }
-    if (blockIdx.x == 0 && tid == 0) a.prefix[a.B] = misc->total_seq_tiles;
     if (tid == 0) misc->count = static_cast<int>(f1 > f0 ? f1 - f0 : 0);
     __syncthreads();
   }
@@ -285,6 +287,9 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the combine grid may be scheduled now; it waits for this grid to complete
+  // before it reads a record
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tmem = misc->tmem_base;
   const uint32_t v_ring = sbase + P.v_ring, k_ring = sbase + P.k_ring;
 
@@ -614,59 +619,166 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
   }
 }
 
-// One block per (sequence, head): merge the per-CTA records of that unit,
-// apply the V up-projection once (Appendix J identity) and normalise.
-__global__ void __launch_bounds__(128)
-decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
-  __shared__ float accs[256];
-  const int u = blockIdx.x, tid = threadIdx.x;
-  const int b = u / a.H, h = u % a.H;
-  const int L = clamp_len(__ldg(a.seq_lens + b), a.L_max);
-  const int nb = (L + kTile - 1) / kTile;
-  float* out = a.out + static_cast<int64_t>(u) * kHeadDim;
-  if (nb == 0) {
-    out[tid] = 0.f;
-    if (tid == 0) a.lse[u] = -INFINITY;
-    return;
-  }
-  const long long total = static_cast<long long>(a.H) * a.prefix[a.B];
-  const long long per = max(1LL, (total + a.grid - 1) / a.grid);
-  const long long F0 = static_cast<long long>(a.H) * a.prefix[b] + static_cast<long long>(h) * nb;
-  const long long F1 = F0 + nb - 1;
-  const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
-  const int rs = a.r_v + kRecordHead;
-  // records of this unit: one per (CTA c in [c0, c1], epilogue warp); a warp that
-  // saw no token of the unit in that CTA wrote m = -inf, l = 0, acc = 0
-  const float* rec0 = a.partials + (static_cast<long long>(u) + c0) * kRecordsPerCta * rs;
-  const int nrec = kRecordsPerCta * (c1 - c0 + 1);
-  float M = -INFINITY;
-  for (int c = 0; c < nrec; ++c) M = fmaxf(M, rec0[static_cast<long long>(c) * rs]);
-  float Lt = 0.f;
-  for (int c = 0; c < nrec; ++c) {
-    const float* r = rec0 + static_cast<long long>(c) * rs;
-    if (r[0] != -INFINITY) Lt += r[1] * exp2f(r[0] - M);
-  }
-  for (int i = tid; i < a.r_v; i += 128) {
-    float v = 0.f;
-    for (int c = 0; c < nrec; ++c) {
-      const float* r = rec0 + static_cast<long long>(c) * rs;
-      if (r[0] != -INFINITY) v = fmaf(r[kRecordHead + i], exp2f(r[0] - M), v);
+// Merge each (sequence, head) unit's split records (log-sum-exp merge of the
+// per-CTA, per-warp (m, l, acc_v) triples), apply the V up-projection once
+// (Appendix J identity) and normalise:
+//   out = (sum_c 2^(m_c - M) acc_c) W_up,v,t^T / (sum_c 2^(m_c - M) l_c) + mu_v,t.
+// Block = (head h, kCombineUnits consecutive sequences).  Before the wait for the
+// decode grid it copies W_up,v,t[h] to shared memory (coalesced, rows padded by
+// one word so that thread e reading row e is conflict-free) and derives the tile
+// prefix of its sequences from seq_lens; after it, warp w loads unit w's records
+// in one batch and merges them, and thread e forms output e of every unit.
+constexpr int kCombineUnits = 2;
+constexpr int kCombineThreads = 128;
+
+size_t combine_smem_bytes(int r_v) {
+  return (static_cast<size_t>(128) * (r_v / 2 + 1) + kCombineUnits * 256 + 2 * kCombineUnits) * 4;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ float csm[];
+  __shared__ int red[kCombineThreads / 32];
+  const int h = blockIdx.x, b0 = blockIdx.y * kCombineUnits;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rw = a.r_v / 2, wpr = rw + 1;   // words per W row, per padded row
+  uint32_t* Ws = reinterpret_cast<uint32_t*>(csm);
+  float* accs = csm + 128 * wpr;                   // [kCombineUnits][256]
+  float* Ms = accs + kCombineUnits * 256;
+  float* Ls = Ms + kCombineUnits;
+
+  // ---- inputs only: W_up,v,t[h] -> shared memory; tiles of sequences < b0 and in total
+  {
+    const uint4* Wg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w_up_v) +
+                                                     static_cast<int64_t>(h) * kHeadDim * a.r_v);
+    const int n16 = 128 * rw / 4;             // 16-byte pieces; a row holds rw / 4 of them
+    constexpr int kMax = 128 * 128 / 4 / kCombineThreads;   // at r_v = 256
+    uint4 v[kMax];
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int i = tid + j * kCombineThreads;
+      v[j] = i < n16 ? __ldg(Wg + i) : make_uint4(0, 0, 0, 0);
     }
-    accs[i] = v;
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      const int i = tid + j * kCombineThreads;
+      if (i < n16) {
+        const int e = i / (rw / 4), k = 4 * (i - e * (rw / 4));
+        uint32_t* d = Ws + e * wpr + k;
+        d[0] = v[j].x; d[1] = v[j].y; d[2] = v[j].z; d[3] = v[j].w;
+      }
+    }
+  }
+  int before = 0, all = 0;   // tiles of sequences [0, b0) and [0, B)
+  for (int bb = tid; bb < a.B; bb += kCombineThreads) {
+    const int n = (clamp_len(__ldg(a.seq_lens + bb), a.L_max) + kTile - 1) / kTile;
+    all += n;
+    if (bb < b0) before += n;
+  }
+  before = __reduce_add_sync(0xffffffffu, before);
+  all = __reduce_add_sync(0xffffffffu, all);
+  if (lane == 0) red[warp] = before;
+  __syncthreads();
+  int pre = 0;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) pre += red[w];
+  __syncthreads();
+  if (lane == 0) red[warp] = all;
+  __syncthreads();
+  int tot = 0;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) tot += red[w];
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // records written
+
+  // ---- warp w < kCombineUnits merges the records of unit (b0 + w, h)
+  float M = -INFINITY, Lt = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  const int b = b0 + warp;
+  if (warp < kCombineUnits && b < a.B) {
+    int pb = pre;   // tiles of sequences before b
+    for (int bb = b0; bb < b; ++bb) pb += (clamp_len(__ldg(a.seq_lens + bb), a.L_max) + kTile - 1) / kTile;
+    const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
+    if (nb > 0) {
+      const long long total = static_cast<long long>(a.H) * tot;
+      const long long per = max(1LL, (total + a.grid - 1) / a.grid);
+      const long long F0 = static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
+      const long long F1 = F0 + nb - 1;
+      const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
+      const int rs = a.r_v + kRecordHead;
+      const long long u = static_cast<long long>(b) * a.H + h;
+      // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
+      // the unit in that CTA wrote m = -inf, l = 0, acc = 0
+      const float* rec0 = a.partials + (u + c0) * kRecordsPerCta * rs;
+      const int nrec = kRecordsPerCta * (c1 - c0 + 1);
+      for (int cb = 0; cb < nrec; cb += 8) {
+        // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
+        // lane + 32 j of each, all in one round of loads
+        const int cl = cb + (lane & 7);
+        const float mh = cl < nrec ? rec0[static_cast<long long>(cl) * rs] : -INFINITY;
+        const float lh = cl < nrec ? rec0[static_cast<long long>(cl) * rs + 1] : 0.f;
+        float x[8][8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int col = lane + 32 * j;
+            x[r][j] = cb + r < nrec && col < a.r_v ? rec0[static_cast<long long>(cb + r) * rs + kRecordHead + col] : 0.f;
+          }
+        const float Mn = fmaxf(M, warp_max(mh));
+        if (Mn != -INFINITY) {
+          const float alpha = M == -INFINITY ? 0.f : exp2f(M - Mn);
+          Lt *= alpha;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] *= alpha;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float mr = __shfl_sync(0xffffffffu, mh, r), lr = __shfl_sync(0xffffffffu, lh, r);
+            const float w = mr == -INFINITY ? 0.f : exp2f(mr - Mn);
+            Lt = fmaf(lr, w, Lt);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[r][j], w, acc[j]);
+          }
+          M = Mn;
+        }
+      }
+    }
+  }
+  if (warp < kCombineUnits) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (lane + 32 * j < a.r_v) accs[warp * 256 + lane + 32 * j] = acc[j];
+    if (lane == 0) { Ms[warp] = M; Ls[warp] = Lt; }
   }
   __syncthreads();
-  const __nv_bfloat16* Wv = static_cast<const __nv_bfloat16*>(a.w_up_v) +
-                            (static_cast<int64_t>(h) * kHeadDim + tid) * a.r_v;
-  float o = 0.f;
-  for (int i = 0; i < a.r_v; i += 8) {
-    float wv[8];
-    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(Wv + i)), wv);
+
+  // ---- out[b][h][e] = acc_b . W_e / Lt_b + mu_e, thread e reading row e of W once
+  const int e = tid;
+  float o[kCombineUnits];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) o = fmaf(accs[i + k], wv[k], o);
+  for (int j = 0; j < kCombineUnits; ++j) o[j] = 0.f;
+  const uint32_t* wr = Ws + e * wpr;
+#pragma unroll 4
+  for (int k = 0; k < rw; ++k) {
+    const uint32_t w2 = wr[k];
+    const float wlo = __uint_as_float(w2 << 16), whi = __uint_as_float(w2 & 0xFFFF0000u);
+#pragma unroll
+    for (int j = 0; j < kCombineUnits; ++j) {
+      const float2 av = *reinterpret_cast<const float2*>(accs + j * 256 + 2 * k);
+      o[j] = fmaf(av.x, wlo, fmaf(av.y, whi, o[j]));
+    }
   }
-  const float mu = __ldg(a.mu_v + static_cast<int64_t>(h) * a.mu_hstride + tid);
-  out[tid] = o / Lt + mu;
-  if (tid == 0) a.lse[u] = (M + log2f(Lt)) * kLn2;
+  const float mu = __ldg(a.mu_v + static_cast<int64_t>(h) * a.mu_hstride + e);
+#pragma unroll
+  for (int j = 0; j < kCombineUnits; ++j) {
+    const int bb = b0 + j;
+    if (bb >= a.B) continue;
+    const int64_t uu = static_cast<int64_t>(bb) * a.H + h;
+    const bool empty = Ms[j] == -INFINITY;
+    a.out[uu * kHeadDim + e] = empty ? 0.f : o[j] / Ls[j] + mu;
+    if (e == 0) a.lse[uu] = empty ? -INFINITY : (Ms[j] + log2f(Ls[j])) * kLn2;
+  }
 }
 
 // ------------------------------------------------------------------ fp32 path
@@ -841,7 +953,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cuda
     if (e != cudaSuccess) return e;
     configured = a.plan.bytes;
   }
-  decode_z_kernel<<<a.B * a.H, 64, 0, s>>>(a);
+  decode_z_kernel<<<a.B * a.H, kZThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the decode grid's set-up overlaps the image
@@ -858,8 +970,20 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cuda
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a, maps);
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<a.B * a.H, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  // the combine grid, a programmatic dependent of the decode grid, copies W_up,v
+  // while the decode grid drains
+  const size_t csmem = combine_smem_bytes(a.r_v);
+  static size_t cconfigured = 0;
+  if (cconfigured < csmem) {
+    e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(csmem));
+    if (e != cudaSuccess) return e;
+    cconfigured = csmem;
+  }
+  cfg.gridDim = dim3(a.H, (a.B + kCombineUnits - 1) / kCombineUnits);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = csmem;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, a);
 }
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s) {

@@ -25,18 +25,50 @@ struct alignas(16) EncodeMisc {
   int abort;
 };
 
-// bias[axis][h][k] = sum_u mu[h][u] * W_down[h][u][k]  (fp32)
-template <typename T>
+// bias[axis][h][k] = sum_u mu[h][u] * W_down[h][u][k]  (fp32).  Block = (head,
+// axis): warp w sums rows u = w, w + 8, ...; lane l covers columns 8l..8l+7 with
+// 16-byte loads, sixteen rows in flight; the eight warps' partial sums are added
+// in shared memory.
 __global__ void __launch_bounds__(256) encode_bias_kernel(const __grid_constant__ EncodeArgs a) {
-  const int h = blockIdx.x, axis = blockIdx.y, k = threadIdx.x;
+  __shared__ float part[8][256];
+  const int h = blockIdx.x, axis = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = axis == 0 ? a.r_k : a.r_v;
-  if (k >= r) return;
-  const T* W = static_cast<const T*>(axis == 0 ? a.w_down_k : a.w_down_v) +
-               static_cast<int64_t>(h) * a.Td * r;
+  const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(axis == 0 ? a.w_down_k : a.w_down_v) +
+                           static_cast<int64_t>(h) * a.Td * r;
   const float* mu = (axis == 0 ? a.mu_k : a.mu_v) + static_cast<int64_t>(h) * a.Td;
-  float s = 0.f;
-  for (int u = 0; u < a.Td; ++u) s = fmaf(mu[u], static_cast<float>(W[static_cast<int64_t>(u) * r + k]), s);
-  a.bias[(static_cast<int64_t>(axis) * a.H + h) * 256 + k] = s;
+  const int k = 8 * lane;
+  constexpr int kRows = 16;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (k < r) {
+    for (int u0 = warp; u0 < a.Td; u0 += 8 * kRows) {
+      uint4 wv[kRows];
+      float m[kRows];
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        const int u = u0 + 8 * j;
+        const bool in = u < a.Td;
+        wv[j] = in ? __ldg(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(u) * r + k)) : make_uint4(0, 0, 0, 0);
+        m[j] = in ? __ldg(mu + u) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        float w8[8];
+        unpack_bf16x8(wv[j], w8);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] = fmaf(m[j], w8[t], acc[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) part[warp][k + t] = acc[t];
+  }
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t < r) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += part[w][t];
+    a.bias[(static_cast<int64_t>(axis) * a.H + h) * 256 + t] = s;
+  }
 }
 
 __device__ __forceinline__ bool slot_ok(const EncodeArgs& a, int sid, int p) {
@@ -219,7 +251,7 @@ bool make_encode_plan(int r_k, int r_v, int Td, EncodePlan* p) {
 cudaError_t launch_encode_bf16(const EncodeArgs& a, const EncodePlan& plan, const EncodeMaps& m,
                                cudaStream_t s) {
   if (a.N == 0) return cudaSuccess;
-  encode_bias_kernel<__nv_bfloat16><<<dim3(a.H, 2), 256, 0, s>>>(a);
+  encode_bias_kernel<<<dim3(a.H, 2), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   static int configured = 0;

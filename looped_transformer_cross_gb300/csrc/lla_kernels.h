@@ -50,7 +50,6 @@ struct DecodeArgs {
   float* out;                        // [B][H][128]
   float* lse;                        // [B][H]
   uint32_t* status;                  // workspace status word
-  int32_t* prefix;                   // [B+1] tile prefix over sequences
   float* partials;                   // [(B*H + kMaxGrid) * 4][r_v + 4] records per (unit, CTA, warp)
   float* scores;                     // fp32 path: [B][H][L_max]
   uint8_t* zimg;                     // bf16 path: per-unit query-operand images

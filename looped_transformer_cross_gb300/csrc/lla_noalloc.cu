@@ -6,7 +6,7 @@
 // GPU, or a latency-critical serving path that must never call cudaMalloc
 // (which can synchronise the device and can fail at run time).  Such callers
 // still own their inputs and outputs; only the decode scratch (split-KV
-// records, the tile prefix and the status word) moves into a fixed array that
+// records, the query-operand images and the status word) moves into a fixed array that
 // this library defines.
 //
 // The array is a file-scope __device__ variable of LLA_NOALLOC_SCRATCH_BYTES:

@@ -322,6 +322,16 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Eight packed bf16 values (16 bytes, lower index in the low half) widened to fp32.
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
 // Warp maximum in one instruction (sm_100+); NaN inputs are ignored like fmaxf.
 __device__ __forceinline__ float warp_max_redux(float v) {
   float r;
