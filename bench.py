@@ -35,6 +35,14 @@ from looped_transformer_cross_gb300 import lla  # noqa: E402
 from looped_transformer_cross_gb300.synth import WORKLOADS, make_decode_inputs, widen  # noqa: E402
 
 METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe roofline"
+
+# DRAM bytes (read + write) of decode_bf16_kernel per latent token-head, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 8-sequence variant
+# of the bench layer.  Valid only for the decode source whose sha256 starts with
+# TRAFFIC_SRC_SHA; any other source reports traffic as unknown (null).
+TRAFFIC_PER_TOKEN_HEAD = (263.985408e6 + 4.192768e6) / (31042 * 16)
+TRAFFIC_SRC_SHA = "9abbc21afa8206ef"
+DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 UNIT = "latent tokens/s per layer-loop"
 
 
@@ -134,9 +142,10 @@ class DecodeStep:
             if ev is not None:
                 ev[1][t].record()
 
-    # launches of this library's kernels per step: encode (bias + GEMM) + T x (decode + combine)
+    # launches of this library's kernels per step: encode (bias + GEMM) + T x (query
+    # images + decode + combine)
     def launches(self):
-        return 2 + 2 * self.w.T
+        return 2 + 3 * self.w.T
 
 
 def barrier(dist_on):
@@ -249,6 +258,10 @@ def run_ours(args, dist_on, rank, world, device):
     lat_bytes = step.tokens * w.H * (w.r_k + w.r_v) * 2
     hbm, _, src = peaks()
     achieved = lat_bytes / t_call / 1e9
+    import hashlib
+    with open(DECODE_SRC, "rb") as f:
+        same_src = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC_SRC_SHA)
+    traffic = TRAFFIC_PER_TOKEN_HEAD * step.tokens * w.H if same_src else None
 
     e2e_steps = max(3, min(args.steps, 200))
     e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
@@ -266,8 +279,10 @@ def run_ours(args, dist_on, rank, world, device):
                    "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
                        step.inp["cache_k"].numel() * 2 * (1 + w.r_v / w.r_k) / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
-                     "kernel": "lla_decode_attn (decode_bf16_kernel + decode_combine_kernel)",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "traffic_kernel": "decode_bf16_kernel",
+                     "kernel": "lla_decode_attn (decode_z_kernel + decode_bf16_kernel + "
+                               "decode_combine_kernel)",
                      "algorithmic_bytes_per_launch": lat_bytes, "launch_ms": t_call * 1e3,
                      "peak_source": src},
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -61,6 +61,10 @@ WORKLOADS = {
     # Ouro-1.4B-shaped single layer, rho = 4, 32 ragged sequences of 3584..4096 tokens
     "ouro1.4b_rho4_b32_4k": Workload("ouro1.4b_rho4_b32_4k", T=4, H=16, d=128, r_k=96,
                                      r_v=160, B=32, L_max=4096, len_lo=3584, len_hi=4096),
+    # the same layer with 8 sequences (about 250 MB of latents, still above L2): the
+    # small case for kernel profiles
+    "ouro1.4b_rho4_b8_4k": Workload("ouro1.4b_rho4_b8_4k", T=4, H=16, d=128, r_k=96,
+                                    r_v=160, B=8, L_max=4096, len_lo=3584, len_hi=4096),
     # rho = 21.3 at serving batch: 768 sequences x 4096, 24-layer stack + new-token encode
     "ouro1.4b_rho21_b768_4k": Workload("ouro1.4b_rho21_b768_4k", T=4, H=16, d=128, r_k=16,
                                        r_v=32, B=768, L_max=4096, len_lo=4096, len_hi=4096,
