@@ -59,6 +59,18 @@ struct Walker {
   int b, h, t, nb, L;
 };
 
+// Position in a ring of n mbarrier-guarded slots: the slot index and the parity
+// of the slot's current use, advanced without division (the role warps share
+// their sub-partitions with the epilogue warps, so their per-tile scalar work
+// is kept small).
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) { slot = 0; phase ^= 1u; }
+  }
+};
+
 __device__ __forceinline__ int clamp_len(int L, int64_t L_max) {
   return L < 0 ? 0 : (L > L_max ? static_cast<int>(L_max) : L);
 }
@@ -302,12 +314,13 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     if (lane == 0) {
       Walker wk = start, wv = start;
       int issued_k = 0, issued_v = 0, issued_z = 0, unit = -1;
+      RingPos kr, vr, zr;
       for (int i = 0; i < count + P.vlag; ++i) {
         if (i < count) {
           if (i == 0 || wk.t == 0) {
-            ++unit;
-            const int zb = unit % P.NZ;
-            if (unit >= P.NZ && !mbar_wait(bar(misc->zfree[zb]), ((unit / P.NZ) - 1) & 1, abort, a.status)) break;
+            if (++unit > 0) zr.next(P.NZ);
+            const int zb = zr.slot;
+            if (unit >= P.NZ && !mbar_wait(bar(misc->zfree[zb]), zr.phase ^ 1u, abort, a.status)) break;
             if (unit == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // images written
             const uint32_t zf = bar(misc->zfull[zb]);
             mbar_arrive_expect_tx(zf, P.kplan.bytes + 4096);
@@ -316,8 +329,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
             bulk_load(sbase + P.aug_b + zb * 4096, img + P.kplan.bytes, 4096, zf);
             issued_z = unit + 1;
           }
-          const int sk = i % P.SK;
-          if (!mbar_wait(bar(misc->kempty[sk]), ((i / P.SK) & 1) ^ 1, abort, a.status)) break;
+          const int sk = kr.slot;
+          if (!mbar_wait(bar(misc->kempty[sk]), kr.phase ^ 1u, abort, a.status)) break;
           const uint32_t kb = bar(misc->kfull[sk]);
           mbar_arrive_expect_tx(kb, P.kplan.bytes);
           const int z = wk.b * a.H + wk.h, y = wk.t * kTile;
@@ -325,18 +338,20 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
             tma_load_3d(k_ring + sk * P.k_stage + P.kplan.off[c], &maps.k[chunk_map_index(P.kplan.width[c])],
                         kb, P.kplan.start[c], y, z);
           issued_k = i + 1;
+          kr.next(P.SK);
           walker_advance(wk, a);
         }
         const int j = i - P.vlag;
         if (j >= 0) {
-          const int sv = j % P.SV;
-          if (!mbar_wait(bar(misc->vempty[sv]), ((j / P.SV) & 1) ^ 1, abort, a.status)) break;
+          const int sv = vr.slot;
+          if (!mbar_wait(bar(misc->vempty[sv]), vr.phase ^ 1u, abort, a.status)) break;
           const uint32_t vb = bar(misc->vfull[sv]);
           mbar_arrive_expect_tx(vb, P.vplan.bytes);
           const uint32_t vs = v_ring + sv * P.v_stage;
           const int z = wv.b * a.H + wv.h, y = wv.t * kTile;
           for (int c = 0; c < P.vplan.n; ++c) tma_load_3d(vs + P.vplan.off[c], &maps.v, vb, P.vplan.start[c], y, z);
           issued_v = j + 1;
+          vr.next(P.SV);
           walker_advance(wv, a);
         }
       }
@@ -361,13 +376,14 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4;
       Walker w = start;
       int unit = -1;
-      for (int i = 0; i < count; ++i) {
+      RingPos kr, zr;
+      for (int i = 0; i < count; ++i, kr.next(P.SK)) {
         if (i == 0 || w.t == 0) {
-          ++unit;
-          if (!mbar_wait(bar(misc->zfull[unit % P.NZ]), (unit / P.NZ) & 1, abort, a.status)) break;
+          if (++unit > 0) zr.next(P.NZ);
+          if (!mbar_wait(bar(misc->zfull[zr.slot]), zr.phase, abort, a.status)) break;
         }
-        const int sk = i % P.SK, ub = i & 1, zb = unit % P.NZ;
-        if (!mbar_wait(bar(misc->kfull[sk]), (i / P.SK) & 1, abort, a.status)) break;
+        const int sk = kr.slot, ub = i & 1, zb = zr.slot;
+        if (!mbar_wait(bar(misc->kfull[sk]), kr.phase, abort, a.status)) break;
         if (i >= 2 && !mbar_wait(bar(misc->vdone[ub]), ((i - 2) >> 1) & 1, abort, a.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + ub * 128;
@@ -407,9 +423,10 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       const uint64_t dv0 = umma_desc(v_ring, kTile * 64, 512, kSw64);
       const uint32_t vst = static_cast<uint32_t>(P.v_stage) >> 4;
       Walker wv = start;
-      for (int j = 0; j < count; ++j) {
-        const int sv = j % P.SV, jb = j & 1;
-        if (!mbar_wait(bar(misc->vfull[sv]), (j / P.SV) & 1, abort, a.status)) break;
+      RingPos vr;
+      for (int j = 0; j < count; ++j, vr.next(P.SV)) {
+        const int sv = vr.slot, jb = j & 1;
+        if (!mbar_wait(bar(misc->vfull[sv]), vr.phase, abort, a.status)) break;
         if (!mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status)) break;
         // rows past the sequence end: skip whole 16-token steps, zero the rest of a
         // partial step (they may hold anything; their weights are 0 and 0 * x stays 0)
