@@ -583,13 +583,15 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           if (!(ok = warp_wait(bar(misc->vdone[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort, a.status))) break;
           tc_fence_after();
           const float alpha = exp2f(m_ref - m_tile);
-          for (int c = 0; c < a.r_v; c += 32) {
-            float v[32];
-            tmem_ld_x32(tmem + lane_base + kDCol + c, v);
+          // (16 columns at a time: a small body keeps the per-tile loop compact)
+          for (int c = 0; c < a.r_v; c += 16) {
+            float v[16];
+            tmem_ld_x16(tmem + lane_base + kDCol + c, v);
             tmem_wait_ld();
+            uint32_t w16[16];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] *= alpha;
-            tmem_st_x32(tmem + lane_base + kDCol + c, v);
+            for (int k = 0; k < 16; ++k) w16[k] = __float_as_uint(v[k] * alpha);
+            tmem_st_x16(tmem + lane_base + kDCol + c, w16);
           }
           tmem_wait_st();
           l_run *= alpha;

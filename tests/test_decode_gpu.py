@@ -109,6 +109,24 @@ def test_softmax_weights_normalised():
     np.testing.assert_allclose(out.cpu().numpy(), 1.0, rtol=0, atol=2e-6)
 
 
+def test_growing_scores_rescale_accumulators():
+    """K latents scaled up along each sequence (x1 .. x4): later tiles' score maxima
+    exceed the running reference by more than the lazy-rescale threshold (2^8), so
+    accumulators are rescaled (16 times over these 12 units, at warp level, by the
+    oracle's scores) and once more across CTA splits.  The ramp stays moderate:
+    the bf16 query operand carries a ~2^-9 relative error per score term, so the
+    lse error grows with the score magnitude (|lse| <= 12 here)."""
+    w = workload(T=2, H=4, r_k=96, r_v=160, B=3, L_max=1500)
+    inp = _inputs(w, 15, lens=[1500, 1200, 700])
+    ramp = torch.linspace(1.0, 4.0, w.L_max, device="cuda").view(1, 1, w.L_max, 1)
+    inp["cache_k"] = (inp["cache_k"].float() * ramp).to(inp["cache_k"].dtype).contiguous()
+    for t in range(w.T):
+        compare(w, inp, t)
+    # and the mirror image: the largest scores first, no rescale after the first tile
+    inp["cache_k"] = inp["cache_k"].flip(2).contiguous()
+    compare(w, inp, 0)
+
+
 def test_out_of_range_lengths_flagged():
     w = workload(B=2, L_max=128)
     inp = _inputs(w, 13, lens=[128, 5])
