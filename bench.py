@@ -40,8 +40,8 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 8-sequence variant
 # of the bench layer.  Valid only for the decode source whose sha256 starts with
 # TRAFFIC_SRC_SHA; any other source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = (263.985408e6 + 4.192768e6) / (31042 * 16)
-TRAFFIC_SRC_SHA = "9abbc21afa8206ef"
+TRAFFIC_PER_TOKEN_HEAD = (263.994368e6 + 4.025344e6) / (31042 * 16)
+TRAFFIC_SRC_SHA = "51f1eadfe3c1e845"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 UNIT = "latent tokens/s per layer-loop"
 
