@@ -2,6 +2,7 @@
 // argument checks, workspace layout, TMA descriptors and kernel launches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -48,7 +49,7 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t partials, bias, scores, zimg, zimg_stride, total;
+  size_t partials, rec_ml, bias, scores, zimg, zimg_stride, total;
 };
 
 // Bytes of one unit's query-operand image: Z (128 rows x r_k bf16, K-chunk
@@ -60,6 +61,23 @@ size_t zimg_stride(int r_k) {
 WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   WsLayout w{};
   size_t off = 256;  // status word
+  if (d->variant == LLA_2D) {
+    // run records of the pair kernel, encode bias (one "head" of width T*H*d),
+    // fp32 scores, per-sequence query-operand images
+    const size_t nrec = static_cast<size_t>(2) * (static_cast<size_t>(B) + kMaxPairs);
+    w.partials = off; off += al256(nrec * d->H * d->r_v * 4);
+    w.rec_ml = off;   off += al256(nrec * d->H * 2 * 4);
+    w.bias = off;     off += al256(static_cast<size_t>(2) * 256 * 4);
+    w.scores = off;
+    if (d->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * d->H * L_max * 4);
+    w.zimg = off;
+    if (d->dtype == LLA_BF16 && d->r_k <= 128) {
+      w.zimg_stride = decode2d_zimg_stride(d->H, d->r_k);
+      off += al256(static_cast<size_t>(B) * w.zimg_stride);
+    }
+    w.total = off;
+    return w;
+  }
   w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * kRecordsPerCta * (d->r_v + kRecordHead) * 4);
   w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
   w.scores = off;
@@ -80,7 +98,6 @@ lla_status check_dims(const lla_dims* d) {
   if (!(d->rope_base > 0.f) || !std::isfinite(d->rope_base)) return LLA_ERR_INVALID_ARG;
   if (d->d_head != kHeadDim) return LLA_ERR_UNSUPPORTED;
   if (d->r_k % 16 || d->r_v % 16 || d->r_k > 256 || d->r_v > 256) return LLA_ERR_UNSUPPORTED;
-  if (d->variant == LLA_2D) return LLA_ERR_UNSUPPORTED;
   return LLA_OK;
 }
 
@@ -162,6 +179,49 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
 
   const int H = dims->H, d = dims->d_head;
   const int esize = dims->dtype == LLA_BF16 ? 2 : 4;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dims->variant == LLA_2D && dims->dtype == LLA_BF16) {
+    // LLA-2D: one latent per token shared by the H heads (CTA-pair kernel)
+    Decode2dArgs a{};
+    if (!make_decode2d_plan(H, dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
+    a.B = cache.B;
+    a.H = H;
+    a.r_k = dims->r_k;
+    a.r_v = dims->r_v;
+    a.rope_style = dims->rope_style;
+    a.L_max = cache.L_max;
+    a.rope_len = rope_len;
+    a.q = q;
+    a.seq_lens = seq_lens;
+    a.q_pos = q_pos;
+    a.w_up_k = static_cast<const uint8_t*>(w_up_k) + static_cast<size_t>(loop_t) * H * d * dims->r_k * esize;
+    a.w_up_v = static_cast<const uint8_t*>(w_up_v) + static_cast<size_t>(loop_t) * H * d * dims->r_v * esize;
+    a.mu_k = mu_k + static_cast<size_t>(loop_t) * H * d;
+    a.mu_v = mu_v + static_cast<size_t>(loop_t) * H * d;
+    a.rope_cos = rope_cos;
+    a.rope_sin = rope_sin;
+    a.out = out;
+    a.lse = lse;
+    a.status = reinterpret_cast<uint32_t*>(ws);
+    a.rec_acc = reinterpret_cast<float*>(ws + wl.partials);
+    a.rec_ml = reinterpret_cast<float*>(ws + wl.rec_ml);
+    a.zimg = ws + wl.zimg;
+    a.zimg_stride = static_cast<int64_t>(wl.zimg_stride);
+    a.zchunk_bytes = static_cast<int64_t>(H) * d * 128;
+    const int sms = sm_count();
+    if (sms <= 1) return LLA_ERR_CUDA;
+    const int64_t max_blocks = static_cast<int64_t>(cache.B) * ((cache.L_max + kBlock2dTokens - 1) / kBlock2dTokens);
+    a.pairs = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms / 2, kMaxPairs), std::max<int64_t>(1, max_blocks)));
+    Decode2dMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const uint64_t rows = static_cast<uint64_t>(cache.L_max), seqs = static_cast<uint64_t>(cache.B);
+    if (!make_map_3d(&maps.k, cache.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_k, rows, seqs, 64, kTile, 1))
+      return LLA_ERR_CUDA;
+    if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, seqs, 64, 16, 1))
+      return LLA_ERR_CUDA;
+    return launch_decode2d_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  }
   DecodeArgs a{};
   a.B = cache.B;
   a.H = H;
@@ -170,7 +230,9 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   a.rope_style = dims->rope_style;
   a.L_max = cache.L_max;
   a.rope_len = rope_len;
-  a.mu_hstride = static_cast<int64_t>(dims->T) * d;
+  // per-head mu [H][T*d]; LLA-2D mu [T*H*d] with the loop-t slice [H][d]
+  a.mu_hstride = dims->variant == LLA_2D ? d : static_cast<int64_t>(dims->T) * d;
+  a.shared_latent = dims->variant == LLA_2D ? 1 : 0;
   a.q = q;
   a.seq_lens = seq_lens;
   a.q_pos = q_pos;
@@ -178,19 +240,18 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   a.cache_v = cache.v;
   a.w_up_k = static_cast<const uint8_t*>(w_up_k) + static_cast<size_t>(loop_t) * H * d * dims->r_k * esize;
   a.w_up_v = static_cast<const uint8_t*>(w_up_v) + static_cast<size_t>(loop_t) * H * d * dims->r_v * esize;
-  a.mu_k = mu_k + static_cast<size_t>(loop_t) * d;
-  a.mu_v = mu_v + static_cast<size_t>(loop_t) * d;
+  const size_t mu_loop = dims->variant == LLA_2D ? static_cast<size_t>(H) * d : d;
+  a.mu_k = mu_k + loop_t * mu_loop;
+  a.mu_v = mu_v + loop_t * mu_loop;
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;
   a.out = out;
   a.lse = lse;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.partials = reinterpret_cast<float*>(ws + wl.partials);
   a.scores = reinterpret_cast<float*>(ws + wl.scores);
   a.zimg = ws + wl.zimg;
   a.zimg_stride = static_cast<int64_t>(wl.zimg_stride);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (dims->dtype == LLA_F32) return launch_decode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 
@@ -229,8 +290,9 @@ lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, in
 
   EncodeArgs a{};
   a.N = N;
-  a.H = dims->H;
-  a.Td = dims->T * dims->d_head;
+  // LLA-2D: one latent per token from the whole stack x in R^{T*H*d} (one "head")
+  a.H = dims->variant == LLA_2D ? 1 : dims->H;
+  a.Td = dims->T * dims->d_head * (dims->variant == LLA_2D ? dims->H : 1);
   a.r_k = dims->r_k;
   a.r_v = dims->r_v;
   a.B = cache.B;

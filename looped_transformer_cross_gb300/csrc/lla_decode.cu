@@ -827,7 +827,8 @@ decode_f32_scores_kernel(const __grid_constant__ DecodeArgs a) {
     qrot[i0] = qv[i0] * c - qv[i1] * s;
     qrot[i1] = qv[i0] * s + qv[i1] * c;
   }
-  const float* C = static_cast<const float*>(a.cache_k) + (static_cast<int64_t>(u) * a.L_max + j0) * a.r_k;
+  const int64_t cu = a.shared_latent ? b : u;   // LLA-2D: every head reads the sequence's latent
+  const float* C = static_cast<const float*>(a.cache_k) + (cu * a.L_max + j0) * a.r_k;
   const float* W = static_cast<const float*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
   const int rows = min(kTile, static_cast<int>(a.L_max - j0));
   float kh[kHeadDim];
@@ -900,7 +901,8 @@ decode_f32_values_kernel(const __grid_constant__ DecodeArgs a) {
     z += p;
   }
   z = block_reduce(z, red, false);   // also orders the p writes before the reads below
-  const float* Cv = static_cast<const float*>(a.cache_v) + static_cast<int64_t>(u) * a.L_max * a.r_v;
+  const float* Cv =
+      static_cast<const float*>(a.cache_v) + static_cast<int64_t>(a.shared_latent ? b : u) * a.L_max * a.r_v;
   if (tid < a.r_v) {
     float v = 0.f;
     for (int j = 0; j < L; ++j) v = fmaf(sc[j], Cv[static_cast<int64_t>(j) * a.r_v + tid], v);

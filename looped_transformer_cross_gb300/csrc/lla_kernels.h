@@ -35,6 +35,7 @@ struct DecodePlan {
 
 struct DecodeArgs {
   int B, H, r_k, r_v, rope_style, grid;
+  int shared_latent;                 // fp32 path: 1 = LLA-2D cache [B][L_max][r] read by every head
   int64_t L_max, rope_len, mu_hstride;
   const void* q;                     // [B][H][128]
   const int32_t* seq_lens;           // [B]
@@ -66,6 +67,54 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p);
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
+
+// ----------------------------------------------------------------- LLA-2D decode
+
+constexpr int kDecode2dThreads = 320;   // producer, MMA/relay, 8 epilogue warps
+constexpr int kBlock2dTokens = 512;     // tokens of a pair block: 2 tiles per CTA
+constexpr int kMax2dHeads = 16;         // heads of one shared latent (value MMA N = 32)
+constexpr int kMaxPairs = kMaxGrid / 2;
+
+// Shared-memory plan of the LLA-2D decode kernel (byte offsets from a 1024-aligned base).
+struct Decode2dPlan {
+  int nkc;                           // 64-wide K chunks of a latent / query-operand row (r_k <= 128)
+  int nvh;                           // 128-row halves of r_v (value MMA M = 256 per pair)
+  int k_stage, z_stage, v_stage;     // ring stage strides
+  int k_ring, z_ring, v_ring, p, scores, misc;
+  int bytes;
+};
+
+struct Decode2dArgs {
+  int B, H, r_k, r_v, rope_style, pairs;
+  int64_t L_max, rope_len;
+  const void* q;                     // [B][H][128]
+  const int32_t* seq_lens;           // [B]
+  const int32_t* q_pos;              // [B]
+  const void* w_up_k;                // loop-t slice [H*128][r_k]
+  const void* w_up_v;                // loop-t slice [H*128][r_v]
+  const float* mu_k;                 // loop-t slice [H*128]
+  const float* mu_v;
+  const float* rope_cos;             // [rope_len][64]
+  const float* rope_sin;
+  float* out;                        // [B][H][128]
+  float* lse;                        // [B][H]
+  uint32_t* status;
+  float* rec_acc;                    // [2 * (B + pairs)][H][r_v] run records
+  float* rec_ml;                     // [2 * (B + pairs)][H][2]   (m, l) of each record
+  uint8_t* zimg;                     // per sequence: nkc chunks of [H*128 rows][128 B], then fp32 bias [H*128]
+  int64_t zimg_stride;               // bytes per sequence image
+  int64_t zchunk_bytes;              // H * 128 * 128
+  Decode2dPlan plan;
+};
+
+struct Decode2dMaps {
+  CUtensorMap k;                     // latent K: box (64, 128, 1) over (r_k, L_max, B), 128B swizzle
+  CUtensorMap v;                     // latent V: box (64, 16, 1) over (r_v, L_max, B), 128B swizzle
+};
+
+bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p);
+size_t decode2d_zimg_stride(int H, int r_k);
+cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cudaStream_t s);
 
 // ----------------------------------------------------------------- encode
 
