@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -49,7 +50,7 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t partials, rec_ml, bias, scores, zimg, zimg_stride, total;
+  size_t partials, rec_ml, bias, scores, zimg, zimg_stride, trig16, total;
 };
 
 // Bytes of one unit's query-operand image: Z (128 rows x r_k bf16, K-chunk
@@ -75,6 +76,9 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
       w.zimg_stride = decode2d_zimg_stride(d->H, d->r_k);
       off += al256(static_cast<size_t>(B) * w.zimg_stride);
     }
+    // f16 RoPE rows of the decode epilogue (positions up to L_max rounded to a block)
+    w.trig16 = off;
+    if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(decode2d_trig_rows(L_max, INT64_MAX)) * 256);
     w.total = off;
     return w;
   }
@@ -209,6 +213,8 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
     a.zimg = ws + wl.zimg;
     a.zimg_stride = static_cast<int64_t>(wl.zimg_stride);
     a.zchunk_bytes = static_cast<int64_t>(H) * d * 128;
+    a.trig16 = reinterpret_cast<uint32_t*>(ws + wl.trig16);
+    a.trig_rows = decode2d_trig_rows(cache.L_max, rope_len);
     const int sms = sm_count();
     if (sms <= 1) return LLA_ERR_CUDA;
     const int64_t max_blocks = static_cast<int64_t>(cache.B) * ((cache.L_max + kBlock2dTokens - 1) / kBlock2dTokens);

@@ -80,11 +80,6 @@ struct RingPos {
   __device__ __forceinline__ void next(int n) {
     if (++slot == n) { slot = 0; phase ^= 1u; }
   }
-  __device__ __forceinline__ RingPos plus(int k, int n) const {
-    RingPos r = *this;
-    for (int j = 0; j < k; ++j) r.next(n);
-    return r;
-  }
 };
 
 // Block of one sequence: tokens [512 kb, 512 kb + 512).
@@ -109,32 +104,19 @@ __device__ __forceinline__ void walk_advance(Walker2d& w, const Decode2dArgs& a)
   }
 }
 
-// Order of the 2H score stages of a block: heads in groups of four; in a group
-// every head's tile-slot-0 stage, then every head's tile-slot-1 stage.  A group's
-// query-operand windows are therefore all in flight together (kNZ = 4), and slot
-// 0's tile is released a whole group before the block ends.
+// Order of the 2H score stages of a block: head by head, tile slot 0 then tile
+// slot 1, so the two epilogue warp groups (one per tile slot) take turns and work
+// in parallel; head h's query window is needed by stages 2h and 2h + 1 only.
 struct StageIt {
-  int H, g = 0, i = 0, m, h, hh, s;
-  __device__ __forceinline__ explicit StageIt(int H_) : H(H_) {
-    m = H < 4 ? H : 4;
-    set();
-  }
-  __device__ __forceinline__ void set() {
-    s = i >= m ? 1 : 0;
-    hh = s ? i - m : i;
-    h = 4 * g + hh;
-  }
+  int H, st = 0, h = 0, s = 0;
+  __device__ __forceinline__ explicit StageIt(int H_) : H(H_) {}
   __device__ __forceinline__ void next() {
-    if (++i == 2 * m) {
-      ++g;
-      i = 0;
-      const int left = H - 4 * g;
-      m = left < 4 ? left : 4;
-    }
-    set();
+    ++st;
+    h = st >> 1;
+    s = st & 1;
   }
-  __device__ __forceinline__ bool first_tile_use() const { return g == 0 && hh == 0; }
-  __device__ __forceinline__ bool last_tile_use() const { return 4 * g + m >= H && hh == m - 1; }
+  __device__ __forceinline__ bool first_tile_use() const { return h == 0; }
+  __device__ __forceinline__ bool last_tile_use() const { return h == H - 1; }
 };
 
 // Value chunk c of the previous block is issued after stage `place(c)` of the
@@ -152,18 +134,35 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
 //   row h*128 + f      : sc (q'_i0 W_i0 + q'_i1 W_i1),  bias sc (q'_i0 mu_i0 + q'_i1 mu_i1)
 //   row h*128 + 64 + f : sc (q'_i1 W_i0 - q'_i0 W_i1),  bias sc (q'_i1 mu_i0 - q'_i0 mu_i1)
 // with W = W_up,k,t,h (rows h*128 + e of the loop-t slice) and mu = mu_k,t,h, so
-// that sum_f cos(j th_f) (U_f + bias_f) + sin(j th_f) (U_64+f + bias_64+f) with
-// U = c_j Z^T is log2(e) RoPE(q, q_pos).RoPE(k_j, j) / sqrt(d) for the key of
-// Eq. (3).  Layout per sequence: nkc chunks of [H*128 rows][64 bf16] in the
-// 128-byte swizzle of a K-major operand (row n swizzled by n mod 8), then the
-// fp32 bias [H*128].  Block = (sequence, head).
+// that sum_f cos(j th_f) U_f + sin(j th_f) U_64+f with U = c_j Z^T + bias is
+// log2(e) RoPE(q, q_pos).RoPE(k_j, j) / sqrt(d) for the key of Eq. (3).  Layout
+// per sequence: nkc chunks of [H*128 rows][64 bf16] in the 128-byte swizzle of a
+// K-major operand (row n swizzled by n mod 8), then the bias operand [H*128
+// rows][16 bf16] (32-byte swizzle): column 0 = bias rounded to bf16, column 1 =
+// the rounding remainder, so a 16-wide MMA against ones in columns 0 and 1 adds
+// the bias in ~16-bit precision.  Blocks = (sequence, head); the blocks after
+// them write the f16 copy of the RoPE table the epilogue reads (64 rows each).
 constexpr int kZThreads = 256;
+constexpr int kTrigRowsPerBlock = 64;
 __global__ void __launch_bounds__(kZThreads) decode2d_z_kernel(const __grid_constant__ Decode2dArgs a) {
   // the decode grid may start its set-up now; it waits for this grid before it
   // copies an image
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float qs[2][64];
   const int u = blockIdx.x, tid = threadIdx.x;
+  if (u >= a.B * a.H) {
+    // RoPE rows as f16 pairs: row p = {cos(p th_2i), cos(p th_2i+1)} i < 32, then sin
+    const int64_t r0 = static_cast<int64_t>(u - a.B * a.H) * kTrigRowsPerBlock;
+    for (int i = tid; i < kTrigRowsPerBlock * 64; i += kZThreads) {
+      const int64_t r = r0 + i / 64;
+      const int c = i % 64;            // pair index: 0..31 cos, 32..63 sin
+      if (r >= a.trig_rows) break;
+      const float* src = (c < 32 ? a.rope_cos : a.rope_sin) + r * 64 + 2 * (c & 31);
+      const __half2 v = __floats2half2_rn(src[0], src[1]);
+      a.trig16[r * 64 + c] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return;
+  }
   const int b = u / a.H, h = u - (u / a.H) * a.H;
   if (clamp_len(__ldg(a.seq_lens + b), a.L_max) == 0) return;
   uint8_t* img = a.zimg + static_cast<int64_t>(b) * a.zimg_stride;
@@ -204,9 +203,17 @@ __global__ void __launch_bounds__(kZThreads) decode2d_z_kernel(const __grid_cons
     const float q1 = (x0 * sq + x1 * cq) * scale;   // sc * q'_i1
     qs[0][f] = q0;
     qs[1][f] = q1;
-    float* bias = reinterpret_cast<float*>(img + a.plan.nkc * a.zchunk_bytes) + h * kHeadDim;
-    bias[f] = q0 * m0 + q1 * m1;
-    bias[64 + f] = q1 * m0 - q0 * m1;
+    const float bias[2] = {q0 * m0 + q1 * m1, q1 * m0 - q0 * m1};
+    uint8_t* ab = img + a.plan.nkc * a.zchunk_bytes;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int n = h * kHeadDim + f + 64 * half;
+      const __nv_bfloat16 zh = __float2bfloat16_rn(bias[half]);
+      const __nv_bfloat16 zl = __float2bfloat16_rn(bias[half] - __bfloat162float(zh));
+      const uint32_t pair = bf16x2_bits(__halves2bfloat162(zh, zl));
+      *reinterpret_cast<uint4*>(ab + swizzle_offset(n * 32, 32)) = make_uint4(pair, 0, 0, 0);
+      *reinterpret_cast<uint4*>(ab + swizzle_offset(n * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
+    }
   }
   __syncthreads();
 #pragma unroll
@@ -312,7 +319,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     }
     for (int s = 0; s < kNZ; ++s) {
       mbar_init(bar(misc->zfull[s]), 1);
-      mbar_init(bar(misc->zempty[s]), 1 + 8);   // the pair commit + the 8 epilogue warps (bias reads)
+      mbar_init(bar(misc->zempty[s]), 1);       // the pair commit after the window's last MMA
       mbar_init(bar(misc->zpeer[s]), 1);
     }
     for (int s = 0; s < kNV; ++s) {
@@ -337,6 +344,12 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
   // P rows of heads >= H stay zero
   for (int i = tid; i < kVChunks * 512 / 16; i += kDecode2dThreads)
     reinterpret_cast<uint4*>(sm + P.p)[i] = make_uint4(0, 0, 0, 0);
+  // bias operand A: columns 0 and 1 of every token row are 1 (they meet bias hi / lo)
+  if (tid < kTile) {
+    const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
+    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(tid * 32, 32)) = make_uint4(ones, 0, 0, 0);
+    *reinterpret_cast<uint4*>(sm + P.aug_a + swizzle_offset(tid * 32 + 16, 32)) = make_uint4(0, 0, 0, 0);
+  }
   fence_proxy_async_smem();
   __syncthreads();
   cluster_sync();   // the peer's barriers exist before any remote arrive
@@ -410,13 +423,13 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
               images_ready = true;
             }
             const uint32_t fb = bar(misc->zfull[sz]);
-            mbar_arrive_expect_tx(fb, P.nkc * 8192 + 512);
+            mbar_arrive_expect_tx(fb, P.nkc * 8192 + 2048);
             const uint8_t* img = a.zimg + static_cast<int64_t>(w.b) * a.zimg_stride;
             const uint32_t dst = sbase + P.z_ring + sz * P.z_stage;
             const int64_t row0 = static_cast<int64_t>(it.h) * kHeadDim + 64 * rank;
             for (int c = 0; c < P.nkc; ++c)
               bulk_load(dst + c * 8192, img + c * a.zchunk_bytes + row0 * kZRowBytes, 8192, fb);
-            bulk_load(dst + P.nkc * 8192, img + P.nkc * a.zchunk_bytes + it.h * 512, 512, fb);
+            bulk_load(dst + P.nkc * 8192, img + P.nkc * a.zchunk_bytes + row0 * 32, 2048, fb);
             ++issued_z;
             zr.next(kNZ);
           }
@@ -488,10 +501,22 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     }
   } else if (warp == 1) {
     // ======================================================== pair MMA issuer (even CTA)
+    // The issuing thread shares its sub-partition with two epilogue warps, so the
+    // loop is kept lean: base descriptors per ring (a slot adds slot * stride to the
+    // address field), K steps unrolled with constant offsets.
     if (lane == 0) {
       const uint32_t idesc_u = umma_idesc_bf16(256, 128, false, false);
       const uint32_t idesc_v = umma_idesc_bf16(256, 32, true, false);
       const int ksteps = a.r_k / 16;
+      const uint64_t dA0 = umma_desc(sbase + P.k_ring, 16, 1024, kSw128);
+      const uint64_t dZ0 = umma_desc(sbase + P.z_ring, 16, 1024, kSw128);
+      const uint64_t dZb0 = umma_desc(sbase + P.z_ring + P.nkc * 8192, 16, 256, kSw32);
+      const uint64_t daug = umma_desc(sbase + P.aug_a, 16, 256, kSw32);
+      // MN-major value operand: 64-row r_v boxes 2 KB apart (LBO), 8 token rows 1 KB apart (SBO)
+      const uint64_t dV0 = umma_desc(sbase + P.v_ring, 2048, 1024, kSw128);
+      const uint64_t dP0 = umma_desc(sbase + P.p, 16, 256, kSw32);
+      const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4, zst = static_cast<uint32_t>(P.z_stage) >> 4,
+                     vst = static_cast<uint32_t>(P.v_stage) >> 4;
       Walker2d w = start, wp = start;
       RingPos kr, zr, vr, ur;
       bool ok = true, prev_run_start = true;
@@ -507,12 +532,10 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         if (valid > 0) {
           zero_v_tail(sv, valid);
           tc_fence_after();
-          // MN-major A: 64-row r_v boxes 2 KB apart (LBO), 8 token rows 1 KB apart (SBO)
-          const uint64_t av = umma_desc(sbase + P.v_ring + sv * P.v_stage, 2048, 1024, kSw128);
-          const uint64_t bp = umma_desc(sbase + P.p + c * 512, 16, 256, kSw32);
+          const uint64_t av = dV0 + sv * vst, bp = dP0 + c * (512 >> 4);
           const uint32_t acc = (c > 0 || !run_start) ? 1u : 0u;
-          for (int hv = 0; hv < P.nvh; ++hv)
-            umma_bf16_pair(tmem + kDvCol + 32 * hv, av + hv * (4096 >> 4), bp, idesc_v, acc);
+          umma_bf16_pair(tmem + kDvCol, av, bp, idesc_v, acc);
+          if (P.nvh > 1) umma_bf16_pair(tmem + kDvCol + 32, av + (4096 >> 4), bp, idesc_v, acc);
         }
         umma_commit_pair(bar(misc->vempty[sv]));
         if (c == kVChunks - 1) umma_commit_pair(bar(misc->vdone));
@@ -521,47 +544,47 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       };
       for (int n = 0; n < count && ok; ++n) {
         const bool run_start = n == 0 || w.kb == 0;
-        StageIt it(a.H);
-        int vc = 0;
-        RingPos zbase = zr;
-        int ts0 = 0, ts1 = 0;
-        for (int st = 0; st < 2 * a.H; ++st, it.next()) {
-          if (it.i == 0) {   // a group starts: its windows occupy the next it.m ring positions
-            zbase = zr;
-            zr = zr.plus(it.m, kNZ);
-          }
-          if (it.first_tile_use()) {
-            if (!(ok = mbar_wait(bar(misc->kfull[kr.slot]), kr.phase, abort, a.status))) break;
-            if (!(ok = mbar_wait_cluster(bar(misc->kpeer[kr.slot]), kr.phase, abort, a.status))) break;
-            if (it.s == 0) ts0 = kr.slot; else ts1 = kr.slot;
-            kr.next(kNK);
-          }
-          const int ts = it.s ? ts1 : ts0;
-          const RingPos zw = zbase.plus(it.hh, kNZ);
-          if (it.s == 0) {
-            if (!(ok = mbar_wait(bar(misc->zfull[zw.slot]), zw.phase, abort, a.status))) break;
-            if (!(ok = mbar_wait_cluster(bar(misc->zpeer[zw.slot]), zw.phase, abort, a.status))) break;
-          }
-          const int su = ur.slot;
-          if (!(ok = mbar_wait_cluster(bar(misc->uempty[su]), ur.phase ^ 1u, abort, a.status))) break;
-          tc_fence_after();
-          const uint64_t a0 = umma_desc(sbase + P.k_ring + ts * P.k_stage, 16, 1024, kSw128);
-          const uint64_t b0 = umma_desc(sbase + P.z_ring + zw.slot * P.z_stage, 16, 1024, kSw128);
-          for (int k = 0; k < ksteps; ++k) {
-            const uint32_t ka = (k >> 2) * (16384 >> 4) + (k & 3) * 2;
-            const uint32_t kz = (k >> 2) * (8192 >> 4) + (k & 3) * 2;
-            umma_bf16_pair(tmem + 128 * su, a0 + ka, b0 + kz, idesc_u, k > 0 ? 1u : 0u);
-          }
-          umma_commit_pair(bar(misc->ufull[it.s][su]));
-          if (it.s == 1) umma_commit_pair(bar(misc->zempty[zw.slot]));
-          if (it.last_tile_use()) umma_commit_pair(bar(misc->kempty[ts]));
-          ur.next(kNU);
-          if (n > 0) {
-            while (ok && vc < kVChunks && vchunk_stage(vc, a.H) == st) {
-              ok = issue_v(wp, prev_run_start, vc, n - 1);
-              ++vc;
+        int vc = 0, ts0 = 0, ts1 = 0;
+        for (int h = 0; h < a.H && ok; ++h) {
+          // head h's query window: the next Z ring position
+          const int zs = zr.slot;
+          if (!(ok = mbar_wait(bar(misc->zfull[zs]), zr.phase, abort, a.status))) break;
+          if (!(ok = mbar_wait_cluster(bar(misc->zpeer[zs]), zr.phase, abort, a.status))) break;
+          zr.next(kNZ);
+          const uint64_t b0 = dZ0 + zs * zst, bb = dZb0 + zs * zst;
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            if (h == 0) {   // the block's tile s, first use
+              if (!(ok = mbar_wait(bar(misc->kfull[kr.slot]), kr.phase, abort, a.status))) break;
+              if (!(ok = mbar_wait_cluster(bar(misc->kpeer[kr.slot]), kr.phase, abort, a.status))) break;
+              if (s == 0) ts0 = kr.slot; else ts1 = kr.slot;
+              kr.next(kNK);
             }
-            if (!ok) break;
+            const int ts = s ? ts1 : ts0;
+            const int su = ur.slot;
+            if (!(ok = mbar_wait_cluster(bar(misc->uempty[su]), ur.phase ^ 1u, abort, a.status))) break;
+            tc_fence_after();
+            const uint64_t a0 = dA0 + ts * kst;
+            const uint32_t d = tmem + 128 * su;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              // 64-wide K chunks: A chunks 16 KB apart, Z chunks 8 KB apart; 32 B per K step
+              if (k < ksteps)
+                umma_bf16_pair(d, a0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
+                               b0 + (k >> 2) * (8192 >> 4) + (k & 3) * 2, idesc_u, k > 0 ? 1u : 0u);
+            }
+            umma_bf16_pair(d, daug, bb, idesc_u, 1u);   // + bias
+            umma_commit_pair(bar(misc->ufull[s][su]));
+            if (s == 1) umma_commit_pair(bar(misc->zempty[zs]));
+            if (h == a.H - 1) umma_commit_pair(bar(misc->kempty[ts]));
+            ur.next(kNU);
+            if (n > 0) {
+              const int st = 2 * h + s;
+              while (ok && vc < kVChunks && vchunk_stage(vc, a.H) == st) {
+                ok = issue_v(wp, prev_run_start, vc, n - 1);
+                ++vc;
+              }
+            }
           }
         }
         prev_run_start = run_start;
@@ -584,17 +607,18 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     uint8_t* pbuf = sm + P.p;
     const int H = a.H;
 
-    float cs[128];   // cos(j th_f) for f < 64, then sin(j th_f), for this thread's token j
+    // cos/sin(j th_f) of this thread's token j as f16 pairs: cs2[i] = (f = 2i, 2i + 1),
+    // cos for i < 32, sin for i >= 32 (the f16 rounding error, 2^-12, is below the
+    // bf16 query operand's)
+    uint32_t cs2[64];
     auto load_trig = [&](const Walker2d& wb) {
       int64_t j = static_cast<int64_t>(wb.kb) * kBlock2dTokens + rank * 256 + wg * kTile + row;
-      if (j >= a.rope_len) j = a.rope_len - 1;   // past the sequence end: masked anyway
-      const float4* c4 = reinterpret_cast<const float4*>(a.rope_cos + j * 64);
-      const float4* s4 = reinterpret_cast<const float4*>(a.rope_sin + j * 64);
+      if (j >= a.trig_rows) j = a.trig_rows - 1;   // past the sequence end: masked anyway
+      const uint4* t4 = reinterpret_cast<const uint4*>(a.trig16 + j * 64);
 #pragma unroll
-      for (int f = 0; f < 16; ++f) {
-        const float4 c = __ldg(c4 + f), s = __ldg(s4 + f);
-        cs[4 * f] = c.x; cs[4 * f + 1] = c.y; cs[4 * f + 2] = c.z; cs[4 * f + 3] = c.w;
-        cs[64 + 4 * f] = s.x; cs[64 + 4 * f + 1] = s.y; cs[64 + 4 * f + 2] = s.z; cs[64 + 4 * f + 3] = s.w;
+      for (int i = 0; i < 16; ++i) {
+        const uint4 v = __ldg(t4 + i);
+        cs2[4 * i] = v.x; cs2[4 * i + 1] = v.y; cs2[4 * i + 2] = v.z; cs2[4 * i + 3] = v.w;
       }
     };
     auto epi_sync = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
@@ -624,6 +648,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
 
     Walker2d w = start;
     int prev_b = start.b;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the f16 RoPE rows are written
     load_trig(w);
     bool ok = true;
     uint32_t uph = 0;   // this group's phase bit of each score buffer's ufull
@@ -632,39 +657,34 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       {
         const int jtok = w.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + wg * kTile + row;
         const bool valid = jtok < w.L;
-        // this warp group's stages of the block: st = 8 g + 4 wg + hh, head h = 4 g + hh;
-        // score buffer (2 H n + st) mod 3, query window (H n + h) mod 4
+        // this warp group's stages of the block: st = 2 h + wg; score buffer (2 H n + st) mod 3
         const uint32_t gbase = static_cast<uint32_t>(2 * H) * n;
-        const uint32_t zbase = static_cast<uint32_t>(H) * n;
-        for (int g = 0; g < H / 4; ++g) {
+        {
 #pragma unroll 1
-          for (int hh = 0; hh < 4; ++hh) {
-            const int h = 4 * g + hh;
-            const uint32_t G = gbase + 8 * g + 4 * wg + hh;
+          for (int h = 0; h < H; ++h) {
+            const uint32_t G = gbase + 2 * h + wg;
             const uint32_t uslot = G % kNU;
-            const uint32_t zslot = (zbase + h) & (kNZ - 1);
             if (ok) ok = warp_wait(bar(misc->ufull[wg][uslot]), (uph >> uslot) & 1u, abort, a.status);
             uph ^= 1u << uslot;
             float s = -INFINITY;
             if (ok) {
               tc_fence_after();
-              const float4* bias =
-                  reinterpret_cast<const float4*>(sm + P.z_ring + zslot * P.z_stage + P.nkc * 8192);
               const uint32_t tU = tmem + lane_base + 128 * uslot;
               float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-              for (int cc = 0; cc < 16; ++cc) {
-                float u[8];
-                tmem_ld_x8(tU + 8 * cc, u);
+              for (int hf = 0; hf < 2; ++hf) {   // 64 columns per round, two loads in flight
+                float u0[32], u1[32];
+                tmem_ld_x32(tU + 64 * hf, u0);
+                tmem_ld_x32(tU + 64 * hf + 32, u1);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i4 = 0; i4 < 2; ++i4) {
-                  const float4 bb = bias[2 * cc + i4];
-                  const int c0 = 8 * cc + 4 * i4;
-                  acc0 = fmaf(u[4 * i4] + bb.x, cs[c0], acc0);
-                  acc1 = fmaf(u[4 * i4 + 1] + bb.y, cs[c0 + 1], acc1);
-                  acc0 = fmaf(u[4 * i4 + 2] + bb.z, cs[c0 + 2], acc0);
-                  acc1 = fmaf(u[4 * i4 + 3] + bb.w, cs[c0 + 3], acc1);
+                for (int i = 0; i < 16; ++i) {
+                  const float2 t0 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + i]));
+                  const float2 t1 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + 16 + i]));
+                  acc0 = fmaf(u0[2 * i], t0.x, acc0);
+                  acc1 = fmaf(u0[2 * i + 1], t0.y, acc1);
+                  acc0 = fmaf(u1[2 * i], t1.x, acc0);
+                  acc1 = fmaf(u1[2 * i + 1], t1.y, acc1);
                 }
               }
               if (valid) s = acc0 + acc1;
@@ -672,15 +692,14 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
             }
             scores[h * 256 + tid_e] = s;
             __syncwarp();
-            if (lane == 0) {
-              arrive_even(bar(misc->uempty[uslot]));
-              mbar_arrive(bar(misc->zempty[zslot]));   // this warp is done with the window's bias
-            }
+            if (lane == 0) arrive_even(bar(misc->uempty[uslot]));
           }
         }
       }
       Walker2d wn = w;
       walk_advance(wn, a);
+      // this thread's token rows are no longer needed: fetch the next block's now
+      if (n + 1 < count) load_trig(wn);
 
       // ---- end of block: exact per-head maximum over the CTA's 256 tokens
       epi_sync();
@@ -758,7 +777,6 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       }
       __syncwarp();
       if (lane == 0) arrive_even(bar(misc->pfull));
-      if (n + 1 < count) load_trig(wn);
       prev_b = w.b;
       w = wn;
     }
@@ -926,13 +944,14 @@ bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p) {
   p->nkc = (r_k + 63) / 64;
   p->nvh = (r_v + 127) / 128;
   p->k_stage = p->nkc * 16384;
-  p->z_stage = p->nkc * 8192 + 1024;   // half window rows, then the head's 512-byte bias
+  p->z_stage = p->nkc * 8192 + 2048;   // half window rows, then their 16-wide bias operand
   p->v_stage = p->nvh * 4096;
   int off = 0;
   p->k_ring = off; off += kNK * p->k_stage;
   p->z_ring = off; off += kNZ * p->z_stage;
   p->v_ring = off; off += kNV * p->v_stage;
   p->p = off;      off += kVChunks * 512;
+  p->aug_a = off;  off += 4096;
   p->scores = off; off += H * 256 * 4;
   p->misc = off;   off += 4096;
   p->bytes = off + 1024;
@@ -941,8 +960,14 @@ bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p) {
 
 size_t decode2d_zimg_stride(int H, int r_k) {
   const size_t nkc = (r_k + 63) / 64;
-  const size_t b = nkc * H * kHeadDim * kZRowBytes + static_cast<size_t>(H) * kHeadDim * 4;
+  const size_t b = nkc * H * kHeadDim * kZRowBytes + static_cast<size_t>(H) * kHeadDim * 32;
   return (b + 1023) / 1024 * 1024;
+}
+
+int64_t decode2d_trig_rows(int64_t L_max, int64_t rope_len) {
+  // positions a block can touch: up to L_max rounded up to a whole block
+  const int64_t need = (L_max + kBlock2dTokens - 1) / kBlock2dTokens * kBlock2dTokens;
+  return need < rope_len ? need : rope_len;
 }
 
 cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cudaStream_t s) {
@@ -970,7 +995,8 @@ cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cuda
   a.pairs = std::min(a.pairs, std::min(max_pairs, kMaxPairs));
   if (a.pairs < 1) a.pairs = 1;
 
-  decode2d_z_kernel<<<a.B * a.H, kZThreads, 0, s>>>(a);
+  const int trig_blocks = static_cast<int>((a.trig_rows + kTrigRowsPerBlock - 1) / kTrigRowsPerBlock);
+  decode2d_z_kernel<<<a.B * a.H + trig_blocks, kZThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

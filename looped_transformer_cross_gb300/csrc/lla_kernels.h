@@ -80,7 +80,7 @@ struct Decode2dPlan {
   int nkc;                           // 64-wide K chunks of a latent / query-operand row (r_k <= 128)
   int nvh;                           // 128-row halves of r_v (value MMA M = 256 per pair)
   int k_stage, z_stage, v_stage;     // ring stage strides
-  int k_ring, z_ring, v_ring, p, scores, misc;
+  int k_ring, z_ring, v_ring, p, aug_a, scores, misc;
   int bytes;
 };
 
@@ -101,9 +101,12 @@ struct Decode2dArgs {
   uint32_t* status;
   float* rec_acc;                    // [2 * (B + pairs)][H][r_v] run records
   float* rec_ml;                     // [2 * (B + pairs)][H][2]   (m, l) of each record
-  uint8_t* zimg;                     // per sequence: nkc chunks of [H*128 rows][128 B], then fp32 bias [H*128]
+  uint8_t* zimg;                     // per sequence: nkc chunks of [H*128 rows][128 B], then the bias
+                                     // operand [H*128 rows][16 bf16] (32 B rows)
   int64_t zimg_stride;               // bytes per sequence image
   int64_t zchunk_bytes;              // H * 128 * 128
+  uint32_t* trig16;                  // [trig_rows][64] f16 pairs: cos(p th_2i), cos(p th_2i+1), then sin
+  int64_t trig_rows;                 // rows of trig16 (positions 0 .. trig_rows - 1)
   Decode2dPlan plan;
 };
 
@@ -114,6 +117,7 @@ struct Decode2dMaps {
 
 bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p);
 size_t decode2d_zimg_stride(int H, int r_k);
+int64_t decode2d_trig_rows(int64_t L_max, int64_t rope_len);
 cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cudaStream_t s);
 
 // ----------------------------------------------------------------- encode

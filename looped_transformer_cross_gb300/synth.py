@@ -76,6 +76,10 @@ WORKLOADS = {
     # LLA-2D: one latent per token for all heads, r = (128, 256), 256 x 8192
     "lla2d_b256_8k": Workload("lla2d_b256_8k", T=4, H=16, d=128, r_k=128, r_v=256, B=256,
                               L_max=8192, len_lo=8192, len_hi=8192, variant=1),
+    # the same with 32 sequences (about 200 MB of latents, still above L2): the small
+    # case for kernel profiles
+    "lla2d_b32_8k": Workload("lla2d_b32_8k", T=4, H=16, d=128, r_k=128, r_v=256, B=32,
+                             L_max=8192, len_lo=8192, len_hi=8192, variant=1),
 }
 
 
