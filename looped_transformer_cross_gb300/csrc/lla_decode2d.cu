@@ -56,14 +56,16 @@ constexpr uint32_t kDvCol = 384;   // TMEM column of the value accumulators (2 x
 constexpr int kZRowBytes = 128;    // one 64-wide bf16 chunk row
 
 struct alignas(16) Misc2d {
-  uint64_t kfull[kNK], kempty[kNK], kpeer[kNK];
-  uint64_t zfull[kNZ], zempty[kNZ], zpeer[kNZ];
-  uint64_t vfull[kNV], vempty[kNV], vpeer[kNV];
+  // full barriers: in the even CTA they also take the odd CTA's relay arrive (count
+  // 2), so one wait covers both halves of a pair operand
+  uint64_t kfull[kNK], kempty[kNK];
+  uint64_t zfull[kNZ], zempty[kNZ];
+  uint64_t vfull[kNV], vempty[kNV];
   // Score buffers: ufull per epilogue warp group (the group of a stage is its tile
   // slot), so that a group, which skips the other group's stages, never waits on a
   // barrier phase more than one completion ahead; uempty has one waiter (the issuer).
   uint64_t ufull[2][kNU], uempty[kNU];
-  uint64_t pfull, vdone, mma_done;
+  uint64_t pfull, vdone, mma_done[2];
   uint32_t tmem_base;
   int abort;
   int start_b, start_kb, count, total_blocks;
@@ -104,25 +106,13 @@ __device__ __forceinline__ void walk_advance(Walker2d& w, const Decode2dArgs& a)
   }
 }
 
-// Order of the 2H score stages of a block: head by head, tile slot 0 then tile
-// slot 1, so the two epilogue warp groups (one per tile slot) take turns and work
-// in parallel; head h's query window is needed by stages 2h and 2h + 1 only.
-struct StageIt {
-  int H, st = 0, h = 0, s = 0;
-  __device__ __forceinline__ explicit StageIt(int H_) : H(H_) {}
-  __device__ __forceinline__ void next() {
-    ++st;
-    h = st >> 1;
-    s = st & 1;
-  }
-  __device__ __forceinline__ bool first_tile_use() const { return h == 0; }
-  __device__ __forceinline__ bool last_tile_use() const { return h == H - 1; }
-};
-
-// Value chunk c of the previous block is issued after stage `place(c)` of the
-// current one (the first chunk three stages in, so the previous block's weights
-// exist by then).
-__device__ __forceinline__ int vchunk_stage(int c, int H) { return min(2 * c + 3, 2 * H - 1); }
+// Score stages of a block: head by head, tile slot 0 then tile slot 1 (stage
+// st = 2h + s), so the two epilogue warp groups (one per tile slot) take turns.
+// Two issuer warps share the work: one issues the tile-slot-0 stages and the value
+// MMAs, the other the tile-slot-1 stages, so one warp's waits and commits overlap
+// the other's MMAs.  Value chunk c of the previous block follows head vchunk_head(c)
+// in every role's order (the first one two heads in, once that block's weights exist).
+__device__ __forceinline__ int vchunk_head(int c, int H) { return min(c + 2, H - 1); }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<uint32_t*>(&v);
@@ -312,20 +302,18 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
   // ---------------------------------------------------------- set-up
   auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
   if (tid == 0) {
+    const uint32_t nfull = rank == 0 ? 2 : 1;   // + the odd CTA's relay in the even CTA
     for (int s = 0; s < kNK; ++s) {
-      mbar_init(bar(misc->kfull[s]), 1);
+      mbar_init(bar(misc->kfull[s]), nfull);
       mbar_init(bar(misc->kempty[s]), 1);
-      mbar_init(bar(misc->kpeer[s]), 1);
     }
     for (int s = 0; s < kNZ; ++s) {
-      mbar_init(bar(misc->zfull[s]), 1);
-      mbar_init(bar(misc->zempty[s]), 1);       // the pair commit after the window's last MMA
-      mbar_init(bar(misc->zpeer[s]), 1);
+      mbar_init(bar(misc->zfull[s]), nfull);
+      mbar_init(bar(misc->zempty[s]), 2);       // both issuers' commits after the window's MMAs
     }
     for (int s = 0; s < kNV; ++s) {
-      mbar_init(bar(misc->vfull[s]), 1);
+      mbar_init(bar(misc->vfull[s]), nfull);
       mbar_init(bar(misc->vempty[s]), 1);
-      mbar_init(bar(misc->vpeer[s]), 1);
     }
     for (int s = 0; s < kNU; ++s) {
       mbar_init(bar(misc->ufull[0][s]), 1);
@@ -334,7 +322,8 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     }
     mbar_init(bar(misc->pfull), 16);             // 8 epilogue warps of each CTA
     mbar_init(bar(misc->vdone), 1);
-    mbar_init(bar(misc->mma_done), 1);
+    mbar_init(bar(misc->mma_done[0]), 1);
+    mbar_init(bar(misc->mma_done[1]), 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -380,9 +369,8 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
 
   if (warp == 0) {
     // ======================================================== TMA producer (each CTA)
-    // Loads in the order the MMA issuer needs them: per score stage the block's
-    // latent tile on its first use and head h's query window on its first use,
-    // then the value chunks of the previous block placed after that stage.
+    // Per block: both latent tiles, then per head its query window, with the value
+    // chunks of the previous block after head vchunk_head(c) -- the issuers' order.
     if (lane == 0) {
       Walker2d w = start, wp = start;
       RingPos kr, zr, vr;
@@ -401,45 +389,37 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         return true;
       };
       for (int n = 0; n < count && ok; ++n) {
-        StageIt it(a.H);
+        for (int s = 0; s < 2 && ok; ++s) {   // the block's two latent tiles
+          const int sk = kr.slot;
+          if (!(ok = mbar_wait(bar(misc->kempty[sk]), kr.phase ^ 1u, abort, a.status))) break;
+          const uint32_t fb = bar(misc->kfull[sk]);
+          mbar_arrive_expect_tx(fb, P.nkc * 16384);
+          const int y = w.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + kTile * s;
+          for (int c = 0; c < P.nkc; ++c)
+            tma_load_3d(sbase + P.k_ring + sk * P.k_stage + c * 16384, &maps.k, fb, 64 * c, y, w.b);
+          ++issued_k;
+          kr.next(kNK);
+        }
         int vc = 0;
-        for (int st = 0; st < 2 * a.H; ++st, it.next()) {
-          if (it.first_tile_use()) {
-            const int sk = kr.slot;
-            if (!(ok = mbar_wait(bar(misc->kempty[sk]), kr.phase ^ 1u, abort, a.status))) break;
-            const uint32_t fb = bar(misc->kfull[sk]);
-            mbar_arrive_expect_tx(fb, P.nkc * 16384);
-            const int y = w.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + kTile * it.s;
-            for (int c = 0; c < P.nkc; ++c)
-              tma_load_3d(sbase + P.k_ring + sk * P.k_stage + c * 16384, &maps.k, fb, 64 * c, y, w.b);
-            ++issued_k;
-            kr.next(kNK);
+        for (int h = 0; h < a.H && ok; ++h) {
+          const int sz = zr.slot;
+          if (!(ok = mbar_wait(bar(misc->zempty[sz]), zr.phase ^ 1u, abort, a.status))) break;
+          if (!images_ready) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");   // images written
+            images_ready = true;
           }
-          if (it.s == 0) {
-            const int sz = zr.slot;
-            if (!(ok = mbar_wait(bar(misc->zempty[sz]), zr.phase ^ 1u, abort, a.status))) break;
-            if (!images_ready) {
-              asm volatile("griddepcontrol.wait;" ::: "memory");   // images written
-              images_ready = true;
-            }
-            const uint32_t fb = bar(misc->zfull[sz]);
-            mbar_arrive_expect_tx(fb, P.nkc * 8192 + 2048);
-            const uint8_t* img = a.zimg + static_cast<int64_t>(w.b) * a.zimg_stride;
-            const uint32_t dst = sbase + P.z_ring + sz * P.z_stage;
-            const int64_t row0 = static_cast<int64_t>(it.h) * kHeadDim + 64 * rank;
-            for (int c = 0; c < P.nkc; ++c)
-              bulk_load(dst + c * 8192, img + c * a.zchunk_bytes + row0 * kZRowBytes, 8192, fb);
-            bulk_load(dst + P.nkc * 8192, img + P.nkc * a.zchunk_bytes + row0 * 32, 2048, fb);
-            ++issued_z;
-            zr.next(kNZ);
-          }
-          if (n > 0) {
-            while (ok && vc < kVChunks && vchunk_stage(vc, a.H) == st) {
-              ok = load_v(wp, vc);
-              ++vc;
-            }
-            if (!ok) break;
-          }
+          const uint32_t fb = bar(misc->zfull[sz]);
+          mbar_arrive_expect_tx(fb, P.nkc * 8192 + 2048);
+          const uint8_t* img = a.zimg + static_cast<int64_t>(w.b) * a.zimg_stride;
+          const uint32_t dst = sbase + P.z_ring + sz * P.z_stage;
+          const int64_t row0 = static_cast<int64_t>(h) * kHeadDim + 64 * rank;
+          for (int c = 0; c < P.nkc; ++c)
+            bulk_load(dst + c * 8192, img + c * a.zchunk_bytes + row0 * kZRowBytes, 8192, fb);
+          bulk_load(dst + P.nkc * 8192, img + P.nkc * a.zchunk_bytes + row0 * 32, 2048, fb);
+          ++issued_z;
+          zr.next(kNZ);
+          if (n > 0)
+            while (ok && vc < kVChunks && vchunk_head(vc, a.H) == h) ok = load_v(wp, vc++);
         }
         wp = w;
         walk_advance(w, a);
@@ -458,8 +438,8 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     }
   } else if (warp == 1 && rank == 1) {
     // ======================================================== relay (odd CTA)
-    // Forwards each completed load of this CTA to the MMA issuer of the even CTA,
-    // in the issuer's order.
+    // Forwards each completed load of this CTA to the even CTA's full barrier, in
+    // the producer's order.
     if (lane == 0) {
       Walker2d w = start, wp = start;
       RingPos kr, zr, vr;
@@ -468,42 +448,37 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         const int sv = vr.slot;
         if (!mbar_wait(bar(misc->vfull[sv]), vr.phase, abort, a.status)) return false;
         zero_v_tail(sv, wb.L - (wb.kb * kBlock2dTokens + 256 + 16 * c));
-        mbar_arrive_cluster(bar(misc->vpeer[sv]), 0);
+        mbar_arrive_cluster(bar(misc->vfull[sv]), 0);
         vr.next(kNV);
         return true;
       };
       for (int n = 0; n < count && ok; ++n) {
-        StageIt it(a.H);
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (!(ok = mbar_wait(bar(misc->kfull[kr.slot]), kr.phase, abort, a.status))) break;
+          mbar_arrive_cluster(bar(misc->kfull[kr.slot]), 0);
+          kr.next(kNK);
+        }
         int vc = 0;
-        for (int st = 0; st < 2 * a.H; ++st, it.next()) {
-          if (it.first_tile_use()) {
-            if (!(ok = mbar_wait(bar(misc->kfull[kr.slot]), kr.phase, abort, a.status))) break;
-            mbar_arrive_cluster(bar(misc->kpeer[kr.slot]), 0);
-            kr.next(kNK);
-          }
-          if (it.s == 0) {
-            if (!(ok = mbar_wait(bar(misc->zfull[zr.slot]), zr.phase, abort, a.status))) break;
-            mbar_arrive_cluster(bar(misc->zpeer[zr.slot]), 0);
-            zr.next(kNZ);
-          }
-          if (n > 0) {
-            while (ok && vc < kVChunks && vchunk_stage(vc, a.H) == st) {
-              ok = relay_v(wp, vc);
-              ++vc;
-            }
-            if (!ok) break;
-          }
+        for (int h = 0; h < a.H && ok; ++h) {
+          if (!(ok = mbar_wait(bar(misc->zfull[zr.slot]), zr.phase, abort, a.status))) break;
+          mbar_arrive_cluster(bar(misc->zfull[zr.slot]), 0);
+          zr.next(kNZ);
+          if (n > 0)
+            while (ok && vc < kVChunks && vchunk_head(vc, a.H) == h) ok = relay_v(wp, vc++);
         }
         wp = w;
         walk_advance(w, a);
       }
       for (int c = 0; ok && c < kVChunks; ++c) ok = relay_v(wp, c);
     }
-  } else if (warp == 1) {
-    // ======================================================== pair MMA issuer (even CTA)
-    // The issuing thread shares its sub-partition with two epilogue warps, so the
-    // loop is kept lean: base descriptors per ring (a slot adds slot * stride to the
-    // address field), K steps unrolled with constant offsets.
+  } else if ((warp == 1 || warp == 10) && rank == 0) {
+    // ======================================================== pair MMA issuers (even CTA)
+    // Warp 1 issues the tile-slot-0 stages and every value MMA, warp 10 the
+    // tile-slot-1 stages.  Ring positions follow from global counters (block n,
+    // head h): tile 2n + sel, window nH + h, stage 2Hn + 2h + sel.  The loop is kept
+    // lean (the issuing threads share their sub-partitions with epilogue warps):
+    // base descriptors per ring, K steps unrolled with constant offsets.
+    const int sel = warp == 1 ? 0 : 1;
     if (lane == 0) {
       const uint32_t idesc_u = umma_idesc_bf16(256, 128, false, false);
       const uint32_t idesc_v = umma_idesc_bf16(256, 32, true, false);
@@ -517,8 +492,9 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       const uint64_t dP0 = umma_desc(sbase + P.p, 16, 256, kSw32);
       const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4, zst = static_cast<uint32_t>(P.z_stage) >> 4,
                      vst = static_cast<uint32_t>(P.v_stage) >> 4;
+      const uint32_t H = static_cast<uint32_t>(a.H);
       Walker2d w = start, wp = start;
-      RingPos kr, zr, vr, ur;
+      RingPos vr;
       bool ok = true, prev_run_start = true;
       // Value MMAs of chunk c of block `pblk` (walker wb): D_v[half] += C_v^T P over
       // the chunk's 16 tokens of each CTA; chunks wholly past the sequence end
@@ -526,8 +502,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       auto issue_v = [&](const Walker2d& wb, bool run_start, int c, int pblk) -> bool {
         if (c == 0 && !mbar_wait_cluster(bar(misc->pfull), pblk & 1, abort, a.status)) return false;
         const int sv = vr.slot;
-        if (!mbar_wait(bar(misc->vfull[sv]), vr.phase, abort, a.status)) return false;
-        if (!mbar_wait_cluster(bar(misc->vpeer[sv]), vr.phase, abort, a.status)) return false;
+        if (!mbar_wait_cluster(bar(misc->vfull[sv]), vr.phase, abort, a.status)) return false;
         const int valid = wb.L - (wb.kb * kBlock2dTokens + 16 * c);
         if (valid > 0) {
           zero_v_tail(sv, valid);
@@ -542,62 +517,47 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         vr.next(kNV);
         return true;
       };
-      for (int n = 0; n < count && ok; ++n) {
+      for (uint32_t n = 0; n < static_cast<uint32_t>(count) && ok; ++n) {
         const bool run_start = n == 0 || w.kb == 0;
-        int vc = 0, ts0 = 0, ts1 = 0;
-        for (int h = 0; h < a.H && ok; ++h) {
-          // head h's query window: the next Z ring position
-          const int zs = zr.slot;
-          if (!(ok = mbar_wait(bar(misc->zfull[zs]), zr.phase, abort, a.status))) break;
-          if (!(ok = mbar_wait_cluster(bar(misc->zpeer[zs]), zr.phase, abort, a.status))) break;
-          zr.next(kNZ);
-          const uint64_t b0 = dZ0 + zs * zst, bb = dZb0 + zs * zst;
+        const uint32_t tile = 2 * n + sel, ts = tile % kNK;
+        if (!(ok = mbar_wait_cluster(bar(misc->kfull[ts]), (tile / kNK) & 1u, abort, a.status))) break;
+        const uint64_t a0 = dA0 + ts * kst;
+        int vc = 0;
+        for (uint32_t h = 0; h < H && ok; ++h) {
+          const uint32_t zi = n * H + h, zs = zi & (kNZ - 1);
+          if (!(ok = mbar_wait_cluster(bar(misc->zfull[zs]), (zi / kNZ) & 1u, abort, a.status))) break;
+          const uint32_t G = 2 * H * n + 2 * h + sel, su = G % kNU;
+          if (!(ok = mbar_wait_cluster(bar(misc->uempty[su]), ((G / kNU) & 1u) ^ 1u, abort, a.status))) break;
+          tc_fence_after();
+          const uint64_t b0 = dZ0 + zs * zst;
+          const uint32_t d = tmem + 128 * su;
 #pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            if (h == 0) {   // the block's tile s, first use
-              if (!(ok = mbar_wait(bar(misc->kfull[kr.slot]), kr.phase, abort, a.status))) break;
-              if (!(ok = mbar_wait_cluster(bar(misc->kpeer[kr.slot]), kr.phase, abort, a.status))) break;
-              if (s == 0) ts0 = kr.slot; else ts1 = kr.slot;
-              kr.next(kNK);
-            }
-            const int ts = s ? ts1 : ts0;
-            const int su = ur.slot;
-            if (!(ok = mbar_wait_cluster(bar(misc->uempty[su]), ur.phase ^ 1u, abort, a.status))) break;
-            tc_fence_after();
-            const uint64_t a0 = dA0 + ts * kst;
-            const uint32_t d = tmem + 128 * su;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              // 64-wide K chunks: A chunks 16 KB apart, Z chunks 8 KB apart; 32 B per K step
-              if (k < ksteps)
-                umma_bf16_pair(d, a0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
-                               b0 + (k >> 2) * (8192 >> 4) + (k & 3) * 2, idesc_u, k > 0 ? 1u : 0u);
-            }
-            umma_bf16_pair(d, daug, bb, idesc_u, 1u);   // + bias
-            umma_commit_pair(bar(misc->ufull[s][su]));
-            if (s == 1) umma_commit_pair(bar(misc->zempty[zs]));
-            if (h == a.H - 1) umma_commit_pair(bar(misc->kempty[ts]));
-            ur.next(kNU);
-            if (n > 0) {
-              const int st = 2 * h + s;
-              while (ok && vc < kVChunks && vchunk_stage(vc, a.H) == st) {
-                ok = issue_v(wp, prev_run_start, vc, n - 1);
-                ++vc;
-              }
-            }
+          for (int k = 0; k < 8; ++k) {
+            // 64-wide K chunks: A chunks 16 KB apart, Z chunks 8 KB apart; 32 B per K step
+            if (k < ksteps)
+              umma_bf16_pair(d, a0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
+                             b0 + (k >> 2) * (8192 >> 4) + (k & 3) * 2, idesc_u, k > 0 ? 1u : 0u);
           }
+          umma_bf16_pair(d, daug, dZb0 + zs * zst, idesc_u, 1u);   // + bias
+          umma_commit_pair(bar(misc->ufull[sel][su]));
+          umma_commit_pair(bar(misc->zempty[zs]));
+          if (h == H - 1) umma_commit_pair(bar(misc->kempty[ts]));
+          if (sel == 0 && n > 0)
+            while (ok && vc < kVChunks && vchunk_head(vc, a.H) == static_cast<int>(h))
+              ok = issue_v(wp, prev_run_start, vc++, n - 1);
         }
         prev_run_start = run_start;
         wp = w;
         walk_advance(w, a);
       }
-      for (int c = 0; ok && c < kVChunks; ++c) ok = issue_v(wp, prev_run_start, c, count - 1);
+      if (sel == 0)
+        for (int c = 0; ok && c < kVChunks; ++c) ok = issue_v(wp, prev_run_start, c, count - 1);
       // this thread's MMAs complete before TMEM is released
-      umma_commit_pair(bar(misc->mma_done));
+      umma_commit_pair(bar(misc->mma_done[sel]));
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      while (!mbar_try_wait(bar(misc->mma_done[sel]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 10) {
     // ======================================================== epilogue (warps 2-9)
     // Warps 2-5 serve tile slot 0, warps 6-9 tile slot 1; one token per thread.
     const int we = warp - 2, wg = we >> 2, q = warp & 3;
