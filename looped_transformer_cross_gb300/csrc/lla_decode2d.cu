@@ -70,8 +70,10 @@ struct alignas(16) Misc2d {
   int abort;
   int start_b, start_kb, count, total_blocks;
   float mx[8][kMax2dHeads];   // per epilogue warp: block maximum of each head
-  float lp[8][kMax2dHeads];   // per epilogue warp: block sum of the weights of each head
-  float m_ref[kMax2dHeads], l_run[kMax2dHeads];
+  float lp[8][kMax2dHeads];   // per epilogue warp: a run's sum of the weights of each head
+  float m_ref[kMax2dHeads];   // softmax reference of each head (log2 units)
+  float m_new[kMax2dHeads], alpha[kMax2dHeads];   // the block's new reference, rescale factor
+  float m_rec[kMax2dHeads];   // reference of a finished run (for its record)
   int scan[kDecode2dThreads];
 };
 static_assert(sizeof(Misc2d) <= 4096, "misc region");
@@ -108,10 +110,8 @@ __device__ __forceinline__ void walk_advance(Walker2d& w, const Decode2dArgs& a)
 
 // Score stages of a block: head by head, tile slot 0 then tile slot 1 (stage
 // st = 2h + s), so the two epilogue warp groups (one per tile slot) take turns.
-// Two issuer warps share the work: one issues the tile-slot-0 stages and the value
-// MMAs, the other the tile-slot-1 stages, so one warp's waits and commits overlap
-// the other's MMAs.  Value chunk c of the previous block follows head vchunk_head(c)
-// in every role's order (the first one two heads in, once that block's weights exist).
+// Value chunk c of the previous block follows head vchunk_head(c) in every role's
+// order (the first one two heads in, once that block's weights exist).
 __device__ __forceinline__ int vchunk_head(int c, int H) { return min(c + 2, H - 1); }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
@@ -309,7 +309,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     }
     for (int s = 0; s < kNZ; ++s) {
       mbar_init(bar(misc->zfull[s]), nfull);
-      mbar_init(bar(misc->zempty[s]), 2);       // both issuers' commits after the window's MMAs
+      mbar_init(bar(misc->zempty[s]), 1);       // the issuer's commit after the window's MMAs
     }
     for (int s = 0; s < kNV; ++s) {
       mbar_init(bar(misc->vfull[s]), nfull);
@@ -471,14 +471,12 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       }
       for (int c = 0; ok && c < kVChunks; ++c) ok = relay_v(wp, c);
     }
-  } else if ((warp == 1 || warp == 10) && rank == 0) {
-    // ======================================================== pair MMA issuers (even CTA)
-    // Warp 1 issues the tile-slot-0 stages and every value MMA, warp 10 the
-    // tile-slot-1 stages.  Ring positions follow from global counters (block n,
-    // head h): tile 2n + sel, window nH + h, stage 2Hn + 2h + sel.  The loop is kept
-    // lean (the issuing threads share their sub-partitions with epilogue warps):
-    // base descriptors per ring, K steps unrolled with constant offsets.
-    const int sel = warp == 1 ? 0 : 1;
+  } else if (warp == 1) {
+    // ======================================================== pair MMA issuer (even CTA)
+    // One thread issues every MMA of the pair.  Ring positions follow from global
+    // counters (block n, head h): tiles 2n, 2n + 1, window nH + h, stage 2Hn + 2h + s.
+    // The loop is kept lean (the issuing thread shares its sub-partition with two
+    // epilogue warps): base descriptors per ring, K steps unrolled with constant offsets.
     if (lane == 0) {
       const uint32_t idesc_u = umma_idesc_bf16(256, 128, false, false);
       const uint32_t idesc_v = umma_idesc_bf16(256, 32, true, false);
@@ -519,30 +517,38 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       };
       for (uint32_t n = 0; n < static_cast<uint32_t>(count) && ok; ++n) {
         const bool run_start = n == 0 || w.kb == 0;
-        const uint32_t tile = 2 * n + sel, ts = tile % kNK;
-        if (!(ok = mbar_wait_cluster(bar(misc->kfull[ts]), (tile / kNK) & 1u, abort, a.status))) break;
-        const uint64_t a0 = dA0 + ts * kst;
+        uint32_t ts[2];
+        for (int s = 0; s < 2 && ok; ++s) {
+          const uint32_t tile = 2 * n + s;
+          ts[s] = tile % kNK;
+          ok = mbar_wait_cluster(bar(misc->kfull[ts[s]]), (tile / kNK) & 1u, abort, a.status);
+        }
         int vc = 0;
         for (uint32_t h = 0; h < H && ok; ++h) {
           const uint32_t zi = n * H + h, zs = zi & (kNZ - 1);
           if (!(ok = mbar_wait_cluster(bar(misc->zfull[zs]), (zi / kNZ) & 1u, abort, a.status))) break;
-          const uint32_t G = 2 * H * n + 2 * h + sel, su = G % kNU;
-          if (!(ok = mbar_wait_cluster(bar(misc->uempty[su]), ((G / kNU) & 1u) ^ 1u, abort, a.status))) break;
-          tc_fence_after();
-          const uint64_t b0 = dZ0 + zs * zst;
-          const uint32_t d = tmem + 128 * su;
+          const uint64_t b0 = dZ0 + zs * zst, bb = dZb0 + zs * zst;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            // 64-wide K chunks: A chunks 16 KB apart, Z chunks 8 KB apart; 32 B per K step
-            if (k < ksteps)
-              umma_bf16_pair(d, a0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
-                             b0 + (k >> 2) * (8192 >> 4) + (k & 3) * 2, idesc_u, k > 0 ? 1u : 0u);
+          for (int s = 0; s < 2; ++s) {
+            const uint32_t G = 2 * H * n + 2 * h + s, su = G % kNU;
+            if (!(ok = mbar_wait_cluster(bar(misc->uempty[su]), ((G / kNU) & 1u) ^ 1u, abort, a.status))) break;
+            tc_fence_after();
+            const uint64_t a0 = dA0 + ts[s] * kst;
+            const uint32_t d = tmem + 128 * su;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              // 64-wide K chunks: A chunks 16 KB apart, Z chunks 8 KB apart; 32 B per K step
+              if (k < ksteps)
+                umma_bf16_pair(d, a0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
+                               b0 + (k >> 2) * (8192 >> 4) + (k & 3) * 2, idesc_u, k > 0 ? 1u : 0u);
+            }
+            umma_bf16_pair(d, daug, bb, idesc_u, 1u);   // + bias
+            umma_commit_pair(bar(misc->ufull[s][su]));
+            if (h == H - 1) umma_commit_pair(bar(misc->kempty[ts[s]]));
           }
-          umma_bf16_pair(d, daug, dZb0 + zs * zst, idesc_u, 1u);   // + bias
-          umma_commit_pair(bar(misc->ufull[sel][su]));
+          if (!ok) break;
           umma_commit_pair(bar(misc->zempty[zs]));
-          if (h == H - 1) umma_commit_pair(bar(misc->kempty[ts]));
-          if (sel == 0 && n > 0)
+          if (n > 0)
             while (ok && vc < kVChunks && vchunk_head(vc, a.H) == static_cast<int>(h))
               ok = issue_v(wp, prev_run_start, vc++, n - 1);
         }
@@ -550,12 +556,11 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         wp = w;
         walk_advance(w, a);
       }
-      if (sel == 0)
-        for (int c = 0; ok && c < kVChunks; ++c) ok = issue_v(wp, prev_run_start, c, count - 1);
+      for (int c = 0; ok && c < kVChunks; ++c) ok = issue_v(wp, prev_run_start, c, count - 1);
       // this thread's MMAs complete before TMEM is released
-      umma_commit_pair(bar(misc->mma_done[sel]));
+      umma_commit_pair(bar(misc->mma_done[0]));
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(bar(misc->mma_done[sel]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      while (!mbar_try_wait(bar(misc->mma_done[0]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
   } else if (warp >= 2 && warp < 10) {
     // ======================================================== epilogue (warps 2-9)
@@ -585,11 +590,16 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     auto arrive_even = [&](uint32_t b) {
       if (rank == 0) mbar_arrive(b); else mbar_arrive_cluster(b, 0);
     };
+    // Each thread keeps its token's running sum of the weights of every head (lt);
+    // the sums of the 256 tokens are reduced only when a run's record is written.
+    float lt[kMax2dHeads];
+#pragma unroll
+    for (int h = 0; h < kMax2dHeads; ++h) lt[h] = 0.f;
     // One record per (run, head): m, l and this CTA's share of acc_v (the half of
-    // r_v this warp group reads).
-    auto write_record = [&](int b) {
+    // r_v this warp group reads).  Called by all 256 epilogue threads (it syncs).
+    auto write_record = [&](int b, bool live) {
       const int64_t rec = 2LL * (b + pair) + rank;
-      if (wg < P.nvh) {
+      if (live && wg < P.nvh) {
         float v[16];
         tmem_ld_x16(tmem + lane_base + kDvCol + 32 * wg + 16 * rank, v);
         tmem_wait_ld();
@@ -600,9 +610,20 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
             if (h < H) a.rec_acc[(rec * H + h) * a.r_v + r] = v[h];
         }
       }
-      if (tid_e < H) {
-        a.rec_ml[(rec * H + tid_e) * 2] = misc->m_ref[tid_e];
-        a.rec_ml[(rec * H + tid_e) * 2 + 1] = misc->l_run[tid_e];
+#pragma unroll
+      for (int h = 0; h < kMax2dHeads; ++h) {
+        if (h < H) {
+          const float ls = warp_sum(lt[h]);
+          if (lane == 0) misc->lp[we][h] = ls;
+        }
+      }
+      epi_sync();
+      if (live && tid_e < H) {
+        float l = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 8; ++ww) l += misc->lp[ww][tid_e];
+        a.rec_ml[(rec * H + tid_e) * 2] = misc->m_rec[tid_e];
+        a.rec_ml[(rec * H + tid_e) * 2 + 1] = l;
       }
     };
 
@@ -619,40 +640,42 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         const bool valid = jtok < w.L;
         // this warp group's stages of the block: st = 2 h + wg; score buffer (2 H n + st) mod 3
         const uint32_t gbase = static_cast<uint32_t>(2 * H) * n;
-        {
 #pragma unroll 1
-          for (int h = 0; h < H; ++h) {
-            const uint32_t G = gbase + 2 * h + wg;
-            const uint32_t uslot = G % kNU;
-            if (ok) ok = warp_wait(bar(misc->ufull[wg][uslot]), (uph >> uslot) & 1u, abort, a.status);
-            uph ^= 1u << uslot;
-            float s = -INFINITY;
-            if (ok) {
-              tc_fence_after();
-              const uint32_t tU = tmem + lane_base + 128 * uslot;
-              float acc0 = 0.f, acc1 = 0.f;
+        for (int h = 0; h < H; ++h) {
+          const uint32_t G = gbase + 2 * h + wg;
+          const uint32_t uslot = G % kNU;
+          if (ok) ok = warp_wait(bar(misc->ufull[wg][uslot]), (uph >> uslot) & 1u, abort, a.status);
+          uph ^= 1u << uslot;
+          float s = -INFINITY;
+          if (ok) {
+            tc_fence_after();
+            const uint32_t tU = tmem + lane_base + 128 * uslot;
+            float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {   // 64 columns per round, two loads in flight
-                float u0[32], u1[32];
-                tmem_ld_x32(tU + 64 * hf, u0);
-                tmem_ld_x32(tU + 64 * hf + 32, u1);
-                tmem_wait_ld();
+            for (int hf = 0; hf < 2; ++hf) {   // 64 columns per round, two loads in flight
+              float u0[32], u1[32];
+              tmem_ld_x32(tU + 64 * hf, u0);
+              tmem_ld_x32(tU + 64 * hf + 32, u1);
+              tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const float2 t0 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + i]));
-                  const float2 t1 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + 16 + i]));
-                  acc0 = fmaf(u0[2 * i], t0.x, acc0);
-                  acc1 = fmaf(u0[2 * i + 1], t0.y, acc1);
-                  acc0 = fmaf(u1[2 * i], t1.x, acc0);
-                  acc1 = fmaf(u1[2 * i + 1], t1.y, acc1);
-                }
+              for (int i = 0; i < 16; ++i) {
+                const float2 t0 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + i]));
+                const float2 t1 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + 16 + i]));
+                acc0 = fmaf(u0[2 * i], t0.x, acc0);
+                acc1 = fmaf(u0[2 * i + 1], t0.y, acc1);
+                acc0 = fmaf(u1[2 * i], t1.x, acc0);
+                acc1 = fmaf(u1[2 * i + 1], t1.y, acc1);
               }
-              if (valid) s = acc0 + acc1;
-              tc_fence_before();
             }
-            scores[h * 256 + tid_e] = s;
-            __syncwarp();
-            if (lane == 0) arrive_even(bar(misc->uempty[uslot]));
+            if (valid) s = acc0 + acc1;
+            tc_fence_before();
+          }
+          scores[h * 256 + tid_e] = s;
+          const float wm = warp_max_redux(s);   // this warp's maximum of head h over its 32 tokens
+          __syncwarp();
+          if (lane == 0) {
+            arrive_even(bar(misc->uempty[uslot]));
+            misc->mx[we][h] = wm;
           }
         }
       }
@@ -661,39 +684,41 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       // this thread's token rows are no longer needed: fetch the next block's now
       if (n + 1 < count) load_trig(wn);
 
-      // ---- end of block: exact per-head maximum over the CTA's 256 tokens
+      // ---- end of block: exact per-head maximum over the CTA's 256 tokens sets the
+      // reference (raised lazily: only when the block maximum exceeds it by 2^8)
       epi_sync();
+      if (tid_e < H) {
+        const int h = tid_e;
+        float mb = misc->mx[0][h];
 #pragma unroll
-      for (int h = 0; h < kMax2dHeads; ++h) {
-        if (h < H) {
-          const float m = warp_max_redux(scores[h * 256 + tid_e]);
-          if (lane == 0) misc->mx[we][h] = m;
-        }
+        for (int ww = 1; ww < 8; ++ww) mb = fmaxf(mb, misc->mx[ww][h]);
+        const float mo = misc->m_ref[h];
+        const float base = run_start ? -INFINITY : mo;
+        const float mn = mb > base + kRescaleLog2 ? mb : base;
+        misc->m_new[h] = mn;
+        misc->alpha[h] = (run_start || mn == base) ? 1.f : exp2f(base - mn);
+        if (run_start) misc->m_rec[h] = mo;   // the finished run's reference
+        misc->m_ref[h] = mn;
       }
       epi_sync();
       // the previous block's value MMAs are complete: D_v and P may be touched
-      if (n > 0 && ok) {
-        ok = warp_wait(bar(misc->vdone), (n - 1) & 1, abort, a.status);
+      if (n > 0) {
+        if (ok) ok = warp_wait(bar(misc->vdone), (n - 1) & 1, abort, a.status);
         tc_fence_after();
       }
       // a run ended with the previous block: its record, before D_v is reused
-      if (n > 0 && run_start && ok) write_record(prev_b);
+      if (n > 0 && run_start) write_record(prev_b, ok);
       bool rescale = false;
 #pragma unroll
       for (int h = 0; h < kMax2dHeads; ++h) {
         if (h < H) {
-          float mb = misc->mx[0][h];
-#pragma unroll
-          for (int ww = 1; ww < 8; ++ww) mb = fmaxf(mb, misc->mx[ww][h]);
-          const float mo = run_start ? -INFINITY : misc->m_ref[h];
-          const float mn = mb > mo + kRescaleLog2 ? mb : mo;
-          if (!run_start && mn != mo) rescale = true;
+          const float mn = misc->m_new[h], al = misc->alpha[h];
+          if (al != 1.f) rescale = true;
           const float p = mn == -INFINITY ? 0.f : exp2f(scores[h * 256 + tid_e] - mn);
           const __nv_bfloat16 pb = __float2bfloat16_rn(p);
           *reinterpret_cast<__nv_bfloat16*>(pbuf + (tid_e >> 4) * 512 +
                                             swizzle_offset(h * 32 + (tid_e & 15) * 2, 32)) = pb;
-          const float ls = warp_sum(__bfloat162float(pb));
-          if (lane == 0) misc->lp[we][h] = ls;
+          lt[h] = (run_start ? 0.f : lt[h] * al) + __bfloat162float(pb);
         }
       }
       // the reference of some head rose: rescale this CTA's accumulators (columns = heads)
@@ -704,49 +729,24 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         tmem_wait_ld();
         uint32_t o[16];
 #pragma unroll
-        for (int h = 0; h < kMax2dHeads; ++h) {
-          float alpha = 1.f;
-          if (h < H) {
-            float mb = misc->mx[0][h];
-#pragma unroll
-            for (int ww = 1; ww < 8; ++ww) mb = fmaxf(mb, misc->mx[ww][h]);
-            const float mo = misc->m_ref[h];
-            const float mn = mb > mo + kRescaleLog2 ? mb : mo;
-            if (mn != mo) alpha = exp2f(mo - mn);
-          }
-          o[h] = __float_as_uint(v[h] * alpha);
-        }
+        for (int h = 0; h < kMax2dHeads; ++h) o[h] = __float_as_uint(h < H ? v[h] * misc->alpha[h] : v[h]);
         tmem_st_x16(dcol, o);
         tmem_wait_st();
       }
       fence_proxy_async_smem();   // P visible to the value MMA
       tc_fence_before();
-      epi_sync();
-      if (tid_e < H) {
-        const int h = tid_e;
-        float mb = misc->mx[0][h];
-#pragma unroll
-        for (int ww = 1; ww < 8; ++ww) mb = fmaxf(mb, misc->mx[ww][h]);
-        const float mo = run_start ? -INFINITY : misc->m_ref[h];
-        const float mn = mb > mo + kRescaleLog2 ? mb : mo;
-        float l = run_start ? 0.f : misc->l_run[h] * (mn != mo ? exp2f(mo - mn) : 1.f);
-#pragma unroll
-        for (int ww = 0; ww < 8; ++ww) l += misc->lp[ww][h];
-        misc->l_run[h] = l;
-        misc->m_ref[h] = mn;
-      }
       __syncwarp();
       if (lane == 0) arrive_even(bar(misc->pfull));
       prev_b = w.b;
       w = wn;
     }
     // the last run: its record once the last value MMAs are complete
-    epi_sync();
+    if (tid_e < H) misc->m_rec[tid_e] = misc->m_ref[tid_e];
     if (ok) {
       ok = warp_wait(bar(misc->vdone), (count - 1) & 1, abort, a.status);
       tc_fence_after();
     }
-    if (ok) write_record(prev_b);
+    write_record(prev_b, ok);
   }
 
   tc_fence_before();

@@ -70,7 +70,7 @@ cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
 
 // ----------------------------------------------------------------- LLA-2D decode
 
-constexpr int kDecode2dThreads = 352;   // producer, issuer/relay, 8 epilogue warps, second issuer
+constexpr int kDecode2dThreads = 320;   // producer, MMA issuer / relay, 8 epilogue warps
 constexpr int kBlock2dTokens = 512;     // tokens of a pair block: 2 tiles per CTA
 constexpr int kMax2dHeads = 16;         // heads of one shared latent (value MMA N = 32)
 constexpr int kMaxPairs = kMaxGrid / 2;
