@@ -224,7 +224,7 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
     const uint64_t rows = static_cast<uint64_t>(cache.L_max), seqs = static_cast<uint64_t>(cache.B);
     if (!make_map_3d(&maps.k, cache.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_k, rows, seqs, 64, kTile, 1))
       return LLA_ERR_CUDA;
-    if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, seqs, 64, 16, 1))
+    if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, seqs, 64, 32, 1))
       return LLA_ERR_CUDA;
     return launch_decode2d_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   }

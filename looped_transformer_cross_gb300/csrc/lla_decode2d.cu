@@ -24,7 +24,7 @@
 //  * Epilogue warps (one token per thread, fixed for the block) form the rotary
 //    score s = sum_f cos(j th_f) (U_f + b_f) + sin(j th_f) (U_64+f + b_64+f) from
 //    the token's cos/sin row held in registers (b = the mu_k term), and keep the
-//    block's scores in shared memory.  At the end of a block an exact per-head
+//    block's scores in TMEM.  At the end of a block an exact per-head
 //    maximum over the CTA's 256 tokens sets the softmax reference (raised lazily,
 //    by more than 2^8), P (bf16, heads x tokens) is written, and the value MMA
 //    D_v += C_v^T P (M = r_v rows, N = heads; Appendix J) accumulates in TMEM over
@@ -49,9 +49,11 @@ constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
 constexpr float kRescaleLog2 = 8.f;                 // lazy reference threshold (log2 units)
 constexpr int kNK = 3;        // latent tile slots (two per block)
 constexpr int kNZ = 4;        // query-operand windows in flight (a group of four heads)
-constexpr int kNV = 3;        // value chunk slots
+constexpr int kNV = 2;        // value chunk slots
 constexpr int kNU = 3;        // TMEM score buffers (128 columns each)
-constexpr int kVChunks = 16;  // 16-token value chunks of a CTA's 256 block tokens
+constexpr int kVChunks = 8;   // 32-token value chunks of a CTA's 256 block tokens
+constexpr int kVTok = 32;     // tokens per value chunk (two 16-token K steps)
+constexpr uint32_t kScoreCol = 448;   // TMEM columns of the block's scores: 16 per warp group
 constexpr uint32_t kDvCol = 384;   // TMEM column of the value accumulators (2 x 32)
 constexpr int kZRowBytes = 128;    // one 64-wide bf16 chunk row
 
@@ -112,7 +114,7 @@ __device__ __forceinline__ void walk_advance(Walker2d& w, const Decode2dArgs& a)
 // st = 2h + s), so the two epilogue warp groups (one per tile slot) take turns.
 // Value chunk c of the previous block follows head vchunk_head(c) in every role's
 // order (the first one two heads in, once that block's weights exist).
-__device__ __forceinline__ int vchunk_head(int c, int H) { return min(c + 2, H - 1); }
+__device__ __forceinline__ int vchunk_head(int c, int H) { return min(2 * c + 2, H - 1); }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<uint32_t*>(&v);
@@ -305,11 +307,11 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     const uint32_t nfull = rank == 0 ? 2 : 1;   // + the odd CTA's relay in the even CTA
     for (int s = 0; s < kNK; ++s) {
       mbar_init(bar(misc->kfull[s]), nfull);
-      mbar_init(bar(misc->kempty[s]), 1);
+      mbar_init(bar(misc->kempty[s]), 4);       // the tile's warp group, after its last stage
     }
     for (int s = 0; s < kNZ; ++s) {
       mbar_init(bar(misc->zfull[s]), nfull);
-      mbar_init(bar(misc->zempty[s]), 1);       // the issuer's commit after the window's MMAs
+      mbar_init(bar(misc->zempty[s]), 4);       // warp group 1, after the window's last stage
     }
     for (int s = 0; s < kNV; ++s) {
       mbar_init(bar(misc->vfull[s]), nfull);
@@ -331,7 +333,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     prefetch_tmap(&maps.v);
   }
   // P rows of heads >= H stay zero
-  for (int i = tid; i < kVChunks * 512 / 16; i += kDecode2dThreads)
+  for (int i = tid; i < 16 * 512 / 16; i += kDecode2dThreads)
     reinterpret_cast<uint4*>(sm + P.p)[i] = make_uint4(0, 0, 0, 0);
   // bias operand A: columns 0 and 1 of every token row are 1 (they meet bias hi / lo)
   if (tid < kTile) {
@@ -356,14 +358,14 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
   // Zero value-chunk rows past the sequence end (they may hold anything; their
   // weights are 0, and 0 * x must stay 0 in the value MMA).
   auto zero_v_tail = [&](int sv, int valid) {
-    if (valid >= 16) return;
+    if (valid >= kVTok) return;
     const int r0 = valid < 0 ? 0 : valid;
     uint8_t* vs = sm + P.v_ring + sv * P.v_stage;
     for (int bx = 0; bx < 2 * P.nvh; ++bx)
-      for (int r = r0; r < 16; ++r)
+      for (int r = r0; r < kVTok; ++r)
 #pragma unroll
         for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<uint4*>(vs + bx * 2048 + r * kZRowBytes + g * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vs + bx * 4096 + r * kZRowBytes + g * 16) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   };
 
@@ -380,10 +382,10 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         const int sv = vr.slot;
         if (!mbar_wait(bar(misc->vempty[sv]), vr.phase ^ 1u, abort, a.status)) return false;
         const uint32_t fb = bar(misc->vfull[sv]);
-        mbar_arrive_expect_tx(fb, P.nvh * 4096);
-        const int y = wb.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + 16 * c;
+        mbar_arrive_expect_tx(fb, P.nvh * 8192);
+        const int y = wb.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + kVTok * c;
         const uint32_t dst = sbase + P.v_ring + sv * P.v_stage;
-        for (int bx = 0; bx < 2 * P.nvh; ++bx) tma_load_3d(dst + bx * 2048, &maps.v, fb, 64 * bx, y, wb.b);
+        for (int bx = 0; bx < 2 * P.nvh; ++bx) tma_load_3d(dst + bx * 4096, &maps.v, fb, 64 * bx, y, wb.b);
         ++issued_v;
         vr.next(kNV);
         return true;
@@ -447,7 +449,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       auto relay_v = [&](const Walker2d& wb, int c) -> bool {
         const int sv = vr.slot;
         if (!mbar_wait(bar(misc->vfull[sv]), vr.phase, abort, a.status)) return false;
-        zero_v_tail(sv, wb.L - (wb.kb * kBlock2dTokens + 256 + 16 * c));
+        zero_v_tail(sv, wb.L - (wb.kb * kBlock2dTokens + 256 + kVTok * c));
         mbar_arrive_cluster(bar(misc->vfull[sv]), 0);
         vr.next(kNV);
         return true;
@@ -485,8 +487,8 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       const uint64_t dZ0 = umma_desc(sbase + P.z_ring, 16, 1024, kSw128);
       const uint64_t dZb0 = umma_desc(sbase + P.z_ring + P.nkc * 8192, 16, 256, kSw32);
       const uint64_t daug = umma_desc(sbase + P.aug_a, 16, 256, kSw32);
-      // MN-major value operand: 64-row r_v boxes 2 KB apart (LBO), 8 token rows 1 KB apart (SBO)
-      const uint64_t dV0 = umma_desc(sbase + P.v_ring, 2048, 1024, kSw128);
+      // MN-major value operand: 64-row r_v boxes 4 KB apart (LBO), 8 token rows 1 KB apart (SBO)
+      const uint64_t dV0 = umma_desc(sbase + P.v_ring, 4096, 1024, kSw128);
       const uint64_t dP0 = umma_desc(sbase + P.p, 16, 256, kSw32);
       const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4, zst = static_cast<uint32_t>(P.z_stage) >> 4,
                      vst = static_cast<uint32_t>(P.v_stage) >> 4;
@@ -501,14 +503,20 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
         if (c == 0 && !mbar_wait_cluster(bar(misc->pfull), pblk & 1, abort, a.status)) return false;
         const int sv = vr.slot;
         if (!mbar_wait_cluster(bar(misc->vfull[sv]), vr.phase, abort, a.status)) return false;
-        const int valid = wb.L - (wb.kb * kBlock2dTokens + 16 * c);
+        const int valid = wb.L - (wb.kb * kBlock2dTokens + kVTok * c);
         if (valid > 0) {
           zero_v_tail(sv, valid);
           tc_fence_after();
-          const uint64_t av = dV0 + sv * vst, bp = dP0 + c * (512 >> 4);
-          const uint32_t acc = (c > 0 || !run_start) ? 1u : 0u;
-          umma_bf16_pair(tmem + kDvCol, av, bp, idesc_v, acc);
-          if (P.nvh > 1) umma_bf16_pair(tmem + kDvCol + 32, av + (4096 >> 4), bp, idesc_v, acc);
+          const uint64_t av = dV0 + sv * vst, bp = dP0 + 2 * c * (512 >> 4);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {   // 16-token K steps: +2 KB in the chunk, +512 B in P
+            if (16 * k >= valid) break;   // (wholly past the end in both CTAs)
+            const uint32_t acc = (c > 0 || k > 0 || !run_start) ? 1u : 0u;
+            umma_bf16_pair(tmem + kDvCol, av + k * (2048 >> 4), bp + k * (512 >> 4), idesc_v, acc);
+            if (P.nvh > 1)
+              umma_bf16_pair(tmem + kDvCol + 32, av + (8192 >> 4) + k * (2048 >> 4), bp + k * (512 >> 4), idesc_v,
+                             acc);
+          }
         }
         umma_commit_pair(bar(misc->vempty[sv]));
         if (c == kVChunks - 1) umma_commit_pair(bar(misc->vdone));
@@ -544,10 +552,8 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
             }
             umma_bf16_pair(d, daug, bb, idesc_u, 1u);   // + bias
             umma_commit_pair(bar(misc->ufull[s][su]));
-            if (h == H - 1) umma_commit_pair(bar(misc->kempty[ts[s]]));
           }
           if (!ok) break;
-          umma_commit_pair(bar(misc->zempty[zs]));
           if (n > 0)
             while (ok && vc < kVChunks && vchunk_head(vc, a.H) == static_cast<int>(h))
               ok = issue_v(wp, prev_run_start, vc++, n - 1);
@@ -568,7 +574,6 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     const int we = warp - 2, wg = we >> 2, q = warp & 3;
     const int row = 32 * q + lane, tid_e = wg * kTile + row;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    float* scores = reinterpret_cast<float*>(sm + P.scores);
     uint8_t* pbuf = sm + P.p;
     const int H = a.H;
 
@@ -670,12 +675,18 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
             if (valid) s = acc0 + acc1;
             tc_fence_before();
           }
-          scores[h * 256 + tid_e] = s;
+          tmem_st_x1(tmem + lane_base + kScoreCol + 16 * wg + h, __float_as_uint(s));
           const float wm = warp_max_redux(s);   // this warp's maximum of head h over its 32 tokens
+          tmem_wait_st();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) {
             arrive_even(bar(misc->uempty[uslot]));
             misc->mx[we][h] = wm;
+            // the MMAs of this stage are complete: window h is free after group 1's
+            // stage, the block's tile of this group after its last stage
+            if (wg == 1) mbar_arrive(bar(misc->zempty[(static_cast<uint32_t>(H) * n + h) & (kNZ - 1)]));
+            if (h == H - 1) mbar_arrive(bar(misc->kempty[(2u * n + wg) % kNK]));
           }
         }
       }
@@ -709,12 +720,15 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
       // a run ended with the previous block: its record, before D_v is reused
       if (n > 0 && run_start) write_record(prev_b, ok);
       bool rescale = false;
+      float sc[16];   // this token's scores of the block, one per head
+      tmem_ld_x16(tmem + lane_base + kScoreCol + 16 * wg, sc);
+      tmem_wait_ld();
 #pragma unroll
       for (int h = 0; h < kMax2dHeads; ++h) {
         if (h < H) {
           const float mn = misc->m_new[h], al = misc->alpha[h];
           if (al != 1.f) rescale = true;
-          const float p = mn == -INFINITY ? 0.f : exp2f(scores[h * 256 + tid_e] - mn);
+          const float p = mn == -INFINITY ? 0.f : exp2f(sc[h] - mn);
           const __nv_bfloat16 pb = __float2bfloat16_rn(p);
           *reinterpret_cast<__nv_bfloat16*>(pbuf + (tid_e >> 4) * 512 +
                                             swizzle_offset(h * 32 + (tid_e & 15) * 2, 32)) = pb;
@@ -905,14 +919,13 @@ bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p) {
   p->nvh = (r_v + 127) / 128;
   p->k_stage = p->nkc * 16384;
   p->z_stage = p->nkc * 8192 + 2048;   // half window rows, then their 16-wide bias operand
-  p->v_stage = p->nvh * 4096;
+  p->v_stage = p->nvh * 8192;   // 32 tokens x (128 r_v) x 2 B per half
   int off = 0;
   p->k_ring = off; off += kNK * p->k_stage;
   p->z_ring = off; off += kNZ * p->z_stage;
   p->v_ring = off; off += kNV * p->v_stage;
-  p->p = off;      off += kVChunks * 512;
+  p->p = off;      off += 16 * 512;   // P: 16-token K chunks of 16 head rows
   p->aug_a = off;  off += 4096;
-  p->scores = off; off += H * 256 * 4;
   p->misc = off;   off += 4096;
   p->bytes = off + 1024;
   return p->bytes <= kSmemLimit;

@@ -80,7 +80,7 @@ struct Decode2dPlan {
   int nkc;                           // 64-wide K chunks of a latent / query-operand row (r_k <= 128)
   int nvh;                           // 128-row halves of r_v (value MMA M = 256 per pair)
   int k_stage, z_stage, v_stage;     // ring stage strides
-  int k_ring, z_ring, v_ring, p, aug_a, scores, misc;
+  int k_ring, z_ring, v_ring, p, aug_a, misc;
   int bytes;
 };
 
@@ -112,7 +112,7 @@ struct Decode2dArgs {
 
 struct Decode2dMaps {
   CUtensorMap k;                     // latent K: box (64, 128, 1) over (r_k, L_max, B), 128B swizzle
-  CUtensorMap v;                     // latent V: box (64, 16, 1) over (r_v, L_max, B), 128B swizzle
+  CUtensorMap v;                     // latent V: box (64, 32, 1) over (r_v, L_max, B), 128B swizzle
 };
 
 bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p);
