@@ -43,6 +43,12 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 TRAFFIC_PER_TOKEN_HEAD = (263.994368e6 + 4.025344e6) / (31042 * 16)
 TRAFFIC_SRC_SHA = "51f1eadfe3c1e845"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
+# The same for the LLA-2D kernel, per latent token (all heads), from the 32-sequence
+# variant of the LLA-2D layer; valid only for the source whose sha256 starts with
+# TRAFFIC2D_SRC_SHA.
+TRAFFIC2D_PER_TOKEN = (224.002816e6 + 4.921088e6) / (32 * 8192)
+TRAFFIC2D_SRC_SHA = "82da47c747901f36"
+DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
 UNIT = "latent tokens/s per layer-loop"
 
 
@@ -279,8 +285,12 @@ def run_ours(args, dist_on, rank, world, device):
         # the tensor pipe (about 700 flop per latent byte at H = 16, r = (128, 256))
         flops = step.tokens * w.H * (2 * w.d * w.r_k + 2 * w.r_v)
         achieved = flops / t_call / 1e12
+        import hashlib
+        with open(DECODE2D_SRC, "rb") as f:
+            same_src = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC2D_SRC_SHA)
+        traffic = TRAFFIC2D_PER_TOKEN * step.tokens if same_src else None
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
-                "frac": achieved / tflops, "traffic": None, "traffic_kernel": "decode2d_bf16_kernel",
+                "frac": achieved / tflops, "traffic": traffic, "traffic_kernel": "decode2d_bf16_kernel",
                 "kernel": "lla_decode_attn (decode2d_z_kernel + decode2d_bf16_kernel + "
                           "decode2d_combine_kernel)",
                 "algorithmic_flops_per_launch": flops,

@@ -133,6 +133,10 @@ lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, in
  * The new token's own K/V are attended only if the caller has encoded them
  * into slot q_pos (the paper's latent-store decoder reads every cached token
  * back through its latent); lse lets a caller merge further exact terms.
+ * LLA_2D (§3 "The LLA-2D variant"): every head h reads the sequence's one latent
+ * and reconstructs with rows h*d .. h*d+d-1 of W_up,t; mu_t is the loop-t slice
+ * [H*d] of mu [T*H*d] (index (t*H + h)*d + e).  The bf16 kernel runs on pairs of
+ * CTAs (thread-block clusters of two).
  */
 lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
                            lla_cache cache, const int32_t* seq_lens, const int32_t* q_pos,
