@@ -49,6 +49,11 @@ DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_d
 TRAFFIC2D_PER_TOKEN = (224.002816e6 + 4.921088e6) / (32 * 8192)
 TRAFFIC2D_SRC_SHA = "82da47c747901f36"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
+# Same for decode_small_kernel (the per-head kernel at small ranks), from a capture
+# of the 64-sequence variant of the rho = 21.3 layer; None until one is taken.
+TRAFFIC_SMALL_PER_TOKEN_HEAD = None
+TRAFFIC_SMALL_SRC_SHA = None
+DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 UNIT = "latent tokens/s per layer-loop"
 
 
@@ -270,13 +275,17 @@ def run_ours(args, dist_on, rank, world, device):
         lat_bytes = step.tokens * w.H * (w.r_k + w.r_v) * 2
         achieved = lat_bytes / t_call / 1e9
         import hashlib
-        with open(DECODE_SRC, "rb") as f:
-            same_src = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC_SRC_SHA)
-        traffic = TRAFFIC_PER_TOKEN_HEAD * step.tokens * w.H if same_src else None
+        small = lla.decode_kernel(step.dm) == "small-rank"
+        src_file, sha, per_th = ((DECODE_SMALL_SRC, TRAFFIC_SMALL_SRC_SHA, TRAFFIC_SMALL_PER_TOKEN_HEAD)
+                                 if small else (DECODE_SRC, TRAFFIC_SRC_SHA, TRAFFIC_PER_TOKEN_HEAD))
+        with open(src_file, "rb") as f:
+            same_src = sha is not None and hashlib.sha256(f.read()).hexdigest().startswith(sha)
+        traffic = per_th * step.tokens * w.H if same_src else None
+        kern = "decode_small_kernel" if small else "decode_bf16_kernel"
+        zk = "decode_small_z_kernel" if small else "decode_z_kernel"
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": traffic, "traffic_kernel": "decode_bf16_kernel",
-                "kernel": "lla_decode_attn (decode_z_kernel + decode_bf16_kernel + "
-                          "decode_combine_kernel)",
+                "frac": achieved / hbm, "traffic": traffic, "traffic_kernel": kern,
+                "kernel": "lla_decode_attn (%s + %s + decode_combine_kernel)" % (zk, kern),
                 "algorithmic_bytes_per_launch": lat_bytes, "launch_ms": t_call * 1e3,
                 "peak_source": src}
     else:

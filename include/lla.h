@@ -56,8 +56,10 @@ typedef enum {
     LLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented shape/variant/dtype  */
     LLA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed              */
     LLA_ERR_TIMEOUT = 4,       /* a kernel's bounded wait expired (device word)  */
-    LLA_ERR_DEVICE_ARG = 5     /* out-of-range seq_lens/q_pos/seq_idx/pos seen
+    LLA_ERR_DEVICE_ARG = 5,    /* out-of-range seq_lens/q_pos/seq_idx/pos seen
                                   by a kernel (device word)                       */
+    LLA_ERR_RANGE = 6          /* a folded query operand left the f16 range of
+                                  the small-rank decode path (device word)        */
 } lla_status;
 
 typedef enum { LLA_BF16 = 0, LLA_F32 = 1 } lla_dtype;
@@ -176,6 +178,15 @@ lla_status lla_decode_attn_noalloc(const lla_dims* dims, int loop_t, const void*
                                    const float* mu_k, const float* mu_v,
                                    const float* rope_cos, const float* rope_sin, int64_t rope_len,
                                    float* out, float* lse, void* stream);
+
+/* Name of the kernel family lla_decode_attn runs for `dims` (host-only, no
+ * launch): "fp32" (LLA_F32), "pair-2d" (LLA_2D bf16: CTA pairs), "small-rank"
+ * (LLA_PER_HEAD bf16 with r_k in {16, 32}, r_v in {32, 64} and an even H <= 16
+ * whose H query images and a 4-slot latent ring fit in shared memory:
+ * positions split over CTAs, RoPE applied by the tensor cores), "tile"
+ * (every other LLA_PER_HEAD bf16 shape: 128-token tiles over (sequence, head)
+ * split over CTAs), or NULL for invalid or unsupported dims. */
+const char* lla_decode_kernel(const lla_dims* dims);
 
 /* Workspace bytes for calls with at most B sequences of L_max slots and
  * encode batches of at most max_N tokens, on the current CUDA device.

@@ -29,6 +29,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 3-D tiled map over a dense row-major tensor [d2][d1][d0] of `esize`-byte elements.
+// Swizzle = the atom matching the box row bytes (128 / 64 / 32 B).
 bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t d0,
                  uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
   auto enc = tensor_map_encoder();
@@ -59,6 +60,13 @@ size_t zimg_stride(int r_k) {
   return (static_cast<size_t>(make_chunk_plan(r_k, kTile).bytes) + 4096 + 127) / 128 * 128;
 }
 
+// Per-head bf16 decode at small ranks runs the small-rank kernel (its shapes and
+// shared-memory plan decide); every other per-head bf16 shape the tile kernel.
+bool small_path(const lla_dims* d) {
+  DecodeSmallPlan p;
+  return d->variant == LLA_PER_HEAD && d->dtype == LLA_BF16 && make_decode_small_plan(d->H, d->r_k, d->r_v, &p);
+}
+
 WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   WsLayout w{};
   size_t off = 256;  // status word
@@ -79,6 +87,25 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
     // f16 RoPE rows of the decode epilogue (positions up to L_max rounded to a block)
     w.trig16 = off;
     if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(decode2d_trig_rows(L_max, INT64_MAX)) * 256);
+    w.total = off;
+    return w;
+  }
+  if (small_path(d)) {
+    // small-rank kernel: records per (sequence + CTA, head, warp), per-unit query
+    // images, f16 RoPE rows
+    // (a CTA index is below min(kMaxGrid, positions): the grid never exceeds either)
+    const size_t max_pos = static_cast<size_t>(B) * ((L_max + kTile - 1) / kTile);
+    w.partials = off;
+    off += al256((static_cast<size_t>(B) + std::min<size_t>(kMaxGrid, std::max<size_t>(1, max_pos))) * d->H *
+                 kRecordsPerCta * (d->r_v + kRecordHead) * 4);
+    w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
+    w.scores = off;
+    w.zimg = off;
+    // one image per (sequence, head set) of 4 heads (2 when H mod 4 = 2)
+    w.zimg_stride = decode_small_img_stride(d->H, d->r_k);
+    off += al256(static_cast<size_t>(B) * (d->H % 4 == 0 ? d->H / 4 : d->H / 2) * w.zimg_stride);
+    w.trig16 = off;
+    off += al256(static_cast<size_t>(decode_small_trig_rows(L_max, INT64_MAX)) * 256);
     w.total = off;
     return w;
   }
@@ -126,8 +153,21 @@ const char* lla_status_string(lla_status s) {
     case LLA_ERR_CUDA: return "CUDA error";
     case LLA_ERR_TIMEOUT: return "a kernel wait timed out";
     case LLA_ERR_DEVICE_ARG: return "out-of-range seq_lens/q_pos/seq_idx/pos seen on the device";
+    case LLA_ERR_RANGE: return "a folded query operand exceeded the f16 range (small-rank decode)";
   }
   return "unknown status";
+}
+
+const char* lla_decode_kernel(const lla_dims* dims) {
+  if (check_dims(dims) != LLA_OK) return nullptr;
+  if (dims->dtype == LLA_F32) return "fp32";
+  if (dims->variant == LLA_2D) {
+    Decode2dPlan p;
+    return make_decode2d_plan(dims->H, dims->r_k, dims->r_v, &p) ? "pair-2d" : nullptr;
+  }
+  if (small_path(dims)) return "small-rank";
+  DecodePlan p;
+  return make_decode_plan(dims->r_k, dims->r_v, &p) ? "tile" : nullptr;
 }
 
 size_t lla_workspace_size(const lla_dims* dims, int B, int64_t L_max, int max_N) {
@@ -261,14 +301,24 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
 
   if (dims->dtype == LLA_F32) return launch_decode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 
-  if (!make_decode_plan(dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
   const int sms = sm_count();
   if (sms <= 0) return LLA_ERR_CUDA;
+  const uint64_t rows = static_cast<uint64_t>(cache.L_max), units = static_cast<uint64_t>(cache.B) * H;
+  if (small_path(dims)) {
+    // small ranks: positions split over the CTAs, every head of a position in one CTA
+    make_decode_small_plan(H, dims->r_k, dims->r_v, &a.splan);
+    a.pos_major = 1;
+    a.trig16 = reinterpret_cast<uint32_t*>(ws + wl.trig16);
+    a.trig_rows = decode_small_trig_rows(cache.L_max, rope_len);
+    const int64_t max_pos = static_cast<int64_t>(cache.B) * ((cache.L_max + kTile - 1) / kTile);
+    a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_pos)));
+    return launch_decode_small_bf16(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  }
+  if (!make_decode_plan(dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
   const int64_t max_tiles = static_cast<int64_t>(cache.B) * H * ((cache.L_max + kTile - 1) / kTile);
   a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_tiles)));
   DecodeMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  const uint64_t rows = static_cast<uint64_t>(cache.L_max), units = static_cast<uint64_t>(cache.B) * H;
   for (int c = 0; c < a.plan.kplan.n; ++c) {
     const int w = a.plan.kplan.width[c];
     if (!make_map_3d(&maps.k[chunk_map_index(w)], cache.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_k, rows,

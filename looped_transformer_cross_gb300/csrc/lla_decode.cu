@@ -720,30 +720,40 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
     for (int bb = b0; bb < b; ++bb) pb += (clamp_len(__ldg(a.seq_lens + bb), a.L_max) + kTile - 1) / kTile;
     const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
     if (nb > 0) {
-      const long long total = static_cast<long long>(a.H) * tot;
+      // Tile-major split (per-head kernel): CTA ranges over the flat (sequence,
+      // head, tile) list, records ((b H + h) + c) 4 + warp.  Position-major split
+      // (small-rank kernel): ranges over (sequence, tile) with every head inner,
+      // records ((b + c) H + h) 4 + warp.
+      const long long total = a.pos_major ? tot : static_cast<long long>(a.H) * tot;
       const long long per = max(1LL, (total + a.grid - 1) / a.grid);
-      const long long F0 = static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
+      const long long F0 = a.pos_major ? pb : static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
       const long long F1 = F0 + nb - 1;
       const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
       const int rs = a.r_v + kRecordHead;
       const long long u = static_cast<long long>(b) * a.H + h;
+      const long long base = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * kRecordsPerCta
+                                         : (u + c0) * kRecordsPerCta;
+      const long long cstride = a.pos_major ? static_cast<long long>(kRecordsPerCta) * a.H : kRecordsPerCta;
+      // record r of the unit: CTA c0 + r / 4, warp r % 4
+      auto rec_at = [&](int r) {
+        return a.partials + (base + (r / kRecordsPerCta) * cstride + r % kRecordsPerCta) * rs;
+      };
       // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
       // the unit in that CTA wrote m = -inf, l = 0, acc = 0
-      const float* rec0 = a.partials + (u + c0) * kRecordsPerCta * rs;
       const int nrec = kRecordsPerCta * (c1 - c0 + 1);
       for (int cb = 0; cb < nrec; cb += 8) {
         // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
         // lane + 32 j of each, all in one round of loads
         const int cl = cb + (lane & 7);
-        const float mh = cl < nrec ? rec0[static_cast<long long>(cl) * rs] : -INFINITY;
-        const float lh = cl < nrec ? rec0[static_cast<long long>(cl) * rs + 1] : 0.f;
+        const float mh = cl < nrec ? rec_at(cl)[0] : -INFINITY;
+        const float lh = cl < nrec ? rec_at(cl)[1] : 0.f;
         float x[8][8];
 #pragma unroll
         for (int r = 0; r < 8; ++r)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int col = lane + 32 * j;
-            x[r][j] = cb + r < nrec && col < a.r_v ? rec0[static_cast<long long>(cb + r) * rs + kRecordHead + col] : 0.f;
+            x[r][j] = cb + r < nrec && col < a.r_v ? rec_at(cb + r)[kRecordHead + col] : 0.f;
           }
         const float Mn = fmaxf(M, warp_max(mh));
         if (Mn != -INFINITY) {
@@ -991,19 +1001,30 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cuda
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a, maps);
   if (e != cudaSuccess) return e;
+  return launch_decode_combine(a, s);
+}
+
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
   // the combine grid, a programmatic dependent of the decode grid, copies W_up,v
   // while the decode grid drains
   const size_t csmem = combine_smem_bytes(a.r_v);
   static size_t cconfigured = 0;
   if (cconfigured < csmem) {
-    e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(csmem));
+    cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(csmem));
     if (e != cudaSuccess) return e;
     cconfigured = csmem;
   }
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.H, (a.B + kCombineUnits - 1) / kCombineUnits);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = csmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_combine_kernel, a);
 }
 

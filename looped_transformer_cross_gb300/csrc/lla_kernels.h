@@ -33,6 +33,27 @@ struct DecodePlan {
   int bytes;                         // total dynamic smem incl. alignment slack
 };
 
+// Shared-memory plan of the per-head small-rank kernel (byte offsets from a
+// 1024-aligned base): the query images of the current sequence, a ring of
+// (K tile, V tile) slots, per-warp softmax state and the barriers.  Heads are
+// taken nwg at a time ("head sets", one head per epilogue group): a set's image
+// stacks its heads' Z rows and bias rows as one MMA B operand of N rows.
+struct DecodeSmallPlan {
+  int nwg;                           // epilogue warp groups in use = heads per set (4 if H % 4 == 0, else 2)
+  int nsets;                         // head sets per position (H / nwg)
+  int N;                             // set image rows = G columns (MMA N): nwg (r_k + 2) rounded up to 16
+  int img;                           // bytes of one set image (2 chunks of N rows x 128 B)
+  int NG;                            // G buffers in TMEM (one set each)
+  int k_tile, v_tile, slot;          // bytes of a K tile, a V tile, a ring slot
+  int NS;                            // ring slots (a multiple of nwg)
+  int imgs, ring, acc, ml, misc;
+  int bytes;                         // total dynamic smem incl. alignment slack
+};
+
+constexpr int kSmallThreads = 576;      // producer, MMA issuer, 4 x 4 epilogue warps
+constexpr int kSmallMaxHeads = 16;      // every head's query image stays resident
+constexpr int kSmallMaxNS = 8;
+
 struct DecodeArgs {
   int B, H, r_k, r_v, rope_style, grid;
   int shared_latent;                 // fp32 path: 1 = LLA-2D cache [B][L_max][r] read by every head
@@ -55,7 +76,11 @@ struct DecodeArgs {
   float* scores;                     // fp32 path: [B][H][L_max]
   uint8_t* zimg;                     // bf16 path: per-unit query-operand images
   int64_t zimg_stride;               // bytes per unit image (Z chunks, then 4 KB bias operand)
+  uint32_t* trig16;                  // small-rank path: f16 RoPE rows [trig_rows][64 pairs] (cos, then sin)
+  int64_t trig_rows;
+  int pos_major;                     // records indexed ((b + cta) H + h) 4 + warp (small-rank path)
   DecodePlan plan;
+  DecodeSmallPlan splan;
 };
 
 struct DecodeMaps {
@@ -64,6 +89,12 @@ struct DecodeMaps {
 };
 
 bool make_decode_plan(int r_k, int r_v, DecodePlan* p);
+bool make_decode_small_plan(int H, int r_k, int r_v, DecodeSmallPlan* p);
+size_t decode_small_img_stride(int H, int r_k);   // bytes per (sequence, head set) image
+int64_t decode_small_trig_rows(int64_t L_max, int64_t rope_len);
+cudaError_t launch_decode_small_bf16(const DecodeArgs& a, cudaStream_t s);
+// Merge a unit's split records, apply W_up,v once and normalise (both per-head paths).
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);

@@ -277,6 +277,12 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn_m
          | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with f16 A/B (format 0) and fp32 accumulation,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Issue one MMA.  No "memory" clobber: the operands are read by the async proxy,
 // ordered by the mbarrier waits before and the tcgen05.commit after (both of
 // which carry one); volatile keeps issue order among the tcgen05 statements.
@@ -419,6 +425,14 @@ __device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, float (&v)[4]) {
                : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 32 bits, 2 consecutive columns per lane.
+__device__ __forceinline__ void tmem_ld_x2(uint32_t taddr, float (&v)[2]) {
+  uint32_t r[2];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+  v[0] = __uint_as_float(r[0]);
+  v[1] = __uint_as_float(r[1]);
 }
 
 // Named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads).

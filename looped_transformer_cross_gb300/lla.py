@@ -20,7 +20,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "liblla.so")
 
-LLA_OK, LLA_ERR_INVALID_ARG, LLA_ERR_UNSUPPORTED, LLA_ERR_CUDA, LLA_ERR_TIMEOUT, LLA_ERR_DEVICE_ARG = range(6)
+(LLA_OK, LLA_ERR_INVALID_ARG, LLA_ERR_UNSUPPORTED, LLA_ERR_CUDA, LLA_ERR_TIMEOUT, LLA_ERR_DEVICE_ARG,
+ LLA_ERR_RANGE) = range(7)
 LLA_BF16, LLA_F32 = 0, 1
 LLA_PER_HEAD, LLA_2D = 0, 1
 LLA_ROPE_HALF, LLA_ROPE_INTERLEAVED = 0, 1
@@ -69,6 +70,8 @@ def lib():
             L.lla_device_status.restype = ctypes.c_int
             L.lla_status_string.argtypes = [ctypes.c_int]
             L.lla_status_string.restype = ctypes.c_char_p
+            L.lla_decode_kernel.argtypes = [pd]
+            L.lla_decode_kernel.restype = ctypes.c_char_p
             L.lla_abi_version.argtypes = []
             L.lla_abi_version.restype = ctypes.c_int
             _lib = L
@@ -77,6 +80,13 @@ def lib():
 
 def status_string(status: int) -> str:
     return lib().lla_status_string(int(status)).decode()
+
+
+def decode_kernel(dm: Dims) -> Optional[str]:
+    """Kernel family lla_decode_attn runs for these dims ("tile", "small-rank",
+    "pair-2d", "fp32"), or None if they are invalid or unsupported."""
+    r = lib().lla_decode_kernel(ctypes.byref(dm))
+    return None if r is None else r.decode()
 
 
 def dims(T, H, r_k, r_v, d_head=128, variant=LLA_PER_HEAD, dtype=LLA_BF16, rope_base=10000.0,

@@ -69,6 +69,10 @@ WORKLOADS = {
     "ouro1.4b_rho21_b768_4k": Workload("ouro1.4b_rho21_b768_4k", T=4, H=16, d=128, r_k=16,
                                        r_v=32, B=768, L_max=4096, len_lo=4096, len_hi=4096,
                                        layers=24, N_encode=768),
+    # the same layer at 64 sequences (0.4 GB of latents, above L2): the profiling case
+    "ouro1.4b_rho21_b64_4k": Workload("ouro1.4b_rho21_b64_4k", T=4, H=16, d=128, r_k=16,
+                                      r_v=32, B=64, L_max=4096, len_lo=4096, len_hi=4096,
+                                      layers=24, N_encode=64),
     # long context: 64 sequences x 16384, 48-layer stack, prefill encode of every token
     "ouro_rho4_b64_16k": Workload("ouro_rho4_b64_16k", T=4, H=16, d=128, r_k=96, r_v=160,
                                   B=64, L_max=16384, len_lo=16384, len_hi=16384, layers=48,

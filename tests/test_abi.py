@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings(L):
-    for s in range(6):
+    for s in range(7):
         assert lla.status_string(s) and lla.status_string(s) != "unknown status"
     assert lla.status_string(99) == "unknown status"
 
@@ -113,3 +113,22 @@ def test_misaligned_pointer_rejected(L):
     cache = lla.Cache(p, p, 1, 128)
     st = L.lla_decode_attn(ctypes.byref(dm), 0, p, cache, p, p, p, p, p, p, p, p, 128, p, p, p, 1 << 30, None)
     assert st == lla.LLA_ERR_INVALID_ARG
+
+
+def test_decode_kernel_dispatch(L):
+    """Which decode kernel family each shape takes (host-side decision, no launch)."""
+    d = lambda *a, **k: lla.decode_kernel(lla.dims(*a, **k))
+    assert d(4, 16, 16, 32) == "small-rank"          # Ouro-1.4B at rho = 21.3
+    assert d(4, 2, 32, 64) == "small-rank"
+    assert d(4, 6, 32, 64) == "small-rank"           # two epilogue groups (H mod 4 = 2)
+    assert d(4, 8, 32, 32) == "small-rank"
+    assert d(4, 8, 32, 64) == "tile"                 # four groups would get one slot each
+    assert d(4, 16, 16, 64) == "tile"                # ring would be 2 slots
+    assert d(4, 16, 32, 64) == "tile"                # 16 query images do not fit
+    assert d(4, 3, 16, 32) == "tile"                 # odd H
+    assert d(4, 18, 16, 32) == "tile"                # more heads than resident images
+    assert d(4, 16, 96, 160) == "tile"
+    assert d(4, 16, 48, 80) == "tile"
+    assert d(4, 16, 128, 256, variant=lla.LLA_2D) == "pair-2d"
+    assert d(4, 16, 16, 32, dtype=lla.LLA_F32) == "fp32"
+    assert d(4, 16, 16, 32, d_head=64) is None
