@@ -303,6 +303,7 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
 
   const int sms = sm_count();
   if (sms <= 0) return LLA_ERR_CUDA;
+  a.combine_units = decode_combine_units(cache.B, H, sms);
   const uint64_t rows = static_cast<uint64_t>(cache.L_max), units = static_cast<uint64_t>(cache.B) * H;
   if (small_path(dims)) {
     // small ranks: positions split over the CTAs, every head of a position in one CTA

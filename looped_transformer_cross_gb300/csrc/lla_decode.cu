@@ -29,6 +29,7 @@
 //
 #include "lla_kernels.h"
 
+#include <algorithm>
 #include <cmath>
 
 namespace lla {
@@ -645,25 +646,32 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
 // Block = (head h, kCombineUnits consecutive sequences).  Before the wait for the
 // decode grid it copies W_up,v,t[h] to shared memory (coalesced, rows padded by
 // one word so that thread e reading row e is conflict-free) and derives the tile
-// prefix of its sequences from seq_lens; after it, warp w loads unit w's records
-// in one batch and merges them, and thread e forms output e of every unit.
-constexpr int kCombineUnits = 2;
-constexpr int kCombineThreads = 128;
+// prefix of its sequences from seq_lens; after it, warp w merges the records of
+// units w and w + 8 (one batch of loads per 8 records), and thread (half, e) forms
+// output e of the half's 8 units.  Up to sixteen units per block (a.combine_units,
+// sized by the launcher so that the grid still fills the GPU) share the W staging
+// and keep the number of small, latency-bound blocks low at serving batch sizes.
+constexpr int kCombineUnits = 16;
 
-size_t combine_smem_bytes(int r_v) {
-  return (static_cast<size_t>(128) * (r_v / 2 + 1) + kCombineUnits * 256 + 2 * kCombineUnits) * 4;
+size_t combine_smem_bytes(int r_v, int units) {
+  return (static_cast<size_t>(128) * (r_v / 2 + 1) + units * 256 + 2 * units) * 4;
 }
 
+// kCombineThreads = 128: at most 4 units per block (small batches); 256: up to 16.
+// NJ: record columns per lane (r_v <= 32 NJ).
+template <int kCombineThreads, int NJ>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr int kCombineWarps = kCombineThreads / 32;
   extern __shared__ float csm[];
   __shared__ int red[kCombineThreads / 32];
-  const int h = blockIdx.x, b0 = blockIdx.y * kCombineUnits;
+  const int cu = a.combine_units;
+  const int h = blockIdx.x, b0 = blockIdx.y * cu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rw = a.r_v / 2, wpr = rw + 1;   // words per W row, per padded row
   uint32_t* Ws = reinterpret_cast<uint32_t*>(csm);
-  float* accs = csm + 128 * wpr;                   // [kCombineUnits][256]
-  float* Ms = accs + kCombineUnits * 256;
-  float* Ls = Ms + kCombineUnits;
+  float* accs = csm + 128 * wpr;                   // [cu][256]
+  float* Ms = accs + cu * 256;
+  float* Ls = Ms + cu;
 
   // ---- inputs only: W_up,v,t[h] -> shared memory; tiles of sequences < b0 and in total
   {
@@ -709,103 +717,107 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
 
   asm volatile("griddepcontrol.wait;" ::: "memory");   // records written
 
-  // ---- warp w < kCombineUnits merges the records of unit (b0 + w, h)
-  float M = -INFINITY, Lt = 0.f;
-  float acc[8];
+  // ---- warp w merges the records of units (b0 + w, h) and (b0 + w + 8, h)
+  for (int ui = warp; ui < cu; ui += kCombineWarps) {
+    float M = -INFINITY, Lt = 0.f;
+    float acc[NJ];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-  const int b = b0 + warp;
-  if (warp < kCombineUnits && b < a.B) {
-    int pb = pre;   // tiles of sequences before b
-    for (int bb = b0; bb < b; ++bb) pb += (clamp_len(__ldg(a.seq_lens + bb), a.L_max) + kTile - 1) / kTile;
-    const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
-    if (nb > 0) {
-      // Tile-major split (per-head kernel): CTA ranges over the flat (sequence,
-      // head, tile) list, records ((b H + h) + c) 4 + warp.  Position-major split
-      // (small-rank kernel): ranges over (sequence, tile) with every head inner,
-      // records ((b + c) H + h) 4 + warp.
-      const long long total = a.pos_major ? tot : static_cast<long long>(a.H) * tot;
-      const long long per = max(1LL, (total + a.grid - 1) / a.grid);
-      const long long F0 = a.pos_major ? pb : static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
-      const long long F1 = F0 + nb - 1;
-      const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
-      const int rs = a.r_v + kRecordHead;
-      const long long u = static_cast<long long>(b) * a.H + h;
-      const long long base = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * kRecordsPerCta
-                                         : (u + c0) * kRecordsPerCta;
-      const long long cstride = a.pos_major ? static_cast<long long>(kRecordsPerCta) * a.H : kRecordsPerCta;
-      // record r of the unit: CTA c0 + r / 4, warp r % 4
-      auto rec_at = [&](int r) {
-        return a.partials + (base + (r / kRecordsPerCta) * cstride + r % kRecordsPerCta) * rs;
-      };
-      // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
-      // the unit in that CTA wrote m = -inf, l = 0, acc = 0
-      const int nrec = kRecordsPerCta * (c1 - c0 + 1);
-      for (int cb = 0; cb < nrec; cb += 8) {
-        // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
-        // lane + 32 j of each, all in one round of loads
-        const int cl = cb + (lane & 7);
-        const float mh = cl < nrec ? rec_at(cl)[0] : -INFINITY;
-        const float lh = cl < nrec ? rec_at(cl)[1] : 0.f;
-        float x[8][8];
+    for (int j = 0; j < NJ; ++j) acc[j] = 0.f;
+    const int b = b0 + ui;
+    if (b < a.B) {
+      int pb = pre;   // tiles of sequences before b
+      for (int bb = b0; bb < b; ++bb) pb += (clamp_len(__ldg(a.seq_lens + bb), a.L_max) + kTile - 1) / kTile;
+      const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
+      if (nb > 0) {
+        // Tile-major split (per-head kernel): CTA ranges over the flat (sequence,
+        // head, tile) list, records ((b H + h) + c) 4 + warp.  Position-major split
+        // (small-rank kernel): ranges over (sequence, tile) with every head inner,
+        // records ((b + c) H + h) 4 + warp.
+        const long long total = a.pos_major ? tot : static_cast<long long>(a.H) * tot;
+        const long long per = max(1LL, (total + a.grid - 1) / a.grid);
+        const long long F0 = a.pos_major ? pb : static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
+        const long long F1 = F0 + nb - 1;
+        const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
+        const int rs = a.r_v + kRecordHead;
+        const long long u = static_cast<long long>(b) * a.H + h;
+        const long long base = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * kRecordsPerCta
+                                           : (u + c0) * kRecordsPerCta;
+        const long long cstride = a.pos_major ? static_cast<long long>(kRecordsPerCta) * a.H : kRecordsPerCta;
+        // record r of the unit: CTA c0 + r / 4, warp r % 4
+        auto rec_at = [&](int r) {
+          return a.partials + (base + (r / kRecordsPerCta) * cstride + r % kRecordsPerCta) * rs;
+        };
+        // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
+        // the unit in that CTA wrote m = -inf, l = 0, acc = 0
+        const int nrec = kRecordsPerCta * (c1 - c0 + 1);
+        for (int cb = 0; cb < nrec; cb += 8) {
+          // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
+          // lane + 32 j of each, all in one round of loads
+          const int cl = cb + (lane & 7);
+          const float mh = cl < nrec ? rec_at(cl)[0] : -INFINITY;
+          const float lh = cl < nrec ? rec_at(cl)[1] : 0.f;
+          float x[8][NJ];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+          for (int r = 0; r < 8; ++r)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int col = lane + 32 * j;
-            x[r][j] = cb + r < nrec && col < a.r_v ? rec_at(cb + r)[kRecordHead + col] : 0.f;
+            for (int j = 0; j < NJ; ++j) {
+              const int col = lane + 32 * j;
+              x[r][j] = cb + r < nrec && col < a.r_v ? rec_at(cb + r)[kRecordHead + col] : 0.f;
+            }
+          const float Mn = fmaxf(M, warp_max(mh));
+          if (Mn != -INFINITY) {
+            const float alpha = M == -INFINITY ? 0.f : exp2f(M - Mn);
+            Lt *= alpha;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) acc[j] *= alpha;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const float mr = __shfl_sync(0xffffffffu, mh, r), lr = __shfl_sync(0xffffffffu, lh, r);
+              const float w = mr == -INFINITY ? 0.f : exp2f(mr - Mn);
+              Lt = fmaf(lr, w, Lt);
+#pragma unroll
+              for (int j = 0; j < NJ; ++j) acc[j] = fmaf(x[r][j], w, acc[j]);
+            }
+            M = Mn;
           }
-        const float Mn = fmaxf(M, warp_max(mh));
-        if (Mn != -INFINITY) {
-          const float alpha = M == -INFINITY ? 0.f : exp2f(M - Mn);
-          Lt *= alpha;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] *= alpha;
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const float mr = __shfl_sync(0xffffffffu, mh, r), lr = __shfl_sync(0xffffffffu, lh, r);
-            const float w = mr == -INFINITY ? 0.f : exp2f(mr - Mn);
-            Lt = fmaf(lr, w, Lt);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[r][j], w, acc[j]);
-          }
-          M = Mn;
         }
       }
     }
-  }
-  if (warp < kCombineUnits) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (lane + 32 * j < a.r_v) accs[warp * 256 + lane + 32 * j] = acc[j];
-    if (lane == 0) { Ms[warp] = M; Ls[warp] = Lt; }
+    for (int j = 0; j < NJ; ++j)
+      if (lane + 32 * j < a.r_v) accs[ui * 256 + lane + 32 * j] = acc[j];
+    if (lane == 0) { Ms[ui] = M; Ls[ui] = Lt; }
   }
   __syncthreads();
 
-  // ---- out[b][h][e] = acc_b . W_e / Lt_b + mu_e, thread e reading row e of W once
-  const int e = tid;
-  float o[kCombineUnits];
+  // ---- out[b][h][e] = acc_b . W_e / Lt_b + mu_e, thread (half, e) reading row e of W once
+  constexpr int kHalf = kCombineThreads == 256 ? kCombineUnits / 2 : 4;
+  const int e = tid & (kHeadDim - 1), j0 = (tid >> 7) * kHalf;
+  float o[kHalf];
 #pragma unroll
-  for (int j = 0; j < kCombineUnits; ++j) o[j] = 0.f;
+  for (int j = 0; j < kHalf; ++j) o[j] = 0.f;
   const uint32_t* wr = Ws + e * wpr;
 #pragma unroll 4
   for (int k = 0; k < rw; ++k) {
     const uint32_t w2 = wr[k];
     const float wlo = __uint_as_float(w2 << 16), whi = __uint_as_float(w2 & 0xFFFF0000u);
 #pragma unroll
-    for (int j = 0; j < kCombineUnits; ++j) {
-      const float2 av = *reinterpret_cast<const float2*>(accs + j * 256 + 2 * k);
-      o[j] = fmaf(av.x, wlo, fmaf(av.y, whi, o[j]));
+    for (int j = 0; j < kHalf; ++j) {
+      if (j0 + j < cu) {   // accs holds cu units
+        const float2 av = *reinterpret_cast<const float2*>(accs + (j0 + j) * 256 + 2 * k);
+        o[j] = fmaf(av.x, wlo, fmaf(av.y, whi, o[j]));
+      }
     }
   }
   const float mu = __ldg(a.mu_v + static_cast<int64_t>(h) * a.mu_hstride + e);
 #pragma unroll
-  for (int j = 0; j < kCombineUnits; ++j) {
+  for (int jj = 0; jj < kHalf; ++jj) {
+    const int j = j0 + jj;
     const int bb = b0 + j;
-    if (bb >= a.B) continue;
+    if (j >= cu || bb >= a.B) continue;
     const int64_t uu = static_cast<int64_t>(bb) * a.H + h;
     const bool empty = Ms[j] == -INFINITY;
-    a.out[uu * kHeadDim + e] = empty ? 0.f : o[j] / Ls[j] + mu;
+    a.out[uu * kHeadDim + e] = empty ? 0.f : o[jj] / Ls[j] + mu;
     if (e == 0) a.lse[uu] = empty ? -INFINITY : (Ms[j] + log2f(Ls[j])) * kLn2;
   }
 }
@@ -1004,20 +1016,31 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cuda
   return launch_decode_combine(a, s);
 }
 
+int decode_combine_units(int B, int H, int sms) {
+  // two units per block (128 threads) unless the batch gives more than about two
+  // blocks per SM that way; then up to 16 per block (256 threads)
+  const long long u = static_cast<long long>(B) * H / (2LL * (sms > 0 ? sms : 1));
+  return u <= 2 ? 2 : static_cast<int>(std::min<long long>(kCombineUnits, u));
+}
+
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
   // the combine grid, a programmatic dependent of the decode grid, copies W_up,v
   // while the decode grid drains
-  const size_t csmem = combine_smem_bytes(a.r_v);
-  static size_t cconfigured = 0;
-  if (cconfigured < csmem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool wide = a.combine_units > 4, narrow_v = a.r_v <= 64;
+  const int which = (wide ? 2 : 0) + (narrow_v ? 1 : 0);
+  void (*const kern[4])(DecodeArgs) = {decode_combine_kernel<128, 8>, decode_combine_kernel<128, 2>,
+                                       decode_combine_kernel<256, 8>, decode_combine_kernel<256, 2>};
+  const size_t csmem = combine_smem_bytes(a.r_v, a.combine_units);
+  static size_t cconfigured[4] = {0, 0, 0, 0};
+  if (cconfigured[which] < csmem) {
+    cudaError_t e = cudaFuncSetAttribute(kern[which], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(csmem));
     if (e != cudaSuccess) return e;
-    cconfigured = csmem;
+    cconfigured[which] = csmem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.H, (a.B + kCombineUnits - 1) / kCombineUnits);
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.gridDim = dim3(a.H, (a.B + a.combine_units - 1) / a.combine_units);
+  cfg.blockDim = dim3(wide ? 256 : 128);
   cfg.dynamicSmemBytes = csmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1025,7 +1048,7 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, a);
+  return cudaLaunchKernelEx(&cfg, kern[which], a);
 }
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s) {

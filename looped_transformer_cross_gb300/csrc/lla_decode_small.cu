@@ -114,31 +114,44 @@ __device__ __forceinline__ uint32_t half2_bits(__half2 v) { return *reinterpret_
 //             k = 64 + f -> sc (q'_i1 mu_i0 - q'_i0 mu_i1)
 // so that sum_n c_j,n (R_j . Z row n) + R_j . (bias rows) equals
 // log2(e) RoPE(q, q_pos).RoPE(k_j, j) / sqrt(d) for the key of Eq. (3).  A value
-// beyond the f16 range records LLA_ERR_RANGE.  Blocks = (sequence, head); the
-// blocks after them write the f16 RoPE rows: row p = {cos(p th_2i), cos(p th_2i+1)}
-// for i < 32, then the sines, two per 32-bit word (lower frequency in the low half).
+// beyond the f16 range records LLA_ERR_RANGE.  Block = (head h, kZSeqs sequences):
+// W_up,k,t[h] is staged once and serves every sequence of the block, and the
+// rotated queries of all of them are formed in one round of loads.  The first
+// blocks write the f16 RoPE rows: row p = {cos(p th_2i), cos(p th_2i+1)} for
+// i < 32, then the sines, two per 32-bit word (lower frequency in the low half).
 constexpr int kSZThreads = 256;
+constexpr int kZSeqs = 8;
 __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid_constant__ DecodeArgs a) {
   // the decode grid may start its set-up now; it waits for this grid before it
   // copies an image or reads a RoPE row
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float qs[2][64];          // sc q'_i0, sc q'_i1 per frequency
-  __shared__ float bs[128];            // bias per RoPE coordinate
+  __shared__ __align__(16) float qs[kZSeqs][2][64];  // sc q'_i0, sc q'_i1 per sequence and frequency
+  __shared__ __align__(16) float bs[kZSeqs][128];    // bias per sequence and RoPE coordinate
   __shared__ float Ws[kHeadDim * 33];  // W_up,k,t[h] as fp32 [128][r_k] (row stride r_k + 1)
-  const int u = blockIdx.x, tid = threadIdx.x;
-  if (u >= a.B * a.H) {
-    const int64_t r0 = static_cast<int64_t>(u - a.B * a.H) * kTrigRowsPerBlock;
-    for (int i = tid; i < kTrigRowsPerBlock * 64; i += kSZThreads) {
+  __shared__ bool live[kZSeqs];        // sequence exists and is not empty
+  const int ntb = static_cast<int>((a.trig_rows + kTrigRowsPerBlock - 1) / kTrigRowsPerBlock);
+  const int tid = threadIdx.x;
+  if (static_cast<int>(blockIdx.x) < ntb) {
+    // RoPE rows first (the decode grid needs all of them): every load in flight at once
+    constexpr int kPer = kTrigRowsPerBlock * 64 / kSZThreads;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTrigRowsPerBlock;
+    float2 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kSZThreads, c = i % 64;
+      const int64_t r = min(r0 + i / 64, a.trig_rows - 1);
+      v[j] = *reinterpret_cast<const float2*>((c < 32 ? a.rope_cos : a.rope_sin) + r * 64 + 2 * (c & 31));
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kSZThreads;
       const int64_t r = r0 + i / 64;
-      const int c = i % 64;
-      if (r >= a.trig_rows) break;
-      const float* src = (c < 32 ? a.rope_cos : a.rope_sin) + r * 64 + 2 * (c & 31);
-      a.trig16[r * 64 + c] = half2_bits(__floats2half2_rn(src[0], src[1]));
+      if (r < a.trig_rows) a.trig16[r * 64 + i % 64] = half2_bits(__floats2half2_rn(v[j].x, v[j].y));
     }
     return;
   }
-  const int b = u / a.H, h = u - (u / a.H) * a.H;
-  if (clamp_len(__ldg(a.seq_lens + b), a.L_max) == 0) return;
+  const int u = static_cast<int>(blockIdx.x) - ntb;
+  const int h = u % a.H, b0 = (u / a.H) * kZSeqs;
   const int rk = a.r_k, ws = rk + 1;
   const int nwg = a.splan.nwg, N = a.splan.N, hl = h % nwg;
   const __nv_bfloat16* W =
@@ -150,8 +163,10 @@ __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid
 #pragma unroll
     for (int e = 0; e < 8; ++e) Ws[row * ws + col + e] = w8[e];
   }
-  if (tid < 64) {
-    const int f = tid;
+  const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
+  for (int i = tid; i < kZSeqs * 64; i += kSZThreads) {
+    const int sb = i / 64, f = i % 64, b = b0 + sb;
+    if (b >= a.B) break;
     int qp = __ldg(a.q_pos + b);
     if (qp < 0 || qp >= a.rope_len) {
       if (f == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
@@ -161,7 +176,6 @@ __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid
     const int i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
     const __nv_bfloat16* qv =
         static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(b) * a.H + h) * kHeadDim;
-    const float* mu = a.mu_k + static_cast<int64_t>(h) * a.mu_hstride;
     const float cq = __ldg(a.rope_cos + static_cast<int64_t>(qp) * 64 + f);
     const float sq = __ldg(a.rope_sin + static_cast<int64_t>(qp) * 64 + f);
     const float x0 = __bfloat162float(qv[i0]), x1 = __bfloat162float(qv[i1]);
@@ -169,42 +183,66 @@ __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid
     const float scale = kLog2e * kInvSqrtD;
     const float q0 = (x0 * cq - x1 * sq) * scale;
     const float q1 = (x0 * sq + x1 * cq) * scale;
-    qs[0][f] = q0;
-    qs[1][f] = q1;
-    bs[f] = q0 * m0 + q1 * m1;
-    bs[64 + f] = q1 * m0 - q0 * m1;
+    qs[sb][0][f] = q0;
+    qs[sb][1][f] = q1;
+    bs[sb][f] = q0 * m0 + q1 * m1;
+    bs[sb][64 + f] = q1 * m0 - q0 * m1;
   }
+  if (tid < kZSeqs) live[tid] = b0 + tid < a.B && clamp_len(__ldg(a.seq_lens + b0 + tid), a.L_max) > 0;
   __syncthreads();
-  uint8_t* img = a.zimg + (static_cast<int64_t>(b) * a.splan.nsets + h / nwg) * a.zimg_stride;
-  // this head's rows: Z (r_k), bias hi, bias lo; head 0 of the set also zeroes the padding
-  const int npad = hl == 0 ? N - nwg * (rk + 2) : 0;
-  bool bad = false;
-  for (int it = tid; it < (rk + 2 + npad) * 16; it += kSZThreads) {
-    const int r = it >> 4, g = it & 15;   // local row r, 16-byte granule g (coordinates 8g..8g+7)
-    float v[8];
+  // Item = (row r of this head, 16-byte granule g = coordinates 8g..8g+7): its W
+  // values and destination are set up once and serve every sequence of the block.
+  // Rows: Z (r_k), bias hi, bias lo; head 0 of the set also zeroes the padding.
+  const int rows = rk + 2 + (hl == 0 ? N - nwg * (rk + 2) : 0);
+  float amax = 0.f;   // largest |value| written (f16 range check)
+  for (int it = tid; it < rows * 16; it += kSZThreads) {
+    const int r = it >> 4, g = it & 15, f0 = 8 * (g & 7);
+    const bool sin_half = g >= 8;
+    float w0[8], w1[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int k = 8 * g + e, f = k & 63;
+      const int f = f0 + e;
       const int i0 = a.rope_style == 0 ? f : 2 * f;
       const int i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
-      float x = 0.f;
-      if (r < rk) {
-        const float w0 = Ws[i0 * ws + r], w1 = Ws[i1 * ws + r];
-        x = k < 64 ? qs[0][f] * w0 + qs[1][f] * w1 : qs[1][f] * w0 - qs[0][f] * w1;
-      } else if (r == rk) {
-        x = __half2float(__float2half_rn(bs[k]));
-      } else if (r == rk + 1) {
-        x = bs[k] - __half2float(__float2half_rn(bs[k]));
-      }
-      bad |= !(fabsf(x) <= kF16Max);
-      v[e] = x;
+      w0[e] = r < rk ? Ws[i0 * ws + r] : 0.f;
+      w1[e] = r < rk ? Ws[i1 * ws + r] : 0.f;
     }
     const int n = r < rk ? hl * rk + r : r < rk + 2 ? nwg * rk + 2 * hl + (r - rk) : nwg * (rk + 2) + (r - rk - 2);
-    const uint4 w = make_uint4(half2_bits(__floats2half2_rn(v[0], v[1])), half2_bits(__floats2half2_rn(v[2], v[3])),
-                               half2_bits(__floats2half2_rn(v[4], v[5])), half2_bits(__floats2half2_rn(v[6], v[7])));
-    *reinterpret_cast<uint4*>(img + (g >> 3) * (N * 128) + swizzle_offset(n * 128 + (g & 7) * 16, 128)) = w;
+    const uint32_t off = (g >> 3) * (N * 128) + swizzle_offset(n * 128 + (g & 7) * 16, 128);
+    for (int sb = 0; sb < kZSeqs; ++sb) {
+      if (!live[sb]) continue;   // past the batch or an empty sequence: never read
+      float v[8];
+      if (r < rk) {
+        const float4* q0p = reinterpret_cast<const float4*>(&qs[sb][0][f0]);
+        const float4* q1p = reinterpret_cast<const float4*>(&qs[sb][1][f0]);
+        const float4 a0 = q0p[0], a1 = q0p[1], c0 = q1p[0], c1 = q1p[1];
+        const float q0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float q1[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          v[e] = sin_half ? q1[e] * w0[e] - q0[e] * w1[e] : q0[e] * w0[e] + q1[e] * w1[e];
+      } else if (r < rk + 2) {
+        const float4* bp = reinterpret_cast<const float4*>(&bs[sb][8 * g]);
+        const float4 u0 = bp[0], u1 = bp[1];
+        const float bb[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float hi = __half2float(__float2half_rn(bb[e]));
+          v[e] = r == rk ? hi : bb[e] - hi;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+      const uint4 w = make_uint4(half2_bits(__floats2half2_rn(v[0], v[1])), half2_bits(__floats2half2_rn(v[2], v[3])),
+                                 half2_bits(__floats2half2_rn(v[4], v[5])), half2_bits(__floats2half2_rn(v[6], v[7])));
+      *reinterpret_cast<uint4*>(a.zimg + (static_cast<int64_t>(b0 + sb) * a.splan.nsets + h / nwg) * a.zimg_stride +
+                                off) = w;
+    }
   }
-  if (bad) record_status(a.status, LLA_ERR_RANGE);
+  if (amax > kF16Max) record_status(a.status, LLA_ERR_RANGE);   // (NaN queries stay NaN, as on every path)
 }
 
 template <int RK, int RV>
@@ -606,7 +644,8 @@ cudaError_t launch_small_instance(const DecodeArgs& a, cudaStream_t s) {
     configured = a.splan.bytes;
   }
   const int trig_blocks = static_cast<int>((a.trig_rows + kTrigRowsPerBlock - 1) / kTrigRowsPerBlock);
-  decode_small_z_kernel<<<a.B * a.H + trig_blocks, kSZThreads, 0, s>>>(a);
+  const int z_blocks = a.H * ((a.B + kZSeqs - 1) / kZSeqs);
+  decode_small_z_kernel<<<z_blocks + trig_blocks, kSZThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the decode grid's set-up overlaps the image

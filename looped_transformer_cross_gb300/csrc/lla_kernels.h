@@ -79,6 +79,7 @@ struct DecodeArgs {
   uint32_t* trig16;                  // small-rank path: f16 RoPE rows [trig_rows][64 pairs] (cos, then sin)
   int64_t trig_rows;
   int pos_major;                     // records indexed ((b + cta) H + h) 4 + warp (small-rank path)
+  int combine_units;                 // sequences per combine block (1..16)
   DecodePlan plan;
   DecodeSmallPlan splan;
 };
@@ -95,6 +96,8 @@ int64_t decode_small_trig_rows(int64_t L_max, int64_t rope_len);
 cudaError_t launch_decode_small_bf16(const DecodeArgs& a, cudaStream_t s);
 // Merge a unit's split records, apply W_up,v once and normalise (both per-head paths).
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
+// Sequences per combine block: as many as keep about two blocks per SM, at most 16.
+int decode_combine_units(int B, int H, int sms);
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
