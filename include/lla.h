@@ -148,6 +148,39 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
                            float* out, float* lse,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * lla_window_attn — exact attention over each sequence's window of recent
+ * tokens, merged into a latent-store result ("Hybrid Latent Attention for Looped
+ * Language Models", §3.4 "Exact sliding window", Eq. (4), and Appendix I
+ * "Serving Implementation").  Eq. (4) takes one softmax over the latent tokens
+ * before the window and the window's exact keys; with `out`/`lse` holding
+ * lla_decode_attn's result for the latent tokens (seq_lens = their count) at
+ * loop t, this call computes the window's own softmax and merges the two by
+ * log-sum-exp, which equals that single softmax.  Any lla_dims variant; the
+ * window is per head in both.
+ *   q         device  [B][H][d]        the query lla_decode_attn took
+ *   k_win     device  [B][H][W][d]     exact keys of loop t, BEFORE RoPE
+ *   v_win     device  [B][H][W][d]     exact values of loop t
+ *   win_len   device  int32 [B]        window tokens in use, 0..W
+ *   win_pos   device  int32 [B]        position of window token 0; token w is
+ *                                      rotated at win_pos[b] + w
+ *   q_pos     device  int32 [B]        as for lla_decode_attn
+ *   rope_cos/_sin, rope_len            as for lla_decode_attn; every window
+ *                                      position must be < rope_len
+ *   out, lse  device  fp32 [B][H][d], [B][H]   in: latent part; out: merged
+ *                                      (rows with win_len 0 are left as they are)
+ *   workspace device  >= 256 bytes: the status word (lla_device_status)
+ * q, k_win and v_win use the storage dtype (bf16 or fp32).  A win_len outside
+ * [0, W] or a window reaching past rope_len skips that sequence's window, a
+ * q_pos outside [0, rope_len) is clamped; both record LLA_ERR_DEVICE_ARG.
+ * W == 0 or B == 0 launches nothing.
+ */
+lla_status lla_window_attn(const lla_dims* dims, int B, int W, const void* q,
+                           const void* k_win, const void* v_win, const int32_t* win_len,
+                           const int32_t* win_pos, const int32_t* q_pos,
+                           const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                           float* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
 /* Size of the fixed scratch array behind lla_decode_attn_noalloc (64 MiB). */
 #define LLA_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -332,6 +332,41 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
+lla_status lla_window_attn(const lla_dims* dims, int B, int W, const void* q, const void* k_win,
+                           const void* v_win, const int32_t* win_len, const int32_t* win_pos,
+                           const int32_t* q_pos, const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                           float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  lla_status st = check_dims(dims);
+  if (st != LLA_OK) return st;
+  if (B < 0 || W < 0 || rope_len < 1) return LLA_ERR_INVALID_ARG;
+  if (B == 0 || W == 0) return LLA_OK;
+  if (static_cast<int64_t>(B) * dims->H > (int64_t(1) << 30)) return LLA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k_win, v_win, win_len, win_pos, q_pos, rope_cos, rope_sin, out, lse, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LLA_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return LLA_ERR_INVALID_ARG;
+  WindowArgs a{};
+  a.B = B;
+  a.H = dims->H;
+  a.W = W;
+  a.rope_style = dims->rope_style;
+  a.rope_len = rope_len;
+  a.q = q;
+  a.k_win = k_win;
+  a.v_win = v_win;
+  a.win_len = win_len;
+  a.win_pos = win_pos;
+  a.q_pos = q_pos;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  a.out = out;
+  a.lse = lse;
+  a.status = static_cast<uint32_t*>(workspace);
+  return launch_window_attn(a, dims->dtype == LLA_BF16, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LLA_OK
+             : LLA_ERR_CUDA;
+}
+
 lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, int N, const int32_t* seq_idx,
                       const int32_t* pos, const void* w_down_k, const void* w_down_v, const float* mu_k,
                       const float* mu_v, lla_cache cache, void* workspace, size_t ws_bytes, void* stream) {

@@ -102,6 +102,26 @@ int decode_combine_units(int B, int H, int sms);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
 
+// ----------------------------------------------------------------- exact window
+
+struct WindowArgs {
+  int B, H, W, rope_style;
+  int64_t rope_len;
+  const void* q;                     // [B][H][128] (storage dtype)
+  const void* k_win;                 // [B][H][W][128] exact keys of the loop, before RoPE
+  const void* v_win;                 // [B][H][W][128]
+  const int32_t* win_len;            // [B] valid window tokens
+  const int32_t* win_pos;            // [B] position of window token 0
+  const int32_t* q_pos;              // [B]
+  const float* rope_cos;             // [rope_len][64]
+  const float* rope_sin;
+  float* out;                        // [B][H][128] in: latent part, out: merged
+  float* lse;                        // [B][H]      likewise (natural log)
+  uint32_t* status;
+};
+
+cudaError_t launch_window_attn(const WindowArgs& a, bool bf16, cudaStream_t s);
+
 // ----------------------------------------------------------------- LLA-2D decode
 
 constexpr int kDecode2dThreads = 320;   // producer, MMA issuer / relay, 8 epilogue warps

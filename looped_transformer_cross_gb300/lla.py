@@ -70,6 +70,9 @@ def lib():
             L.lla_device_status.restype = ctypes.c_int
             L.lla_status_string.argtypes = [ctypes.c_int]
             L.lla_status_string.restype = ctypes.c_char_p
+            L.lla_window_attn.argtypes = [pd, ctypes.c_int, ctypes.c_int, vp, vp, vp, i32p, i32p, i32p,
+                                          fp, fp, ctypes.c_int64, fp, fp, vp, ctypes.c_size_t, vp]
+            L.lla_window_attn.restype = ctypes.c_int
             L.lla_decode_kernel.argtypes = [pd]
             L.lla_decode_kernel.restype = ctypes.c_char_p
             L.lla_abi_version.argtypes = []
@@ -158,6 +161,19 @@ def decode_attn(dm: Dims, loop_t: int, q, cache_k, cache_v, seq_lens, q_pos, w_u
                                _ptr(lse), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "lla_decode_attn")
+
+
+def window_attn(dm: Dims, q, k_win, v_win, win_len, win_pos, q_pos, rope_cos, rope_sin, out, lse,
+                workspace, stream=None):
+    """lla_window_attn: exact attention over each sequence's window of recent tokens
+    (k_win / v_win [B][H][W][d], keys before RoPE, token w at position win_pos[b] + w),
+    merged in place into ``out`` / ``lse`` holding lla_decode_attn's latent result."""
+    B, W = int(k_win.shape[0]), int(k_win.shape[2])
+    st = lib().lla_window_attn(ctypes.byref(dm), B, W, _ptr(q), _ptr(k_win), _ptr(v_win), _ptr(win_len),
+                               _ptr(win_pos), _ptr(q_pos), _ptr(rope_cos), _ptr(rope_sin),
+                               int(rope_cos.shape[0]), _ptr(out), _ptr(lse), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "lla_window_attn")
 
 
 def device_status(workspace, stream=None, clear=True) -> int:

@@ -148,6 +148,27 @@ def make_decode_inputs(w: Workload, seed: int, device="cpu", with_encode: bool =
     return out
 
 
+def make_window_inputs(w: Workload, W: int, seed: int, seq_lens: torch.Tensor, device="cpu",
+                       win_len: Optional[torch.Tensor] = None) -> dict:
+    """Exact window of the W newest tokens per sequence (the hybrid layout of the HLA
+    page's §3.4): k_win / v_win [B][H][W][d] ~ N(0, 1) in the storage dtype (keys
+    before RoPE), win_len [B] (default W), win_pos = seq_lens (the window follows the
+    latent tokens) and q_pos = the newest window token's position."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(seed))
+    sd = storage_dtype(w)
+    B, H, d = w.B, w.H, w.d
+    out = {"k_win": _normal(gen, (B, H, W, d), 1.0, sd, dev), "v_win": _normal(gen, (B, H, W, d), 1.0, sd, dev)}
+    if win_len is None:
+        win_len = torch.full((B,), W, dtype=torch.int32)
+    out["win_len"] = win_len.to(device=dev, dtype=torch.int32)
+    out["win_pos"] = seq_lens.to(device=dev, dtype=torch.int32).clone()
+    last = out["win_pos"] + out["win_len"] - 1
+    out["q_pos"] = torch.where(out["win_len"] > 0, last, (out["win_pos"] - 1).clamp_min(0)).to(torch.int32)
+    return out
+
+
 def widen(t: torch.Tensor):
     """Exact widening of a stored tensor to a float64 numpy array (for the oracle)."""
     return t.detach().to("cpu").to(torch.float64).numpy()

@@ -84,6 +84,9 @@ def lib():
             L.oracle_sdpa.argtypes = [pd, ctypes.c_int, ctypes.c_long, dp, dp, dp, ip, ip,
                                       ctypes.c_long, dp, dp]
             L.oracle_sdpa.restype = ctypes.c_int
+            L.oracle_hybrid.argtypes = [pd, ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_long, dp, dp, dp,
+                                        ip, ip, dp, dp, dp, dp, dp, dp, ip, ip, dp, dp]
+            L.oracle_hybrid.restype = ctypes.c_int
             L.oracle_num_threads.argtypes = []
             L.oracle_num_threads.restype = ctypes.c_int
             _lib = L
@@ -168,6 +171,36 @@ def decode(dm: OracleDims, t, q, cache_k, cache_v, seq_lens, q_pos, w_up_k, w_up
     if rc != 0:
         raise ValueError("oracle_decode failed (%d)" % rc)
     return out, lse, scores
+
+
+def hybrid(dm: OracleDims, t, q, cache_k, cache_v, n_lat, q_pos, w_up_k, w_up_v, mu_k, mu_v,
+           k_win, v_win, n_win, win_pos):
+    """Eq. (4) of the HLA page at loop ``t``: one softmax over the latent tokens
+    j < n_lat[b] and the exact window tokens w < n_win[b] (positions win_pos[b] + w).
+    k_win / v_win are [B][H][W][d], keys before RoPE.  Returns (out, lse)."""
+    q, qp = _d(q)
+    ck, ckp = _d(cache_k)
+    cv, cvp = _d(cache_v)
+    nl, nlp = _i(n_lat)
+    qpos, qposp = _i(q_pos)
+    wk, wkp = _d(w_up_k)
+    wv, wvp = _d(w_up_v)
+    mk, mkp = _d(mu_k)
+    mv, mvp = _d(mu_v)
+    kw, kwp = _d(k_win)
+    vw, vwp = _d(v_win)
+    nw, nwp = _i(n_win)
+    wpos, wposp = _i(win_pos)
+    B, L_max, W = q.shape[0], ck.shape[2], kw.shape[2]
+    out = np.zeros((B, dm.H, dm.d))
+    lse = np.zeros((B, dm.H))
+    rc = lib().oracle_hybrid(ctypes.byref(dm), int(t), B, L_max, W, qp, ckp, cvp, nlp, qposp,
+                             wkp, wvp, mkp, mvp, kwp, vwp, nwp, wposp,
+                             out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                             lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    if rc != 0:
+        raise ValueError("oracle_hybrid failed (%d)" % rc)
+    return out, lse
 
 
 def sdpa(dm: OracleDims, q, k, v, seq_lens, q_pos, pos_offset=0):

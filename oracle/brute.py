@@ -89,3 +89,33 @@ def decode_2d(t, q, cache_k, cache_v, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_
             out[b, h] = (w / w.sum()) @ V
             lse[b, h] = s.max() + np.log(w.sum())
     return out, lse
+
+
+def hybrid_per_head(t, q, cache_k, cache_v, n_lat, q_pos, w_up_k, w_up_v, mu_k, mu_v,
+                    k_win, v_win, n_win, win_pos, base=10000.0, style=0):
+    """Hybrid attention with an exact window ("Hybrid Latent Attention for Looped
+    Language Models", §3.4 Eq. (4)): the latent tokens' K/V stacks (Eq. (3) of the
+    LLA page) and the window's exact K/V are concatenated, every key is rotated by
+    its own rotation matrix, and one softmax runs over the whole row.  k_win /
+    v_win [B][H][W][d] (keys before RoPE), window token w at position win_pos[b] + w."""
+    B, H, d = q.shape
+    out = np.zeros((B, H, d))
+    lse = np.zeros((B, H))
+    for b in range(B):
+        nl, nw = int(n_lat[b]), int(n_win[b])
+        for h in range(H):
+            if nl + nw == 0:
+                lse[b, h] = -np.inf
+                continue
+            K = reconstruct(cache_k[b, h, :nl], w_up_k[t, h], mu_k[h, t * d:(t + 1) * d])
+            V = reconstruct(cache_v[b, h, :nl], w_up_v[t, h], mu_v[h, t * d:(t + 1) * d])
+            K = np.concatenate([K, k_win[b, h, :nw]], axis=0)
+            V = np.concatenate([V, v_win[b, h, :nw]], axis=0)
+            pos = list(range(nl)) + [int(win_pos[b]) + w for w in range(nw)]
+            qr = rotation_matrix(d, q_pos[b], base, style) @ q[b, h]
+            Kr = np.stack([rotation_matrix(d, pos[j], base, style) @ K[j] for j in range(nl + nw)])
+            s = Kr @ qr / np.sqrt(d)
+            w = np.exp(s - s.max())
+            out[b, h] = (w / w.sum()) @ V
+            lse[b, h] = s.max() + np.log(w.sum())
+    return out, lse

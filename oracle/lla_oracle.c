@@ -256,6 +256,77 @@ int oracle_decode(const oracle_dims* dm, int t, int B, long L_max,
     return bad ? 2 : 0;
 }
 
+/* "Hybrid Latent Attention for Looped Language Models" §3.4 Eq. (4), written out:
+ * the latent tokens' scores and the window tokens' scores form one vector, one
+ * softmax normalises it, and each weight multiplies its own token's value. */
+int oracle_hybrid(const oracle_dims* dm, int t, int B, long L_max, long W,
+                  const double* q, const double* cache_k, const double* cache_v,
+                  const int* n_lat, const int* q_pos,
+                  const double* w_up_k, const double* w_up_v,
+                  const double* mu_k, const double* mu_v,
+                  const double* k_win, const double* v_win, const int* n_win,
+                  const int* win_pos, double* out, double* lse) {
+    if (!dims_ok(dm) || dm->variant != 0 || t < 0 || t >= dm->T || B < 0 || L_max < 0 || W < 0)
+        return 1;
+    const int H = dm->H, d = dm->d, rk = dm->r_k, rv = dm->r_v;
+    for (int b = 0; b < B; ++b)
+        if (n_lat[b] < 0 || n_lat[b] > L_max || n_win[b] < 0 || n_win[b] > W) return 1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(|:bad)
+    for (long bh = 0; bh < (long)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        const long nl = n_lat[b], nw = n_win[b], n = nl + nw;
+        double* o = out + bh * d;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        if (n == 0) {
+            lse[bh] = -INFINITY;
+            continue;
+        }
+        const double* Wk = w_up_k + (((long)t * H + h) * d) * rk;
+        const double* Wv = w_up_v + (((long)t * H + h) * d) * rv;
+        const double* muk_t = mu_k + (long)h * dm->T * d + (long)t * d;
+        const double* muv_t = mu_v + (long)h * dm->T * d + (long)t * d;
+        double* qr = (double*)malloc(sizeof(double) * d);
+        double* kh = (double*)malloc(sizeof(double) * d);
+        double* kr = (double*)malloc(sizeof(double) * d);
+        double* vh = (double*)malloc(sizeof(double) * d);
+        double* s = (double*)malloc(sizeof(double) * n);
+        double* p = (double*)malloc(sizeof(double) * n);
+        rope_rotate(dm, q + bh * d, (double)q_pos[b], qr);
+        const double scale = 1.0 / sqrt((double)d);
+        for (long j = 0; j < n; ++j) {
+            if (j < nl) {   /* latent token j */
+                reconstruct(cache_k + (bh * L_max + j) * rk, Wk, muk_t, d, rk, kh);
+                rope_rotate(dm, kh, (double)j, kr);
+            } else {        /* window token w = j - nl */
+                const long w = j - nl;
+                rope_rotate(dm, k_win + (bh * W + w) * d, (double)(win_pos[b] + w), kr);
+            }
+            double acc = 0.0;
+            for (int e = 0; e < d; ++e) acc += qr[e] * kr[e];
+            s[j] = acc * scale;
+        }
+        double m, z;
+        softmax(s, n, p, &m, &z);
+        double psum = 0.0;
+        for (long j = 0; j < n; ++j) psum += p[j];
+        if (fabs(psum - 1.0) > 1e-12) bad |= 1;
+        for (long j = 0; j < n; ++j) {
+            const double* v;
+            if (j < nl) {
+                reconstruct(cache_v + (bh * L_max + j) * rv, Wv, muv_t, d, rv, vh);
+                v = vh;
+            } else {
+                v = v_win + (bh * W + (j - nl)) * d;
+            }
+            for (int e = 0; e < d; ++e) o[e] += p[j] * v[e];
+        }
+        lse[bh] = m + log(z);
+        free(qr); free(kh); free(kr); free(vh); free(s); free(p);
+    }
+    return bad ? 2 : 0;
+}
+
 int oracle_sdpa(const oracle_dims* dm, int B, long L_max, const double* q,
                 const double* k, const double* v, const int* seq_lens,
                 const int* q_pos, long pos_offset, double* out, double* lse) {

@@ -90,6 +90,25 @@ int oracle_sdpa(const oracle_dims* dm, int B, long L_max, const double* q,
                 const double* k, const double* v, const int* seq_lens,
                 const int* q_pos, long pos_offset, double* out, double* lse);
 
+/* Hybrid attention with an exact window ("Hybrid Latent Attention for Looped
+ * Language Models", §3.4 "Exact sliding window", Eq. (4)): one softmax over
+ *   latent scores  s_j  for cached tokens j < n_lat[b] (keys and values
+ *                  reconstructed by Eq. (3) of the LLA page, key rotated at j),
+ *   exact scores   s_w  for window tokens w < n_win[b] (pre-RoPE keys k_win and
+ *                  values v_win given, key rotated at win_pos[b] + w),
+ * query rotated at q_pos[b]; out = sum of p times the token's value (latent:
+ * reconstructed, window: exact), lse = ln sum exp(s).  Per-head variant only.
+ * Layouts as oracle_decode, plus k_win / v_win [B][H][W][d].  An empty row
+ * (n_lat + n_win == 0) gives out = 0 and lse = -inf.  Returns 2 if a softmax row
+ * fails to sum to 1 within 1e-12. */
+int oracle_hybrid(const oracle_dims* dm, int t, int B, long L_max, long W,
+                  const double* q, const double* cache_k, const double* cache_v,
+                  const int* n_lat, const int* q_pos,
+                  const double* w_up_k, const double* w_up_v,
+                  const double* mu_k, const double* mu_v,
+                  const double* k_win, const double* v_win, const int* n_win,
+                  const int* win_pos, double* out, double* lse);
+
 /* Threads the oracle's OpenMP loops use. */
 int oracle_num_threads(void);
 

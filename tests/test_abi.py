@@ -132,3 +132,16 @@ def test_decode_kernel_dispatch(L):
     assert d(4, 16, 128, 256, variant=lla.LLA_2D) == "pair-2d"
     assert d(4, 16, 16, 32, dtype=lla.LLA_F32) == "fp32"
     assert d(4, 16, 16, 32, d_head=64) is None
+
+
+def test_window_rejects_bad_arguments_on_host(L):
+    dm = lla.dims(4, 2, 16, 32)
+    call = lambda d, B=1, W=8, rope_len=128, ws=1 << 20: L.lla_window_attn(
+        ctypes.byref(d), B, W, None, None, None, None, None, None, None, None, rope_len, None, None, None, ws, None)
+    assert call(dm) == lla.LLA_ERR_INVALID_ARG                       # null pointers
+    assert call(dm, B=-1) == lla.LLA_ERR_INVALID_ARG
+    assert call(dm, W=-1) == lla.LLA_ERR_INVALID_ARG
+    assert call(dm, rope_len=0) == lla.LLA_ERR_INVALID_ARG
+    assert call(lla.dims(4, 2, 16, 32, d_head=64)) == lla.LLA_ERR_UNSUPPORTED
+    assert call(dm, B=0) == lla.LLA_OK                               # nothing to do
+    assert call(dm, W=0) == lla.LLA_OK
