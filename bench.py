@@ -32,7 +32,8 @@ sys.path.insert(0, ROOT)
 
 from looped_transformer_cross_gb300 import build as lla_build  # noqa: E402
 from looped_transformer_cross_gb300 import lla  # noqa: E402
-from looped_transformer_cross_gb300.synth import WORKLOADS, make_decode_inputs, widen  # noqa: E402
+from looped_transformer_cross_gb300.synth import (WORKLOADS, make_decode_inputs,  # noqa: E402
+                                                  make_window_inputs, widen)
 
 METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe roofline"
 
@@ -125,28 +126,37 @@ class ClockSampler:
 # ----------------------------------------------------------------- our arm
 
 class DecodeStep:
-    """One layer's state on the device and the per-step call sequence."""
+    """One layer's state on the device and the per-step call sequence.  With a window
+    W > 0 each decode call is followed by lla_window_attn over an exact window of the
+    W newest tokens (the HLA page's hybrid layout, §3.4 Eq. (4)) placed after the
+    latent tokens."""
 
-    def __init__(self, w, seed, device):
+    def __init__(self, w, seed, device, window=0):
         self.w = w
+        self.window = window
         self.inp = make_decode_inputs(w, seed, device=device, with_encode=True)
+        if window > 0:
+            self.win = make_window_inputs(w, window, seed + 5, self.inp["seq_lens"], device=device)
+            self.inp["q_pos"] = self.win["q_pos"]
         g = torch.Generator(device=device)
         g.manual_seed(seed + 7)
         # one query per loop (the model's query changes from loop to loop)
         self.q = (torch.randn((w.T, w.B, w.H, w.d), generator=g, device=device)
                   .to(self.inp["q"].dtype).contiguous())
         self.dm = lla.dims(w.T, w.H, w.r_k, w.r_v, variant=w.variant, rope_base=w.rope_base)
-        c, s = lla.rope_table(self.dm, max(w.L_max, 128))
+        c, s = lla.rope_table(self.dm, max(w.L_max + window, 128))
         self.cos, self.sin = c.to(device), s.to(device)
         self.ws = lla.make_workspace(self.dm, w.B, w.L_max, w.B, device=device)
         self.seq_idx = torch.arange(w.B, dtype=torch.int32, device=device)
         self.out = torch.empty((w.T, w.B, w.H, w.d), dtype=torch.float32, device=device)
         self.lse = torch.empty((w.T, w.B, w.H), dtype=torch.float32, device=device)
         self.tokens = int(self.inp["seq_lens"].sum().item())
+        self.enc_pos = (self.inp["seq_lens"] - 1).clamp(0, w.L_max - 1).to(torch.int32)
 
     def run(self, ev=None):
         i, dm = self.inp, self.dm
-        lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, i["q_pos"], i["w_down_k"], i["w_down_v"],
+        # the new token's latent: slot seq_lens - 1 (the query's own slot without a window)
+        lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, self.enc_pos, i["w_down_k"], i["w_down_v"],
                    i["mu_k"], i["mu_v"], i["cache_k"], i["cache_v"], self.ws)
         for t in range(self.w.T):
             if ev is not None:
@@ -156,11 +166,17 @@ class DecodeStep:
                             self.out[t], self.lse[t], self.ws)
             if ev is not None:
                 ev[1][t].record()
+            if self.window > 0:
+                v = self.win
+                lla.window_attn(dm, self.q[t], v["k_win"], v["v_win"], v["win_len"], v["win_pos"],
+                                i["q_pos"], self.cos, self.sin, self.out[t], self.lse[t], self.ws)
+                if ev is not None:
+                    ev[2][t].record()
 
     # launches of this library's kernels per step: encode (bias + GEMM) + T x (query
-    # images + decode + combine)
+    # images + decode + combine [+ window])
     def launches(self):
-        return 2 + 3 * self.w.T
+        return 2 + (4 if self.window > 0 else 3) * self.w.T
 
 
 def barrier(dist_on):
@@ -238,7 +254,7 @@ def run_ours(args, dist_on, rank, world, device):
     w = WORKLOADS[args.workload]
     lla_build.build()
     lla.lib()
-    step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device)
+    step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device, window=args.window)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -247,7 +263,7 @@ def run_ours(args, dist_on, rank, world, device):
         raise RuntimeError("device status after warm-up: " + lla.status_string(st))
 
     T = w.T
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(T)] for _ in range(2)]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(T)] for _ in range(3)]
           for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -306,6 +322,20 @@ def run_ours(args, dist_on, rank, world, device):
                 "latent_bytes_per_launch": step.tokens * (w.r_k + w.r_v) * 2,
                 "launch_ms": t_call * 1e3, "peak_source": src + " (bf16 sustained)"}
 
+    win = None
+    if args.window > 0:
+        # exact-window call: window K/V + query read, out / lse read and written
+        wdur = float(np.mean([ev[k][1][t].elapsed_time(ev[k][2][t]) / 1e3
+                              for k in range(args.steps) for t in range(T)]))
+        esz = 2 if w.dtype == "bf16" else 4
+        wtok = int(step.win["win_len"].sum().item())
+        wbytes = wtok * w.H * 2 * w.d * esz + w.B * w.H * (w.d * esz + 2 * (w.d + 1) * 4)
+        wach = wbytes / wdur / 1e9
+        win = {"W": args.window, "window_tokens_per_call": wtok * w.H, "call_ms": wdur * 1e3,
+               "roofline": {"bound": "hbm", "achieved": wach, "peak": hbm, "unit": "GB/s", "frac": wach / hbm,
+                            "traffic": None, "kernel": "lla_window_attn (window_attn_kernel)",
+                            "algorithmic_bytes_per_launch": wbytes, "peak_source": src}}
+
     e2e_steps = max(3, min(args.steps, 200))
     e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
     e2e_dt = max_over_ranks(e2e_dt, dist_on, device)
@@ -316,6 +346,7 @@ def run_ours(args, dist_on, rank, world, device):
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "variant": "LLA-2D" if w.variant else "per-head",
+                   **({"exact_window": args.window} if args.window > 0 else {}),
                    "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
                    "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi],
                    "latent_tokens_per_gpu": step.tokens, "parallelism": "dp%d" % world,
@@ -323,6 +354,7 @@ def run_ours(args, dist_on, rank, world, device):
                    "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
                        step.inp["cache_k"].numel() * 2 * (1 + w.r_v / w.r_k) / 1e9)},
         "roofline": roof,
+        **({"window": win} if win else {}),
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clk.summary(),
@@ -372,6 +404,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ouro1.4b_rho4_b32_4k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", type=int, default=0,
+                    help="also run lla_window_attn over an exact window of this many newest tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
