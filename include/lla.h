@@ -165,8 +165,8 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
  *   win_pos   device  int32 [B]        position of window token 0; token w is
  *                                      rotated at win_pos[b] + w
  *   q_pos     device  int32 [B]        as for lla_decode_attn
- *   rope_cos/_sin, rope_len            as for lla_decode_attn; every window
- *                                      position must be < rope_len
+ *   rope_cos/_sin, rope_len            as for lla_decode_attn (rope_len >= 128);
+ *                                      every window position must be < rope_len
  *   out, lse  device  fp32 [B][H][d], [B][H]   in: latent part; out: merged
  *                                      (rows with win_len 0 are left as they are)
  *   workspace device  >= 256 bytes: the status word (lla_device_status)

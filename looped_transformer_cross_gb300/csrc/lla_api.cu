@@ -338,7 +338,7 @@ lla_status lla_window_attn(const lla_dims* dims, int B, int W, const void* q, co
                            float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
   lla_status st = check_dims(dims);
   if (st != LLA_OK) return st;
-  if (B < 0 || W < 0 || rope_len < 1) return LLA_ERR_INVALID_ARG;
+  if (B < 0 || W < 0 || rope_len < kTile) return LLA_ERR_INVALID_ARG;
   if (B == 0 || W == 0) return LLA_OK;
   if (static_cast<int64_t>(B) * dims->H > (int64_t(1) << 30)) return LLA_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k_win, v_win, win_len, win_pos, q_pos, rope_cos, rope_sin, out, lse, workspace};

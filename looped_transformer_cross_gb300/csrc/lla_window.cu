@@ -130,6 +130,10 @@ __global__ void __launch_bounds__(kWinThreads) window_attn_kernel(const __grid_c
                      (x.z * c.y - x.w * s.y) * sc, (x.z * s.y + x.w * c.y) * sc);
   }
 
+  // cos / sin of kWinWarps theta_f for the lane's frequencies (table row kWinWarps)
+  const float2 cs = __ldg(reinterpret_cast<const float2*>(a.rope_cos + kWinWarps * 64 + 2 * lane));
+  const float2 sn = __ldg(reinterpret_cast<const float2*>(a.rope_sin + kWinWarps * 64 + 2 * lane));
+
   // ---- online softmax of this warp's window tokens (every kWinWarps-th of a chunk),
   // kUnroll per step: the step's scores come out of one shuffle reduce-scatter
   // (lanes 4i .. 4i + 3 end with token i's sum), then one broadcast per weight
@@ -143,12 +147,19 @@ __global__ void __launch_bounds__(kWinThreads) window_attn_kernel(const __grid_c
     // together, after the barrier below)
     const bool got = warp_wait(smem_u32(&full[ci & 1]), (ci >> 1) & 1, &abort_flag, a.status);
     for (int w0 = warp; got && w0 < cn; w0 += kWinWarps * kUnroll) {
+      // the step's tokens sit kWinWarps positions apart: one table row for its first
+      // token, the others by rotating with R(kWinWarps) (angle sum; positions of
+      // masked tokens may run past the table, their weights are 0)
       float2 cc[kUnroll], ss[kUnroll];
+      {
+        const int64_t p = static_cast<int64_t>(p0) + c0 + w0;
+        cc[0] = __ldg(reinterpret_cast<const float2*>(a.rope_cos + p * 64 + 2 * lane));
+        ss[0] = __ldg(reinterpret_cast<const float2*>(a.rope_sin + p * 64 + 2 * lane));
+      }
 #pragma unroll
-      for (int i = 0; i < kUnroll; ++i) {
-        const int64_t p = static_cast<int64_t>(p0) + c0 + min(w0 + i * kWinWarps, cn - 1);
-        cc[i] = __ldg(reinterpret_cast<const float2*>(a.rope_cos + p * 64 + 2 * lane));
-        ss[i] = __ldg(reinterpret_cast<const float2*>(a.rope_sin + p * 64 + 2 * lane));
+      for (int i = 1; i < kUnroll; ++i) {
+        cc[i] = make_float2(fmaf(cc[i - 1].x, cs.x, -ss[i - 1].x * sn.x), fmaf(cc[i - 1].y, cs.y, -ss[i - 1].y * sn.y));
+        ss[i] = make_float2(fmaf(ss[i - 1].x, cs.x, cc[i - 1].x * sn.x), fmaf(ss[i - 1].y, cs.y, cc[i - 1].y * sn.y));
       }
       float part[kUnroll];
 #pragma unroll

@@ -142,6 +142,7 @@ def test_window_rejects_bad_arguments_on_host(L):
     assert call(dm, B=-1) == lla.LLA_ERR_INVALID_ARG
     assert call(dm, W=-1) == lla.LLA_ERR_INVALID_ARG
     assert call(dm, rope_len=0) == lla.LLA_ERR_INVALID_ARG
+    assert call(dm, rope_len=127) == lla.LLA_ERR_INVALID_ARG
     assert call(lla.dims(4, 2, 16, 32, d_head=64)) == lla.LLA_ERR_UNSUPPORTED
     assert call(dm, B=0) == lla.LLA_OK                               # nothing to do
     assert call(dm, W=0) == lla.LLA_OK
