@@ -41,8 +41,8 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 8-sequence variant
 # of the bench layer.  Valid only for the decode source whose sha256 starts with
 # TRAFFIC_SRC_SHA; any other source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = (263.994368e6 + 4.025344e6) / (31042 * 16)
-TRAFFIC_SRC_SHA = "51f1eadfe3c1e845"
+TRAFFIC_PER_TOKEN_HEAD = (263.959808e6 + 4.089600e6) / (31042 * 16)
+TRAFFIC_SRC_SHA = "4be32f8da99499c2"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D kernel, per latent token (all heads), from the 32-sequence
 # variant of the LLA-2D layer; valid only for the source whose sha256 starts with
@@ -51,9 +51,9 @@ TRAFFIC2D_PER_TOKEN = (224.002816e6 + 4.921088e6) / (32 * 8192)
 TRAFFIC2D_SRC_SHA = "82da47c747901f36"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
 # Same for decode_small_kernel (the per-head kernel at small ranks), from a capture
-# of the 64-sequence variant of the rho = 21.3 layer; None until one is taken.
-TRAFFIC_SMALL_PER_TOKEN_HEAD = None
-TRAFFIC_SMALL_SRC_SHA = None
+# of the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
+TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.888832e6 + 3.641344e6) / (64 * 4096 * 16)
+TRAFFIC_SMALL_SRC_SHA = "6183fa766422f3df"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 UNIT = "latent tokens/s per layer-loop"
 
