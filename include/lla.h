@@ -181,6 +181,36 @@ lla_status lla_window_attn(const lla_dims* dims, int B, int W, const void* q,
                            const float* rope_cos, const float* rope_sin, int64_t rope_len,
                            float* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * lla_decode_attn_decoupled — absorbed decoupled-RoPE decode (LLA paper,
+ * Appendix J "Absorbed attention"; the path its Table 13 times).  The K
+ * up-projection moves to the query side (an MLA-style content path on the
+ * latents without RoPE) and position enters through a small explicit rotary
+ * branch of d_rope = 64 dimensions per token and head, stored once for all loops:
+ *   s_j = (q_c . (c_k,j W_up,k,t^T + mu_k,t) + RoPE(q_r, q_pos) . RoPE(r_j, j))
+ *         / sqrt(d + d_rope),
+ *   out = sum_j softmax(s)_j (c_v,j W_up,v,t^T + mu_v,t),  lse = ln sum_j exp(s_j).
+ * This is a different function from lla_decode_attn (no RoPE on the content
+ * keys); a model must have been trained or adapted for it (Appendix J, Table 14).
+ * LLA_PER_HEAD only; d_rope must be 64; r_k <= 128 on the bf16 kernel.
+ *   q          device  [B][H][d + d_rope]   content part then rotary part
+ *   k_rope     device  [B][H][L_max][d_rope] rotary keys before RoPE (storage dtype)
+ *   rope_cos/_sin      [rope_len][d_rope/2] for the rotary branch: lla_rope_table
+ *                      with lla_dims.d_head = d_rope (theta_f = base^(-2f/d_rope));
+ *                      rope_len >= max(L_max, 128)
+ *   workspace          >= lla_decoupled_workspace_size() bytes, first 256 zero
+ * Everything else as lla_decode_attn (cache, seq_lens, q_pos, W_up, mu, out, lse).
+ */
+size_t lla_decoupled_workspace_size(const lla_dims* dims, int d_rope, int B, int64_t L_max);
+lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rope, const void* q,
+                                     lla_cache cache, const void* k_rope,
+                                     const int32_t* seq_lens, const int32_t* q_pos,
+                                     const void* w_up_k, const void* w_up_v,
+                                     const float* mu_k, const float* mu_v,
+                                     const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                                     float* out, float* lse,
+                                     void* workspace, size_t ws_bytes, void* stream);
+
 /* Size of the fixed scratch array behind lla_decode_attn_noalloc (64 MiB). */
 #define LLA_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -304,6 +304,7 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   const int sms = sm_count();
   if (sms <= 0) return LLA_ERR_CUDA;
   a.combine_units = decode_combine_units(cache.B, H, sms);
+  a.records_per_cta = kRecordsPerCta;
   const uint64_t rows = static_cast<uint64_t>(cache.L_max), units = static_cast<uint64_t>(cache.B) * H;
   if (small_path(dims)) {
     // small ranks: positions split over the CTAs, every head of a position in one CTA
@@ -330,6 +331,77 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 32, kTile, 1))
     return LLA_ERR_CUDA;
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+size_t lla_decoupled_workspace_size(const lla_dims* dims, int d_rope, int B, int64_t L_max) {
+  if (check_dims(dims) != LLA_OK || dims->variant != LLA_PER_HEAD || d_rope != 64 || B < 0 || L_max < 0) return 0;
+  // status word, records [(B H + grid) 16][r_v + 4] (grid <= kMaxGrid), fp32 mode: scores
+  size_t off = 256;
+  off += al256((static_cast<size_t>(B) * dims->H + kMaxGrid) * kDecoupledRecords * (dims->r_v + kRecordHead) * 4);
+  if (dims->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * dims->H * L_max * 4);
+  return off;
+}
+
+lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rope, const void* q, lla_cache cache,
+                                     const void* k_rope, const int32_t* seq_lens, const int32_t* q_pos,
+                                     const void* w_up_k, const void* w_up_v, const float* mu_k, const float* mu_v,
+                                     const float* rope_cos, const float* rope_sin, int64_t rope_len, float* out,
+                                     float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  lla_status st = check_dims(dims);
+  if (st != LLA_OK) return st;
+  if (dims->variant != LLA_PER_HEAD || d_rope != 64) return LLA_ERR_UNSUPPORTED;
+  if (loop_t < 0 || loop_t >= dims->T || cache.B < 0 || cache.L_max < 1) return LLA_ERR_INVALID_ARG;
+  if (cache.B == 0) return LLA_OK;
+  if (cache.L_max > (int64_t(1) << 30) || static_cast<int64_t>(cache.B) * dims->H > (int64_t(1) << 30))
+    return LLA_ERR_UNSUPPORTED;
+  if (rope_len < cache.L_max || rope_len < kTile) return LLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, cache.k, cache.v, k_rope, seq_lens, q_pos, w_up_k, w_up_v, mu_k,
+                        mu_v, rope_cos, rope_sin, out, lse, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LLA_ERR_INVALID_ARG;
+  const size_t need = lla_decoupled_workspace_size(dims, d_rope, cache.B, cache.L_max);
+  if (ws_bytes < need) return LLA_ERR_INVALID_ARG;
+  const int H = dims->H, d = dims->d_head;
+  const int esize = dims->dtype == LLA_BF16 ? 2 : 4;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a{};
+  a.B = cache.B;
+  a.H = H;
+  a.r_k = dims->r_k;
+  a.r_v = dims->r_v;
+  a.rope_style = dims->rope_style;
+  a.L_max = cache.L_max;
+  a.rope_len = rope_len;
+  a.mu_hstride = static_cast<int64_t>(dims->T) * d;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.q_pos = q_pos;
+  a.cache_k = cache.k;
+  a.cache_v = cache.v;
+  a.k_rope = k_rope;
+  a.d_rope = d_rope;
+  a.w_up_k = static_cast<const uint8_t*>(w_up_k) + static_cast<size_t>(loop_t) * H * d * dims->r_k * esize;
+  a.w_up_v = static_cast<const uint8_t*>(w_up_v) + static_cast<size_t>(loop_t) * H * d * dims->r_v * esize;
+  a.mu_k = mu_k + static_cast<size_t>(loop_t) * d;
+  a.mu_v = mu_v + static_cast<size_t>(loop_t) * d;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  a.out = out;
+  a.lse = lse;
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.partials = reinterpret_cast<float*>(ws + 256);
+  a.scores = reinterpret_cast<float*>(
+      ws + 256 + al256((static_cast<size_t>(cache.B) * H + kMaxGrid) * kDecoupledRecords * (dims->r_v + kRecordHead) * 4));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dims->dtype == LLA_F32) return launch_decoupled_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  if (decoupled_smem_bytes(dims->r_k) > static_cast<size_t>(kSmemLimit)) return LLA_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  if (sms <= 0) return LLA_ERR_CUDA;
+  const int64_t max_tiles = static_cast<int64_t>(cache.B) * H * ((cache.L_max + kTile - 1) / kTile);
+  a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_tiles)));
+  a.combine_units = decode_combine_units(cache.B, H, sms);
+  a.records_per_cta = kDecoupledRecords;
+  return launch_decoupled_bf16(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
 lla_status lla_window_attn(const lla_dims* dims, int B, int W, const void* q, const void* k_win,

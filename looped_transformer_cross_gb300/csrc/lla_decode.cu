@@ -730,9 +730,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
       const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
       if (nb > 0) {
         // Tile-major split (per-head kernel): CTA ranges over the flat (sequence,
-        // head, tile) list, records ((b H + h) + c) 4 + warp.  Position-major split
+        // head, tile) list, records ((b H + h) + c) R + warp.  Position-major split
         // (small-rank kernel): ranges over (sequence, tile) with every head inner,
-        // records ((b + c) H + h) 4 + warp.
+        // records ((b + c) H + h) R + warp.  R = 4 (one per epilogue warp) or 16
+        // (decoupled kernel: four groups of four warps).
         const long long total = a.pos_major ? tot : static_cast<long long>(a.H) * tot;
         const long long per = max(1LL, (total + a.grid - 1) / a.grid);
         const long long F0 = a.pos_major ? pb : static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
@@ -740,16 +741,14 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
         const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
         const int rs = a.r_v + kRecordHead;
         const long long u = static_cast<long long>(b) * a.H + h;
-        const long long base = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * kRecordsPerCta
-                                           : (u + c0) * kRecordsPerCta;
-        const long long cstride = a.pos_major ? static_cast<long long>(kRecordsPerCta) * a.H : kRecordsPerCta;
-        // record r of the unit: CTA c0 + r / 4, warp r % 4
-        auto rec_at = [&](int r) {
-          return a.partials + (base + (r / kRecordsPerCta) * cstride + r % kRecordsPerCta) * rs;
-        };
+        const int R = a.records_per_cta;
+        const long long base = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * R : (u + c0) * R;
+        const long long cstride = a.pos_major ? static_cast<long long>(R) * a.H : R;
+        // record r of the unit: CTA c0 + r / R, warp r % R
+        auto rec_at = [&](int r) { return a.partials + (base + (r / R) * cstride + r % R) * rs; };
         // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
         // the unit in that CTA wrote m = -inf, l = 0, acc = 0
-        const int nrec = kRecordsPerCta * (c1 - c0 + 1);
+        const int nrec = R * (c1 - c0 + 1);
         for (int cb = 0; cb < nrec; cb += 8) {
           // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
           // lane + 32 j of each, all in one round of loads
@@ -1049,6 +1048,11 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern[which], a);
+}
+
+cudaError_t launch_decode_f32_values(const DecodeArgs& a, cudaStream_t s) {
+  decode_f32_values_kernel<<<a.B * a.H, 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s) {

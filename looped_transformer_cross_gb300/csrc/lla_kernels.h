@@ -80,6 +80,9 @@ struct DecodeArgs {
   int64_t trig_rows;
   int pos_major;                     // records indexed ((b + cta) H + h) 4 + warp (small-rank path)
   int combine_units;                 // sequences per combine block (1..16)
+  int records_per_cta;               // records per (unit, CTA): 4, or 16 (decoupled kernel)
+  const void* k_rope;                // decoupled path: rotary keys [B][H][L_max][d_rope]
+  int d_rope;                        // decoupled path: rotary branch width (0: full-RoPE path)
   DecodePlan plan;
   DecodeSmallPlan splan;
 };
@@ -98,6 +101,15 @@ cudaError_t launch_decode_small_bf16(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 // Sequences per combine block: as many as keep about two blocks per SM, at most 16.
 int decode_combine_units(int B, int H, int sms);
+
+// Absorbed decoupled-RoPE decode (content path on the latents + rotary branch).
+constexpr int kDecoupledThreads = 544;  // producer warp + 4 groups of 4 warps
+constexpr int kDecoupledRecords = 16;   // records per (unit, CTA): one per group warp
+cudaError_t launch_decoupled_bf16(const DecodeArgs& a, cudaStream_t s);
+size_t decoupled_smem_bytes(int r_k);
+// fp32 softmax over a.scores and the V path (shared by the fp32 decode paths).
+cudaError_t launch_decode_f32_values(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decoupled_f32(const DecodeArgs& a, cudaStream_t s);
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);

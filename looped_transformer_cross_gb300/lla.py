@@ -73,6 +73,11 @@ def lib():
             L.lla_window_attn.argtypes = [pd, ctypes.c_int, ctypes.c_int, vp, vp, vp, i32p, i32p, i32p,
                                           fp, fp, ctypes.c_int64, fp, fp, vp, ctypes.c_size_t, vp]
             L.lla_window_attn.restype = ctypes.c_int
+            L.lla_decoupled_workspace_size.argtypes = [pd, ctypes.c_int, ctypes.c_int, ctypes.c_int64]
+            L.lla_decoupled_workspace_size.restype = ctypes.c_size_t
+            L.lla_decode_attn_decoupled.argtypes = [pd, ctypes.c_int, ctypes.c_int, vp, Cache, vp, i32p, i32p, vp, vp,
+                                                    fp, fp, fp, fp, ctypes.c_int64, fp, fp, vp, ctypes.c_size_t, vp]
+            L.lla_decode_attn_decoupled.restype = ctypes.c_int
             L.lla_decode_kernel.argtypes = [pd]
             L.lla_decode_kernel.restype = ctypes.c_char_p
             L.lla_abi_version.argtypes = []
@@ -174,6 +179,28 @@ def window_attn(dm: Dims, q, k_win, v_win, win_len, win_pos, q_pos, rope_cos, ro
                                int(rope_cos.shape[0]), _ptr(out), _ptr(lse), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "lla_window_attn")
+
+
+def decoupled_workspace(dm: Dims, d_rope: int, B: int, L_max: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for lla_decode_attn_decoupled."""
+    n = lib().lla_decoupled_workspace_size(ctypes.byref(dm), int(d_rope), int(B), int(L_max))
+    if n == 0:
+        raise LLAError(LLA_ERR_INVALID_ARG, "lla_decoupled_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_attn_decoupled(dm: Dims, loop_t: int, q, cache_k, cache_v, k_rope, seq_lens, q_pos, w_up_k,
+                          w_up_v, mu_k, mu_v, rope_cos, rope_sin, out, lse, workspace, stream=None):
+    """lla_decode_attn_decoupled: absorbed decoupled-RoPE decode (content on the latents,
+    a d_rope = k_rope.shape[3] rotary branch); q is [B][H][d + d_rope]."""
+    B, L_max = int(cache_k.shape[0]), int(cache_k.shape[2])
+    cache = Cache(ctypes.c_void_p(cache_k.data_ptr()), ctypes.c_void_p(cache_v.data_ptr()), B, L_max)
+    st = lib().lla_decode_attn_decoupled(ctypes.byref(dm), int(loop_t), int(k_rope.shape[3]), _ptr(q), cache,
+                                         _ptr(k_rope), _ptr(seq_lens), _ptr(q_pos), _ptr(w_up_k), _ptr(w_up_v),
+                                         _ptr(mu_k), _ptr(mu_v), _ptr(rope_cos), _ptr(rope_sin),
+                                         int(rope_cos.shape[0]), _ptr(out), _ptr(lse), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "lla_decode_attn_decoupled")
 
 
 def device_status(workspace, stream=None, clear=True) -> int:

@@ -169,6 +169,17 @@ def make_window_inputs(w: Workload, W: int, seed: int, seq_lens: torch.Tensor, d
     return out
 
 
+def make_decoupled_inputs(w: Workload, seed: int, device="cpu", d_rope: int = 64) -> dict:
+    """The decoupled-RoPE decode's extra inputs: rotary keys k_rope [B][H][L_max][d_rope]
+    ~ N(0, 1) and the query [B][H][d + d_rope] ~ N(0, 1), in the storage dtype."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(seed))
+    sd = storage_dtype(w)
+    return {"k_rope": _normal(gen, (w.B, w.H, w.L_max, d_rope), 1.0, sd, dev),
+            "q": _normal(gen, (w.B, w.H, w.d + d_rope), 1.0, sd, dev)}
+
+
 def widen(t: torch.Tensor):
     """Exact widening of a stored tensor to a float64 numpy array (for the oracle)."""
     return t.detach().to("cpu").to(torch.float64).numpy()

@@ -87,6 +87,9 @@ def lib():
             L.oracle_hybrid.argtypes = [pd, ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_long, dp, dp, dp,
                                         ip, ip, dp, dp, dp, dp, dp, dp, ip, ip, dp, dp]
             L.oracle_hybrid.restype = ctypes.c_int
+            L.oracle_decoupled.argtypes = [pd, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long, dp, dp, dp,
+                                           dp, ip, ip, ctypes.c_long, dp, dp, dp, dp, dp, dp]
+            L.oracle_decoupled.restype = ctypes.c_int
             L.oracle_num_threads.argtypes = []
             L.oracle_num_threads.restype = ctypes.c_int
             _lib = L
@@ -200,6 +203,32 @@ def hybrid(dm: OracleDims, t, q, cache_k, cache_v, n_lat, q_pos, w_up_k, w_up_v,
                              lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     if rc != 0:
         raise ValueError("oracle_hybrid failed (%d)" % rc)
+    return out, lse
+
+
+def decoupled(dm: OracleDims, t, q, cache_k, cache_v, k_rope, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v,
+              pos_offset=0):
+    """Absorbed decoupled-RoPE decode at loop ``t`` (LLA page, Appendix J): q [B][H][d + d_rope],
+    k_rope [B][H][L_max][d_rope], the rest as :func:`decode`.  Returns (out, lse)."""
+    q, qp = _d(q)
+    ck, ckp = _d(cache_k)
+    cv, cvp = _d(cache_v)
+    kr, krp = _d(k_rope)
+    sl, slp = _i(seq_lens)
+    qpos, qposp = _i(q_pos)
+    wk, wkp = _d(w_up_k)
+    wv, wvp = _d(w_up_v)
+    mk, mkp = _d(mu_k)
+    mv, mvp = _d(mu_v)
+    B, L_max, d_rope = q.shape[0], ck.shape[2], kr.shape[3]
+    out = np.zeros((B, dm.H, dm.d))
+    lse = np.zeros((B, dm.H))
+    rc = lib().oracle_decoupled(ctypes.byref(dm), int(t), int(d_rope), B, L_max, qp, ckp, cvp, krp, slp, qposp,
+                                int(pos_offset), wkp, wvp, mkp, mvp,
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    if rc != 0:
+        raise ValueError("oracle_decoupled failed (%d)" % rc)
     return out, lse
 
 

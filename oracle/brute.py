@@ -119,3 +119,32 @@ def hybrid_per_head(t, q, cache_k, cache_v, n_lat, q_pos, w_up_k, w_up_v, mu_k, 
             out[b, h] = (w / w.sum()) @ V
             lse[b, h] = s.max() + np.log(w.sum())
     return out, lse
+
+
+def decoupled_per_head(t, q, cache_k, cache_v, k_rope, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v,
+                       base=10000.0, style=0):
+    """Absorbed decoupled-RoPE decode (LLA page, Appendix J "Absorbed attention"):
+    concatenated keys [content (Eq. (3), unrotated) ; R(j) r_j] against the query
+    [q_c ; R(q_pos) q_r], the d_rope-wide rotation an explicit matrix, one softmax,
+    scale 1/sqrt(d + d_rope).  q [B][H][d + d_rope], k_rope [B][H][L_max][d_rope]."""
+    B, H, dq = q.shape
+    d_rope = k_rope.shape[3]
+    d = dq - d_rope
+    out = np.zeros((B, H, d))
+    lse = np.zeros((B, H))
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(H):
+            if L == 0:
+                lse[b, h] = -np.inf
+                continue
+            K = reconstruct(cache_k[b, h, :L], w_up_k[t, h], mu_k[h, t * d:(t + 1) * d])
+            V = reconstruct(cache_v[b, h, :L], w_up_v[t, h], mu_v[h, t * d:(t + 1) * d])
+            Rk = np.stack([rotation_matrix(d_rope, j, base, style) @ k_rope[b, h, j] for j in range(L)])
+            qfull = np.concatenate([q[b, h, :d], rotation_matrix(d_rope, q_pos[b], base, style) @ q[b, h, d:]])
+            Kfull = np.concatenate([K, Rk], axis=1)
+            s = Kfull @ qfull / np.sqrt(dq)
+            w = np.exp(s - s.max())
+            out[b, h] = (w / w.sum()) @ V
+            lse[b, h] = s.max() + np.log(w.sum())
+    return out, lse

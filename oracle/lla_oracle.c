@@ -327,6 +327,79 @@ int oracle_hybrid(const oracle_dims* dm, int t, int B, long L_max, long W,
     return bad ? 2 : 0;
 }
 
+/* RoPE over a d_rope-wide branch: frequencies base^(-2f/d_rope), f < d_rope/2,
+ * pairs (f, f + d_rope/2) or (2f, 2f + 1) as dm->rope_style. */
+static void rope_rotate_branch(const oracle_dims* dm, int d_rope, const double* x, double pos,
+                               double* y) {
+    for (int f = 0; f < d_rope / 2; ++f) {
+        const int i0 = dm->rope_style == 0 ? f : 2 * f;
+        const int i1 = dm->rope_style == 0 ? f + d_rope / 2 : 2 * f + 1;
+        const double ang = pos * pow(dm->rope_base, -2.0 * f / d_rope);
+        const double c = cos(ang), s = sin(ang);
+        y[i0] = x[i0] * c - x[i1] * s;
+        y[i1] = x[i0] * s + x[i1] * c;
+    }
+}
+
+/* LLA page, Appendix J "Absorbed attention" (decoupled rotary branch). */
+int oracle_decoupled(const oracle_dims* dm, int t, int d_rope, int B, long L_max,
+                     const double* q, const double* cache_k, const double* cache_v,
+                     const double* k_rope, const int* seq_lens, const int* q_pos,
+                     long pos_offset, const double* w_up_k, const double* w_up_v,
+                     const double* mu_k, const double* mu_v, double* out, double* lse) {
+    if (!dims_ok(dm) || dm->variant != 0 || t < 0 || t >= dm->T || B < 0 || L_max < 0 ||
+        d_rope < 2 || d_rope % 2)
+        return 1;
+    const int H = dm->H, d = dm->d, rk = dm->r_k, rv = dm->r_v, dq = d + d_rope;
+    for (int b = 0; b < B; ++b)
+        if (seq_lens[b] < 0 || seq_lens[b] > L_max) return 1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(|:bad)
+    for (long bh = 0; bh < (long)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        const long L = seq_lens[b];
+        double* o = out + bh * d;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        if (L == 0) {
+            lse[bh] = -INFINITY;
+            continue;
+        }
+        const double* Wk = w_up_k + (((long)t * H + h) * d) * rk;
+        const double* Wv = w_up_v + (((long)t * H + h) * d) * rv;
+        const double* muk_t = mu_k + (long)h * dm->T * d + (long)t * d;
+        const double* muv_t = mu_v + (long)h * dm->T * d + (long)t * d;
+        const double* qv = q + bh * dq;
+        double* kh = (double*)malloc(sizeof(double) * d);
+        double* vh = (double*)malloc(sizeof(double) * d);
+        double* qr = (double*)malloc(sizeof(double) * d_rope);
+        double* kr = (double*)malloc(sizeof(double) * d_rope);
+        double* s = (double*)malloc(sizeof(double) * L);
+        double* p = (double*)malloc(sizeof(double) * L);
+        rope_rotate_branch(dm, d_rope, qv + d, (double)(q_pos[b] + pos_offset), qr);
+        const double scale = 1.0 / sqrt((double)dq);
+        for (long j = 0; j < L; ++j) {
+            reconstruct(cache_k + (bh * L_max + j) * rk, Wk, muk_t, d, rk, kh);
+            rope_rotate_branch(dm, d_rope, k_rope + (bh * L_max + j) * d_rope, (double)(j + pos_offset), kr);
+            double acc = 0.0;
+            for (int e = 0; e < d; ++e) acc += qv[e] * kh[e];
+            for (int e = 0; e < d_rope; ++e) acc += qr[e] * kr[e];
+            s[j] = acc * scale;
+        }
+        double m, z;
+        softmax(s, L, p, &m, &z);
+        double psum = 0.0;
+        for (long j = 0; j < L; ++j) psum += p[j];
+        if (fabs(psum - 1.0) > 1e-12) bad |= 1;
+        for (long j = 0; j < L; ++j) {
+            reconstruct(cache_v + (bh * L_max + j) * rv, Wv, muv_t, d, rv, vh);
+            for (int e = 0; e < d; ++e) o[e] += p[j] * vh[e];
+        }
+        lse[bh] = m + log(z);
+        free(kh); free(vh); free(qr); free(kr); free(s); free(p);
+    }
+    return bad ? 2 : 0;
+}
+
 int oracle_sdpa(const oracle_dims* dm, int B, long L_max, const double* q,
                 const double* k, const double* v, const int* seq_lens,
                 const int* q_pos, long pos_offset, double* out, double* lse) {

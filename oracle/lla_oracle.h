@@ -109,6 +109,24 @@ int oracle_hybrid(const oracle_dims* dm, int t, int B, long L_max, long W,
                   const double* k_win, const double* v_win, const int* n_win,
                   const int* win_pos, double* out, double* lse);
 
+/* Absorbed decoupled-RoPE decode at loop t (LLA page, Appendix J "Absorbed
+ * attention": an MLA-style NoPE content path on the latents plus a small explicit
+ * rotary branch shared across the loops), per-head variant, written out:
+ *   content key   k_j = c_k,j W_up,k,t^T + mu_k,t           (Eq. (3), no rotation)
+ *   rotary key    r_j = k_rope[b][h][j] (d_rope values, one per token for all loops)
+ *   query         q = [q_c (d) ; q_r (d_rope)]
+ *   s_j = (q_c . k_j + RoPE(q_r, q_pos) . RoPE(r_j, j)) / sqrt(d + d_rope)
+ * with the rotary branch's frequencies theta_f = base^(-2f/d_rope) and the
+ * dimension pairs of dm->rope_style over d_rope; out = sum_j p_j v_j with
+ * v_j = c_v,j W_up,v,t^T + mu_v,t, lse = ln sum_j exp(s_j).  Layouts: q
+ * [B][H][d + d_rope]; k_rope [B][H][L_max][d_rope]; the rest as oracle_decode.
+ * Returns 2 if a softmax row fails to sum to 1 within 1e-12. */
+int oracle_decoupled(const oracle_dims* dm, int t, int d_rope, int B, long L_max,
+                     const double* q, const double* cache_k, const double* cache_v,
+                     const double* k_rope, const int* seq_lens, const int* q_pos,
+                     long pos_offset, const double* w_up_k, const double* w_up_v,
+                     const double* mu_k, const double* mu_v, double* out, double* lse);
+
 /* Threads the oracle's OpenMP loops use. */
 int oracle_num_threads(void);
 
