@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 from looped_transformer_cross_gb300 import build as lla_build  # noqa: E402
 from looped_transformer_cross_gb300 import lla  # noqa: E402
 from looped_transformer_cross_gb300.synth import (WORKLOADS, make_decode_inputs,  # noqa: E402
-                                                  make_window_inputs, widen)
+                                                  make_decoupled_inputs, make_window_inputs, widen)
 
 METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe roofline"
 
@@ -56,6 +56,7 @@ TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.888832e6 + 3.641344e6) / (64 * 4096 * 16)
 TRAFFIC_SMALL_SRC_SHA = "6183fa766422f3df"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 UNIT = "latent tokens/s per layer-loop"
+D_ROPE = 64   # rotary dimensions of the decoupled-RoPE decode
 
 
 def peaks():
@@ -131,9 +132,10 @@ class DecodeStep:
     W newest tokens (the HLA page's hybrid layout, §3.4 Eq. (4)) placed after the
     latent tokens."""
 
-    def __init__(self, w, seed, device, window=0):
+    def __init__(self, w, seed, device, window=0, decoupled=False):
         self.w = w
         self.window = window
+        self.decoupled = decoupled
         self.inp = make_decode_inputs(w, seed, device=device, with_encode=True)
         if window > 0:
             self.win = make_window_inputs(w, window, seed + 5, self.inp["seq_lens"], device=device)
@@ -152,6 +154,16 @@ class DecodeStep:
         self.lse = torch.empty((w.T, w.B, w.H), dtype=torch.float32, device=device)
         self.tokens = int(self.inp["seq_lens"].sum().item())
         self.enc_pos = (self.inp["seq_lens"] - 1).clamp(0, w.L_max - 1).to(torch.int32)
+        if decoupled:
+            # absorbed decoupled-RoPE decode (LLA Appendix J): rotary keys of d_rope = 64
+            # per (token, head) beside the latents, queries [B][H][d + 64]
+            self.k_rope = make_decoupled_inputs(w, seed + 9, device=device)["k_rope"]
+            self.q = (torch.randn((w.T, w.B, w.H, w.d + D_ROPE), generator=g, device=device)
+                      .to(self.inp["q"].dtype).contiguous())
+            rdm = lla.dims(w.T, w.H, w.r_k, w.r_v, d_head=D_ROPE, rope_base=w.rope_base)
+            c, s = lla.rope_table(rdm, max(w.L_max, 128))
+            self.cos_r, self.sin_r = c.to(device), s.to(device)
+            self.dws = lla.decoupled_workspace(self.dm, D_ROPE, w.B, w.L_max, device=device)
 
     def run(self, ev=None):
         i, dm = self.inp, self.dm
@@ -161,9 +173,14 @@ class DecodeStep:
         for t in range(self.w.T):
             if ev is not None:
                 ev[0][t].record()
-            lla.decode_attn(dm, t, self.q[t], i["cache_k"], i["cache_v"], i["seq_lens"], i["q_pos"],
-                            i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"], self.cos, self.sin,
-                            self.out[t], self.lse[t], self.ws)
+            if self.decoupled:
+                lla.decode_attn_decoupled(dm, t, self.q[t], i["cache_k"], i["cache_v"], self.k_rope,
+                                          i["seq_lens"], i["q_pos"], i["w_up_k"], i["w_up_v"], i["mu_k"],
+                                          i["mu_v"], self.cos_r, self.sin_r, self.out[t], self.lse[t], self.dws)
+            else:
+                lla.decode_attn(dm, t, self.q[t], i["cache_k"], i["cache_v"], i["seq_lens"], i["q_pos"],
+                                i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"], self.cos, self.sin,
+                                self.out[t], self.lse[t], self.ws)
             if ev is not None:
                 ev[1][t].record()
             if self.window > 0:
@@ -174,9 +191,11 @@ class DecodeStep:
                     ev[2][t].record()
 
     # launches of this library's kernels per step: encode (bias + GEMM) + T x (query
-    # images + decode + combine [+ window])
+    # images + decode + combine [+ window]); the decoupled kernel builds its absorbed
+    # query itself (decode + combine)
     def launches(self):
-        return 2 + (4 if self.window > 0 else 3) * self.w.T
+        per = 2 if self.decoupled else 3
+        return 2 + (per + (1 if self.window > 0 else 0)) * self.w.T
 
 
 def barrier(dist_on):
@@ -225,9 +244,10 @@ def e2e_run(step: DecodeStep, steps: int):
     return dt, h2d, d2h
 
 
-def oracle_sample(w, inp_dev, q_dev, budget_s=12.0):
+def oracle_sample(w, inp_dev, q_dev, budget_s=12.0, k_rope=None):
     """Time the oracle on the first S sequences (all heads, all loops) of the same
-    inputs; S grows from 1 until the run would take about ``budget_s``."""
+    inputs; S grows from 1 until the run would take about ``budget_s``.  With
+    ``k_rope`` it is the decoupled-RoPE decode's oracle."""
     import oracle
     odm = oracle.dims(w.T, w.H, w.d, w.r_k, w.r_v, w.variant, w.rope_base)
     wk, wv = widen(inp_dev["w_up_k"]), widen(inp_dev["w_up_v"])
@@ -236,9 +256,13 @@ def oracle_sample(w, inp_dev, q_dev, budget_s=12.0):
 
     def run(S, loops):
         ck, cv = widen(inp_dev["cache_k"][:S]), widen(inp_dev["cache_v"][:S])
+        kr = widen(k_rope[:S]) if k_rope is not None else None
         t0 = time.perf_counter()
         for t in range(loops):
-            oracle.decode(odm, t, widen(q_dev[t][:S]), ck, cv, lens[:S], lens[:S] - 1, wk, wv, mk, mv)
+            if kr is not None:
+                oracle.decoupled(odm, t, widen(q_dev[t][:S]), ck, cv, kr, lens[:S], lens[:S] - 1, wk, wv, mk, mv)
+            else:
+                oracle.decode(odm, t, widen(q_dev[t][:S]), ck, cv, lens[:S], lens[:S] - 1, wk, wv, mk, mv)
         return time.perf_counter() - t0
 
     t1 = run(1, 1)
@@ -254,7 +278,7 @@ def run_ours(args, dist_on, rank, world, device):
     w = WORKLOADS[args.workload]
     lla_build.build()
     lla.lib()
-    step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device, window=args.window)
+    step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device, window=args.window, decoupled=args.decoupled)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -287,7 +311,16 @@ def run_ours(args, dist_on, rank, world, device):
     durs = [ev[k][0][t].elapsed_time(ev[k][1][t]) / 1e3 for k in range(args.steps) for t in range(T)]
     t_call = float(np.mean(durs))
     hbm, tflops, src = peaks()
-    if w.variant == 0:
+    if args.decoupled:
+        # latent K and V rows plus the rotary key of every token-head, bf16
+        lat_bytes = step.tokens * w.H * (w.r_k + w.r_v + D_ROPE) * 2
+        achieved = lat_bytes / t_call / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "traffic_kernel": "decoupled_bf16_kernel",
+                "kernel": "lla_decode_attn_decoupled (decoupled_bf16_kernel + decode_combine_kernel)",
+                "algorithmic_bytes_per_launch": lat_bytes, "launch_ms": t_call * 1e3,
+                "peak_source": src}
+    elif w.variant == 0:
         lat_bytes = step.tokens * w.H * (w.r_k + w.r_v) * 2
         achieved = lat_bytes / t_call / 1e9
         import hashlib
@@ -347,10 +380,12 @@ def run_ours(args, dist_on, rank, world, device):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "variant": "LLA-2D" if w.variant else "per-head",
                    **({"exact_window": args.window} if args.window > 0 else {}),
+                   **({"decoupled_rope": D_ROPE} if args.decoupled else {}),
                    "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
                    "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi],
                    "latent_tokens_per_gpu": step.tokens, "parallelism": "dp%d" % world,
-                   "step": "lla_encode of %d new tokens + lla_decode_attn for loops 1..%d" % (w.B, T),
+                   "step": "lla_encode of %d new tokens + %s for loops 1..%d" % (
+                       w.B, "lla_decode_attn_decoupled" if args.decoupled else "lla_decode_attn", T),
                    "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
                        step.inp["cache_k"].numel() * 2 * (1 + w.r_v / w.r_k) / 1e9)},
         "roofline": roof,
@@ -360,7 +395,8 @@ def run_ours(args, dist_on, rank, world, device):
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = oracle_sample(w, step.inp, step.q)
+        res["cpu_baseline"] = oracle_sample(w, step.inp, step.q,
+                                            k_rope=step.k_rope if args.decoupled else None)
     return res
 
 
@@ -406,9 +442,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--window", type=int, default=0,
                     help="also run lla_window_attn over an exact window of this many newest tokens")
+    ap.add_argument("--decoupled", action="store_true",
+                    help="decode with lla_decode_attn_decoupled (64 rotary dimensions per token-head)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decoupled and args.window > 0:
+        ap.error("--decoupled and --window do not combine (the window call takes d-wide queries)")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -335,10 +335,16 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
 
 size_t lla_decoupled_workspace_size(const lla_dims* dims, int d_rope, int B, int64_t L_max) {
   if (check_dims(dims) != LLA_OK || dims->variant != LLA_PER_HEAD || d_rope != 64 || B < 0 || L_max < 0) return 0;
-  // status word, records [(B H + grid) 16][r_v + 4] (grid <= kMaxGrid), fp32 mode: scores
+  // status word, records [(B H + grid) 1][r_v + 4] (grid <= kMaxGrid), then the
+  // bf16 kernel's query records [B H][ceil(L_max / 128)][r_k + 68] or the fp32
+  // mode's scores
   size_t off = 256;
   off += al256((static_cast<size_t>(B) * dims->H + kMaxGrid) * kDecoupledRecords * (dims->r_v + kRecordHead) * 4);
-  if (dims->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * dims->H * L_max * 4);
+  if (dims->dtype == LLA_F32)
+    off += al256(static_cast<size_t>(B) * dims->H * L_max * 4);
+  else
+    off += al256(static_cast<size_t>(B) * dims->H * ((L_max + kTile - 1) / kTile) *
+                 decoupled_qrec_floats(dims->r_k) * 4);
   return off;
 }
 
@@ -390,11 +396,15 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
   a.lse = lse;
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.partials = reinterpret_cast<float*>(ws + 256);
-  a.scores = reinterpret_cast<float*>(
-      ws + 256 + al256((static_cast<size_t>(cache.B) * H + kMaxGrid) * kDecoupledRecords * (dims->r_v + kRecordHead) * 4));
+  uint8_t* tail = ws + 256 + al256((static_cast<size_t>(cache.B) * H + kMaxGrid) * kDecoupledRecords *
+                                   (dims->r_v + kRecordHead) * 4);
+  a.scores = reinterpret_cast<float*>(tail);
+  a.zimg = tail;
+  a.zimg_stride = static_cast<int64_t>(decoupled_qrec_floats(dims->r_k)) * 4;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dims->dtype == LLA_F32) return launch_decoupled_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
-  if (decoupled_smem_bytes(dims->r_k) > static_cast<size_t>(kSmemLimit)) return LLA_ERR_UNSUPPORTED;
+  a.ring_slots = decoupled_ring_slots(dims->r_k, dims->r_v);
+  if (a.ring_slots < 2) return LLA_ERR_UNSUPPORTED;
   const int sms = sm_count();
   if (sms <= 0) return LLA_ERR_CUDA;
   const int64_t max_tiles = static_cast<int64_t>(cache.B) * H * ((cache.L_max + kTile - 1) / kTile);

@@ -732,8 +732,8 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
         // Tile-major split (per-head kernel): CTA ranges over the flat (sequence,
         // head, tile) list, records ((b H + h) + c) R + warp.  Position-major split
         // (small-rank kernel): ranges over (sequence, tile) with every head inner,
-        // records ((b + c) H + h) R + warp.  R = 4 (one per epilogue warp) or 16
-        // (decoupled kernel: four groups of four warps).
+        // records ((b + c) H + h) R + warp.  R = 4 (one per epilogue warp) or 1
+        // (decoupled kernel: its warps are merged within the CTA).
         const long long total = a.pos_major ? tot : static_cast<long long>(a.H) * tot;
         const long long per = max(1LL, (total + a.grid - 1) / a.grid);
         const long long F0 = a.pos_major ? pb : static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;

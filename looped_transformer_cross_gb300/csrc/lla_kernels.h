@@ -80,9 +80,10 @@ struct DecodeArgs {
   int64_t trig_rows;
   int pos_major;                     // records indexed ((b + cta) H + h) 4 + warp (small-rank path)
   int combine_units;                 // sequences per combine block (1..16)
-  int records_per_cta;               // records per (unit, CTA): 4, or 16 (decoupled kernel)
+  int records_per_cta;               // records per (unit, CTA): 4, or 1 (decoupled kernel)
   const void* k_rope;                // decoupled path: rotary keys [B][H][L_max][d_rope]
   int d_rope;                        // decoupled path: rotary branch width (0: full-RoPE path)
+  int ring_slots;                    // decoupled path: slots of the key ring
   DecodePlan plan;
   DecodeSmallPlan splan;
 };
@@ -103,10 +104,14 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 int decode_combine_units(int B, int H, int sms);
 
 // Absorbed decoupled-RoPE decode (content path on the latents + rotary branch).
-constexpr int kDecoupledThreads = 544;  // producer warp + 4 groups of 4 warps
-constexpr int kDecoupledRecords = 16;   // records per (unit, CTA): one per group warp
+constexpr int kDecoupledThreads = 512;  // 16 warps of 8 tokens (lane 0 of warp 0 also issues the copies)
+constexpr int kDecoupledRecords = 1;    // records per (unit, CTA): warps merged in the CTA
+// Query kernel, main kernel, combine.  Needs a.zimg (query records per (unit,
+// 128-token tile), a.zimg_stride bytes apart) and a.ring_slots.
 cudaError_t launch_decoupled_bf16(const DecodeArgs& a, cudaStream_t s);
-size_t decoupled_smem_bytes(int r_k);
+int decoupled_qrec_floats(int r_k);     // floats of one unit's query record
+int decoupled_ring_slots(int r_k, int r_v);   // ring slots that fit in shared memory (0: unsupported)
+size_t decoupled_smem_bytes(int r_k, int r_v, int ns);
 // fp32 softmax over a.scores and the V path (shared by the fp32 decode paths).
 cudaError_t launch_decode_f32_values(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decoupled_f32(const DecodeArgs& a, cudaStream_t s);
