@@ -41,8 +41,8 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 8-sequence variant
 # of the bench layer.  Valid only for the decode source whose sha256 starts with
 # TRAFFIC_SRC_SHA; any other source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = (263.959808e6 + 4.089600e6) / (31042 * 16)
-TRAFFIC_SRC_SHA = "4be32f8da99499c2"
+TRAFFIC_PER_TOKEN_HEAD = (263.974912e6 + 3.452928e6) / (31042 * 16)
+TRAFFIC_SRC_SHA = "942b4253787d6137"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D kernel, per latent token (all heads), from the 32-sequence
 # variant of the LLA-2D layer; valid only for the source whose sha256 starts with
@@ -55,6 +55,11 @@ DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla
 TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.888832e6 + 3.641344e6) / (64 * 4096 * 16)
 TRAFFIC_SMALL_SRC_SHA = "6183fa766422f3df"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
+# Same for decoupled_bf16_kernel, per latent token-head (latent K and V rows plus the
+# rotary key), from the 8-sequence variant of the rho = 4 layer.
+TRAFFIC_DEC_PER_TOKEN_HEAD = (320.807936e6 + 3.610112e6) / (31042 * 16)
+TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
+DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
 UNIT = "latent tokens/s per layer-loop"
 D_ROPE = 64   # rotary dimensions of the decoupled-RoPE decode
 
@@ -191,10 +196,9 @@ class DecodeStep:
                     ev[2][t].record()
 
     # launches of this library's kernels per step: encode (bias + GEMM) + T x (query
-    # images + decode + combine [+ window]); the decoupled kernel builds its absorbed
-    # query itself (decode + combine)
+    # images + decode + combine [+ window]); decoupled: query records + decode + combine
     def launches(self):
-        per = 2 if self.decoupled else 3
+        per = 3
         return 2 + (per + (1 if self.window > 0 else 0)) * self.w.T
 
 
@@ -315,9 +319,14 @@ def run_ours(args, dist_on, rank, world, device):
         # latent K and V rows plus the rotary key of every token-head, bf16
         lat_bytes = step.tokens * w.H * (w.r_k + w.r_v + D_ROPE) * 2
         achieved = lat_bytes / t_call / 1e9
+        import hashlib
+        with open(DECOUPLED_SRC, "rb") as f:
+            same_src = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC_DEC_SRC_SHA)
+        traffic = TRAFFIC_DEC_PER_TOKEN_HEAD * step.tokens * w.H if same_src else None
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "traffic_kernel": "decoupled_bf16_kernel",
-                "kernel": "lla_decode_attn_decoupled (decoupled_bf16_kernel + decode_combine_kernel)",
+                "frac": achieved / hbm, "traffic": traffic, "traffic_kernel": "decoupled_bf16_kernel",
+                "kernel": "lla_decode_attn_decoupled (decoupled_query_kernel + decoupled_bf16_kernel + "
+                          "decode_combine_kernel)",
                 "algorithmic_bytes_per_launch": lat_bytes, "launch_ms": t_call * 1e3,
                 "peak_source": src}
     elif w.variant == 0:
