@@ -137,10 +137,11 @@ class DecodeStep:
     W newest tokens (the HLA page's hybrid layout, §3.4 Eq. (4)) placed after the
     latent tokens."""
 
-    def __init__(self, w, seed, device, window=0, decoupled=False):
+    def __init__(self, w, seed, device, window=0, decoupled=False, paged=0):
         self.w = w
         self.window = window
         self.decoupled = decoupled
+        self.paged = paged
         self.inp = make_decode_inputs(w, seed, device=device, with_encode=True)
         if window > 0:
             self.win = make_window_inputs(w, window, seed + 5, self.inp["seq_lens"], device=device)
@@ -159,6 +160,34 @@ class DecodeStep:
         self.lse = torch.empty((w.T, w.B, w.H), dtype=torch.float32, device=device)
         self.tokens = int(self.inp["seq_lens"].sum().item())
         self.enc_pos = (self.inp["seq_lens"] - 1).clamp(0, w.L_max - 1).to(torch.int32)
+        if paged:
+            # page pools [num_pages][H][P][r] with a shuffled page table (the page tables
+            # of "Enabling dynamic computation in Looped LMs", App. A.1); the dense cache
+            # rows are moved into them and the dense cache is dropped
+            P = paged
+            lens = self.inp["seq_lens"].cpu().tolist()
+            max_pages = (w.L_max + P - 1) // P
+            used = [(L + P - 1) // P for L in lens]
+            num_pages = sum(used)
+            perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(seed + 11))
+            bt = torch.full((w.B, max_pages), -1, dtype=torch.int32)
+            k = 0
+            for b, u in enumerate(used):
+                bt[b, :u] = perm[k:k + u].to(torch.int32)
+                k += u
+            self.block_table = bt.to(device)
+            for n, pn in (("cache_k", "pool_k"), ("cache_v", "pool_v")):
+                dense = self.inp[n]
+                pool = torch.empty((num_pages, w.H, P, dense.shape[-1]), dtype=dense.dtype, device=device)
+                for b, u in enumerate(used):
+                    for lp in range(u):
+                        rows = dense[b, :, lp * P:(lp + 1) * P]
+                        pool[int(bt[b, lp]), :, :rows.shape[1]] = rows
+                setattr(self, pn, pool)
+                self.inp[n] = None
+            del dense
+            torch.cuda.empty_cache()
+            self.ws = lla.make_workspace(self.dm, w.B, max_pages * P, w.B, device=device)
         if decoupled:
             # absorbed decoupled-RoPE decode (LLA Appendix J): rotary keys of d_rope = 64
             # per (token, head) beside the latents, queries [B][H][d + 64]
@@ -173,12 +202,20 @@ class DecodeStep:
     def run(self, ev=None):
         i, dm = self.inp, self.dm
         # the new token's latent: slot seq_lens - 1 (the query's own slot without a window)
-        lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, self.enc_pos, i["w_down_k"], i["w_down_v"],
-                   i["mu_k"], i["mu_v"], i["cache_k"], i["cache_v"], self.ws)
+        if self.paged:
+            lla.encode_paged(dm, i["x_k"], i["x_v"], self.seq_idx, self.enc_pos, i["w_down_k"], i["w_down_v"],
+                             i["mu_k"], i["mu_v"], self.pool_k, self.pool_v, self.block_table, self.paged, self.ws)
+        else:
+            lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, self.enc_pos, i["w_down_k"], i["w_down_v"],
+                       i["mu_k"], i["mu_v"], i["cache_k"], i["cache_v"], self.ws)
         for t in range(self.w.T):
             if ev is not None:
                 ev[0][t].record()
-            if self.decoupled:
+            if self.paged:
+                lla.decode_attn_paged(dm, t, self.q[t], self.pool_k, self.pool_v, self.block_table, self.paged,
+                                      i["seq_lens"], i["q_pos"], i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"],
+                                      self.cos, self.sin, self.out[t], self.lse[t], self.ws)
+            elif self.decoupled:
                 lla.decode_attn_decoupled(dm, t, self.q[t], i["cache_k"], i["cache_v"], self.k_rope,
                                           i["seq_lens"], i["q_pos"], i["w_up_k"], i["w_up_v"], i["mu_k"],
                                           i["mu_v"], self.cos_r, self.sin_r, self.out[t], self.lse[t], self.dws)
@@ -194,6 +231,24 @@ class DecodeStep:
                                 i["q_pos"], self.cos, self.sin, self.out[t], self.lse[t], self.ws)
                 if ev is not None:
                     ev[2][t].record()
+
+    def dense_view(self, nseq):
+        """(cache_k, cache_v) of the first nseq sequences as dense [nseq][H][L_max][r]
+        tensors (gathered from the pages when the cache is paged)."""
+        if not self.paged:
+            return self.inp["cache_k"][:nseq], self.inp["cache_v"][:nseq]
+        P, w = self.paged, self.w
+        out = []
+        for pool in (self.pool_k, self.pool_v):
+            d = torch.zeros((nseq, w.H, w.L_max, pool.shape[-1]), dtype=pool.dtype, device=pool.device)
+            bt = self.block_table.cpu()
+            for b in range(nseq):
+                for lp in range(bt.shape[1]):
+                    if int(bt[b, lp]) >= 0:
+                        n = min(P, w.L_max - lp * P)
+                        d[b, :, lp * P:lp * P + n] = pool[int(bt[b, lp]), :, :n]
+            out.append(d)
+        return out[0], out[1]
 
     # launches of this library's kernels per step: encode (bias + GEMM) + T x (query
     # images + decode + combine [+ window]); decoupled: query records + decode + combine
@@ -248,7 +303,7 @@ def e2e_run(step: DecodeStep, steps: int):
     return dt, h2d, d2h
 
 
-def oracle_sample(w, inp_dev, q_dev, budget_s=12.0, k_rope=None):
+def oracle_sample(w, inp_dev, q_dev, budget_s=12.0, k_rope=None, dense=None):
     """Time the oracle on the first S sequences (all heads, all loops) of the same
     inputs; S grows from 1 until the run would take about ``budget_s``.  With
     ``k_rope`` it is the decoupled-RoPE decode's oracle."""
@@ -259,7 +314,8 @@ def oracle_sample(w, inp_dev, q_dev, budget_s=12.0, k_rope=None):
     lens = inp_dev["seq_lens"].cpu().numpy()
 
     def run(S, loops):
-        ck, cv = widen(inp_dev["cache_k"][:S]), widen(inp_dev["cache_v"][:S])
+        dk, dv = dense(S) if dense is not None else (inp_dev["cache_k"][:S], inp_dev["cache_v"][:S])
+        ck, cv = widen(dk), widen(dv)
         kr = widen(k_rope[:S]) if k_rope is not None else None
         t0 = time.perf_counter()
         for t in range(loops):
@@ -282,7 +338,8 @@ def run_ours(args, dist_on, rank, world, device):
     w = WORKLOADS[args.workload]
     lla_build.build()
     lla.lib()
-    step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device, window=args.window, decoupled=args.decoupled)
+    step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device, window=args.window, decoupled=args.decoupled,
+                      paged=args.paged)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -338,7 +395,8 @@ def run_ours(args, dist_on, rank, world, device):
                                  if small else (DECODE_SRC, TRAFFIC_SRC_SHA, TRAFFIC_PER_TOKEN_HEAD))
         with open(src_file, "rb") as f:
             same_src = sha is not None and hashlib.sha256(f.read()).hexdigest().startswith(sha)
-        traffic = per_th * step.tokens * w.H if same_src else None
+        # (the counters were taken on the dense cache; a paged run reports none)
+        traffic = per_th * step.tokens * w.H if same_src and not args.paged else None
         kern = "decode_small_kernel" if small else "decode_bf16_kernel"
         zk = "decode_small_z_kernel" if small else "decode_z_kernel"
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -390,13 +448,14 @@ def run_ours(args, dist_on, rank, world, device):
         "config": {"workload": w.name, "variant": "LLA-2D" if w.variant else "per-head",
                    **({"exact_window": args.window} if args.window > 0 else {}),
                    **({"decoupled_rope": D_ROPE} if args.decoupled else {}),
+                   **({"paged": {"page_size": args.paged, "pages_shuffled": True}} if args.paged else {}),
                    "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
                    "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi],
                    "latent_tokens_per_gpu": step.tokens, "parallelism": "dp%d" % world,
                    "step": "lla_encode of %d new tokens + %s for loops 1..%d" % (
                        w.B, "lla_decode_attn_decoupled" if args.decoupled else "lla_decode_attn", T),
                    "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
-                       step.inp["cache_k"].numel() * 2 * (1 + w.r_v / w.r_k) / 1e9)},
+                       w.B * w.H * w.L_max * (w.r_k + w.r_v) * 2 / 1e9)},
         "roofline": roof,
         **({"window": win} if win else {}),
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -405,7 +464,8 @@ def run_ours(args, dist_on, rank, world, device):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = oracle_sample(w, step.inp, step.q,
-                                            k_rope=step.k_rope if args.decoupled else None)
+                                            k_rope=step.k_rope if args.decoupled else None,
+                                            dense=step.dense_view)
     return res
 
 
@@ -451,11 +511,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--window", type=int, default=0,
                     help="also run lla_window_attn over an exact window of this many newest tokens")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="keep the cache in shuffled pages of this many tokens (lla_decode_attn_paged)")
     ap.add_argument("--decoupled", action="store_true",
                     help="decode with lla_decode_attn_decoupled (64 rotary dimensions per token-head)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.paged and (args.decoupled or WORKLOADS[args.workload].variant != 0):
+        ap.error("--paged takes the per-head decode only")
     if args.decoupled and args.window > 0:
         ap.error("--decoupled and --window do not combine (the window call takes d-wide queries)")
 

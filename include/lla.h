@@ -148,6 +148,52 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
                            float* out, float* lse,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/* A paged per-head latent cache (device), as the page tables of "Enabling
+ * dynamic computation in Looped LMs" (arXiv 2610.09013, §"Ragged KV" and
+ * Appendix A.1 "Page-table aliases for compact K/V storage"): a pool of physical
+ * pages and a logical-to-physical table per sequence.
+ *   k, v         device  pools [num_pages][H][page_size][r_k / r_v]
+ *   block_table  device  int32 [B][max_pages]: logical page p of sequence b
+ *                        (tokens p*page_size .. (p+1)*page_size-1) is physical
+ *                        page block_table[b*max_pages + p]; several entries may
+ *                        name the same page (aliased reads)
+ * The logical capacity per sequence is L_max = max_pages * page_size.  Only the
+ * entries of pages that hold written or read tokens are looked at; an entry
+ * outside [0, num_pages) records LLA_ERR_DEVICE_ARG (reads then use page 0,
+ * writes are skipped), so no access leaves the pool.  Per-head variant only;
+ * the bf16 kernels need page_size to be a multiple of 128 (a 128-token tile
+ * never straddles pages), the fp32 mode takes any page_size >= 1. */
+typedef struct {
+    void* k;
+    void* v;
+    const int32_t* block_table;
+    int B;
+    int max_pages;
+    int page_size;
+    int64_t num_pages;
+} lla_paged_cache;
+
+/*
+ * lla_encode_paged / lla_decode_attn_paged — lla_encode and lla_decode_attn over
+ * a paged cache: token j of (sequence b, head h) lives in row j mod page_size of
+ * head h of page block_table[b][j / page_size].  Every other argument, result
+ * and rule is that of the dense call with L_max = max_pages * page_size (the
+ * workspace is lla_workspace_size(dims, B, max_pages * page_size, N)).
+ * LLA_ERR_UNSUPPORTED: LLA-2D, or bf16 with page_size not a multiple of 128.
+ */
+lla_status lla_encode_paged(const lla_dims* dims, const void* x_k, const void* x_v, int N,
+                            const int32_t* seq_idx, const int32_t* pos,
+                            const void* w_down_k, const void* w_down_v,
+                            const float* mu_k, const float* mu_v,
+                            lla_paged_cache cache, void* workspace, size_t ws_bytes, void* stream);
+lla_status lla_decode_attn_paged(const lla_dims* dims, int loop_t, const void* q,
+                                 lla_paged_cache cache, const int32_t* seq_lens, const int32_t* q_pos,
+                                 const void* w_up_k, const void* w_up_v,
+                                 const float* mu_k, const float* mu_v,
+                                 const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                                 float* out, float* lse,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
 /*
  * lla_window_attn — exact attention over each sequence's window of recent
  * tokens, merged into a latent-store result ("Hybrid Latent Attention for Looped

@@ -202,11 +202,45 @@ lla_status lla_device_status(void* workspace, void* stream, int clear) {
   return static_cast<lla_status>(v);
 }
 
-lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_cache cache,
-                           const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
-                           const void* w_up_v, const float* mu_k, const float* mu_v,
-                           const float* rope_cos, const float* rope_sin, int64_t rope_len, float* out,
-                           float* lse, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The cache a call reads or writes: dense [B][H][L_max][r] rows, or a page pool
+// [num_pages][H][page_size][r] with a block table (L_max = max_pages * page_size).
+struct CacheView {
+  void* k;
+  void* v;
+  int B;
+  int64_t L_max;
+  const int32_t* bt;
+  int page_size;
+  int max_pages;
+  int64_t num_pages;
+};
+
+CacheView dense_view(const lla_cache& c) { return CacheView{c.k, c.v, c.B, c.L_max, nullptr, 0, 0, 0}; }
+
+// Host checks of a paged cache description; LLA_OK also for B == 0.
+lla_status paged_view(const lla_dims* dims, const lla_paged_cache& c, CacheView* v) {
+  if (c.B < 0 || c.max_pages < 1 || c.page_size < 1 || c.num_pages < 1) return LLA_ERR_INVALID_ARG;
+  if (dims->variant != LLA_PER_HEAD) return LLA_ERR_UNSUPPORTED;
+  if (dims->dtype == LLA_BF16 && c.page_size % kTile != 0) return LLA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(c.max_pages) * c.page_size > (int64_t(1) << 30) ||
+      c.num_pages * static_cast<int64_t>(dims->H) >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(c.B) * c.max_pages >= (int64_t(1) << 31))
+    return LLA_ERR_UNSUPPORTED;
+  if (c.B > 0 && (!c.block_table || (reinterpret_cast<uintptr_t>(c.block_table) & 3u) != 0)) return LLA_ERR_INVALID_ARG;
+  *v = CacheView{c.k, c.v, c.B, static_cast<int64_t>(c.max_pages) * c.page_size, c.block_table, c.page_size,
+                 c.max_pages, c.num_pages};
+  return LLA_OK;
+}
+
+lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const CacheView& cache,
+                       const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
+                       const void* w_up_v, const float* mu_k, const float* mu_v,
+                       const float* rope_cos, const float* rope_sin, int64_t rope_len, float* out,
+                       float* lse, void* workspace, size_t ws_bytes, void* stream) {
   lla_status st = check_dims(dims);
   if (st != LLA_OK) return st;
   if (loop_t < 0 || loop_t >= dims->T || cache.B < 0 || cache.L_max < 1) return LLA_ERR_INVALID_ARG;
@@ -284,6 +318,10 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   a.q_pos = q_pos;
   a.cache_k = cache.k;
   a.cache_v = cache.v;
+  a.block_table = cache.bt;
+  a.page_size = cache.page_size;
+  a.max_pages = cache.max_pages;
+  a.num_pages = cache.num_pages;
   a.w_up_k = static_cast<const uint8_t*>(w_up_k) + static_cast<size_t>(loop_t) * H * d * dims->r_k * esize;
   a.w_up_v = static_cast<const uint8_t*>(w_up_v) + static_cast<size_t>(loop_t) * H * d * dims->r_v * esize;
   const size_t mu_loop = dims->variant == LLA_2D ? static_cast<size_t>(H) * d : d;
@@ -305,7 +343,10 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   if (sms <= 0) return LLA_ERR_CUDA;
   a.combine_units = decode_combine_units(cache.B, H, sms);
   a.records_per_cta = kRecordsPerCta;
-  const uint64_t rows = static_cast<uint64_t>(cache.L_max), units = static_cast<uint64_t>(cache.B) * H;
+  // 3-D maps over the dense cache (rows L_max, z = b H + h) or the page pool (rows
+  // page_size, z = page H + h)
+  const uint64_t rows = static_cast<uint64_t>(cache.bt ? cache.page_size : cache.L_max);
+  const uint64_t units = cache.bt ? static_cast<uint64_t>(cache.num_pages) * H : static_cast<uint64_t>(cache.B) * H;
   if (small_path(dims)) {
     // small ranks: positions split over the CTAs, every head of a position in one CTA
     make_decode_small_plan(H, dims->r_k, dims->r_v, &a.splan);
@@ -331,6 +372,32 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_
   if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 32, kTile, 1))
     return LLA_ERR_CUDA;
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q, lla_cache cache,
+                           const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
+                           const void* w_up_v, const float* mu_k, const float* mu_v,
+                           const float* rope_cos, const float* rope_sin, int64_t rope_len, float* out,
+                           float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  return decode_impl(dims, loop_t, q, dense_view(cache), seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v, rope_cos,
+                     rope_sin, rope_len, out, lse, workspace, ws_bytes, stream);
+}
+
+lla_status lla_decode_attn_paged(const lla_dims* dims, int loop_t, const void* q, lla_paged_cache cache,
+                                 const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
+                                 const void* w_up_v, const float* mu_k, const float* mu_v,
+                                 const float* rope_cos, const float* rope_sin, int64_t rope_len, float* out,
+                                 float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  lla_status st = check_dims(dims);
+  if (st != LLA_OK) return st;
+  CacheView v{};
+  if ((st = paged_view(dims, cache, &v)) != LLA_OK) return st;
+  return decode_impl(dims, loop_t, q, v, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v, rope_cos, rope_sin,
+                     rope_len, out, lse, workspace, ws_bytes, stream);
 }
 
 size_t lla_decoupled_workspace_size(const lla_dims* dims, int d_rope, int B, int64_t L_max) {
@@ -449,9 +516,13 @@ lla_status lla_window_attn(const lla_dims* dims, int B, int W, const void* q, co
              : LLA_ERR_CUDA;
 }
 
-lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, int N, const int32_t* seq_idx,
-                      const int32_t* pos, const void* w_down_k, const void* w_down_v, const float* mu_k,
-                      const float* mu_v, lla_cache cache, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+lla_status encode_impl(const lla_dims* dims, const void* x_k, const void* x_v, int N, const int32_t* seq_idx,
+                       const int32_t* pos, const void* w_down_k, const void* w_down_v, const float* mu_k,
+                       const float* mu_v, const CacheView& cache, void* workspace, size_t ws_bytes, void* stream) {
   lla_status st = check_dims(dims);
   if (st != LLA_OK) return st;
   if (N < 0 || cache.B < 0 || cache.L_max < 1) return LLA_ERR_INVALID_ARG;
@@ -481,6 +552,10 @@ lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, in
   a.mu_v = mu_v;
   a.cache_k = cache.k;
   a.cache_v = cache.v;
+  a.block_table = cache.bt;
+  a.page_size = cache.page_size;
+  a.max_pages = cache.max_pages;
+  a.num_pages = cache.num_pages;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.bias = reinterpret_cast<float*>(ws + wl.bias);
@@ -503,6 +578,29 @@ lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, in
     if (!make_map_3d(&m.wv[chunk_map_index(w)], w_down_v, BF, 2, a.r_v, a.Td, a.H, w, 64, 1)) return LLA_ERR_CUDA;
   }
   return launch_encode_bf16(a, plan, m, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+lla_status lla_encode(const lla_dims* dims, const void* x_k, const void* x_v, int N, const int32_t* seq_idx,
+                      const int32_t* pos, const void* w_down_k, const void* w_down_v, const float* mu_k,
+                      const float* mu_v, lla_cache cache, void* workspace, size_t ws_bytes, void* stream) {
+  return encode_impl(dims, x_k, x_v, N, seq_idx, pos, w_down_k, w_down_v, mu_k, mu_v, dense_view(cache), workspace,
+                     ws_bytes, stream);
+}
+
+lla_status lla_encode_paged(const lla_dims* dims, const void* x_k, const void* x_v, int N, const int32_t* seq_idx,
+                            const int32_t* pos, const void* w_down_k, const void* w_down_v, const float* mu_k,
+                            const float* mu_v, lla_paged_cache cache, void* workspace, size_t ws_bytes,
+                            void* stream) {
+  lla_status st = check_dims(dims);
+  if (st != LLA_OK) return st;
+  CacheView v{};
+  if ((st = paged_view(dims, cache, &v)) != LLA_OK) return st;
+  return encode_impl(dims, x_k, x_v, N, seq_idx, pos, w_down_k, w_down_v, mu_k, mu_v, v, workspace, ws_bytes,
+                     stream);
 }
 
 }  // extern "C"

@@ -76,6 +76,31 @@ __device__ __forceinline__ int clamp_len(int L, int64_t L_max) {
   return L < 0 ? 0 : (L > L_max ? static_cast<int>(L_max) : L);
 }
 
+// TMA coordinates (y, z) of tile t of (sequence b, head h) in the 3-D latent maps:
+// rows y within z = b H + h of the dense cache, or, paged (page_size a multiple of
+// the tile), rows within z = page H + h of the pool.
+__device__ __forceinline__ void tile_yz(const DecodeArgs& a, int b, int h, int t, int& y, int& z) {
+  if (a.block_table == nullptr) {
+    z = b * a.H + h;
+    y = t * kTile;
+    return;
+  }
+  const int j = t * kTile, lp = j / a.page_size;
+  int pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + lp);
+  if (pg < 0 || pg >= a.num_pages) {
+    record_status(a.status, LLA_ERR_DEVICE_ARG);
+    pg = 0;
+  }
+  z = pg * a.H + h;
+  y = j - lp * a.page_size;
+}
+
+// Row of token j of unit (b, h) for the fp32 kernels (LLA-2D: one latent per token).
+__device__ __forceinline__ int64_t f32_row(const DecodeArgs& a, int b, int h, int64_t j) {
+  if (a.shared_latent) return static_cast<int64_t>(b) * a.L_max + j;
+  return latent_row(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max, a.H, b, h, j, a.status);
+}
+
 __device__ __forceinline__ void walker_advance(Walker& w, const DecodeArgs& a) {
   if (++w.t < w.nb) return;
   w.t = 0;
@@ -196,6 +221,7 @@ __global__ void __launch_bounds__(kZThreads) decode_z_kernel(const __grid_consta
   }
 }
 
+template <bool kPaged>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ DecodeMaps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -334,7 +360,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           if (!mbar_wait(bar(misc->kempty[sk]), kr.phase ^ 1u, abort, a.status)) break;
           const uint32_t kb = bar(misc->kfull[sk]);
           mbar_arrive_expect_tx(kb, P.kplan.bytes);
-          const int z = wk.b * a.H + wk.h, y = wk.t * kTile;
+          int y = wk.t * kTile, z = wk.b * a.H + wk.h;
+          if constexpr (kPaged) tile_yz(a, wk.b, wk.h, wk.t, y, z);
           for (int c = 0; c < P.kplan.n; ++c)
             tma_load_3d(k_ring + sk * P.k_stage + P.kplan.off[c], &maps.k[chunk_map_index(P.kplan.width[c])],
                         kb, P.kplan.start[c], y, z);
@@ -349,7 +376,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           const uint32_t vb = bar(misc->vfull[sv]);
           mbar_arrive_expect_tx(vb, P.vplan.bytes);
           const uint32_t vs = v_ring + sv * P.v_stage;
-          const int z = wv.b * a.H + wv.h, y = wv.t * kTile;
+          int y = wv.t * kTile, z = wv.b * a.H + wv.h;
+          if constexpr (kPaged) tile_yz(a, wv.b, wv.h, wv.t, y, z);
           for (int c = 0; c < P.vplan.n; ++c) tma_load_3d(vs + P.vplan.off[c], &maps.v, vb, P.vplan.start[c], y, z);
           issued_v = j + 1;
           vr.next(P.SV);
@@ -741,11 +769,11 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
         const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
         const int rs = a.r_v + kRecordHead;
         const long long u = static_cast<long long>(b) * a.H + h;
-        const int R = a.records_per_cta;
+        const int R = a.records_per_cta, rsh = R == 4 ? 2 : 0;   // R is 4 or 1
         const long long base = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * R : (u + c0) * R;
         const long long cstride = a.pos_major ? static_cast<long long>(R) * a.H : R;
         // record r of the unit: CTA c0 + r / R, warp r % R
-        auto rec_at = [&](int r) { return a.partials + (base + (r / R) * cstride + r % R) * rs; };
+        auto rec_at = [&](int r) { return a.partials + (base + (r >> rsh) * cstride + (r & (R - 1))) * rs; };
         // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
         // the unit in that CTA wrote m = -inf, l = 0, acc = 0
         const int nrec = R * (c1 - c0 + 1);
@@ -848,10 +876,11 @@ decode_f32_scores_kernel(const __grid_constant__ DecodeArgs a) {
     qrot[i0] = qv[i0] * c - qv[i1] * s;
     qrot[i1] = qv[i0] * s + qv[i1] * c;
   }
-  const int64_t cu = a.shared_latent ? b : u;   // LLA-2D: every head reads the sequence's latent
-  const float* C = static_cast<const float*>(a.cache_k) + (cu * a.L_max + j0) * a.r_k;
+  // token rows j0.. of the unit (paged: possibly across pages; LLA-2D: every head
+  // reads the sequence's latent); rows past L are not read
+  const float* C = static_cast<const float*>(a.cache_k);
   const float* W = static_cast<const float*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
-  const int rows = min(kTile, static_cast<int>(a.L_max - j0));
+  const int rows = min(kTile, L - j0);
   float kh[kHeadDim];
 #pragma unroll
   for (int e = 0; e < kHeadDim; ++e) kh[e] = 0.f;
@@ -860,7 +889,7 @@ decode_f32_scores_kernel(const __grid_constant__ DecodeArgs a) {
     __syncthreads();
     for (int idx = tid; idx < kTile * 32; idx += 128) {
       const int r = idx / 32, k = idx % 32;
-      ct[r][k] = (r < rows && k < kw) ? C[static_cast<int64_t>(r) * a.r_k + k0 + k] : 0.f;
+      ct[r][k] = (r < rows && k < kw) ? C[f32_row(a, b, h, j0 + r) * a.r_k + k0 + k] : 0.f;
       wt[r][k] = (k < kw) ? W[static_cast<int64_t>(r) * a.r_k + k0 + k] : 0.f;
     }
     __syncthreads();
@@ -922,11 +951,10 @@ decode_f32_values_kernel(const __grid_constant__ DecodeArgs a) {
     z += p;
   }
   z = block_reduce(z, red, false);   // also orders the p writes before the reads below
-  const float* Cv =
-      static_cast<const float*>(a.cache_v) + static_cast<int64_t>(a.shared_latent ? b : u) * a.L_max * a.r_v;
+  const float* Cv = static_cast<const float*>(a.cache_v);
   if (tid < a.r_v) {
     float v = 0.f;
-    for (int j = 0; j < L; ++j) v = fmaf(sc[j], Cv[static_cast<int64_t>(j) * a.r_v + tid], v);
+    for (int j = 0; j < L; ++j) v = fmaf(sc[j], Cv[f32_row(a, b, h, j) * a.r_v + tid], v);
     accs[tid] = v;
   }
   __syncthreads();
@@ -988,12 +1016,14 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
 }
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s) {
-  static int configured = 0;
-  if (configured < a.plan.bytes) {
-    cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         a.plan.bytes);
+  // the dense-cache instantiation carries no page lookup in its producer
+  const bool paged = a.block_table != nullptr;
+  auto kern = paged ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
+  static int configured[2] = {0, 0};
+  if (configured[paged] < a.plan.bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.plan.bytes);
     if (e != cudaSuccess) return e;
-    configured = a.plan.bytes;
+    configured[paged] = a.plan.bytes;
   }
   decode_z_kernel<<<a.B * a.H, kZThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
@@ -1010,7 +1040,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cuda
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a, maps);
+  e = cudaLaunchKernelEx(&cfg, kern, a, maps);
   if (e != cudaSuccess) return e;
   return launch_decode_combine(a, s);
 }

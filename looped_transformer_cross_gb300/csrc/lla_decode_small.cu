@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid
   if (amax > kF16Max) record_status(a.status, LLA_ERR_RANGE);   // (NaN queries stay NaN, as on every path)
 }
 
-template <int RK, int RV>
+template <int RK, int RV, bool kPaged>
 __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int KB = RK * 2, VB = RV * 2; // bytes of a latent K / V row
   constexpr int LPR = RV / 4;             // value step: lanes per V row, 4 columns each
@@ -367,12 +367,21 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
           ++run;
         }
         const uint32_t rows = static_cast<uint32_t>(min(kTile, w.L - w.t * kTile));
+        // rows of head h: (z0 + h) * zrows + y0 (dense: z0 = b H; paged: the tile's page)
+        int64_t z0 = static_cast<int64_t>(w.b) * H, zrows = a.L_max, y0 = static_cast<int64_t>(w.t) * kTile;
+        if constexpr (kPaged) {
+          const int64_t row = latent_row(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max, H, w.b, 0,
+                                         y0, a.status);
+          zrows = a.page_size;
+          z0 = row / zrows;
+          y0 = row - z0 * zrows;
+        }
         for (int h = 0; h < H && ok; ++h) {
           if (!(ok = mbar_wait(bar(misc->empty[sp.slot]), sp.phase ^ 1u, abort, a.status))) break;
           const uint32_t fb = bar(misc->full[sp.slot]);
           mbar_arrive_expect_tx(fb, rows * (KB + VB));
           const uint32_t dst = sbase + P.ring + sp.slot * P.slot;
-          const int64_t r0 = (static_cast<int64_t>(w.b) * H + h) * a.L_max + static_cast<int64_t>(w.t) * kTile;
+          const int64_t r0 = (z0 + h) * zrows + y0;
           bulk_load(dst, static_cast<const uint8_t*>(a.cache_k) + r0 * KB, rows * KB, fb);
           bulk_load(dst + P.k_tile, static_cast<const uint8_t*>(a.cache_v) + r0 * VB, rows * VB, fb);
           ++issued;
@@ -636,12 +645,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
 
 template <int RK, int RV>
 cudaError_t launch_small_instance(const DecodeArgs& a, cudaStream_t s) {
-  static int configured = 0;
-  if (configured < a.splan.bytes) {
-    cudaError_t e = cudaFuncSetAttribute(decode_small_kernel<RK, RV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         a.splan.bytes);
+  // the dense-cache instantiation carries no page lookup in its producer
+  const bool paged = a.block_table != nullptr;
+  auto kern = paged ? decode_small_kernel<RK, RV, true> : decode_small_kernel<RK, RV, false>;
+  static int configured[2] = {0, 0};
+  if (configured[paged] < a.splan.bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.splan.bytes);
     if (e != cudaSuccess) return e;
-    configured = a.splan.bytes;
+    configured[paged] = a.splan.bytes;
   }
   const int trig_blocks = static_cast<int>((a.trig_rows + kTrigRowsPerBlock - 1) / kTrigRowsPerBlock);
   const int z_blocks = a.H * ((a.B + kZSeqs - 1) / kZSeqs);
@@ -660,7 +671,7 @@ cudaError_t launch_small_instance(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_small_kernel<RK, RV>, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace

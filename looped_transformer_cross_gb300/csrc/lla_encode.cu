@@ -170,10 +170,13 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
         p = __ldg(a.pos + n);
         if (!slot_ok(a, sid, p)) record_status(a.status, LLA_ERR_DEVICE_ARG);
       }
-      const bool write = n < a.N && slot_ok(a, sid, p);
+      const int64_t drow = n < a.N && slot_ok(a, sid, p)
+                               ? latent_row_for_write(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max,
+                                                      a.H, sid, h, p, a.status)
+                               : -1;
+      const bool write = drow >= 0;
       const float* bias = a.bias + (static_cast<int64_t>(axis) * a.H + h) * 256;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(axis == 0 ? a.cache_k : a.cache_v) +
-                           ((static_cast<int64_t>(write ? sid : 0) * a.H + h) * a.L_max + (write ? p : 0)) * r;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(axis == 0 ? a.cache_k : a.cache_v) + (write ? drow : 0) * r;
       for (int c0 = 0; c0 < r; c0 += 16) {
         float v[16];
         tmem_ld_x16(tmem + lane_base + c0, v);   // every lane of the warp takes part
@@ -217,8 +220,11 @@ __global__ void __launch_bounds__(256) encode_f32_kernel(const __grid_constant__
   const float* W = static_cast<const float*>(axis == 0 ? a.w_down_k : a.w_down_v) + static_cast<int64_t>(h) * a.Td * r;
   float s = 0.f;
   for (int u = 0; u < a.Td; ++u) s = fmaf(x[u] - mu[u], W[static_cast<int64_t>(u) * r + k], s);
+  const int64_t row =
+      latent_row_for_write(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max, a.H, sid, h, p, a.status);
+  if (row < 0) return;
   float* dst = static_cast<float*>(axis == 0 ? a.cache_k : a.cache_v);
-  dst[((static_cast<int64_t>(sid) * a.H + h) * a.L_max + p) * r + k] = s;
+  dst[row * r + k] = s;
 }
 
 }  // namespace

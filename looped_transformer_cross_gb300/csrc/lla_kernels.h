@@ -84,6 +84,13 @@ struct DecodeArgs {
   const void* k_rope;                // decoupled path: rotary keys [B][H][L_max][d_rope]
   int d_rope;                        // decoupled path: rotary branch width (0: full-RoPE path)
   int ring_slots;                    // decoupled path: slots of the key ring
+  // Paged cache (per-head variant): cache_k / cache_v are page pools
+  // [num_pages][H][page_size][r]; logical page p of sequence b is physical page
+  // block_table[b * max_pages + p].  block_table == nullptr: dense [B][H][L_max][r].
+  const int32_t* block_table;
+  int page_size;
+  int max_pages;
+  int64_t num_pages;
   DecodePlan plan;
   DecodeSmallPlan splan;
 };
@@ -208,6 +215,10 @@ struct EncodeArgs {
   void* cache_v;
   uint32_t* status;
   float* bias;                       // workspace [2][H][256]: mu W_down per head/axis
+  const int32_t* block_table;        // paged cache (as DecodeArgs), or nullptr
+  int page_size;
+  int max_pages;
+  int64_t num_pages;
 };
 
 struct EncodePlan {

@@ -23,6 +23,38 @@ __device__ __forceinline__ void record_status(uint32_t* status, uint32_t code) {
   if (status) atomicCAS(status, 0u, code);
 }
 
+// Row of token j of (sequence b, head h) in a per-head latent cache: dense rows
+// [B][H][L_max], or, with a block table `bt` [B][max_pages], a page pool
+// [num_pages][H][page_size] in which logical page j / page_size of sequence b is
+// physical page bt[b][j / page_size].  A physical page outside [0, num_pages)
+// records LLA_ERR_DEVICE_ARG and stands in page 0, so no access leaves the pool.
+__device__ __forceinline__ int64_t latent_row(const int32_t* bt, int page_size, int max_pages, int64_t num_pages,
+                                              int64_t L_max, int H, int b, int h, int64_t j, uint32_t* status) {
+  if (bt == nullptr) return (static_cast<int64_t>(b) * H + h) * L_max + j;
+  const int64_t lp = j / page_size;
+  int pg = __ldg(bt + static_cast<int64_t>(b) * max_pages + lp);
+  if (pg < 0 || pg >= num_pages) {
+    record_status(status, LLA_ERR_DEVICE_ARG);
+    pg = 0;
+  }
+  return (static_cast<int64_t>(pg) * H + h) * page_size + (j - lp * page_size);
+}
+
+// As latent_row, for writers: an out-of-range physical page records
+// LLA_ERR_DEVICE_ARG and returns -1 (the caller skips the write).
+__device__ __forceinline__ int64_t latent_row_for_write(const int32_t* bt, int page_size, int max_pages,
+                                                        int64_t num_pages, int64_t L_max, int H, int b, int h,
+                                                        int64_t j, uint32_t* status) {
+  if (bt == nullptr) return (static_cast<int64_t>(b) * H + h) * L_max + j;
+  const int64_t lp = j / page_size;
+  const int pg = __ldg(bt + static_cast<int64_t>(b) * max_pages + lp);
+  if (pg < 0 || pg >= num_pages) {
+    record_status(status, LLA_ERR_DEVICE_ARG);
+    return -1;
+  }
+  return (static_cast<int64_t>(pg) * H + h) * page_size + (j - lp * page_size);
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

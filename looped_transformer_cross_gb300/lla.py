@@ -38,6 +38,12 @@ class Cache(ctypes.Structure):
                 ("L_max", ctypes.c_int64)]
 
 
+class PagedCache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("B", ctypes.c_int), ("max_pages", ctypes.c_int), ("page_size", ctypes.c_int),
+                ("num_pages", ctypes.c_int64)]
+
+
 class LLAError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
@@ -78,6 +84,12 @@ def lib():
             L.lla_decode_attn_decoupled.argtypes = [pd, ctypes.c_int, ctypes.c_int, vp, Cache, vp, i32p, i32p, vp, vp,
                                                     fp, fp, fp, fp, ctypes.c_int64, fp, fp, vp, ctypes.c_size_t, vp]
             L.lla_decode_attn_decoupled.restype = ctypes.c_int
+            L.lla_encode_paged.argtypes = [pd, vp, vp, ctypes.c_int, i32p, i32p, vp, vp, fp, fp, PagedCache,
+                                           vp, ctypes.c_size_t, vp]
+            L.lla_encode_paged.restype = ctypes.c_int
+            L.lla_decode_attn_paged.argtypes = [pd, ctypes.c_int, vp, PagedCache, i32p, i32p, vp, vp, fp, fp,
+                                                fp, fp, ctypes.c_int64, fp, fp, vp, ctypes.c_size_t, vp]
+            L.lla_decode_attn_paged.restype = ctypes.c_int
             L.lla_decode_kernel.argtypes = [pd]
             L.lla_decode_kernel.restype = ctypes.c_char_p
             L.lla_abi_version.argtypes = []
@@ -166,6 +178,40 @@ def decode_attn(dm: Dims, loop_t: int, q, cache_k, cache_v, seq_lens, q_pos, w_u
                                _ptr(lse), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "lla_decode_attn")
+
+
+def paged_cache(pool_k, pool_v, block_table, page_size: int) -> PagedCache:
+    """The lla_paged_cache of pools [num_pages][H][page_size][r] and a block table
+    [B][max_pages] (int32, device)."""
+    B, max_pages = int(block_table.shape[0]), int(block_table.shape[1])
+    return PagedCache(ctypes.c_void_p(pool_k.data_ptr()), ctypes.c_void_p(pool_v.data_ptr()),
+                      ctypes.c_void_p(block_table.data_ptr()), B, max_pages, int(page_size),
+                      int(pool_k.shape[0]))
+
+
+def encode_paged(dm: Dims, x_k, x_v, seq_idx, pos, w_down_k, w_down_v, mu_k, mu_v, pool_k, pool_v,
+                 block_table, page_size: int, workspace, stream=None):
+    """lla_encode_paged: latents of N tokens into paged slots (seq_idx[n], pos[n])."""
+    N = int(seq_idx.shape[0])
+    st = lib().lla_encode_paged(ctypes.byref(dm), _ptr(x_k), _ptr(x_v), N, _ptr(seq_idx), _ptr(pos),
+                                _ptr(w_down_k), _ptr(w_down_v), _ptr(mu_k), _ptr(mu_v),
+                                paged_cache(pool_k, pool_v, block_table, page_size),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "lla_encode_paged")
+
+
+def decode_attn_paged(dm: Dims, loop_t: int, q, pool_k, pool_v, block_table, page_size: int, seq_lens,
+                      q_pos, w_up_k, w_up_v, mu_k, mu_v, rope_cos, rope_sin, out, lse, workspace,
+                      stream=None):
+    """lla_decode_attn_paged: lla_decode_attn over a paged cache (pools [num_pages][H][page_size][r],
+    block table [B][max_pages])."""
+    st = lib().lla_decode_attn_paged(ctypes.byref(dm), int(loop_t), _ptr(q),
+                                     paged_cache(pool_k, pool_v, block_table, page_size), _ptr(seq_lens),
+                                     _ptr(q_pos), _ptr(w_up_k), _ptr(w_up_v), _ptr(mu_k), _ptr(mu_v),
+                                     _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]), _ptr(out),
+                                     _ptr(lse), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "lla_decode_attn_paged")
 
 
 def window_attn(dm: Dims, q, k_win, v_win, win_len, win_pos, q_pos, rope_cos, rope_sin, out, lse,

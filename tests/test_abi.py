@@ -146,3 +146,35 @@ def test_window_rejects_bad_arguments_on_host(L):
     assert call(lla.dims(4, 2, 16, 32, d_head=64)) == lla.LLA_ERR_UNSUPPORTED
     assert call(dm, B=0) == lla.LLA_OK                               # nothing to do
     assert call(dm, W=0) == lla.LLA_OK
+
+
+def test_paged_rejects_bad_arguments_on_host(L):
+    """lla_decode_attn_paged / lla_encode_paged: host checks of the page description
+    (no launch)."""
+    tbl = (ctypes.c_int32 * 64)()
+    good_bt = ctypes.c_void_p(ctypes.addressof(tbl))
+
+    def dec(dm, page_size=128, max_pages=4, num_pages=8, B=1, bt=good_bt):
+        cache = lla.PagedCache(None, None, bt, B, max_pages, page_size, num_pages)
+        return L.lla_decode_attn_paged(ctypes.byref(dm), 0, None, cache, None, None, None, None, None, None,
+                                       None, None, 1024, None, None, None, 1 << 20, None)
+
+    def enc(dm, page_size=128):
+        cache = lla.PagedCache(None, None, good_bt, 1, 4, page_size, 8)
+        return L.lla_encode_paged(ctypes.byref(dm), None, None, 4, None, None, None, None, None, None, cache,
+                                  None, 1 << 20, None)
+
+    bf16, f32 = lla.dims(4, 2, 96, 160), lla.dims(4, 2, 96, 160, dtype=lla.LLA_F32)
+    assert dec(bf16, page_size=64) == lla.LLA_ERR_UNSUPPORTED      # bf16 tiles would straddle pages
+    assert dec(bf16, page_size=100) == lla.LLA_ERR_UNSUPPORTED
+    assert enc(bf16, page_size=64) == lla.LLA_ERR_UNSUPPORTED
+    assert dec(lla.dims(4, 2, 96, 160, variant=lla.LLA_2D)) == lla.LLA_ERR_UNSUPPORTED
+    assert dec(bf16, bt=None) == lla.LLA_ERR_INVALID_ARG
+    assert dec(bf16, bt=ctypes.c_void_p(ctypes.addressof(tbl) + 2)) == lla.LLA_ERR_INVALID_ARG
+    assert dec(bf16, max_pages=0) == lla.LLA_ERR_INVALID_ARG
+    assert dec(bf16, num_pages=0) == lla.LLA_ERR_INVALID_ARG
+    assert dec(bf16, page_size=0) == lla.LLA_ERR_INVALID_ARG
+    assert dec(bf16, B=0) == lla.LLA_OK                              # nothing to do
+    # any page size passes the page checks in fp32 mode (then fails on the null pointers)
+    assert dec(f32, page_size=1) == lla.LLA_ERR_INVALID_ARG
+    assert dec(f32, page_size=1, B=0) == lla.LLA_OK
