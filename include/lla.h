@@ -159,8 +159,8 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
  *                        name the same page (aliased reads)
  * The logical capacity per sequence is L_max = max_pages * page_size.  Only the
  * entries of pages that hold written or read tokens are looked at; an entry
- * outside [0, num_pages) records LLA_ERR_DEVICE_ARG (reads then use page 0,
- * writes are skipped), so no access leaves the pool.  Per-head variant only;
+ * outside [0, num_pages) records LLA_ERR_DEVICE_ARG (reads then use a page
+ * inside the pool, writes are skipped), so no access leaves the pool.  Per-head variant only;
  * the bf16 kernels need page_size to be a multiple of 128 (a 128-token tile
  * never straddles pages), the fp32 mode takes any page_size >= 1. */
 typedef struct {

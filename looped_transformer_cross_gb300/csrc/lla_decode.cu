@@ -76,22 +76,11 @@ __device__ __forceinline__ int clamp_len(int L, int64_t L_max) {
   return L < 0 ? 0 : (L > L_max ? static_cast<int>(L_max) : L);
 }
 
-// TMA coordinates (y, z) of tile t of (sequence b, head h) in the 3-D latent maps:
-// rows y within z = b H + h of the dense cache, or, paged (page_size a multiple of
-// the tile), rows within z = page H + h of the pool.
+// TMA coordinates (y, z) of tile t of (sequence b, head h) in the 3-D map over the
+// page pool (page_size a multiple of the tile): rows y within z = page H + h.
 __device__ __forceinline__ void tile_yz(const DecodeArgs& a, int b, int h, int t, int& y, int& z) {
-  if (a.block_table == nullptr) {
-    z = b * a.H + h;
-    y = t * kTile;
-    return;
-  }
   const int j = t * kTile, lp = j / a.page_size;
-  int pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + lp);
-  if (pg < 0 || pg >= a.num_pages) {
-    record_status(a.status, LLA_ERR_DEVICE_ARG);
-    pg = 0;
-  }
-  z = pg * a.H + h;
+  z = page_of(a, b, lp) * a.H + h;
   y = j - lp * a.page_size;
 }
 
@@ -141,6 +130,7 @@ __global__ void __launch_bounds__(kZThreads) decode_z_kernel(const __grid_consta
   const DecodePlan& P = a.plan;
   const int u = blockIdx.x, tid = threadIdx.x;
   const int b = u / a.H, h = u % a.H;
+  if (h == 0) check_block_table(a, b, tid, kZThreads);
   if (clamp_len(__ldg(a.seq_lens + b), a.L_max) == 0) return;
   uint8_t* img = a.zimg + static_cast<int64_t>(u) * a.zimg_stride;
   const __nv_bfloat16* W =

@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid
   }
   const int u = static_cast<int>(blockIdx.x) - ntb;
   const int h = u % a.H, b0 = (u / a.H) * kZSeqs;
+  if (h == 0)
+    for (int sb = 0; sb < kZSeqs && b0 + sb < a.B; ++sb) check_block_table(a, b0 + sb, tid, kSZThreads);
   const int rk = a.r_k, ws = rk + 1;
   const int nwg = a.splan.nwg, N = a.splan.N, hl = h % nwg;
   const __nv_bfloat16* W =
@@ -370,11 +372,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
         // rows of head h: (z0 + h) * zrows + y0 (dense: z0 = b H; paged: the tile's page)
         int64_t z0 = static_cast<int64_t>(w.b) * H, zrows = a.L_max, y0 = static_cast<int64_t>(w.t) * kTile;
         if constexpr (kPaged) {
-          const int64_t row = latent_row(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max, H, w.b, 0,
-                                         y0, a.status);
+          const int lp = static_cast<int>(y0 / a.page_size);
+          z0 = static_cast<int64_t>(page_of(a, w.b, lp)) * H;
           zrows = a.page_size;
-          z0 = row / zrows;
-          y0 = row - z0 * zrows;
+          y0 -= static_cast<int64_t>(lp) * a.page_size;
         }
         for (int h = 0; h < H && ok; ++h) {
           if (!(ok = mbar_wait(bar(misc->empty[sp.slot]), sp.phase ^ 1u, abort, a.status))) break;

@@ -95,6 +95,28 @@ struct DecodeArgs {
   DecodeSmallPlan splan;
 };
 
+// Validation of the block-table entries a paged decode reads: the decode kernels
+// clamp an entry into the pool without checking it, and the query-image kernels
+// (one block per sequence here) record LLA_ERR_DEVICE_ARG for any entry of a
+// logical page holding one of sequence b's tokens that lies outside [0, num_pages).
+__device__ __forceinline__ void check_block_table(const DecodeArgs& a, int b, int tid, int nthreads) {
+  if (a.block_table == nullptr) return;
+  int L = __ldg(a.seq_lens + b);
+  L = L < 0 ? 0 : (L > a.L_max ? static_cast<int>(a.L_max) : L);
+  const int used = (L + a.page_size - 1) / a.page_size;
+  for (int lp = tid; lp < used; lp += nthreads) {
+    const int pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + lp);
+    if (pg < 0 || pg >= a.num_pages) record_status(a.status, LLA_ERR_DEVICE_ARG);
+  }
+}
+
+// Physical page of logical page lp of sequence b for the bf16 decode producers,
+// clamped into the pool (entries were checked by check_block_table).
+__device__ __forceinline__ int page_of(const DecodeArgs& a, int b, int lp) {
+  const int pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + lp);
+  return min(max(pg, 0), static_cast<int>(a.num_pages) - 1);
+}
+
 struct DecodeMaps {
   CUtensorMap k[3];                  // latent K boxes of width 64 / 32 / 16
   CUtensorMap v;                     // latent V boxes of width 32

@@ -186,8 +186,8 @@ def test_paged_encode_layout_exact(dtype, P):
 
 
 def test_paged_out_of_range_page_is_flagged():
-    """A table entry outside [0, num_pages): decode reads page 0 instead and records
-    LLA_ERR_DEVICE_ARG; encode skips the write and records it."""
+    """A table entry outside [0, num_pages): decode reads a page inside the pool
+    instead and records LLA_ERR_DEVICE_ARG; encode skips the write and records it."""
     w = workload(T=2, H=2, r_k=96, r_v=160, B=2, L_max=256)
     lens = [256, 100]
     P = 128
