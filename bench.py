@@ -41,8 +41,8 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 8-sequence variant
 # of the bench layer.  Valid only for the decode source whose sha256 starts with
 # TRAFFIC_SRC_SHA; any other source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = (263.974912e6 + 3.452928e6) / (31042 * 16)
-TRAFFIC_SRC_SHA = "942b4253787d6137"
+TRAFFIC_PER_TOKEN_HEAD = (263.995136e6 + 3.399424e6) / (31042 * 16)
+TRAFFIC_SRC_SHA = "947cdee5130ef540"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D kernel, per latent token (all heads), from the 32-sequence
 # variant of the LLA-2D layer; valid only for the source whose sha256 starts with
@@ -52,8 +52,8 @@ TRAFFIC2D_SRC_SHA = "82da47c747901f36"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
 # Same for decode_small_kernel (the per-head kernel at small ranks), from a capture
 # of the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.888832e6 + 3.641344e6) / (64 * 4096 * 16)
-TRAFFIC_SMALL_SRC_SHA = "6183fa766422f3df"
+TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.847104e6 + 3.685632e6) / (64 * 4096 * 16)
+TRAFFIC_SMALL_SRC_SHA = "5c9c42836764a449"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 # Same for decoupled_bf16_kernel, per latent token-head (latent K and V rows plus the
 # rotary key), from the 8-sequence variant of the rho = 4 layer.
