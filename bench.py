@@ -436,6 +436,56 @@ def run_ours(args, dist_on, rank, world, device):
                             "traffic": None, "kernel": "lla_window_attn (window_attn_kernel)",
                             "algorithmic_bytes_per_launch": wbytes, "peak_source": src}}
 
+    evi = None
+    if args.evict:
+        # token eviction composed with LLA (sink + window budget): lla_evict_window on the
+        # layer (lengths restored before each call, outside the events), then one decode
+        # call per loop over the kept budget
+        sink, window = (int(x) for x in args.evict.split(","))
+        i = step.inp
+        saved = i["seq_lens"].clone()
+        ews = torch.zeros(256, dtype=torch.uint8, device=device)
+        esize = 2 if w.dtype == "bf16" else 4
+        over = [L for L in saved.cpu().tolist() if L > sink + window]
+        units = w.H if w.variant == 0 else 1
+        moved = len(over) * units * window * (w.r_k + w.r_v) * esize * 2
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, min(args.steps, 100))
+        etimes = []
+        for k in range(reps + 3):
+            i["seq_lens"].copy_(saved)
+            e0.record()
+            lla.evict_window(step.dm, i["cache_k"], i["cache_v"], i["seq_lens"], sink, window, ews)
+            e1.record()
+            torch.cuda.synchronize()
+            if k >= 3:
+                etimes.append(e0.elapsed_time(e1) / 1e3)
+        if lla.device_status(ews) != lla.LLA_OK:
+            raise RuntimeError("device status after eviction")
+        t_ev = float(np.mean(etimes))
+        kept = int(i["seq_lens"].sum().item())
+        q_pos_kept = (i["seq_lens"] - 1).clamp(min=0).to(torch.int32)
+        dtimes = []
+        for k in range(reps + 3):
+            e0.record()
+            for t in range(T):
+                lla.decode_attn(step.dm, t, step.q[t], i["cache_k"], i["cache_v"], i["seq_lens"], q_pos_kept,
+                                i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"], step.cos, step.sin, step.out[t],
+                                step.lse[t], step.ws)
+            e1.record()
+            torch.cuda.synchronize()
+            if k >= 3:
+                dtimes.append(e0.elapsed_time(e1) / 1e3 / T)
+        i["seq_lens"].copy_(saved)
+        t_dec = float(np.mean(dtimes))
+        evi = {"sink": sink, "window": window, "sequences_evicted": len(over), "evict_ms": t_ev * 1e3,
+               "roofline": {"bound": "hbm", "achieved": moved / t_ev / 1e9, "peak": hbm, "unit": "GB/s",
+                            "frac": moved / t_ev / 1e9 / hbm, "traffic": None,
+                            "kernel": "lla_evict_window (evict_move_kernel + evict_lens_kernel)",
+                            "algorithmic_bytes_per_launch": moved, "peak_source": src},
+               "decode_over_budget": {"latent_tokens_per_call": kept, "call_ms": t_dec * 1e3,
+                                      "value": kept / t_dec, "unit": UNIT}}
+
     e2e_steps = max(3, min(args.steps, 200))
     e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
     e2e_dt = max_over_ranks(e2e_dt, dist_on, device)
@@ -458,6 +508,7 @@ def run_ours(args, dist_on, rank, world, device):
                        w.B * w.H * w.L_max * (w.r_k + w.r_v) * 2 / 1e9)},
         "roofline": roof,
         **({"window": win} if win else {}),
+        **({"evict": evi} if evi else {}),
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clk.summary(),
@@ -511,6 +562,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--window", type=int, default=0,
                     help="also run lla_window_attn over an exact window of this many newest tokens")
+    ap.add_argument("--evict", default="",
+                    help="SINK,WINDOW: also time lla_evict_window to that budget and decode over it")
     ap.add_argument("--paged", type=int, default=0,
                     help="keep the cache in shuffled pages of this many tokens (lla_decode_attn_paged)")
     ap.add_argument("--decoupled", action="store_true",
@@ -520,6 +573,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.paged and (args.decoupled or WORKLOADS[args.workload].variant != 0):
         ap.error("--paged takes the per-head decode only")
+    if args.evict and (args.paged or args.decoupled):
+        ap.error("--evict runs on the dense cache")
     if args.decoupled and args.window > 0:
         ap.error("--decoupled and --window do not combine (the window call takes d-wide queries)")
 

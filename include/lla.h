@@ -195,6 +195,29 @@ lla_status lla_decode_attn_paged(const lla_dims* dims, int loop_t, const void* q
                                  void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * lla_evict_window — token eviction composed with LLA (LLA paper, Appendix D
+ * "Token-eviction composition table" and Appendix J "Eviction and long-context
+ * prefill"): a StreamingLLM/H2O-style budget keeps each sequence's first `sink`
+ * tokens and its `window` newest, and only their latents stay in the cache.
+ * For every sequence with L = seq_lens[b] > sink + window, the latent rows of
+ * tokens L-window .. L-1 move, in order, to slots sink .. sink+window-1 (every
+ * head, K and V, in place) and seq_lens[b] becomes sink + window; sequences at
+ * or below the budget are untouched.  A later lla_decode_attn rotates slot j at
+ * position j, i.e. positions within the kept cache (StreamingLLM's re-indexing);
+ * the query's position is then its slot in the kept cache.  Rows past the new
+ * length keep stale latents.
+ *   cache      dense cache, as for lla_decode_attn (any variant, dtype)
+ *   seq_lens   device int32 [B], read and rewritten; a length outside
+ *              [0, L_max] is left alone and records LLA_ERR_DEVICE_ARG
+ *   sink, window  >= 0, sink + window >= 1
+ *   workspace  device, >= 256 bytes: the status word
+ * Asynchronous on `stream`; decode calls after it on the same stream see the new
+ * lengths.
+ */
+lla_status lla_evict_window(const lla_dims* dims, lla_cache cache, int32_t* seq_lens, int sink,
+                            int window, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * lla_window_attn — exact attention over each sequence's window of recent
  * tokens, merged into a latent-store result ("Hybrid Latent Attention for Looped
  * Language Models", §3.4 "Exact sliding window", Eq. (4), and Appendix I

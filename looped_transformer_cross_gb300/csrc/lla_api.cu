@@ -481,6 +481,34 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
   return launch_decoupled_bf16(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
+lla_status lla_evict_window(const lla_dims* dims, lla_cache cache, int32_t* seq_lens, int sink, int window,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  lla_status st = check_dims(dims);
+  if (st != LLA_OK) return st;
+  if (cache.B < 0 || cache.L_max < 1 || sink < 0 || window < 0 || sink + window < 1) return LLA_ERR_INVALID_ARG;
+  if (cache.B == 0) return LLA_OK;
+  if (cache.L_max > (int64_t(1) << 30) || static_cast<int64_t>(cache.B) * dims->H > (int64_t(1) << 30))
+    return LLA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {cache.k, cache.v, seq_lens, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LLA_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return LLA_ERR_INVALID_ARG;
+  EvictArgs a{};
+  a.B = cache.B;
+  a.units_per_seq = dims->variant == LLA_2D ? 1 : dims->H;
+  a.r_k = dims->r_k;
+  a.r_v = dims->r_v;
+  a.esize = dims->dtype == LLA_BF16 ? 2 : 4;
+  a.sink = sink;
+  a.window = window;
+  a.L_max = cache.L_max;
+  a.cache_k = cache.k;
+  a.cache_v = cache.v;
+  a.seq_lens = seq_lens;
+  a.status = static_cast<uint32_t*>(workspace);
+  return launch_evict_window(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
 lla_status lla_window_attn(const lla_dims* dims, int B, int W, const void* q, const void* k_win,
                            const void* v_win, const int32_t* win_len, const int32_t* win_pos,
                            const int32_t* q_pos, const float* rope_cos, const float* rope_sin, int64_t rope_len,

@@ -117,6 +117,20 @@ __device__ __forceinline__ int page_of(const DecodeArgs& a, int b, int lp) {
   return min(max(pg, 0), static_cast<int>(a.num_pages) - 1);
 }
 
+// Token eviction (sink + window budget) over a dense latent cache.
+struct EvictArgs {
+  int B;
+  int units_per_seq;                 // H (per-head) or 1 (LLA-2D)
+  int r_k, r_v, esize;
+  int sink, window;
+  int64_t L_max;
+  void* cache_k;                     // [B][units_per_seq][L_max][r] rows
+  void* cache_v;
+  int32_t* seq_lens;                 // [B], updated to sink + window where over budget
+  uint32_t* status;
+};
+cudaError_t launch_evict_window(const EvictArgs& a, cudaStream_t s);
+
 struct DecodeMaps {
   CUtensorMap k[3];                  // latent K boxes of width 64 / 32 / 16
   CUtensorMap v;                     // latent V boxes of width 32

@@ -90,6 +90,8 @@ def lib():
             L.lla_decode_attn_paged.argtypes = [pd, ctypes.c_int, vp, PagedCache, i32p, i32p, vp, vp, fp, fp,
                                                 fp, fp, ctypes.c_int64, fp, fp, vp, ctypes.c_size_t, vp]
             L.lla_decode_attn_paged.restype = ctypes.c_int
+            L.lla_evict_window.argtypes = [pd, Cache, i32p, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+            L.lla_evict_window.restype = ctypes.c_int
             L.lla_decode_kernel.argtypes = [pd]
             L.lla_decode_kernel.restype = ctypes.c_char_p
             L.lla_abi_version.argtypes = []
@@ -212,6 +214,17 @@ def decode_attn_paged(dm: Dims, loop_t: int, q, pool_k, pool_v, block_table, pag
                                      _ptr(lse), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "lla_decode_attn_paged")
+
+
+def evict_window(dm: Dims, cache_k, cache_v, seq_lens, sink: int, window: int, workspace, stream=None):
+    """lla_evict_window: keep each sequence's `sink` first and `window` newest latents
+    (moved in order to slots sink..), rewriting seq_lens in place."""
+    B = int(cache_k.shape[0])
+    L_max = int(cache_k.shape[2] if dm.variant == LLA_PER_HEAD else cache_k.shape[1])
+    cache = Cache(ctypes.c_void_p(cache_k.data_ptr()), ctypes.c_void_p(cache_v.data_ptr()), B, L_max)
+    st = lib().lla_evict_window(ctypes.byref(dm), cache, _ptr(seq_lens), int(sink), int(window), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "lla_evict_window")
 
 
 def window_attn(dm: Dims, q, k_win, v_win, win_len, win_pos, q_pos, rope_cos, rope_sin, out, lse,
