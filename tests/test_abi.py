@@ -178,3 +178,24 @@ def test_paged_rejects_bad_arguments_on_host(L):
     # any page size passes the page checks in fp32 mode (then fails on the null pointers)
     assert dec(f32, page_size=1) == lla.LLA_ERR_INVALID_ARG
     assert dec(f32, page_size=1, B=0) == lla.LLA_OK
+
+
+def test_evict_rejects_bad_arguments_on_host(L):
+    buf = (ctypes.c_char * 1024)()
+    base = ctypes.addressof(buf)
+    p = ctypes.c_void_p(base + (16 - base % 16) % 16)
+    dm = lla.dims(4, 2, 96, 160)
+
+    def call(sink=4, window=256, B=1, ptr=p, ws=256, d=dm):
+        cache = lla.Cache(ptr, ptr, B, 300)
+        return L.lla_evict_window(ctypes.byref(d), cache, ptr, sink, window, ptr, ws, None)
+
+    assert call(sink=-1) == lla.LLA_ERR_INVALID_ARG
+    assert call(window=-1) == lla.LLA_ERR_INVALID_ARG
+    assert call(sink=0, window=0) == lla.LLA_ERR_INVALID_ARG        # an empty budget
+    assert call(B=-1) == lla.LLA_ERR_INVALID_ARG
+    assert call(ptr=None) == lla.LLA_ERR_INVALID_ARG
+    assert call(ptr=ctypes.c_void_p(p.value + 4)) == lla.LLA_ERR_INVALID_ARG
+    assert call(ws=255) == lla.LLA_ERR_INVALID_ARG
+    assert call(d=lla.dims(4, 2, 96, 160, d_head=64)) == lla.LLA_ERR_UNSUPPORTED
+    assert call(B=0) == lla.LLA_OK                                  # nothing to do
