@@ -143,6 +143,12 @@ class DecodeStep:
         self.decoupled = decoupled
         self.paged = paged
         self.inp = make_decode_inputs(w, seed, device=device, with_encode=True)
+        # a workload with a prefill stack (x for every cached position) keeps it aside:
+        # the decode step encodes only each sequence's new token, the first B rows
+        self.prefill_x = None
+        if self.inp["x_k"].shape[0] > w.B:
+            self.prefill_x = (self.inp["x_k"], self.inp["x_v"])
+            self.inp["x_k"], self.inp["x_v"] = self.inp["x_k"][:w.B], self.inp["x_v"][:w.B]
         if window > 0:
             self.win = make_window_inputs(w, window, seed + 5, self.inp["seq_lens"], device=device)
             self.inp["q_pos"] = self.win["q_pos"]
@@ -276,6 +282,44 @@ def sum_over_ranks(x, dist_on, device):
     t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
     return float(t.item())
+
+
+def prefill_run(step: DecodeStep, reps: int, hbm: float, src: str):
+    """lla_encode of the workload's whole prefill stack: every cached position of every
+    sequence, one [tokens x T*d] . [T*d x r] product per head and axis (Eq. (2) of the
+    LLA page), written into a second cache so the decode layer stays as it was.  Each
+    call is timed with CUDA events on the launching stream; x (tens of GB) is far larger
+    than L2.  Algorithmic bytes: x_k and x_v read once, every latent written once
+    (W_down and mu, under 1 MB, left out)."""
+    w, i = step.w, step.inp
+    xk, xv = step.prefill_x
+    dev = xk.device
+    seq_idx = torch.arange(w.B, dtype=torch.int32, device=dev).repeat_interleave(w.L_max)
+    pos = torch.arange(w.L_max, dtype=torch.int32, device=dev).repeat(w.B)
+    pk, pv = torch.empty_like(i["cache_k"]), torch.empty_like(i["cache_v"])
+    n = int(seq_idx.shape[0])
+    moved = ((xk.numel() + xv.numel()) * xk.element_size() + (pk.numel() + pv.numel()) * pk.element_size())
+    flops = 2.0 * xk.numel() * (w.r_k + w.r_v)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for k in range(reps + 2):
+        e0.record()
+        lla.encode(step.dm, xk, xv, seq_idx, pos, i["w_down_k"], i["w_down_v"], i["mu_k"], i["mu_v"],
+                   pk, pv, step.ws)
+        e1.record()
+        torch.cuda.synchronize()
+        if k >= 2:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    if lla.device_status(step.ws) != lla.LLA_OK:
+        raise RuntimeError("device status after the prefill encode")
+    t = float(np.mean(times))
+    del pk, pv
+    return {"tokens": n, "heads": w.H if w.variant == 0 else 1, "encode_ms": t * 1e3,
+            "value": n / t, "unit": "prefill tokens/s per layer", "tflops": flops / t / 1e12,
+            "roofline": {"bound": "hbm", "achieved": moved / t / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": moved / t / 1e9 / hbm, "traffic": None,
+                         "kernel": "lla_encode (encode_bias_kernel + encode_bf16_kernel)",
+                         "algorithmic_bytes_per_launch": moved, "peak_source": src}}
 
 
 def e2e_run(step: DecodeStep, steps: int):
@@ -486,6 +530,8 @@ def run_ours(args, dist_on, rank, world, device):
                "decode_over_budget": {"latent_tokens_per_call": kept, "call_ms": t_dec * 1e3,
                                       "value": kept / t_dec, "unit": UNIT}}
 
+    pre = prefill_run(step, max(3, min(args.steps, 10)), hbm, src) if args.prefill else None
+
     e2e_steps = max(3, min(args.steps, 200))
     e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
     e2e_dt = max_over_ranks(e2e_dt, dist_on, device)
@@ -509,6 +555,7 @@ def run_ours(args, dist_on, rank, world, device):
         "roofline": roof,
         **({"window": win} if win else {}),
         **({"evict": evi} if evi else {}),
+        **({"prefill": pre} if pre else {}),
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clk.summary(),
@@ -568,7 +615,13 @@ def main():
                     help="keep the cache in shuffled pages of this many tokens (lla_decode_attn_paged)")
     ap.add_argument("--decoupled", action="store_true",
                     help="decode with lla_decode_attn_decoupled (64 rotary dimensions per token-head)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="also time lla_encode of the workload's whole prefill stack (ouro_rho4_b64_16k)")
     args = ap.parse_args()
+    if args.prefill:
+        pw = WORKLOADS[args.workload]
+        if pw.N_encode != pw.B * pw.L_max or args.paged:
+            ap.error("--prefill needs a workload with a prefill stack (ouro_rho4_b64_16k) and the dense cache")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.paged and (args.decoupled or WORKLOADS[args.workload].variant != 0):

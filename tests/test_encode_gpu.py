@@ -220,3 +220,46 @@ def test_encode_then_decode_chain_bf16():
         err = (np.abs(go - ro).max(-1) / np.maximum(np.abs(ro).max(-1), 1e-6)).max()
         assert err <= 2e-2, err
         assert np.abs(lse.double().cpu().numpy() - rl).max() <= 2e-2
+
+
+def test_encode_prefill_full_size_sampled():
+    """The long-context prefill at full size, in the launch configuration the bench
+    times: lla_encode of every position of 64 sequences x 16384 tokens x 16 heads
+    (1,048,576 tokens, x about 34 GB) in one call.  Every cache slot must be written
+    (no canary left: a property that holds at any size), and sampled tokens (the
+    first and last, both sides of tile and sequence boundaries, and random ones)
+    must agree with the oracle's Eq. (2) under the bound of the random-input test."""
+    from looped_transformer_cross_gb300.synth import WORKLOADS
+    w = WORKLOADS["ouro_rho4_b64_16k"]
+    B, H, L_max, N = w.B, w.H, w.L_max, w.N_encode
+    assert N == B * L_max
+    if torch.cuda.mem_get_info()[0] < 90e9:
+        pytest.skip("needs about 90 GB of free device memory")
+    inp = make_decode_inputs(w, 20260003, device="cuda", with_encode=True)
+    ck, cv = inp.pop("cache_k").fill_(CANARY), inp.pop("cache_v").fill_(CANARY)
+    seq_idx = torch.arange(B, dtype=torch.int32, device="cuda").repeat_interleave(L_max)
+    pos = torch.arange(L_max, dtype=torch.int32, device="cuda").repeat(B)
+    st = _encode(w, inp["x_k"], inp["x_v"], seq_idx, pos, inp["w_down_k"], inp["w_down_v"],
+                 inp["mu_k"], inp["mu_v"], ck, cv)
+    assert st == lla.LLA_OK
+    assert not bool((ck == CANARY).any()) and not bool((cv == CANARY).any())
+    g = np.random.default_rng(5)
+    picks = [0, 127, 128, L_max - 1, L_max, N - 129, N - 128, N - 1]
+    picks = np.unique(np.concatenate([picks, g.choice(N, size=40, replace=False)]))
+    S = picks.shape[0]
+    idx = torch.tensor(picks, dtype=torch.int64, device="cuda")
+    dm = oracle_dims(w)
+    zeros = np.zeros(S, dtype=np.int32)
+    for cache, x, wd, mu, r in ((ck, "x_k", "w_down_k", "mu_k", w.r_k), (cv, "x_v", "w_down_v", "mu_v", w.r_v)):
+        xs = widen(inp[x][idx])                          # [S][H][T*d]
+        si = np.arange(S, dtype=np.int32)
+        exact, rounded, mag = (np.zeros((S, H, 1, r)) for _ in range(3))
+        oracle.encode(dm, xs, si, zeros, widen(inp[wd]), widen(inp[mu]), r, exact)
+        oracle.encode(dm, xs, si, zeros, widen(inp[wd]), widen(inp[mu]), r, rounded, round_to_bf16=True)
+        oracle.encode(dm, np.abs(xs - widen(inp[mu])[None]), si, zeros, np.abs(widen(inp[wd])),
+                      np.zeros_like(widen(inp[mu])), r, mag)
+        got = cache[idx // L_max, :, idx % L_max].double().cpu().numpy()   # [S][H][r]
+        exact, rounded, mag = exact[:, :, 0], rounded[:, :, 0], mag[:, :, 0]
+        half_ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(got), 2.0 ** -126))) - 8)
+        assert np.all(np.abs(got - exact) <= half_ulp + 2.0 ** -20 * mag)
+        assert (got == rounded).mean() > 0.99
