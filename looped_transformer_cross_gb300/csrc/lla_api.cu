@@ -592,6 +592,8 @@ lla_status encode_impl(const lla_dims* dims, const void* x_k, const void* x_v, i
 
   EncodePlan plan;
   if (!make_encode_plan(dims->r_k, dims->r_v, a.Td, &plan)) return LLA_ERR_UNSUPPORTED;
+  plan.sms = sm_count();
+  if (plan.sms <= 0) return LLA_ERR_CUDA;
   EncodeMaps m;
   std::memset(&m, 0, sizeof(m));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -4,11 +4,13 @@
 //     c = (x - mu) W_down ,  x = [x_1; ...; x_T] in R^{T d}
 // for every token and head, written into the token's cache slot.
 //
-// bf16 path: one CTA per (128-token tile, head, axis K/V).  TMA streams
-// 64-wide K-slices of x (K-major) and W_down (MN-major) through a ring; warp 1
-// issues tcgen05 MMAs accumulating x W_down in TMEM; four epilogue warps (one
-// token per TMEM lane) subtract mu W_down (computed once per call by a small
-// kernel), round to bf16 and store the latent row.  Computing x W - mu W
+// bf16 path: a persistent grid (one CTA per SM) over units of (128-token tile,
+// head, axis K/V).  TMA streams 64-wide K-slices of x (K-major) and W_down
+// (MN-major) through a ring that runs on across units; warp 1 issues tcgen05
+// MMAs accumulating x W_down in one of two TMEM accumulators; four epilogue warps
+// (one token per TMEM lane) subtract mu W_down (computed once per call by a small
+// kernel), round to bf16 and store the latent row while the next unit's MMAs
+// fill the other accumulator.  Computing x W - mu W
 // instead of (x - mu) W is exact in real arithmetic.
 //
 // fp32 path: one block per (token, head, axis), the literal sum in fp32.
@@ -20,7 +22,8 @@ namespace {
 
 struct alignas(16) EncodeMisc {
   uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t dfull;
+  uint64_t dfull[2], dempty[2];     // accumulator full (MMA commit) / drained (epilogue)
+  uint64_t mdone;                    // every MMA of the CTA complete
   uint32_t tmem_base;
   int abort;
 };
@@ -75,6 +78,27 @@ __device__ __forceinline__ bool slot_ok(const EncodeArgs& a, int sid, int p) {
   return sid >= 0 && sid < a.B && p >= 0 && p < a.L_max;
 }
 
+// Unit u of the persistent schedule: (token tile, head, axis), heads fastest, then
+// the axis, then the tile, so the CTAs running at one time read neighbouring rows
+// of x (one token's heads are contiguous).
+struct EncodeUnit {
+  int tile, h, axis;
+};
+
+__device__ __forceinline__ EncodeUnit encode_unit(int64_t u, int H) {
+  EncodeUnit e;
+  e.h = static_cast<int>(u % H);
+  const int64_t q = u / H;
+  e.axis = static_cast<int>(q & 1);
+  e.tile = static_cast<int>(q >> 1);
+  return e;
+}
+
+// Persistent: one CTA per SM walks units blockIdx.x, blockIdx.x + gridDim.x, ...
+// The x / W_down ring runs on across units (its position is the count of k-blocks
+// this CTA has issued), and two TMEM accumulators alternate between units, so
+// the epilogue of one unit overlaps the copies and MMAs of the next.  With r > 256
+// (LLA-2D) one accumulator takes all 512 columns and the units take turns.
 __global__ void __launch_bounds__(kEncodeThreads, 1)
 encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__ EncodePlan P,
                    const __grid_constant__ EncodeMaps maps) {
@@ -84,17 +108,21 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
   EncodeMisc* misc = reinterpret_cast<EncodeMisc*>(sm + P.misc);
   volatile int* abort = &misc->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, h = blockIdx.y, axis = blockIdx.z;
-  const int r = axis == 0 ? a.r_k : a.r_v;
-  const ChunkPlan& bp = axis == 0 ? P.bk : P.bv;
-  const CUtensorMap* xmap = axis == 0 ? &maps.xk : &maps.xv;
-  const CUtensorMap* wmaps = axis == 0 ? maps.wk : maps.wv;
   const int KB = a.Td / 64;
+  const uint32_t S = static_cast<uint32_t>(P.S);
+  const int64_t nunits = static_cast<int64_t>((a.N + 127) / 128) * a.H * 2;
   auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
+  // accumulator buffer of this CTA's j-th unit, and how often it was used before
+  auto acc_buf = [&](int64_t j) { return P.nacc == 2 ? static_cast<int>(j & 1) : 0; };
+  auto acc_use = [&](int64_t j) { return P.nacc == 2 ? (j >> 1) : j; };
 
   if (tid == 0) {
     for (int s = 0; s < P.S; ++s) { mbar_init(bar(misc->full[s]), 1); mbar_init(bar(misc->empty[s]), 1); }
-    mbar_init(bar(misc->dfull), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(misc->dfull[b]), 1);
+      mbar_init(bar(misc->dempty[b]), 4);   // one arrive per epilogue warp
+    }
+    mbar_init(bar(misc->mdone), 1);
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -109,61 +137,87 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint32_t bytes = 128 * 64 * 2 + bp.bytes;
-      int issued = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % P.S;
-        if (!mbar_wait(bar(misc->empty[s]), ((kb / P.S) & 1) ^ 1, abort, a.status)) break;
-        const uint32_t fb = bar(misc->full[s]);
-        mbar_arrive_expect_tx(fb, bytes);
-        const uint32_t st = sbase + P.ring + s * P.stage;
-        tma_load_3d(st + P.a_off, xmap, fb, kb * 64, h, tile * 128);
-        for (int c = 0; c < bp.n; ++c)
-          tma_load_3d(st + P.b_off + bp.off[c], &wmaps[chunk_map_index(bp.width[c])], fb, bp.start[c],
-                      kb * 64, h);
-        issued = kb + 1;
+      uint32_t g = 0;   // k-blocks issued by this CTA: the ring position
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const EncodeUnit e = encode_unit(u, a.H);
+        const ChunkPlan& bp = e.axis == 0 ? P.bk : P.bv;
+        const CUtensorMap* xmap = e.axis == 0 ? &maps.xk : &maps.xv;
+        const CUtensorMap* wmaps = e.axis == 0 ? maps.wk : maps.wv;
+        const uint32_t bytes = 128 * 64 * 2 + bp.bytes;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const uint32_t s = g % S;
+          if (!(ok = mbar_wait(bar(misc->empty[s]), ((g / S) & 1) ^ 1, abort, a.status))) break;
+          const uint32_t fb = bar(misc->full[s]);
+          mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t st = sbase + P.ring + s * P.stage;
+          tma_load_3d(st + P.a_off, xmap, fb, kb * 64, e.h, e.tile * 128);
+          for (int c = 0; c < bp.n; ++c)
+            tma_load_3d(st + P.b_off + bp.off[c], &wmaps[chunk_map_index(bp.width[c])], fb, bp.start[c],
+                        kb * 64, e.h);
+        }
       }
-      for (int kb = max(0, issued - P.S); kb < issued; ++kb) {
+      // the copies still in flight land before the CTA exits
+      for (uint32_t k = g > S ? g - S : 0; k < g; ++k) {
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(bar(misc->full[kb % P.S]), (kb / P.S) & 1) &&
-               global_timer_ns() - t0 < kWaitLimitNs) {}
+        while (!mbar_try_wait(bar(misc->full[k % S]), (k / S) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      uint32_t g = 0;
       bool ok = true;
-      for (int kb = 0; kb < KB && ok; ++kb) {
-        const int s = kb % P.S;
-        if (!(ok = mbar_wait(bar(misc->full[s]), (kb / P.S) & 1, abort, a.status))) break;
+      int64_t j = 0;
+      for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++j) {
+        const EncodeUnit e = encode_unit(u, a.H);
+        const ChunkPlan& bp = e.axis == 0 ? P.bk : P.bv;
+        const int ab = acc_buf(j);
+        // the epilogue has read this accumulator's previous unit out of TMEM
+        if (!(ok = mbar_wait(bar(misc->dempty[ab]), (acc_use(j) & 1) ^ 1, abort, a.status))) break;
         tc_fence_after();
-        const uint32_t st = sbase + P.ring + s * P.stage;
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t ad = umma_desc(st + P.a_off + k * 32, 16, 1024, kSw128);
-          // N-runs: up to four 64-wide chunks per MMA, narrower chunks alone
-          for (int c = 0; c < bp.n;) {
-            const int w = bp.width[c];
-            int nch = 1;
-            if (w == 64) while (c + nch < bp.n && bp.width[c + nch] == 64 && nch < 4) ++nch;
-            const int rb = w * 2;
-            const uint64_t bd = umma_desc(st + P.b_off + bp.off[c] + k * 16 * rb, 64 * rb, 8 * rb,
-                                          sw_mode_for_row_bytes(rb));
-            umma_bf16(tmem + bp.start[c], ad, bd, umma_idesc_bf16(128, w * nch, false, true),
-                      (kb > 0 || k > 0) ? 1u : 0u);
-            c += nch;
+        const uint32_t acc = tmem + static_cast<uint32_t>(ab * P.acc_stride);
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const uint32_t s = g % S;
+          if (!(ok = mbar_wait(bar(misc->full[s]), (g / S) & 1, abort, a.status))) break;
+          tc_fence_after();
+          const uint32_t st = sbase + P.ring + s * P.stage;
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = umma_desc(st + P.a_off + k * 32, 16, 1024, kSw128);
+            // N-runs: up to four 64-wide chunks per MMA, narrower chunks alone
+            for (int c = 0; c < bp.n;) {
+              const int w = bp.width[c];
+              int nch = 1;
+              if (w == 64) while (c + nch < bp.n && bp.width[c + nch] == 64 && nch < 4) ++nch;
+              const int rb = w * 2;
+              const uint64_t bd = umma_desc(st + P.b_off + bp.off[c] + k * 16 * rb, 64 * rb, 8 * rb,
+                                            sw_mode_for_row_bytes(rb));
+              umma_bf16(acc + bp.start[c], ad, bd, umma_idesc_bf16(128, w * nch, false, true),
+                        (kb > 0 || k > 0) ? 1u : 0u);
+              c += nch;
+            }
           }
+          umma_commit(bar(misc->empty[s]));
         }
-        umma_commit(bar(misc->empty[s]));
+        if (ok) umma_commit(bar(misc->dfull[ab]));
       }
-      umma_commit(bar(misc->dfull));
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(bar(misc->dfull), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      // every MMA this thread issued is complete before TMEM is released
+      if (g > 0) {
+        umma_commit(bar(misc->mdone));
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar(misc->mdone), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
     }
   } else {
     const int q = warp & 3, row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    if (warp_wait(bar(misc->dfull), 0, abort, a.status)) {
+    int64_t j = 0;
+    for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x, ++j) {
+      const EncodeUnit e = encode_unit(u, a.H);
+      const int r = e.axis == 0 ? a.r_k : a.r_v;
+      const int ab = acc_buf(j);
+      if (!warp_wait(bar(misc->dfull[ab]), acc_use(j) & 1, abort, a.status)) break;
       tc_fence_after();
-      const int n = tile * 128 + row;
+      const int n = e.tile * 128 + row;
       int sid = -1, p = -1;
       if (n < a.N) {
         sid = __ldg(a.seq_idx + n);
@@ -172,14 +226,16 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
       }
       const int64_t drow = n < a.N && slot_ok(a, sid, p)
                                ? latent_row_for_write(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max,
-                                                      a.H, sid, h, p, a.status)
+                                                      a.H, sid, e.h, p, a.status)
                                : -1;
       const bool write = drow >= 0;
-      const float* bias = a.bias + (static_cast<int64_t>(axis) * a.H + h) * 256;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(axis == 0 ? a.cache_k : a.cache_v) + (write ? drow : 0) * r;
+      const float* bias = a.bias + (static_cast<int64_t>(e.axis) * a.H + e.h) * 256;
+      __nv_bfloat16* dst =
+          static_cast<__nv_bfloat16*>(e.axis == 0 ? a.cache_k : a.cache_v) + (write ? drow : 0) * r;
+      const uint32_t acc = tmem + static_cast<uint32_t>(ab * P.acc_stride) + lane_base;
       for (int c0 = 0; c0 < r; c0 += 16) {
         float v[16];
-        tmem_ld_x16(tmem + lane_base + c0, v);   // every lane of the warp takes part
+        tmem_ld_x16(acc + c0, v);   // every lane of the warp takes part
         tmem_wait_ld();
         if (write) {
           uint32_t wds[8];
@@ -194,6 +250,10 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
           d4[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
         }
       }
+      // this warp's rows are out of the accumulator: the MMA thread may reuse it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(misc->dempty[ab]));
     }
   }
   tc_fence_before();
@@ -248,9 +308,10 @@ bool make_encode_plan(int r_k, int r_v, int Td, EncodePlan* p) {
   p->misc = S * p->stage;
   p->bytes = p->misc + 1024 + 1024;
   const int rmax = r_k > r_v ? r_k : r_v;
-  int cols = 32;
-  while (cols < rmax) cols <<= 1;
-  p->tmem_cols = cols;
+  // two accumulators of 256 columns when both ranks fit, else one of 512
+  p->nacc = rmax <= 256 ? 2 : 1;
+  p->acc_stride = 256;
+  p->tmem_cols = 512;
   return true;
 }
 
@@ -266,7 +327,9 @@ cudaError_t launch_encode_bf16(const EncodeArgs& a, const EncodePlan& plan, cons
     if (e != cudaSuccess) return e;
     configured = plan.bytes;
   }
-  const dim3 grid((a.N + 127) / 128, a.H, 2);
+  // persistent: one CTA per SM (or per unit, when there are fewer units)
+  const int64_t units = static_cast<int64_t>((a.N + 127) / 128) * a.H * 2;
+  const int grid = static_cast<int>(units < plan.sms ? units : plan.sms);
   encode_bf16_kernel<<<grid, kEncodeThreads, plan.bytes, s>>>(a, plan, m);
   return cudaGetLastError();
 }

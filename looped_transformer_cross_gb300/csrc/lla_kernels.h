@@ -264,6 +264,8 @@ struct EncodePlan {
   int a_off, b_off;                  // inside a stage
   int ring, misc, bytes;
   int tmem_cols;
+  int nacc, acc_stride;              // TMEM accumulators (1 or 2) and their column stride
+  int sms;                           // persistent grid size (set by the caller)
 };
 
 struct EncodeMaps {
