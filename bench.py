@@ -530,7 +530,11 @@ def run_ours(args, dist_on, rank, world, device):
                "decode_over_budget": {"latent_tokens_per_call": kept, "call_ms": t_dec * 1e3,
                                       "value": kept / t_dec, "unit": UNIT}}
 
-    pre = prefill_run(step, max(3, min(args.steps, 10)), hbm, src) if args.prefill else None
+    pre = None
+    if args.prefill:
+        with ClockSampler(torch.cuda.current_device()) as pclk:
+            pre = prefill_run(step, max(3, min(args.steps, 10)), hbm, src)
+        pre["clocks"] = pclk.summary()
 
     e2e_steps = max(3, min(args.steps, 200))
     e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
