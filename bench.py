@@ -322,6 +322,21 @@ def prefill_run(step: DecodeStep, reps: int, hbm: float, src: str):
                          "algorithmic_bytes_per_launch": moved, "peak_source": src}}
 
 
+def arm_config(w, args, tokens, world):
+    """The bench line's ``config``: the same object on both arms."""
+    return {"workload": w.name, "variant": "LLA-2D" if w.variant else "per-head",
+            **({"exact_window": args.window} if args.window > 0 else {}),
+            **({"decoupled_rope": D_ROPE} if args.decoupled else {}),
+            **({"paged": {"page_size": args.paged, "pages_shuffled": True}} if args.paged else {}),
+            "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
+            "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi],
+            "latent_tokens_per_gpu": tokens, "parallelism": "dp%d" % world,
+            "step": "lla_encode of %d new tokens + %s for loops 1..%d" % (
+                w.B, "lla_decode_attn_decoupled" if args.decoupled else "lla_decode_attn", w.T),
+            "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
+                w.B * w.H * w.L_max * (w.r_k + w.r_v) * 2 / 1e9)}
+
+
 def e2e_run(step: DecodeStep, steps: int):
     """Same step through the public API with the per-step inputs coming from pinned
     host memory and the results read back: new-token stacks, queries, lengths
@@ -545,17 +560,7 @@ def run_ours(args, dist_on, rank, world, device):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "variant": "LLA-2D" if w.variant else "per-head",
-                   **({"exact_window": args.window} if args.window > 0 else {}),
-                   **({"decoupled_rope": D_ROPE} if args.decoupled else {}),
-                   **({"paged": {"page_size": args.paged, "pages_shuffled": True}} if args.paged else {}),
-                   "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
-                   "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi],
-                   "latent_tokens_per_gpu": step.tokens, "parallelism": "dp%d" % world,
-                   "step": "lla_encode of %d new tokens + %s for loops 1..%d" % (
-                       w.B, "lla_decode_attn_decoupled" if args.decoupled else "lla_decode_attn", T),
-                   "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
-                       w.B * w.H * w.L_max * (w.r_k + w.r_v) * 2 / 1e9)},
+        "config": arm_config(w, args, step.tokens, world),
         "roofline": roof,
         **({"window": win} if win else {}),
         **({"evict": evi} if evi else {}),
@@ -596,8 +601,8 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
-                       "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi]},
+            "config": arm_config(w, args, int(inp["seq_lens"].sum().item()),
+                                 int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
