@@ -393,6 +393,35 @@ def oracle_sample(w, inp_dev, q_dev, budget_s=12.0, k_rope=None, dense=None):
                       "loops) in %.2f s" % (S, w.B, w.H, w.T, tokens, dt)}
 
 
+def oracle_prefill_sample(w, inp_dev, x_dev, budget_s=8.0):
+    """Time the oracle's encode (Eq. (2), both axes, all heads) on the first S tokens of
+    the prefill stack; S grows from 128 until the run would take about ``budget_s``."""
+    import oracle
+    odm = oracle.dims(w.T, w.H, w.d, w.r_k, w.r_v, w.variant, w.rope_base)
+    wd = (widen(inp_dev["w_down_k"]), widen(inp_dev["w_down_v"]))
+    mu = (widen(inp_dev["mu_k"]), widen(inp_dev["mu_v"]))
+    units = w.H if w.variant == 0 else 1
+
+    def run(S):
+        xs = (widen(x_dev[0][:S]), widen(x_dev[1][:S]))
+        si = np.zeros(S, dtype=np.int32)
+        po = np.arange(S, dtype=np.int32)
+        shape = (1, units, S) if w.variant == 0 else (1, S)
+        outs = (np.zeros(shape + (w.r_k,)), np.zeros(shape + (w.r_v,)))
+        t0 = time.perf_counter()
+        for a in range(2):
+            oracle.encode(odm, xs[a], si, po, wd[a], mu[a], (w.r_k, w.r_v)[a], outs[a], round_to_bf16=True)
+        return time.perf_counter() - t0
+
+    t1 = run(128)
+    S = int(max(128, min(x_dev[0].shape[0], 128 * budget_s / max(t1, 1e-3))))
+    dt = run(S)
+    return {"value": S / dt, "unit": "prefill tokens/s per layer", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "first %d of %d tokens of the prefill stack (one sequence's positions), all %d heads, "
+                      "both axes, in %.2f s" % (S, x_dev[0].shape[0], w.H, dt)}
+
+
 def run_ours(args, dist_on, rank, world, device):
     w = WORKLOADS[args.workload]
     lla_build.build()
@@ -550,6 +579,8 @@ def run_ours(args, dist_on, rank, world, device):
         with ClockSampler(torch.cuda.current_device()) as pclk:
             pre = prefill_run(step, max(3, min(args.steps, 10)), hbm, src)
         pre["clocks"] = pclk.summary()
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            pre["cpu_baseline"] = oracle_prefill_sample(w, step.inp, step.prefill_x)
 
     e2e_steps = max(3, min(args.steps, 200))
     e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
