@@ -97,8 +97,9 @@ __device__ __forceinline__ EncodeUnit encode_unit(int64_t u, int H) {
 // Persistent: one CTA per SM walks units blockIdx.x, blockIdx.x + gridDim.x, ...
 // The x / W_down ring runs on across units (its position is the count of k-blocks
 // this CTA has issued), and two TMEM accumulators alternate between units, so
-// the epilogue of one unit overlaps the copies and MMAs of the next.  With r > 256
-// (LLA-2D) one accumulator takes all 512 columns and the units take turns.
+// the epilogue of one unit overlaps the copies and MMAs of the next.  (The plan's
+// one-accumulator mode, for ranks above 256, is never chosen while the host checks
+// cap r_k and r_v at 256.)
 __global__ void __launch_bounds__(kEncodeThreads, 1)
 encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__ EncodePlan P,
                    const __grid_constant__ EncodeMaps maps) {
@@ -308,7 +309,7 @@ bool make_encode_plan(int r_k, int r_v, int Td, EncodePlan* p) {
   p->misc = S * p->stage;
   p->bytes = p->misc + 1024 + 1024;
   const int rmax = r_k > r_v ? r_k : r_v;
-  // two accumulators of 256 columns when both ranks fit, else one of 512
+  // two accumulators of 256 columns (every rank the host checks admit), else one of 512
   p->nacc = rmax <= 256 ? 2 : 1;
   p->acc_stride = 256;
   p->tmem_cols = 512;
