@@ -177,3 +177,26 @@ def test_ouro_rho4_b32_4k_sampled():
 def test_ouro_rho21_b768_4k_sampled():
     """rho = 21.3 at serving batch (768 x 4096, one layer); three sequences checked."""
     _sampled_full_size("ouro1.4b_rho21_b768_4k", [0, 400, 767], t=1)
+
+
+def test_ouro_rho4_b64_16k_sampled():
+    """The long-context layer (64 sequences x 16384 tokens, rho = 4) in the launch the
+    bench times: all 1024 (sequence, head) units of 128 tiles in one call.  Every
+    sequence spans 2048 tiles, more than twice one CTA's equal share of the 131,072
+    tiles, so each checked sequence has units cut between CTAs; positions reach 16383
+    and each unit's running maximum and sum cover 128 tiles.  Four sequences (first,
+    last and two inside) are checked against the oracle at two loops."""
+    w = WORKLOADS["ouro_rho4_b64_16k"]
+    inp = make_decode_inputs(w, 20260000 + 3, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles_per_seq = w.H * (w.L_max // 128)
+    assert tiles_per_seq > 2 * (w.B * tiles_per_seq) // min(sms, 1024)
+    bsel = [0, 21, 42, 63]
+    for t in (0, 3):
+        out, lse, st = gpu_decode(w, inp, t)
+        assert st == lla.LLA_OK
+        go, gl = out.cpu().double().numpy(), lse.cpu().double().numpy()
+        assert np.all(np.isfinite(go)) and np.all(np.isfinite(gl))
+        ro, rl = oracle_decode(w, inp, t, bsel=bsel)
+        e_o, e_l = rel_err(go[bsel], ro), lse_err(gl[bsel], rl)
+        assert e_o <= 2e-2 and e_l <= 2e-2, (t, e_o, e_l)
