@@ -299,10 +299,12 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
  *   - The first call on each device looks up the array's device address with
  *     the device current; make that first call before any stream capture.
  *   - The array is shared by every call and keeps the last call's contents;
- *     the status word is cleared on `stream` before each launch.  Calls that
- *     overlap on the GPU race and must be serialised by the caller.  The
- *     kernels' device status of this variant is not readable through
- *     lla_device_status (there is no workspace pointer to pass).
+ *     once the host checks have passed, the status word is cleared on `stream`
+ *     before the first launch (a call rejected on the host enqueues nothing).
+ *     Calls that overlap on the GPU race and must be serialised by the caller.
+ *   - The kernels' device status (LLA_ERR_DEVICE_ARG, LLA_ERR_TIMEOUT,
+ *     LLA_ERR_RANGE) is read with lla_device_status(NULL, stream, clear) on
+ *     the same device.
  */
 lla_status lla_decode_attn_noalloc(const lla_dims* dims, int loop_t, const void* q,
                                    lla_cache cache, const int32_t* seq_lens, const int32_t* q_pos,
@@ -331,7 +333,9 @@ size_t lla_workspace_size(const lla_dims* dims, int B, int64_t L_max, int max_N)
 lla_status lla_rope_table(const lla_dims* dims, int64_t n_pos, float* cos_out, float* sin_out);
 
 /* Synchronise `stream`, then return the status word the kernels recorded in
- * `workspace` (LLA_OK if none); clear it when `clear` is non-zero. */
+ * `workspace` (LLA_OK if none); clear it when `clear` is non-zero.  With
+ * workspace == NULL the word read is that of lla_decode_attn_noalloc's fixed
+ * scratch on the current device. */
 lla_status lla_device_status(void* workspace, void* stream, int clear);
 
 /* Static description of a status code. */

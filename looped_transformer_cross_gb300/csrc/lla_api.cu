@@ -193,7 +193,11 @@ lla_status lla_rope_table(const lla_dims* dims, int64_t n_pos, float* cos_out, f
 }
 
 lla_status lla_device_status(void* workspace, void* stream, int clear) {
-  if (!workspace) return LLA_ERR_INVALID_ARG;
+  if (!workspace) {
+    // no workspace: the status word of lla_decode_attn_noalloc's scratch on this device
+    const lla_status st = noalloc_scratch_address(&workspace);
+    if (st != LLA_OK) return st;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t v = 0;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LLA_ERR_CUDA;
@@ -240,7 +244,8 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
                        const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
                        const void* w_up_v, const float* mu_k, const float* mu_v,
                        const float* rope_cos, const float* rope_sin, int64_t rope_len, float* out,
-                       float* lse, void* workspace, size_t ws_bytes, void* stream) {
+                       float* lse, void* workspace, size_t ws_bytes, void* stream,
+                       bool clear_status = false) {
   lla_status st = check_dims(dims);
   if (st != LLA_OK) return st;
   if (loop_t < 0 || loop_t >= dims->T || cache.B < 0 || cache.L_max < 1) return LLA_ERR_INVALID_ARG;
@@ -259,6 +264,9 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   const int esize = dims->dtype == LLA_BF16 ? 2 : 4;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every host check has passed: zero the status word first when asked to (the
+  // entry point without a workspace), then launch
+  auto ready = [&]() { return !clear_status || cudaMemsetAsync(ws, 0, 256, s) == cudaSuccess; };
   if (dims->variant == LLA_2D && dims->dtype == LLA_BF16) {
     // LLA-2D: one latent per token shared by the H heads (CTA-pair kernel)
     Decode2dArgs a{};
@@ -300,6 +308,7 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
       return LLA_ERR_CUDA;
     if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, seqs, 64, 32, 1))
       return LLA_ERR_CUDA;
+    if (!ready()) return LLA_ERR_CUDA;
     return launch_decode2d_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   }
   DecodeArgs a{};
@@ -337,7 +346,10 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   a.zimg = ws + wl.zimg;
   a.zimg_stride = static_cast<int64_t>(wl.zimg_stride);
 
-  if (dims->dtype == LLA_F32) return launch_decode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  if (dims->dtype == LLA_F32) {
+    if (!ready()) return LLA_ERR_CUDA;
+    return launch_decode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  }
 
   const int sms = sm_count();
   if (sms <= 0) return LLA_ERR_CUDA;
@@ -355,6 +367,7 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
     a.trig_rows = decode_small_trig_rows(cache.L_max, rope_len);
     const int64_t max_pos = static_cast<int64_t>(cache.B) * ((cache.L_max + kTile - 1) / kTile);
     a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_pos)));
+    if (!ready()) return LLA_ERR_CUDA;
     return launch_decode_small_bf16(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   }
   if (!make_decode_plan(dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
@@ -371,6 +384,7 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   // V latents: 32-column boxes (a tail box zero-filled past r_v), 64B swizzle
   if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 32, kTile, 1))
     return LLA_ERR_CUDA;
+  if (!ready()) return LLA_ERR_CUDA;
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
@@ -399,6 +413,23 @@ lla_status lla_decode_attn_paged(const lla_dims* dims, int loop_t, const void* q
   return decode_impl(dims, loop_t, q, v, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v, rope_cos, rope_sin,
                      rope_len, out, lse, workspace, ws_bytes, stream);
 }
+
+}  // extern "C"
+
+namespace lla {
+
+lla_status decode_attn_status_cleared(const lla_dims* dims, int loop_t, const void* q, lla_cache cache,
+                                      const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
+                                      const void* w_up_v, const float* mu_k, const float* mu_v,
+                                      const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                                      float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  return decode_impl(dims, loop_t, q, dense_view(cache), seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v, rope_cos,
+                     rope_sin, rope_len, out, lse, workspace, ws_bytes, stream, true);
+}
+
+}  // namespace lla
+
+extern "C" {
 
 size_t lla_decoupled_workspace_size(const lla_dims* dims, int d_rope, int B, int64_t L_max) {
   if (check_dims(dims) != LLA_OK || dims->variant != LLA_PER_HEAD || d_rope != 64 || B < 0 || L_max < 0) return 0;

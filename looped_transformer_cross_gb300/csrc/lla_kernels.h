@@ -278,4 +278,17 @@ cudaError_t launch_encode_bf16(const EncodeArgs& a, const EncodePlan& plan, cons
                                cudaStream_t s);
 cudaError_t launch_encode_f32(const EncodeArgs& a, cudaStream_t s);
 
+// ----------------------------------------------------------------- scratch without allocation
+
+// Device address of the library's fixed scratch array on the current device (looked
+// up once per device, defined in lla_noalloc.cu).
+lla_status noalloc_scratch_address(void** out);
+// lla_decode_attn that zeroes the status word on `stream` after every host check has
+// passed and before its first launch (a call the host checks reject enqueues nothing).
+lla_status decode_attn_status_cleared(const lla_dims* dims, int loop_t, const void* q, lla_cache cache,
+                                      const int32_t* seq_lens, const int32_t* q_pos, const void* w_up_k,
+                                      const void* w_up_v, const float* mu_k, const float* mu_v,
+                                      const float* rope_cos, const float* rope_sin, int64_t rope_len,
+                                      float* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
 }  // namespace lla

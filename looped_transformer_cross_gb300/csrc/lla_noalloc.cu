@@ -14,9 +14,10 @@
 // code cannot use the array's name as a device address, so the first call on
 // each device looks the address up with cudaGetSymbolAddress (that device
 // current) and caches it.  Every call shares the array and it keeps the last
-// call's contents; the status word is cleared on the caller's stream before
-// each launch.  Calls that overlap on the GPU (different streams, or several
-// host threads) race on the array and must be serialised by the caller.
+// call's contents; the status word is cleared on the caller's stream once the
+// host checks have passed, before the first launch, and lla_device_status with
+// no workspace reads it back.  Calls that overlap on the GPU (different streams,
+// or several host threads) race on the array and must be serialised by the caller.
 #include <mutex>
 
 #include "lla_kernels.h"
@@ -28,6 +29,10 @@ __device__ __align__(256) uint8_t g_noalloc_scratch[LLA_NOALLOC_SCRATCH_BYTES];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+
+namespace lla {
 
 // Device address of g_noalloc_scratch on the current device (looked up once).
 lla_status noalloc_scratch_address(void** out) {
@@ -44,7 +49,7 @@ lla_status noalloc_scratch_address(void** out) {
   return LLA_OK;
 }
 
-}  // namespace
+}  // namespace lla
 
 extern "C" lla_status lla_decode_attn_noalloc(const lla_dims* dims, int loop_t, const void* q,
                                               lla_cache cache, const int32_t* seq_lens,
@@ -59,10 +64,10 @@ extern "C" lla_status lla_decode_attn_noalloc(const lla_dims* dims, int loop_t, 
                            rope_cos, rope_sin, rope_len, out, lse, nullptr, 0, stream);
   if (need > LLA_NOALLOC_SCRATCH_BYTES) return LLA_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  const lla_status st = noalloc_scratch_address(&scratch);
+  const lla_status st = lla::noalloc_scratch_address(&scratch);
   if (st != LLA_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return LLA_ERR_CUDA;
-  return lla_decode_attn(dims, loop_t, q, cache, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v,
-                         rope_cos, rope_sin, rope_len, out, lse, scratch, LLA_NOALLOC_SCRATCH_BYTES, s);
+  // the status word is zeroed on `stream` only once every host check has passed
+  return lla::decode_attn_status_cleared(dims, loop_t, q, cache, seq_lens, q_pos, w_up_k, w_up_v, mu_k, mu_v,
+                                         rope_cos, rope_sin, rope_len, out, lse, scratch,
+                                         LLA_NOALLOC_SCRATCH_BYTES, stream);
 }
