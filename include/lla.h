@@ -35,6 +35,12 @@
  *   lla_workspace_size() bytes.  Its first 256 bytes hold the status word and
  *   must be zero before the first call; the rest is scratch.  Calls that
  *   share a workspace must be ordered on one stream.
+ * - Test hook of the timeout path: while the 32-bit word at byte 4 of the
+ *   workspace holds LLA_TEST_STALL, the per-head bf16 tile decode kernel
+ *   ("tile" in lla_decode_kernel) waits on a barrier that one arrival short
+ *   never completes; the wait expires after about one second and the call's
+ *   status becomes LLA_ERR_TIMEOUT (outputs undefined).  Zero the word to
+ *   resume normal calls.
  * - Constraints: d_head == 128; r_k and r_v multiples of 16 in [16, 256];
  *   T >= 1; H >= 1.  Other shapes return LLA_ERR_UNSUPPORTED.
  */
@@ -49,6 +55,10 @@ extern "C" {
 #endif
 
 #define LLA_ABI_VERSION 1
+
+/* Value of workspace word 1 (byte offset 4) that makes the next tile decode
+ * kernel's bounded wait expire (see the test hook above). */
+#define LLA_TEST_STALL 0x4C415453u
 
 typedef enum {
     LLA_OK = 0,

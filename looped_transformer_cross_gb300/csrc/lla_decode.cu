@@ -284,11 +284,16 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
   // ---------------------------------------------------------- set-up
   auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
   if (tid == 0) {
+    // Test hook of the timeout path: while word 1 of the status block holds
+    // LLA_TEST_STALL, the first weights barrier expects one arrival more than the four
+    // epilogue warps give, so the value-MMA issuer's bounded wait on it expires (the
+    // kernel records LLA_ERR_TIMEOUT and every role returns).
+    const uint32_t stall = __ldcg(a.status + 1) == LLA_TEST_STALL ? 1u : 0u;
     for (int s = 0; s < P.SK; ++s) { mbar_init(bar(misc->kfull[s]), 1); mbar_init(bar(misc->kempty[s]), 1); }
     for (int s = 0; s < P.SV; ++s) { mbar_init(bar(misc->vfull[s]), 1); mbar_init(bar(misc->vempty[s]), 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(misc->ufull[i]), 1);
-      mbar_init(bar(misc->pfull[i]), 4);
+      mbar_init(bar(misc->pfull[i]), 4 + (i == 0 ? stall : 0u));
       mbar_init(bar(misc->vdone[i]), 1);
       mbar_init(bar(misc->zfull[i]), 1);
       mbar_init(bar(misc->zfree[i]), 1);
