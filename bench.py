@@ -16,6 +16,7 @@ workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -61,6 +62,7 @@ TRAFFIC_DEC_PER_TOKEN_HEAD = (320.807936e6 + 3.610112e6) / (31042 * 16)
 TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
 DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
 UNIT = "latent tokens/s per layer-loop"
+DEFAULT_WORKLOAD = "ouro1.4b_rho4_b32_4k"
 D_ROPE = 64   # rotary dimensions of the decoupled-RoPE decode
 
 
@@ -77,11 +79,14 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while active, each
+    sample stamped with the host clock on arrival; ``summary(t0, t1)`` keeps the
+    samples taken between t0 and t1."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, index: int):
         self.index, self.proc, self.lines = index, None, []
@@ -90,7 +95,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -100,7 +105,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def wait_live(self, timeout_s=3.0):
+        """Wait (bounded) for the first sample, so the sampler runs before the work."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.01)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -110,10 +121,12 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        window = "timed region"
+        pick = [ln for ts, ln in self.lines if (t0 is None or ts >= t0) and (t1 is None or ts <= t1)]
         sm, smax, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in pick:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 8:
                 continue
@@ -126,23 +139,33 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax or None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
 # ----------------------------------------------------------------- our arm
 
 class DecodeStep:
-    """One layer's state on the device and the per-step call sequence.  With a window
-    W > 0 each decode call is followed by lla_window_attn over an exact window of the
-    W newest tokens (the HLA page's hybrid layout, §3.4 Eq. (4)) placed after the
-    latent tokens."""
+    """The layers' state on the device and the per-step call sequence: for each of
+    ``layers`` layers, lla_encode of the sequences' new token and lla_decode_attn for
+    loops 1..T.  Layer l reads layer buffer l mod nbuf, where nbuf is the number of
+    distinct layer caches that fit in device memory (a stack larger than HBM cycles
+    its buffers); every layer has its own queries and outputs.  With a window W > 0
+    (one layer) each decode call is followed by lla_window_attn over an exact window
+    of the W newest tokens (the HLA page's hybrid layout, §3.4 Eq. (4)) placed after
+    the latent tokens."""
 
-    def __init__(self, w, seed, device, window=0, decoupled=False, paged=0):
+    def __init__(self, w, seed, device, window=0, decoupled=False, paged=0, layers=1, prefill=False):
+        if layers > 1 and (window or decoupled or paged):
+            raise ValueError("a multi-layer step runs the dense per-layer decode only")
+        self.nlayers = layers
         self.w = w
         self.window = window
         self.decoupled = decoupled
         self.paged = paged
-        self.inp = make_decode_inputs(w, seed, device=device, with_encode=True)
+        # the prefill stack (x for every cached position) is drawn only when the prefill
+        # leg will encode it; otherwise the new-token rows alone
+        wd = w if prefill else dataclasses.replace(w, N_encode=min(w.N_encode, w.B))
+        self.inp = make_decode_inputs(wd, seed, device=device, with_encode=True)
         # a workload with a prefill stack (x for every cached position) keeps it aside:
         # the decode step encodes only each sequence's new token, the first B rows
         self.prefill_x = None
@@ -154,16 +177,32 @@ class DecodeStep:
             self.inp["q_pos"] = self.win["q_pos"]
         g = torch.Generator(device=device)
         g.manual_seed(seed + 7)
-        # one query per loop (the model's query changes from loop to loop)
-        self.q = (torch.randn((w.T, w.B, w.H, w.d), generator=g, device=device)
-                  .to(self.inp["q"].dtype).contiguous())
+        # one query per layer and loop (the model's query changes from loop to loop)
+        self.qL = (torch.randn((layers, w.T, w.B, w.H, w.d), generator=g, device=device)
+                   .to(self.inp["q"].dtype).contiguous())
+        self.q = self.qL[0]
+        # further layer buffers: each its own cache, codec and new-token stacks, drawn
+        # with its own seed, the lengths shared; as many as fit in device memory
+        self.bufs = [self.inp]
+        if layers > 1:
+            per_layer = sum(self.inp[k].numel() * self.inp[k].element_size() for k in ("cache_k", "cache_v"))
+            free = torch.cuda.mem_get_info(device)[0]
+            nbuf = int(min(layers, max(1, (free - 8e9 - per_layer) // per_layer)))
+            wl = dataclasses.replace(w, N_encode=0)   # new-token rows only
+            for l in range(1, nbuf):
+                li = make_decode_inputs(wl, seed + 100 * l, device=device, with_encode=True,
+                                        seq_lens=self.inp["seq_lens"])
+                li["seq_lens"], li["q_pos"] = self.inp["seq_lens"], self.inp["q_pos"]
+                del li["q"]
+                self.bufs.append(li)
         self.dm = lla.dims(w.T, w.H, w.r_k, w.r_v, variant=w.variant, rope_base=w.rope_base)
         c, s = lla.rope_table(self.dm, max(w.L_max + window, 128))
         self.cos, self.sin = c.to(device), s.to(device)
         self.ws = lla.make_workspace(self.dm, w.B, w.L_max, w.B, device=device)
         self.seq_idx = torch.arange(w.B, dtype=torch.int32, device=device)
-        self.out = torch.empty((w.T, w.B, w.H, w.d), dtype=torch.float32, device=device)
-        self.lse = torch.empty((w.T, w.B, w.H), dtype=torch.float32, device=device)
+        self.outL = torch.empty((layers, w.T, w.B, w.H, w.d), dtype=torch.float32, device=device)
+        self.lseL = torch.empty((layers, w.T, w.B, w.H), dtype=torch.float32, device=device)
+        self.out, self.lse = self.outL[0], self.lseL[0]
         self.tokens = int(self.inp["seq_lens"].sum().item())
         self.enc_pos = (self.inp["seq_lens"] - 1).clamp(0, w.L_max - 1).to(torch.int32)
         if paged:
@@ -206,6 +245,8 @@ class DecodeStep:
             self.dws = lla.decoupled_workspace(self.dm, D_ROPE, w.B, w.L_max, device=device)
 
     def run(self, ev=None):
+        if self.nlayers > 1:
+            return self.run_layers(ev)
         i, dm = self.inp, self.dm
         # the new token's latent: slot seq_lens - 1 (the query's own slot without a window)
         if self.paged:
@@ -238,6 +279,21 @@ class DecodeStep:
                 if ev is not None:
                     ev[2][t].record()
 
+    def run_layers(self, ev=None):
+        dm, T = self.dm, self.w.T
+        for l in range(self.nlayers):
+            i = self.bufs[l % len(self.bufs)]
+            lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, self.enc_pos, i["w_down_k"], i["w_down_v"],
+                       i["mu_k"], i["mu_v"], i["cache_k"], i["cache_v"], self.ws)
+            for t in range(T):
+                if ev is not None:
+                    ev[0][l * T + t].record()
+                lla.decode_attn(dm, t, self.qL[l, t], i["cache_k"], i["cache_v"], i["seq_lens"], i["q_pos"],
+                                i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"], self.cos, self.sin,
+                                self.outL[l, t], self.lseL[l, t], self.ws)
+                if ev is not None:
+                    ev[1][l * T + t].record()
+
     def dense_view(self, nseq):
         """(cache_k, cache_v) of the first nseq sequences as dense [nseq][H][L_max][r]
         tensors (gathered from the pages when the cache is paged)."""
@@ -260,7 +316,7 @@ class DecodeStep:
     # images + decode + combine [+ window]); decoupled: query records + decode + combine
     def launches(self):
         per = 3
-        return 2 + (per + (1 if self.window > 0 else 0)) * self.w.T
+        return (2 + (per + (1 if self.window > 0 else 0)) * self.w.T) * self.nlayers
 
 
 def barrier(dist_on):
@@ -322,7 +378,7 @@ def prefill_run(step: DecodeStep, reps: int, hbm: float, src: str):
                          "algorithmic_bytes_per_launch": moved, "peak_source": src}}
 
 
-def arm_config(w, args, tokens, world):
+def arm_config(w, args, tokens, world, layers=1):
     """The bench line's ``config``: the same object on both arms."""
     return {"workload": w.name, "variant": "LLA-2D" if w.variant else "per-head",
             **({"exact_window": args.window} if args.window > 0 else {}),
@@ -331,8 +387,10 @@ def arm_config(w, args, tokens, world):
             "T": w.T, "H": w.H, "d_head": w.d, "r_k": w.r_k,
             "r_v": w.r_v, "batch_per_gpu": w.B, "seq_len_range": [w.len_lo, w.len_hi],
             "latent_tokens_per_gpu": tokens, "parallelism": "dp%d" % world,
-            "step": "lla_encode of %d new tokens + %s for loops 1..%d" % (
-                w.B, "lla_decode_attn_decoupled" if args.decoupled else "lla_decode_attn", w.T),
+            "layers_per_step": layers,
+            "step": "%slla_encode of %d new tokens + %s for loops 1..%d" % (
+                "per layer: " if layers > 1 else "", w.B,
+                "lla_decode_attn_decoupled" if args.decoupled else "lla_decode_attn", w.T),
             "l2": "inputs larger than L2 (%.2f GB of latents per GPU)" % (
                 w.B * w.H * w.L_max * (w.r_k + w.r_v) * 2 / 1e9)}
 
@@ -341,22 +399,24 @@ def e2e_run(step: DecodeStep, steps: int):
     """Same step through the public API with the per-step inputs coming from pinned
     host memory and the results read back: new-token stacks, queries, lengths
     (host->device) and out/lse (device->host)."""
-    i = step.inp
-    host_in = {k: i[k].cpu().pin_memory() for k in ("x_k", "x_v", "seq_lens", "q_pos")}
-    host_q = step.q.cpu().pin_memory()
-    host_out = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
-    host_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_q.numel() * host_q.element_size()
+    # every layer buffer's new-token stacks, the lengths, every layer's queries in; the
+    # last layer's out / lse back (all of them for a one-layer step)
+    pairs = [(b[k], b[k].cpu().pin_memory()) for b in step.bufs for k in ("x_k", "x_v")]
+    pairs += [(step.inp[k], step.inp[k].cpu().pin_memory()) for k in ("seq_lens", "q_pos")]
+    pairs.append((step.qL, step.qL.cpu().pin_memory()))
+    out_dev, lse_dev = step.outL[-1], step.lseL[-1]
+    host_out = torch.empty(out_dev.shape, dtype=torch.float32).pin_memory()
+    host_lse = torch.empty(lse_dev.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
     d2h = host_out.numel() * 4 + host_lse.numel() * 4
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        for k, v in host_in.items():
-            i[k].copy_(v, non_blocking=True)
-        step.q.copy_(host_q, non_blocking=True)
+        for dev, h in pairs:
+            dev.copy_(h, non_blocking=True)
         step.run()
-        host_out.copy_(step.out, non_blocking=True)
-        host_lse.copy_(step.lse, non_blocking=True)
+        host_out.copy_(out_dev, non_blocking=True)
+        host_lse.copy_(lse_dev, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     dt = time.perf_counter() - t0
     return dt, h2d, d2h
@@ -422,42 +482,57 @@ def oracle_prefill_sample(w, inp_dev, x_dev, budget_s=8.0):
                       "both axes, in %.2f s" % (S, x_dev[0].shape[0], w.H, dt)}
 
 
-def run_ours(args, dist_on, rank, world, device):
-    w = WORKLOADS[args.workload]
-    lla_build.build()
-    lla.lib()
+def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
+    """Time ``steps`` steps of workload ``w`` (``layers`` layers per step) after
+    ``args.warmup`` warm-up steps; the result line's measured fields.  ``legs`` runs
+    the optional legs the arguments ask for (window, eviction, prefill)."""
     step = DecodeStep(w, 20260000 + 1 + 1000 * rank, device, window=args.window, decoupled=args.decoupled,
-                      paged=args.paged)
-    for _ in range(args.warmup):
-        step.run()
-    torch.cuda.synchronize()
-    st = lla.device_status(step.ws)
-    if st != lla.LLA_OK:
-        raise RuntimeError("device status after warm-up: " + lla.status_string(st))
-
+                      paged=args.paged, layers=layers, prefill=legs and args.prefill)
     T = w.T
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(T)] for _ in range(3)]
-          for _ in range(args.steps)]
+    LT = T * layers
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(LT)] for _ in range(3)]
+          for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
+        clk.wait_live()
+        for _ in range(args.warmup):
+            step.run()
+        torch.cuda.synchronize()
+        st = lla.device_status(step.ws)
+        if st != lla.LLA_OK:
+            raise RuntimeError("device status after warm-up: " + lla.status_string(st))
         barrier(dist_on)
         torch.cuda.synchronize()
+        h0 = time.perf_counter()
         start.record()
-        for k in range(args.steps):
+        for k in range(steps):
             step.run(ev[k])
         stop.record()
         torch.cuda.synchronize()
+        h1 = time.perf_counter()
+        clocks = clk.summary(h0, h1)
+        if clocks["samples"] < 3:
+            # a timed region shorter than three samples: the same step, untimed, right
+            # after it for about 0.4 s, and the clock record taken over those repeats
+            h2 = time.perf_counter()
+            while time.perf_counter() - h2 < 0.4:
+                for _ in range(max(1, min(steps, 50))):
+                    step.run()
+                torch.cuda.synchronize()
+            clocks = clk.summary(h2, time.perf_counter())
+            clocks["window"] = "untimed repeats of the step right after the timed region (%.0f ms, shorter " \
+                               "than three %d ms samples)" % ((h1 - h0) * 1e3, clk.PERIOD_MS)
         barrier(dist_on)
     elapsed = start.elapsed_time(stop) / 1e3
     st = lla.device_status(step.ws)
     if st != lla.LLA_OK:
         raise RuntimeError("device status after timing: " + lla.status_string(st))
     t_max = max_over_ranks(elapsed, dist_on, device)
-    tokens_all = sum_over_ranks(float(step.tokens * T * args.steps), dist_on, device)
+    tokens_all = sum_over_ranks(float(step.tokens * LT * steps), dist_on, device)
     value = tokens_all / t_max
 
     # dominant kernel: the decode call (main kernel + its small combine), timed per launch
-    durs = [ev[k][0][t].elapsed_time(ev[k][1][t]) / 1e3 for k in range(args.steps) for t in range(T)]
+    durs = [ev[k][0][t].elapsed_time(ev[k][1][t]) / 1e3 for k in range(steps) for t in range(LT)]
     t_call = float(np.mean(durs))
     hbm, tflops, src = peaks()
     if args.decoupled:
@@ -511,10 +586,10 @@ def run_ours(args, dist_on, rank, world, device):
                 "launch_ms": t_call * 1e3, "peak_source": src + " (bf16 sustained)"}
 
     win = None
-    if args.window > 0:
+    if legs and args.window > 0:
         # exact-window call: window K/V + query read, out / lse read and written
         wdur = float(np.mean([ev[k][1][t].elapsed_time(ev[k][2][t]) / 1e3
-                              for k in range(args.steps) for t in range(T)]))
+                              for k in range(steps) for t in range(T)]))
         esz = 2 if w.dtype == "bf16" else 4
         wtok = int(step.win["win_len"].sum().item())
         wbytes = wtok * w.H * 2 * w.d * esz + w.B * w.H * (w.d * esz + 2 * (w.d + 1) * 4)
@@ -525,7 +600,7 @@ def run_ours(args, dist_on, rank, world, device):
                             "algorithmic_bytes_per_launch": wbytes, "peak_source": src}}
 
     evi = None
-    if args.evict:
+    if legs and args.evict:
         # token eviction composed with LLA (sink + window budget): lla_evict_window on the
         # layer (lengths restored before each call, outside the events), then one decode
         # call per loop over the kept budget
@@ -575,35 +650,72 @@ def run_ours(args, dist_on, rank, world, device):
                                       "value": kept / t_dec, "unit": UNIT}}
 
     pre = None
-    if args.prefill:
+    if legs and args.prefill:
         with ClockSampler(torch.cuda.current_device()) as pclk:
+            pclk.wait_live()
             pre = prefill_run(step, max(3, min(args.steps, 10)), hbm, src)
         pre["clocks"] = pclk.summary()
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             pre["cpu_baseline"] = oracle_prefill_sample(w, step.inp, step.prefill_x)
 
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = max(3, min(steps, 200))
     e2e_dt, h2d, d2h = e2e_run(step, e2e_steps)
     e2e_dt = max_over_ranks(e2e_dt, dist_on, device)
-    e2e_val = sum_over_ranks(float(step.tokens * T * e2e_steps), dist_on, device) / e2e_dt
+    e2e_val = sum_over_ranks(float(step.tokens * LT * e2e_steps), dist_on, device) / e2e_dt
 
     res = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": t_max / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": arm_config(w, args, step.tokens, world),
+        "config": arm_config(w, args, step.tokens, world, layers),
+        **({"layer_buffers": len(step.bufs)} if layers > 1 else {}),
         "roofline": roof,
         **({"window": win} if win else {}),
         **({"evict": evi} if evi else {}),
         **({"prefill": pre} if pre else {}),
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": step.launches() * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": step.launches() * steps,
+        "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = oracle_sample(w, step.inp, step.q,
                                             k_rope=step.k_rope if args.decoupled else None,
                                             dense=step.dense_view)
+    del step
+    torch.cuda.empty_cache()
+    return res
+
+
+# the second Ouro-1.4B 4k-context workload, measured beside the headline in the default run
+SECOND = "ouro1.4b_rho21_b768_4k"
+SECOND_MAX_STEPS = 40
+
+
+def step_layers(args, w):
+    """Layers per step: --layers, else the workload's stack (one layer when an optional
+    leg that works on a single layer is asked for)."""
+    if args.layers:
+        return args.layers
+    if args.window or args.decoupled or args.paged or args.evict or args.prefill:
+        return 1
+    return w.layers
+
+
+def run_ours(args, dist_on, rank, world, device):
+    w = WORKLOADS[args.workload]
+    lla_build.build()
+    lla.lib()
+    res = measure(args, w, args.steps, step_layers(args, w), dist_on, rank, world, device)
+    if (args.workload == DEFAULT_WORKLOAD and not args.no_second and not
+            (args.window or args.decoupled or args.paged or args.evict or args.prefill or args.layers)):
+        # rho = 21.3 at serving batch (768 x 4096), the full step of its 24-layer stack:
+        # 24 new-token encodes and 96 decode calls (the other Ouro-1.4B 4k workload)
+        w2 = WORKLOADS[SECOND]
+        n2 = min(args.steps, SECOND_MAX_STEPS)
+        sub = measure(args, w2, n2, w2.layers, dist_on, rank, world, device, legs=False)
+        res[SECOND.split("_", 1)[1].rsplit("_", 1)[0]] = {
+            k: sub[k] for k in ("value", "unit", "steps", "warmup", "ms_per_step", "config", "layer_buffers",
+                                "roofline", "e2e", "gpu_launches", "clocks", "cpu_baseline") if k in sub}
     return res
 
 
@@ -614,7 +726,10 @@ def run_reference(args):
     workload per step (first sequence, all heads, one loop per step, cycling t)."""
     import oracle
     w = WORKLOADS[args.workload]
-    inp = make_decode_inputs(w, 20260000 + 1, device="cuda" if torch.cuda.is_available() else "cpu")
+    # drawn exactly as the GPU arm's step draws it (with the new-token stacks), so the
+    # lengths, and hence the config, are the same
+    inp = make_decode_inputs(dataclasses.replace(w, N_encode=min(w.N_encode, w.B)), 20260000 + 1,
+                             device="cuda" if torch.cuda.is_available() else "cpu", with_encode=True)
     odm = oracle.dims(w.T, w.H, w.d, w.r_k, w.r_v, w.variant, w.rope_base)
     S = 1
     ck, cv, q = widen(inp["cache_k"][:S]), widen(inp["cache_v"][:S]), widen(inp["q"][:S])
@@ -633,7 +748,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": arm_config(w, args, int(inp["seq_lens"].sum().item()),
-                                 int(os.environ.get("WORLD_SIZE", "1"))),
+                                 int(os.environ.get("WORLD_SIZE", "1")), step_layers(args, w)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -645,8 +760,12 @@ def main():
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ouro1.4b_rho4_b32_4k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers per step (default: the workload's stack; buffers cycle when it exceeds HBM)")
+    ap.add_argument("--no-second", action="store_true",
+                    help="skip the second Ouro-1.4B 4k workload the default run measures (rho = 21.3, 768 x 4096)")
     ap.add_argument("--window", type=int, default=0,
                     help="also run lla_window_attn over an exact window of this many newest tokens")
     ap.add_argument("--evict", default="",
