@@ -166,38 +166,72 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // MMA runs of each axis: all 64-wide W chunks in one MMA (N up to 256), then the
+      // 32- and 16-wide chunk alone.  Descriptors are built once, for ring stage 0; a
+      // stage and a k-step only add offsets (building a descriptor per MMA made the
+      // issuing thread, not the tensor pipe, set the rate).
+      uint64_t rdesc[2][3];
+      uint32_t ridesc[2][3], rcol[2][3], rkstep[2][3];
+      int nrun[2];
+#pragma unroll
+      for (int ax = 0; ax < 2; ++ax) {
+        const ChunkPlan& bp = ax == 0 ? P.bk : P.bv;
+        int c = 0, n = 0;
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+          rdesc[ax][r] = 0; ridesc[ax][r] = 0; rcol[ax][r] = 0; rkstep[ax][r] = 0;
+          if (c < bp.n) {
+            const int w = bp.width[c];
+            int nch = 1;
+            if (w == 64) while (c + nch < bp.n && bp.width[c + nch] == 64 && nch < 4) ++nch;
+            const int rb = w * 2;
+            rdesc[ax][r] = umma_desc(sbase + P.ring + P.b_off + bp.off[c], 64 * rb, 8 * rb, sw_mode_for_row_bytes(rb));
+            ridesc[ax][r] = umma_idesc_bf16(128, w * nch, false, true);
+            rcol[ax][r] = static_cast<uint32_t>(bp.start[c]);
+            rkstep[ax][r] = static_cast<uint32_t>(16 * rb) >> 4;
+            c += nch;
+            n = r + 1;
+          }
+        }
+        nrun[ax] = n;
+      }
+      const uint64_t adesc = umma_desc(sbase + P.ring + P.a_off, 16, 1024, kSw128);
+      const uint32_t stage16 = static_cast<uint32_t>(P.stage) >> 4;
       uint32_t g = 0;
       bool ok = true;
       int64_t j = 0;
       for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++j) {
         const EncodeUnit e = encode_unit(u, a.H);
-        const ChunkPlan& bp = e.axis == 0 ? P.bk : P.bv;
+        const int nr = e.axis == 0 ? nrun[0] : nrun[1];
+        uint64_t bdesc[3];
+        uint32_t idesc[3], col[3], kstep[3];
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+          bdesc[r] = e.axis == 0 ? rdesc[0][r] : rdesc[1][r];
+          idesc[r] = e.axis == 0 ? ridesc[0][r] : ridesc[1][r];
+          col[r] = e.axis == 0 ? rcol[0][r] : rcol[1][r];
+          kstep[r] = e.axis == 0 ? rkstep[0][r] : rkstep[1][r];
+        }
         const int ab = acc_buf(j);
         // the epilogue has read this accumulator's previous unit out of TMEM
         if (!(ok = mbar_wait(bar(misc->dempty[ab]), (acc_use(j) & 1) ^ 1, abort, a.status))) break;
         tc_fence_after();
         const uint32_t acc = tmem + static_cast<uint32_t>(ab * P.acc_stride);
+        uint32_t s = g % S;
         for (int kb = 0; kb < KB; ++kb, ++g) {
-          const uint32_t s = g % S;
           if (!(ok = mbar_wait(bar(misc->full[s]), (g / S) & 1, abort, a.status))) break;
           tc_fence_after();
-          const uint32_t st = sbase + P.ring + s * P.stage;
+          const uint32_t so = s * stage16;
+#pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = umma_desc(st + P.a_off + k * 32, 16, 1024, kSw128);
-            // N-runs: up to four 64-wide chunks per MMA, narrower chunks alone
-            for (int c = 0; c < bp.n;) {
-              const int w = bp.width[c];
-              int nch = 1;
-              if (w == 64) while (c + nch < bp.n && bp.width[c + nch] == 64 && nch < 4) ++nch;
-              const int rb = w * 2;
-              const uint64_t bd = umma_desc(st + P.b_off + bp.off[c] + k * 16 * rb, 64 * rb, 8 * rb,
-                                            sw_mode_for_row_bytes(rb));
-              umma_bf16(acc + bp.start[c], ad, bd, umma_idesc_bf16(128, w * nch, false, true),
-                        (kb > 0 || k > 0) ? 1u : 0u);
-              c += nch;
-            }
+#pragma unroll
+            for (int r = 0; r < 3; ++r)
+              if (r < nr)
+                umma_bf16(acc + col[r], adesc + so + 2 * k, bdesc[r] + so + k * kstep[r], idesc[r],
+                          (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(bar(misc->empty[s]));
+          s = s + 1 == S ? 0 : s + 1;
         }
         if (ok) umma_commit(bar(misc->dfull[ab]));
       }
@@ -216,39 +250,59 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
       const EncodeUnit e = encode_unit(u, a.H);
       const int r = e.axis == 0 ? a.r_k : a.r_v;
       const int ab = acc_buf(j);
-      if (!warp_wait(bar(misc->dfull[ab]), acc_use(j) & 1, abort, a.status)) break;
-      tc_fence_after();
+      // this lane's token slot is read before the accumulator wait, so the load's
+      // latency hides behind the unit's MMAs
       const int n = e.tile * 128 + row;
       int sid = -1, p = -1;
       if (n < a.N) {
         sid = __ldg(a.seq_idx + n);
         p = __ldg(a.pos + n);
-        if (!slot_ok(a, sid, p)) record_status(a.status, LLA_ERR_DEVICE_ARG);
       }
+      if (!warp_wait(bar(misc->dfull[ab]), acc_use(j) & 1, abort, a.status)) break;
+      tc_fence_after();
+      if (n < a.N && !slot_ok(a, sid, p)) record_status(a.status, LLA_ERR_DEVICE_ARG);
       const int64_t drow = n < a.N && slot_ok(a, sid, p)
                                ? latent_row_for_write(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max,
                                                       a.H, sid, e.h, p, a.status)
                                : -1;
       const bool write = drow >= 0;
-      const float* bias = a.bias + (static_cast<int64_t>(e.axis) * a.H + e.h) * 256;
+      const float4* bias4 = reinterpret_cast<const float4*>(a.bias + (static_cast<int64_t>(e.axis) * a.H + e.h) * 256);
       __nv_bfloat16* dst =
           static_cast<__nv_bfloat16*>(e.axis == 0 ? a.cache_k : a.cache_v) + (write ? drow : 0) * r;
       const uint32_t acc = tmem + static_cast<uint32_t>(ab * P.acc_stride) + lane_base;
-      for (int c0 = 0; c0 < r; c0 += 16) {
-        float v[16];
-        tmem_ld_x16(acc + c0, v);   // every lane of the warp takes part
-        tmem_wait_ld();
-        if (write) {
-          uint32_t wds[8];
+      // 32 columns per TMEM load (a 16-column tail when r is an odd multiple of 16);
+      // the bias columns load while the TMEM load is in flight
+      for (int c0 = 0; c0 < r; c0 += 32) {
+        const bool full32 = r - c0 >= 32;
+        float v[32], v16[16], bb[32];
+        if (full32)
+          tmem_ld_x32(acc + c0, v);   // every lane of the warp takes part
+        else
+          tmem_ld_x16(acc + c0, v16);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i] - bias[c0 + 2 * i],
-                                                            v[2 * i + 1] - bias[c0 + 2 * i + 1]);
+        for (int i = 0; i < 8; ++i) {
+          const float4 t = (full32 || i < 4) ? __ldg(bias4 + (c0 >> 2) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          bb[4 * i] = t.x; bb[4 * i + 1] = t.y; bb[4 * i + 2] = t.z; bb[4 * i + 3] = t.w;
+        }
+        tmem_wait_ld();
+        if (!full32) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = v16[i];
+        }
+        if (write) {
+          uint32_t wds[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i] - bb[2 * i], v[2 * i + 1] - bb[2 * i + 1]);
             wds[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
           uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
           d4[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
           d4[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+          if (full32) {
+            d4[2] = make_uint4(wds[8], wds[9], wds[10], wds[11]);
+            d4[3] = make_uint4(wds[12], wds[13], wds[14], wds[15]);
+          }
         }
       }
       // this warp's rows are out of the accumulator: the MMA thread may reuse it

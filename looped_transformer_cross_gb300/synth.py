@@ -72,7 +72,7 @@ WORKLOADS = {
     # the same layer at 64 sequences (0.4 GB of latents, above L2): the profiling case
     "ouro1.4b_rho21_b64_4k": Workload("ouro1.4b_rho21_b64_4k", T=4, H=16, d=128, r_k=16,
                                       r_v=32, B=64, L_max=4096, len_lo=4096, len_hi=4096,
-                                      layers=24, N_encode=64),
+                                      N_encode=64),
     # long context: 64 sequences x 16384, 48-layer stack, prefill encode of every token
     "ouro_rho4_b64_16k": Workload("ouro_rho4_b64_16k", T=4, H=16, d=128, r_k=96, r_v=160,
                                   B=64, L_max=16384, len_lo=16384, len_hi=16384, layers=48,
@@ -80,11 +80,11 @@ WORKLOADS = {
     # the long-context layer with 8 sequences (1.07 GB of latents): the case for kernel
     # profiles at 16k tokens per sequence
     "ouro_rho4_b8_16k": Workload("ouro_rho4_b8_16k", T=4, H=16, d=128, r_k=96, r_v=160,
-                                 B=8, L_max=16384, len_lo=16384, len_hi=16384, layers=48),
+                                 B=8, L_max=16384, len_lo=16384, len_hi=16384),
     # the long-context prefill at 4 sequences (65,536 tokens x 16 heads, 2.1 GB of x):
     # the case for profiles of the prefill encode
     "ouro_rho4_b4_16k": Workload("ouro_rho4_b4_16k", T=4, H=16, d=128, r_k=96, r_v=160,
-                                 B=4, L_max=16384, len_lo=16384, len_hi=16384, layers=48,
+                                 B=4, L_max=16384, len_lo=16384, len_hi=16384,
                                  N_encode=4 * 16384),
     # LLA-2D: one latent per token for all heads, r = (128, 256), 256 x 8192
     "lla2d_b256_8k": Workload("lla2d_b256_8k", T=4, H=16, d=128, r_k=128, r_v=256, B=256,
