@@ -314,8 +314,14 @@ class DecodeStep:
 
     # launches of this library's kernels per step: encode (bias + GEMM) + T x (query
     # images + decode + combine [+ window]); decoupled: query records + decode + combine
+    def gathers_rows(self):
+        """True when the paged decode runs the row-gathering kernel (tile-kernel shapes
+        in pages that are neither a multiple of 128 tokens nor 8, 16, 32 or 64)."""
+        P = self.paged
+        return bool(P) and lla.decode_kernel(self.dm) == "tile" and not (P % 128 == 0 or (P % 8 == 0 and 128 % P == 0))
+
     def launches(self):
-        per = 3
+        per = 1 if self.gathers_rows() else 3
         return (2 + (per + (1 if self.window > 0 else 0)) * self.w.T) * self.nlayers
 
 
@@ -562,9 +568,12 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
         traffic = per_th * step.tokens * w.H if same_src and not args.paged else None
         kern = "decode_small_kernel" if small else "decode_bf16_kernel"
         zk = "decode_small_z_kernel" if small else "decode_z_kernel"
+        kname = "lla_decode_attn (%s + %s + decode_combine_kernel)" % (zk, kern)
+        if step.gathers_rows():
+            kern, kname = "decode_paged_generic_kernel", "lla_decode_attn_paged (decode_paged_generic_kernel)"
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic, "traffic_kernel": kern,
-                "kernel": "lla_decode_attn (%s + %s + decode_combine_kernel)" % (zk, kern),
+                "kernel": kname,
                 "algorithmic_bytes_per_launch": lat_bytes, "launch_ms": t_call * 1e3,
                 "peak_source": src}
     else:

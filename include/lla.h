@@ -171,8 +171,11 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
  * entries of pages that hold written or read tokens are looked at; an entry
  * outside [0, num_pages) records LLA_ERR_DEVICE_ARG (reads then use a page
  * inside the pool, writes are skipped), so no access leaves the pool.  Per-head variant only;
- * the bf16 kernels need page_size to be a multiple of 128 (a 128-token tile
- * never straddles pages), the fp32 mode takes any page_size >= 1. */
+ * any page_size >= 1 in both storage types.  In bf16 the tile kernel copies a
+ * 128-token tile whole when page_size is a multiple of 128, as 128/P page pieces when
+ * P is 8, 16, 32 or 64, and other page sizes (one-token pages, as vLLM's) run a
+ * kernel that gathers token rows one by one (correct, much slower); the small-rank
+ * kernel copies each tile's rows page by page at any page size. */
 typedef struct {
     void* k;
     void* v;
@@ -189,7 +192,7 @@ typedef struct {
  * head h of page block_table[b][j / page_size].  Every other argument, result
  * and rule is that of the dense call with L_max = max_pages * page_size (the
  * workspace is lla_workspace_size(dims, B, max_pages * page_size, N)).
- * LLA_ERR_UNSUPPORTED: LLA-2D, or bf16 with page_size not a multiple of 128.
+ * LLA_ERR_UNSUPPORTED: LLA-2D.
  */
 lla_status lla_encode_paged(const lla_dims* dims, const void* x_k, const void* x_v, int N,
                             const int32_t* seq_idx, const int32_t* pos,

@@ -229,7 +229,6 @@ CacheView dense_view(const lla_cache& c) { return CacheView{c.k, c.v, c.B, c.L_m
 lla_status paged_view(const lla_dims* dims, const lla_paged_cache& c, CacheView* v) {
   if (c.B < 0 || c.max_pages < 1 || c.page_size < 1 || c.num_pages < 1) return LLA_ERR_INVALID_ARG;
   if (dims->variant != LLA_PER_HEAD) return LLA_ERR_UNSUPPORTED;
-  if (dims->dtype == LLA_BF16 && c.page_size % kTile != 0) return LLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(c.max_pages) * c.page_size > (int64_t(1) << 30) ||
       c.num_pages * static_cast<int64_t>(dims->H) >= (int64_t(1) << 31) ||
       static_cast<int64_t>(c.B) * c.max_pages >= (int64_t(1) << 31))
@@ -359,6 +358,8 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   // page_size, z = page H + h)
   const uint64_t rows = static_cast<uint64_t>(cache.bt ? cache.page_size : cache.L_max);
   const uint64_t units = cache.bt ? static_cast<uint64_t>(cache.num_pages) * H : static_cast<uint64_t>(cache.B) * H;
+  // a TMA box is one tile, or one page when pages are smaller than a tile
+  const uint32_t box_rows = static_cast<uint32_t>(cache.bt && cache.page_size < kTile ? cache.page_size : kTile);
   if (small_path(dims)) {
     // small ranks: positions split over the CTAs, every head of a position in one CTA
     make_decode_small_plan(H, dims->r_k, dims->r_v, &a.splan);
@@ -371,6 +372,11 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
     return launch_decode_small_bf16(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   }
   if (!make_decode_plan(dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
+  if (cache.bt && !tile_kernel_page_size(cache.page_size)) {
+    // pages the tile kernel's copies do not take: rows gathered one by one
+    if (!ready()) return LLA_ERR_CUDA;
+    return launch_decode_paged_generic(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  }
   const int64_t max_tiles = static_cast<int64_t>(cache.B) * H * ((cache.L_max + kTile - 1) / kTile);
   a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_tiles)));
   DecodeMaps maps;
@@ -378,11 +384,11 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   for (int c = 0; c < a.plan.kplan.n; ++c) {
     const int w = a.plan.kplan.width[c];
     if (!make_map_3d(&maps.k[chunk_map_index(w)], cache.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_k, rows,
-                     units, w, kTile, 1))
+                     units, w, box_rows, 1))
       return LLA_ERR_CUDA;
   }
   // V latents: 32-column boxes (a tail box zero-filled past r_v), 64B swizzle
-  if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 32, kTile, 1))
+  if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 32, box_rows, 1))
     return LLA_ERR_CUDA;
   if (!ready()) return LLA_ERR_CUDA;
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;

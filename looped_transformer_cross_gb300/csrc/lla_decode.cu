@@ -84,6 +84,32 @@ __device__ __forceinline__ void tile_yz(const DecodeArgs& a, int b, int h, int t
   y = j - lp * a.page_size;
 }
 
+// One latent tile (K or V: chunk plan `cp`, map of chunk c from `map_of`) of (sequence
+// b, head h, tile t; L tokens) from the page pool into `dst`, completing on `fb`.  A
+// tile inside one page is one box per chunk; with pages of P < 128 tokens (P a
+// multiple of 8 dividing 128, so every piece starts on a swizzle atom) it is one box
+// of P rows per chunk and page, and only the pages holding tokens below L are read.
+template <bool kPieces, typename MapOf>
+__device__ __forceinline__ void paged_tile_load(const DecodeArgs& a, int b, int h, int t, int L, uint32_t dst,
+                                                uint32_t fb, const ChunkPlan& cp, MapOf map_of) {
+  if constexpr (!kPieces) {
+    mbar_arrive_expect_tx(fb, cp.bytes);
+    int y, z;
+    tile_yz(a, b, h, t, y, z);
+    for (int c = 0; c < cp.n; ++c) tma_load_3d(dst + cp.off[c], map_of(c), fb, cp.start[c], y, z);
+    return;
+  }
+  const int pg = a.page_size;
+  const int np = (min(kTile, L - t * kTile) + pg - 1) / pg;
+  mbar_arrive_expect_tx(fb, static_cast<uint32_t>(cp.bytes / kTile * pg * np));
+  const int lp0 = t * (kTile / pg);
+  for (int i = 0; i < np; ++i) {
+    const int z = page_of(a, b, lp0 + i) * a.H + h;
+    for (int c = 0; c < cp.n; ++c)
+      tma_load_3d(dst + cp.off[c] + i * pg * cp.width[c] * 2, map_of(c), fb, cp.start[c], 0, z);
+  }
+}
+
 // Row of token j of unit (b, h) for the fp32 kernels (LLA-2D: one latent per token).
 __device__ __forceinline__ int64_t f32_row(const DecodeArgs& a, int b, int h, int64_t j) {
   if (a.shared_latent) return static_cast<int64_t>(b) * a.L_max + j;
@@ -211,7 +237,9 @@ __global__ void __launch_bounds__(kZThreads) decode_z_kernel(const __grid_consta
   }
 }
 
-template <bool kPaged>
+// kPage: 0 dense cache, 1 page pool with a tile inside one page (pages of a multiple
+// of 128 tokens), 2 page pool with tiles cut into page pieces (pages of 8..64 tokens)
+template <int kPage>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ DecodeMaps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -354,12 +382,16 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           const int sk = kr.slot;
           if (!mbar_wait(bar(misc->kempty[sk]), kr.phase ^ 1u, abort, a.status)) break;
           const uint32_t kb = bar(misc->kfull[sk]);
-          mbar_arrive_expect_tx(kb, P.kplan.bytes);
-          int y = wk.t * kTile, z = wk.b * a.H + wk.h;
-          if constexpr (kPaged) tile_yz(a, wk.b, wk.h, wk.t, y, z);
-          for (int c = 0; c < P.kplan.n; ++c)
-            tma_load_3d(k_ring + sk * P.k_stage + P.kplan.off[c], &maps.k[chunk_map_index(P.kplan.width[c])],
-                        kb, P.kplan.start[c], y, z);
+          if constexpr (kPage != 0) {
+            paged_tile_load<kPage == 2>(a, wk.b, wk.h, wk.t, wk.L, k_ring + sk * P.k_stage, kb, P.kplan,
+                            [&](int c) { return &maps.k[chunk_map_index(P.kplan.width[c])]; });
+          } else {
+            mbar_arrive_expect_tx(kb, P.kplan.bytes);
+            const int y = wk.t * kTile, z = wk.b * a.H + wk.h;
+            for (int c = 0; c < P.kplan.n; ++c)
+              tma_load_3d(k_ring + sk * P.k_stage + P.kplan.off[c], &maps.k[chunk_map_index(P.kplan.width[c])],
+                          kb, P.kplan.start[c], y, z);
+          }
           issued_k = i + 1;
           kr.next(P.SK);
           walker_advance(wk, a);
@@ -369,11 +401,14 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           const int sv = vr.slot;
           if (!mbar_wait(bar(misc->vempty[sv]), vr.phase ^ 1u, abort, a.status)) break;
           const uint32_t vb = bar(misc->vfull[sv]);
-          mbar_arrive_expect_tx(vb, P.vplan.bytes);
           const uint32_t vs = v_ring + sv * P.v_stage;
-          int y = wv.t * kTile, z = wv.b * a.H + wv.h;
-          if constexpr (kPaged) tile_yz(a, wv.b, wv.h, wv.t, y, z);
-          for (int c = 0; c < P.vplan.n; ++c) tma_load_3d(vs + P.vplan.off[c], &maps.v, vb, P.vplan.start[c], y, z);
+          if constexpr (kPage != 0) {
+            paged_tile_load<kPage == 2>(a, wv.b, wv.h, wv.t, wv.L, vs, vb, P.vplan, [&](int) { return &maps.v; });
+          } else {
+            mbar_arrive_expect_tx(vb, P.vplan.bytes);
+            const int y = wv.t * kTile, z = wv.b * a.H + wv.h;
+            for (int c = 0; c < P.vplan.n; ++c) tma_load_3d(vs + P.vplan.off[c], &maps.v, vb, P.vplan.start[c], y, z);
+          }
           issued_v = j + 1;
           vr.next(P.SV);
           walker_advance(wv, a);
@@ -1011,14 +1046,15 @@ bool make_decode_plan(int r_k, int r_v, DecodePlan* p) {
 }
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s) {
-  // the dense-cache instantiation carries no page lookup in its producer
-  const bool paged = a.block_table != nullptr;
-  auto kern = paged ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
-  static int configured[2] = {0, 0};
-  if (configured[paged] < a.plan.bytes) {
+  // the dense-cache instantiation carries no page lookup in its producer, the
+  // whole-page one no piece loop
+  const int page = a.block_table == nullptr ? 0 : a.page_size >= kTile ? 1 : 2;
+  auto kern = page == 0 ? decode_bf16_kernel<0> : page == 1 ? decode_bf16_kernel<1> : decode_bf16_kernel<2>;
+  static int configured[3] = {0, 0, 0};
+  if (configured[page] < a.plan.bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.plan.bytes);
     if (e != cudaSuccess) return e;
-    configured[paged] = a.plan.bytes;
+    configured[page] = a.plan.bytes;
   }
   decode_z_kernel<<<a.B * a.H, kZThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();

@@ -369,22 +369,30 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
           ++run;
         }
         const uint32_t rows = static_cast<uint32_t>(min(kTile, w.L - w.t * kTile));
-        // rows of head h: (z0 + h) * zrows + y0 (dense: z0 = b H; paged: the tile's page)
-        int64_t z0 = static_cast<int64_t>(w.b) * H, zrows = a.L_max, y0 = static_cast<int64_t>(w.t) * kTile;
-        if constexpr (kPaged) {
-          const int lp = static_cast<int>(y0 / a.page_size);
-          z0 = static_cast<int64_t>(page_of(a, w.b, lp)) * H;
-          zrows = a.page_size;
-          y0 -= static_cast<int64_t>(lp) * a.page_size;
-        }
+        // rows of head h: (z0 + h) * zrows + y0 (dense: z0 = b H)
+        const int64_t z0 = static_cast<int64_t>(w.b) * H, zrows = a.L_max, y0 = static_cast<int64_t>(w.t) * kTile;
         for (int h = 0; h < H && ok; ++h) {
           if (!(ok = mbar_wait(bar(misc->empty[sp.slot]), sp.phase ^ 1u, abort, a.status))) break;
           const uint32_t fb = bar(misc->full[sp.slot]);
           mbar_arrive_expect_tx(fb, rows * (KB + VB));
           const uint32_t dst = sbase + P.ring + sp.slot * P.slot;
-          const int64_t r0 = (z0 + h) * zrows + y0;
-          bulk_load(dst, static_cast<const uint8_t*>(a.cache_k) + r0 * KB, rows * KB, fb);
-          bulk_load(dst + P.k_tile, static_cast<const uint8_t*>(a.cache_v) + r0 * VB, rows * VB, fb);
+          if constexpr (kPaged) {
+            // one pair of copies per page the tile's rows lie in (pages of any size)
+            for (uint32_t j = 0; j < rows;) {
+              const int64_t tok = y0 + j;
+              const int lp = static_cast<int>(tok / a.page_size);
+              const uint32_t off = static_cast<uint32_t>(tok - static_cast<int64_t>(lp) * a.page_size);
+              const uint32_t span = min(static_cast<uint32_t>(a.page_size) - off, rows - j);
+              const int64_t r0 = (static_cast<int64_t>(page_of(a, w.b, lp)) * H + h) * a.page_size + off;
+              bulk_load(dst + j * KB, static_cast<const uint8_t*>(a.cache_k) + r0 * KB, span * KB, fb);
+              bulk_load(dst + P.k_tile + j * VB, static_cast<const uint8_t*>(a.cache_v) + r0 * VB, span * VB, fb);
+              j += span;
+            }
+          } else {
+            const int64_t r0 = (z0 + h) * zrows + y0;
+            bulk_load(dst, static_cast<const uint8_t*>(a.cache_k) + r0 * KB, rows * KB, fb);
+            bulk_load(dst + P.k_tile, static_cast<const uint8_t*>(a.cache_v) + r0 * VB, rows * VB, fb);
+          }
           ++issued;
           sp.next(1, P.NS);
         }

@@ -162,6 +162,16 @@ cudaError_t launch_decoupled_f32(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
 
+// Page sizes the tile kernel's copy path takes: whole tiles inside a page (a multiple
+// of 128 tokens) or a tile as 128/P pieces of P tokens (P a multiple of 8 dividing 128).
+__host__ __device__ inline bool tile_kernel_page_size(int P) {
+  return P > 0 && (P % 128 == 0 || (P % 8 == 0 && 128 % P == 0));
+}
+// bf16 decode over a paged cache of any page size (the tile kernel's other page sizes):
+// one CTA per (sequence, head), rows gathered through the block table.
+cudaError_t launch_decode_paged_generic(const DecodeArgs& a, cudaStream_t s);
+size_t decode_paged_generic_smem(int r_k, int r_v);
+
 // ----------------------------------------------------------------- exact window
 
 struct WindowArgs {

@@ -165,9 +165,6 @@ def test_paged_rejects_bad_arguments_on_host(L):
                                   None, 1 << 20, None)
 
     bf16, f32 = lla.dims(4, 2, 96, 160), lla.dims(4, 2, 96, 160, dtype=lla.LLA_F32)
-    assert dec(bf16, page_size=64) == lla.LLA_ERR_UNSUPPORTED      # bf16 tiles would straddle pages
-    assert dec(bf16, page_size=100) == lla.LLA_ERR_UNSUPPORTED
-    assert enc(bf16, page_size=64) == lla.LLA_ERR_UNSUPPORTED
     assert dec(lla.dims(4, 2, 96, 160, variant=lla.LLA_2D)) == lla.LLA_ERR_UNSUPPORTED
     assert dec(bf16, bt=None) == lla.LLA_ERR_INVALID_ARG
     assert dec(bf16, bt=ctypes.c_void_p(ctypes.addressof(tbl) + 2)) == lla.LLA_ERR_INVALID_ARG
@@ -175,8 +172,13 @@ def test_paged_rejects_bad_arguments_on_host(L):
     assert dec(bf16, num_pages=0) == lla.LLA_ERR_INVALID_ARG
     assert dec(bf16, page_size=0) == lla.LLA_ERR_INVALID_ARG
     assert dec(bf16, B=0) == lla.LLA_OK                              # nothing to do
-    # any page size passes the page checks in fp32 mode (then fails on the null pointers)
-    assert dec(f32, page_size=1) == lla.LLA_ERR_INVALID_ARG
+    # any page size passes the page checks, in both storage types (then the call fails
+    # on the null pointers)
+    for P in (1, 8, 16, 64, 100, 128, 256):
+        assert dec(bf16, page_size=P) == lla.LLA_ERR_INVALID_ARG
+        assert dec(f32, page_size=P) == lla.LLA_ERR_INVALID_ARG
+        assert enc(bf16, page_size=P) == lla.LLA_ERR_INVALID_ARG
+    assert dec(bf16, page_size=1, B=0) == lla.LLA_OK
     assert dec(f32, page_size=1, B=0) == lla.LLA_OK
 
 

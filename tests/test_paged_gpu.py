@@ -90,8 +90,11 @@ def _check(w, inp, pool_k, pool_v, bt, P, t, style=0):
     assert e_o <= TOL[w.dtype] and e_l <= TOL[w.dtype], (e_o, e_l)
 
 
-@pytest.mark.parametrize("P", [128, 256])
+@pytest.mark.parametrize("P", [1, 8, 16, 64, 100, 128, 256])
 def test_paged_decode_tile_kernel(P):
+    """The tile kernel's shapes in every kind of page: whole tiles inside a page
+    (128, 256), a tile as 128/P page pieces (8, 16, 64), and pages the tile copies do
+    not take, whose rows are gathered one by one (1: the vLLM setting, 100)."""
     w = workload(T=2, H=4, r_k=96, r_v=160, B=5, L_max=400)
     lens = [400, 1, 129, 0, 256]
     inp = make_decode_inputs(w, 700 + P, device="cuda", seq_lens=torch.tensor(lens, dtype=torch.int32))
@@ -102,14 +105,15 @@ def test_paged_decode_tile_kernel(P):
         _check(w, inp, pk, pv, bt, P, t)
 
 
-@pytest.mark.parametrize("style", [0, 1])
-def test_paged_decode_small_rank_kernel(style):
+@pytest.mark.parametrize("style,P", [(0, 128), (1, 128), (0, 1), (1, 16), (0, 24)])
+def test_paged_decode_small_rank_kernel(style, P):
+    """The small-rank kernel copies a head-tile's rows page by page, so it takes every
+    page size: one-token pages, 16, 24 (a page boundary inside a tile) and 128."""
     w = workload(T=2, H=4, r_k=16, r_v=32, B=4, L_max=300)
     lens = [300, 128, 0, 5]
-    P = 128
     inp = make_decode_inputs(w, 710 + style, device="cuda", seq_lens=torch.tensor(lens, dtype=torch.int32))
     assert lla.decode_kernel(lla_dims(w, style)) == "small-rank"
-    bt, npg = _table(lens, P, math.ceil(w.L_max / P), 711)
+    bt, npg = _table(lens, P, math.ceil(w.L_max / P), 711 + P)
     pk, pv = _pools(inp, bt, P, lens, npg)
     for t in range(w.T):
         _check(w, inp, pk, pv, bt, P, t, style)
@@ -142,7 +146,7 @@ def test_paged_decode_aliased_prefix():
     _check(w, inp, pk, pv, bt, P, 1)
 
 
-@pytest.mark.parametrize("dtype,P", [("bf16", 128), ("f32", 16)])
+@pytest.mark.parametrize("dtype,P", [("bf16", 128), ("bf16", 16), ("bf16", 1), ("f32", 16)])
 def test_paged_encode_layout_exact(dtype, P):
     """Selector W_down and small-integer x: every latent is one x entry exactly and
     lands in row pos % P of head h of page bt[seq][pos // P]; every other pool row
@@ -214,12 +218,12 @@ def test_paged_out_of_range_page_is_flagged():
     assert changed and all(c[0] == pg and c[2] == row for c in changed)
 
 
-def test_paged_bench_layer_sampled():
-    """The Ouro-1.4B rho = 4 layer (32 x 3584..4096) in 256-token pages, shuffled;
-    sequences 0 and 31 against the oracle."""
+@pytest.mark.parametrize("P", [256, 16])
+def test_paged_bench_layer_sampled(P):
+    """The Ouro-1.4B rho = 4 layer (32 x 3584..4096) in 256- and 16-token pages,
+    shuffled, in the launch the bench times; sequences 0 and 31 against the oracle."""
     w = WORKLOADS["ouro1.4b_rho4_b32_4k"]
     inp = make_decode_inputs(w, 760, device="cuda")
-    P = 256
     lens = inp["seq_lens"].cpu().numpy()
     max_pages = w.L_max // P
     bt, npg = _table(lens, P, max_pages, 761)
