@@ -39,11 +39,14 @@ from looped_transformer_cross_gb300.synth import (WORKLOADS, make_decode_inputs,
 METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe roofline"
 
 # DRAM bytes (read + write) of decode_bf16_kernel per latent token-head, from one ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the 8-sequence variant
-# of the bench layer.  Valid only for the decode source whose sha256 starts with
-# TRAFFIC_SRC_SHA; any other source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = (263.995136e6 + 3.399424e6) / (31042 * 16)
-TRAFFIC_SRC_SHA = "947cdee5130ef540"
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) each of the 8-sequence
+# variants of the 4k-context bench layer (ouro1.4b_rho4_b8_4k) and of the long-context
+# layer (ouro_rho4_b8_16k); a workload takes the capture of its context length.
+# Valid only for the decode source whose sha256 starts with TRAFFIC_SRC_SHA; any other
+# source reports traffic as unknown (null).
+TRAFFIC_PER_TOKEN_HEAD = {4096: (263.966208e6 + 3.191552e6) / (31042 * 16),
+                          16384: (1080.890368e6 + 3.592704e6) / (8 * 16384 * 16)}
+TRAFFIC_SRC_SHA = "45b84bcebf40e291"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D kernel, per latent token (all heads), from the 32-sequence
 # variant of the LLA-2D layer; valid only for the source whose sha256 starts with
@@ -53,8 +56,8 @@ TRAFFIC2D_SRC_SHA = "82da47c747901f36"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
 # Same for decode_small_kernel (the per-head kernel at small ranks), from a capture
 # of the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.847104e6 + 3.685632e6) / (64 * 4096 * 16)
-TRAFFIC_SMALL_SRC_SHA = "5c9c42836764a449"
+TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.880128e6 + 3.652096e6) / (64 * 4096 * 16)
+TRAFFIC_SMALL_SRC_SHA = "9491176ae68ec838"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 # Same for decoupled_bf16_kernel, per latent token-head (latent K and V rows plus the
 # rotary key), from the 8-sequence variant of the rho = 4 layer.
@@ -560,8 +563,9 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
         achieved = lat_bytes / t_call / 1e9
         import hashlib
         small = lla.decode_kernel(step.dm) == "small-rank"
+        per_tile = TRAFFIC_PER_TOKEN_HEAD[min(TRAFFIC_PER_TOKEN_HEAD, key=lambda L: abs(L - w.L_max))]
         src_file, sha, per_th = ((DECODE_SMALL_SRC, TRAFFIC_SMALL_SRC_SHA, TRAFFIC_SMALL_PER_TOKEN_HEAD)
-                                 if small else (DECODE_SRC, TRAFFIC_SRC_SHA, TRAFFIC_PER_TOKEN_HEAD))
+                                 if small else (DECODE_SRC, TRAFFIC_SRC_SHA, per_tile))
         with open(src_file, "rb") as f:
             same_src = sha is not None and hashlib.sha256(f.read()).hexdigest().startswith(sha)
         # (the counters were taken on the dense cache; a paged run reports none)

@@ -36,12 +36,16 @@ def _encode(w, x_k, x_v, seq_idx, pos, wdk, wdv, mu_k, mu_v, ck, cv):
     return lla.device_status(ws)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("rk,rv", [(96, 160), (16, 32), (48, 80), (256, 240)])
-def test_encode_layout_structured_exact(dtype, rk, rv):
+@pytest.mark.parametrize("dtype,rk,rv,N", [
+    ("bf16", 96, 160, 130), ("bf16", 16, 32, 130), ("bf16", 48, 80, 130), ("bf16", 256, 240, 130),
+    ("f32", 96, 160, 130), ("f32", 16, 32, 130), ("f32", 48, 80, 130), ("f32", 256, 240, 130),
+    # a batch of 33 tiles with a 4-token tail, spread over the persistent grid
+    ("bf16", 96, 160, 4100), ("bf16", 128, 256, 4100), ("bf16", 32, 64, 4100)])
+def test_encode_layout_structured_exact(dtype, rk, rv, N):
     """Selector W_down and small-integer x: every latent is one x entry exactly, it lands in
     slot (seq_idx[n], h, pos[n]) and every other slot keeps its canary."""
-    T, H, d, B, L_max, N = 2, 3, 128, 3, 200, 130   # N spans two token tiles
+    T, H, d, B = 2, 3, 128, 3
+    L_max = 200 if N <= 200 else 1400   # N spans two token tiles, or 33
     w = workload(T=T, H=H, r_k=rk, r_v=rv, B=B, L_max=L_max, dtype=dtype)
     sd = torch.bfloat16 if dtype == "bf16" else torch.float32
     g = np.random.default_rng(3)
@@ -75,13 +79,14 @@ def test_encode_layout_structured_exact(dtype, rk, rv):
         assert np.all(got[~touched] == CANARY)
 
 
-@pytest.mark.parametrize("rk,rv", [(96, 160), (16, 32)])
-def test_encode_random_vs_oracle_bf16(rk, rv):
+@pytest.mark.parametrize("rk,rv,N", [(96, 160, 300), (16, 32, 300), (96, 160, 4100)])
+def test_encode_random_vs_oracle_bf16(rk, rv, N):
     """Each GPU latent must be the bf16 rounding of a value within the fp32
     accumulation bound 2^-20 * sum_u |x_u - mu_u| |W_uk| of the exact sum (the
     kernel rounds an fp32 dot product of T*d terms), and almost all must equal the
-    oracle's fp64 sum rounded to bf16."""
-    T, H, d, B, L_max, N = 4, 4, 128, 4, 160, 300
+    oracle's fp64 sum rounded to bf16.  N = 4100: 33 tiles over the persistent grid."""
+    T, H, d, B = 4, 4, 128, 4
+    L_max = 160 if N <= 640 else 1100
     w = workload(T=T, H=H, r_k=rk, r_v=rv, B=B, L_max=L_max, N_encode=N)
     inp = make_decode_inputs(w, 31, device="cuda", with_encode=True)
     g = np.random.default_rng(4)
