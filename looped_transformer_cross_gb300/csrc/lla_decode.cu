@@ -99,11 +99,13 @@ __device__ __forceinline__ void paged_tile_load(const DecodeArgs& a, int b, int 
     for (int c = 0; c < cp.n; ++c) tma_load_3d(dst + cp.off[c], map_of(c), fb, cp.start[c], y, z);
     return;
   }
-  const int pg = a.page_size;
+  // (called by the whole producer warp: lane i issues the boxes of page i)
+  const int pg = a.page_size, lane = threadIdx.x & 31;
   const int np = (min(kTile, L - t * kTile) + pg - 1) / pg;
-  mbar_arrive_expect_tx(fb, static_cast<uint32_t>(cp.bytes / kTile * pg * np));
+  if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(cp.bytes / kTile * pg * np));
+  __syncwarp();
   const int lp0 = t * (kTile / pg);
-  for (int i = 0; i < np; ++i) {
+  for (int i = lane; i < np; i += 32) {
     const int z = page_of(a, b, lp0 + i) * a.H + h;
     for (int c = 0; c < cp.n; ++c)
       tma_load_3d(dst + cp.off[c] + i * pg * cp.width[c] * 2, map_of(c), fb, cp.start[c], 0, z);
@@ -361,7 +363,14 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     // unit % NZ once the score MMAs of the buffer's previous unit are done.  Per
     // tile: K tile i, then V tile i - vlag (a V stage is held until the tile's
     // softmax weights exist, so it is filled as late as still hides the load).
-    if (lane == 0) {
+    // With page pieces the whole warp runs the loop (lane 0 waits and the warp
+    // follows its decision) and each lane issues one page's boxes.
+    constexpr bool kWarp = kPage == 2;
+    auto pwait = [&](uint32_t b, uint32_t parity) -> bool {
+      if constexpr (kWarp) return warp_wait(b, parity, abort, a.status);
+      else return mbar_wait(b, parity, abort, a.status);
+    };
+    if (lane == 0 || kWarp) {
       Walker wk = start, wv = start;
       int issued_k = 0, issued_v = 0, issued_z = 0, unit = -1;
       RingPos kr, vr, zr;
@@ -370,17 +379,22 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           if (i == 0 || wk.t == 0) {
             if (++unit > 0) zr.next(P.NZ);
             const int zb = zr.slot;
-            if (unit >= P.NZ && !mbar_wait(bar(misc->zfree[zb]), zr.phase ^ 1u, abort, a.status)) break;
-            if (unit == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // images written
-            const uint32_t zf = bar(misc->zfull[zb]);
-            mbar_arrive_expect_tx(zf, P.kplan.bytes + 4096);
-            const uint8_t* img = a.zimg + static_cast<int64_t>(wk.b * a.H + wk.h) * a.zimg_stride;
-            bulk_load(sbase + P.z + zb * P.z_stage, img, P.kplan.bytes, zf);
-            bulk_load(sbase + P.aug_b + zb * 4096, img + P.kplan.bytes, 4096, zf);
+            if (unit >= P.NZ && !pwait(bar(misc->zfree[zb]), zr.phase ^ 1u)) break;
+            // images written.  Only the producer waits for decode_z_kernel's grid, so
+            // nothing that grid writes (images, the status word) may be read by another
+            // warp of this kernel: the others see its output only through these copies.
+            if (unit == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (!kWarp || lane == 0) {
+              const uint32_t zf = bar(misc->zfull[zb]);
+              mbar_arrive_expect_tx(zf, P.kplan.bytes + 4096);
+              const uint8_t* img = a.zimg + static_cast<int64_t>(wk.b * a.H + wk.h) * a.zimg_stride;
+              bulk_load(sbase + P.z + zb * P.z_stage, img, P.kplan.bytes, zf);
+              bulk_load(sbase + P.aug_b + zb * 4096, img + P.kplan.bytes, 4096, zf);
+            }
             issued_z = unit + 1;
           }
           const int sk = kr.slot;
-          if (!mbar_wait(bar(misc->kempty[sk]), kr.phase ^ 1u, abort, a.status)) break;
+          if (!pwait(bar(misc->kempty[sk]), kr.phase ^ 1u)) break;
           const uint32_t kb = bar(misc->kfull[sk]);
           if constexpr (kPage != 0) {
             paged_tile_load<kPage == 2>(a, wk.b, wk.h, wk.t, wk.L, k_ring + sk * P.k_stage, kb, P.kplan,
@@ -399,7 +413,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
         const int j = i - P.vlag;
         if (j >= 0) {
           const int sv = vr.slot;
-          if (!mbar_wait(bar(misc->vempty[sv]), vr.phase ^ 1u, abort, a.status)) break;
+          if (!pwait(bar(misc->vempty[sv]), vr.phase ^ 1u)) break;
           const uint32_t vb = bar(misc->vfull[sv]);
           const uint32_t vs = v_ring + sv * P.v_stage;
           if constexpr (kPage != 0) {
@@ -421,9 +435,11 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           while (!mbar_try_wait(bar(full[i % n]), (i / n) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
         }
       };
-      drain(misc->kfull, P.SK, issued_k);
-      drain(misc->vfull, P.SV, issued_v);
-      drain(misc->zfull, P.NZ, issued_z);
+      if (lane == 0) {
+        drain(misc->kfull, P.SK, issued_k);
+        drain(misc->vfull, P.SV, issued_v);
+        drain(misc->zfull, P.NZ, issued_z);
+      }
     }
   } else if (warp == 1) {
     // ======================================================== score-MMA issuer

@@ -247,7 +247,10 @@ __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid
   if (amax > kF16Max) record_status(a.status, LLA_ERR_RANGE);   // (NaN queries stay NaN, as on every path)
 }
 
-template <int RK, int RV, bool kPaged>
+// kPage: 0 dense cache, 1 page pool with pages of a multiple of 128 tokens (a
+// head-tile inside one page: one pair of copies), 2 page pool of any other page size
+// (a head-tile's rows copied page by page, the copies spread over the producer warp)
+template <int RK, int RV, int kPage>
 __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int KB = RK * 2, VB = RV * 2; // bytes of a latent K / V row
   constexpr int LPR = RV / 4;             // value step: lanes per V row, 4 columns each
@@ -347,8 +350,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
     // Per run (the CTA's positions of one sequence): the head-set images, each
     // once the MMAs of the previous run's image in that buffer are done.  Per
     // head-tile: its K and V rows (contiguous in the cache) into the next ring slot
-    // with two plain bulk copies of the rows below the sequence length.
-    if (lane == 0) {
+    // with two plain bulk copies of the rows below the sequence length.  With a
+    // paged cache the whole warp runs the loop (lane 0 waits, the warp follows its
+    // decision) and lane i issues the copies of the tile's i-th page.
+    constexpr bool kWarp = kPage == 2;
+    auto pwait = [&](uint32_t b, uint32_t parity) -> bool {
+      if constexpr (kWarp) return warp_wait(b, parity, abort, a.status);
+      else return mbar_wait(b, parity, abort, a.status);
+    };
+    if (lane == 0 || kWarp) {
       PosWalker w = start;
       SlotPos sp{0, 0u};
       int run = 0, issued = 0, imgs = 0;
@@ -358,37 +368,48 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
         if (run_start) {
           imgs = 0;
           for (int s = 0; s < nsets && ok; ++s) {
-            if (run > 0 && !(ok = mbar_wait(bar(misc->img_empty[s]), (run - 1) & 1, abort, a.status))) break;
+            if (run > 0 && !(ok = pwait(bar(misc->img_empty[s]), (run - 1) & 1))) break;
             if (lp == 0 && s == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // images written
-            const uint32_t fb = bar(misc->img_full[s]);
-            mbar_arrive_expect_tx(fb, P.img);
-            bulk_load(sbase + P.imgs + s * P.img,
-                      a.zimg + (static_cast<int64_t>(w.b) * nsets + s) * a.zimg_stride, P.img, fb);
+            if (!kWarp || lane == 0) {
+              const uint32_t fb = bar(misc->img_full[s]);
+              mbar_arrive_expect_tx(fb, P.img);
+              bulk_load(sbase + P.imgs + s * P.img,
+                        a.zimg + (static_cast<int64_t>(w.b) * nsets + s) * a.zimg_stride, P.img, fb);
+            }
             imgs = s + 1;
           }
           ++run;
         }
         const uint32_t rows = static_cast<uint32_t>(min(kTile, w.L - w.t * kTile));
-        // rows of head h: (z0 + h) * zrows + y0 (dense: z0 = b H)
-        const int64_t z0 = static_cast<int64_t>(w.b) * H, zrows = a.L_max, y0 = static_cast<int64_t>(w.t) * kTile;
+        // rows of head h: (z0 + h) * zrows + y0 (dense: z0 = b H; whole pages: the tile's page)
+        int64_t z0 = static_cast<int64_t>(w.b) * H, zrows = a.L_max, y0 = static_cast<int64_t>(w.t) * kTile;
+        if constexpr (kPage == 1) {
+          const int lp = static_cast<int>(y0 / a.page_size);
+          z0 = static_cast<int64_t>(page_of(a, w.b, lp)) * H;
+          zrows = a.page_size;
+          y0 -= static_cast<int64_t>(lp) * a.page_size;
+        }
         for (int h = 0; h < H && ok; ++h) {
-          if (!(ok = mbar_wait(bar(misc->empty[sp.slot]), sp.phase ^ 1u, abort, a.status))) break;
+          if (!(ok = pwait(bar(misc->empty[sp.slot]), sp.phase ^ 1u))) break;
           const uint32_t fb = bar(misc->full[sp.slot]);
-          mbar_arrive_expect_tx(fb, rows * (KB + VB));
           const uint32_t dst = sbase + P.ring + sp.slot * P.slot;
-          if constexpr (kPaged) {
-            // one pair of copies per page the tile's rows lie in (pages of any size)
-            for (uint32_t j = 0; j < rows;) {
-              const int64_t tok = y0 + j;
-              const int lp = static_cast<int>(tok / a.page_size);
-              const uint32_t off = static_cast<uint32_t>(tok - static_cast<int64_t>(lp) * a.page_size);
-              const uint32_t span = min(static_cast<uint32_t>(a.page_size) - off, rows - j);
-              const int64_t r0 = (static_cast<int64_t>(page_of(a, w.b, lp)) * H + h) * a.page_size + off;
+          if constexpr (kWarp) {
+            // one pair of copies per page the tile's rows lie in (pages of any size, a
+            // page boundary possibly inside the tile): lane i takes page lp0 + i
+            if (lane == 0) mbar_arrive_expect_tx(fb, rows * (KB + VB));
+            __syncwarp();
+            const int64_t pg = a.page_size;
+            const int64_t lp0 = y0 / pg, np = (y0 + rows - 1) / pg - lp0 + 1;
+            for (int64_t i = lane; i < np; i += 32) {
+              const int64_t t0 = max(y0, (lp0 + i) * pg), t1 = min(y0 + rows, (lp0 + i + 1) * pg);
+              const uint32_t j = static_cast<uint32_t>(t0 - y0), span = static_cast<uint32_t>(t1 - t0);
+              const int64_t r0 = (static_cast<int64_t>(page_of(a, w.b, static_cast<int>(lp0 + i))) * H + h) * pg +
+                                 (t0 - (lp0 + i) * pg);
               bulk_load(dst + j * KB, static_cast<const uint8_t*>(a.cache_k) + r0 * KB, span * KB, fb);
               bulk_load(dst + P.k_tile + j * VB, static_cast<const uint8_t*>(a.cache_v) + r0 * VB, span * VB, fb);
-              j += span;
             }
           } else {
+            mbar_arrive_expect_tx(fb, rows * (KB + VB));
             const int64_t r0 = (z0 + h) * zrows + y0;
             bulk_load(dst, static_cast<const uint8_t*>(a.cache_k) + r0 * KB, rows * KB, fb);
             bulk_load(dst + P.k_tile, static_cast<const uint8_t*>(a.cache_v) + r0 * VB, rows * VB, fb);
@@ -399,13 +420,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
         pos_advance(w, a);
       }
       // Let every copy this CTA issued land before the CTA can exit.
-      for (int i = max(0, issued - P.NS); i < issued; ++i) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(bar(misc->full[i % P.NS]), (i / P.NS) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
-      }
-      for (int s = 0; s < imgs; ++s) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(bar(misc->img_full[s]), (run - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      if (lane == 0) {
+        for (int i = max(0, issued - P.NS); i < issued; ++i) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(bar(misc->full[i % P.NS]), (i / P.NS) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+        }
+        for (int s = 0; s < imgs; ++s) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(bar(misc->img_full[s]), (run - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+        }
       }
     }
   } else if (warp == 1) {
@@ -654,14 +677,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
 
 template <int RK, int RV>
 cudaError_t launch_small_instance(const DecodeArgs& a, cudaStream_t s) {
-  // the dense-cache instantiation carries no page lookup in its producer
-  const bool paged = a.block_table != nullptr;
-  auto kern = paged ? decode_small_kernel<RK, RV, true> : decode_small_kernel<RK, RV, false>;
-  static int configured[2] = {0, 0};
-  if (configured[paged] < a.splan.bytes) {
+  // the dense-cache instantiation carries no page lookup in its producer, the
+  // whole-page one no per-page loop
+  const int page = a.block_table == nullptr ? 0 : a.page_size % kTile == 0 ? 1 : 2;
+  auto kern = page == 0 ? decode_small_kernel<RK, RV, 0>
+                        : page == 1 ? decode_small_kernel<RK, RV, 1> : decode_small_kernel<RK, RV, 2>;
+  static int configured[3] = {0, 0, 0};
+  if (configured[page] < a.splan.bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.splan.bytes);
     if (e != cudaSuccess) return e;
-    configured[paged] = a.splan.bytes;
+    configured[page] = a.splan.bytes;
   }
   const int trig_blocks = static_cast<int>((a.trig_rows + kTrigRowsPerBlock - 1) / kTrigRowsPerBlock);
   const int z_blocks = a.H * ((a.B + kZSeqs - 1) / kZSeqs);
