@@ -235,6 +235,24 @@ __global__ void __launch_bounds__(kZThreads) decode2d_z_kernel(const __grid_cons
   }
 }
 
+// Spinning form of mbar_wait_cluster (no suspend hint): for the issuer's waits on
+// barriers whose arrivals come from the epilogue warps of both CTAs.
+__device__ __forceinline__ bool mbar_spin_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint32_t* status) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        record_status(status, LLA_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecode2dThreads, 1)
 decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_constant__ Decode2dMaps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -539,7 +557,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             const uint32_t G = 2 * H * n + 2 * h + s, su = G % kNU;
-            if (!(ok = mbar_wait_cluster(bar(misc->uempty[su]), ((G / kNU) & 1u) ^ 1u, abort, a.status))) break;
+            if (!(ok = mbar_spin_cluster(bar(misc->uempty[su]), ((G / kNU) & 1u) ^ 1u, abort, a.status))) break;
             tc_fence_after();
             const uint64_t a0 = dA0 + ts[s] * kst;
             const uint32_t d = tmem + 128 * su;
@@ -594,6 +612,17 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
     auto epi_sync = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     auto arrive_even = [&](uint32_t b) {
       if (rank == 0) mbar_arrive(b); else mbar_arrive_cluster(b, 0);
+    };
+    // score-buffer release: this thread's TMEM reads completed (tcgen05.wait::ld) and
+    // were fenced before the arrive, so the peer's later MMA into the buffer cannot
+    // overtake them; nothing else needs to be made visible, so no cluster release
+    auto release_u = [&](uint32_t b) {
+      if (rank == 0) {
+        mbar_arrive(b);
+      } else {
+        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(b, 0))
+                     : "memory");
+      }
     };
     // Each thread keeps its token's running sum of the weights of every head (lt);
     // the sums of the 256 tokens are reduced only when a run's record is written.
@@ -681,7 +710,7 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            arrive_even(bar(misc->uempty[uslot]));
+            release_u(bar(misc->uempty[uslot]));
             misc->mx[we][h] = wm;
             // the MMAs of this stage are complete: window h is free after group 1's
             // stage, the block's tile of this group after its last stage
