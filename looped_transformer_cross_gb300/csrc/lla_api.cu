@@ -30,6 +30,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 3-D tiled map over a dense row-major tensor [d2][d1][d0] of `esize`-byte elements.
 // Swizzle = the atom matching the box row bytes (128 / 64 / 32 B).
+// 3-D map with explicit byte strides of dimensions 1 and 2 and an explicit swizzle.
+bool make_map_3d_strided(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1,
+                         uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+                         CUtensorMapSwizzle sw) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t d0,
                  uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
   auto enc = tensor_map_encoder();
@@ -51,7 +65,7 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t partials, rec_ml, bias, scores, zimg, zimg_stride, trig16, total;
+  size_t partials, rec_ml, bias, scores, zimg, zimg_stride, trig16, pw, grp_ml, total;
 };
 
 // Bytes of one unit's query-operand image: Z (128 rows x r_k bf16, K-chunk
@@ -71,7 +85,7 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
   WsLayout w{};
   size_t off = 256;  // status word
   if (d->variant == LLA_2D) {
-    // run records of the pair kernel, encode bias (one "head" of width T*H*d),
+    // run records of the value kernel, encode bias (one "head" of width T*H*d),
     // fp32 scores, per-sequence query-operand images
     const size_t nrec = static_cast<size_t>(2) * (static_cast<size_t>(B) + kMaxPairs);
     w.partials = off; off += al256(nrec * d->H * d->r_v * 4);
@@ -84,9 +98,17 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
       w.zimg_stride = decode2d_zimg_stride(d->H, d->r_k);
       off += al256(static_cast<size_t>(B) * w.zimg_stride);
     }
-    // f16 RoPE rows of the decode epilogue (positions up to L_max rounded to a block)
+    // softmax weights (bf16 [B][H][tiles * 128]) and per-32-token-group (m, l) of the
+    // score kernel
+    const size_t tiles = static_cast<size_t>((L_max + kTile - 1) / kTile);
+    // the transposed RoPE table [128][positions] fp32, positions up to L_max rounded
+    // up to a whole 256-token block
     w.trig16 = off;
-    if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(decode2d_trig_rows(L_max, INT64_MAX)) * 256);
+    if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(128) * decode2d_trig_rows(L_max) * 4);
+    w.pw = off;
+    if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(B) * d->H * tiles * kTile * 2);
+    w.grp_ml = off;
+    if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(B) * d->H * tiles * 4 * 2 * 4);
     w.total = off;
     return w;
   }
@@ -267,7 +289,8 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   // entry point without a workspace), then launch
   auto ready = [&]() { return !clear_status || cudaMemsetAsync(ws, 0, 256, s) == cudaSuccess; };
   if (dims->variant == LLA_2D && dims->dtype == LLA_BF16) {
-    // LLA-2D: one latent per token shared by the H heads (CTA-pair kernel)
+    // LLA-2D: one latent per token shared by the H heads (CTA-pair score kernel,
+    // value kernel)
     Decode2dArgs a{};
     if (!make_decode2d_plan(H, dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
     a.B = cache.B;
@@ -294,18 +317,36 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
     a.zimg = ws + wl.zimg;
     a.zimg_stride = static_cast<int64_t>(wl.zimg_stride);
     a.zchunk_bytes = static_cast<int64_t>(H) * d * 128;
-    a.trig16 = reinterpret_cast<uint32_t*>(ws + wl.trig16);
-    a.trig_rows = decode2d_trig_rows(cache.L_max, rope_len);
+    a.ntiles = (cache.L_max + kTile - 1) / kTile;
+    a.trig_rows = decode2d_trig_rows(cache.L_max);
+    a.trigT = reinterpret_cast<float*>(ws + wl.trig16);
+    a.pw = reinterpret_cast<uint16_t*>(ws + wl.pw);
+    a.grp_ml = reinterpret_cast<float*>(ws + wl.grp_ml);
     const int sms = sm_count();
     if (sms <= 1) return LLA_ERR_CUDA;
     const int64_t max_blocks = static_cast<int64_t>(cache.B) * ((cache.L_max + kBlock2dTokens - 1) / kBlock2dTokens);
     a.pairs = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms / 2, kMaxPairs), std::max<int64_t>(1, max_blocks)));
+    a.units = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid),
+                                                 std::max<int64_t>(1, static_cast<int64_t>(cache.B) * a.ntiles)));
     Decode2dMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     const uint64_t rows = static_cast<uint64_t>(cache.L_max), seqs = static_cast<uint64_t>(cache.B);
     if (!make_map_3d(&maps.k, cache.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_k, rows, seqs, 64, kTile, 1))
       return LLA_ERR_CUDA;
-    if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, seqs, 64, 32, 1))
+    if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, seqs, 64, kTile, 1))
+      return LLA_ERR_CUDA;
+    // query-operand images as stored (pre-swizzled rows of 128 B, then the 32-byte
+    // bias rows), one image per sequence
+    const uint64_t zrows = static_cast<uint64_t>(a.plan.nkc) * H * d;
+    if (!make_map_3d_strided(&maps.z, a.zimg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, zrows, seqs, 128,
+                             static_cast<uint64_t>(a.zimg_stride), 64, kTile, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return LLA_ERR_CUDA;
+    if (!make_map_3d_strided(&maps.zb, a.zimg + zrows * 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 16,
+                             static_cast<uint64_t>(H) * d, seqs, 32, static_cast<uint64_t>(a.zimg_stride), 16,
+                             kTile, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return LLA_ERR_CUDA;
+    if (!make_map_3d(&maps.p, a.pw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.ntiles) * kTile,
+                     static_cast<uint64_t>(H), seqs, 64, static_cast<uint32_t>(H), 1))
       return LLA_ERR_CUDA;
     if (!ready()) return LLA_ERR_CUDA;
     return launch_decode2d_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;

@@ -8,31 +8,31 @@
 // k_{t,h} = c_k W_up,k,t,h^T + mu_k,t,h.  One call (one layer, one loop, all heads
 // and sequences) therefore contracts [tokens x r_k] with [r_k x H*128]: at H = 16,
 // r_k = 128 that is about 0.5 MFLOP per cached token and ~700 flop per latent
-// byte, so the call is bound by the tensor pipe, not by HBM.
+// byte, so the score pass is bound by the tensor pipe, not by HBM.
 //
-// Design (CTA pairs, tcgen05 cta_group::2):
-//  * Work is cut into blocks of 512 tokens of one sequence; each pair of CTAs
-//    (a cluster of two on neighbouring SMs) takes a contiguous range of blocks.
-//    CTA `rank` holds the block's K latent tiles at rows 256*rank + {0, 128}.
-//  * For every head h and tile slot the pair MMA U = C_k Z_h^T runs with
-//    M = 256 tokens (128 from each CTA), N = 128, K = r_k.  Z_h is the query
-//    operand of the per-head kernel (the RoPE-rotated, scaled query folded into
-//    W_up,k,t,h, built by decode2d_z_kernel); its rows are split between the two
-//    CTAs, so each SM receives half of every head's operand.  The latent tiles
-//    stay resident while the H operands stream through, which keeps both the
-//    shared-memory read rate of the MMAs and the per-SM copy rate within bounds.
-//  * Epilogue warps (one token per thread, fixed for the block) form the rotary
-//    score s = sum_f cos(j th_f) (U_f + b_f) + sin(j th_f) (U_64+f + b_64+f) from
-//    the token's cos/sin row held in registers (b = the mu_k term), and keep the
-//    block's scores in TMEM.  At the end of a block an exact per-head
-//    maximum over the CTA's 256 tokens sets the softmax reference (raised lazily,
-//    by more than 2^8), P (bf16, heads x tokens) is written, and the value MMA
-//    D_v += C_v^T P (M = r_v rows, N = heads; Appendix J) accumulates in TMEM over
-//    the blocks of a sequence.  The value MMAs of block n run interleaved with
-//    the score MMAs of block n + 1.
-//  * When a CTA's run of a sequence ends it writes one record (m, l, acc_v) per
-//    head; decode2d_combine_kernel merges the records of a sequence (log-sum-exp
-//    merge) and applies the V up-projection once.
+// Four launches:
+//  1. decode2d_z_kernel: the query operand Z of every (sequence, head) (the
+//     RoPE-rotated, scaled query folded into W_up,k,t,h) and an f16 RoPE table.
+//  2. decode2d_score_kernel (CTA pairs, tcgen05 cta_group::2): blocks of 256 tokens
+//     of one sequence; CTA `rank` holds the block's K latent tile at rows
+//     256 kb + 128 rank.  Each stage is one pair MMA U = C_k [Z_2p; Z_2p+1]^T over
+//     a pair of heads (M = 256 tokens, N = 256, K = r_k), the even CTA supplying
+//     head 2p's 128 operand rows and the odd CTA head 2p+1's.  A pair MMA issues
+//     at most about one per 70 cycles, so N = 256 (128 cycles of tensor work per
+//     MMA) keeps the pipe fed where N = 128 could not.  Both CTAs' copies of an
+//     operand complete on one barrier of the even CTA (cta_group::2 copies).  The
+//     two 256-column score buffers fill TMEM.  Epilogue warps (one token per
+//     thread, warp group g takes head 2p + g) form the rotary score
+//     s = sum_f cos(j th_f) U_f + sin(j th_f) U_64+f from the token's cos/sin row
+//     held in registers and write, per 32-token group (one warp), the weights
+//     p = 2^(s - m) (bf16) with m = ceil(max s), an integer, and (m, sum p).
+//  3. decode2d_value_kernel (one CTA per SM): D_v = sum_j p_j c_v,j for every head
+//     over contiguous runs of 128-token tiles, on the tensor cores (M = 128 r_v
+//     rows, N = 16 heads, K = tokens; Appendix J), the weights of each group first
+//     scaled by 2^(m_group - M_run) (exact: both are integers), one record
+//     (M_run, l_run, D_v) per run.
+//  4. decode2d_combine_kernel: merges the records of a sequence (log-sum-exp
+//     merge) and applies the V up-projection once.
 //
 #include "lla_kernels.h"
 
@@ -46,39 +46,27 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
-constexpr float kRescaleLog2 = 8.f;                 // lazy reference threshold (log2 units)
-constexpr int kNK = 3;        // latent tile slots (two per block)
-constexpr int kNZ = 4;        // query-operand windows in flight (a group of four heads)
-constexpr int kNV = 2;        // value chunk slots
-constexpr int kNU = 3;        // TMEM score buffers (128 columns each)
-constexpr int kVChunks = 8;   // 32-token value chunks of a CTA's 256 block tokens
-constexpr int kVTok = 32;     // tokens per value chunk (two 16-token K steps)
-constexpr uint32_t kScoreCol = 448;   // TMEM columns of the block's scores: 16 per warp group
-constexpr uint32_t kDvCol = 384;   // TMEM column of the value accumulators (2 x 32)
+constexpr int kSNK = 3;        // latent tile slots of the score kernel (one tile per block)
+constexpr int kSNZ = 3;        // query-operand windows in flight (one head per CTA each)
 constexpr int kZRowBytes = 128;    // one 64-wide bf16 chunk row
+constexpr int kVTile = 128;        // tokens of a value tile (= score tile)
+constexpr int kVS = 3;             // value ring stages
 
-struct alignas(16) Misc2d {
-  // full barriers: in the even CTA they also take the odd CTA's relay arrive (count
-  // 2), so one wait covers both halves of a pair operand
-  uint64_t kfull[kNK], kempty[kNK];
-  uint64_t zfull[kNZ], zempty[kNZ];
-  uint64_t vfull[kNV], vempty[kNV];
-  // Score buffers: ufull per epilogue warp group (the group of a stage is its tile
-  // slot), so that a group, which skips the other group's stages, never waits on a
-  // barrier phase more than one completion ahead; uempty has one waiter (the issuer).
-  uint64_t ufull[2][kNU], uempty[kNU];
-  uint64_t pfull, vdone, mma_done[2];
+struct alignas(16) MiscScore {
+  // full barriers (used in the even CTA): the copies of both CTAs complete on them
+  uint64_t kfull[kSNK], kempty[kSNK];
+  uint64_t zfull[kSNZ], zempty[kSNZ];
+  // score buffers: ufull takes the MMA commit; uempty (used in the even CTA) the
+  // 8 epilogue warps of both CTAs
+  uint64_t ufull[2], uempty[2];
+  uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
   int start_b, start_kb, count, total_blocks;
-  float mx[8][kMax2dHeads];   // per epilogue warp: block maximum of each head
-  float lp[8][kMax2dHeads];   // per epilogue warp: a run's sum of the weights of each head
-  float m_ref[kMax2dHeads];   // softmax reference of each head (log2 units)
-  float m_new[kMax2dHeads], alpha[kMax2dHeads];   // the block's new reference, rescale factor
-  float m_rec[kMax2dHeads];   // reference of a finished run (for its record)
-  int scan[kDecode2dThreads];
+  float xch[2][2][kTile];   // [stage parity][head of the pair][token]: the other group's half score
+  int scan[kScore2dThreads];
 };
-static_assert(sizeof(Misc2d) <= 4096, "misc region");
+static_assert(sizeof(MiscScore) <= 4096, "misc region");
 
 struct RingPos {
   int slot = 0;
@@ -88,7 +76,7 @@ struct RingPos {
   }
 };
 
-// Block of one sequence: tokens [512 kb, 512 kb + 512).
+// Block of one sequence: tokens [256 kb, 256 kb + 256).
 struct Walker2d {
   int b, kb, nb, L;
 };
@@ -98,6 +86,7 @@ __device__ __forceinline__ int clamp_len(int L, int64_t L_max) {
 }
 
 __device__ __forceinline__ int nblocks(int L) { return (L + kBlock2dTokens - 1) / kBlock2dTokens; }
+__device__ __forceinline__ int ntiles_of(int L) { return (L + kVTile - 1) / kVTile; }
 
 __device__ __forceinline__ void walk_advance(Walker2d& w, const Decode2dArgs& a) {
   if (++w.kb < w.nb) return;
@@ -109,12 +98,6 @@ __device__ __forceinline__ void walk_advance(Walker2d& w, const Decode2dArgs& a)
     if (w.nb > 0) return;
   }
 }
-
-// Score stages of a block: head by head, tile slot 0 then tile slot 1 (stage
-// st = 2h + s), so the two epilogue warp groups (one per tile slot) take turns.
-// Value chunk c of the previous block follows head vchunk_head(c) in every role's
-// order (the first one two heads in, once that block's weights exist).
-__device__ __forceinline__ int vchunk_head(int c, int H) { return min(2 * c + 2, H - 1); }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<uint32_t*>(&v);
@@ -133,9 +116,11 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
 // rows][16 bf16] (32-byte swizzle): column 0 = bias rounded to bf16, column 1 =
 // the rounding remainder, so a 16-wide MMA against ones in columns 0 and 1 adds
 // the bias in ~16-bit precision.  Blocks = (sequence, head); the blocks after
-// them write the f16 copy of the RoPE table the epilogue reads (64 rows each).
+// them write the RoPE table transposed, trigT[c][j] = cos(j th_c) (c < 64) or
+// sin(j th_c-64), so that the epilogue's loads of 32 consecutive tokens coalesce
+// (32 tokens per block).
 constexpr int kZThreads = 256;
-constexpr int kTrigRowsPerBlock = 64;
+constexpr int kTrigTokensPerBlock = 32;
 __global__ void __launch_bounds__(kZThreads) decode2d_z_kernel(const __grid_constant__ Decode2dArgs a) {
   // the decode grid may start its set-up now; it waits for this grid before it
   // copies an image
@@ -143,15 +128,18 @@ __global__ void __launch_bounds__(kZThreads) decode2d_z_kernel(const __grid_cons
   __shared__ float qs[2][64];
   const int u = blockIdx.x, tid = threadIdx.x;
   if (u >= a.B * a.H) {
-    // RoPE rows as f16 pairs: row p = {cos(p th_2i), cos(p th_2i+1)} i < 32, then sin
-    const int64_t r0 = static_cast<int64_t>(u - a.B * a.H) * kTrigRowsPerBlock;
-    for (int i = tid; i < kTrigRowsPerBlock * 64; i += kZThreads) {
-      const int64_t r = r0 + i / 64;
-      const int c = i % 64;            // pair index: 0..31 cos, 32..63 sin
-      if (r >= a.trig_rows) break;
-      const float* src = (c < 32 ? a.rope_cos : a.rope_sin) + r * 64 + 2 * (c & 31);
-      const __half2 v = __floats2half2_rn(src[0], src[1]);
-      a.trig16[r * 64 + c] = *reinterpret_cast<const uint32_t*>(&v);
+    __shared__ float tr[128][kTrigTokensPerBlock + 1];
+    const int64_t j0 = static_cast<int64_t>(u - a.B * a.H) * kTrigTokensPerBlock;
+    for (int i = tid; i < kTrigTokensPerBlock * 128; i += kZThreads) {
+      const int jj = i / 128, c = i % 128;
+      int64_t j = j0 + jj;
+      if (j >= a.rope_len) j = a.rope_len - 1;   // rows past the table: masked tokens
+      tr[c][jj] = __ldg((c < 64 ? a.rope_cos : a.rope_sin) + j * 64 + (c & 63));
+    }
+    __syncthreads();
+    for (int i = tid; i < kTrigTokensPerBlock * 128; i += kZThreads) {
+      const int c = i / kTrigTokensPerBlock, jj = i % kTrigTokensPerBlock;
+      a.trigT[c * a.trig_rows + j0 + jj] = tr[c][jj];
     }
     return;
   }
@@ -235,13 +223,69 @@ __global__ void __launch_bounds__(kZThreads) decode2d_z_kernel(const __grid_cons
   }
 }
 
-// Spinning form of mbar_wait_cluster (no suspend hint): for the issuer's waits on
-// barriers whose arrivals come from the epilogue warps of both CTAs.
-__device__ __forceinline__ bool mbar_spin_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                  uint32_t* status) {
+
+// d = a * b + d on a pair of f32 lanes (one packed instruction)
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "mov.b64 pd, {%0, %1};\n\tfma.rn.f32x2 pd, pa, pb, pd;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Contiguous share `part` of `parts` of the work units (blocks or tiles) of all
+// sequences, in sequence order: its first (sequence, unit) and its length.  Every
+// thread of the CTA calls it (it synchronises); scan holds kThreads ints.
+template <int kThreads, typename CountOf>
+__device__ void share_of(const Decode2dArgs& a, CountOf count_of, long long part, long long parts, int* scan,
+                         int* start_b, int* start_k, int* count, int* total) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per_thr = (a.B + kThreads - 1) / kThreads;
+  const int b0 = min(a.B, tid * per_thr), b1 = min(a.B, b0 + per_thr);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += count_of(b);
+  scan[tid] = local;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int kPer = kThreads / 32;
+    int v[kPer];
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) { v[i] = scan[lane * kPer + i]; s += v[i]; }
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int excl = incl - s;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) { scan[lane * kPer + i] = excl; excl += v[i]; }
+    if (lane == 31) *total = incl;
+  }
+  __syncthreads();
+  const long long NB = *total;
+  const long long lo = part * NB / parts, hi = (part + 1) * NB / parts;
+  long long P0 = scan[tid];
+  for (int b = b0; b < b1; ++b) {
+    const int nb = count_of(b);
+    if (nb > 0 && lo < hi && P0 <= lo && lo < P0 + nb) {
+      *start_b = b;
+      *start_k = static_cast<int>(lo - P0);
+    }
+    P0 += nb;
+  }
+  if (tid == 0) *count = static_cast<int>(hi - lo);
+  __syncthreads();
+}
+
+// Spinning form of the bounded wait (no suspend hint): for the issuer, whose every
+// wait is on the critical path of the tensor pipe.  Its barriers are its own CTA's:
+// the copies of both CTAs complete on them, and the score-buffer releases carry no
+// data (the TMEM reads they announce were waited for and fenced).
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 255u) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -253,63 +297,30 @@ __device__ __forceinline__ bool mbar_spin_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecode2dThreads, 1)
-decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_constant__ Decode2dMaps maps) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScore2dThreads, 1)
+decode2d_score_kernel(const __grid_constant__ Decode2dArgs a, const __grid_constant__ Decode2dMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Decode2dPlan& P = a.plan;
   const uint32_t sbase = smem_u32(sm);
-  Misc2d* misc = reinterpret_cast<Misc2d*>(sm + P.misc);
+  MiscScore* misc = reinterpret_cast<MiscScore*>(sm + P.misc);
   volatile int* abort = &misc->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_cta_rank();
   const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int HP = a.H / 2;   // stages (head pairs) of a block
 
   // ---------------------------------------------------------- work range (same in both CTAs)
-  {
-    const int per_thr = (a.B + kDecode2dThreads - 1) / kDecode2dThreads;
-    const int b0 = min(a.B, tid * per_thr), b1 = min(a.B, b0 + per_thr);
-    int local = 0;
-    for (int b = b0; b < b1; ++b) {
+  if (tid == 0) misc->abort = 0;
+  if (blockIdx.x == 0 && tid < a.B) {
+    for (int b = tid; b < a.B; b += kScore2dThreads) {
       const int L0 = __ldg(a.seq_lens + b);
-      if ((L0 < 0 || L0 > a.L_max) && blockIdx.x == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
-      local += nblocks(clamp_len(L0, a.L_max));
+      if (L0 < 0 || L0 > a.L_max) record_status(a.status, LLA_ERR_DEVICE_ARG);
     }
-    misc->scan[tid] = local;
-    if (tid == 0) misc->abort = 0;
-    __syncthreads();
-    if (warp == 0) {
-      constexpr int kPer = kDecode2dThreads / 32;
-      int v[kPer];
-      int s = 0;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) { v[i] = misc->scan[lane * kPer + i]; s += v[i]; }
-      int incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      int excl = incl - s;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) { misc->scan[lane * kPer + i] = excl; excl += v[i]; }
-      if (lane == 31) misc->total_blocks = incl;
-    }
-    __syncthreads();
-    const long long NB = misc->total_blocks;
-    const long long lo = pair * NB / a.pairs, hi = (pair + 1) * NB / a.pairs;
-    long long P0 = misc->scan[tid];
-    for (int b = b0; b < b1; ++b) {
-      const int nb = nblocks(clamp_len(__ldg(a.seq_lens + b), a.L_max));
-      if (nb > 0 && lo < hi && P0 <= lo && lo < P0 + nb) {
-        misc->start_b = b;
-        misc->start_kb = static_cast<int>(lo - P0);
-      }
-      P0 += nb;
-    }
-    if (tid == 0) misc->count = static_cast<int>(hi - lo);
-    __syncthreads();
   }
+  share_of<kScore2dThreads>(
+      a, [&](int b) { return nblocks(clamp_len(__ldg(a.seq_lens + b), a.L_max)); }, pair, a.pairs, misc->scan,
+      &misc->start_b, &misc->start_kb, &misc->count, &misc->total_blocks);
   const int count = misc->count;
   if (count == 0) return;   // both CTAs of the pair leave here together
 
@@ -322,37 +333,26 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
   // ---------------------------------------------------------- set-up
   auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
   if (tid == 0) {
-    const uint32_t nfull = rank == 0 ? 2 : 1;   // + the odd CTA's relay in the even CTA
-    for (int s = 0; s < kNK; ++s) {
-      mbar_init(bar(misc->kfull[s]), nfull);
-      mbar_init(bar(misc->kempty[s]), 4);       // the tile's warp group, after its last stage
+    for (int s = 0; s < kSNK; ++s) {
+      mbar_init(bar(misc->kfull[s]), 1);        // the even producer's expect_tx (both CTAs' bytes)
+      mbar_init(bar(misc->kempty[s]), 1);       // MMA commit after the block's last stage
     }
-    for (int s = 0; s < kNZ; ++s) {
-      mbar_init(bar(misc->zfull[s]), nfull);
-      mbar_init(bar(misc->zempty[s]), 4);       // warp group 1, after the window's last stage
+    for (int s = 0; s < kSNZ; ++s) {
+      mbar_init(bar(misc->zfull[s]), 1);
+      mbar_init(bar(misc->zempty[s]), 1);       // MMA commit of the window's stage
     }
-    for (int s = 0; s < kNV; ++s) {
-      mbar_init(bar(misc->vfull[s]), nfull);
-      mbar_init(bar(misc->vempty[s]), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(misc->ufull[s]), 1);
+      mbar_init(bar(misc->uempty[s]), 16);      // 8 epilogue warps of each CTA
     }
-    for (int s = 0; s < kNU; ++s) {
-      mbar_init(bar(misc->ufull[0][s]), 1);
-      mbar_init(bar(misc->ufull[1][s]), 1);
-      mbar_init(bar(misc->uempty[s]), 8);        // 4 epilogue warps of each CTA
-    }
-    mbar_init(bar(misc->pfull), 16);             // 8 epilogue warps of each CTA
-    mbar_init(bar(misc->vdone), 1);
-    mbar_init(bar(misc->mma_done[0]), 1);
-    mbar_init(bar(misc->mma_done[1]), 1);
+    mbar_init(bar(misc->mma_done), 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.k);
-    prefetch_tmap(&maps.v);
+    prefetch_tmap(&maps.z);
+    prefetch_tmap(&maps.zb);
   }
-  // P rows of heads >= H stay zero
-  for (int i = tid; i < 16 * 512 / 16; i += kDecode2dThreads)
-    reinterpret_cast<uint4*>(sm + P.p)[i] = make_uint4(0, 0, 0, 0);
   // bias operand A: columns 0 and 1 of every token row are 1 (they meet bias hi / lo)
   if (tid < kTile) {
     const uint32_t ones = bf16x2_bits(__floats2bfloat162_rn(1.f, 1.f));
@@ -369,59 +369,37 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the combine grid may be scheduled now; it waits for this grid to complete
+  // the value grid may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tmem = misc->tmem_base;
 
-  // Zero value-chunk rows past the sequence end (they may hold anything; their
-  // weights are 0, and 0 * x must stay 0 in the value MMA).
-  auto zero_v_tail = [&](int sv, int valid) {
-    if (valid >= kVTok) return;
-    const int r0 = valid < 0 ? 0 : valid;
-    uint8_t* vs = sm + P.v_ring + sv * P.v_stage;
-    for (int bx = 0; bx < 2 * P.nvh; ++bx)
-      for (int r = r0; r < kVTok; ++r)
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<uint4*>(vs + bx * 4096 + r * kZRowBytes + g * 16) = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-  };
-
   if (warp == 0) {
     // ======================================================== TMA producer (each CTA)
-    // Per block: both latent tiles, then per head its query window, with the value
-    // chunks of the previous block after head vchunk_head(c) -- the issuers' order.
+    // Per block: the latent tile, then per head pair this CTA's head of the pair
+    // (2p + rank): its 128 query-operand rows and their bias rows.  The copies of
+    // both CTAs complete on the even CTA's full barrier, which the even producer
+    // arms with the bytes of both.
     if (lane == 0) {
-      Walker2d w = start, wp = start;
-      RingPos kr, zr, vr;
-      int issued_k = 0, issued_z = 0, issued_v = 0;
+      Walker2d w = start;
+      RingPos kr, zr;
+      int issued_k = 0, issued_z = 0;
       bool ok = true, images_ready = false;
-      auto load_v = [&](const Walker2d& wb, int c) -> bool {
-        const int sv = vr.slot;
-        if (!mbar_wait(bar(misc->vempty[sv]), vr.phase ^ 1u, abort, a.status)) return false;
-        const uint32_t fb = bar(misc->vfull[sv]);
-        mbar_arrive_expect_tx(fb, P.nvh * 8192);
-        const int y = wb.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + kVTok * c;
-        const uint32_t dst = sbase + P.v_ring + sv * P.v_stage;
-        for (int bx = 0; bx < 2 * P.nvh; ++bx) tma_load_3d(dst + bx * 4096, &maps.v, fb, 64 * bx, y, wb.b);
-        ++issued_v;
-        vr.next(kNV);
-        return true;
-      };
+      // latents stream through once; a sequence's query operand is read by every block
+      const uint64_t pol_stream = l2_policy_evict_first(), pol_keep = l2_policy_evict_last();
       for (int n = 0; n < count && ok; ++n) {
-        for (int s = 0; s < 2 && ok; ++s) {   // the block's two latent tiles
+        {
           const int sk = kr.slot;
           if (!(ok = mbar_wait(bar(misc->kempty[sk]), kr.phase ^ 1u, abort, a.status))) break;
           const uint32_t fb = bar(misc->kfull[sk]);
-          mbar_arrive_expect_tx(fb, P.nkc * 16384);
-          const int y = w.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + kTile * s;
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * P.nkc * 16384);
+          const uint32_t fbe = map_to_rank(fb, 0);
+          const int y = w.kb * kBlock2dTokens + static_cast<int>(rank) * kTile;
           for (int c = 0; c < P.nkc; ++c)
-            tma_load_3d(sbase + P.k_ring + sk * P.k_stage + c * 16384, &maps.k, fb, 64 * c, y, w.b);
+            tma_load_3d_pair(sbase + P.k_ring + sk * P.k_stage + c * 16384, &maps.k, fbe, 64 * c, y, w.b, pol_stream);
           ++issued_k;
-          kr.next(kNK);
+          kr.next(kSNK);
         }
-        int vc = 0;
-        for (int h = 0; h < a.H && ok; ++h) {
+        for (int p = 0; p < HP && ok; ++p) {
           const int sz = zr.slot;
           if (!(ok = mbar_wait(bar(misc->zempty[sz]), zr.phase ^ 1u, abort, a.status))) break;
           if (!images_ready) {
@@ -429,192 +407,107 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
             images_ready = true;
           }
           const uint32_t fb = bar(misc->zfull[sz]);
-          mbar_arrive_expect_tx(fb, P.nkc * 8192 + 2048);
-          const uint8_t* img = a.zimg + static_cast<int64_t>(w.b) * a.zimg_stride;
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (P.nkc * 16384 + 4096));
+          const uint32_t fbe = map_to_rank(fb, 0);
           const uint32_t dst = sbase + P.z_ring + sz * P.z_stage;
-          const int64_t row0 = static_cast<int64_t>(h) * kHeadDim + 64 * rank;
+          const int row0 = (2 * p + static_cast<int>(rank)) * kHeadDim;
           for (int c = 0; c < P.nkc; ++c)
-            bulk_load(dst + c * 8192, img + c * a.zchunk_bytes + row0 * kZRowBytes, 8192, fb);
-          bulk_load(dst + P.nkc * 8192, img + P.nkc * a.zchunk_bytes + row0 * 32, 2048, fb);
+            tma_load_3d_pair(dst + c * 16384, &maps.z, fbe, 0, c * a.H * kHeadDim + row0, w.b, pol_keep);
+          tma_load_3d_pair(dst + P.nkc * 16384, &maps.zb, fbe, 0, row0, w.b, pol_keep);
           ++issued_z;
-          zr.next(kNZ);
-          if (n > 0)
-            while (ok && vc < kVChunks && vchunk_head(vc, a.H) == h) ok = load_v(wp, vc++);
+          zr.next(kSNZ);
         }
-        wp = w;
         walk_advance(w, a);
       }
-      for (int c = 0; ok && c < kVChunks; ++c) ok = load_v(wp, c);   // the last block's values
-      // every copy this CTA issued lands before the CTA can exit
-      auto drain = [&](uint64_t* full, int n, int issued) {
-        for (int i = max(0, issued - n); i < issued; ++i) {
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(bar(full[i % n]), (i / n) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
-        }
-      };
-      drain(misc->kfull, kNK, issued_k);
-      drain(misc->zfull, kNZ, issued_z);
-      drain(misc->vfull, kNV, issued_v);
-    }
-  } else if (warp == 1 && rank == 1) {
-    // ======================================================== relay (odd CTA)
-    // Forwards each completed load of this CTA to the even CTA's full barrier, in
-    // the producer's order.
-    if (lane == 0) {
-      Walker2d w = start, wp = start;
-      RingPos kr, zr, vr;
-      bool ok = true;
-      auto relay_v = [&](const Walker2d& wb, int c) -> bool {
-        const int sv = vr.slot;
-        if (!mbar_wait(bar(misc->vfull[sv]), vr.phase, abort, a.status)) return false;
-        zero_v_tail(sv, wb.L - (wb.kb * kBlock2dTokens + 256 + kVTok * c));
-        mbar_arrive_cluster(bar(misc->vfull[sv]), 0);
-        vr.next(kNV);
-        return true;
-      };
-      for (int n = 0; n < count && ok; ++n) {
-        for (int s = 0; s < 2 && ok; ++s) {
-          if (!(ok = mbar_wait(bar(misc->kfull[kr.slot]), kr.phase, abort, a.status))) break;
-          mbar_arrive_cluster(bar(misc->kfull[kr.slot]), 0);
-          kr.next(kNK);
-        }
-        int vc = 0;
-        for (int h = 0; h < a.H && ok; ++h) {
-          if (!(ok = mbar_wait(bar(misc->zfull[zr.slot]), zr.phase, abort, a.status))) break;
-          mbar_arrive_cluster(bar(misc->zfull[zr.slot]), 0);
-          zr.next(kNZ);
-          if (n > 0)
-            while (ok && vc < kVChunks && vchunk_head(vc, a.H) == h) ok = relay_v(wp, vc++);
-        }
-        wp = w;
-        walk_advance(w, a);
+      // every copy of the pair lands before the CTAs can exit (the odd CTA's copies
+      // count on the even CTA's barriers; the final cluster barrier holds it)
+      if (rank == 0) {
+        auto drain = [&](uint64_t* full, int n, int issued) {
+          for (int i = max(0, issued - n); i < issued; ++i) {
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar(full[i % n]), (i / n) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+          }
+        };
+        drain(misc->kfull, kSNK, issued_k);
+        drain(misc->zfull, kSNZ, issued_z);
       }
-      for (int c = 0; ok && c < kVChunks; ++c) ok = relay_v(wp, c);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && rank == 0) {
     // ======================================================== pair MMA issuer (even CTA)
-    // One thread issues every MMA of the pair.  Ring positions follow from global
-    // counters (block n, head h): tiles 2n, 2n + 1, window nH + h, stage 2Hn + 2h + s.
-    // The loop is kept lean (the issuing thread shares its sub-partition with two
-    // epilogue warps): base descriptors per ring, K steps unrolled with constant offsets.
-    if (lane == 0) {
-      const uint32_t idesc_u = umma_idesc_bf16(256, 128, false, false);
-      const uint32_t idesc_v = umma_idesc_bf16(256, 32, true, false);
-      const int ksteps = a.r_k / 16;
-      const uint64_t dA0 = umma_desc(sbase + P.k_ring, 16, 1024, kSw128);
-      const uint64_t dZ0 = umma_desc(sbase + P.z_ring, 16, 1024, kSw128);
-      const uint64_t dZb0 = umma_desc(sbase + P.z_ring + P.nkc * 8192, 16, 256, kSw32);
-      const uint64_t daug = umma_desc(sbase + P.aug_a, 16, 256, kSw32);
-      // MN-major value operand: 64-row r_v boxes 4 KB apart (LBO), 8 token rows 1 KB apart (SBO)
-      const uint64_t dV0 = umma_desc(sbase + P.v_ring, 4096, 1024, kSw128);
-      const uint64_t dP0 = umma_desc(sbase + P.p, 16, 256, kSw32);
-      const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4, zst = static_cast<uint32_t>(P.z_stage) >> 4,
-                     vst = static_cast<uint32_t>(P.v_stage) >> 4;
-      const uint32_t H = static_cast<uint32_t>(a.H);
-      Walker2d w = start, wp = start;
-      RingPos vr;
-      bool ok = true, prev_run_start = true;
-      // Value MMAs of chunk c of block `pblk` (walker wb): D_v[half] += C_v^T P over
-      // the chunk's 16 tokens of each CTA; chunks wholly past the sequence end
-      // (in both CTAs: the odd CTA's tokens come later) are skipped.
-      auto issue_v = [&](const Walker2d& wb, bool run_start, int c, int pblk) -> bool {
-        if (c == 0 && !mbar_wait_cluster(bar(misc->pfull), pblk & 1, abort, a.status)) return false;
-        const int sv = vr.slot;
-        if (!mbar_wait_cluster(bar(misc->vfull[sv]), vr.phase, abort, a.status)) return false;
-        const int valid = wb.L - (wb.kb * kBlock2dTokens + kVTok * c);
-        if (valid > 0) {
-          zero_v_tail(sv, valid);
-          tc_fence_after();
-          const uint64_t av = dV0 + sv * vst, bp = dP0 + 2 * c * (512 >> 4);
+    // The whole warp runs the loop (warp-uniform descriptors) and one elected lane
+    // issues.  Stage G (block n, head pair p) uses score buffer G & 1, latent slot
+    // n mod 3 and query window G mod 3; it releases the window and, after the
+    // block's last stage, the latent slot by MMA commit.
+    const uint32_t idesc = umma_idesc_bf16(256, 256, false, false);
+    const int ksteps = a.r_k / 16;
+    const uint64_t dA0 = umma_desc(sbase + P.k_ring, 16, 1024, kSw128);
+    const uint64_t dZ0 = umma_desc(sbase + P.z_ring, 16, 1024, kSw128);
+    const uint64_t dZb0 = umma_desc(sbase + P.z_ring + P.nkc * 16384, 16, 256, kSw32);
+    const uint64_t daug = umma_desc(sbase + P.aug_a, 16, 256, kSw32);
+    const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4, zst = static_cast<uint32_t>(P.z_stage) >> 4;
+    // every lane polls each barrier; the vote keeps the warp's decision uniform (a
+    // wait that gave up in any lane ends the loop in all of them)
+    auto agree = [](bool r) { return __all_sync(0xffffffffu, r); };
+    bool ok = true;
+    uint32_t G = 0;
+    for (uint32_t n = 0; n < static_cast<uint32_t>(count) && ok; ++n) {
+      const uint32_t ts = n % kSNK;
+      if (!(ok = agree(mbar_spin(bar(misc->kfull[ts]), (n / kSNK) & 1u, abort, a.status)))) break;
+      const uint64_t a0 = dA0 + ts * kst;
+      for (int p = 0; p < HP && ok; ++p, ++G) {
+        const uint32_t zs = G % kSNZ, buf = G & 1u;
+        if (!(ok = agree(mbar_spin(bar(misc->zfull[zs]), (G / kSNZ) & 1u, abort, a.status)))) break;
+        if (!(ok = agree(mbar_spin(bar(misc->uempty[buf]), ((G >> 1) & 1u) ^ 1u, abort, a.status)))) break;
+        tc_fence_after();
+        const uint64_t b0 = dZ0 + zs * zst, bb = dZb0 + zs * zst;
+        const uint32_t d = tmem + 256 * buf;
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {   // 16-token K steps: +2 KB in the chunk, +512 B in P
-            if (16 * k >= valid) break;   // (wholly past the end in both CTAs)
-            const uint32_t acc = (c > 0 || k > 0 || !run_start) ? 1u : 0u;
-            umma_bf16_pair(tmem + kDvCol, av + k * (2048 >> 4), bp + k * (512 >> 4), idesc_v, acc);
-            if (P.nvh > 1)
-              umma_bf16_pair(tmem + kDvCol + 32, av + (8192 >> 4) + k * (2048 >> 4), bp + k * (512 >> 4), idesc_v,
-                             acc);
-          }
+        for (int k = 0; k < 8; ++k) {
+          // 64-wide K chunks 16 KB apart in both operands; 32 B per K step
+          if (k < ksteps)
+            umma_bf16_pair_warp(d, a0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2, b0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
+                                idesc, k > 0 ? 1u : 0u);
         }
-        umma_commit_pair(bar(misc->vempty[sv]));
-        if (c == kVChunks - 1) umma_commit_pair(bar(misc->vdone));
-        vr.next(kNV);
-        return true;
-      };
-      for (uint32_t n = 0; n < static_cast<uint32_t>(count) && ok; ++n) {
-        const bool run_start = n == 0 || w.kb == 0;
-        uint32_t ts[2];
-        for (int s = 0; s < 2 && ok; ++s) {
-          const uint32_t tile = 2 * n + s;
-          ts[s] = tile % kNK;
-          ok = mbar_wait_cluster(bar(misc->kfull[ts[s]]), (tile / kNK) & 1u, abort, a.status);
-        }
-        int vc = 0;
-        for (uint32_t h = 0; h < H && ok; ++h) {
-          const uint32_t zi = n * H + h, zs = zi & (kNZ - 1);
-          if (!(ok = mbar_wait_cluster(bar(misc->zfull[zs]), (zi / kNZ) & 1u, abort, a.status))) break;
-          const uint64_t b0 = dZ0 + zs * zst, bb = dZb0 + zs * zst;
-#pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            const uint32_t G = 2 * H * n + 2 * h + s, su = G % kNU;
-            if (!(ok = mbar_spin_cluster(bar(misc->uempty[su]), ((G / kNU) & 1u) ^ 1u, abort, a.status))) break;
-            tc_fence_after();
-            const uint64_t a0 = dA0 + ts[s] * kst;
-            const uint32_t d = tmem + 128 * su;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              // 64-wide K chunks: A chunks 16 KB apart, Z chunks 8 KB apart; 32 B per K step
-              if (k < ksteps)
-                umma_bf16_pair(d, a0 + (k >> 2) * (16384 >> 4) + (k & 3) * 2,
-                               b0 + (k >> 2) * (8192 >> 4) + (k & 3) * 2, idesc_u, k > 0 ? 1u : 0u);
-            }
-            umma_bf16_pair(d, daug, bb, idesc_u, 1u);   // + bias
-            umma_commit_pair(bar(misc->ufull[s][su]));
-          }
-          if (!ok) break;
-          if (n > 0)
-            while (ok && vc < kVChunks && vchunk_head(vc, a.H) == static_cast<int>(h))
-              ok = issue_v(wp, prev_run_start, vc++, n - 1);
-        }
-        prev_run_start = run_start;
-        wp = w;
-        walk_advance(w, a);
+        umma_bf16_pair_warp(d, daug, bb, idesc, 1u);   // + bias
+        umma_commit_pair_warp(bar(misc->ufull[buf]));
+        umma_commit_pair_warp(bar(misc->zempty[zs]));
+        if (p == HP - 1) umma_commit_pair_warp(bar(misc->kempty[ts]));
       }
-      for (int c = 0; ok && c < kVChunks; ++c) ok = issue_v(wp, prev_run_start, c, count - 1);
-      // this thread's MMAs complete before TMEM is released
-      umma_commit_pair(bar(misc->mma_done[0]));
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(bar(misc->mma_done[0]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
+    // this warp's MMAs complete before TMEM is released
+    umma_commit_pair_warp(bar(misc->mma_done));
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
   } else if (warp >= 2 && warp < 10) {
     // ======================================================== epilogue (warps 2-9)
-    // Warps 2-5 serve tile slot 0, warps 6-9 tile slot 1; one token per thread.
-    const int we = warp - 2, wg = we >> 2, q = warp & 3;
-    const int row = 32 * q + lane, tid_e = wg * kTile + row;
+    // One token per thread (TMEM lane); warp group g holds the frequencies
+    // f in [32 g, 32 g + 32) of the rotary score of both heads of a stage:
+    //   s_h = sum_f cos(j th_f) U_h,f + sin(j th_f) U_h,64+f,
+    // adds the other group's half through shared memory and takes head 2p + g's
+    // softmax weights.
+    const int we = warp - 2, g = we >> 2, q = warp & 3;
+    const int row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    uint8_t* pbuf = sm + P.p;
     const int H = a.H;
+    const int64_t prow = a.ntiles * kVTile;   // weights per (sequence, head)
+    const int64_t ngroups = a.ntiles * 4;     // 32-token groups per (sequence, head)
 
-    // cos/sin(j th_f) of this thread's token j as f16 pairs: cs2[i] = (f = 2i, 2i + 1),
-    // cos for i < 32, sin for i >= 32 (the f16 rounding error, 2^-12, is below the
-    // bf16 query operand's)
-    uint32_t cs2[64];
+    // cos / sin(j th_f) of this thread's token j for its 32 frequencies, from the
+    // transposed table (a warp's 32 tokens are one 128-byte line per frequency)
+    float cs[32], sn[32];
     auto load_trig = [&](const Walker2d& wb) {
-      int64_t j = static_cast<int64_t>(wb.kb) * kBlock2dTokens + rank * 256 + wg * kTile + row;
-      if (j >= a.trig_rows) j = a.trig_rows - 1;   // past the sequence end: masked anyway
-      const uint4* t4 = reinterpret_cast<const uint4*>(a.trig16 + j * 64);
+      const int64_t j = static_cast<int64_t>(wb.kb) * kBlock2dTokens + rank * kTile + row;
+      const float* tc = a.trigT + static_cast<int64_t>(32 * g) * a.trig_rows + j;
+      const float* ts = tc + 64 * a.trig_rows;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint4 v = __ldg(t4 + i);
-        cs2[4 * i] = v.x; cs2[4 * i + 1] = v.y; cs2[4 * i + 2] = v.z; cs2[4 * i + 3] = v.w;
+      for (int i = 0; i < 32; ++i) {
+        cs[i] = tc[i * a.trig_rows];
+        sn[i] = ts[i * a.trig_rows];
       }
     };
     auto epi_sync = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-    auto arrive_even = [&](uint32_t b) {
-      if (rank == 0) mbar_arrive(b); else mbar_arrive_cluster(b, 0);
-    };
     // score-buffer release: this thread's TMEM reads completed (tcgen05.wait::ld) and
-    // were fenced before the arrive, so the peer's later MMA into the buffer cannot
+    // were fenced before the arrive, so the pair's later MMA into the buffer cannot
     // overtake them; nothing else needs to be made visible, so no cluster release
     auto release_u = [&](uint32_t b) {
       if (rank == 0) {
@@ -624,172 +517,80 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
                      : "memory");
       }
     };
-    // Each thread keeps its token's running sum of the weights of every head (lt);
-    // the sums of the 256 tokens are reduced only when a run's record is written.
-    float lt[kMax2dHeads];
+    // sum over this group's frequencies of one head: cos part u_c, sin part u_s
+    auto half_score = [&](const float (&u_c)[32], const float (&u_s)[32]) {
+      float x0 = 0.f, x1 = 0.f, y0 = 0.f, y1 = 0.f;
 #pragma unroll
-    for (int h = 0; h < kMax2dHeads; ++h) lt[h] = 0.f;
-    // One record per (run, head): m, l and this CTA's share of acc_v (the half of
-    // r_v this warp group reads).  Called by all 256 epilogue threads (it syncs).
-    auto write_record = [&](int b, bool live) {
-      const int64_t rec = 2LL * (b + pair) + rank;
-      if (live && wg < P.nvh) {
-        float v[16];
-        tmem_ld_x16(tmem + lane_base + kDvCol + 32 * wg + 16 * rank, v);
-        tmem_wait_ld();
-        const int r = kTile * wg + row;
-        if (r < a.r_v) {
-#pragma unroll
-          for (int h = 0; h < kMax2dHeads; ++h)
-            if (h < H) a.rec_acc[(rec * H + h) * a.r_v + r] = v[h];
-        }
+      for (int i = 0; i < 16; ++i) {
+        ffma2(x0, x1, u_c[2 * i], u_c[2 * i + 1], cs[2 * i], cs[2 * i + 1]);
+        ffma2(y0, y1, u_s[2 * i], u_s[2 * i + 1], sn[2 * i], sn[2 * i + 1]);
       }
-#pragma unroll
-      for (int h = 0; h < kMax2dHeads; ++h) {
-        if (h < H) {
-          const float ls = warp_sum(lt[h]);
-          if (lane == 0) misc->lp[we][h] = ls;
-        }
-      }
-      epi_sync();
-      if (live && tid_e < H) {
-        float l = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < 8; ++ww) l += misc->lp[ww][tid_e];
-        a.rec_ml[(rec * H + tid_e) * 2] = misc->m_rec[tid_e];
-        a.rec_ml[(rec * H + tid_e) * 2 + 1] = l;
-      }
+      return (x0 + x1) + (y0 + y1);
     };
 
     Walker2d w = start;
-    int prev_b = start.b;
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // the f16 RoPE rows are written
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the transposed RoPE table is written
     load_trig(w);
     bool ok = true;
-    uint32_t uph = 0;   // this group's phase bit of each score buffer's ufull
+    uint32_t G = 0;
     for (int n = 0; n < count; ++n) {
-      const bool run_start = n == 0 || w.kb == 0;
-      {
-        const int jtok = w.kb * kBlock2dTokens + static_cast<int>(rank) * 256 + wg * kTile + row;
-        const bool valid = jtok < w.L;
-        // this warp group's stages of the block: st = 2 h + wg; score buffer (2 H n + st) mod 3
-        const uint32_t gbase = static_cast<uint32_t>(2 * H) * n;
+      const int tile_tok = w.kb * kBlock2dTokens + static_cast<int>(rank) * kTile;
+      const int j = tile_tok + row;
+      const bool valid = j < w.L;
+      const bool tvalid = tile_tok < w.L;     // the tile holds a token of the sequence
+      const int64_t grp = tile_tok / 32 + q;  // this warp's 32 tokens
 #pragma unroll 1
-        for (int h = 0; h < H; ++h) {
-          const uint32_t G = gbase + 2 * h + wg;
-          const uint32_t uslot = G % kNU;
-          if (ok) ok = warp_wait(bar(misc->ufull[wg][uslot]), (uph >> uslot) & 1u, abort, a.status);
-          uph ^= 1u << uslot;
-          float s = -INFINITY;
-          if (ok) {
-            tc_fence_after();
-            const uint32_t tU = tmem + lane_base + 128 * uslot;
-            float acc0 = 0.f, acc1 = 0.f;
+      for (int p = 0; p < HP; ++p, ++G) {
+        const uint32_t buf = G & 1u;
+        if (ok) ok = warp_wait(bar(misc->ufull[buf]), (G >> 1) & 1u, abort, a.status);
+        bool released = false;
+        float part[2] = {0.f, 0.f};   // this group's half of head 2p, 2p + 1
+        if (ok) {
+          tc_fence_after();
+          const uint32_t tU = tmem + lane_base + 256 * buf + 32 * g;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {   // 64 columns per round, two loads in flight
-              float u0[32], u1[32];
-              tmem_ld_x32(tU + 64 * hf, u0);
-              tmem_ld_x32(tU + 64 * hf + 32, u1);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float2 t0 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + i]));
-                const float2 t1 = __half22float2(*reinterpret_cast<const __half2*>(&cs2[32 * hf + 16 + i]));
-                acc0 = fmaf(u0[2 * i], t0.x, acc0);
-                acc1 = fmaf(u0[2 * i + 1], t0.y, acc1);
-                acc0 = fmaf(u1[2 * i], t1.x, acc0);
-                acc1 = fmaf(u1[2 * i + 1], t1.y, acc1);
-              }
+          for (int hh = 0; hh < 2; ++hh) {
+            float u_c[32], u_s[32];
+            tmem_ld_x32(tU + 128 * hh, u_c);
+            tmem_ld_x32(tU + 128 * hh + 64, u_s);
+            tmem_wait_ld();
+            if (hh == 1) {
+              // every read of the buffer has completed: hand it back before the sums
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) release_u(bar(misc->uempty[buf]));
+              released = true;
             }
-            if (valid) s = acc0 + acc1;
-            tc_fence_before();
+            part[hh] = half_score(u_c, u_s);
           }
-          tmem_st_x1(tmem + lane_base + kScoreCol + 16 * wg + h, __float_as_uint(s));
-          const float wm = warp_max_redux(s);   // this warp's maximum of head h over its 32 tokens
-          tmem_wait_st();
+        }
+        if (!released) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            release_u(bar(misc->uempty[uslot]));
-            misc->mx[we][h] = wm;
-            // the MMAs of this stage are complete: window h is free after group 1's
-            // stage, the block's tile of this group after its last stage
-            if (wg == 1) mbar_arrive(bar(misc->zempty[(static_cast<uint32_t>(H) * n + h) & (kNZ - 1)]));
-            if (h == H - 1) mbar_arrive(bar(misc->kempty[(2u * n + wg) % kNK]));
-          }
+          if (lane == 0) release_u(bar(misc->uempty[buf]));
+        }
+        // exchange halves: this group keeps head 2p + g
+        const float mine = g ? part[1] : part[0], other = g ? part[0] : part[1];
+        misc->xch[buf][1 - g][row] = other;
+        epi_sync();
+        const float s = valid ? mine + misc->xch[buf][g][row] : -INFINITY;
+        // the group's weights 2^(s - m), m = ceil(max s) over its 32 tokens (-inf
+        // when none of them is in the sequence), and their sum
+        const float m = ceilf(warp_max_redux(s));
+        const __nv_bfloat16 pb = __float2bfloat16_rn(valid ? exp2f(s - m) : 0.f);
+        const int h = 2 * p + g;
+        if (tvalid) a.pw[(static_cast<int64_t>(w.b) * H + h) * prow + j] = __bfloat16_as_ushort(pb);
+        const float l = warp_sum(__bfloat162float(pb));
+        if (tvalid && lane == 0) {
+          float* ml = a.grp_ml + ((static_cast<int64_t>(w.b) * H + h) * ngroups + grp) * 2;
+          ml[0] = m;
+          ml[1] = l;
         }
       }
-      Walker2d wn = w;
-      walk_advance(wn, a);
-      // this thread's token rows are no longer needed: fetch the next block's now
-      if (n + 1 < count) load_trig(wn);
-
-      // ---- end of block: exact per-head maximum over the CTA's 256 tokens sets the
-      // reference (raised lazily: only when the block maximum exceeds it by 2^8)
-      epi_sync();
-      if (tid_e < H) {
-        const int h = tid_e;
-        float mb = misc->mx[0][h];
-#pragma unroll
-        for (int ww = 1; ww < 8; ++ww) mb = fmaxf(mb, misc->mx[ww][h]);
-        const float mo = misc->m_ref[h];
-        const float base = run_start ? -INFINITY : mo;
-        const float mn = mb > base + kRescaleLog2 ? mb : base;
-        misc->m_new[h] = mn;
-        misc->alpha[h] = (run_start || mn == base) ? 1.f : exp2f(base - mn);
-        if (run_start) misc->m_rec[h] = mo;   // the finished run's reference
-        misc->m_ref[h] = mn;
-      }
-      epi_sync();
-      // the previous block's value MMAs are complete: D_v and P may be touched
-      if (n > 0) {
-        if (ok) ok = warp_wait(bar(misc->vdone), (n - 1) & 1, abort, a.status);
-        tc_fence_after();
-      }
-      // a run ended with the previous block: its record, before D_v is reused
-      if (n > 0 && run_start) write_record(prev_b, ok);
-      bool rescale = false;
-      float sc[16];   // this token's scores of the block, one per head
-      tmem_ld_x16(tmem + lane_base + kScoreCol + 16 * wg, sc);
-      tmem_wait_ld();
-#pragma unroll
-      for (int h = 0; h < kMax2dHeads; ++h) {
-        if (h < H) {
-          const float mn = misc->m_new[h], al = misc->alpha[h];
-          if (al != 1.f) rescale = true;
-          const float p = mn == -INFINITY ? 0.f : exp2f(sc[h] - mn);
-          const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + (tid_e >> 4) * 512 +
-                                            swizzle_offset(h * 32 + (tid_e & 15) * 2, 32)) = pb;
-          lt[h] = (run_start ? 0.f : lt[h] * al) + __bfloat162float(pb);
-        }
-      }
-      // the reference of some head rose: rescale this CTA's accumulators (columns = heads)
-      if (rescale && ok && wg < P.nvh) {
-        const uint32_t dcol = tmem + lane_base + kDvCol + 32 * wg + 16 * rank;
-        float v[16];
-        tmem_ld_x16(dcol, v);
-        tmem_wait_ld();
-        uint32_t o[16];
-#pragma unroll
-        for (int h = 0; h < kMax2dHeads; ++h) o[h] = __float_as_uint(h < H ? v[h] * misc->alpha[h] : v[h]);
-        tmem_st_x16(dcol, o);
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();   // P visible to the value MMA
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_even(bar(misc->pfull));
-      prev_b = w.b;
-      w = wn;
+      walk_advance(w, a);
+      // this thread's token row is no longer needed: fetch the next block's now
+      if (n + 1 < count) load_trig(w);
     }
-    // the last run: its record once the last value MMAs are complete
-    if (tid_e < H) misc->m_rec[tid_e] = misc->m_ref[tid_e];
-    if (ok) {
-      ok = warp_wait(bar(misc->vdone), (count - 1) & 1, abort, a.status);
-      tc_fence_after();
-    }
-    write_record(prev_b, ok);
   }
 
   tc_fence_before();
@@ -802,11 +603,317 @@ decode2d_bf16_kernel(const __grid_constant__ Decode2dArgs a, const __grid_consta
   }
 }
 
+struct alignas(16) MiscValue {
+  uint64_t full[kVS], fixed[kVS], empty[kVS];
+  uint64_t dfull[2], dempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int start_b, start_t, count, total_tiles;
+  float mrun[2][kMax2dHeads], lrun[2][kMax2dHeads];   // per run parity: M and l of each head
+  float pm[8][kMax2dHeads], pl[8][kMax2dHeads];       // partial (M, l) of 8 group subsets
+  int scan[kValue2dThreads];
+};
+static_assert(sizeof(MiscValue) <= 4096, "value misc region");
+
+// Tile of one sequence: tokens [128 t, 128 t + 128).
+struct TileWalker {
+  int b, t, nt, L;
+  __device__ __forceinline__ void advance(const Decode2dArgs& a) {
+    if (++t < nt) return;
+    t = 0;
+    while (true) {
+      if (++b >= a.B) { nt = 0; return; }
+      L = clamp_len(__ldg(a.seq_lens + b), a.L_max);
+      nt = ntiles_of(L);
+      if (nt > 0) return;
+    }
+  }
+};
+
+// D_v of every head over runs of 128-token tiles (Appendix J):
+//   D[r][h] = sum_j 2^(m_g(j) - M) p_j,h c_v,j[r],   l[h] = sum_g 2^(m_g - M) l_g,
+// over the 32-token groups g of the run, with M the largest m_g (all of them
+// integers, so each scale is an exact power of two).  One record (M, l, D) per (sequence, CTA).  Roles: warp 0
+// copies (V tile + weight tile per ring stage), warp 1 issues the MMAs (M = 128
+// rows of r_v, N = 16 heads, K = 16 tokens), warps 2-5 scale each weight tile,
+// zero V rows past the sequence end, and write the records.
+__global__ void __launch_bounds__(kValue2dThreads, 1)
+decode2d_value_kernel(const __grid_constant__ Decode2dArgs a, const __grid_constant__ Decode2dMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const Decode2dPlan& P = a.plan;
+  const uint32_t sbase = smem_u32(sm);
+  MiscValue* misc = reinterpret_cast<MiscValue*>(sm + P.v_misc);
+  volatile int* abort = &misc->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) misc->abort = 0;
+  share_of<kValue2dThreads>(
+      a, [&](int b) { return ntiles_of(clamp_len(__ldg(a.seq_lens + b), a.L_max)); }, blockIdx.x, gridDim.x,
+      misc->scan, &misc->start_b, &misc->start_t, &misc->count, &misc->total_tiles);
+  const int count = misc->count;
+  if (count == 0) return;
+  TileWalker start;
+  start.b = misc->start_b;
+  start.t = misc->start_t;
+  start.L = clamp_len(__ldg(a.seq_lens + start.b), a.L_max);
+  start.nt = ntiles_of(start.L);
+
+  auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
+  if (tid == 0) {
+    for (int s = 0; s < kVS; ++s) {
+      mbar_init(bar(misc->full[s]), 1);
+      mbar_init(bar(misc->fixed[s]), 4);   // the 4 scaling warps
+      mbar_init(bar(misc->empty[s]), 1);   // MMA commit
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(misc->dfull[i]), 1);   // MMA commit after a run's last tile
+      mbar_init(bar(misc->dempty[i]), 4);  // the 4 record warps
+    }
+    mbar_init(bar(misc->mma_done), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.v);
+    prefetch_tmap(&maps.p);
+  }
+  // weight rows of heads >= H stay zero (the copies write H rows of each box)
+  for (int s = 0; s < kVS; ++s)
+    for (int i = tid; i < 4096 / 16; i += kValue2dThreads)
+      reinterpret_cast<uint4*>(sm + P.v_ring + s * P.v_stage + P.nvb * 16384)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(&misc->tmem_base), 64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  // the combine grid may be scheduled now; it waits for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the weights and tile maxima are written by the score grid
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      TileWalker w = start;
+      RingPos r;
+      int issued = 0;
+      bool ok = true;
+      const uint64_t pol_stream = l2_policy_evict_first();
+      for (int i = 0; i < count && ok; ++i) {
+        const int s = r.slot;
+        if (!(ok = mbar_wait(bar(misc->empty[s]), r.phase ^ 1u, abort, a.status))) break;
+        const uint32_t fb = bar(misc->full[s]);
+        mbar_arrive_expect_tx(fb, P.nvb * 16384 + 2 * 64 * 2 * a.H);
+        const uint32_t dst = sbase + P.v_ring + s * P.v_stage;
+        const int y = w.t * kVTile;
+        for (int bx = 0; bx < P.nvb; ++bx) tma_load_3d_hint(dst + bx * 16384, &maps.v, fb, 64 * bx, y, w.b, pol_stream);
+        for (int kb = 0; kb < 2; ++kb) tma_load_3d(dst + P.nvb * 16384 + kb * 2048, &maps.p, fb, y + 64 * kb, 0, w.b);
+        ++issued;
+        r.next(kVS);
+        w.advance(a);
+      }
+      for (int i = max(0, issued - kVS); i < issued; ++i) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar(misc->full[i % kVS]), (i / kVS) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer (whole warp)
+    const uint32_t idesc = umma_idesc_bf16(128, 16, true, false);
+    // MN-major V: 64-row r_v boxes 16 KB apart (LBO), 8 token rows 1 KB apart (SBO);
+    // K-major weights: 16 head rows, 64-token boxes 2 KB apart
+    const uint64_t dV0 = umma_desc(sbase + P.v_ring, 16384, 1024, kSw128);
+    const uint64_t dP0 = umma_desc(sbase + P.v_ring + P.nvb * 16384, 16, 1024, kSw128);
+    const uint32_t vst = static_cast<uint32_t>(P.v_stage) >> 4;
+    auto agree = [](bool r) { return __all_sync(0xffffffffu, r); };
+    TileWalker w = start;
+    RingPos r;
+    bool ok = true;
+    uint32_t run = 0;
+    for (int i = 0; i < count && ok; ++i) {
+      const int s = r.slot;
+      const bool run_start = i == 0 || w.t == 0;
+      const bool run_end = i == count - 1 || w.t == w.nt - 1;
+      const uint32_t db = run & 1u;
+      if (!(ok = agree(mbar_wait(bar(misc->fixed[s]), r.phase, abort, a.status)))) break;
+      if (run_start && !(ok = agree(mbar_wait(bar(misc->dempty[db]), ((run >> 1) & 1u) ^ 1u, abort, a.status)))) break;
+      tc_fence_after();
+      const uint64_t av = dV0 + s * vst, bp = dP0 + s * vst;
+      const int valid = w.L - w.t * kVTile;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {   // 16-token K steps: +2 KB in each V box, +32 B in the weight rows
+        if (16 * k >= valid) break;
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci)
+          if (ci < P.nvc)
+            umma_bf16_warp(tmem + 32 * db + 16 * ci, av + ci * ((2 * 16384) >> 4) + k * (2048 >> 4),
+                           bp + (k >> 2) * (2048 >> 4) + (k & 3) * 2, idesc, (!run_start || k > 0) ? 1u : 0u);
+      }
+      umma_commit_warp(bar(misc->empty[s]));
+      if (run_end) {
+        umma_commit_warp(bar(misc->dfull[db]));
+        ++run;
+      }
+      r.next(kVS);
+      w.advance(a);
+    }
+    umma_commit_warp(bar(misc->mma_done));
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+  } else {
+    // ======================================================== scaling and records (warps 2-5)
+    const int ft = tid - 64, q = warp & 3;
+    const int row = 32 * q + lane;                     // r_v row in a 128-row chunk (TMEM lane)
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const int H = a.H;
+    auto grp_sync = []() { asm volatile("bar.sync 2, 128;" ::: "memory"); };
+    // weight row (head) this thread scales, and the 8-token piece of it: the 16-byte
+    // chunk ft & 7 as stored holds logical chunk (ft & 7) ^ (row & 7) (128-byte swizzle)
+    const int hs = ft >> 3, piece = (ft & 7) ^ (hs & 7);
+    const int64_t ngroups = a.ntiles * 4;
+    TileWalker w = start;
+    RingPos r;
+    bool ok = true;
+    uint32_t run = 0;
+    for (int i = 0; i < count; ++i) {
+      const bool run_start = i == 0 || w.t == 0;
+      const bool run_end = i == count - 1 || w.t == w.nt - 1;
+      const int par = run & 1;
+      if (run_start) {
+        // the run: tiles [w.t, te) of sequence w.b; its M and l per head, from 8
+        // partial merges of the groups' (m, l) (groups past the sequence end hold
+        // m = -inf and are skipped)
+        const int te = min(w.nt, w.t + (count - i));
+        const int h = ft & 15, sub = ft >> 4;
+        float M = -INFINITY, l = 0.f;
+        if (h < H) {
+          const float* ml = a.grp_ml + (static_cast<int64_t>(w.b) * H + h) * ngroups * 2;
+          for (int gi = 4 * w.t + sub; gi < 4 * te; gi += 8) {
+            const float m = ml[2 * gi], lg = ml[2 * gi + 1];
+            if (m == -INFINITY) continue;
+            if (m > M) { l = l * exp2f(M - m) + lg; M = m; }
+            else l += lg * exp2f(m - M);
+          }
+        }
+        misc->pm[sub][h] = M;
+        misc->pl[sub][h] = l;
+        grp_sync();
+        if (ft < H) {
+          float Mr = misc->pm[0][ft];
+#pragma unroll
+          for (int u = 1; u < 8; ++u) Mr = fmaxf(Mr, misc->pm[u][ft]);
+          float lr = 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (misc->pm[u][ft] != -INFINITY) lr += misc->pl[u][ft] * exp2f(misc->pm[u][ft] - Mr);
+          misc->mrun[par][ft] = Mr;
+          misc->lrun[par][ft] = lr;
+        }
+        grp_sync();
+      }
+      // 2^(m_g - M_run), an exact power of two, for the group of each of this
+      // thread's two pieces (tokens 64 kb + 8 piece ...)
+      float sc[2] = {0.f, 0.f};
+      if (hs < H) {
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const int64_t gi = 4 * static_cast<int64_t>(w.t) + 2 * kb + (piece >> 2);
+          const float m = a.grp_ml[((static_cast<int64_t>(w.b) * H + hs) * ngroups + gi) * 2];
+          const float Mr = misc->mrun[par][hs];
+          if (m != -INFINITY && Mr != -INFINITY) {
+            const int e = static_cast<int>(m - Mr);
+            sc[kb] = e < -126 ? 0.f : __int_as_float((127 + e) << 23);
+          }
+        }
+      }
+      const int s = r.slot;
+      if (ok) ok = warp_wait(bar(misc->full[s]), r.phase, abort, a.status);
+      uint8_t* st = sm + P.v_ring + s * P.v_stage;
+      if (ok) {
+        // weights: 16 rows of 128 B in each of the two 64-token boxes; thread ft takes
+        // 16 bytes of row hs in both (the swizzle moves chunks within a row only)
+        if (hs < H) {
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            uint4* pp = reinterpret_cast<uint4*>(st + P.nvb * 16384 + kb * 2048) + ft;
+            uint4 v = *pp;
+            uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[c]));
+              u[c] = bf16x2_bits(__floats2bfloat162_rn(f.x * sc[kb], f.y * sc[kb]));
+            }
+            *pp = v;
+          }
+        }
+        // V rows past the sequence end may hold anything: zero them (0 * x stays 0)
+        const int valid = w.L - w.t * kVTile;
+        if (valid < kVTile) {
+          const int per_box = (kVTile - valid) * 8;
+          for (int x = ft; x < P.nvb * per_box; x += 128) {
+            const int bx = x / per_box, rr = valid + (x - bx * per_box) / 8, c16 = x & 7;
+            *reinterpret_cast<uint4*>(st + bx * 16384 + rr * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(misc->fixed[s]));
+      r.next(kVS);
+      if (run_end) {
+        // the run's record, once its last MMAs are complete
+        const uint32_t db = run & 1u;
+        if (ok) ok = warp_wait(bar(misc->dfull[db]), (run >> 1) & 1u, abort, a.status);
+        tc_fence_after();
+        const int64_t rec = static_cast<int64_t>(w.b) + blockIdx.x;
+        if (ok) {
+#pragma unroll
+          for (int ci = 0; ci < 2; ++ci) {
+            if (ci < P.nvc) {
+              float v[16];
+              tmem_ld_x16(tmem + lane_base + 32 * db + 16 * ci, v);
+              tmem_wait_ld();
+              const int rr = 128 * ci + row;
+              if (rr < a.r_v) {
+#pragma unroll
+                for (int h = 0; h < kMax2dHeads; ++h)
+                  if (h < H) a.rec_acc[(rec * H + h) * a.r_v + rr] = v[h];
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(misc->dempty[db]));
+        if (ft < H) {
+          a.rec_ml[(rec * H + ft) * 2] = misc->mrun[par][ft];
+          a.rec_ml[(rec * H + ft) * 2 + 1] = misc->lrun[par][ft];
+        }
+        ++run;
+      }
+      w.advance(a);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
 // Merge the run records of each (sequence, head) by log-sum-exp, apply the V
 // up-projection once (Appendix J identity) and normalise:
 //   out = (sum_c 2^(m_c - M) acc_c) W_up,v,t,h^T / (sum_c 2^(m_c - M) l_c) + mu_v,t,h.
-// A sequence's records come from the pairs whose block ranges overlap it (both
-// CTAs of each).  Block = (head h, two consecutive sequences); W_up,v,t,h is
+// A sequence's records come from the value CTAs whose tile ranges overlap it.  Block = (head h, two consecutive sequences); W_up,v,t,h is
 // staged in shared memory (rows padded by one word) before the wait for the
 // decode grid.
 constexpr int kCombineUnits = 2;
@@ -847,9 +954,9 @@ __global__ void __launch_bounds__(kCombineThreads) decode2d_combine_kernel(const
       }
     }
   }
-  int before = 0, all = 0;   // blocks of sequences [0, b0) and [0, B)
+  int before = 0, all = 0;   // tiles of sequences [0, b0) and [0, B)
   for (int bb = tid; bb < a.B; bb += kCombineThreads) {
-    const int n = nblocks(clamp_len(__ldg(a.seq_lens + bb), a.L_max));
+    const int n = ntiles_of(clamp_len(__ldg(a.seq_lens + bb), a.L_max));
     all += n;
     if (bb < b0) before += n;
   }
@@ -876,16 +983,16 @@ __global__ void __launch_bounds__(kCombineThreads) decode2d_combine_kernel(const
   const int b = b0 + warp;
   if (warp < kCombineUnits && b < a.B) {
     long long B0 = pre;
-    for (int bb = b0; bb < b; ++bb) B0 += nblocks(clamp_len(__ldg(a.seq_lens + bb), a.L_max));
-    const int nb = nblocks(clamp_len(__ldg(a.seq_lens + b), a.L_max));
+    for (int bb = b0; bb < b; ++bb) B0 += ntiles_of(clamp_len(__ldg(a.seq_lens + bb), a.L_max));
+    const int nb = ntiles_of(clamp_len(__ldg(a.seq_lens + b), a.L_max));
     if (nb > 0) {
-      const long long NB = tot, NP = a.pairs;
+      const long long NB = tot, NP = a.units;
       const long long p0 = ((B0 + 1) * NP - 1) / NB, p1 = ((B0 + nb) * NP - 1) / NB;
       for (long long p = p0; p <= p1; ++p) {
         const long long lo = p * NB / NP, hi = (p + 1) * NB / NP;
-        if (max(lo, B0) >= min(hi, B0 + nb)) continue;   // the pair saw no block of b
-        for (int r = 0; r < 2; ++r) {
-          const long long rec = 2 * (b + p) + r;
+        if (max(lo, B0) >= min(hi, B0 + nb)) continue;   // the value CTA saw no tile of b
+        {
+          const long long rec = b + p;
           const float mr = a.rec_ml[(rec * a.H + h) * 2], lr = a.rec_ml[(rec * a.H + h) * 2 + 1];
           const float* ar = a.rec_acc + (rec * a.H + h) * a.r_v;
           float x[8];
@@ -941,23 +1048,28 @@ __global__ void __launch_bounds__(kCombineThreads) decode2d_combine_kernel(const
 
 bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p) {
   *p = Decode2dPlan{};
-  if (H < 4 || H > kMax2dHeads || H % 4 || r_k < 16 || r_k > 128 || r_v < 16 || r_v > 256 || r_k % 16 ||
+  if (H < 2 || H > kMax2dHeads || H % 2 || r_k < 16 || r_k > 128 || r_v < 16 || r_v > 256 || r_k % 16 ||
       r_v % 16)
     return false;
+  // score kernel
   p->nkc = (r_k + 63) / 64;
-  p->nvh = (r_v + 127) / 128;
   p->k_stage = p->nkc * 16384;
-  p->z_stage = p->nkc * 8192 + 2048;   // half window rows, then their 16-wide bias operand
-  p->v_stage = p->nvh * 8192;   // 32 tokens x (128 r_v) x 2 B per half
+  p->z_stage = p->nkc * 16384 + 4096;   // one head's 128 operand rows, then their bias operand
   int off = 0;
-  p->k_ring = off; off += kNK * p->k_stage;
-  p->z_ring = off; off += kNZ * p->z_stage;
-  p->v_ring = off; off += kNV * p->v_stage;
-  p->p = off;      off += 16 * 512;   // P: 16-token K chunks of 16 head rows
+  p->k_ring = off; off += kSNK * p->k_stage;
+  p->z_ring = off; off += kSNZ * p->z_stage;
   p->aug_a = off;  off += 4096;
   p->misc = off;   off += 4096;
   p->bytes = off + 1024;
-  return p->bytes <= kSmemLimit;
+  // value kernel: per stage the V tile (64-wide r_v boxes of 128 tokens), then the
+  // weight tile (two 64-token boxes of 16 head rows)
+  p->nvb = (r_v + 63) / 64;
+  p->nvc = (r_v + 127) / 128;
+  p->v_stage = p->nvb * 16384 + 4096;
+  p->v_ring = 0;
+  p->v_misc = kVS * p->v_stage;
+  p->v_bytes = p->v_misc + 4096 + 1024;
+  return p->bytes <= kSmemLimit && p->v_bytes <= kSmemLimit;
 }
 
 size_t decode2d_zimg_stride(int H, int r_k) {
@@ -966,29 +1078,33 @@ size_t decode2d_zimg_stride(int H, int r_k) {
   return (b + 1023) / 1024 * 1024;
 }
 
-int64_t decode2d_trig_rows(int64_t L_max, int64_t rope_len) {
-  // positions a block can touch: up to L_max rounded up to a whole block
-  const int64_t need = (L_max + kBlock2dTokens - 1) / kBlock2dTokens * kBlock2dTokens;
-  return need < rope_len ? need : rope_len;
+int64_t decode2d_trig_rows(int64_t L_max) {
+  return (L_max + kBlock2dTokens - 1) / kBlock2dTokens * kBlock2dTokens;
 }
 
 cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cudaStream_t s) {
-  static int configured = 0;
+  static int configured = 0, vconfigured = 0;
   if (configured < a.plan.bytes) {
-    cudaError_t e = cudaFuncSetAttribute(decode2d_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode2d_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          a.plan.bytes);
     if (e != cudaSuccess) return e;
     configured = a.plan.bytes;
+  }
+  if (vconfigured < a.plan.v_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(decode2d_value_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         a.plan.v_bytes);
+    if (e != cudaSuccess) return e;
+    vconfigured = a.plan.v_bytes;
   }
   // pairs that can be resident at once (each CTA needs a whole SM)
   static int pairs_for = -1, max_pairs = 0;
   if (pairs_for != a.plan.bytes) {
     cudaLaunchConfig_t occ = {};
     occ.gridDim = dim3(2);
-    occ.blockDim = dim3(kDecode2dThreads);
+    occ.blockDim = dim3(kScore2dThreads);
     occ.dynamicSmemBytes = a.plan.bytes;
     int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, decode2d_bf16_kernel, &occ);
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, decode2d_score_kernel, &occ);
     if (e != cudaSuccess) return e;
     max_pairs = n;
     pairs_for = a.plan.bytes;
@@ -996,14 +1112,14 @@ cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cuda
   if (max_pairs < 1) return cudaErrorLaunchOutOfResources;
   a.pairs = std::min(a.pairs, std::min(max_pairs, kMaxPairs));
   if (a.pairs < 1) a.pairs = 1;
+  if (a.units < 1) a.units = 1;
 
-  const int trig_blocks = static_cast<int>((a.trig_rows + kTrigRowsPerBlock - 1) / kTrigRowsPerBlock);
-  decode2d_z_kernel<<<a.B * a.H + trig_blocks, kZThreads, 0, s>>>(a);
+  decode2d_z_kernel<<<a.B * a.H + static_cast<int>(a.trig_rows / kTrigTokensPerBlock), kZThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.pairs);
-  cfg.blockDim = dim3(kDecode2dThreads);
+  cfg.blockDim = dim3(kScore2dThreads);
   cfg.dynamicSmemBytes = a.plan.bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1011,7 +1127,12 @@ cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cuda
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode2d_bf16_kernel, a, maps);
+  e = cudaLaunchKernelEx(&cfg, decode2d_score_kernel, a, maps);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(a.units);
+  cfg.blockDim = dim3(kValue2dThreads);
+  cfg.dynamicSmemBytes = a.plan.v_bytes;
+  e = cudaLaunchKernelEx(&cfg, decode2d_value_kernel, a, maps);
   if (e != cudaSuccess) return e;
   const size_t csmem = combine_smem_bytes(a.r_v);
   static size_t cconfigured = 0;

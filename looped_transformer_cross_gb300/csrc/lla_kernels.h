@@ -194,23 +194,30 @@ cudaError_t launch_window_attn(const WindowArgs& a, bool bf16, cudaStream_t s);
 
 // ----------------------------------------------------------------- LLA-2D decode
 
-constexpr int kDecode2dThreads = 320;   // producer, MMA issuer / relay, 8 epilogue warps
-constexpr int kBlock2dTokens = 512;     // tokens of a pair block: 2 tiles per CTA
-constexpr int kMax2dHeads = 16;         // heads of one shared latent (value MMA N = 32)
+constexpr int kScore2dThreads = 320;    // producer, MMA issuer / relay, 8 epilogue warps
+constexpr int kBlock2dTokens = 256;     // tokens of a pair block: one 128-token tile per CTA
+constexpr int kMax2dHeads = 16;         // heads of one shared latent (value MMA N = 16)
 constexpr int kMaxPairs = kMaxGrid / 2;
+constexpr int kValue2dThreads = 192;    // producer, MMA issuer, 4 scaling / record warps
 
-// Shared-memory plan of the LLA-2D decode kernel (byte offsets from a 1024-aligned base).
+// Shared-memory plans (byte offsets from a 1024-aligned base) of the LLA-2D score
+// kernel (CTA pairs) and value kernel (one CTA per SM).
 struct Decode2dPlan {
   int nkc;                           // 64-wide K chunks of a latent / query-operand row (r_k <= 128)
-  int nvh;                           // 128-row halves of r_v (value MMA M = 256 per pair)
-  int k_stage, z_stage, v_stage;     // ring stage strides
-  int k_ring, z_ring, v_ring, p, aug_a, misc;
+  int k_stage, z_stage;              // ring stage strides
+  int k_ring, z_ring, aug_a, misc;
   int bytes;
+  int nvb;                           // 64-wide r_v boxes of a value tile (r_v <= 256)
+  int nvc;                           // 128-row r_v chunks (value MMA M = 128)
+  int v_stage;                       // value ring stage: V tile, then the weight tile
+  int v_ring, v_p, v_misc;
+  int v_bytes;
 };
 
 struct Decode2dArgs {
-  int B, H, r_k, r_v, rope_style, pairs;
+  int B, H, r_k, r_v, rope_style, pairs, units;
   int64_t L_max, rope_len;
+  int64_t ntiles;                    // 128-token tiles per sequence slot: ceil(L_max / 128)
   const void* q;                     // [B][H][128]
   const int32_t* seq_lens;           // [B]
   const int32_t* q_pos;              // [B]
@@ -223,25 +230,34 @@ struct Decode2dArgs {
   float* out;                        // [B][H][128]
   float* lse;                        // [B][H]
   uint32_t* status;
-  float* rec_acc;                    // [2 * (B + pairs)][H][r_v] run records
-  float* rec_ml;                     // [2 * (B + pairs)][H][2]   (m, l) of each record
+  float* rec_acc;                    // [B + units][H][r_v] run records of the value kernel
+  float* rec_ml;                     // [B + units][H][2]   (m, l) of each record
   uint8_t* zimg;                     // per sequence: nkc chunks of [H*128 rows][128 B], then the bias
                                      // operand [H*128 rows][16 bf16] (32 B rows)
   int64_t zimg_stride;               // bytes per sequence image
   int64_t zchunk_bytes;              // H * 128 * 128
-  uint32_t* trig16;                  // [trig_rows][64] f16 pairs: cos(p th_2i), cos(p th_2i+1), then sin
-  int64_t trig_rows;                 // rows of trig16 (positions 0 .. trig_rows - 1)
+  float* trigT;                      // [128][trig_rows]: cos(j th_c) for c < 64, then sin(j th_c-64)
+  int64_t trig_rows;                 // positions of trigT: L_max rounded up to a whole block
+  uint16_t* pw;                      // softmax weights, bf16 [B][H][ntiles * 128], each 32-token group
+                                     // relative to 2^m of that group
+  float* grp_ml;                     // [B][H][ntiles * 4][2]: m of each 32-token group (an integer in
+                                     // log2 units, -inf for a group past the sequence end) and the sum
+                                     // of its bf16 weights
   Decode2dPlan plan;
 };
 
 struct Decode2dMaps {
   CUtensorMap k;                     // latent K: box (64, 128, 1) over (r_k, L_max, B), 128B swizzle
-  CUtensorMap v;                     // latent V: box (64, 32, 1) over (r_v, L_max, B), 128B swizzle
+  CUtensorMap z;                     // query-operand images, copied as stored (already swizzled):
+                                     // box (64, 128, 1) over (64, nkc * H * 128 rows, B)
+  CUtensorMap zb;                    // their bias operand: box (16, 128, 1) over (16, H * 128 rows, B)
+  CUtensorMap v;                     // latent V: box (64, 128, 1) over (r_v, L_max, B), 128B swizzle
+  CUtensorMap p;                     // weights: box (64, H, 1) over (ntiles * 128, H, B), 128B swizzle
 };
 
 bool make_decode2d_plan(int H, int r_k, int r_v, Decode2dPlan* p);
 size_t decode2d_zimg_stride(int H, int r_k);
-int64_t decode2d_trig_rows(int64_t L_max, int64_t rope_len);
+int64_t decode2d_trig_rows(int64_t L_max);
 cudaError_t launch_decode2d_bf16(Decode2dArgs& a, const Decode2dMaps& maps, cudaStream_t s);
 
 // ----------------------------------------------------------------- encode
