@@ -65,7 +65,7 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t partials, rec_ml, bias, scores, zimg, zimg_stride, trig16, pw, grp_ml, total;
+  size_t partials, rec_ml, bias, scores, zimg, zimg_stride, trig16, pw, grp_m, total;
 };
 
 // Bytes of one unit's query-operand image: Z (128 rows x r_k bf16, K-chunk
@@ -98,7 +98,7 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
       w.zimg_stride = decode2d_zimg_stride(d->H, d->r_k);
       off += al256(static_cast<size_t>(B) * w.zimg_stride);
     }
-    // softmax weights (bf16 [B][H][tiles * 128]) and per-32-token-group (m, l) of the
+    // softmax weights (bf16 [B][H][tiles * 128]) and per-32-token-group m of the
     // score kernel
     const size_t tiles = static_cast<size_t>((L_max + kTile - 1) / kTile);
     // the transposed RoPE table [128][positions] fp32, positions up to L_max rounded
@@ -107,8 +107,8 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
     if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(128) * decode2d_trig_rows(L_max) * 4);
     w.pw = off;
     if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(B) * d->H * tiles * kTile * 2);
-    w.grp_ml = off;
-    if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(B) * d->H * tiles * 4 * 2 * 4);
+    w.grp_m = off;
+    if (d->dtype == LLA_BF16) off += al256(static_cast<size_t>(B) * d->H * tiles * 4 * 4);
     w.total = off;
     return w;
   }
@@ -321,7 +321,7 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
     a.trig_rows = decode2d_trig_rows(cache.L_max);
     a.trigT = reinterpret_cast<float*>(ws + wl.trig16);
     a.pw = reinterpret_cast<uint16_t*>(ws + wl.pw);
-    a.grp_ml = reinterpret_cast<float*>(ws + wl.grp_ml);
+    a.grp_m = reinterpret_cast<float*>(ws + wl.grp_m);
     const int sms = sm_count();
     if (sms <= 1) return LLA_ERR_CUDA;
     const int64_t max_blocks = static_cast<int64_t>(cache.B) * ((cache.L_max + kBlock2dTokens - 1) / kBlock2dTokens);

@@ -25,12 +25,12 @@
 //     thread, warp group g takes head 2p + g) form the rotary score
 //     s = sum_f cos(j th_f) U_f + sin(j th_f) U_64+f from the token's cos/sin row
 //     held in registers and write, per 32-token group (one warp), the weights
-//     p = 2^(s - m) (bf16) with m = ceil(max s), an integer, and (m, sum p).
+//     p = 2^(s - m) (bf16) with m = ceil(max s), an integer, and m.
 //  3. decode2d_value_kernel (one CTA per SM): D_v = sum_j p_j c_v,j for every head
 //     over contiguous runs of 128-token tiles, on the tensor cores (M = 128 r_v
 //     rows, N = 16 heads, K = tokens; Appendix J), the weights of each group first
-//     scaled by 2^(m_group - M_run) (exact: both are integers), one record
-//     (M_run, l_run, D_v) per run.
+//     scaled by 2^(m_group - M_run) (exact: both are integers) and summed into
+//     l_run, one record (M_run, l_run, D_v) per run.
 //  4. decode2d_combine_kernel: merges the records of a sequence (log-sum-exp
 //     merge) and applies the V up-projection once.
 //
@@ -575,16 +575,13 @@ decode2d_score_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
         epi_sync();
         const float s = valid ? mine + misc->xch[buf][g][row] : -INFINITY;
         // the group's weights 2^(s - m), m = ceil(max s) over its 32 tokens (-inf
-        // when none of them is in the sequence), and their sum
+        // when none of them is in the sequence)
         const float m = ceilf(warp_max_redux(s));
         const __nv_bfloat16 pb = __float2bfloat16_rn(valid ? exp2f(s - m) : 0.f);
         const int h = 2 * p + g;
-        if (tvalid) a.pw[(static_cast<int64_t>(w.b) * H + h) * prow + j] = __bfloat16_as_ushort(pb);
-        const float l = warp_sum(__bfloat162float(pb));
-        if (tvalid && lane == 0) {
-          float* ml = a.grp_ml + ((static_cast<int64_t>(w.b) * H + h) * ngroups + grp) * 2;
-          ml[0] = m;
-          ml[1] = l;
+        if (tvalid) {
+          a.pw[(static_cast<int64_t>(w.b) * H + h) * prow + j] = __bfloat16_as_ushort(pb);
+          if (lane == 0) a.grp_m[(static_cast<int64_t>(w.b) * H + h) * ngroups + grp] = m;
         }
       }
       walk_advance(w, a);
@@ -610,8 +607,8 @@ struct alignas(16) MiscValue {
   uint32_t tmem_base;
   int abort;
   int start_b, start_t, count, total_tiles;
-  float mrun[2][kMax2dHeads], lrun[2][kMax2dHeads];   // per run parity: M and l of each head
-  float pm[8][kMax2dHeads], pl[8][kMax2dHeads];       // partial (M, l) of 8 group subsets
+  float mrun[2][kMax2dHeads];    // per run parity: M of each head
+  float pm[8][kMax2dHeads];      // partial maxima of 8 group subsets
   int scan[kValue2dThreads];
 };
 static_assert(sizeof(MiscValue) <= 4096, "value misc region");
@@ -632,9 +629,10 @@ struct TileWalker {
 };
 
 // D_v of every head over runs of 128-token tiles (Appendix J):
-//   D[r][h] = sum_j 2^(m_g(j) - M) p_j,h c_v,j[r],   l[h] = sum_g 2^(m_g - M) l_g,
+//   D[r][h] = sum_j w_j,h c_v,j[r],   l[h] = sum_j w_j,h,   w_j,h = 2^(m_g(j) - M) p_j,h,
 // over the 32-token groups g of the run, with M the largest m_g (all of them
-// integers, so each scale is an exact power of two).  One record (M, l, D) per (sequence, CTA).  Roles: warp 0
+// integers, so each scale is an exact power of two and w is the bf16 weight the
+// MMA reads).  One record (M, l, D) per (sequence, CTA).  Roles: warp 0
 // copies (V tile + weight tile per ring stage), warp 1 issues the MMAs (M = 128
 // rows of r_v, N = 16 heads, K = 16 tokens), warps 2-5 scale each weight tile,
 // zero V rows past the sequence end, and write the records.
@@ -777,6 +775,7 @@ decode2d_value_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
     // chunk ft & 7 as stored holds logical chunk (ft & 7) ^ (row & 7) (128-byte swizzle)
     const int hs = ft >> 3, piece = (ft & 7) ^ (hs & 7);
     const int64_t ngroups = a.ntiles * 4;
+    float lsum = 0.f;   // this thread's share of the run's l of head hs
     TileWalker w = start;
     RingPos r;
     bool ok = true;
@@ -786,36 +785,25 @@ decode2d_value_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
       const bool run_end = i == count - 1 || w.t == w.nt - 1;
       const int par = run & 1;
       if (run_start) {
-        // the run: tiles [w.t, te) of sequence w.b; its M and l per head, from 8
-        // partial merges of the groups' (m, l) (groups past the sequence end hold
-        // m = -inf and are skipped)
+        // the run: tiles [w.t, te) of sequence w.b; its M per head, the largest m of
+        // its groups (groups past the sequence end hold -inf)
         const int te = min(w.nt, w.t + (count - i));
         const int h = ft & 15, sub = ft >> 4;
-        float M = -INFINITY, l = 0.f;
+        float M = -INFINITY;
         if (h < H) {
-          const float* ml = a.grp_ml + (static_cast<int64_t>(w.b) * H + h) * ngroups * 2;
-          for (int gi = 4 * w.t + sub; gi < 4 * te; gi += 8) {
-            const float m = ml[2 * gi], lg = ml[2 * gi + 1];
-            if (m == -INFINITY) continue;
-            if (m > M) { l = l * exp2f(M - m) + lg; M = m; }
-            else l += lg * exp2f(m - M);
-          }
+          const float* gm = a.grp_m + (static_cast<int64_t>(w.b) * H + h) * ngroups;
+          for (int gi = 4 * w.t + sub; gi < 4 * te; gi += 8) M = fmaxf(M, gm[gi]);
         }
         misc->pm[sub][h] = M;
-        misc->pl[sub][h] = l;
         grp_sync();
         if (ft < H) {
           float Mr = misc->pm[0][ft];
 #pragma unroll
           for (int u = 1; u < 8; ++u) Mr = fmaxf(Mr, misc->pm[u][ft]);
-          float lr = 0.f;
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (misc->pm[u][ft] != -INFINITY) lr += misc->pl[u][ft] * exp2f(misc->pm[u][ft] - Mr);
           misc->mrun[par][ft] = Mr;
-          misc->lrun[par][ft] = lr;
         }
         grp_sync();
+        lsum = 0.f;
       }
       // 2^(m_g - M_run), an exact power of two, for the group of each of this
       // thread's two pieces (tokens 64 kb + 8 piece ...)
@@ -824,7 +812,7 @@ decode2d_value_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
           const int64_t gi = 4 * static_cast<int64_t>(w.t) + 2 * kb + (piece >> 2);
-          const float m = a.grp_ml[((static_cast<int64_t>(w.b) * H + hs) * ngroups + gi) * 2];
+          const float m = a.grp_m[(static_cast<int64_t>(w.b) * H + hs) * ngroups + gi];
           const float Mr = misc->mrun[par][hs];
           if (m != -INFINITY && Mr != -INFINITY) {
             const int e = static_cast<int>(m - Mr);
@@ -847,7 +835,10 @@ decode2d_value_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[c]));
-              u[c] = bf16x2_bits(__floats2bfloat162_rn(f.x * sc[kb], f.y * sc[kb]));
+              const __nv_bfloat162 wv = __floats2bfloat162_rn(f.x * sc[kb], f.y * sc[kb]);
+              const float2 wf = __bfloat1622float2(wv);
+              lsum += wf.x + wf.y;
+              u[c] = bf16x2_bits(wv);
             }
             *pp = v;
           }
@@ -891,9 +882,14 @@ decode2d_value_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(misc->dempty[db]));
-        if (ft < H) {
-          a.rec_ml[(rec * H + ft) * 2] = misc->mrun[par][ft];
-          a.rec_ml[(rec * H + ft) * 2 + 1] = misc->lrun[par][ft];
+        // l: the sum over the 8 threads (lanes) of each head row
+        float l = lsum;
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        if ((ft & 7) == 0 && hs < H) {
+          a.rec_ml[(rec * H + hs) * 2] = misc->mrun[par][hs];
+          a.rec_ml[(rec * H + hs) * 2 + 1] = l;
         }
         ++run;
       }

@@ -240,9 +240,8 @@ struct Decode2dArgs {
   int64_t trig_rows;                 // positions of trigT: L_max rounded up to a whole block
   uint16_t* pw;                      // softmax weights, bf16 [B][H][ntiles * 128], each 32-token group
                                      // relative to 2^m of that group
-  float* grp_ml;                     // [B][H][ntiles * 4][2]: m of each 32-token group (an integer in
-                                     // log2 units, -inf for a group past the sequence end) and the sum
-                                     // of its bf16 weights
+  float* grp_m;                      // [B][H][ntiles * 4]: m of each 32-token group (an integer in
+                                     // log2 units, -inf for a group past the sequence end)
   Decode2dPlan plan;
 };
 
