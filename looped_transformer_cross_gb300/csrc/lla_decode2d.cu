@@ -278,6 +278,32 @@ __device__ void share_of(const Decode2dArgs& a, CountOf count_of, long long part
   __syncthreads();
 }
 
+// Warp-collective wait in which every lane polls (no suspend hint, no broadcast
+// from one lane afterwards): the epilogue's per-stage wait is on its critical path.
+// Bounded like mbar_wait.
+__device__ __forceinline__ bool warp_poll(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint32_t* status) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (__all_sync(0xffffffffu, done != 0)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        record_status(status, LLA_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Spinning form of the bounded wait (no suspend hint): for the issuer, whose every
 // wait is on the critical path of the tensor pipe.  Its barriers are its own CTA's:
 // the copies of both CTAs complete on them, and the score-buffer releases carry no
@@ -542,7 +568,7 @@ decode2d_score_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
 #pragma unroll 1
       for (int p = 0; p < HP; ++p, ++G) {
         const uint32_t buf = G & 1u;
-        if (ok) ok = warp_wait(bar(misc->ufull[buf]), (G >> 1) & 1u, abort, a.status);
+        if (ok) ok = warp_poll(bar(misc->ufull[buf]), (G >> 1) & 1u, abort, a.status);
         bool released = false;
         float part[2] = {0.f, 0.f};   // this group's half of head 2p, 2p + 1
         if (ok) {
@@ -912,11 +938,11 @@ decode2d_value_kernel(const __grid_constant__ Decode2dArgs a, const __grid_const
 // A sequence's records come from the value CTAs whose tile ranges overlap it.  Block = (head h, two consecutive sequences); W_up,v,t,h is
 // staged in shared memory (rows padded by one word) before the wait for the
 // decode grid.
-constexpr int kCombineUnits = 2;
+constexpr int kCombineUnits = 16;   // sequences per block (W_up,v,t,h staged once for all)
 constexpr int kCombineThreads = 128;
 
 size_t combine_smem_bytes(int r_v) {
-  return (static_cast<size_t>(128) * (r_v / 2 + 1) + kCombineUnits * 256 + 2 * kCombineUnits) * 4;
+  return (static_cast<size_t>(128) * (r_v / 2 + 1) + kCombineUnits * 256 + 3 * kCombineUnits) * 4;
 }
 
 __global__ void __launch_bounds__(kCombineThreads) decode2d_combine_kernel(const __grid_constant__ Decode2dArgs a) {
@@ -929,6 +955,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode2d_combine_kernel(const
   float* accs = csm + 128 * wpr;   // [kCombineUnits][256]
   float* Ms = accs + kCombineUnits * 256;
   float* Ls = Ms + kCombineUnits;
+  int* Tp = reinterpret_cast<int*>(Ls + kCombineUnits);   // tiles of the block's sequences before each
   {
     const uint4* Wg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w_up_v) +
                                                      static_cast<int64_t>(h) * kHeadDim * a.r_v);
@@ -970,46 +997,51 @@ __global__ void __launch_bounds__(kCombineThreads) decode2d_combine_kernel(const
 #pragma unroll
   for (int w = 0; w < kCombineThreads / 32; ++w) tot += red[w];
 
+  if (tid == 0) {
+    int t = 0;
+    for (int u = 0; u < kCombineUnits; ++u) {
+      Tp[u] = t;
+      if (b0 + u < a.B) t += ntiles_of(clamp_len(__ldg(a.seq_lens + b0 + u), a.L_max));
+    }
+  }
+  __syncthreads();
+
   asm volatile("griddepcontrol.wait;" ::: "memory");   // records written
 
-  float M = -INFINITY, Lt = 0.f;
-  float acc[8];
+  // warp w merges the records of sequences b0 + w, b0 + w + 4, ...
+  for (int u = warp; u < kCombineUnits; u += kCombineThreads / 32) {
+    const int b = b0 + u;
+    float M = -INFINITY, Lt = 0.f;
+    float acc[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-  const int b = b0 + warp;
-  if (warp < kCombineUnits && b < a.B) {
-    long long B0 = pre;
-    for (int bb = b0; bb < b; ++bb) B0 += ntiles_of(clamp_len(__ldg(a.seq_lens + bb), a.L_max));
-    const int nb = ntiles_of(clamp_len(__ldg(a.seq_lens + b), a.L_max));
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    const int nb = b < a.B ? ntiles_of(clamp_len(__ldg(a.seq_lens + b), a.L_max)) : 0;
     if (nb > 0) {
+      const long long B0 = pre + Tp[u];
       const long long NB = tot, NP = a.units;
       const long long p0 = ((B0 + 1) * NP - 1) / NB, p1 = ((B0 + nb) * NP - 1) / NB;
       for (long long p = p0; p <= p1; ++p) {
         const long long lo = p * NB / NP, hi = (p + 1) * NB / NP;
         if (max(lo, B0) >= min(hi, B0 + nb)) continue;   // the value CTA saw no tile of b
-        {
-          const long long rec = b + p;
-          const float mr = a.rec_ml[(rec * a.H + h) * 2], lr = a.rec_ml[(rec * a.H + h) * 2 + 1];
-          const float* ar = a.rec_acc + (rec * a.H + h) * a.r_v;
-          float x[8];
+        const long long rec = b + p;
+        const float mr = a.rec_ml[(rec * a.H + h) * 2], lr = a.rec_ml[(rec * a.H + h) * 2 + 1];
+        const float* ar = a.rec_acc + (rec * a.H + h) * a.r_v;
+        float x[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) x[j] = lane + 32 * j < a.r_v ? ar[lane + 32 * j] : 0.f;
-          if (mr == -INFINITY) continue;
-          const float Mn = fmaxf(M, mr);
-          const float alpha = M == -INFINITY ? 0.f : exp2f(M - Mn), wr = exp2f(mr - Mn);
-          Lt = fmaf(lr, wr, Lt * alpha);
+        for (int j = 0; j < 8; ++j) x[j] = lane + 32 * j < a.r_v ? ar[lane + 32 * j] : 0.f;
+        if (mr == -INFINITY) continue;
+        const float Mn = fmaxf(M, mr);
+        const float alpha = M == -INFINITY ? 0.f : exp2f(M - Mn), wr = exp2f(mr - Mn);
+        Lt = fmaf(lr, wr, Lt * alpha);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[j], wr, acc[j] * alpha);
-          M = Mn;
-        }
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[j], wr, acc[j] * alpha);
+        M = Mn;
       }
     }
-  }
-  if (warp < kCombineUnits) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (lane + 32 * j < a.r_v) accs[warp * 256 + lane + 32 * j] = acc[j];
-    if (lane == 0) { Ms[warp] = M; Ls[warp] = Lt; }
+      if (lane + 32 * j < a.r_v) accs[u * 256 + lane + 32 * j] = acc[j];
+    if (lane == 0) { Ms[u] = M; Ls[u] = Lt; }
   }
   __syncthreads();
 
