@@ -48,9 +48,9 @@ TRAFFIC_PER_TOKEN_HEAD = {4096: (263.966208e6 + 3.191552e6) / (31042 * 16),
                           16384: (1080.890368e6 + 3.592704e6) / (8 * 16384 * 16)}
 TRAFFIC_SRC_SHA = "45b84bcebf40e291"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
-# The same for the LLA-2D kernel, per latent token (all heads), from the 32-sequence
-# variant of the LLA-2D layer; valid only for the source whose sha256 starts with
-# TRAFFIC2D_SRC_SHA.
+# The same for the LLA-2D score kernel (the dominant one of the LLA-2D call), per
+# latent token (all heads), from the 32-sequence variant of the LLA-2D layer; valid
+# only for the source whose sha256 starts with TRAFFIC2D_SRC_SHA.
 TRAFFIC2D_PER_TOKEN = (224.002816e6 + 4.921088e6) / (32 * 8192)
 TRAFFIC2D_SRC_SHA = "82da47c747901f36"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
@@ -601,9 +601,9 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
             same_src = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC2D_SRC_SHA)
         traffic = TRAFFIC2D_PER_TOKEN * step.tokens if same_src else None
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
-                "frac": achieved / tflops, "traffic": traffic, "traffic_kernel": "decode2d_bf16_kernel",
-                "kernel": "lla_decode_attn (decode2d_z_kernel + decode2d_bf16_kernel + "
-                          "decode2d_combine_kernel)",
+                "frac": achieved / tflops, "traffic": traffic, "traffic_kernel": "decode2d_score_kernel",
+                "kernel": "lla_decode_attn (decode2d_z_kernel + decode2d_score_kernel + "
+                          "decode2d_value_kernel + decode2d_combine_kernel)",
                 "algorithmic_flops_per_launch": flops,
                 "latent_bytes_per_launch": step.tokens * (w.r_k + w.r_v) * 2,
                 "launch_ms": t_call * 1e3, "peak_source": src + " (bf16 sustained)"}

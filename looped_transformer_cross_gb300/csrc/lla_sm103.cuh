@@ -130,12 +130,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Warp-collective form: lane 0 alone polls (polls from every lane would crowd
-// the shared-memory pipe that tcgen05 and TMA traffic also use), then the warp
-// synchronises, which orders lane 0's acquire of the phase before every lane's
-// later reads, and all lanes leave converged with lane 0's decision.
+// Warp-collective form.  Every lane first tests the phase once: a phase that has
+// already completed (the common case on a pipeline that keeps up) costs one test
+// and one vote, and each lane has made its own acquire.  Otherwise lane 0 alone
+// waits (polls from every lane would crowd the shared-memory pipe that tcgen05 and
+// TMA traffic also use), then the warp synchronises, which orders lane 0's acquire
+// of the phase before every lane's later reads, and all lanes leave converged with
+// lane 0's decision.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status);
   __syncwarp();
