@@ -445,7 +445,10 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     // ======================================================== score-MMA issuer
     // U[i & 1] = C_k(i) Z^T (+ bias).  The columns of U[i & 1] last held P(i-2),
     // the A operand of value MMA i-2 (issued by warp 6), so K(i) waits for it.
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform descriptors); one elected lane
+    // issues, and every lane polls the barriers (the vote keeps the decision uniform).
+    {
+      auto agree = [](bool r) { return __all_sync(0xffffffffu, r); };
       const uint32_t idesc_k = umma_idesc_bf16(128, 128, false, false);
       const uint64_t daa = umma_desc(sbase + P.aug_a, 16, 256, kSw32);
       const uint32_t kst = static_cast<uint32_t>(P.k_stage) >> 4;
@@ -455,11 +458,11 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       for (int i = 0; i < count; ++i, kr.next(P.SK)) {
         if (i == 0 || w.t == 0) {
           if (++unit > 0) zr.next(P.NZ);
-          if (!mbar_wait(bar(misc->zfull[zr.slot]), zr.phase, abort, a.status)) break;
+          if (!agree(mbar_wait(bar(misc->zfull[zr.slot]), zr.phase, abort, a.status))) break;
         }
         const int sk = kr.slot, ub = i & 1, zb = zr.slot;
-        if (!mbar_wait(bar(misc->kfull[sk]), kr.phase, abort, a.status)) break;
-        if (i >= 2 && !mbar_wait(bar(misc->vdone[ub]), ((i - 2) >> 1) & 1, abort, a.status)) break;
+        if (!agree(mbar_wait(bar(misc->kfull[sk]), kr.phase, abort, a.status))) break;
+        if (i >= 2 && !agree(mbar_wait(bar(misc->vdone[ub]), ((i - 2) >> 1) & 1, abort, a.status))) break;
         tc_fence_after();
         const uint32_t d = tmem + ub * 128;
         const uint32_t so = sk * kst;
@@ -471,18 +474,18 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           const uint64_t a0 = umma_desc(k_ring + P.kplan.off[c], 16, 8 * rb, lay) + so;
           const uint64_t b0 = umma_desc(zreg + P.kplan.off[c], 16, 8 * rb, lay);
           for (int k = 0; k < P.kplan.width[c] / 16; ++k) {
-            umma_bf16(d, a0 + 2 * k, b0 + 2 * k, idesc_k, acc);
+            umma_bf16_warp(d, a0 + 2 * k, b0 + 2 * k, idesc_k, acc);
             acc = 1;
           }
         }
-        umma_bf16(d, daa, umma_desc(sbase + P.aug_b + zb * 4096, 16, 256, kSw32), idesc_k, 1);
-        umma_commit(bar(misc->kempty[sk]));
-        umma_commit(bar(misc->ufull[ub]));
-        if (w.t == w.nb - 1) umma_commit(bar(misc->zfree[zb]));   // unit's Z no longer read
+        umma_bf16_warp(d, daa, umma_desc(sbase + P.aug_b + zb * 4096, 16, 256, kSw32), idesc_k, 1);
+        umma_commit_warp(bar(misc->kempty[sk]));
+        umma_commit_warp(bar(misc->ufull[ub]));
+        if (w.t == w.nb - 1) umma_commit_warp(bar(misc->zfree[zb]));   // unit's Z no longer read
         walker_advance(w, a);
       }
-      // this thread's MMAs complete before TMEM is released
-      umma_commit(bar(misc->mma_done[0]));
+      // this warp's MMAs complete before TMEM is released
+      umma_commit_warp(bar(misc->mma_done[0]));
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar(misc->mma_done[0]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
@@ -490,8 +493,9 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
     // ======================================================== value-MMA issuer
     // D += P(j) C_v(j): P(j) from TMEM (written by the epilogue over U[j & 1]), the
     // V tile as the MN-major B operand.  The accumulator is never cleared by an
-    // MMA: the epilogue zeroes it when a unit starts.
-    if (lane == 0) {
+    // MMA: the epilogue zeroes it when a unit starts.  Whole warp, as above.
+    {
+      auto agree = [](bool r) { return __all_sync(0xffffffffu, r); };
       const uint32_t idesc_v = umma_idesc_bf16(128, a.r_v, false, true);
       // 32-column chunks 8 KB apart (LBO), 8 token rows 512 B apart (SBO); a
       // 16-token K step is +1 KB (+64 in the address field)
@@ -501,31 +505,32 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
       RingPos vr;
       for (int j = 0; j < count; ++j, vr.next(P.SV)) {
         const int sv = vr.slot, jb = j & 1;
-        if (!mbar_wait(bar(misc->vfull[sv]), vr.phase, abort, a.status)) break;
-        if (!mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status)) break;
+        if (!agree(mbar_wait(bar(misc->vfull[sv]), vr.phase, abort, a.status))) break;
+        if (!agree(mbar_wait(bar(misc->pfull[jb]), (j >> 1) & 1, abort, a.status))) break;
         // rows past the sequence end: skip whole 16-token steps, zero the rest of a
         // partial step (they may hold anything; their weights are 0 and 0 * x stays 0)
         const int valid = wv.L - wv.t * kTile;
         const int steps = valid >= kTile ? kTile / 16 : (valid + 15) / 16;
         if (valid < steps * 16) {
           uint8_t* vs = sm + P.v_ring + sv * P.v_stage;
-          for (int c = 0; c < P.vplan.n; ++c)
-            for (int r = valid; r < steps * 16; ++r)
-#pragma unroll
-              for (int g = 0; g < 4; ++g)
-                *reinterpret_cast<uint4*>(vs + P.vplan.off[c] + swizzle_offset(r * 64 + g * 16, 64)) =
-                    make_uint4(0, 0, 0, 0);
+          const int per_c = (steps * 16 - valid) * 4;
+          for (int x = lane; x < P.vplan.n * per_c; x += 32) {
+            const int c = x / per_c, r = valid + (x - c * per_c) / 4, g = x & 3;
+            *reinterpret_cast<uint4*>(vs + P.vplan.off[c] + swizzle_offset(r * 64 + g * 16, 64)) =
+                make_uint4(0, 0, 0, 0);
+          }
           fence_proxy_async_smem();
+          __syncwarp();
         }
         tc_fence_after();
         const uint64_t b0 = dv0 + sv * vst;
         const uint32_t pa = tmem + jb * 128;
-        for (int k = 0; k < steps; ++k) umma_bf16_ts(tmem + kDCol, pa + 8 * k, b0 + 64 * k, idesc_v, 1u);
-        umma_commit(bar(misc->vempty[sv]));
-        umma_commit(bar(misc->vdone[jb]));
+        for (int k = 0; k < steps; ++k) umma_bf16_ts_warp(tmem + kDCol, pa + 8 * k, b0 + 64 * k, idesc_v, 1u);
+        umma_commit_warp(bar(misc->vempty[sv]));
+        umma_commit_warp(bar(misc->vdone[jb]));
         walker_advance(wv, a);
       }
-      umma_commit(bar(misc->mma_done[1]));
+      umma_commit_warp(bar(misc->mma_done[1]));
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar(misc->mma_done[1]), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
