@@ -436,7 +436,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
     // Per position and head set: G = R_tile [set image], A = the position's RoPE
     // rows in TMEM (K-major f16, 8 columns per 16 coordinates), B = the set image
     // (K-major, 128B swizzle, two chunks of 64 coordinates), D = the next G buffer.
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform descriptors); one elected lane
+    // issues, every lane polls the barriers and the vote keeps the decision uniform.
+    {
+      auto agree = [](bool r) { return __all_sync(0xffffffffu, r); };
       const uint32_t idesc = umma_idesc_f16(128, P.N);
       const uint32_t chunk = static_cast<uint32_t>(P.N) * 128;
       PosWalker w = start;
@@ -447,10 +450,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
         const bool run_start = lp == 0 || w.t == 0;
         const bool run_end = lp == count - 1 || w.t == w.nb - 1;
         const uint32_t tb = lp & 1;
-        if (!(ok = mbar_wait(bar(misc->trig_full[tb]), (lp >> 1) & 1, abort, a.status))) break;
+        if (!(ok = agree(mbar_wait(bar(misc->trig_full[tb]), (lp >> 1) & 1, abort, a.status)))) break;
         for (int s = 0; s < nsets; ++s) {
-          if (run_start && !(ok = mbar_wait(bar(misc->img_full[s]), run & 1, abort, a.status))) break;
-          if (!(ok = mbar_wait(bar(misc->gempty[gp.slot]), gp.phase ^ 1u, abort, a.status))) break;
+          if (run_start && !(ok = agree(mbar_wait(bar(misc->img_full[s]), run & 1, abort, a.status)))) break;
+          if (!(ok = agree(mbar_wait(bar(misc->gempty[gp.slot]), gp.phase ^ 1u, abort, a.status)))) break;
           tc_fence_after();
           const uint32_t d = tmem + kGCol + gp.slot * P.N;
           const uint32_t at = tmem + kTrigCol + tb * 64;
@@ -458,17 +461,17 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t bd = umma_desc(ib + (kk >> 2) * chunk, 16, 1024, kSw128) + 2 * (kk & 3);
-            umma_bf16_ts(d, at + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
+            umma_bf16_ts_warp(d, at + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(misc->gfull[gp.slot]));
-          if (run_end) umma_commit(bar(misc->img_empty[s]));   // the set image is no longer read
+          umma_commit_warp(bar(misc->gfull[gp.slot]));
+          if (run_end) umma_commit_warp(bar(misc->img_empty[s]));   // the set image is no longer read
           gp.next(1, P.NG);
         }
         if (run_start) ++run;
         pos_advance(w, a);
       }
-      // this thread's MMAs complete before TMEM is released
-      umma_commit(bar(misc->mma_done));
+      // this warp's MMAs complete before TMEM is released
+      umma_commit_warp(bar(misc->mma_done));
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }

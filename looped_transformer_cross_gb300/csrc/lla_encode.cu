@@ -165,7 +165,10 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform descriptors); one elected lane
+    // issues, every lane polls the barriers and the vote keeps the decision uniform.
+    {
+      auto agree = [](bool r) { return __all_sync(0xffffffffu, r); };
       // MMA runs of each axis: all 64-wide W chunks in one MMA (N up to 256), then the
       // 32- and 16-wide chunk alone.  Descriptors are built once, for ring stage 0; a
       // stage and a k-step only add offsets (building a descriptor per MMA made the
@@ -214,12 +217,12 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
         }
         const int ab = acc_buf(j);
         // the epilogue has read this accumulator's previous unit out of TMEM
-        if (!(ok = mbar_wait(bar(misc->dempty[ab]), (acc_use(j) & 1) ^ 1, abort, a.status))) break;
+        if (!(ok = agree(mbar_wait(bar(misc->dempty[ab]), (acc_use(j) & 1) ^ 1, abort, a.status)))) break;
         tc_fence_after();
         const uint32_t acc = tmem + static_cast<uint32_t>(ab * P.acc_stride);
         uint32_t s = g % S;
         for (int kb = 0; kb < KB; ++kb, ++g) {
-          if (!(ok = mbar_wait(bar(misc->full[s]), (g / S) & 1, abort, a.status))) break;
+          if (!(ok = agree(mbar_wait(bar(misc->full[s]), (g / S) & 1, abort, a.status)))) break;
           tc_fence_after();
           const uint32_t so = s * stage16;
 #pragma unroll
@@ -227,17 +230,17 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
 #pragma unroll
             for (int r = 0; r < 3; ++r)
               if (r < nr)
-                umma_bf16(acc + col[r], adesc + so + 2 * k, bdesc[r] + so + k * kstep[r], idesc[r],
-                          (kb > 0 || k > 0) ? 1u : 0u);
+                umma_bf16_warp(acc + col[r], adesc + so + 2 * k, bdesc[r] + so + k * kstep[r], idesc[r],
+                               (kb > 0 || k > 0) ? 1u : 0u);
           }
-          umma_commit(bar(misc->empty[s]));
+          umma_commit_warp(bar(misc->empty[s]));
           s = s + 1 == S ? 0 : s + 1;
         }
-        if (ok) umma_commit(bar(misc->dfull[ab]));
+        if (ok) umma_commit_warp(bar(misc->dfull[ab]));
       }
-      // every MMA this thread issued is complete before TMEM is released
+      // every MMA this warp issued is complete before TMEM is released
       if (g > 0) {
-        umma_commit(bar(misc->mdone));
+        umma_commit_warp(bar(misc->mdone));
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(bar(misc->mdone), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
