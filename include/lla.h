@@ -41,8 +41,9 @@
  *   never completes; the wait expires after about one second and the call's
  *   status becomes LLA_ERR_TIMEOUT (outputs undefined).  Zero the word to
  *   resume normal calls.
- * - Constraints: d_head == 128; r_k and r_v multiples of 16 in [16, 256];
- *   T >= 1; H >= 1.  Other shapes return LLA_ERR_UNSUPPORTED.
+ * - Constraints: d_head == 128; r_k and r_v multiples of 16 in [16, 256]
+ *   (LLA_PER_HEAD) or [16, 512] (LLA_2D, one latent per token, "The LLA-2D
+ *   variant"); T >= 1; H >= 1.  Other shapes return LLA_ERR_UNSUPPORTED.
  */
 #ifndef LLA_H
 #define LLA_H
@@ -327,7 +328,11 @@ lla_status lla_decode_attn_noalloc(const lla_dims* dims, int loop_t, const void*
                                    float* out, float* lse, void* stream);
 
 /* Name of the kernel family lla_decode_attn runs for `dims` (host-only, no
- * launch): "fp32" (LLA_F32), "pair-2d" (LLA_2D bf16: CTA pairs), "small-rank"
+ * launch): "fp32" (LLA_F32), "pair-2d" (LLA_2D bf16 with an even H <= 16,
+ * r_k <= 128 and r_v <= 256: CTA-pair score kernel on the tensor cores, then a
+ * tensor-core value kernel), "plain-2d" (every other LLA_2D bf16 shape: the
+ * plain per-(sequence, head) kernels in fp32 arithmetic over the bf16 storage;
+ * correct, not tuned), "small-rank"
  * (LLA_PER_HEAD bf16 with r_k in {16, 32}, r_v in {32, 64} and an even H <= 16
  * whose H query images and a 4-slot latent ring fit in shared memory:
  * positions split over CTAs, RoPE applied by the tensor cores), "tile"

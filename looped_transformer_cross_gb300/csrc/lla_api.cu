@@ -90,9 +90,13 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
     const size_t nrec = static_cast<size_t>(2) * (static_cast<size_t>(B) + kMaxPairs);
     w.partials = off; off += al256(nrec * d->H * d->r_v * 4);
     w.rec_ml = off;   off += al256(nrec * d->H * 2 * 4);
-    w.bias = off;     off += al256(static_cast<size_t>(2) * 256 * 4);
+    w.bias = off;     off += al256(static_cast<size_t>(2) * kMaxRank2d * 4);
+    // fp32 scores of the plain kernels (fp32 storage, and bf16 shapes the CTA-pair
+    // kernels do not take)
     w.scores = off;
-    if (d->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * d->H * L_max * 4);
+    Decode2dPlan pp;
+    if (d->dtype == LLA_F32 || !make_decode2d_plan(d->H, d->r_k, d->r_v, &pp))
+      off += al256(static_cast<size_t>(B) * d->H * L_max * 4);
     w.zimg = off;
     if (d->dtype == LLA_BF16 && d->r_k <= 128) {
       w.zimg_stride = decode2d_zimg_stride(d->H, d->r_k);
@@ -120,7 +124,7 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
     w.partials = off;
     off += al256((static_cast<size_t>(B) + std::min<size_t>(kMaxGrid, std::max<size_t>(1, max_pos))) * d->H *
                  kRecordsPerCta * (d->r_v + kRecordHead) * 4);
-    w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
+    w.bias = off; off += al256(static_cast<size_t>(2) * d->H * kMaxRank2d * 4);
     w.scores = off;
     w.zimg = off;
     // one image per (sequence, head set) of 4 heads (2 when H mod 4 = 2)
@@ -132,7 +136,7 @@ WsLayout ws_layout(const lla_dims* d, int B, int64_t L_max) {
     return w;
   }
   w.partials = off; off += al256((static_cast<size_t>(B) * d->H + kMaxGrid) * kRecordsPerCta * (d->r_v + kRecordHead) * 4);
-  w.bias = off; off += al256(static_cast<size_t>(2) * d->H * 256 * 4);
+  w.bias = off; off += al256(static_cast<size_t>(2) * d->H * kMaxRank2d * 4);
   w.scores = off;
   if (d->dtype == LLA_F32) off += al256(static_cast<size_t>(B) * d->H * L_max * 4);
   w.zimg = off;
@@ -150,7 +154,8 @@ lla_status check_dims(const lla_dims* d) {
   if (d->rope_style != LLA_ROPE_HALF && d->rope_style != LLA_ROPE_INTERLEAVED) return LLA_ERR_INVALID_ARG;
   if (!(d->rope_base > 0.f) || !std::isfinite(d->rope_base)) return LLA_ERR_INVALID_ARG;
   if (d->d_head != kHeadDim) return LLA_ERR_UNSUPPORTED;
-  if (d->r_k % 16 || d->r_v % 16 || d->r_k > 256 || d->r_v > 256) return LLA_ERR_UNSUPPORTED;
+  const int rmax = d->variant == LLA_2D ? kMaxRank2d : kMaxRankPerHead;
+  if (d->r_k % 16 || d->r_v % 16 || d->r_k > rmax || d->r_v > rmax) return LLA_ERR_UNSUPPORTED;
   return LLA_OK;
 }
 
@@ -185,7 +190,7 @@ const char* lla_decode_kernel(const lla_dims* dims) {
   if (dims->dtype == LLA_F32) return "fp32";
   if (dims->variant == LLA_2D) {
     Decode2dPlan p;
-    return make_decode2d_plan(dims->H, dims->r_k, dims->r_v, &p) ? "pair-2d" : nullptr;
+    return make_decode2d_plan(dims->H, dims->r_k, dims->r_v, &p) ? "pair-2d" : "plain-2d";
   }
   if (small_path(dims)) return "small-rank";
   DecodePlan p;
@@ -288,11 +293,14 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   // every host check has passed: zero the status word first when asked to (the
   // entry point without a workspace), then launch
   auto ready = [&]() { return !clear_status || cudaMemsetAsync(ws, 0, 256, s) == cudaSuccess; };
-  if (dims->variant == LLA_2D && dims->dtype == LLA_BF16) {
+  Decode2dPlan plan2d;
+  const bool pair2d = dims->variant == LLA_2D && dims->dtype == LLA_BF16 &&
+                      make_decode2d_plan(H, dims->r_k, dims->r_v, &plan2d);
+  if (pair2d) {
     // LLA-2D: one latent per token shared by the H heads (CTA-pair score kernel,
     // value kernel)
     Decode2dArgs a{};
-    if (!make_decode2d_plan(H, dims->r_k, dims->r_v, &a.plan)) return LLA_ERR_UNSUPPORTED;
+    a.plan = plan2d;
     a.B = cache.B;
     a.H = H;
     a.r_k = dims->r_k;
@@ -389,6 +397,12 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   if (dims->dtype == LLA_F32) {
     if (!ready()) return LLA_ERR_CUDA;
     return launch_decode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  }
+  if (dims->variant == LLA_2D) {
+    // LLA-2D shapes outside the CTA-pair kernels' range: the plain kernels over bf16
+    if (cache.bt) return LLA_ERR_UNSUPPORTED;
+    if (!ready()) return LLA_ERR_CUDA;
+    return launch_decode_plain_bf16(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   }
 
   const int sms = sm_count();

@@ -902,8 +902,14 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
 
 // ------------------------------------------------------------------ fp32 path
 
+// Element loads of the plain path: fp32 storage, or bf16 storage widened to fp32
+// (the LLA-2D shapes the CTA-pair kernels do not take).
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
 // Scores s_j = RoPE(q).RoPE(k_j)/sqrt(d), k_j reconstructed per Eq. (3) in fp32.
 // Block = (unit, 128-token tile); thread = token.
+template <typename T>
 __global__ void __launch_bounds__(128)
 decode_f32_scores_kernel(const __grid_constant__ DecodeArgs a) {
   __shared__ float qrot[kHeadDim];
@@ -919,18 +925,19 @@ decode_f32_scores_kernel(const __grid_constant__ DecodeArgs a) {
     if (tid == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
     qp = qp < 0 ? 0 : static_cast<int>(a.rope_len - 1);
   }
-  const float* qv = static_cast<const float*>(a.q) + static_cast<int64_t>(u) * kHeadDim;
+  const T* qv = static_cast<const T*>(a.q) + static_cast<int64_t>(u) * kHeadDim;
   if (tid < 64) {
     const int f = tid;
     const int i0 = a.rope_style == 0 ? f : 2 * f, i1 = a.rope_style == 0 ? f + 64 : 2 * f + 1;
     const float c = a.rope_cos[static_cast<int64_t>(qp) * 64 + f], s = a.rope_sin[static_cast<int64_t>(qp) * 64 + f];
-    qrot[i0] = qv[i0] * c - qv[i1] * s;
-    qrot[i1] = qv[i0] * s + qv[i1] * c;
+    const float x0 = ldf(qv + i0), x1 = ldf(qv + i1);
+    qrot[i0] = x0 * c - x1 * s;
+    qrot[i1] = x0 * s + x1 * c;
   }
   // token rows j0.. of the unit (paged: possibly across pages; LLA-2D: every head
   // reads the sequence's latent); rows past L are not read
-  const float* C = static_cast<const float*>(a.cache_k);
-  const float* W = static_cast<const float*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
+  const T* C = static_cast<const T*>(a.cache_k);
+  const T* W = static_cast<const T*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * a.r_k;
   const int rows = min(kTile, L - j0);
   float kh[kHeadDim];
 #pragma unroll
@@ -940,8 +947,8 @@ decode_f32_scores_kernel(const __grid_constant__ DecodeArgs a) {
     __syncthreads();
     for (int idx = tid; idx < kTile * 32; idx += 128) {
       const int r = idx / 32, k = idx % 32;
-      ct[r][k] = (r < rows && k < kw) ? C[f32_row(a, b, h, j0 + r) * a.r_k + k0 + k] : 0.f;
-      wt[r][k] = (k < kw) ? W[static_cast<int64_t>(r) * a.r_k + k0 + k] : 0.f;
+      ct[r][k] = (r < rows && k < kw) ? ldf(C + f32_row(a, b, h, j0 + r) * a.r_k + k0 + k) : 0.f;
+      wt[r][k] = (k < kw) ? ldf(W + static_cast<int64_t>(r) * a.r_k + k0 + k) : 0.f;
     }
     __syncthreads();
     for (int k = 0; k < 32; ++k) {
@@ -978,10 +985,11 @@ __device__ float block_reduce(float v, float* red, bool is_max) {
 }
 
 // Softmax over the unit's scores, then out = (sum_j p_j c_v,j) W_up,v,t^T / Z + mu_v,t.
+template <typename T>
 __global__ void __launch_bounds__(256)
 decode_f32_values_kernel(const __grid_constant__ DecodeArgs a) {
   __shared__ float red[8];
-  __shared__ float accs[256];
+  __shared__ float accs[kMaxRank2d];
   const int u = blockIdx.x, tid = threadIdx.x;
   const int b = u / a.H, h = u % a.H;
   const int L = clamp_len(__ldg(a.seq_lens + b), a.L_max);
@@ -1002,17 +1010,17 @@ decode_f32_values_kernel(const __grid_constant__ DecodeArgs a) {
     z += p;
   }
   z = block_reduce(z, red, false);   // also orders the p writes before the reads below
-  const float* Cv = static_cast<const float*>(a.cache_v);
-  if (tid < a.r_v) {
+  const T* Cv = static_cast<const T*>(a.cache_v);
+  for (int rr = tid; rr < a.r_v; rr += 256) {
     float v = 0.f;
-    for (int j = 0; j < L; ++j) v = fmaf(sc[j], Cv[f32_row(a, b, h, j) * a.r_v + tid], v);
-    accs[tid] = v;
+    for (int j = 0; j < L; ++j) v = fmaf(sc[j], ldf(Cv + f32_row(a, b, h, j) * a.r_v + rr), v);
+    accs[rr] = v;
   }
   __syncthreads();
   if (tid < kHeadDim) {
-    const float* Wv = static_cast<const float*>(a.w_up_v) + (static_cast<int64_t>(h) * kHeadDim + tid) * a.r_v;
+    const T* Wv = static_cast<const T*>(a.w_up_v) + (static_cast<int64_t>(h) * kHeadDim + tid) * a.r_v;
     float o = 0.f;
-    for (int i = 0; i < a.r_v; ++i) o = fmaf(accs[i], Wv[i], o);
+    for (int i = 0; i < a.r_v; ++i) o = fmaf(accs[i], ldf(Wv + i), o);
     out[tid] = o / z + a.mu_v[static_cast<int64_t>(h) * a.mu_hstride + tid];
   }
   if (tid == 0) a.lse[u] = m + logf(z);
@@ -1133,16 +1141,25 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_decode_f32_values(const DecodeArgs& a, cudaStream_t s) {
-  decode_f32_values_kernel<<<a.B * a.H, 256, 0, s>>>(a);
+  decode_f32_values_kernel<float><<<a.B * a.H, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s) {
   const dim3 g1(a.B * a.H, static_cast<unsigned>((a.L_max + kTile - 1) / kTile));
-  decode_f32_scores_kernel<<<g1, 128, 0, s>>>(a);
+  decode_f32_scores_kernel<float><<<g1, 128, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_f32_values_kernel<<<a.B * a.H, 256, 0, s>>>(a);
+  decode_f32_values_kernel<float><<<a.B * a.H, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_plain_bf16(const DecodeArgs& a, cudaStream_t s) {
+  const dim3 g1(a.B * a.H, static_cast<unsigned>((a.L_max + kTile - 1) / kTile));
+  decode_f32_scores_kernel<__nv_bfloat16><<<g1, 128, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_f32_values_kernel<__nv_bfloat16><<<a.B * a.H, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

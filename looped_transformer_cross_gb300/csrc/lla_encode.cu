@@ -29,17 +29,18 @@ struct alignas(16) EncodeMisc {
 };
 
 // bias[axis][h][k] = sum_u mu[h][u] * W_down[h][u][k]  (fp32).  Block = (head,
-// axis): warp w sums rows u = w, w + 8, ...; lane l covers columns 8l..8l+7 with
-// 16-byte loads, sixteen rows in flight; the eight warps' partial sums are added
-// in shared memory.
+// axis, 256-column half): warp w sums rows u = w, w + 8, ...; lane l covers columns
+// 8l..8l+7 of the half with 16-byte loads, sixteen rows in flight; the eight warps'
+// partial sums are added in shared memory.
 __global__ void __launch_bounds__(256) encode_bias_kernel(const __grid_constant__ EncodeArgs a) {
   __shared__ float part[8][256];
-  const int h = blockIdx.x, axis = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, axis = blockIdx.y, k0 = 256 * blockIdx.z, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = axis == 0 ? a.r_k : a.r_v;
+  if (k0 >= r) return;
   const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(axis == 0 ? a.w_down_k : a.w_down_v) +
                            static_cast<int64_t>(h) * a.Td * r;
   const float* mu = (axis == 0 ? a.mu_k : a.mu_v) + static_cast<int64_t>(h) * a.Td;
-  const int k = 8 * lane;
+  const int k = k0 + 8 * lane;
   constexpr int kRows = 16;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (k < r) {
@@ -62,15 +63,15 @@ __global__ void __launch_bounds__(256) encode_bias_kernel(const __grid_constant_
       }
     }
 #pragma unroll
-    for (int t = 0; t < 8; ++t) part[warp][k + t] = acc[t];
+    for (int t = 0; t < 8; ++t) part[warp][8 * lane + t] = acc[t];
   }
   __syncthreads();
   const int t = threadIdx.x;
-  if (t < r) {
+  if (k0 + t < r) {
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) s += part[w][t];
-    a.bias[(static_cast<int64_t>(axis) * a.H + h) * 256 + t] = s;
+    a.bias[(static_cast<int64_t>(axis) * a.H + h) * kMaxRank2d + k0 + t] = s;
   }
 }
 
@@ -94,12 +95,15 @@ __device__ __forceinline__ EncodeUnit encode_unit(int64_t u, int H) {
   return e;
 }
 
+// MMA runs per axis: 64-wide W chunks grouped up to N = 256, then a 32- and a
+// 16-wide chunk (ranks up to 512 need four).
+constexpr int kRuns = 4;
+
 // Persistent: one CTA per SM walks units blockIdx.x, blockIdx.x + gridDim.x, ...
 // The x / W_down ring runs on across units (its position is the count of k-blocks
 // this CTA has issued), and two TMEM accumulators alternate between units, so
-// the epilogue of one unit overlaps the copies and MMAs of the next.  (The plan's
-// one-accumulator mode, for ranks above 256, is never chosen while the host checks
-// cap r_k and r_v at 256.)
+// the epilogue of one unit overlaps the copies and MMAs of the next; ranks above
+// 256 (LLA-2D) use one 512-column accumulator.
 __global__ void __launch_bounds__(kEncodeThreads, 1)
 encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__ EncodePlan P,
                    const __grid_constant__ EncodeMaps maps) {
@@ -173,15 +177,15 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
       // 32- and 16-wide chunk alone.  Descriptors are built once, for ring stage 0; a
       // stage and a k-step only add offsets (building a descriptor per MMA made the
       // issuing thread, not the tensor pipe, set the rate).
-      uint64_t rdesc[2][3];
-      uint32_t ridesc[2][3], rcol[2][3], rkstep[2][3];
+      uint64_t rdesc[2][kRuns];
+      uint32_t ridesc[2][kRuns], rcol[2][kRuns], rkstep[2][kRuns];
       int nrun[2];
 #pragma unroll
       for (int ax = 0; ax < 2; ++ax) {
         const ChunkPlan& bp = ax == 0 ? P.bk : P.bv;
         int c = 0, n = 0;
 #pragma unroll
-        for (int r = 0; r < 3; ++r) {
+        for (int r = 0; r < kRuns; ++r) {
           rdesc[ax][r] = 0; ridesc[ax][r] = 0; rcol[ax][r] = 0; rkstep[ax][r] = 0;
           if (c < bp.n) {
             const int w = bp.width[c];
@@ -206,10 +210,10 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
       for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++j) {
         const EncodeUnit e = encode_unit(u, a.H);
         const int nr = e.axis == 0 ? nrun[0] : nrun[1];
-        uint64_t bdesc[3];
-        uint32_t idesc[3], col[3], kstep[3];
+        uint64_t bdesc[kRuns];
+        uint32_t idesc[kRuns], col[kRuns], kstep[kRuns];
 #pragma unroll
-        for (int r = 0; r < 3; ++r) {
+        for (int r = 0; r < kRuns; ++r) {
           bdesc[r] = e.axis == 0 ? rdesc[0][r] : rdesc[1][r];
           idesc[r] = e.axis == 0 ? ridesc[0][r] : ridesc[1][r];
           col[r] = e.axis == 0 ? rcol[0][r] : rcol[1][r];
@@ -228,7 +232,7 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int r = 0; r < 3; ++r)
+            for (int r = 0; r < kRuns; ++r)
               if (r < nr)
                 umma_bf16_warp(acc + col[r], adesc + so + 2 * k, bdesc[r] + so + k * kstep[r], idesc[r],
                                (kb > 0 || k > 0) ? 1u : 0u);
@@ -269,7 +273,7 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
                                                       a.H, sid, e.h, p, a.status)
                                : -1;
       const bool write = drow >= 0;
-      const float4* bias4 = reinterpret_cast<const float4*>(a.bias + (static_cast<int64_t>(e.axis) * a.H + e.h) * 256);
+      const float4* bias4 = reinterpret_cast<const float4*>(a.bias + (static_cast<int64_t>(e.axis) * a.H + e.h) * kMaxRank2d);
       __nv_bfloat16* dst =
           static_cast<__nv_bfloat16*>(e.axis == 0 ? a.cache_k : a.cache_v) + (write ? drow : 0) * r;
       const uint32_t acc = tmem + static_cast<uint32_t>(ab * P.acc_stride) + lane_base;
@@ -325,24 +329,25 @@ encode_bf16_kernel(const __grid_constant__ EncodeArgs a, const __grid_constant__
 
 // fp32: literal c[k] = sum_u (x[u] - mu[u]) W[u][k]; block = (token, head, axis).
 __global__ void __launch_bounds__(256) encode_f32_kernel(const __grid_constant__ EncodeArgs a) {
-  const int n = blockIdx.x, h = blockIdx.y, axis = blockIdx.z, k = threadIdx.x;
+  const int n = blockIdx.x, h = blockIdx.y, axis = blockIdx.z;
   const int r = axis == 0 ? a.r_k : a.r_v;
   const int sid = __ldg(a.seq_idx + n), p = __ldg(a.pos + n);
   if (!slot_ok(a, sid, p)) {
-    if (k == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
+    if (threadIdx.x == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
     return;
   }
-  if (k >= r) return;
-  const float* x = static_cast<const float*>(axis == 0 ? a.x_k : a.x_v) + (static_cast<int64_t>(n) * a.H + h) * a.Td;
-  const float* mu = (axis == 0 ? a.mu_k : a.mu_v) + static_cast<int64_t>(h) * a.Td;
-  const float* W = static_cast<const float*>(axis == 0 ? a.w_down_k : a.w_down_v) + static_cast<int64_t>(h) * a.Td * r;
-  float s = 0.f;
-  for (int u = 0; u < a.Td; ++u) s = fmaf(x[u] - mu[u], W[static_cast<int64_t>(u) * r + k], s);
   const int64_t row =
       latent_row_for_write(a.block_table, a.page_size, a.max_pages, a.num_pages, a.L_max, a.H, sid, h, p, a.status);
   if (row < 0) return;
+  const float* x = static_cast<const float*>(axis == 0 ? a.x_k : a.x_v) + (static_cast<int64_t>(n) * a.H + h) * a.Td;
+  const float* mu = (axis == 0 ? a.mu_k : a.mu_v) + static_cast<int64_t>(h) * a.Td;
+  const float* W = static_cast<const float*>(axis == 0 ? a.w_down_k : a.w_down_v) + static_cast<int64_t>(h) * a.Td * r;
   float* dst = static_cast<float*>(axis == 0 ? a.cache_k : a.cache_v);
-  dst[row * r + k] = s;
+  for (int k = threadIdx.x; k < r; k += blockDim.x) {
+    float s = 0.f;
+    for (int u = 0; u < a.Td; ++u) s = fmaf(x[u] - mu[u], W[static_cast<int64_t>(u) * r + k], s);
+    dst[row * r + k] = s;
+  }
 }
 
 }  // namespace
@@ -376,7 +381,7 @@ bool make_encode_plan(int r_k, int r_v, int Td, EncodePlan* p) {
 cudaError_t launch_encode_bf16(const EncodeArgs& a, const EncodePlan& plan, const EncodeMaps& m,
                                cudaStream_t s) {
   if (a.N == 0) return cudaSuccess;
-  encode_bias_kernel<<<dim3(a.H, 2), 256, 0, s>>>(a);
+  encode_bias_kernel<<<dim3(a.H, 2, 2), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   static int configured = 0;

@@ -13,6 +13,8 @@ namespace lla {
 
 constexpr int kMaxStages = 8;
 constexpr int kMaxGrid = 1024;          // upper bound on decode CTAs (workspace sizing)
+constexpr int kMaxRankPerHead = 256;    // r_k, r_v of the per-head variant
+constexpr int kMaxRank2d = 512;         // r_k, r_v of LLA-2D
 constexpr int kDecodeThreads = 224;     // producer, score-MMA, 4 epilogue, value-MMA warps
 constexpr int kWarpVMma = 6;            // decode warp issuing the value MMAs
 constexpr int kRecordsPerCta = 4;       // split records per (unit, CTA): one per epilogue warp
@@ -161,6 +163,9 @@ cudaError_t launch_decoupled_f32(const DecodeArgs& a, cudaStream_t s);
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
+// The same plain kernels over bf16 storage (fp32 arithmetic): the LLA-2D shapes
+// the CTA-pair kernels do not take (ranks above 128 / 256, odd or > 16 heads).
+cudaError_t launch_decode_plain_bf16(const DecodeArgs& a, cudaStream_t s);
 
 // Page sizes the tile kernel's copy path takes: whole tiles inside a page (a multiple
 // of 128 tokens) or a tile as 128/P pieces of P tokens (P a multiple of 8 dividing 128).
@@ -275,7 +280,7 @@ struct EncodeArgs {
   void* cache_k;
   void* cache_v;
   uint32_t* status;
-  float* bias;                       // workspace [2][H][256]: mu W_down per head/axis
+  float* bias;                       // workspace [2][H][512]: mu W_down per head/axis
   const int32_t* block_table;        // paged cache (as DecodeArgs), or nullptr
   int page_size;
   int max_pages;

@@ -611,15 +611,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ----------------------------------------------------------------- latent chunks
 
-// A latent row of rank r (multiple of 16, <= 256) is split into chunks of 64,
+// A latent row of rank r (multiple of 16, <= 512) is split into chunks of 64,
 // 32 and 16 elements (largest first), or into equal chunks of 32.  Each chunk is
 // one TMA box and one shared-memory region whose rows are 128 / 64 / 32 bytes
 // wide, matching the 128B / 64B / 32B swizzle atoms that TMA writes and UMMA reads.
 struct ChunkPlan {
-  int n;            // number of chunks (<= 8)
-  int start[8];     // first element of chunk c
-  int width[8];     // elements in chunk c (64, 32 or 16)
-  int off[8];       // byte offset of chunk c in a 128-row tile
+  int n;            // number of chunks (<= 9 at r <= 512; 32-wide plans <= 8 at r <= 256)
+  int start[16];    // first element of chunk c
+  int width[16];    // elements in chunk c (64, 32 or 16)
+  int off[16];      // byte offset of chunk c in a 128-row tile
   int bytes;        // bytes of a 128-row tile (all chunks)
 };
 

@@ -1,12 +1,13 @@
 """Parity of the LLA-2D path (one latent per token shared by all heads) with the oracle.
 
-lla_decode_attn with variant LLA_2D runs the CTA-pair kernel (bf16) or the SIMT
-fp32 kernels; lla_encode maps the whole stack x in R^{T*H*d} to one latent.  The
-oracle computes the plain definition (every head's K/V reconstructed from the
-shared latent, RoPE, softmax) in fp64 on the same stored tensors.  Cases span
-several 512-token pair blocks, ragged tails (a CTA of the pair with no valid
-token, partial 16-token value chunks), empty sequences and runs split between
-CTA pairs.
+lla_decode_attn with variant LLA_2D runs the CTA-pair score kernel and the value
+kernel (bf16, H even <= 16, r_k <= 128, r_v <= 256), else the plain kernels (fp32
+storage, or bf16 at other head counts and at ranks up to 512); lla_encode maps the
+whole stack x in R^{T*H*d} to one latent.  The oracle computes the plain
+definition (every head's K/V reconstructed from the shared latent, RoPE, softmax)
+in fp64 on the same stored tensors.  Cases span several 256-token pair blocks,
+ragged tails (a CTA of the pair with no valid token, partial 16-token value
+steps), empty sequences and runs split between CTA pairs and value CTAs.
 """
 import numpy as np
 import pytest
@@ -97,8 +98,9 @@ def test_2d_softmax_weights_normalised():
 
 
 def test_2d_growing_scores_rescale_accumulators():
-    """K latents scaled up along the sequence: block maxima overtake the reference by
-    more than 2^8, so the value accumulators are rescaled in TMEM."""
+    """K latents scaled up along the sequence: the 32-token groups' references span a
+    wide range, so the value kernel scales most groups' weights by large powers of two
+    (and flushes the smallest to zero) before the value MMA."""
     w = w2d(H=4, B=2, L_max=2600)
     inp = _inputs(w, 45, [2600, 1800])
     ramp = torch.linspace(1.0, 4.0, w.L_max, device="cuda").view(1, w.L_max, 1)
@@ -130,14 +132,78 @@ def test_2d_repeated_calls_are_deterministic():
 
 
 def test_2d_unsupported_shapes():
-    """Head counts that are not a multiple of 4 (or above 16) and r_k > 128 are
-    refused by the bf16 LLA-2D kernel before any launch."""
-    for H, rk in ((3, 128), (20, 128), (4, 256)):
-        w = w2d(H=H, r_k=rk, r_v=128, B=1, L_max=64)
+    """Ranks above 512 (the LLA-2D limit) are refused before any launch: no kernel
+    family, no workspace size, LLA_ERR_UNSUPPORTED from the call itself."""
+    for rk, rv in ((528, 128), (128, 528)):
+        w = w2d(H=4, r_k=rk, r_v=rv, B=1, L_max=64)
+        dm = lla_dims(w)
+        assert lla.decode_kernel(dm) is None
+        with pytest.raises(lla.LLAError):
+            lla.make_workspace(dm, 1, 64)
         inp = _inputs(w, 48, [64])
         with pytest.raises(lla.LLAError) as e:
-            gpu_decode(w, inp, 0)
+            gpu_decode(w, inp, 0, workspace=torch.zeros(1 << 20, dtype=torch.uint8, device="cuda"))
         assert e.value.status == lla.LLA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("H,rk,rv", [(4, 256, 512), (2, 512, 128), (3, 128, 256), (20, 64, 128),
+                                     (4, 496, 384)])
+def test_2d_bf16_plain_shapes(H, rk, rv):
+    """Shapes outside the CTA-pair kernels' range (ranks above 128 / 256, odd or more
+    than 16 heads) run the plain kernels over bf16 storage: parity, ragged lengths."""
+    w = w2d(H=H, r_k=rk, r_v=rv, B=3, L_max=300)
+    assert lla.decode_kernel(lla_dims(w)) == "plain-2d"
+    inp = _inputs(w, 500 + H + rk + rv, [300, 129, 0])
+    compare(w, inp, 1)
+
+
+def test_2d_pair_shapes_take_the_pair_kernels():
+    for H, rk, rv in ((2, 16, 16), (16, 128, 256), (6, 64, 96)):
+        assert lla.decode_kernel(lla_dims(w2d(H=H, r_k=rk, r_v=rv))) == "pair-2d"
+
+
+def test_2d_f32_rank_512():
+    w = w2d(H=4, r_k=512, r_v=512, B=2, L_max=200, dtype="f32")
+    inp = _inputs(w, 52, [200, 77])
+    compare(w, inp, 0)
+
+
+@pytest.mark.parametrize("dtype,rk,rv", [("bf16", 512, 384), ("bf16", 496, 272), ("f32", 512, 320)])
+def test_2d_encode_large_ranks(dtype, rk, rv):
+    """Encode at LLA-2D ranks above 256 (one 512-column accumulator in the bf16 kernel):
+    each latent within half a bf16 spacing plus the fp32 accumulation bound of the
+    Eq. (2) sum (bf16), or within the sequential-summation bound (fp32)."""
+    T, H, B, L_max, N = 2, 4, 2, 80, 150
+    w = w2d(T=T, H=H, r_k=rk, r_v=rv, B=B, L_max=L_max, N_encode=N, dtype=dtype)
+    inp = make_decode_inputs(w, 53, device="cuda", with_encode=True)
+    seq_idx = torch.tensor(np.arange(N) % B, dtype=torch.int32, device="cuda")
+    pos = torch.tensor(np.arange(N) // B, dtype=torch.int32, device="cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    ck = torch.full((B, L_max, rk), CANARY, dtype=tdt, device="cuda")
+    cv = torch.full((B, L_max, rv), CANARY, dtype=tdt, device="cuda")
+    dm = lla_dims(w)
+    wsp = lla.make_workspace(dm, B, L_max, N)
+    lla.encode(dm, inp["x_k"], inp["x_v"], seq_idx, pos, inp["w_down_k"], inp["w_down_v"],
+               inp["mu_k"], inp["mu_v"], ck, cv, wsp)
+    assert lla.device_status(wsp) == lla.LLA_OK
+    od = oracle_dims(w)
+    si, po = seq_idx.cpu().numpy(), pos.cpu().numpy()
+    for cache, x, wd, mu, r in ((ck, "x_k", "w_down_k", "mu_k", rk), (cv, "x_v", "w_down_v", "mu_v", rv)):
+        exact = np.full((B, L_max, r), CANARY)
+        oracle.encode(od, widen(inp[x]), si, po, widen(inp[wd]), widen(inp[mu]), r, exact)
+        mag = np.zeros((B, L_max, r))
+        oracle.encode(od, np.abs(widen(inp[x]) - widen(inp[mu])[None]), si, po, np.abs(widen(inp[wd])),
+                      np.zeros_like(widen(inp[mu])), r, mag)
+        got = cache.double().cpu().numpy()
+        touched = got != CANARY
+        assert touched.sum() == N * r
+        if dtype == "bf16":
+            half_ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(got), 2.0 ** -126))) - 8)
+            bound = half_ulp + 2.0 ** -20 * mag
+        else:
+            # sequential fp32 sum of T*H*d products: at most n u sum|terms|
+            bound = T * H * 128 * 2.0 ** -24 * mag + 1e-30
+        assert np.all(np.abs(got - exact)[touched] <= bound[touched])
 
 
 def test_2d_encode_layout_structured_exact():
