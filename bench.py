@@ -44,20 +44,20 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # layer (ouro_rho4_b8_16k); a workload takes the capture of its context length.
 # Valid only for the decode source whose sha256 starts with TRAFFIC_SRC_SHA; any other
 # source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = {4096: (263.966208e6 + 3.191552e6) / (31042 * 16),
-                          16384: (1080.890368e6 + 3.592704e6) / (8 * 16384 * 16)}
-TRAFFIC_SRC_SHA = "45b84bcebf40e291"
+TRAFFIC_PER_TOKEN_HEAD = {4096: (263.996928e6 + 3.185920e6) / (31042 * 16),
+                          16384: (1080.883712e6 + 3.314432e6) / (8 * 16384 * 16)}
+TRAFFIC_SRC_SHA = "8aaf3f230435c6c0"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D score kernel (the dominant one of the LLA-2D call), per
 # latent token (all heads), from the 32-sequence variant of the LLA-2D layer; valid
 # only for the source whose sha256 starts with TRAFFIC2D_SRC_SHA.
-TRAFFIC2D_PER_TOKEN = (224.002816e6 + 4.921088e6) / (32 * 8192)
-TRAFFIC2D_SRC_SHA = "82da47c747901f36"
+TRAFFIC2D_PER_TOKEN = (90.234624e6 + 4.024320e6) / (32 * 8192)
+TRAFFIC2D_SRC_SHA = "7100f488412d4d9a"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
 # Same for decode_small_kernel (the per-head kernel at small ranks), from a capture
 # of the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.880128e6 + 3.652096e6) / (64 * 4096 * 16)
-TRAFFIC_SMALL_SRC_SHA = "9491176ae68ec838"
+TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.886784e6 + 3.384576e6) / (64 * 4096 * 16)
+TRAFFIC_SMALL_SRC_SHA = "baa9d750f5db22b1"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 # Same for decoupled_bf16_kernel, per latent token-head (latent K and V rows plus the
 # rotary key), from the 8-sequence variant of the rho = 4 layer.
@@ -67,8 +67,8 @@ DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "ll
 # DRAM bytes of encode_bf16_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
 # for the encode source whose sha256 starts with TRAFFIC_ENC_SRC_SHA.
-TRAFFIC_ENC_PER_TOKEN = (2152.830e6 + 516.694e6) / 65536
-TRAFFIC_ENC_SRC_SHA = "4734b96d1bccc7a9"
+TRAFFIC_ENC_PER_TOKEN = (2152.749056e6 + 516.128512e6) / 65536
+TRAFFIC_ENC_SRC_SHA = "f54a455bce512352"
 ENCODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_encode.cu")
 UNIT = "latent tokens/s per layer-loop"
 DEFAULT_WORKLOAD = "ouro1.4b_rho4_b32_4k"
