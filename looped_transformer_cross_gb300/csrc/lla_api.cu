@@ -682,13 +682,23 @@ lla_status encode_impl(const lla_dims* dims, const void* x_k, const void* x_v, i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dims->dtype == LLA_F32) return launch_encode_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 
-  EncodePlan plan;
-  if (!make_encode_plan(dims->r_k, dims->r_v, a.Td, &plan)) return LLA_ERR_UNSUPPORTED;
-  plan.sms = sm_count();
-  if (plan.sms <= 0) return LLA_ERR_CUDA;
   EncodeMaps m;
   std::memset(&m, 0, sizeof(m));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  EncodePlan plan;
+  if (make_encode_pair_plan(dims->r_k, dims->r_v, a.Td, &plan)) {
+    // CTA pairs: x tiles and 16-column W_down boxes
+    plan.sms = sm_count();
+    if (plan.sms <= 1) return LLA_ERR_CUDA;
+    if (!make_map_3d(&m.xk, x_k, BF, 2, a.Td, a.H, N, 64, 1, 128)) return LLA_ERR_CUDA;
+    if (!make_map_3d(&m.xv, x_v, BF, 2, a.Td, a.H, N, 64, 1, 128)) return LLA_ERR_CUDA;
+    if (!make_map_3d(&m.wk[2], w_down_k, BF, 2, a.r_k, a.Td, a.H, 16, 64, 1)) return LLA_ERR_CUDA;
+    if (!make_map_3d(&m.wv[2], w_down_v, BF, 2, a.r_v, a.Td, a.H, 16, 64, 1)) return LLA_ERR_CUDA;
+    return launch_encode_pair(a, plan, m, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  }
+  if (!make_encode_plan(dims->r_k, dims->r_v, a.Td, &plan)) return LLA_ERR_UNSUPPORTED;
+  plan.sms = sm_count();
+  if (plan.sms <= 0) return LLA_ERR_CUDA;
   if (!make_map_3d(&m.xk, x_k, BF, 2, a.Td, a.H, N, 64, 1, 128)) return LLA_ERR_CUDA;
   if (!make_map_3d(&m.xv, x_v, BF, 2, a.Td, a.H, N, 64, 1, 128)) return LLA_ERR_CUDA;
   for (int c = 0; c < plan.bk.n; ++c) {

@@ -304,6 +304,9 @@ struct EncodeMaps {
 };
 
 bool make_encode_plan(int r_k, int r_v, int Td, EncodePlan* p);
+// CTA-pair encode (ranks multiples of 32 up to 256): one pair MMA covers two tiles
+bool make_encode_pair_plan(int r_k, int r_v, int Td, EncodePlan* p);
+cudaError_t launch_encode_pair(const EncodeArgs& a, const EncodePlan& plan, const EncodeMaps& m, cudaStream_t s);
 cudaError_t launch_encode_bf16(const EncodeArgs& a, const EncodePlan& plan, const EncodeMaps& m,
                                cudaStream_t s);
 cudaError_t launch_encode_f32(const EncodeArgs& a, cudaStream_t s);
