@@ -64,7 +64,7 @@ DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", 
 TRAFFIC_DEC_PER_TOKEN_HEAD = (320.807936e6 + 3.610112e6) / (31042 * 16)
 TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
 DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
-# DRAM bytes of encode_bf16_kernel per prefill token (all heads, both axes), from one
+# DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
 # for the encode source whose sha256 starts with TRAFFIC_ENC_SRC_SHA.
 TRAFFIC_ENC_PER_TOKEN = (2152.749056e6 + 516.128512e6) / 65536
@@ -392,8 +392,8 @@ def prefill_run(step: DecodeStep, reps: int, hbm: float, src: str):
     return {"tokens": n, "heads": w.H if w.variant == 0 else 1, "encode_ms": t * 1e3,
             "value": n / t, "unit": "prefill tokens/s per layer", "tflops": flops / t / 1e12,
             "roofline": {"bound": "hbm", "achieved": moved / t / 1e9, "peak": hbm, "unit": "GB/s",
-                         "frac": moved / t / 1e9 / hbm, "traffic": traffic, "traffic_kernel": "encode_bf16_kernel",
-                         "kernel": "lla_encode (encode_bias_kernel + encode_bf16_kernel)",
+                         "frac": moved / t / 1e9 / hbm, "traffic": traffic, "traffic_kernel": "encode_pair_kernel",
+                         "kernel": "lla_encode (encode_bias_kernel + encode_pair_kernel)",
                          "algorithmic_bytes_per_launch": moved, "peak_source": src}}
 
 
