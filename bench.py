@@ -67,8 +67,8 @@ DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "ll
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
 # for the encode source whose sha256 starts with TRAFFIC_ENC_SRC_SHA.
-TRAFFIC_ENC_PER_TOKEN = (2152.749056e6 + 516.128512e6) / 65536
-TRAFFIC_ENC_SRC_SHA = "f54a455bce512352"
+TRAFFIC_ENC_PER_TOKEN = (2198.692352e6 + 481.901568e6) / 65536
+TRAFFIC_ENC_SRC_SHA = "34fa9d1b5ce18a15"
 ENCODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_encode.cu")
 UNIT = "latent tokens/s per layer-loop"
 DEFAULT_WORKLOAD = "ouro1.4b_rho4_b32_4k"
