@@ -64,6 +64,11 @@ DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", 
 TRAFFIC_DEC_PER_TOKEN_HEAD = (320.807936e6 + 3.610112e6) / (31042 * 16)
 TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
 DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
+# Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores);
+# None until a capture of the current source is taken.
+TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = None
+TRAFFIC_DEC_SMALL_SRC_SHA = None
+DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_small.cu")
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
 # for the encode source whose sha256 starts with TRAFFIC_ENC_SRC_SHA.
@@ -559,13 +564,17 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
         lat_bytes = step.tokens * w.H * (w.r_k + w.r_v + D_ROPE) * 2
         achieved = lat_bytes / t_call / 1e9
         import hashlib
-        with open(DECOUPLED_SRC, "rb") as f:
-            same_src = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC_DEC_SRC_SHA)
-        traffic = TRAFFIC_DEC_PER_TOKEN_HEAD * step.tokens * w.H if same_src else None
+        small = lla.decoupled_kernel(step.dm, D_ROPE) == "small-rank"
+        src_file, sha, per_th = ((DECOUPLED_SMALL_SRC, TRAFFIC_DEC_SMALL_SRC_SHA, TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD)
+                                 if small else (DECOUPLED_SRC, TRAFFIC_DEC_SRC_SHA, TRAFFIC_DEC_PER_TOKEN_HEAD))
+        with open(src_file, "rb") as f:
+            same_src = sha is not None and hashlib.sha256(f.read()).hexdigest().startswith(sha)
+        traffic = per_th * step.tokens * w.H if same_src else None
+        main = "decoupled_small_kernel" if small else "decoupled_bf16_kernel"
+        query = "decoupled_small_z_kernel" if small else "decoupled_query_kernel"
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": traffic, "traffic_kernel": "decoupled_bf16_kernel",
-                "kernel": "lla_decode_attn_decoupled (decoupled_query_kernel + decoupled_bf16_kernel + "
-                          "decode_combine_kernel)",
+                "frac": achieved / hbm, "traffic": traffic, "traffic_kernel": main,
+                "kernel": "lla_decode_attn_decoupled (%s + %s + decode_combine_kernel)" % (query, main),
                 "algorithmic_bytes_per_launch": lat_bytes, "launch_ms": t_call * 1e3,
                 "peak_source": src}
     elif w.variant == 0:

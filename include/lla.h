@@ -340,6 +340,15 @@ lla_status lla_decode_attn_noalloc(const lla_dims* dims, int loop_t, const void*
  * split over CTAs), or NULL for invalid or unsupported dims. */
 const char* lla_decode_kernel(const lla_dims* dims);
 
+/* Name of the kernel family lla_decode_attn_decoupled runs for `dims` and
+ * d_rope (host-only, no launch): "fp32" (LLA_F32), "small-rank" (bf16 with r_k in
+ * {16, 32}, r_v in {32, 64} and an even H <= 16: positions split over CTAs,
+ * rotary branch and content score on the tensor cores, fp32 cos/sin per token),
+ * "tile" (every other bf16 shape with r_k <= 128: 128-token tiles over
+ * (sequence, head), scores on the CUDA cores), or NULL for invalid or
+ * unsupported dims (LLA_2D, d_rope != 64). */
+const char* lla_decoupled_kernel(const lla_dims* dims, int d_rope);
+
 /* Workspace bytes for calls with at most B sequences of L_max slots and
  * encode batches of at most max_N tokens, on the current CUDA device.
  * Returns 0 for invalid dims. */

@@ -86,6 +86,8 @@ struct DecodeArgs {
   const void* k_rope;                // decoupled path: rotary keys [B][H][L_max][d_rope]
   int d_rope;                        // decoupled path: rotary branch width (0: full-RoPE path)
   int ring_slots;                    // decoupled path: slots of the key ring
+  float* trigT;                      // decoupled small-rank path: fp32 RoPE table [64][trig_rows]
+  float* qb0;                        // decoupled small-rank path: sc q_c . mu_k per (sequence, head)
   // Paged cache (per-head variant): cache_k / cache_v are page pools
   // [num_pages][H][page_size][r]; logical page p of sequence b is physical page
   // block_table[b * max_pages + p].  block_table == nullptr: dense [B][H][L_max][r].
@@ -157,6 +159,18 @@ cudaError_t launch_decoupled_bf16(const DecodeArgs& a, cudaStream_t s);
 int decoupled_qrec_floats(int r_k);     // floats of one unit's query record
 int decoupled_ring_slots(int r_k, int r_v);   // ring slots that fit in shared memory (0: unsupported)
 size_t decoupled_smem_bytes(int r_k, int r_v, int ns);
+// Small ranks (r_k in {16, 32}, r_v in {32, 64}, H even <= 16): rotary branch and
+// content score on the tensor cores, position-major split (a.pos_major = 1, four
+// records per CTA).  Needs a.zimg (B images per (sequence, head),
+// decoupled_small_img_stride bytes apart), a.qb0 [B H], a.trigT [64][a.trig_rows].
+struct DecoupledMaps {
+  CUtensorMap kr;                    // rotary keys [B H][L_max][64], boxes 64 x 128 (128-byte swizzle)
+  CUtensorMap ck;                    // K latents [B H][L_max][r_k], boxes 16 x 128 (32-byte swizzle)
+};
+bool decoupled_small_supported(int H, int r_k, int r_v);
+size_t decoupled_small_img_stride(int r_k);
+int64_t decoupled_small_trig_rows(int64_t L_max);
+cudaError_t launch_decoupled_small(const DecodeArgs& a, const DecoupledMaps& m, cudaStream_t s);
 // fp32 softmax over a.scores and the V path (shared by the fp32 decode paths).
 cudaError_t launch_decode_f32_values(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decoupled_f32(const DecodeArgs& a, cudaStream_t s);

@@ -94,6 +94,8 @@ def lib():
             L.lla_evict_window.restype = ctypes.c_int
             L.lla_decode_kernel.argtypes = [pd]
             L.lla_decode_kernel.restype = ctypes.c_char_p
+            L.lla_decoupled_kernel.argtypes = [pd, ctypes.c_int]
+            L.lla_decoupled_kernel.restype = ctypes.c_char_p
             L.lla_abi_version.argtypes = []
             L.lla_abi_version.restype = ctypes.c_int
             _lib = L
@@ -108,6 +110,13 @@ def decode_kernel(dm: Dims) -> Optional[str]:
     """Kernel family lla_decode_attn runs for these dims ("tile", "small-rank",
     "pair-2d", "fp32"), or None if they are invalid or unsupported."""
     r = lib().lla_decode_kernel(ctypes.byref(dm))
+    return None if r is None else r.decode()
+
+
+def decoupled_kernel(dm: Dims, d_rope: int = 64) -> Optional[str]:
+    """Kernel family lla_decode_attn_decoupled runs for these dims ("small-rank",
+    "tile", "fp32"), or None if they are invalid or unsupported."""
+    r = lib().lla_decoupled_kernel(ctypes.byref(dm), int(d_rope))
     return None if r is None else r.decode()
 
 

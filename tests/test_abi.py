@@ -134,6 +134,23 @@ def test_decode_kernel_dispatch(L):
     assert d(4, 16, 16, 32, d_head=64) is None
 
 
+def test_decoupled_kernel_dispatch(L):
+    """Which decoupled-RoPE kernel family each shape takes (host-side, no launch)."""
+    d = lambda *a, d_rope=64, **k: lla.decoupled_kernel(lla.dims(*a, **k), d_rope)
+    assert d(4, 16, 16, 32) == "small-rank"          # Ouro-1.4B at rho = 21.3
+    assert d(4, 16, 32, 64) == "small-rank"
+    assert d(4, 2, 16, 64) == "small-rank"
+    assert d(4, 6, 32, 32) == "small-rank"           # three heads per epilogue group
+    assert d(4, 3, 16, 32) == "tile"                 # odd H
+    assert d(4, 18, 16, 32) == "tile"                # more heads than resident images
+    assert d(4, 16, 48, 80) == "tile"
+    assert d(4, 16, 96, 160) == "tile"               # Ouro-1.4B at rho = 4
+    assert d(4, 16, 16, 32, dtype=lla.LLA_F32) == "fp32"
+    assert d(4, 16, 16, 32, d_rope=32) is None
+    assert d(4, 16, 16, 32, variant=lla.LLA_2D) is None
+    assert d(4, 16, 256, 256) is None                # r_k above the tile kernel's 128
+
+
 def test_window_rejects_bad_arguments_on_host(L):
     dm = lla.dims(4, 2, 16, 32)
     call = lambda d, B=1, W=8, rope_len=128, ws=1 << 20: L.lla_window_attn(
