@@ -64,10 +64,10 @@ DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", 
 TRAFFIC_DEC_PER_TOKEN_HEAD = (320.807936e6 + 3.610112e6) / (31042 * 16)
 TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
 DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
-# Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores);
-# None until a capture of the current source is taken.
-TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = None
-TRAFFIC_DEC_SMALL_SRC_SHA = None
+# Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores),
+# from the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
+TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.403648e6 + 3.484928e6) / (64 * 4096 * 16)
+TRAFFIC_DEC_SMALL_SRC_SHA = "ccb9befb5134559b"
 DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_small.cu")
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
