@@ -258,9 +258,12 @@ class DecodeStep:
             self.cos_r, self.sin_r = c.to(device), s.to(device)
             self.dws = lla.decoupled_workspace(self.dm, D_ROPE, w.B, w.L_max, device=device)
 
-    def run(self, ev=None):
+    def run(self, ev=None, group=False):
+        """One step.  ``ev``: events [start][end][window end] per decode call; with
+        ``group`` only the start of the first and the end of the last decode call of
+        each layer are recorded (no event between consecutive calls)."""
         if self.nlayers > 1:
-            return self.run_layers(ev)
+            return self.run_layers(ev, group)
         i, dm = self.inp, self.dm
         # the new token's latent: slot seq_lens - 1 (the query's own slot without a window)
         if self.paged:
@@ -270,7 +273,7 @@ class DecodeStep:
             lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, self.enc_pos, i["w_down_k"], i["w_down_v"],
                        i["mu_k"], i["mu_v"], i["cache_k"], i["cache_v"], self.ws)
         for t in range(self.w.T):
-            if ev is not None:
+            if ev is not None and (not group or t == 0):
                 ev[0][t].record()
             if self.paged:
                 lla.decode_attn_paged(dm, t, self.q[t], self.pool_k, self.pool_v, self.block_table, self.paged,
@@ -284,7 +287,7 @@ class DecodeStep:
                 lla.decode_attn(dm, t, self.q[t], i["cache_k"], i["cache_v"], i["seq_lens"], i["q_pos"],
                                 i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"], self.cos, self.sin,
                                 self.out[t], self.lse[t], self.ws)
-            if ev is not None:
+            if ev is not None and (not group or t == self.w.T - 1):
                 ev[1][t].record()
             if self.window > 0:
                 v = self.win
@@ -293,19 +296,19 @@ class DecodeStep:
                 if ev is not None:
                     ev[2][t].record()
 
-    def run_layers(self, ev=None):
+    def run_layers(self, ev=None, group=False):
         dm, T = self.dm, self.w.T
         for l in range(self.nlayers):
             i = self.bufs[l % len(self.bufs)]
             lla.encode(dm, i["x_k"], i["x_v"], self.seq_idx, self.enc_pos, i["w_down_k"], i["w_down_v"],
                        i["mu_k"], i["mu_v"], i["cache_k"], i["cache_v"], self.ws)
             for t in range(T):
-                if ev is not None:
+                if ev is not None and (not group or t == 0):
                     ev[0][l * T + t].record()
                 lla.decode_attn(dm, t, self.qL[l, t], i["cache_k"], i["cache_v"], i["seq_lens"], i["q_pos"],
                                 i["w_up_k"], i["w_up_v"], i["mu_k"], i["mu_v"], self.cos, self.sin,
                                 self.outL[l, t], self.lseL[l, t], self.ws)
-                if ev is not None:
+                if ev is not None and (not group or t == T - 1):
                     ev[1][l * T + t].record()
 
     def dense_view(self, nseq):
@@ -514,6 +517,10 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
                       paged=args.paged, layers=layers, prefill=legs and args.prefill)
     T = w.T
     LT = T * layers
+    # Decode-call timing: events around each layer's T consecutive calls (one call's
+    # time = the group's / T; no event between calls, so back-to-back calls run as
+    # they would untimed), or around every call when the window call follows each one
+    group = not (legs and args.window > 0)
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(LT)] for _ in range(3)]
           for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -530,7 +537,7 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
         h0 = time.perf_counter()
         start.record()
         for k in range(steps):
-            step.run(ev[k])
+            step.run(ev[k], group)
         stop.record()
         torch.cuda.synchronize()
         h1 = time.perf_counter()
@@ -556,7 +563,11 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
     value = tokens_all / t_max
 
     # dominant kernel: the decode call (main kernel + its small combine), timed per launch
-    durs = [ev[k][0][t].elapsed_time(ev[k][1][t]) / 1e3 for k in range(steps) for t in range(LT)]
+    if group:
+        durs = [ev[k][0][l * T].elapsed_time(ev[k][1][l * T + T - 1]) / 1e3 / T
+                for k in range(steps) for l in range(layers)]
+    else:
+        durs = [ev[k][0][t].elapsed_time(ev[k][1][t]) / 1e3 for k in range(steps) for t in range(LT)]
     t_call = float(np.mean(durs))
     hbm, tflops, src = peaks()
     if args.decoupled:
@@ -616,6 +627,10 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
                 "algorithmic_flops_per_launch": flops,
                 "latent_bytes_per_launch": step.tokens * (w.r_k + w.r_v) * 2,
                 "launch_ms": t_call * 1e3, "peak_source": src + " (bf16 sustained)"}
+
+    roof["launch_timing"] = ("CUDA events around each layer's %d back-to-back decode calls in the timed steps; "
+                             "launch_ms = group time / %d" % (T, T)) if group else \
+        "CUDA events around every decode call in the timed steps"
 
     win = None
     if legs and args.window > 0:

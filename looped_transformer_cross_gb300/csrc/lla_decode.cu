@@ -151,6 +151,9 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
 // so a warp loads contiguous W row segments and writes whole swizzled rows.
 constexpr int kZThreads = 256;
 __global__ void __launch_bounds__(kZThreads) decode_z_kernel(const __grid_constant__ DecodeArgs a) {
+  // launched as a programmatic dependent of whatever precedes the call on the
+  // stream: nothing is read before that grid has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the decode kernel may start its set-up now; it waits for this grid before
   // it reads an image
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -740,6 +743,9 @@ size_t combine_smem_bytes(int r_v, int units) {
 // NJ: record columns per lane (r_v <= 32 NJ).
 template <int kCombineThreads, int NJ>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const __grid_constant__ DecodeArgs a) {
+  // the next call's image grid may be scheduled now; it waits for this grid to
+  // complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kCombineWarps = kCombineThreads / 32;
   extern __shared__ float csm[];
   __shared__ int red[kCombineThreads / 32];
@@ -826,7 +832,9 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
         // record r of the unit: CTA c0 + r / R, warp r % R
         auto rec_at = [&](int r) { return a.partials + (base + (r >> rsh) * cstride + (r & (R - 1))) * rs; };
         // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
-        // the unit in that CTA wrote m = -inf, l = 0, acc = 0
+        // the unit in that CTA wrote m = -inf, l = 0, acc = 0.  (CTA ranges are
+        // [c per, (c + 1) per): only CTAs past the last tile are empty, never one
+        // between c0 and c1.)
         const int nrec = R * (c1 - c0 + 1);
         for (int cb = 0; cb < nrec; cb += 8) {
           // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
@@ -1085,11 +1093,12 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodeMaps& maps, cuda
     if (e != cudaSuccess) return e;
     configured[page] = a.plan.bytes;
   }
-  decode_z_kernel<<<a.B * a.H, kZThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  // programmatic dependent launches: the image grid is scheduled while the previous
+  // grid on the stream drains (it waits for it before reading anything); the decode
+  // grid's set-up overlaps the image grid; its producer waits for that grid before
+  // the first image copy
+  cudaError_t e = launch_pdl(decode_z_kernel, dim3(a.B * a.H), dim3(kZThreads), 0, s, a);
   if (e != cudaSuccess) return e;
-  // programmatic dependent launch: the decode grid's set-up overlaps the image
-  // kernel; its producer waits for that grid before the first image copy
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kDecodeThreads);

@@ -122,6 +122,9 @@ __device__ __forceinline__ uint32_t half2_bits(__half2 v) { return *reinterpret_
 constexpr int kSZThreads = 256;
 constexpr int kZSeqs = 8;
 __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid_constant__ DecodeArgs a) {
+  // launched as a programmatic dependent of whatever precedes the call on the
+  // stream: nothing is read before that grid has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the decode grid may start its set-up now; it waits for this grid before it
   // copies an image or reads a RoPE row
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -693,8 +696,7 @@ cudaError_t launch_small_instance(const DecodeArgs& a, cudaStream_t s) {
   }
   const int trig_blocks = static_cast<int>((a.trig_rows + kTrigRowsPerBlock - 1) / kTrigRowsPerBlock);
   const int z_blocks = a.H * ((a.B + kZSeqs - 1) / kZSeqs);
-  decode_small_z_kernel<<<z_blocks + trig_blocks, kSZThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_small_z_kernel, dim3(z_blocks + trig_blocks), dim3(kSZThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the decode grid's set-up overlaps the image
   // kernel; it waits for that grid before the first image copy / RoPE row read

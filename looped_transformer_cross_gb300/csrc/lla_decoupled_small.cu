@@ -182,6 +182,9 @@ struct SlotPos {
 //    rows 2-15 zero; each block in the 32-byte swizzle.  sc b0 goes to qb0[b H + h].
 //    Empty sequences are skipped (never read).
 __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __grid_constant__ DecodeArgs a) {
+  // launched as a programmatic dependent of whatever precedes the call on the
+  // stream: nothing is read before that grid has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the decode grid may start its set-up now; it waits for this grid before it
   // copies an image or reads the table
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -700,8 +703,7 @@ cudaError_t launch_decoupled_small(const DecodeArgs& a, const DecoupledMaps& m, 
   if (!make_ds_plan(a.H, a.r_k, a.r_v, &P)) return cudaErrorInvalidValue;
   const int trig_blocks = static_cast<int>((a.trig_rows + kTrigJ - 1) / kTrigJ);
   const int z_blocks = a.H * ((a.B + kDzSeqs - 1) / kDzSeqs);
-  decoupled_small_z_kernel<<<z_blocks + trig_blocks, kDzThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decoupled_small_z_kernel, dim3(z_blocks + trig_blocks), dim3(kDzThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   if (a.r_k == 16 && a.r_v == 32) e = launch_instance<16, 32>(a, m, P.bytes, s);
   else if (a.r_k == 16 && a.r_v == 64) e = launch_instance<16, 64>(a, m, P.bytes, s);

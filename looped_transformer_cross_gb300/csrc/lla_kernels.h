@@ -99,6 +99,26 @@ struct DecodeArgs {
   DecodeSmallPlan splan;
 };
 
+// Launch `kern` as a programmatic dependent of the previous grid on stream `s`: its
+// blocks may be scheduled while that grid drains, so the kernel must execute
+// griddepcontrol.wait before it reads or writes anything that grid (or an earlier
+// one) produces or consumes.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Validation of the block-table entries a paged decode reads: the decode kernels
 // clamp an entry into the pool without checking it, and the query-image kernels
 // (one block per sequence here) record LLA_ERR_DEVICE_ARG for any entry of a
