@@ -44,9 +44,9 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # layer (ouro_rho4_b8_16k); a workload takes the capture of its context length.
 # Valid only for the decode source whose sha256 starts with TRAFFIC_SRC_SHA; any other
 # source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = {4096: (263.996928e6 + 3.185920e6) / (31042 * 16),
-                          16384: (1080.883712e6 + 3.314432e6) / (8 * 16384 * 16)}
-TRAFFIC_SRC_SHA = "8aaf3f230435c6c0"
+TRAFFIC_PER_TOKEN_HEAD = {4096: (263.983104e6 + 3.294720e6) / (31042 * 16),
+                          16384: (1080.887296e6 + 3.670272e6) / (8 * 16384 * 16)}
+TRAFFIC_SRC_SHA = "5202cd14c4a209f0"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D score kernel (the dominant one of the LLA-2D call), per
 # latent token (all heads), from the 32-sequence variant of the LLA-2D layer; valid
@@ -56,8 +56,8 @@ TRAFFIC2D_SRC_SHA = "7100f488412d4d9a"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
 # Same for decode_small_kernel (the per-head kernel at small ranks), from a capture
 # of the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.886784e6 + 3.384576e6) / (64 * 4096 * 16)
-TRAFFIC_SMALL_SRC_SHA = "baa9d750f5db22b1"
+TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.876544e6 + 3.633920e6) / (64 * 4096 * 16)
+TRAFFIC_SMALL_SRC_SHA = "6579fd99196d23a6"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 # Same for decoupled_bf16_kernel, per latent token-head (latent K and V rows plus the
 # rotary key), from the 8-sequence variant of the rho = 4 layer.
@@ -66,8 +66,8 @@ TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
 DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
 # Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores),
 # from the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.403648e6 + 3.484928e6) / (64 * 4096 * 16)
-TRAFFIC_DEC_SMALL_SRC_SHA = "ccb9befb5134559b"
+TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.464064e6 + 3.409408e6) / (64 * 4096 * 16)
+TRAFFIC_DEC_SMALL_SRC_SHA = "5577288d0b0dc301"
 DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_small.cu")
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
