@@ -100,6 +100,10 @@ __host__ __device__ inline bool make_ds_plan(int H, int r_k, int r_v, DsPlan* p)
   const int fixed = imgs + acc + ml + misc + 1024;
   int NS = (kSmemLimit - fixed) / p->slot;
   NS = NS < kMaxNS ? NS : kMaxNS;
+  // a slot always serves the same epilogue group: a group's consecutive uses of a
+  // slot are then consecutive phases of its barriers (a parity wait must never be
+  // more than one phase ahead)
+  NS -= NS % kEpiGroups;
   if (NS < 2) return false;
   p->NS = NS;
   int off = 0;
