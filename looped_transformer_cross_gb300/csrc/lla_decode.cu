@@ -739,6 +739,14 @@ size_t combine_smem_bytes(int r_v, int units) {
   return (static_cast<size_t>(128) * (r_v / 2 + 1) + units * 256 + 2 * units) * 4;
 }
 
+// d = a * b + d on a pair of fp32 lanes (one packed instruction).
+__device__ __forceinline__ void fma_pair(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "mov.b64 pd, {%0, %1};\n\tfma.rn.f32x2 pd, pa, pb, pd;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // kCombineThreads = 128: at most 4 units per block (small batches); 256: up to 16.
 // NJ: record columns per lane (r_v <= 32 NJ).
 template <int kCombineThreads, int NJ>
@@ -800,73 +808,88 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
 #pragma unroll
   for (int w = 0; w < kCombineThreads / 32; ++w) tot += red[w];
 
+  // ---- inputs only: where each of this warp's units (b0 + w, h), (b0 + w + 8, h)
+  // has its records, and this thread's mu
+  // Tile-major split (per-head kernel): CTA ranges over the flat (sequence, head,
+  // tile) list, records ((b H + h) + c) R + warp.  Position-major split (small-rank
+  // kernels): ranges over (sequence, tile) with every head inner, records
+  // ((b + c) H + h) R + warp.  R = 4 (one per epilogue warp) or 1 (decoupled tile
+  // kernel: its warps are merged within the CTA).  A unit's records: one per (CTA c
+  // in [c0, c1], epilogue warp); a warp that saw no token of the unit in that CTA
+  // wrote m = -inf, l = 0, acc = 0.  (CTA ranges are [c per, (c + 1) per): only CTAs
+  // past the last tile are empty, never one between c0 and c1.)
+  constexpr int kUPW = kCombineThreads == 256 ? 2 : 1;   // units per warp (cu <= 16 / <= 4)
+  const int R = a.records_per_cta, rsh = R == 4 ? 2 : 0;   // R is 4 or 1
+  const int rs = a.r_v + kRecordHead;
+  const long long cstride = a.pos_major ? static_cast<long long>(R) * a.H : R;
+  long long ubase[kUPW];
+  int unrec[kUPW];
+#pragma unroll
+  for (int q = 0; q < kUPW; ++q) {
+    const int ui = warp + q * kCombineWarps, b = b0 + ui;
+    ubase[q] = 0;
+    unrec[q] = 0;
+    if (ui >= cu || b >= a.B) continue;
+    int pb = pre;   // tiles of sequences before b
+    for (int bb = b0; bb < b; ++bb) pb += (clamp_len(__ldg(a.seq_lens + bb), a.L_max) + kTile - 1) / kTile;
+    const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
+    if (nb == 0) continue;
+    const long long total = a.pos_major ? tot : static_cast<long long>(a.H) * tot;
+    const long long per = max(1LL, (total + a.grid - 1) / a.grid);
+    const long long F0 = a.pos_major ? pb : static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
+    const long long F1 = F0 + nb - 1;
+    const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
+    const long long u = static_cast<long long>(b) * a.H + h;
+    ubase[q] = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * R : (u + c0) * R;
+    unrec[q] = R * (c1 - c0 + 1);
+  }
+  const int e = tid & (kHeadDim - 1);
+  const float mu = __ldg(a.mu_v + static_cast<int64_t>(h) * a.mu_hstride + e);
+
   asm volatile("griddepcontrol.wait;" ::: "memory");   // records written
 
-  // ---- warp w merges the records of units (b0 + w, h) and (b0 + w + 8, h)
-  for (int ui = warp; ui < cu; ui += kCombineWarps) {
+  // ---- warp w merges the records of its units
+#pragma unroll
+  for (int q = 0; q < kUPW; ++q) {
+    const int ui = warp + q * kCombineWarps;
+    if (ui >= cu) break;
     float M = -INFINITY, Lt = 0.f;
     float acc[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) acc[j] = 0.f;
-    const int b = b0 + ui;
-    if (b < a.B) {
-      int pb = pre;   // tiles of sequences before b
-      for (int bb = b0; bb < b; ++bb) pb += (clamp_len(__ldg(a.seq_lens + bb), a.L_max) + kTile - 1) / kTile;
-      const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
-      if (nb > 0) {
-        // Tile-major split (per-head kernel): CTA ranges over the flat (sequence,
-        // head, tile) list, records ((b H + h) + c) R + warp.  Position-major split
-        // (small-rank kernel): ranges over (sequence, tile) with every head inner,
-        // records ((b + c) H + h) R + warp.  R = 4 (one per epilogue warp) or 1
-        // (decoupled kernel: its warps are merged within the CTA).
-        const long long total = a.pos_major ? tot : static_cast<long long>(a.H) * tot;
-        const long long per = max(1LL, (total + a.grid - 1) / a.grid);
-        const long long F0 = a.pos_major ? pb : static_cast<long long>(a.H) * pb + static_cast<long long>(h) * nb;
-        const long long F1 = F0 + nb - 1;
-        const int c0 = static_cast<int>(F0 / per), c1 = static_cast<int>(F1 / per);
-        const int rs = a.r_v + kRecordHead;
-        const long long u = static_cast<long long>(b) * a.H + h;
-        const int R = a.records_per_cta, rsh = R == 4 ? 2 : 0;   // R is 4 or 1
-        const long long base = a.pos_major ? ((b + c0) * static_cast<long long>(a.H) + h) * R : (u + c0) * R;
-        const long long cstride = a.pos_major ? static_cast<long long>(R) * a.H : R;
-        // record r of the unit: CTA c0 + r / R, warp r % R
-        auto rec_at = [&](int r) { return a.partials + (base + (r >> rsh) * cstride + (r & (R - 1))) * rs; };
-        // one per (CTA c in [c0, c1], epilogue warp); a warp that saw no token of
-        // the unit in that CTA wrote m = -inf, l = 0, acc = 0.  (CTA ranges are
-        // [c per, (c + 1) per): only CTAs past the last tile are empty, never one
-        // between c0 and c1.)
-        const int nrec = R * (c1 - c0 + 1);
-        for (int cb = 0; cb < nrec; cb += 8) {
-          // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
-          // lane + 32 j of each, all in one round of loads
-          const int cl = cb + (lane & 7);
-          const float mh = cl < nrec ? rec_at(cl)[0] : -INFINITY;
-          const float lh = cl < nrec ? rec_at(cl)[1] : 0.f;
-          float x[8][NJ];
+    const long long base = ubase[q];
+    const int nrec = unrec[q];
+    // record r of the unit: CTA c0 + r / R, warp r % R
+    auto rec_at = [&](int r) { return a.partials + (base + (r >> rsh) * cstride + (r & (R - 1))) * rs; };
+    for (int cb = 0; cb < nrec; cb += 8) {
+      // heads (m, l) of records cb..cb+7 in lanes 0..7, and this lane's columns
+      // lane + 32 j of each, all in one round of loads
+      const int cl = cb + (lane & 7);
+      const float mh = cl < nrec ? rec_at(cl)[0] : -INFINITY;
+      const float lh = cl < nrec ? rec_at(cl)[1] : 0.f;
+      float x[8][NJ];
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
+      for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-              const int col = lane + 32 * j;
-              x[r][j] = cb + r < nrec && col < a.r_v ? rec_at(cb + r)[kRecordHead + col] : 0.f;
-            }
-          const float Mn = fmaxf(M, warp_max(mh));
-          if (Mn != -INFINITY) {
-            const float alpha = M == -INFINITY ? 0.f : exp2f(M - Mn);
-            Lt *= alpha;
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) acc[j] *= alpha;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const float mr = __shfl_sync(0xffffffffu, mh, r), lr = __shfl_sync(0xffffffffu, lh, r);
-              const float w = mr == -INFINITY ? 0.f : exp2f(mr - Mn);
-              Lt = fmaf(lr, w, Lt);
-#pragma unroll
-              for (int j = 0; j < NJ; ++j) acc[j] = fmaf(x[r][j], w, acc[j]);
-            }
-            M = Mn;
-          }
+        for (int j = 0; j < NJ; ++j) {
+          const int col = lane + 32 * j;
+          x[r][j] = cb + r < nrec && col < a.r_v ? rec_at(cb + r)[kRecordHead + col] : 0.f;
         }
+      const float Mn = fmaxf(M, warp_max(mh));
+      if (Mn != -INFINITY) {
+        const float alpha = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        Lt *= alpha;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) acc[j] *= alpha;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float mr = __shfl_sync(0xffffffffu, mh, r), lr = __shfl_sync(0xffffffffu, lh, r);
+          const float w = mr == -INFINITY ? 0.f : exp2f(mr - Mn);
+          Lt = fmaf(lr, w, Lt);
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) acc[j] = fmaf(x[r][j], w, acc[j]);
+        }
+        M = Mn;
       }
     }
 #pragma unroll
@@ -876,14 +899,15 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
   }
   __syncthreads();
 
-  // ---- out[b][h][e] = acc_b . W_e / Lt_b + mu_e, thread (half, e) reading row e of W once
+  // ---- out[b][h][e] = acc_b . W_e / Lt_b + mu_e, thread (half, e) reading row e of W
+  // once; even and odd columns summed in the two lanes of a packed FMA
   constexpr int kHalf = kCombineThreads == 256 ? kCombineUnits / 2 : 4;
-  const int e = tid & (kHeadDim - 1), j0 = (tid >> 7) * kHalf;
-  float o[kHalf];
+  const int j0 = (tid >> 7) * kHalf;
+  float ox[kHalf], oy[kHalf];
 #pragma unroll
-  for (int j = 0; j < kHalf; ++j) o[j] = 0.f;
+  for (int j = 0; j < kHalf; ++j) { ox[j] = 0.f; oy[j] = 0.f; }
   const uint32_t* wr = Ws + e * wpr;
-#pragma unroll 4
+#pragma unroll 8
   for (int k = 0; k < rw; ++k) {
     const uint32_t w2 = wr[k];
     const float wlo = __uint_as_float(w2 << 16), whi = __uint_as_float(w2 & 0xFFFF0000u);
@@ -891,11 +915,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
     for (int j = 0; j < kHalf; ++j) {
       if (j0 + j < cu) {   // accs holds cu units
         const float2 av = *reinterpret_cast<const float2*>(accs + (j0 + j) * 256 + 2 * k);
-        o[j] = fmaf(av.x, wlo, fmaf(av.y, whi, o[j]));
+        fma_pair(ox[j], oy[j], av.x, av.y, wlo, whi);
       }
     }
   }
-  const float mu = __ldg(a.mu_v + static_cast<int64_t>(h) * a.mu_hstride + e);
 #pragma unroll
   for (int jj = 0; jj < kHalf; ++jj) {
     const int j = j0 + jj;
@@ -903,7 +926,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
     if (j >= cu || bb >= a.B) continue;
     const int64_t uu = static_cast<int64_t>(bb) * a.H + h;
     const bool empty = Ms[j] == -INFINITY;
-    a.out[uu * kHeadDim + e] = empty ? 0.f : o[jj] / Ls[j] + mu;
+    a.out[uu * kHeadDim + e] = empty ? 0.f : (ox[jj] + oy[jj]) / Ls[j] + mu;
     if (e == 0) a.lse[uu] = empty ? -INFINITY : (Ms[j] + log2f(Ls[j])) * kLn2;
   }
 }
