@@ -735,8 +735,10 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
 // and keep the number of small, latency-bound blocks low at serving batch sizes.
 constexpr int kCombineUnits = 16;
 
+// W_up,v rows padded to r_v / 2 + 4 words: 16-byte aligned, and eight threads
+// reading eight consecutive rows at one column touch 32 distinct banks.
 size_t combine_smem_bytes(int r_v, int units) {
-  return (static_cast<size_t>(128) * (r_v / 2 + 1) + units * 256 + 2 * units) * 4;
+  return (static_cast<size_t>(128) * (r_v / 2 + 4) + units * 256 + 2 * units) * 4;
 }
 
 // d = a * b + d on a pair of fp32 lanes (one packed instruction).
@@ -760,7 +762,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
   const int cu = a.combine_units;
   const int h = blockIdx.x, b0 = blockIdx.y * cu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rw = a.r_v / 2, wpr = rw + 1;   // words per W row, per padded row
+  const int rw = a.r_v / 2, wpr = rw + 4;   // words per W row, per padded row
   uint32_t* Ws = reinterpret_cast<uint32_t*>(csm);
   float* accs = csm + 128 * wpr;                   // [cu][256]
   float* Ms = accs + cu * 256;
@@ -783,8 +785,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
       const int i = tid + j * kCombineThreads;
       if (i < n16) {
         const int e = i / (rw / 4), k = 4 * (i - e * (rw / 4));
-        uint32_t* d = Ws + e * wpr + k;
-        d[0] = v[j].x; d[1] = v[j].y; d[2] = v[j].z; d[3] = v[j].w;
+        *reinterpret_cast<uint4*>(Ws + e * wpr + k) = v[j];
       }
     }
   }
@@ -906,16 +907,20 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
   float ox[kHalf], oy[kHalf];
 #pragma unroll
   for (int j = 0; j < kHalf; ++j) { ox[j] = 0.f; oy[j] = 0.f; }
-  const uint32_t* wr = Ws + e * wpr;
-#pragma unroll 8
-  for (int k = 0; k < rw; ++k) {
-    const uint32_t w2 = wr[k];
-    const float wlo = __uint_as_float(w2 << 16), whi = __uint_as_float(w2 & 0xFFFF0000u);
+  const uint4* wr = reinterpret_cast<const uint4*>(Ws + e * wpr);
+#pragma unroll 2
+  for (int k4 = 0; k4 < rw / 4; ++k4) {   // columns 8 k4 .. 8 k4 + 7
+    float wf[8];
+    unpack_bf16x8(wr[k4], wf);
 #pragma unroll
     for (int j = 0; j < kHalf; ++j) {
       if (j0 + j < cu) {   // accs holds cu units
-        const float2 av = *reinterpret_cast<const float2*>(accs + (j0 + j) * 256 + 2 * k);
-        fma_pair(ox[j], oy[j], av.x, av.y, wlo, whi);
+        const float4* ap = reinterpret_cast<const float4*>(accs + (j0 + j) * 256) + 2 * k4;
+        const float4 a0 = ap[0], a1 = ap[1];
+        fma_pair(ox[j], oy[j], a0.x, a0.y, wf[0], wf[1]);
+        fma_pair(ox[j], oy[j], a0.z, a0.w, wf[2], wf[3]);
+        fma_pair(ox[j], oy[j], a1.x, a1.y, wf[4], wf[5]);
+        fma_pair(ox[j], oy[j], a1.z, a1.w, wf[6], wf[7]);
       }
     }
   }
@@ -1151,7 +1156,9 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
   const int which = (wide ? 2 : 0) + (narrow_v ? 1 : 0);
   void (*const kern[4])(DecodeArgs) = {decode_combine_kernel<128, 8>, decode_combine_kernel<128, 2>,
                                        decode_combine_kernel<256, 8>, decode_combine_kernel<256, 2>};
-  const size_t csmem = combine_smem_bytes(a.r_v, a.combine_units);
+  // at least 76 KB: two blocks per SM, so the blocks, placed as the decode grid's CTAs
+  // leave their SMs, spread over more of them
+  const size_t csmem = std::max<size_t>(combine_smem_bytes(a.r_v, a.combine_units), 76 * 1024);
   static size_t cconfigured[4] = {0, 0, 0, 0};
   if (cconfigured[which] < csmem) {
     cudaError_t e = cudaFuncSetAttribute(kern[which], cudaFuncAttributeMaxDynamicSharedMemorySize,
