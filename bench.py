@@ -44,9 +44,9 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # layer (ouro_rho4_b8_16k); a workload takes the capture of its context length.
 # Valid only for the decode source whose sha256 starts with TRAFFIC_SRC_SHA; any other
 # source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = {4096: (263.983104e6 + 3.294720e6) / (31042 * 16),
-                          16384: (1080.887296e6 + 3.670272e6) / (8 * 16384 * 16)}
-TRAFFIC_SRC_SHA = "5202cd14c4a209f0"
+TRAFFIC_PER_TOKEN_HEAD = {4096: (263.992064e6 + 2.904064e6) / (31042 * 16),
+                          16384: (1080.888064e6 + 3.384576e6) / (8 * 16384 * 16)}
+TRAFFIC_SRC_SHA = "9882cac615125235"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D score kernel (the dominant one of the LLA-2D call), per
 # latent token (all heads), from the 32-sequence variant of the LLA-2D layer; valid
@@ -66,8 +66,8 @@ TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
 DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
 # Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores),
 # from the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.464064e6 + 3.409408e6) / (64 * 4096 * 16)
-TRAFFIC_DEC_SMALL_SRC_SHA = "5577288d0b0dc301"
+TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.399808e6 + 2.981376e6) / (64 * 4096 * 16)
+TRAFFIC_DEC_SMALL_SRC_SHA = "0f6f97446d1053e5"
 DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_small.cu")
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
