@@ -424,7 +424,9 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   const uint32_t box_rows = static_cast<uint32_t>(cache.bt && cache.page_size < kTile ? cache.page_size : kTile);
   if (small_path(dims)) {
     // small ranks: positions split over the CTAs, every head of a position in one CTA
-    make_decode_small_plan(H, dims->r_k, dims->r_v, &a.splan);
+    // pages of 8..64 tokens: one copy per page for a whole head set, if it fits
+    if (!(cache.bt && make_decode_small_setpage_plan(H, dims->r_k, dims->r_v, cache.page_size, &a.splan)))
+      make_decode_small_plan(H, dims->r_k, dims->r_v, &a.splan);
     a.pos_major = 1;
     a.trig16 = reinterpret_cast<uint32_t*>(ws + wl.trig16);
     a.trig_rows = decode_small_trig_rows(cache.L_max, rope_len);

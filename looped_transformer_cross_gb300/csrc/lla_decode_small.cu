@@ -252,7 +252,11 @@ __global__ void __launch_bounds__(kSZThreads) decode_small_z_kernel(const __grid
 
 // kPage: 0 dense cache, 1 page pool with pages of a multiple of 128 tokens (a
 // head-tile inside one page: one pair of copies), 2 page pool of any other page size
-// (a head-tile's rows copied page by page, the copies spread over the producer warp)
+// (a head-tile's rows copied page by page, the copies spread over the producer warp),
+// 3 page pool with pages of 8..64 tokens in the set-page layout: a ring slot holds
+// one head set's tile, [K: page][head][row] then [V: page][head][row], filled with
+// one pair of copies per page (the set's heads are contiguous in a page), so the
+// copies are nwg times fewer and larger; every epilogue group reads every slot.
 template <int RK, int RV, int kPage>
 __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int KB = RK * 2, VB = RV * 2; // bytes of a latent K / V row
@@ -328,7 +332,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
   // ---------------------------------------------------------- set-up
   auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
   if (tid == 0) {
-    for (int s = 0; s < P.NS; ++s) { mbar_init(bar(misc->full[s]), 1); mbar_init(bar(misc->empty[s]), 4); }
+    for (int s = 0; s < P.NS; ++s) {
+      mbar_init(bar(misc->full[s]), 1);
+      mbar_init(bar(misc->empty[s]), kPage == 3 ? 4 * nwg : 4);
+    }
     for (int s = 0; s < nsets; ++s) { mbar_init(bar(misc->img_full[s]), 1); mbar_init(bar(misc->img_empty[s]), 1); }
     mbar_init(bar(misc->trig_full[0]), 4 * nwg);
     mbar_init(bar(misc->trig_full[1]), 4 * nwg);
@@ -356,7 +363,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
     // with two plain bulk copies of the rows below the sequence length.  With a
     // paged cache the whole warp runs the loop (lane 0 waits, the warp follows its
     // decision) and lane i issues the copies of the tile's i-th page.
-    constexpr bool kWarp = kPage == 2;
+    constexpr bool kWarp = kPage >= 2;
     auto pwait = [&](uint32_t b, uint32_t parity) -> bool {
       if constexpr (kWarp) return warp_wait(b, parity, abort, a.status);
       else return mbar_wait(b, parity, abort, a.status);
@@ -392,6 +399,28 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
           zrows = a.page_size;
           y0 -= static_cast<int64_t>(lp) * a.page_size;
         }
+        if constexpr (kPage == 3) {
+          // one slot per head set: lane i copies page lp0 + i of the tile for the
+          // set's heads (K and V), every copy completing on the slot's barrier
+          const int lg = P.log2P, pg = 1 << lg;
+          const int np = (static_cast<int>(rows) + pg - 1) >> lg;
+          const int64_t lp0 = y0 >> lg;
+          const uint32_t kbytes = static_cast<uint32_t>(nwg * KB) << lg, vbytes = static_cast<uint32_t>(nwg * VB) << lg;
+          for (int s = 0; s < nsets && ok; ++s) {
+            if (!(ok = pwait(bar(misc->empty[sp.slot]), sp.phase ^ 1u))) break;
+            const uint32_t fb = bar(misc->full[sp.slot]);
+            const uint32_t dst = sbase + P.ring + sp.slot * P.slot;
+            if (lane == 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(np) * (kbytes + vbytes));
+            __syncwarp();
+            for (int i = lane; i < np; i += 32) {
+              const int64_t r0 = (static_cast<int64_t>(page_of(a, w.b, static_cast<int>(lp0 + i))) * H + s * nwg) << lg;
+              bulk_load(dst + i * kbytes, static_cast<const uint8_t*>(a.cache_k) + r0 * KB, kbytes, fb);
+              bulk_load(dst + nwg * P.k_tile + i * vbytes, static_cast<const uint8_t*>(a.cache_v) + r0 * VB, vbytes, fb);
+            }
+            ++issued;
+            sp.next(1, P.NS);
+          }
+        } else
         for (int h = 0; h < H && ok; ++h) {
           if (!(ok = pwait(bar(misc->empty[sp.slot]), sp.phase ^ 1u))) break;
           const uint32_t fb = bar(misc->full[sp.slot]);
@@ -528,7 +557,17 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
       trig_write(w1, 1);
     }
 
-    SlotPos sp{wg, 0u};   // ring slot of this group's next head-tile (every nwg-th)
+    // ring slot of this group's next head-tile (every nwg-th; with set slots every one)
+    SlotPos sp{kPage == 3 ? 0 : wg, 0u};
+    // set-page layout: byte offset of this head's K row `row` and of V row r in a slot
+    const int lgP = kPage == 3 ? P.log2P : 0;
+    const uint32_t krow3 = kPage == 3 ? static_cast<uint32_t>(((row >> lgP) * nwg * KB << lgP) +
+                                                              ((wg << lgP) + (row & ((1 << lgP) - 1))) * KB)
+                                      : 0u;
+    auto vrow3 = [&](int r) -> uint32_t {
+      return static_cast<uint32_t>(nwg * P.k_tile + ((r >> lgP) * nwg * VB << lgP) +
+                                   ((wg << lgP) + (r & ((1 << lgP) - 1))) * VB);
+    };
     SlotPos gp{0, 0u};    // G buffer of the next head set
     const uint32_t gz = kGCol + wg * RK, gbias = kGCol + nwg * RK + 2 * wg;   // this head's G columns
     bool ok = true;
@@ -582,7 +621,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
 #pragma unroll
         for (int c = 0; c < RK / 8; ++c) {
           float x[8];
-          unpack_bf16x8(*reinterpret_cast<const uint4*>(kt + row * KB + 16 * c), x);
+          if constexpr (kPage == 3)
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(kt + krow3 + 16 * c), x);
+          else
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(kt + row * KB + 16 * c), x);
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             s0 = fmaf(x[e], g[8 * c + e], s0);
@@ -605,8 +647,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
         // ---- rows past the sequence end hold stale data: zero them (own row)
         if (nvalid < kTile) {
           if (!valid) {
+            uint8_t* vr = kPage == 3 ? const_cast<uint8_t*>(kt) + vrow3(row) : vt + row * VB;
 #pragma unroll
-            for (int c = 0; c < VB / 16; ++c) *reinterpret_cast<uint4*>(vt + row * VB + 16 * c) = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < VB / 16; ++c) *reinterpret_cast<uint4*>(vr + 16 * c) = make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
         }
@@ -618,7 +661,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
         for (int i = 0; i < LPR; ++i) {
           const int tk = RPL * i + rg;
           const float pv = __shfl_sync(0xffffffffu, p, tk);
-          const uint2 v = *reinterpret_cast<const uint2*>(vt + (32 * q + tk) * VB + 8 * cg);
+          const uint2 v = kPage == 3 ? *reinterpret_cast<const uint2*>(kt + vrow3(32 * q + tk) + 8 * cg)
+                                     : *reinterpret_cast<const uint2*>(vt + (32 * q + tk) * VB + 8 * cg);
           a4[0] = fmaf(pv, __uint_as_float(v.x << 16), a4[0]);
           a4[1] = fmaf(pv, __uint_as_float(v.x & 0xFFFF0000u), a4[1]);
           a4[2] = fmaf(pv, __uint_as_float(v.y << 16), a4[2]);
@@ -633,7 +677,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) decode_small_kernel(const __
         if (nvalid < kTile) fence_proxy_async_smem();   // zeroed rows before the next bulk copy
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(misc->empty[sp.slot]));
-        sp.next(nwg, P.NS);
+        sp.next(kPage == 3 ? 1 : nwg, P.NS);
 
         // ---- fold into the warp's state; a run's last tile writes the record
         // (m, l, -, -, acc) of (sequence, head, CTA, warp)
@@ -685,10 +729,12 @@ template <int RK, int RV>
 cudaError_t launch_small_instance(const DecodeArgs& a, cudaStream_t s) {
   // the dense-cache instantiation carries no page lookup in its producer, the
   // whole-page one no per-page loop
-  const int page = a.block_table == nullptr ? 0 : a.page_size % kTile == 0 ? 1 : 2;
-  auto kern = page == 0 ? decode_small_kernel<RK, RV, 0>
-                        : page == 1 ? decode_small_kernel<RK, RV, 1> : decode_small_kernel<RK, RV, 2>;
-  static int configured[3] = {0, 0, 0};
+  const int page = a.block_table == nullptr ? 0 : a.page_size % kTile == 0 ? 1 : a.splan.log2P > 0 ? 3 : 2;
+  auto kern = page == 0   ? decode_small_kernel<RK, RV, 0>
+              : page == 1 ? decode_small_kernel<RK, RV, 1>
+              : page == 2 ? decode_small_kernel<RK, RV, 2>
+                          : decode_small_kernel<RK, RV, 3>;
+  static int configured[4] = {0, 0, 0, 0};
   if (configured[page] < a.splan.bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.splan.bytes);
     if (e != cudaSuccess) return e;
@@ -743,6 +789,27 @@ bool make_decode_small_plan(int H, int r_k, int r_v, DecodeSmallPlan* p) {
   p->ml = off;   off += ml;
   p->misc = off; off += kSmallMiscBytes;
   p->bytes = off + 1024;
+  return p->bytes <= kSmemLimit;
+}
+
+bool make_decode_small_setpage_plan(int H, int r_k, int r_v, int page_size, DecodeSmallPlan* p) {
+  if (page_size != 8 && page_size != 16 && page_size != 32 && page_size != 64) return false;
+  if (!make_decode_small_plan(H, r_k, r_v, p)) return false;
+  auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  const int fixed = p->bytes - p->NS * p->slot;   // everything but the ring
+  const int slot = al(p->nwg * (p->k_tile + p->v_tile), 1024);
+  const int NS = std::min((kSmemLimit - fixed) / slot, kSmallMaxNS);
+  if (NS < 2) return false;
+  const int shift = NS * slot - p->NS * p->slot;   // ring growth (the ring precedes acc, ml, misc)
+  p->slot = slot;
+  p->NS = NS;
+  p->acc += shift;
+  p->ml += shift;
+  p->misc += shift;
+  p->bytes += shift;
+  int lg = 0;
+  while ((1 << lg) < page_size) ++lg;
+  p->log2P = lg;
   return p->bytes <= kSmemLimit;
 }
 

@@ -50,6 +50,8 @@ struct DecodeSmallPlan {
   int NS;                            // ring slots (a multiple of nwg)
   int imgs, ring, acc, ml, misc;
   int bytes;                         // total dynamic smem incl. alignment slack
+  int log2P;                         // set-page layout (pages of 8..64 tokens): log2 of the page
+                                     // size, each ring slot one head set's tile; 0 otherwise
 };
 
 constexpr int kSmallThreads = 576;      // producer, MMA issuer, 4 x 4 epilogue warps
@@ -162,6 +164,10 @@ struct DecodeMaps {
 
 bool make_decode_plan(int r_k, int r_v, DecodePlan* p);
 bool make_decode_small_plan(int H, int r_k, int r_v, DecodeSmallPlan* p);
+// The small-rank kernel over a page pool with pages of 8, 16, 32 or 64 tokens:
+// ring slots of a whole head set, filled with one copy per page for the set's heads
+// (contiguous in the pool).  False if two such slots do not fit.
+bool make_decode_small_setpage_plan(int H, int r_k, int r_v, int page_size, DecodeSmallPlan* p);
 size_t decode_small_img_stride(int H, int r_k);   // bytes per (sequence, head set) image
 int64_t decode_small_trig_rows(int64_t L_max, int64_t rope_len);
 cudaError_t launch_decode_small_bf16(const DecodeArgs& a, cudaStream_t s);

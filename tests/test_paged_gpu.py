@@ -119,6 +119,22 @@ def test_paged_decode_small_rank_kernel(style, P):
         _check(w, inp, pk, pv, bt, P, t, style)
 
 
+@pytest.mark.parametrize("H,P", [(4, 8), (4, 32), (4, 64), (6, 16), (16, 16)])
+def test_paged_decode_small_rank_set_pages(H, P):
+    """Pages of 8..64 tokens on the small-rank kernel take the set-page layout: one
+    copy per page for a whole head set (its heads lie together in a page), every
+    epilogue group reading every ring slot; two-head sets (H = 6) and four-head sets,
+    a last tile of a few rows in a part-filled page, an empty sequence."""
+    w = workload(T=2, H=H, r_k=16, r_v=32, B=4, L_max=300)
+    lens = [300, 128, 0, 5]
+    inp = make_decode_inputs(w, 730 + H + P, device="cuda", seq_lens=torch.tensor(lens, dtype=torch.int32))
+    assert lla.decode_kernel(lla_dims(w)) == "small-rank"
+    bt, npg = _table(lens, P, math.ceil(w.L_max / P), 731 + P)
+    pk, pv = _pools(inp, bt, P, lens, npg)
+    for t in range(w.T):
+        _check(w, inp, pk, pv, bt, P, t)
+
+
 @pytest.mark.parametrize("P", [1, 16])
 def test_paged_decode_fp32_any_page_size(P):
     """fp32 mode takes any page size, down to the one-token pages of the page's own
