@@ -59,11 +59,10 @@ DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla
 TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.876544e6 + 3.633920e6) / (64 * 4096 * 16)
 TRAFFIC_SMALL_SRC_SHA = "6579fd99196d23a6"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
-# Same for decoupled_bf16_kernel, per latent token-head (latent K and V rows plus the
-# rotary key), from the 8-sequence variant of the rho = 4 layer.
-TRAFFIC_DEC_PER_TOKEN_HEAD = (320.807936e6 + 3.610112e6) / (31042 * 16)
-TRAFFIC_DEC_SRC_SHA = "3d93ef124467072d"
-DECOUPLED_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled.cu")
+# Same for decoupled_tile_kernel (the tensor-core decoupled kernel at larger ranks),
+# from the 8-sequence variant of the rho = 4 layer (ouro1.4b_rho4_b8_4k).
+TRAFFIC_DEC_TILE_PER_TOKEN_HEAD = (326.040320e6 + 3.235328e6) / (31042 * 16)
+TRAFFIC_DEC_TILE_SRC_SHA = "4225a449fd2a407d"
 # Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores),
 # from the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
 TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.399808e6 + 2.981376e6) / (64 * 4096 * 16)
@@ -577,12 +576,13 @@ def measure(args, w, steps, layers, dist_on, rank, world, device, legs=True):
         import hashlib
         small = lla.decoupled_kernel(step.dm, D_ROPE) == "small-rank"
         src_file, sha, per_th = ((DECOUPLED_SMALL_SRC, TRAFFIC_DEC_SMALL_SRC_SHA, TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD)
-                                 if small else (DECOUPLED_SRC, TRAFFIC_DEC_SRC_SHA, TRAFFIC_DEC_PER_TOKEN_HEAD))
+                                 if small else (DECOUPLED_SMALL_SRC, TRAFFIC_DEC_TILE_SRC_SHA,
+                                                TRAFFIC_DEC_TILE_PER_TOKEN_HEAD))
         with open(src_file, "rb") as f:
             same_src = sha is not None and hashlib.sha256(f.read()).hexdigest().startswith(sha)
         traffic = per_th * step.tokens * w.H if same_src else None
-        main = "decoupled_small_kernel" if small else "decoupled_bf16_kernel"
-        query = "decoupled_small_z_kernel" if small else "decoupled_query_kernel"
+        main = "decoupled_small_kernel" if small else "decoupled_tile_kernel"
+        query = "decoupled_small_z_kernel"
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic, "traffic_kernel": main,
                 "kernel": "lla_decode_attn_decoupled (%s + %s + decode_combine_kernel)" % (query, main),

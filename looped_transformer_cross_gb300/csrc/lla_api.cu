@@ -201,7 +201,7 @@ const char* lla_decoupled_kernel(const lla_dims* dims, int d_rope) {
   if (check_dims(dims) != LLA_OK || dims->variant != LLA_PER_HEAD || d_rope != 64) return nullptr;
   if (dims->dtype == LLA_F32) return "fp32";
   if (decoupled_small_supported(dims->H, dims->r_k, dims->r_v)) return "small-rank";
-  return decoupled_ring_slots(dims->r_k, dims->r_v) >= 2 ? "tile" : nullptr;
+  return decoupled_tile_supported(dims->r_k, dims->r_v) ? "tile" : nullptr;
 }
 
 size_t lla_workspace_size(const lla_dims* dims, int B, int64_t L_max, int max_N) {
@@ -504,13 +504,19 @@ extern "C" {
 size_t lla_decoupled_workspace_size(const lla_dims* dims, int d_rope, int B, int64_t L_max) {
   if (check_dims(dims) != LLA_OK || dims->variant != LLA_PER_HEAD || d_rope != 64 || B < 0 || L_max < 0) return 0;
   size_t off = 256;   // status word
-  if (dims->dtype == LLA_BF16 && decoupled_small_supported(dims->H, dims->r_k, dims->r_v)) {
-    // small-rank kernel: records per (sequence + CTA, head, warp) (a CTA index is
-    // below min(kMaxGrid, positions)), B images per (sequence, head), sc b0 per
-    // (sequence, head), the fp32 RoPE table [64][trig_rows]
+  const bool small = dims->dtype == LLA_BF16 && decoupled_small_supported(dims->H, dims->r_k, dims->r_v);
+  if (small || (dims->dtype == LLA_BF16 && decoupled_tile_supported(dims->r_k, dims->r_v))) {
+    // tensor-core kernels: records per (sequence + CTA, head, warp) (small ranks; a
+    // CTA index is below min(kMaxGrid, positions)) or per (unit + CTA, warp) (tile
+    // kernel, eight warps), B images per (sequence, head), sc b0 per (sequence,
+    // head), the fp32 RoPE table [64][trig_rows]
     const size_t max_pos = static_cast<size_t>(B) * ((L_max + kTile - 1) / kTile);
-    off += al256((static_cast<size_t>(B) + std::min<size_t>(kMaxGrid, std::max<size_t>(1, max_pos))) * dims->H *
-                 kRecordsPerCta * (dims->r_v + kRecordHead) * 4);
+    if (small)
+      off += al256((static_cast<size_t>(B) + std::min<size_t>(kMaxGrid, std::max<size_t>(1, max_pos))) * dims->H *
+                   kRecordsPerCta * (dims->r_v + kRecordHead) * 4);
+    else
+      off += al256((static_cast<size_t>(B) * dims->H + kMaxGrid) * kDecoupledTileRecords *
+                   (dims->r_v + kRecordHead) * 4);
     off += al256(static_cast<size_t>(B) * dims->H * decoupled_small_img_stride(dims->r_k));
     off += al256(static_cast<size_t>(B) * dims->H * 4);
     off += al256(static_cast<size_t>(decoupled_small_trig_rows(L_max)) * 64 * 4);
@@ -576,15 +582,20 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.partials = reinterpret_cast<float*>(ws + 256);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dims->dtype == LLA_BF16 && decoupled_small_supported(H, dims->r_k, dims->r_v)) {
-    // small ranks: rotary branch and content score on the tensor cores, positions
-    // split over the CTAs with every head of a position in one CTA
+  const bool small = dims->dtype == LLA_BF16 && decoupled_small_supported(H, dims->r_k, dims->r_v);
+  if (small || (dims->dtype == LLA_BF16 && decoupled_tile_supported(dims->r_k, dims->r_v))) {
+    // rotary branch and content score on the tensor cores: small ranks with positions
+    // split over the CTAs and every head of a position in one CTA, other ranks with
+    // 128-token tiles of one (sequence, head) split over the CTAs
     const int sms = sm_count();
     if (sms <= 0) return LLA_ERR_CUDA;
     const int64_t max_pos = static_cast<int64_t>(cache.B) * ((cache.L_max + kTile - 1) / kTile);
-    uint8_t* p = ws + 256 + al256((static_cast<size_t>(cache.B) +
-                                   std::min<size_t>(kMaxGrid, std::max<int64_t>(1, max_pos))) *
-                                  H * kRecordsPerCta * (dims->r_v + kRecordHead) * 4);
+    uint8_t* p = ws + 256 +
+                 (small ? al256((static_cast<size_t>(cache.B) +
+                                 std::min<size_t>(kMaxGrid, std::max<int64_t>(1, max_pos))) *
+                                H * kRecordsPerCta * (dims->r_v + kRecordHead) * 4)
+                        : al256((static_cast<size_t>(cache.B) * H + kMaxGrid) * kDecoupledTileRecords *
+                                (dims->r_v + kRecordHead) * 4));
     a.zimg = p;
     a.zimg_stride = static_cast<int64_t>(decoupled_small_img_stride(dims->r_k));
     p += al256(static_cast<size_t>(cache.B) * H * a.zimg_stride);
@@ -592,9 +603,10 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
     p += al256(static_cast<size_t>(cache.B) * H * 4);
     a.trigT = reinterpret_cast<float*>(p);
     a.trig_rows = decoupled_small_trig_rows(cache.L_max);
-    a.pos_major = 1;
-    a.records_per_cta = kRecordsPerCta;
-    a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_pos)));
+    a.pos_major = small ? 1 : 0;
+    a.records_per_cta = small ? kRecordsPerCta : kDecoupledTileRecords;
+    const int64_t work = small ? max_pos : max_pos * H;   // positions, or head-tiles
+    a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, work)));
     a.combine_units = decode_combine_units(cache.B, H, sms);
     const uint64_t units = static_cast<uint64_t>(cache.B) * H, rows = static_cast<uint64_t>(cache.L_max);
     DecoupledMaps maps;
@@ -602,7 +614,9 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
     if (!make_map_3d(&maps.kr, k_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, rows, units, 64, kTile, 1) ||
         !make_map_3d(&maps.ck, cache.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_k, rows, units, 16, kTile, 1))
       return LLA_ERR_CUDA;
-    return launch_decoupled_small(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+    return (small ? launch_decoupled_small(a, maps, s) : launch_decoupled_tile(a, maps, s)) == cudaSuccess
+               ? LLA_OK
+               : LLA_ERR_CUDA;
   }
   uint8_t* tail = ws + 256 + al256((static_cast<size_t>(cache.B) * H + kMaxGrid) * kDecoupledRecords *
                                    (dims->r_v + kRecordHead) * 4);

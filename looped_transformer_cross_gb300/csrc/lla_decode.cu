@@ -814,13 +814,14 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
   // Tile-major split (per-head kernel): CTA ranges over the flat (sequence, head,
   // tile) list, records ((b H + h) + c) R + warp.  Position-major split (small-rank
   // kernels): ranges over (sequence, tile) with every head inner, records
-  // ((b + c) H + h) R + warp.  R = 4 (one per epilogue warp) or 1 (decoupled tile
-  // kernel: its warps are merged within the CTA).  A unit's records: one per (CTA c
+  // ((b + c) H + h) R + warp.  R = 4 (one per epilogue warp), 8 (decoupled tile-major
+  // tensor-core kernel: two groups of four) or 1 (decoupled CUDA-core kernel: its
+  // warps are merged within the CTA).  A unit's records: one per (CTA c
   // in [c0, c1], epilogue warp); a warp that saw no token of the unit in that CTA
   // wrote m = -inf, l = 0, acc = 0.  (CTA ranges are [c per, (c + 1) per): only CTAs
   // past the last tile are empty, never one between c0 and c1.)
   constexpr int kUPW = kCombineThreads == 256 ? 2 : 1;   // units per warp (cu <= 16 / <= 4)
-  const int R = a.records_per_cta, rsh = R == 4 ? 2 : 0;   // R is 4 or 1
+  const int R = a.records_per_cta, rsh = R == 8 ? 3 : R == 4 ? 2 : 0;   // R is 8, 4 or 1
   const int rs = a.r_v + kRecordHead;
   const long long cstride = a.pos_major ? static_cast<long long>(R) * a.H : R;
   long long ubase[kUPW];

@@ -192,15 +192,17 @@ __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __g
   // the decode grid may start its set-up now; it waits for this grid before it
   // copies an image or reads the table
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float Ws[kHeadDim * 33];            // W_up,k,t[h] fp32 [128][r_k] (row stride r_k + 1)
+  // W_up,k,t[h] as bf16 [128][r_k] (row stride r_k + 2, r_k <= 128); the table
+  // blocks use the same bytes as an fp32 [64][kTrigJ + 1] transpose tile
+  __shared__ __align__(16) uint8_t wraw[kHeadDim * (128 + 2) * 2];
   __shared__ __align__(16) float qc[kDzSeqs][kHeadDim];
   __shared__ float qa[kDzSeqs][kRope / 2], qb[kDzSeqs][kRope / 2];   // sc q'_i0, sc q'_i1
-  __shared__ float wsc[kDzSeqs][32];             // sc w
+  __shared__ float wsc[kDzSeqs][128];            // sc w
   __shared__ bool live[kDzSeqs];
   const int tid = threadIdx.x;
   const int ntb = static_cast<int>((a.trig_rows + kTrigJ - 1) / kTrigJ);
   if (static_cast<int>(blockIdx.x) < ntb) {
-    float* tile = Ws;                            // [64 columns][kTrigJ + 1]
+    float* tile = reinterpret_cast<float*>(wraw);   // [64 columns][kTrigJ + 1]
     const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kTrigJ;
     for (int i = tid; i < kTrigJ * 64; i += kDzThreads) {
       const int jj = i / 64, c = i % 64, f = c >> 1;
@@ -218,16 +220,17 @@ __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __g
   }
   const int u = static_cast<int>(blockIdx.x) - ntb;
   const int h = u % a.H, b0 = (u / a.H) * kDzSeqs;
-  const int rk = a.r_k, ws = rk + 1, nk = rk / 16;
+  const int rk = a.r_k, ws = rk + 2, nk = rk / 16;
+  __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(wraw);
   const float sc = kLog2e * kInvSqrtDR;
   const __nv_bfloat16* W =
       static_cast<const __nv_bfloat16*>(a.w_up_k) + static_cast<int64_t>(h) * kHeadDim * rk;
   for (int i = tid; i < kHeadDim * rk / 8; i += kDzThreads) {
-    float w8[8];
-    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(W) + i), w8);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(W) + i);
+    const __nv_bfloat16* v8 = reinterpret_cast<const __nv_bfloat16*>(&v);
     const int row = (8 * i) / rk, col = (8 * i) % rk;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) Ws[row * ws + col + e] = w8[e];
+    for (int e = 0; e < 8; ++e) Wb[row * ws + col + e] = v8[e];
   }
   const int qrow = kHeadDim + kRope;
   for (int i = tid; i < kDzSeqs * kHeadDim; i += kDzThreads) {
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __g
     const int sb = i / rk, n = i % rk;
     float s = 0.f;
 #pragma unroll 8
-    for (int e = 0; e < kHeadDim; ++e) s = fmaf(qc[sb][e], Ws[e * ws + n], s);
+    for (int e = 0; e < kHeadDim; ++e) s = fmaf(qc[sb][e], __bfloat162float(Wb[e * ws + n]), s);
     wsc[sb][n] = s * sc;
   }
   {
@@ -691,6 +694,447 @@ cudaError_t launch_instance(const DecodeArgs& a, const DecoupledMaps& m, int byt
   return cudaLaunchKernelEx(&cfg, kern, a, m);
 }
 
+
+// ================================================================ tile-major kernel
+// Larger ranks (r_k up to 128, r_v up to 256).  A unit's B image stays small (4 KB +
+// r_k / 16 x 512 B), but a head-tile's rotary and K rows grow (16 KB + r_k x 256 B)
+// and a position's head-tiles no longer fit beside every head's image, so the work
+// is tile-major as in the per-head tile kernel: 128-token tiles over (sequence,
+// head) in contiguous ranges per CTA, the unit's image copied once per unit into
+// one of two buffers.  The MMA chain is the small-rank kernel's.  The V rows do not
+// pass through shared memory: the producer asks L2 for each tile's V rows as it
+// issues the tile's copies, and each epilogue warp reads its 32 tokens' rows with
+// coalesced 4-byte loads (lane = pairs of V columns), keeping sum_j p_j c_v,j for
+// its columns in registers while the unit lasts.  Two epilogue groups take
+// alternate tiles; both walk every tile and close every unit, so each warp writes
+// one record per (unit, CTA): eight per (unit, CTA).
+constexpr int kDtThreads = 320;
+constexpr int kDtMaxNS = 8;
+
+struct alignas(16) DtMisc {
+  uint64_t full[kDtMaxNS], empty[kDtMaxNS];   // ring slots (rotary + K tiles), consumed by the MMAs
+  uint64_t img_full[2], img_empty[2];         // unit images (unit parity)
+  uint64_t gfull[kNG], gempty[kNG];           // D buffers (one head-tile each)
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int start_b, start_h, start_t, count;
+  int total_seq_tiles;
+  int scan[kDtThreads];
+};
+
+struct DtPlan {
+  int nk;           // content K-steps (r_k / 16)
+  int img;          // bytes of one image buffer (1024-aligned)
+  int slot;         // ring slot: rotary tile + K latent boxes
+  int NS;           // ring slots
+  int imgs, ring, misc, bytes;
+};
+
+__host__ __device__ inline bool make_dt_plan(int r_k, int r_v, DtPlan* p) {
+  if (r_k < 16 || r_k > 128 || r_k % 16 || r_v < 16 || r_v > 256 || r_v % 16) return false;
+  p->nk = r_k / 16;
+  p->img = al_up(4 * kRotBlock + p->nk * kConBlock, 1024);
+  p->slot = al_up(kRTile + p->nk * kCkBox, 1024);
+  const int misc = al_up(static_cast<int>(sizeof(DtMisc)), 16);
+  int NS = (kSmemLimit - 2 * p->img - misc - 1024) / p->slot;
+  NS = NS < kDtMaxNS ? NS : kDtMaxNS;
+  if (NS < 2) return false;
+  p->NS = NS;
+  int off = 0;
+  p->imgs = off; off += 2 * p->img;
+  p->ring = off; off += NS * p->slot;
+  p->misc = off; off += misc;
+  p->bytes = off + 1024;
+  return p->bytes <= kSmemLimit;
+}
+
+// Walk over head-tiles (sequence b, head h, tile t) in order, skipping empty sequences.
+struct TileWalker {
+  int b, h, t, nb, L;
+};
+
+__device__ __forceinline__ void tile_advance(TileWalker& w, const DecodeArgs& a) {
+  if (++w.t < w.nb) return;
+  w.t = 0;
+  if (++w.h < a.H) return;
+  w.h = 0;
+  while (true) {
+    ++w.b;
+    if (w.b >= a.B) { w.nb = 0; return; }
+    w.L = clamp_len(__ldg(a.seq_lens + w.b), a.L_max);
+    w.nb = (w.L + kTile - 1) / kTile;
+    if (w.nb > 0) return;
+  }
+}
+
+// NPL: pairs of V columns per lane, ceil(r_v / 64)
+template <int NPL>
+__global__ void __launch_bounds__(kDtThreads, 1)
+    decoupled_tile_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ DecoupledMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  DtPlan P;
+  make_dt_plan(a.r_k, a.r_v, &P);
+  const uint32_t sbase = smem_u32(sm);
+  DtMisc* misc = reinterpret_cast<DtMisc*>(sm + P.misc);
+  volatile int* abort = &misc->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.H, NS = P.NS, NK = P.nk;
+  const int VB = a.r_v * 2;   // bytes of a latent V row
+
+  // ---------------------------------------------------------- work range
+  // head-tiles (sequence, head, tile) in order; CTA c takes [c per, (c + 1) per)
+  {
+    const int per_thr = (a.B + kDtThreads - 1) / kDtThreads;
+    const int b0 = min(a.B, tid * per_thr), b1 = min(a.B, b0 + per_thr);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int L0 = __ldg(a.seq_lens + b);
+      if ((L0 < 0 || L0 > a.L_max) && blockIdx.x == 0) record_status(a.status, LLA_ERR_DEVICE_ARG);
+      local += (clamp_len(L0, a.L_max) + kTile - 1) / kTile;
+    }
+    misc->scan[tid] = local;
+    if (tid == 0) misc->abort = 0;
+    __syncthreads();
+    if (warp == 0) {
+      constexpr int kPer = kDtThreads / 32;
+      int v[kPer];
+      int s = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) { v[i] = misc->scan[lane * kPer + i]; s += v[i]; }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      int excl = incl - s;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) { misc->scan[lane * kPer + i] = excl; excl += v[i]; }
+      if (lane == 31) misc->total_seq_tiles = incl;
+    }
+    __syncthreads();
+    const long long total = static_cast<long long>(H) * misc->total_seq_tiles;
+    const long long per = max(1LL, (total + a.grid - 1) / a.grid);
+    const long long f0 = static_cast<long long>(blockIdx.x) * per;
+    const long long f1 = min(total, f0 + per);
+    long long P0 = misc->scan[tid];
+    for (int b = b0; b < b1; ++b) {
+      const int nb = (clamp_len(__ldg(a.seq_lens + b), a.L_max) + kTile - 1) / kTile;
+      if (nb > 0 && f0 < f1 && H * P0 <= f0 && f0 < H * (P0 + nb)) {
+        const long long rem = f0 - H * P0;
+        misc->start_b = b;
+        misc->start_h = static_cast<int>(rem / nb);
+        misc->start_t = static_cast<int>(rem % nb);
+      }
+      P0 += nb;
+    }
+    if (tid == 0) misc->count = static_cast<int>(f1 > f0 ? f1 - f0 : 0);
+    __syncthreads();
+  }
+  const int count = misc->count;
+  if (count == 0) return;
+
+  TileWalker start;
+  start.b = misc->start_b;
+  start.h = misc->start_h;
+  start.t = misc->start_t;
+  start.L = clamp_len(__ldg(a.seq_lens + start.b), a.L_max);
+  start.nb = (start.L + kTile - 1) / kTile;
+
+  // ---------------------------------------------------------- set-up
+  auto bar = [&](const uint64_t& m) { return smem_u32(&m); };
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) { mbar_init(bar(misc->full[s]), 1); mbar_init(bar(misc->empty[s]), 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(bar(misc->img_full[i]), 1); mbar_init(bar(misc->img_empty[i]), 1); }
+    for (int g = 0; g < kNG; ++g) { mbar_init(bar(misc->gfull[g]), 1); mbar_init(bar(misc->gempty[g]), 4); }
+    mbar_init(bar(misc->mma_done), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(&misc->tmem_base), 512);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // the combine grid may be scheduled now; it waits for this grid to complete
+  // before it reads a record
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t tmem = misc->tmem_base;
+
+  if (warp == 0) {
+    // ======================================================== producer
+    // Per unit: its image into buffer unit & 1, once the MMAs of the unit two back
+    // are done with it.  Per head-tile: the rotary tile and the K latent boxes (TMA,
+    // swizzled as the MMA reads them; rows past the cache end read as zero, rows
+    // past the sequence end are masked), and an L2 prefetch of its V rows.
+    if (lane == 0) {
+      prefetch_tmap(&maps.kr);
+      prefetch_tmap(&maps.ck);
+      const uint64_t pol = l2_policy_evict_first();
+      const uint64_t pol_keep = l2_policy_evict_last();
+      TileWalker w = start;
+      SlotPos sp{0, 0u};
+      int unit = -1, issued = 0;
+      bool ok = true;
+      for (int lp = 0; lp < count && ok; ++lp) {
+        const int z = w.b * H + w.h;
+        if (lp == 0 || w.t == 0) {
+          ++unit;
+          const int ib = unit & 1;
+          if (unit >= 2 && !(ok = mbar_wait(bar(misc->img_empty[ib]), ((unit >> 1) - 1) & 1, abort, a.status))) break;
+          if (unit == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // images written
+          const uint32_t fb = bar(misc->img_full[ib]);
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.zimg_stride));
+          bulk_load(sbase + P.imgs + ib * P.img, a.zimg + static_cast<int64_t>(z) * a.zimg_stride,
+                    static_cast<uint32_t>(a.zimg_stride), fb);
+        }
+        if (!(ok = mbar_wait(bar(misc->empty[sp.slot]), sp.phase ^ 1u, abort, a.status))) break;
+        const uint32_t fb = bar(misc->full[sp.slot]);
+        const uint32_t dst = sbase + P.ring + sp.slot * P.slot;
+        const int y = w.t * kTile;
+        const uint32_t rows = static_cast<uint32_t>(min(kTile, w.L - y));
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kRTile + NK * kCkBox));
+        tma_load_3d_hint(dst, &maps.kr, fb, 0, y, z, pol);
+        for (int kb = 0; kb < NK; ++kb) tma_load_3d_hint(dst + kRTile + kb * kCkBox, &maps.ck, fb, 16 * kb, y, z, pol);
+        // the V rows stay in L2 until the epilogue reads them (it reads them with an
+        // evict-first policy, so they leave once used)
+        prefetch_l2_bulk_hint(static_cast<const uint8_t*>(a.cache_v) + (static_cast<int64_t>(z) * a.L_max + y) * VB,
+                              rows * VB, pol_keep);
+        ++issued;
+        sp.next(1, NS);
+        tile_advance(w, a);
+      }
+      // Let every copy this CTA issued land before the CTA can exit.
+      for (int i = max(0, issued - NS); i < issued; ++i) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar(misc->full[i % NS]), (i / NS) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+      for (int u = max(0, unit - 1); u <= unit; ++u) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar(misc->img_full[u & 1]), (u >> 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer
+    // Per head-tile, into the next D buffer: the four rotary MMAs and the content
+    // MMAs (as the small-rank kernel); its commit frees the ring slot and, at the
+    // unit's last tile here, the image buffer.
+    auto agree = [](bool r) { return __all_sync(0xffffffffu, r); };
+    const uint32_t idesc_rot = umma_idesc_bf16(128, 32, false, false);
+    const uint32_t idesc_con = umma_idesc_bf16(128, 16, false, false);
+    const int style = a.rope_style;
+    TileWalker w = start;
+    SlotPos sp{0, 0u}, gp{0, 0u};
+    int unit = -1;
+    bool ok = true;
+    for (int lp = 0; lp < count && ok; ++lp) {
+      const bool unit_end = lp == count - 1 || w.t == w.nb - 1;
+      if (lp == 0 || w.t == 0) {
+        ++unit;
+        if (!(ok = agree(mbar_wait(bar(misc->img_full[unit & 1]), (unit >> 1) & 1, abort, a.status)))) break;
+      }
+      if (!(ok = agree(mbar_wait(bar(misc->full[sp.slot]), sp.phase, abort, a.status)))) break;
+      if (!(ok = agree(mbar_wait(bar(misc->gempty[gp.slot]), gp.phase ^ 1u, abort, a.status)))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + gp.slot * kDCols;
+      const uint32_t ra = sbase + P.ring + sp.slot * P.slot;
+      const uint32_t ib = sbase + P.imgs + (unit & 1) * P.img;
+      const uint64_t a_rot = umma_desc(ra, 16, 1024, kSw128);
+#pragma unroll
+      for (int G = 0; G < 2; ++G)
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          umma_bf16_warp(d + 32 * G, a_rot + 2 * rot_kstep(style, G, kk),
+                         umma_desc(ib + (2 * G + kk) * kRotBlock, 16, 256, kSw32), idesc_rot, kk);
+      for (int kb = 0; kb < NK; ++kb)
+        umma_bf16_warp(d + 64, umma_desc(ra + kRTile + kb * kCkBox, 16, 256, kSw32),
+                       umma_desc(ib + 4 * kRotBlock + kb * kConBlock, 16, 256, kSw32), idesc_con, kb);
+      umma_commit_warp(bar(misc->gfull[gp.slot]));
+      umma_commit_warp(bar(misc->empty[sp.slot]));                       // the slot's rows are read
+      if (unit_end) umma_commit_warp(bar(misc->img_empty[unit & 1]));   // the image is no longer read
+      gp.next(1, kNG);
+      sp.next(1, NS);
+      tile_advance(w, a);
+    }
+    // this warp's MMAs complete before TMEM is released
+    umma_commit_warp(bar(misc->mma_done));
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar(misc->mma_done), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+  } else {
+    // ======================================================== epilogue (warps 2-9)
+    // Group g takes the CTA's head-tiles lp = g mod 2 (D buffers g, g + 2, g + 4);
+    // thread (TMEM quadrant q, lane) owns token row 32 q + lane of a tile, and lane
+    // the V column pairs lane + 32 i of its warp's sum.
+    const int we = warp - 2, g = we >> 2, q = warp & 3;
+    const int row = 32 * q + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const int npairs = a.r_v / 2;
+    const uint64_t pol_v = l2_policy_evict_first();   // V rows: read once
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // table and sc b0 written
+    SlotPos gp{g, 0u};
+    TileWalker w = start;
+    float m = -INFINITY, l = 0.f, qb0 = 0.f;
+    float acc[2 * NPL];
+    bool ok = true;
+    for (int lp = 0; lp < count && ok; ++lp) {
+      const bool unit_start = lp == 0 || w.t == 0;
+      const bool unit_end = lp == count - 1 || w.t == w.nb - 1;
+      const int64_t u = static_cast<int64_t>(w.b) * H + w.h;
+      if (unit_start) {
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int i = 0; i < 2 * NPL; ++i) acc[i] = 0.f;
+        qb0 = __ldg(a.qb0 + u);
+      }
+      if ((lp & 1) == g) {
+        const int nvalid = min(kTile, w.L - w.t * kTile);
+        const bool valid = row < nvalid;
+        // V rows of the warp's tokens (valid ones only; lane = column pairs): the first
+        // 8 tokens' loads go out before anything else of the tile, the other 24 once
+        // the score is formed, so both wait behind other work
+        const int nv = min(32, max(0, nvalid - 32 * q));
+        const uint32_t* vrows = static_cast<const uint32_t*>(a.cache_v) +
+                                (u * a.L_max + static_cast<int64_t>(w.t) * kTile + 32 * q) * npairs;
+        uint32_t va[8][NPL];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+          for (int i = 0; i < NPL; ++i) {
+            const int pr = lane + 32 * i;
+            va[k][i] = k < nv && pr < npairs ? ldg_hint(vrows + static_cast<int64_t>(k) * npairs + pr, pol_v) : 0u;
+          }
+        // cos / sin of this token's position
+        float cs[kRope];
+        {
+          int64_t j = static_cast<int64_t>(w.t) * kTile + row;
+          if (j >= a.trig_rows) j = a.trig_rows - 1;   // past the cache end: masked anyway
+          const float* tp = a.trigT + j;
+#pragma unroll
+          for (int c = 0; c < kRope; ++c) cs[c] = __ldg(tp + c * a.trig_rows);
+        }
+        if (!(ok = warp_wait(bar(misc->gfull[gp.slot]), gp.phase, abort, a.status))) break;
+        tc_fence_after();
+        // ---- s_j = sc b0 + content (hi + lo) + sum_f U_f cos + V_f sin (log2 units),
+        // the 64 (U, V) columns read from TMEM in two halves
+        float x0 = 0.f, x1 = 0.f, y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f, t0 = 0.f, t1 = 0.f;
+        float uc[2];
+        {
+          const uint32_t gb = tmem + lane_base + gp.slot * kDCols;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float uu[32];
+            tmem_ld_x32(gb + 32 * hf, uu);
+            if (hf == 1) tmem_ld_x2(gb + 64, uc);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              fma_pair(x0, x1, uu[2 * i], uu[2 * i + 1], cs[32 * hf + 2 * i], cs[32 * hf + 2 * i + 1]);
+              fma_pair(y0, y1, uu[2 * i + 2], uu[2 * i + 3], cs[32 * hf + 2 * i + 2], cs[32 * hf + 2 * i + 3]);
+              fma_pair(z0, z1, uu[2 * i + 4], uu[2 * i + 5], cs[32 * hf + 2 * i + 4], cs[32 * hf + 2 * i + 5]);
+              fma_pair(t0, t1, uu[2 * i + 6], uu[2 * i + 7], cs[32 * hf + 2 * i + 6], cs[32 * hf + 2 * i + 7]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(misc->gempty[gp.slot]));
+        gp.next(kEpiGroups, kNG);
+        const float sr = ((x0 + x1) + (y0 + y1)) + ((z0 + z1) + (t0 + t1));
+        const float s = valid ? (qb0 + (uc[0] + uc[1])) + sr : -INFINITY;
+
+        // ---- online softmax per warp, reference raised lazily (by more than 2^8)
+        const float mt = warp_max_redux(s);
+        if (mt > m + kRescaleLog2) {
+          const float alpha = m == -INFINITY ? 0.f : exp2f(m - mt);
+          l *= alpha;
+#pragma unroll
+          for (int i = 0; i < 2 * NPL; ++i) acc[i] *= alpha;
+          m = mt;
+        }
+        const float p = valid ? exp2f(s - m) : 0.f;
+        l += warp_sum(p);
+
+        // ---- sum_j p_j c_v,j (a token past the sequence end has p = 0 and v = 0)
+        if (nv > 8) {
+          uint32_t vb[24][NPL];
+#pragma unroll
+          for (int k = 0; k < 24; ++k)
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+              const int pr = lane + 32 * i;
+              vb[k][i] = 8 + k < nv && pr < npairs ? ldg_hint(vrows + static_cast<int64_t>(8 + k) * npairs + pr, pol_v) : 0u;
+            }
+#pragma unroll
+          for (int k = 0; k < 24; ++k) {
+            const float pv = __shfl_sync(0xffffffffu, p, 8 + k);
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+              acc[2 * i] = fmaf(pv, __uint_as_float(vb[k][i] << 16), acc[2 * i]);
+              acc[2 * i + 1] = fmaf(pv, __uint_as_float(vb[k][i] & 0xFFFF0000u), acc[2 * i + 1]);
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float pv = __shfl_sync(0xffffffffu, p, k);
+#pragma unroll
+          for (int i = 0; i < NPL; ++i) {
+            acc[2 * i] = fmaf(pv, __uint_as_float(va[k][i] << 16), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(pv, __uint_as_float(va[k][i] & 0xFFFF0000u), acc[2 * i + 1]);
+          }
+        }
+      }
+      if (unit_end) {
+        // record (m, l, -, -, acc) of (unit, CTA, group, warp); a group that took no
+        // tile of the unit here writes m = -inf, l = 0, acc = 0
+        float* rec = a.partials +
+                     ((u + blockIdx.x) * kDecoupledTileRecords + g * 4 + q) * (a.r_v + kRecordHead);
+        if (lane == 0) { rec[0] = m; rec[1] = l; }
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int pr = lane + 32 * i;
+          if (pr < npairs) *reinterpret_cast<float2*>(rec + kRecordHead + 2 * pr) = make_float2(acc[2 * i], acc[2 * i + 1]);
+        }
+      }
+      tile_advance(w, a);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int NPL>
+cudaError_t launch_tile_instance(const DecodeArgs& a, const DecoupledMaps& m, int bytes, cudaStream_t s) {
+  auto kern = decoupled_tile_kernel<NPL>;
+  static int configured = 0;
+  if (configured < bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    configured = bytes;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kDtThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, m);
+}
+
 }  // namespace
 
 bool decoupled_small_supported(int H, int r_k, int r_v) {
@@ -701,6 +1145,28 @@ bool decoupled_small_supported(int H, int r_k, int r_v) {
 size_t decoupled_small_img_stride(int r_k) { return static_cast<size_t>(4 * kRotBlock + (r_k / 16) * kConBlock); }
 
 int64_t decoupled_small_trig_rows(int64_t L_max) { return (L_max + kTile - 1) / kTile * kTile; }
+
+bool decoupled_tile_supported(int r_k, int r_v) {
+  DtPlan p;
+  return make_dt_plan(r_k, r_v, &p);
+}
+
+cudaError_t launch_decoupled_tile(const DecodeArgs& a, const DecoupledMaps& m, cudaStream_t s) {
+  DtPlan P;
+  if (!make_dt_plan(a.r_k, a.r_v, &P) || a.records_per_cta != kDecoupledTileRecords) return cudaErrorInvalidValue;
+  const int trig_blocks = static_cast<int>((a.trig_rows + kTrigJ - 1) / kTrigJ);
+  const int z_blocks = a.H * ((a.B + kDzSeqs - 1) / kDzSeqs);
+  cudaError_t e = launch_pdl(decoupled_small_z_kernel, dim3(z_blocks + trig_blocks), dim3(kDzThreads), 0, s, a);
+  if (e != cudaSuccess) return e;
+  switch ((a.r_v + 63) / 64) {
+    case 1: e = launch_tile_instance<1>(a, m, P.bytes, s); break;
+    case 2: e = launch_tile_instance<2>(a, m, P.bytes, s); break;
+    case 3: e = launch_tile_instance<3>(a, m, P.bytes, s); break;
+    default: e = launch_tile_instance<4>(a, m, P.bytes, s); break;
+  }
+  if (e != cudaSuccess) return e;
+  return launch_decode_combine(a, s);
+}
 
 cudaError_t launch_decoupled_small(const DecodeArgs& a, const DecoupledMaps& m, cudaStream_t s) {
   DsPlan P;

@@ -197,6 +197,12 @@ bool decoupled_small_supported(int H, int r_k, int r_v);
 size_t decoupled_small_img_stride(int r_k);
 int64_t decoupled_small_trig_rows(int64_t L_max);
 cudaError_t launch_decoupled_small(const DecodeArgs& a, const DecoupledMaps& m, cudaStream_t s);
+// Other bf16 shapes with r_k <= 128, r_v <= 256: the same MMA chain over 128-token
+// tiles of one (sequence, head) (tile-major split, a.pos_major = 0, eight records
+// per CTA), V read from L2 by the epilogue.  Same workspace regions as above.
+constexpr int kDecoupledTileRecords = 8;
+bool decoupled_tile_supported(int r_k, int r_v);
+cudaError_t launch_decoupled_tile(const DecodeArgs& a, const DecoupledMaps& m, cudaStream_t s);
 // fp32 softmax over a.scores and the V path (shared by the fp32 decode paths).
 cudaError_t launch_decode_f32_values(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decoupled_f32(const DecodeArgs& a, cudaStream_t s);

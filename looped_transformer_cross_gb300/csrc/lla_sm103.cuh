@@ -342,6 +342,26 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Ask L2 to fetch [src, src + bytes) (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
+// Same, with an L2 eviction-priority policy for the fetched lines.
+__device__ __forceinline__ void prefetch_l2_bulk_hint(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+// Read-only 32-bit load with an L2 eviction-priority policy.
+__device__ __forceinline__ uint32_t ldg_hint(const uint32_t* p, uint64_t policy) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(policy));
+  return v;
+}
+
 __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                                uint64_t policy) {
   asm volatile(
