@@ -67,7 +67,7 @@ TRAFFIC_DEC_TILE_SRC_SHA = "4225a449fd2a407d"
 # from the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
 TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.399808e6 + 2.981376e6) / (64 * 4096 * 16)
 TRAFFIC_DEC_SMALL_SRC_SHA = "0f6f97446d1053e5"
-DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_small.cu")
+DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_tc.cu")
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
 # for the encode source whose sha256 starts with TRAFFIC_ENC_SRC_SHA.

@@ -522,14 +522,9 @@ size_t lla_decoupled_workspace_size(const lla_dims* dims, int d_rope, int B, int
     off += al256(static_cast<size_t>(decoupled_small_trig_rows(L_max)) * 64 * 4);
     return off;
   }
-  // records [(B H + grid) 1][r_v + 4] (grid <= kMaxGrid), then the bf16 kernel's
-  // query records [B H][ceil(L_max / 128)][r_k + 68] or the fp32 mode's scores
-  off += al256((static_cast<size_t>(B) * dims->H + kMaxGrid) * kDecoupledRecords * (dims->r_v + kRecordHead) * 4);
-  if (dims->dtype == LLA_F32)
-    off += al256(static_cast<size_t>(B) * dims->H * L_max * 4);
-  else
-    off += al256(static_cast<size_t>(B) * dims->H * ((L_max + kTile - 1) / kTile) *
-                 decoupled_qrec_floats(dims->r_k) * 4);
+  if (dims->dtype == LLA_BF16) return 0;   // bf16 shapes neither tensor-core kernel takes
+  // fp32 mode: scores [B][H][L_max]
+  off += al256(static_cast<size_t>(B) * dims->H * L_max * 4);
   return off;
 }
 
@@ -618,21 +613,9 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
                ? LLA_OK
                : LLA_ERR_CUDA;
   }
-  uint8_t* tail = ws + 256 + al256((static_cast<size_t>(cache.B) * H + kMaxGrid) * kDecoupledRecords *
-                                   (dims->r_v + kRecordHead) * 4);
-  a.scores = reinterpret_cast<float*>(tail);
-  a.zimg = tail;
-  a.zimg_stride = static_cast<int64_t>(decoupled_qrec_floats(dims->r_k)) * 4;
-  if (dims->dtype == LLA_F32) return launch_decoupled_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
-  a.ring_slots = decoupled_ring_slots(dims->r_k, dims->r_v);
-  if (a.ring_slots < 2) return LLA_ERR_UNSUPPORTED;
-  const int sms = sm_count();
-  if (sms <= 0) return LLA_ERR_CUDA;
-  const int64_t max_tiles = static_cast<int64_t>(cache.B) * H * ((cache.L_max + kTile - 1) / kTile);
-  a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, max_tiles)));
-  a.combine_units = decode_combine_units(cache.B, H, sms);
-  a.records_per_cta = kDecoupledRecords;
-  return launch_decoupled_bf16(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  if (dims->dtype != LLA_F32) return LLA_ERR_UNSUPPORTED;   // bf16 shapes neither tensor-core kernel takes
+  a.scores = reinterpret_cast<float*>(ws + 256);
+  return launch_decoupled_f32(a, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
 lla_status lla_evict_window(const lla_dims* dims, lla_cache cache, int32_t* seq_lens, int sink, int window,

@@ -1,7 +1,9 @@
-// lla_decoupled_small.cu — absorbed decoupled-RoPE decode at small latent ranks
-// (r_k in {16, 32}, r_v in {32, 64}) with the rotary branch on the tensor cores
-// ("Looped Latent Attention: Cross-Loop KV Compression for Looped Transformers",
-// arXiv 2607.15456v2, Appendix J "Absorbed attention", Tables 13-14).
+// lla_decoupled_tc.cu — absorbed decoupled-RoPE decode in bf16 storage with the
+// rotary branch and the content score on the tensor cores ("Looped Latent
+// Attention: Cross-Loop KV Compression for Looped Transformers", arXiv
+// 2607.15456v2, Appendix J "Absorbed attention", Tables 13-14): a position-major
+// kernel for small ranks (r_k in {16, 32}, r_v in {32, 64}, even H <= 16) and a
+// tile-major one for the other ranks up to (128, 256), both fed by one image kernel.
 //
 // At small ranks the 64-wide rotary key is most of a token's bytes (128 of 224 B
 // per head at (16, 32)), so the rotary score has to cost the CUDA cores next to

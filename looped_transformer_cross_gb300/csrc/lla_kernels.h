@@ -87,7 +87,6 @@ struct DecodeArgs {
   int records_per_cta;               // records per (unit, CTA): 4, or 1 (decoupled kernel)
   const void* k_rope;                // decoupled path: rotary keys [B][H][L_max][d_rope]
   int d_rope;                        // decoupled path: rotary branch width (0: full-RoPE path)
-  int ring_slots;                    // decoupled path: slots of the key ring
   float* trigT;                      // decoupled small-rank path: fp32 RoPE table [64][trig_rows]
   float* qb0;                        // decoupled small-rank path: sc q_c . mu_k per (sequence, head)
   // Paged cache (per-head variant): cache_k / cache_v are page pools
@@ -177,14 +176,6 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 int decode_combine_units(int B, int H, int sms);
 
 // Absorbed decoupled-RoPE decode (content path on the latents + rotary branch).
-constexpr int kDecoupledThreads = 512;  // 16 warps of 8 tokens (lane 0 of warp 0 also issues the copies)
-constexpr int kDecoupledRecords = 1;    // records per (unit, CTA): warps merged in the CTA
-// Query kernel, main kernel, combine.  Needs a.zimg (query records per (unit,
-// 128-token tile), a.zimg_stride bytes apart) and a.ring_slots.
-cudaError_t launch_decoupled_bf16(const DecodeArgs& a, cudaStream_t s);
-int decoupled_qrec_floats(int r_k);     // floats of one unit's query record
-int decoupled_ring_slots(int r_k, int r_v);   // ring slots that fit in shared memory (0: unsupported)
-size_t decoupled_smem_bytes(int r_k, int r_v, int ns);
 // Small ranks (r_k in {16, 32}, r_v in {32, 64}, H even <= 16): rotary branch and
 // content score on the tensor cores, position-major split (a.pos_major = 1, four
 // records per CTA).  Needs a.zimg (B images per (sequence, head),
