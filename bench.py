@@ -56,17 +56,17 @@ TRAFFIC2D_SRC_SHA = "7100f488412d4d9a"
 DECODE2D_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode2d.cu")
 # Same for decode_small_kernel (the per-head kernel at small ranks), from a capture
 # of the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.876544e6 + 3.633920e6) / (64 * 4096 * 16)
-TRAFFIC_SMALL_SRC_SHA = "6579fd99196d23a6"
+TRAFFIC_SMALL_PER_TOKEN_HEAD = (412.849152e6 + 3.808256e6) / (64 * 4096 * 16)
+TRAFFIC_SMALL_SRC_SHA = "d9a74db4c583c522"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 # Same for decoupled_tile_kernel (the tensor-core decoupled kernel at larger ranks),
 # from the 8-sequence variant of the rho = 4 layer (ouro1.4b_rho4_b8_4k).
-TRAFFIC_DEC_TILE_PER_TOKEN_HEAD = (326.040320e6 + 3.235328e6) / (31042 * 16)
-TRAFFIC_DEC_TILE_SRC_SHA = "4225a449fd2a407d"
+TRAFFIC_DEC_TILE_PER_TOKEN_HEAD = (326.408704e6 + 3.348224e6) / (31042 * 16)
+TRAFFIC_DEC_TILE_SRC_SHA = "ae9e40b4520cbf2f"
 # Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores),
 # from the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.399808e6 + 2.981376e6) / (64 * 4096 * 16)
-TRAFFIC_DEC_SMALL_SRC_SHA = "0f6f97446d1053e5"
+TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.379328e6 + 3.052800e6) / (64 * 4096 * 16)
+TRAFFIC_DEC_SMALL_SRC_SHA = "ae9e40b4520cbf2f"
 DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_tc.cu")
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
