@@ -344,9 +344,9 @@ const char* lla_decode_kernel(const lla_dims* dims);
  * d_rope (host-only, no launch): "fp32" (LLA_F32), "small-rank" (bf16 with r_k in
  * {16, 32}, r_v in {32, 64} and an even H <= 16: positions split over CTAs,
  * rotary branch and content score on the tensor cores, fp32 cos/sin per token),
- * "tile" (every other bf16 shape with r_k <= 128: 128-token tiles over
- * (sequence, head), scores on the CUDA cores), or NULL for invalid or
- * unsupported dims (LLA_2D, d_rope != 64). */
+ * "tile" (every other bf16 shape with r_k <= 128 and r_v <= 256: 128-token
+ * tiles over (sequence, head), the same tensor-core score, V read from L2), or
+ * NULL for invalid or unsupported dims (LLA_2D, d_rope != 64, larger ranks). */
 const char* lla_decoupled_kernel(const lla_dims* dims, int d_rope);
 
 /* Workspace bytes for calls with at most B sequences of L_max slots and
