@@ -603,6 +603,9 @@ lla_status lla_decode_attn_decoupled(const lla_dims* dims, int loop_t, int d_rop
     const int64_t work = small ? max_pos : max_pos * H;   // positions, or head-tiles
     a.grid = static_cast<int>(std::min<int64_t>(std::min<int64_t>(sms, kMaxGrid), std::max<int64_t>(1, work)));
     a.combine_units = decode_combine_units(cache.B, H, sms);
+    // image blocks of up to 8 sequences, fewer when that leaves SMs idle
+    a.z_seqs = static_cast<int>(std::min<int64_t>(
+        8, std::max<int64_t>(1, (static_cast<int64_t>(cache.B) * H + 2 * sms - 1) / (2 * sms))));
     const uint64_t units = static_cast<uint64_t>(cache.B) * H, rows = static_cast<uint64_t>(cache.L_max);
     DecoupledMaps maps;
     std::memset(&maps, 0, sizeof(maps));

@@ -59,7 +59,7 @@ constexpr int kConBlock = 512;                       // content B block: 16 rows
 constexpr int kRTile = kTile * kRope * 2;            // rotary tile: 128 rows x 128 B
 constexpr int kCkBox = kTile * 32;                   // K latent box: 128 rows x 16 columns
 constexpr int kDzThreads = 256;
-constexpr int kDzSeqs = 8;                           // sequences per image block
+constexpr int kDzSeqs = 8;                           // sequences per image block at most (a.z_seqs)
 constexpr int kTrigJ = 64;                           // positions per trig-table block
 
 static_assert(kNG * kDCols <= 512, "TMEM columns");
@@ -179,7 +179,8 @@ struct SlotPos {
 //    (rows past the caller's table repeat its last row; only masked tokens read
 //    them), so that a warp reading one column for 32 consecutive tokens reads one
 //    128-byte line.
-//  * Block (head h, kDzSeqs sequences): W_up,k,t[h] is staged once; per sequence
+//  * Block (head h, a.z_seqs <= kDzSeqs sequences; fewer when the batch is small, so
+//    that the grid still covers the SMs): W_up,k,t[h] is staged once; per sequence
 //    w = W_up,k,t[h]^T q_c, b0 = q_c . mu_k,t[h] and q' = RoPE(q_r, q_pos), all
 //    times sc, then the head's B image at zimg + (b H + h) zimg_stride: rotary
 //    block (G, kk) at (2 G + kk) 1 KB, row 2 f' + v of frequency f = 16 G + f'
@@ -221,7 +222,8 @@ __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __g
     return;
   }
   const int u = static_cast<int>(blockIdx.x) - ntb;
-  const int h = u % a.H, b0 = (u / a.H) * kDzSeqs;
+  const int zs = a.z_seqs;
+  const int h = u % a.H, b0 = (u / a.H) * zs;
   const int rk = a.r_k, ws = rk + 2, nk = rk / 16;
   __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(wraw);
   const float sc = kLog2e * kInvSqrtDR;
@@ -237,11 +239,11 @@ __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __g
   const int qrow = kHeadDim + kRope;
   for (int i = tid; i < kDzSeqs * kHeadDim; i += kDzThreads) {
     const int sb = i / kHeadDim, e = i % kHeadDim, b = b0 + sb;
-    qc[sb][e] = b < a.B ? __bfloat162float(static_cast<const __nv_bfloat16*>(
+    qc[sb][e] = sb < zs && b < a.B ? __bfloat162float(static_cast<const __nv_bfloat16*>(
                               a.q)[(static_cast<int64_t>(b) * a.H + h) * qrow + e])
                         : 0.f;
   }
-  for (int i = tid; i < kDzSeqs * (kRope / 2); i += kDzThreads) {
+  for (int i = tid; i < zs * (kRope / 2); i += kDzThreads) {
     const int sb = i / (kRope / 2), f = i % (kRope / 2), b = b0 + sb;
     if (b >= a.B) break;
     int qp = __ldg(a.q_pos + b);
@@ -259,9 +261,10 @@ __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __g
     qa[sb][f] = (x0 * c - x1 * s) * sc;
     qb[sb][f] = (x0 * s + x1 * c) * sc;
   }
-  if (tid < kDzSeqs) live[tid] = b0 + tid < a.B && clamp_len(__ldg(a.seq_lens + b0 + tid), a.L_max) > 0;
+  if (tid < kDzSeqs)
+    live[tid] = tid < zs && b0 + tid < a.B && clamp_len(__ldg(a.seq_lens + b0 + tid), a.L_max) > 0;
   __syncthreads();
-  for (int i = tid; i < kDzSeqs * rk; i += kDzThreads) {
+  for (int i = tid; i < zs * rk; i += kDzThreads) {
     const int sb = i / rk, n = i % rk;
     float s = 0.f;
 #pragma unroll 8
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kDzThreads) decoupled_small_z_kernel(const __g
   // image granules (16 B = 8 columns of one row): 4 rotary blocks x 32 rows x 2,
   // then nk content blocks x 16 rows x 2
   const int ng = 256 + 32 * nk;
-  for (int it = tid; it < kDzSeqs * ng; it += kDzThreads) {
+  for (int it = tid; it < zs * ng; it += kDzThreads) {
     const int sb = it / ng, gi = it % ng;
     if (!live[sb]) continue;
     float v[8];
@@ -1157,7 +1160,8 @@ cudaError_t launch_decoupled_tile(const DecodeArgs& a, const DecoupledMaps& m, c
   DtPlan P;
   if (!make_dt_plan(a.r_k, a.r_v, &P) || a.records_per_cta != kDecoupledTileRecords) return cudaErrorInvalidValue;
   const int trig_blocks = static_cast<int>((a.trig_rows + kTrigJ - 1) / kTrigJ);
-  const int z_blocks = a.H * ((a.B + kDzSeqs - 1) / kDzSeqs);
+  if (a.z_seqs < 1 || a.z_seqs > kDzSeqs) return cudaErrorInvalidValue;
+  const int z_blocks = a.H * ((a.B + a.z_seqs - 1) / a.z_seqs);
   cudaError_t e = launch_pdl(decoupled_small_z_kernel, dim3(z_blocks + trig_blocks), dim3(kDzThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   switch ((a.r_v + 63) / 64) {
@@ -1174,7 +1178,8 @@ cudaError_t launch_decoupled_small(const DecodeArgs& a, const DecoupledMaps& m, 
   DsPlan P;
   if (!make_ds_plan(a.H, a.r_k, a.r_v, &P)) return cudaErrorInvalidValue;
   const int trig_blocks = static_cast<int>((a.trig_rows + kTrigJ - 1) / kTrigJ);
-  const int z_blocks = a.H * ((a.B + kDzSeqs - 1) / kDzSeqs);
+  if (a.z_seqs < 1 || a.z_seqs > kDzSeqs) return cudaErrorInvalidValue;
+  const int z_blocks = a.H * ((a.B + a.z_seqs - 1) / a.z_seqs);
   cudaError_t e = launch_pdl(decoupled_small_z_kernel, dim3(z_blocks + trig_blocks), dim3(kDzThreads), 0, s, a);
   if (e != cudaSuccess) return e;
   if (a.r_k == 16 && a.r_v == 32) e = launch_instance<16, 32>(a, m, P.bytes, s);

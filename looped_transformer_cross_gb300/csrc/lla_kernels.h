@@ -87,6 +87,7 @@ struct DecodeArgs {
   int records_per_cta;               // records per (unit, CTA): 4, or 1 (decoupled kernel)
   const void* k_rope;                // decoupled path: rotary keys [B][H][L_max][d_rope]
   int d_rope;                        // decoupled path: rotary branch width (0: full-RoPE path)
+  int z_seqs;                        // decoupled tensor-core paths: sequences per image block (1..8)
   float* trigT;                      // decoupled small-rank path: fp32 RoPE table [64][trig_rows]
   float* qb0;                        // decoupled small-rank path: sc q_c . mu_k per (sequence, head)
   // Paged cache (per-head variant): cache_k / cache_v are page pools
