@@ -44,9 +44,9 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # layer (ouro_rho4_b8_16k); a workload takes the capture of its context length.
 # Valid only for the decode source whose sha256 starts with TRAFFIC_SRC_SHA; any other
 # source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = {4096: (263.992064e6 + 2.904064e6) / (31042 * 16),
-                          16384: (1080.888064e6 + 3.384576e6) / (8 * 16384 * 16)}
-TRAFFIC_SRC_SHA = "9882cac615125235"
+TRAFFIC_PER_TOKEN_HEAD = {4096: (263.980800e6 + 3.536896e6) / (31042 * 16),
+                          16384: (1080.880896e6 + 3.590400e6) / (8 * 16384 * 16)}
+TRAFFIC_SRC_SHA = "a7337359a0719124"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D score kernel (the dominant one of the LLA-2D call), per
 # latent token (all heads), from the 32-sequence variant of the LLA-2D layer; valid
@@ -61,12 +61,12 @@ TRAFFIC_SMALL_SRC_SHA = "d9a74db4c583c522"
 DECODE_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode_small.cu")
 # Same for decoupled_tile_kernel (the tensor-core decoupled kernel at larger ranks),
 # from the 8-sequence variant of the rho = 4 layer (ouro1.4b_rho4_b8_4k).
-TRAFFIC_DEC_TILE_PER_TOKEN_HEAD = (326.408704e6 + 3.348224e6) / (31042 * 16)
-TRAFFIC_DEC_TILE_SRC_SHA = "ae9e40b4520cbf2f"
+TRAFFIC_DEC_TILE_PER_TOKEN_HEAD = (326.490112e6 + 3.213824e6) / (31042 * 16)
+TRAFFIC_DEC_TILE_SRC_SHA = "682bdfb06f9c87d1"
 # Same for decoupled_small_kernel (small ranks, rotary branch on the tensor cores),
 # from the 64-sequence variant of the rho = 21.3 layer (ouro1.4b_rho21_b64_4k).
-TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.379328e6 + 3.052800e6) / (64 * 4096 * 16)
-TRAFFIC_DEC_SMALL_SRC_SHA = "ae9e40b4520cbf2f"
+TRAFFIC_DEC_SMALL_PER_TOKEN_HEAD = (945.438720e6 + 2.848000e6) / (64 * 4096 * 16)
+TRAFFIC_DEC_SMALL_SRC_SHA = "682bdfb06f9c87d1"
 DECOUPLED_SMALL_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decoupled_tc.cu")
 # DRAM bytes of encode_pair_kernel per prefill token (all heads, both axes), from one
 # ncu capture of the 4-sequence prefill (ouro_rho4_b4_16k: 65,536 tokens); valid only
