@@ -149,6 +149,23 @@ def test_decoupled_kernel_dispatch(L):
     assert d(4, 16, 16, 32, d_rope=32) is None
     assert d(4, 16, 16, 32, variant=lla.LLA_2D) is None
     assert d(4, 16, 256, 256) is None                # r_k above the tile kernel's 128
+    assert d(4, 16, 128, 256) == "tile"              # the tile kernel's largest ranks
+    assert d(4, 16, 144, 160) is None
+
+
+def test_decoupled_workspace_sizes(L):
+    """Workspace bytes of the decoupled call: the tensor-core kernels' records, images,
+    sc b0 and cos/sin table grow with the batch and the context; bf16 shapes no kernel
+    takes report 0 (the call returns LLA_ERR_UNSUPPORTED); fp32 mode holds the scores."""
+    ws = lambda *a, B=32, L_max=4096, **k: L.lla_decoupled_workspace_size(ctypes.byref(lla.dims(*a, **k)), 64, B, L_max)
+    small, tile = ws(4, 16, 16, 32), ws(4, 16, 96, 160)
+    assert small > 0 and tile > 0
+    # B images of 4 KB + 512 B per 16 K-latent columns, for every (sequence, head)
+    assert tile - ws(4, 16, 96, 160, B=31) >= 16 * (4096 + 6 * 512)
+    assert ws(4, 16, 96, 160, L_max=8192) > tile                      # cos/sin table rows
+    assert ws(4, 16, 144, 160) == 0
+    assert ws(4, 16, 96, 160, dtype=lla.LLA_F32) >= 256 + 32 * 16 * 4096 * 4   # scores
+    assert L.lla_decoupled_workspace_size(ctypes.byref(lla.dims(4, 16, 96, 160)), 32, 32, 4096) == 0
 
 
 def test_window_rejects_bad_arguments_on_host(L):
