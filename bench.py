@@ -337,7 +337,21 @@ class DecodeStep:
         return bool(P) and lla.decode_kernel(self.dm) == "tile" and not (P % 128 == 0 or (P % 8 == 0 and 128 % P == 0))
 
     def launches(self):
-        per = 1 if self.gathers_rows() else 3
+        """Library kernel launches per step: the encode's two, then per decode call its
+        family's (row gather 1; fp32 and plain LLA-2D 2; tile, small-rank and decoupled
+        3: images, decode, combine; LLA-2D on CTA pairs 4: images, score, value,
+        combine) and the window call's one."""
+        fam = lla.decode_kernel(self.dm)
+        if self.gathers_rows():
+            per = 1
+        elif self.decoupled:
+            per = 2 if lla.decoupled_kernel(self.dm, D_ROPE) == "fp32" else 3
+        elif fam == "pair-2d":
+            per = 4
+        elif fam in ("fp32", "plain-2d"):
+            per = 2
+        else:
+            per = 3
         return (2 + (per + (1 if self.window > 0 else 0)) * self.w.T) * self.nlayers
 
 
