@@ -342,13 +342,8 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// Ask L2 to fetch [src, src + bytes) (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-               : "memory");
-}
-
-// Same, with an L2 eviction-priority policy for the fetched lines.
+// Ask L2 to fetch [src, src + bytes) (16-byte aligned, size a multiple of 16) under
+// an L2 eviction-priority policy for the fetched lines.
 __device__ __forceinline__ void prefetch_l2_bulk_hint(const void* src, uint32_t bytes, uint64_t policy) {
   asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(reinterpret_cast<uint64_t>(src)),
                "r"(bytes), "l"(policy)
