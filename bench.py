@@ -44,9 +44,9 @@ METRIC = "decode-attn latent-KV tokens/s per layer-loop; % HBM or tensor-pipe ro
 # layer (ouro_rho4_b8_16k); a workload takes the capture of its context length.
 # Valid only for the decode source whose sha256 starts with TRAFFIC_SRC_SHA; any other
 # source reports traffic as unknown (null).
-TRAFFIC_PER_TOKEN_HEAD = {4096: (263.980800e6 + 3.536896e6) / (31042 * 16),
-                          16384: (1080.880896e6 + 3.590400e6) / (8 * 16384 * 16)}
-TRAFFIC_SRC_SHA = "a7337359a0719124"
+TRAFFIC_PER_TOKEN_HEAD = {4096: (263.988736e6 + 3.217408e6) / (31042 * 16),
+                          16384: (1080.879104e6 + 3.529472e6) / (8 * 16384 * 16)}
+TRAFFIC_SRC_SHA = "2b90f83646e16cdd"
 DECODE_SRC = os.path.join(ROOT, "looped_transformer_cross_gb300", "csrc", "lla_decode.cu")
 # The same for the LLA-2D score kernel (the dominant one of the LLA-2D call), per
 # latent token (all heads), from the 32-sequence variant of the LLA-2D layer; valid

@@ -454,6 +454,20 @@ lla_status decode_impl(const lla_dims* dims, int loop_t, const void* q, const Ca
   // V latents: 32-column boxes (a tail box zero-filled past r_v), 64B swizzle
   if (!make_map_3d(&maps.v, cache.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims->r_v, rows, units, 32, box_rows, 1))
     return LLA_ERR_CUDA;
+  // pages of 8..64 tokens with whole 32-column chunks: one box per page for all of V
+  // (rows, chunks and page-heads as the outer dimensions of a 4-D view of the pool)
+  if (cache.bt && cache.page_size < kTile && dims->r_v % 32 == 0) {
+    auto enc = tensor_map_encoder();
+    const cuuint64_t d4[4] = {32, static_cast<cuuint64_t>(cache.page_size), static_cast<cuuint64_t>(dims->r_v / 32), units};
+    const cuuint64_t s4[3] = {static_cast<cuuint64_t>(dims->r_v) * 2, 64,
+                              static_cast<cuuint64_t>(cache.page_size) * dims->r_v * 2};
+    const cuuint32_t b4[4] = {32, static_cast<cuuint32_t>(cache.page_size), static_cast<cuuint32_t>(dims->r_v / 32), 1};
+    const cuuint32_t e4[4] = {1, 1, 1, 1};
+    if (enc && enc(&maps.v4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache.v), d4, s4, b4, e4,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      a.v_page_major = 1;
+  }
   if (!ready()) return LLA_ERR_CUDA;
   return launch_decode_bf16(a, maps, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }

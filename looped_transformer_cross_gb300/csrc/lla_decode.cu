@@ -419,8 +419,23 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           if (!pwait(bar(misc->vempty[sv]), vr.phase ^ 1u)) break;
           const uint32_t vb = bar(misc->vfull[sv]);
           const uint32_t vs = v_ring + sv * P.v_stage;
-          if constexpr (kPage != 0) {
-            paged_tile_load<kPage == 2>(a, wv.b, wv.h, wv.t, wv.L, vs, vb, P.vplan, [&](int) { return &maps.v; });
+          if constexpr (kPage == 2) {
+            if (a.v_page_major) {
+              // one box per page holding tokens below the length: [chunk][P rows][32],
+              // page i of the tile at i * (chunks * P * 64) bytes (lane i issues page i)
+              const int pg = a.page_size;
+              const uint32_t region = static_cast<uint32_t>(P.vplan.n * pg * 64);
+              const int np = (min(kTile, wv.L - wv.t * kTile) + pg - 1) / pg;
+              if (lane == 0) mbar_arrive_expect_tx(vb, region * np);
+              __syncwarp();
+              const int lp0 = wv.t * (kTile / pg);
+              for (int i = lane; i < np; i += 32)
+                tma_load_4d(vs + i * region, &maps.v4, vb, 0, 0, 0, page_of(a, wv.b, lp0 + i) * a.H + wv.h);
+            } else {
+              paged_tile_load<true>(a, wv.b, wv.h, wv.t, wv.L, vs, vb, P.vplan, [&](int) { return &maps.v; });
+            }
+          } else if constexpr (kPage != 0) {
+            paged_tile_load<false>(a, wv.b, wv.h, wv.t, wv.L, vs, vb, P.vplan, [&](int) { return &maps.v; });
           } else {
             mbar_arrive_expect_tx(vb, P.vplan.bytes);
             const int y = wv.t * kTile, z = wv.b * a.H + wv.h;
@@ -519,6 +534,14 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           const int per_c = (steps * 16 - valid) * 4;
           for (int x = lane; x < P.vplan.n * per_c; x += 32) {
             const int c = x / per_c, r = valid + (x - c * per_c) / 4, g = x & 3;
+            if constexpr (kPage == 2) {
+              if (a.v_page_major) {   // page-major: page r / P, chunk c, row r % P
+                const int pg = a.page_size;
+                *reinterpret_cast<uint4*>(vs + (r / pg) * (P.vplan.n * pg * 64) + c * pg * 64 +
+                                          swizzle_offset((r % pg) * 64 + g * 16, 64)) = make_uint4(0, 0, 0, 0);
+                continue;
+              }
+            }
             *reinterpret_cast<uint4*>(vs + P.vplan.off[c] + swizzle_offset(r * 64 + g * 16, 64)) =
                 make_uint4(0, 0, 0, 0);
           }
@@ -526,9 +549,28 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__
           __syncwarp();
         }
         tc_fence_after();
-        const uint64_t b0 = dv0 + sv * vst;
         const uint32_t pa = tmem + jb * 128;
-        for (int k = 0; k < steps; ++k) umma_bf16_ts_warp(tmem + kDCol, pa + 8 * k, b0 + 64 * k, idesc_v, 1u);
+        if constexpr (kPage == 2) {
+          if (a.v_page_major) {
+            // page-major V: chunks P * 64 B apart (LBO); 8-row groups 512 B apart within
+            // a page of >= 16 rows, one page region apart with 8-row pages (SBO); the
+            // 16-token K step k starts at page 16 k / P, row 16 k % P
+            const int pg = a.page_size;
+            const uint32_t region = static_cast<uint32_t>(P.vplan.n * pg * 64);
+            const uint64_t dpm = umma_desc(v_ring + sv * P.v_stage, static_cast<uint32_t>(pg * 64),
+                                           pg >= 16 ? 512u : region, kSw64);
+            for (int k = 0; k < steps; ++k) {
+              const uint32_t off = static_cast<uint32_t>((16 * k) / pg) * region + static_cast<uint32_t>((16 * k) % pg) * 64;
+              umma_bf16_ts_warp(tmem + kDCol, pa + 8 * k, dpm + (off >> 4), idesc_v, 1u);
+            }
+          } else {
+            const uint64_t b0 = dv0 + sv * vst;
+            for (int k = 0; k < steps; ++k) umma_bf16_ts_warp(tmem + kDCol, pa + 8 * k, b0 + 64 * k, idesc_v, 1u);
+          }
+        } else {
+          const uint64_t b0 = dv0 + sv * vst;
+          for (int k = 0; k < steps; ++k) umma_bf16_ts_warp(tmem + kDCol, pa + 8 * k, b0 + 64 * k, idesc_v, 1u);
+        }
         umma_commit_warp(bar(misc->vempty[sv]));
         umma_commit_warp(bar(misc->vdone[jb]));
         walker_advance(wv, a);

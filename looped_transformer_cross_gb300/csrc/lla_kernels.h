@@ -99,6 +99,7 @@ struct DecodeArgs {
   int64_t num_pages;
   DecodePlan plan;
   DecodeSmallPlan splan;
+  int v_page_major;                  // tile kernel, page pieces: V tile stored page-major (maps.v4)
 };
 
 // Launch `kern` as a programmatic dependent of the previous grid on stream `s`: its
@@ -160,6 +161,10 @@ cudaError_t launch_evict_window(const EvictArgs& a, cudaStream_t s);
 struct DecodeMaps {
   CUtensorMap k[3];                  // latent K boxes of width 64 / 32 / 16
   CUtensorMap v;                     // latent V boxes of width 32
+  // page pool with pages of 8..64 tokens and r_v a multiple of 32: one page of V as
+  // one box [chunk][P rows][32 columns] (4-D view: columns, rows, 32-column chunks,
+  // page-head), the page-major V layout of the tile kernel (DecodeArgs::v_page_major)
+  CUtensorMap v4;
 };
 
 bool make_decode_plan(int r_k, int r_v, DecodePlan* p);

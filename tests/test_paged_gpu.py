@@ -90,12 +90,15 @@ def _check(w, inp, pool_k, pool_v, bt, P, t, style=0):
     assert e_o <= TOL[w.dtype] and e_l <= TOL[w.dtype], (e_o, e_l)
 
 
-@pytest.mark.parametrize("P", [1, 8, 16, 64, 100, 128, 256])
-def test_paged_decode_tile_kernel(P):
+@pytest.mark.parametrize("P,r_v", [(1, 160), (8, 160), (16, 160), (32, 160), (64, 160), (100, 160),
+                                   (128, 160), (256, 160), (16, 144)])
+def test_paged_decode_tile_kernel(P, r_v):
     """The tile kernel's shapes in every kind of page: whole tiles inside a page
-    (128, 256), a tile as 128/P page pieces (8, 16, 64), and pages the tile copies do
-    not take, whose rows are gathered one by one (1: the vLLM setting, 100)."""
-    w = workload(T=2, H=4, r_k=96, r_v=160, B=5, L_max=400)
+    (128, 256), a tile as 128/P page pieces (8, 16, 32, 64: with r_v a multiple of 32
+    one box per page holds all of its V columns, else one box per 32-column chunk and
+    page, the last zero-filled past r_v), and pages the tile copies do not take, whose
+    rows are gathered one by one (1: the vLLM setting, 100)."""
+    w = workload(T=2, H=4, r_k=96, r_v=r_v, B=5, L_max=400)
     lens = [400, 1, 129, 0, 256]
     inp = make_decode_inputs(w, 700 + P, device="cuda", seq_lens=torch.tensor(lens, dtype=torch.int32))
     assert lla.decode_kernel(lla_dims(w)) == "tile"
