@@ -87,10 +87,33 @@ def test_round_bf16_matches_library_conversion():
     g = _rng(1)
     vals = np.concatenate([g.standard_normal(20000).astype(np.float32),
                            (g.standard_normal(2000) * 1e-30).astype(np.float32),
-                           (g.standard_normal(2000) * 1e30).astype(np.float32)])
+                           (g.standard_normal(2000) * 1e30).astype(np.float32),
+                           # below 2^-126: bf16 subnormals, spaced 2^-133
+                           (g.standard_normal(2000) * 2.0 ** -128).astype(np.float32),
+                           (g.standard_normal(500) * 2.0 ** -136).astype(np.float32),
+                           # next to the largest finite bf16 (2^127 (2 - 2^-7)): some
+                           # stay finite, the rest round to infinity
+                           (np.sign(g.standard_normal(2000)) *
+                            g.uniform(3.37e38, 3.40e38, 2000)).astype(np.float32)])
     ref = torch.from_numpy(vals).to(torch.bfloat16).to(torch.float64).numpy()
     got = np.array([oracle.round_bf16(float(v)) for v in vals])
+    assert np.isinf(ref).any() and np.isfinite(ref[-2000:]).any()
+    assert (np.abs(ref[(ref != 0) & np.isfinite(ref)]) < 2.0 ** -126).any()
     assert np.array_equal(got, ref)
+
+
+def test_round_bf16_edges():
+    """Edges of the bf16 range written out: the largest finite value, the midpoint to
+    2^128 (ties to the even neighbour, which is past the range: infinity), the smallest
+    subnormal 2^-133 and half of it (a tie to the even neighbour, zero)."""
+    big = 2.0 ** 127 * (2 - 2.0 ** -7)
+    assert oracle.round_bf16(big) == big
+    assert oracle.round_bf16(2.0 ** 127 * (2 - 2.0 ** -8)) == np.inf
+    assert oracle.round_bf16(-(2.0 ** 127 * (2 - 2.0 ** -8) - 2.0 ** 110)) == -big
+    assert oracle.round_bf16(2.0 ** -133) == 2.0 ** -133
+    assert oracle.round_bf16(2.0 ** -134) == 0.0
+    assert oracle.round_bf16(3 * 2.0 ** -134) == 2.0 ** -132
+    assert oracle.round_bf16(1.4 * 2.0 ** -130) == 2.0 ** -130 + 3 * 2.0 ** -133
 
 
 def test_round_bf16_ties_to_even():
