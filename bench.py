@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
+import datetime
 import json
 import os
 import statistics
@@ -353,6 +354,21 @@ class DecodeStep:
         else:
             per = 3
         return (2 + (per + (1 if self.window > 0 else 0)) * self.w.T) * self.nlayers
+
+
+# A rank that dies or never joins must not hold the others forever: every collective of
+# the bench (the barriers around the timed region, the max of the elapsed time, the sum of
+# the tokens) ends with an error after this many seconds.
+PG_TIMEOUT_S = float(os.environ.get("LLA_BENCH_PG_TIMEOUT_S", "600"))
+
+
+def init_dist(backend, device=None, timeout_s=None):
+    """One process group over the launcher's env (RANK, WORLD_SIZE, MASTER_*), with a
+    bounded timeout on every collective."""
+    kw = {"timeout": datetime.timedelta(seconds=PG_TIMEOUT_S if timeout_s is None else timeout_s)}
+    if device is not None:
+        kw["device_id"] = device
+    torch.distributed.init_process_group(backend, **kw)
 
 
 def barrier(dist_on):
@@ -864,7 +880,7 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     if dist_on:
-        torch.distributed.init_process_group("nccl", device_id=device)
+        init_dist("nccl", device)
     try:
         res = run_ours(args, dist_on, rank, world, device)
         if rank == 0:
