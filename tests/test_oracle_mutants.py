@@ -1,12 +1,14 @@
 """The oracle's pins catch plausible mistakes: each case below plants one mistake in a
 scratch copy of ``oracle/`` (a dropped term, a wrong sign, a transposed operand, a
-swapped or shifted index), rebuilds it there and runs the CPU pin tests
+swapped or shifted index, a wrapper passing the wrong argument), rebuilds it there and runs the CPU pin tests
 (``tests/test_oracle_*.py``) against the copy; every case must make at least one pin
 fail.  Nothing here touches the oracle in the tree or any GPU code.
 
 Left out as equivalent: writing the eviction budget test as ``L < S + W`` instead of
-``L <= S + W`` (at L = S + W both keep every token in order) and the absorbed-value
-mean scaled by 1 instead of the weight sum (the weights sum to one).
+``L <= S + W`` (at L = S + W both keep every token in order), the absorbed-value mean
+scaled by 1 instead of the weight sum (the weights sum to one), and a wrapper dropping the
+position offset it passes for both the query and the keys (rotary scores depend only on
+position differences, so a shift common to both changes nothing).
 """
 import os
 import py_compile
@@ -101,6 +103,10 @@ MUTANTS = [
      "return int(bt[b, j % page_size]), j // page_size", "slot with page and row swapped"),
     ("oracle/paged.py", "rows = dense[b, :, lp * P:min((lp + 1) * P, L), :]",
      "rows = dense[b, :, lp * P + 1:min((lp + 1) * P + 1, L), :]", "scatter shifted by one row"),
+    ("oracle/__init__.py", "slp, qposp,\n                             int(pos_offset), wkp, wvp, mkp, mvp,",
+     "slp, qposp,\n                             int(pos_offset), wkp, wvp, mvp, mkp,", "decode wrapper swaps the K and V means"),
+    ("oracle/__init__.py", "kwp, vwp, nwp, wposp", "vwp, kwp, nwp, wposp", "hybrid wrapper swaps window keys and values"),
+    ("oracle/__init__.py", "B, L_max, 1 if round_to_bf16 else 0)", "B, L_max, 0)", "encode wrapper never rounds to bf16"),
     ("oracle/evict.py", "list(range(L - window, L))", "list(range(L - window - 1, L - 1))", "eviction window off by one"),
     ("oracle/evict.py", "= cache[b][:, keep]", "= cache[b][:, sorted(keep, reverse=True)]", "kept tokens in reverse"),
 ]

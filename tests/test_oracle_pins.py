@@ -342,6 +342,31 @@ def test_encode_of_mean_is_zero():
     assert np.all(cache[0, :, 0] == 5.0) and np.all(cache[0, :, 2] == 5.0)
 
 
+@pytest.mark.parametrize("variant", [0, 1])
+def test_encode_rounds_each_latent_once_to_bf16(variant):
+    """With rounding asked for, each stored latent is the nearest bf16 of the exact sum
+    (R6): equal to the unrounded encode rounded element by element, every value on the
+    bf16 grid (a float32 -> bf16 library round trip leaves it unchanged), and most of the
+    written values differ from the unrounded ones."""
+    g = _rng(31)
+    T, H, d, r, B, L_max, N = 2, 2, 128, 32, 2, 4, 3
+    width = T * d if variant == 0 else T * H * d
+    shape_x = (N, H, width) if variant == 0 else (N, width)
+    shape_w = (H, width, r) if variant == 0 else (width, r)
+    shape_mu = (H, width) if variant == 0 else (width,)
+    shape_c = (B, H, L_max, r) if variant == 0 else (B, L_max, r)
+    x, w, mu = g.standard_normal(shape_x), g.standard_normal(shape_w), g.standard_normal(shape_mu)
+    seq_idx, pos = np.array([1, 0, 1], np.int32), np.array([3, 0, 1], np.int32)
+    dm = oracle.dims(T, H, d, r, r, variant=variant)
+    exact = oracle.encode(dm, x, seq_idx, pos, w, mu, r, np.zeros(shape_c))
+    rounded = oracle.encode(dm, x, seq_idx, pos, w, mu, r, np.zeros(shape_c), round_to_bf16=True)
+    np.testing.assert_array_equal(rounded, np.vectorize(oracle.round_bf16)(exact))
+    lib = torch.from_numpy(rounded.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(rounded, lib)
+    written = N * r * (H if variant == 0 else 1)
+    assert np.count_nonzero(rounded != exact) > written // 2
+
+
 def test_encode_layout_structured_exact():
     """Selector W_down and integer x: c[k] = x[u(k)] exactly, in slot (seq_idx, pos) of head h;
     every other slot keeps its canary."""
