@@ -174,9 +174,11 @@ lla_status lla_decode_attn(const lla_dims* dims, int loop_t, const void* q,
  * inside the pool, writes are skipped), so no access leaves the pool.  Per-head variant only;
  * any page_size >= 1 in both storage types.  In bf16 the tile kernel copies a
  * 128-token tile whole when page_size is a multiple of 128, as 128/P page pieces when
- * P is 8, 16, 32 or 64, and other page sizes (one-token pages, as vLLM's) run a
- * kernel that gathers token rows one by one (correct, much slower); the small-rank
- * kernel copies each tile's rows page by page at any page size. */
+ * P is 8, 16, 32 or 64 (with r_v a multiple of 32, one copy per page holds all of its
+ * V columns), and other page sizes (one-token pages, as vLLM's) run a kernel that
+ * gathers token rows one by one (correct, much slower); the small-rank kernel copies
+ * one page for a whole set of heads when P is 8, 16, 32 or 64, else each tile's rows
+ * page by page (any page size). */
 typedef struct {
     void* k;
     void* v;
