@@ -90,6 +90,9 @@ def lib():
             L.lla_decode_attn_paged.argtypes = [pd, ctypes.c_int, vp, PagedCache, i32p, i32p, vp, vp, fp, fp,
                                                 fp, fp, ctypes.c_int64, fp, fp, vp, ctypes.c_size_t, vp]
             L.lla_decode_attn_paged.restype = ctypes.c_int
+            L.lla_decode_attn_noalloc.argtypes = [pd, ctypes.c_int, vp, Cache, i32p, i32p, vp, vp, fp, fp,
+                                                  fp, fp, ctypes.c_int64, fp, fp, vp]
+            L.lla_decode_attn_noalloc.restype = ctypes.c_int
             L.lla_evict_window.argtypes = [pd, Cache, i32p, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
             L.lla_evict_window.restype = ctypes.c_int
             L.lla_decode_kernel.argtypes = [pd]
@@ -309,11 +312,6 @@ def decode_attn_noalloc(dm: Dims, loop_t: int, q, cache_k, cache_v, seq_lens, q_
     Calls that overlap on the GPU race on that scratch; make the first call on a
     device before any stream capture."""
     f = lib().lla_decode_attn_noalloc
-    if f.restype is not ctypes.c_int:
-        vp = ctypes.c_void_p
-        f.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, vp, Cache, vp, vp, vp, vp, vp, vp, vp, vp,
-                      ctypes.c_int64, vp, vp, vp]
-        f.restype = ctypes.c_int
     B = int(cache_k.shape[0])
     L_max = int(cache_k.shape[2] if dm.variant == LLA_PER_HEAD else cache_k.shape[1])
     cache = Cache(ctypes.c_void_p(cache_k.data_ptr()), ctypes.c_void_p(cache_v.data_ptr()), B, L_max)

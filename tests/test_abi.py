@@ -235,3 +235,31 @@ def test_evict_rejects_bad_arguments_on_host(L):
     assert call(ws=255) == lla.LLA_ERR_INVALID_ARG
     assert call(d=lla.dims(4, 2, 96, 160, d_head=64)) == lla.LLA_ERR_UNSUPPORTED
     assert call(B=0) == lla.LLA_OK                                  # nothing to do
+
+
+def declared_arity():
+    """Parameter count of every function include/lla.h declares (void lists count 0)."""
+    out = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        txt = open(os.path.join(ROOT, "include", fn)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        for name, params in re.findall(r"\b(lla_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", txt, flags=re.S):
+            p = params.strip()
+            out[name] = 0 if p in ("", "void") else p.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(L):
+    """Every function the binding gives ctypes argument types takes as many arguments as
+    the header declares (a drift here would pass garbage through the ABI)."""
+    arity = declared_arity()
+    checked = 0
+    for name, n in arity.items():
+        f = getattr(L, name)
+        if f.argtypes is None:
+            continue
+        assert len(f.argtypes) == n, (name, len(f.argtypes), n)
+        checked += 1
+    assert checked >= 10
