@@ -261,3 +261,39 @@ def test_binding_signatures_match_the_header(L):
         f = getattr(L, name)
         assert f.argtypes is not None, name + " has no ctypes signature in the binding"
         assert len(f.argtypes) == n, (name, len(f.argtypes), n)
+
+
+def _declared_params():
+    """(name, [parameter declaration]) of every prototype in include/lla.h."""
+    out = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        txt = open(os.path.join(ROOT, "include", fn)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        for name, params in re.findall(r"\b(lla_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", txt, flags=re.S):
+            p = " ".join(params.split())
+            out[name] = [] if p in ("", "void") else [x.strip() for x in p.split(",")]
+    return out
+
+
+def test_binding_argument_types_match_the_header(L):
+    """Each argument's ctypes type agrees with the header's C type: pointers as pointers,
+    int as a 32-bit int, int64_t and size_t as 64-bit, the cache descriptors by value."""
+    by_value = {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+                "float": ctypes.c_float, "lla_status": ctypes.c_int, "lla_cache": lla.Cache,
+                "lla_paged_cache": lla.PagedCache}
+    ints = (ctypes.c_int, ctypes.c_uint, ctypes.c_long, ctypes.c_ulong, ctypes.c_longlong,
+            ctypes.c_ulonglong)
+
+    def same(ct, want):
+        return ct is want or (ct in ints and want in ints and ctypes.sizeof(ct) == ctypes.sizeof(want))
+
+    for name, params in _declared_params().items():
+        f = getattr(L, name)
+        for i, (decl, ct) in enumerate(zip(params, f.argtypes)):
+            if "*" in decl:
+                assert ct is ctypes.c_void_p or issubclass(ct, ctypes._Pointer), (name, i, decl, ct)
+            else:
+                want = by_value[decl.replace("const ", "").split()[0]]
+                assert same(ct, want), (name, i, decl, ct)
