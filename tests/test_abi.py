@@ -297,3 +297,33 @@ def test_binding_argument_types_match_the_header(L):
             else:
                 want = by_value[decl.replace("const ", "").split()[0]]
                 assert same(ct, want), (name, i, decl, ct)
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The binding's ctypes structures have the C structures' size and field offsets, as
+    gcc lays them out from include/lla.h (they cross the ABI by value or by pointer)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    specs = {"lla_dims": (lla.Dims, ["T", "H", "d_head", "r_k", "r_v", "variant", "dtype", "rope_base",
+                                     "rope_style"]),
+             "lla_cache": (lla.Cache, ["k", "v", "B", "L_max"]),
+             "lla_paged_cache": (lla.PagedCache, ["k", "v", "block_table", "B", "max_pages", "page_size",
+                                                  "num_pages"])}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "lla.h"', "int main(void) {"]
+    for cname, (_, fields) in specs.items():
+        lines.append('printf("%s size %%zu\\n", sizeof(%s));' % (cname, cname))
+        for f in fields:
+            lines.append('printf("%s %s %%zu\\n", offsetof(%s, %s));' % (cname, f, cname, f))
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    got = dict(line.rsplit(" ", 1) for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                              check=True).stdout.splitlines())
+    for cname, (cls, fields) in specs.items():
+        assert int(got["%s size" % cname]) == ctypes.sizeof(cls), cname
+        for f in fields:
+            assert int(got["%s %s" % (cname, f)]) == getattr(cls, f).offset, (cname, f)
