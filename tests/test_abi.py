@@ -327,3 +327,18 @@ def test_struct_layouts_match_the_header(tmp_path):
         assert int(got["%s size" % cname]) == ctypes.sizeof(cls), cname
         for f in fields:
             assert int(got["%s %s" % (cname, f)]) == getattr(cls, f).offset, (cname, f)
+
+
+def test_enum_constants_match_the_header():
+    """Every enumerator of include/lla.h that the binding names has the header's value, and
+    the binding names every status code."""
+    txt = open(os.path.join(ROOT, "include", "lla.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    values = {n: int(v) for n, v in re.findall(r"\b(LLA_[A-Z0-9_]+)\s*=\s*(\d+)", txt)}
+    statuses = [n for n in values if n == "LLA_OK" or n.startswith("LLA_ERR_")]
+    assert len(statuses) == 7
+    for n in statuses:
+        assert hasattr(lla, n), n
+    for n, v in values.items():
+        if hasattr(lla, n):
+            assert getattr(lla, n) == v, n
