@@ -4,6 +4,8 @@ first weights barrier expect one arrival more than it gets, so the value-MMA
 issuer's wait runs out after about a second.  The call must report
 LLA_ERR_TIMEOUT through the status word, the context must stay usable, and the
 next call on the same (cleared) workspace must return the exact result."""
+import os
+import re
 import time
 
 import pytest
@@ -14,7 +16,9 @@ from looped_transformer_cross_gb300 import lla
 
 pytestmark = pytest.mark.gpu
 
-LLA_TEST_STALL = 0x4C415453
+# the test word's value as include/lla.h defines it
+with open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lla.h")) as _h:
+    LLA_TEST_STALL = int(re.search(r"#define\s+LLA_TEST_STALL\s+(0x[0-9A-Fa-f]+)u?", _h.read()).group(1), 16)
 
 
 @pytest.fixture(scope="module", autouse=True)
